@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV gather/scatter path on one GB300 (or N independent replicas).
+
+One step = one full pass of the hot path over the Llama-3.1-8B-shaped request:
+  kvx_store_chunks  32768 tokens x 32 layers x K/V (2048 random pages of a 16384-page
+                    pool) gathered into 128 layer-major chunks of 256 tokens (32 MiB each)
+                    in mapped pinned host memory, then
+  kvx_load_chunks   those chunks scattered back into a disjoint set of 2048 fresh pages.
+Each direction moves N = 4 GiB over the host link; value = 2N per step / step time (GB/s).
+Inputs (4 GiB each way) are larger than L2 (129 MB), so no L2 flush is needed.
+
+Also measured in the same run and printed on the same JSON line:
+  host_link_peak  one 4 GiB pinned cudaMemcpyAsync per direction (the store/load roofline);
+  transform       kvx_transform_hbm gather + scatter of the same request with the chunks in
+                  HBM, against the measured HBM copy peak;
+  dma_baseline    one cudaMemcpyAsync per (chunk, layer, kv, page) segment, both ways;
+  cpu_baseline    the CPU oracle on a bounded sample of the same workload, all host cores;
+  e2e             the same step timed on the host clock through the C ABI, with the page
+                  tables uploaded from pinned host memory and the status word read back.
+
+--impl reference times the CPU oracle alone (the reference arm of this comparison).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "KV store/load GB/s vs measured host-link peak; HBM transform GB/s vs HBM peak"
+GB = 1e9
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-dma-baseline", action="store_true")
+    p.add_argument("--store-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
+    p.add_argument("--load-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
+    p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during a timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def parse_cfg(kvx, ctx, op, text):
+    c = kvx.kvx_default_launch_cfg(ctx, op)
+    if text:
+        vals = [int(x) for x in text.split(",")]
+        for name, v in zip(("sm_cap", "ctas_per_sm", "threads", "unroll", "store_hint"), vals):
+            setattr(c, name, v)
+    return c
+
+
+class EventTimer:
+    def __init__(self, stream):
+        self.stream = stream
+        self.pairs = []
+
+    def start(self):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        return e
+
+    def stop(self, e0):
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(self.stream)
+        self.pairs.append((e0, e1))
+
+    def ms(self):
+        return [a.elapsed_time(b) for a, b in self.pairs]
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("kvx.cu", "kvx_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_gather_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha()
+    for line in open(path):
+        f = dict(x.split("=", 1) for x in line.split() if "=" in x)
+        if f.get("kernel") == kernel and f.get("workload") == workload and \
+                f.get("source_sha") == sha:
+            return float(f["dram_bytes_per_launch"])
+    return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return 6800.0, "fallback (6.8 TB/s)"
+
+
+# ----------------------------------------------------------------------------- cpu baseline
+
+class CpuSample:
+    """The CPU oracle on a bounded sample of the Llama-3.1-8B-shaped workload: 32 chunks of
+    256 tokens x 32 layers x K/V (1 GiB per direction).  The source pool holds exactly the
+    sample's 512 pages in a seeded random order; the load writes a second pool through
+    another random page order.  One pass = oracle store + oracle load."""
+
+    def __init__(self, threads: int):
+        import oracle
+        from paged_kv_gather_gb300 import workloads as wl
+
+        self.oracle = oracle
+        self.threads = threads
+        w = wl.llama8b(num_pages=512, n_tokens=8192)
+        s = w.shape
+        g = torch.Generator()
+        g.manual_seed(w.seed)
+        layer_bytes = s.num_pages * s.page_size * s.token_bytes
+        self.src_flat = torch.randint(0, 256, (s.kv_factor * s.num_layers * layer_bytes,),
+                                      dtype=torch.uint8, generator=g).numpy()
+        self.dst_flat = np.zeros_like(self.src_flat)
+
+        def as_pool(flat):
+            v = flat.reshape(s.kv_factor, s.num_layers, s.num_pages, s.page_size, s.token_bytes)
+            return oracle.Pool([[v[k, l] for l in range(s.num_layers)]
+                                for k in range(s.kv_factor)], s.page_size)
+
+        self.psrc, self.pdst = as_pool(self.src_flat), as_pool(self.dst_flat)
+        self.arena = np.zeros(w.store_arena_bytes, np.uint8)
+        self.chunks = [oracle.Chunk(c.request, c.token_begin, c.n_tokens, c.layer_begin,
+                                    c.n_layers, c.layout, self.arena[c.offset:])
+                       for c in w.store_chunks]
+        rng = np.random.default_rng(w.seed)
+        self.src = [oracle.Request(rng.permutation(512).astype(np.int32), 8192)]
+        self.dst = [oracle.Request(rng.permutation(512).astype(np.int32), 8192)]
+        self.bytes_per_pass = 2 * w.store_bytes()
+
+    def one_pass(self):
+        self.oracle.store(self.psrc, self.src, self.chunks, threads=self.threads)
+        self.oracle.load(self.pdst, self.dst, self.chunks, threads=self.threads)
+
+    def run(self, seconds: float):
+        passes, t0 = 0, time.perf_counter()
+        while True:
+            self.one_pass()
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        return {"value": round(self.bytes_per_pass * passes / el / GB, 3), "unit": "GB/s",
+                "cores": self.threads, "kind": "oracle",
+                "sample": f"{passes} passes of oracle store+load over 32 chunks (8192 tokens x "
+                          f"32 layers x K/V = 1 GiB per direction) of the Llama-3.1-8B-shaped "
+                          f"workload on {self.threads} host threads, {el:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, local = dist_setup(args)
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    sample = CpuSample(threads)
+    for _ in range(args.warmup):
+        sample.one_pass()
+    ms = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        sample.one_pass()
+        ms.append((time.perf_counter() - t0) * 1e3)
+    step_ms = statistics.median(ms)
+    value = round(sample.bytes_per_pass / (step_ms * 1e-3) / GB, 3)
+    base = {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"each step: oracle store+load over 32 chunks (8192 tokens x 32 layers x "
+                      f"K/V = 1 GiB per direction) of the Llama-3.1-8B-shaped workload on "
+                      f"{threads} host threads"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": "llama8b_kv: 32 layers, 8 KV heads x 128, bf16, 16-token "
+                                   "pages, 256-token layer-major chunks; step = store + load "
+                                   "(CPU oracle on a 1 GiB-per-direction sample)",
+                       "parallelism": "none (CPU oracle)"},
+            "cpu_baseline": base,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    from paged_kv_gather_gb300.build import build
+    if rank == 0:
+        build()
+    barrier(world)
+    from paged_kv_gather_gb300 import kvx
+    from paged_kv_gather_gb300 import workloads as wl
+
+    w = wl.llama8b()
+    s = w.shape
+    N = w.store_bytes()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    # Pools: [kv][layer][page][token][bytes], 32 GiB, bf16 N(0,1) values.
+    pools = torch.empty((s.kv_factor, s.num_layers, s.num_pages, s.page_size, s.token_bytes),
+                        dtype=torch.uint8, device=dev)
+    wl.fill_values(pools, s.dtype, wl.values_generator(w.seed, str(dev)))
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src_h = w.store_requests[0].page_table
+    dst_h = w.load_requests[0].page_table
+    src_d = torch.from_numpy(src_h).to(dev)
+    dst_d = torch.from_numpy(dst_h).to(dev)
+    reqs_src = kvx.requests_array([(src_d.data_ptr(), src_h, w.store_requests[0].n_tokens)])
+    reqs_dst = kvx.requests_array([(dst_d.data_ptr(), dst_h, w.load_requests[0].n_tokens)])
+    host = kvx.HostBuffer(w.store_arena_bytes)
+    host.array[:] = 0  # fault in every page before timing
+    chunks_host = kvx.chunks_array(w.store_chunks, host.ptr)
+    ctx = kvx.kvx_create(local)
+    cfg_store = parse_cfg(kvx, ctx, kvx.KVX_OP_STORE, args.store_cfg)
+    cfg_load = parse_cfg(kvx, ctx, kvx.KVX_OP_LOAD, args.load_cfg)
+    cfg_tr = parse_cfg(kvx, ctx, kvx.KVX_OP_GATHER_HBM, args.transform_cfg)
+
+    def step(t_store=None, t_load=None):
+        e = t_store.start() if t_store else None
+        kvx.kvx_store_chunks(ctx, pool, reqs_src, chunks_host, 0, s.num_layers, cfg_store, sh)
+        if e is not None:
+            t_store.stop(e)
+        e = t_load.start() if t_load else None
+        kvx.kvx_load_chunks(ctx, pool, reqs_dst, chunks_host, 0, s.num_layers, cfg_load, sh)
+        if e is not None:
+            t_load.stop(e)
+
+    # ---- host-link peak: one 4 GiB pinned copy per direction
+    link = {}
+    hp = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
+    dp = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for name, fn in (("h2d", lambda: dp.copy_(hp, non_blocking=True)),
+                         ("d2h", lambda: hp.copy_(dp, non_blocking=True))):
+            for _ in range(2):
+                fn()
+            t = EventTimer(stream)
+            for _ in range(5):
+                e = t.start()
+                fn()
+                t.stop(e)
+            stream.synchronize()
+            link[name] = round((4 << 30) / (statistics.median(t.ms()) * 1e-3) / GB, 1)
+    del hp, dp
+
+    # ---- warm-up, then the timed region (device clock)
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    ts, tl = EventTimer(stream), EventTimer(stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_all = EventTimer(stream)
+        e = t_all.start()
+        for _ in range(args.steps):
+            step(ts, tl)
+        t_all.stop(e)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(t_all.ms()[0], world)
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    store_ms = statistics.mean(ts.ms())
+    load_ms = statistics.mean(tl.ms())
+    items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
+
+    # ---- end to end through the C ABI on the host clock
+    pt_host = torch.from_numpy(np.concatenate([src_h, dst_h])).pin_memory()
+    pt_dev = torch.empty_like(pt_host, device=dev)
+    e2e_ms = []
+    for i in range(args.warmup + max(3, args.steps // 2)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            pt_dev.copy_(pt_host, non_blocking=True)
+        r_src = kvx.requests_array([(pt_dev.data_ptr(), src_h, w.store_requests[0].n_tokens)])
+        r_dst = kvx.requests_array([(pt_dev.data_ptr() + 4 * len(src_h), dst_h,
+                                     w.load_requests[0].n_tokens)])
+        kvx.kvx_store_chunks(ctx, pool, r_src, chunks_host, 0, s.num_layers, cfg_store, sh)
+        kvx.kvx_load_chunks(ctx, pool, r_dst, chunks_host, 0, s.num_layers, cfg_load, sh)
+        flags = kvx.kvx_get_status(ctx, sh)  # D2H of the status word + stream sync
+        assert flags == 0
+        if i >= args.warmup:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    desc_bytes = 2 * kvx.kvx_last_launch(ctx)[3]  # packed descriptors of both calls
+    e2e = {"value": round(2 * N / (statistics.median(e2e_ms) * 1e-3) / GB, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(pt_host.numel() * 4 + desc_bytes), "d2h_bytes_per_step": 4,
+           "payload_link_bytes_per_step": 2 * N,
+           "note": "KV payload crosses the host link inside the kernels (zero-copy); the "
+                   "counted copies are the page tables, descriptors and status word"}
+
+    # ---- HBM transform on the same request (chunks in device memory)
+    dchunk = torch.empty(w.store_arena_bytes, dtype=torch.uint8, device=dev)
+    chunks_dev = kvx.chunks_array(w.store_chunks, dchunk.data_ptr())
+    for _ in range(args.warmup):
+        kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_GATHER, pool, reqs_src, chunks_dev, 0,
+                              s.num_layers, cfg_tr, sh)
+        kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_SCATTER, pool, reqs_dst, chunks_dev, 0,
+                              s.num_layers, cfg_tr, sh)
+    tg, tsc = EventTimer(stream), EventTimer(stream)
+    for _ in range(args.steps):
+        e = tg.start()
+        kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_GATHER, pool, reqs_src, chunks_dev, 0,
+                              s.num_layers, cfg_tr, sh)
+        tg.stop(e)
+        e = tsc.start()
+        kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_SCATTER, pool, reqs_dst, chunks_dev, 0,
+                              s.num_layers, cfg_tr, sh)
+        tsc.stop(e)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    hbm_peak, hbm_src = peaks()
+    g_ms, s_ms = statistics.mean(tg.ms()), statistics.mean(tsc.ms())
+    tr_gbs = {"gather": 2 * N / (g_ms * 1e-3) / GB, "scatter": 2 * N / (s_ms * 1e-3) / GB}
+    dom_tr = "gather" if g_ms >= s_ms else "scatter"
+    transform = {
+        "gather_ms": round(g_ms, 4), "scatter_ms": round(s_ms, 4),
+        "gather_gbs_2n": round(tr_gbs["gather"], 1), "scatter_gbs_2n": round(tr_gbs["scatter"], 1),
+        "gather_gbs_n": round(tr_gbs["gather"] / 2, 1),
+        "roofline": {"bound": "hbm", "achieved": round(tr_gbs[dom_tr], 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(tr_gbs[dom_tr] / hbm_peak, 4),
+                     "traffic": recorded_traffic(f"transform_{dom_tr}", "llama8b"),
+                     "kernel": f"kvx_segment_kernel ({dom_tr}, HBM chunks)",
+                     "peak_source": hbm_src,
+                     "algorithmic_bytes": 2 * N},
+        "cfg": cfg_tr.as_dict()}
+    del dchunk
+
+    # ---- per-page DMA baseline (both directions, one pass each after one warm-up)
+    dma = None
+    if not args.no_dma_baseline:
+        res = {}
+        for name, direction, reqs in (("store", kvx.KVX_DIR_GATHER, reqs_src),
+                                      ("load", kvx.KVX_DIR_SCATTER, reqs_dst)):
+            kvx.kvx_dma_baseline(ctx, direction, pool, reqs, chunks_host, 0, s.num_layers, sh)
+            stream.synchronize()
+            t0 = time.perf_counter()
+            n = kvx.kvx_dma_baseline(ctx, direction, pool, reqs, chunks_host, 0, s.num_layers,
+                                     sh)
+            stream.synchronize()
+            el = time.perf_counter() - t0
+            res[name] = {"gbs": round(N / el / GB, 2), "copies": n, "ms": round(el * 1e3, 2)}
+        dma = res
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = CpuSample(os.cpu_count() or 1).run(args.cpu_seconds)
+
+    value = 2 * N * args.steps * world / (total_ms * 1e-3) / GB
+    store_gbs = N / (store_ms * 1e-3) / GB
+    load_gbs = N / (load_ms * 1e-3) / GB
+    dom = "load" if load_ms >= store_ms else "store"
+    dom_gbs = load_gbs if dom == "load" else store_gbs
+    dom_peak = link["h2d"] if dom == "load" else link["d2h"]
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "llama8b_kv: 32 layers, 8 KV heads x 128, bf16 N(0,1), "
+                               "16-token pages, 32768 tokens on 2048 random pages of a "
+                               "16384-page pool, 128 layer-major chunks of 256 tokens (32 MiB) "
+                               "in mapped pinned host memory; step = store + load",
+                   "bytes_per_direction": N, "l2": "inputs larger than L2 (4 GiB per "
+                   "direction), no flush", "parallelism": f"replicas x{world}" if world > 1
+                   else "single GPU"},
+        "roofline": {"bound": "host_link", "achieved": round(dom_gbs, 2), "peak": dom_peak,
+                     "unit": "GB/s", "frac": round(dom_gbs / dom_peak, 4),
+                     "traffic": recorded_traffic(dom, "llama8b"),
+                     "kernel": f"kvx_segment_kernel ({dom})",
+                     "peak_source": "measured in this run: one 4 GiB pinned cudaMemcpyAsync "
+                                    f"{'H2D' if dom == 'load' else 'D2H'}",
+                     "algorithmic_bytes": N, "items_per_launch": items},
+        "store": {"ms": round(store_ms, 4), "gbs": round(store_gbs, 2),
+                  "frac_of_link": round(store_gbs / link["d2h"], 4), "cfg": cfg_store.as_dict()},
+        "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
+                 "frac_of_link": round(load_gbs / link["h2d"], 4), "cfg": cfg_load.as_dict()},
+        "host_link_peak": {"h2d_gbs": link["h2d"], "d2h_gbs": link["d2h"],
+                           "nominal_gbs_per_direction": 450.0,
+                           "nominal_note": "NVLink-C2C 900 GB/s bidirectional"},
+        "transform": transform,
+        "dma_baseline": dma,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    host.close()
+    kvx.kvx_destroy(ctx)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

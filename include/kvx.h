@@ -1,0 +1,256 @@
+/*
+ * kvx.h -- C ABI of the GB300 paged KV-cache gather/scatter library (libkvx.so).
+ *
+ * The operation.  A serving engine keeps a request's KV cache in small fixed pages
+ * (16-64 tokens) scattered through per-layer K and V pools in HBM and found through a
+ * page table.  To move that cache to and from host memory in large contiguous chunks,
+ * GPU threads gather the pages into chunk layout (store) or scatter chunks back into
+ * freshly allocated pages (load), changing the layout on the fly, instead of issuing one
+ * DMA per small page.  Sources:
+ *   - "Strata Guide: Hierarchical Context Caching for Long LLMs", sections "The
+ *     Conflict Between PagedAttention and Transfer Efficiency" (pages and page tables,
+ *     per-page DMA cost), "The Mechanics of GPU-Assisted I/O", "Non-Intrusive Resource
+ *     Sizing" (a small, capped SM count; cache-bypass stores), "Two-Dimensional Memory
+ *     Layout Decoupling" (layer-first GPU layout, page-first host layout) and "Step 1:
+ *     High-Performance GPU-Assisted I/O CUDA Kernel" (page-table lookup per unit);
+ *   - "Tutti: Making SSD-Backed KV Cache Practical for Long-Context LLM Serving",
+ *     section 2 Design 1 (host work O(layers), not O(layers x blocks)) and section 7
+ *     (per-layer retrieve/store interface taking block ids).
+ *
+ * Layouts.
+ *   Page pools (device memory): for each kv in [0, kv_factor) and layer in [0, num_layers)
+ *   one array [num_pages][page_size][token_bytes].  kv 0 is K, kv 1 is V; an MLA latent
+ *   cache uses kv_factor 1.  Token t of request r sits in slot
+ *   page_table_r[t / page_size] * page_size + t % page_size of every pool.
+ *   Chunks hold tokens [token_begin, token_begin + n_tokens) of one request for layers
+ *   [layer_begin, layer_begin + n_layers):
+ *     KVX_CHUNK_LAYER_MAJOR  [layer][kv][token][token_bytes]  (page-first, generalised to
+ *                            a multi-page chunk)
+ *     KVX_CHUNK_TOKEN_MAJOR  [token][layer][kv][token_bytes]
+ *   A call moves only layers inside its window [layer_begin, layer_end) (half-open),
+ *   intersected with each chunk's own layers; chunk offsets stay relative to the chunk's
+ *   own layer_begin.
+ *
+ * Ownership.  The caller owns the pools, page tables, chunk memory and streams.  A
+ * kvx_ctx owns only a small ring of descriptor buffers (pinned host + device) and a
+ * device status word.  Nothing on the transfer path allocates.
+ *
+ * Asynchrony and errors.  Every transfer call validates on the host, packs O(chunks)
+ * descriptors, copies them to the device and launches ONE kernel on the given stream,
+ * then returns.  A host-detected error returns a non-zero kvx_status and launches
+ * nothing; kvx_last_error() then holds a message.  Errors the kernel meets (a page id
+ * outside the pool) set a bit in the device status word and skip that page, without
+ * trapping; kvx_get_status() reads and clears it.  A kvx_ctx must not be used from two
+ * host threads at once.  Descriptor buffers are reused round-robin; before reusing one
+ * the call waits for the kernel that last used it.
+ */
+#ifndef KVX_H
+#define KVX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVX_VERSION 1
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *kvx_stream_t;
+
+typedef enum kvx_status {
+    KVX_OK = 0,
+    KVX_ERR_INVALID_ARG = 1,            /* a size, index, range or pointer is invalid */
+    KVX_ERR_ALIGNMENT = 2,              /* a pointer or token_bytes is not 16-byte aligned */
+    KVX_ERR_NOT_DEVICE_ACCESSIBLE = 3,  /* chunk or pool memory the GPU cannot reach */
+    KVX_ERR_PAGE_OUT_OF_RANGE = 4,      /* a page id outside [0, num_pages) */
+    KVX_ERR_OVERLAP = 5,                /* two loads of one batch write the same page slot */
+    KVX_ERR_CUDA = 6,                   /* a CUDA runtime call failed */
+    KVX_ERR_DEVICE_STATUS = 7,          /* the kernel reported an error (see flags) */
+    KVX_ERR_CAPACITY = 8                /* descriptors exceed the ctx's buffer size */
+} kvx_status;
+
+/* Bits of the device status word (kvx_get_status). */
+#define KVX_DEV_PAGE_OUT_OF_RANGE 0x1u
+
+typedef enum kvx_chunk_layout {
+    KVX_CHUNK_LAYER_MAJOR = 0,
+    KVX_CHUNK_TOKEN_MAJOR = 1
+} kvx_chunk_layout;
+
+/* Direction of kvx_transform_hbm and kvx_dma_baseline. */
+#define KVX_DIR_GATHER 0   /* pages -> chunks (a store) */
+#define KVX_DIR_SCATTER 1  /* chunks -> pages (a load) */
+
+typedef struct kvx_pool {
+    int32_t num_layers;
+    int32_t kv_factor;     /* 2: separate K and V pools; 1: one latent pool (MLA) */
+    int32_t page_size;     /* tokens per page, > 0 */
+    int32_t num_pages;     /* pages in each pool, > 0 */
+    int64_t token_bytes;   /* one token's vector in one pool (heads x head_dim x dtype
+                              bytes); a positive multiple of 16 */
+    void *const *k_pages;  /* HOST array [num_layers] of device pointers: layer l's K pool
+                              [num_pages][page_size][token_bytes], 16-byte aligned */
+    void *const *v_pages;  /* same for V; ignored (may be NULL) when kv_factor == 1 */
+} kvx_pool;
+
+typedef struct kvx_request {
+    const int32_t *page_table;       /* device-accessible [ceil(n_tokens / page_size)]
+                                        physical page ids; read by the kernel */
+    const int32_t *page_table_host;  /* optional host copy of the same table: enables the
+                                        page-range and overlap checks of validation level 2;
+                                        required by kvx_dma_baseline */
+    int32_t n_tokens;                /* tokens in the request, >= 0 */
+    int32_t reserved;                /* set to 0 */
+} kvx_request;
+
+typedef struct kvx_chunk {
+    int32_t request;      /* index into the request array */
+    int32_t token_begin;  /* first token, >= 0 */
+    int32_t n_tokens;     /* tokens, token_begin + n_tokens <= request's n_tokens */
+    int32_t layer_begin;  /* first layer held by the chunk */
+    int32_t n_layers;     /* layers held, layer_begin + n_layers <= num_layers */
+    int32_t layout;       /* kvx_chunk_layout */
+    void *ptr;            /* chunk memory, 16-byte aligned, n_layers x kv_factor x n_tokens
+                             x token_bytes bytes: mapped pinned host memory for
+                             store/load, device memory for kvx_transform_hbm */
+} kvx_chunk;
+
+/* Work mapping of the transfer kernel. */
+#define KVX_MAP_WARP_SEGMENT 0  /* one warp per (chunk, layer, kv, page) segment */
+
+/* Store cache hint for the destination of each 16-byte unit. */
+#define KVX_HINT_DEFAULT 0      /* st.global (write-back) */
+#define KVX_HINT_STREAMING 1    /* st.global.cs (evict-first, cache streaming) */
+
+typedef struct kvx_launch_cfg {
+    int32_t sm_cap;       /* CTAs launched = sm_cap x ctas_per_sm (fewer when the batch has
+                             less work); with ctas_per_sm = 1 the kernel occupies at most
+                             sm_cap SMs.  0 = every SM */
+    int32_t ctas_per_sm;  /* 0 = the operation's default */
+    int32_t threads;      /* threads per CTA, multiple of 32 in [32, 1024]; 0 = default */
+    int32_t unroll;       /* 16-byte loads in flight per lane before its stores: 1, 2, 4
+                             or 8; 0 = default */
+    int32_t store_hint;   /* KVX_HINT_* */
+    int32_t mapping;      /* KVX_MAP_* */
+} kvx_launch_cfg;
+
+typedef struct kvx_ctx kvx_ctx;
+
+/* Operation ids (kvx_default_launch_cfg, kvx_validate). */
+#define KVX_OP_STORE 0        /* pages -> chunks in mapped pinned host memory */
+#define KVX_OP_LOAD 1         /* chunks in mapped pinned host memory -> pages */
+#define KVX_OP_GATHER_HBM 2   /* pages -> chunks in device memory */
+#define KVX_OP_SCATTER_HBM 3  /* chunks in device memory -> pages */
+
+/* ---------------------------------------------------------------- context */
+
+/* Create a context on `device` whose descriptor buffers hold up to
+ * max_descriptor_bytes each (0 = 8 MiB; about 72 bytes per chunk).  Allocates four
+ * pinned host + device descriptor buffers and a device status word.  Requires a GPU. */
+kvx_status kvx_create(kvx_ctx **out, int device, size_t max_descriptor_bytes);
+
+/* Synchronize with every kernel the context launched, then free its buffers. */
+void kvx_destroy(kvx_ctx *ctx);
+
+/* 0: no validation.  1 (default): O(chunks) arithmetic checks of every size, range and
+ * alignment.  2: also page ids and load-destination overlap against page_table_host
+ * (O(tokens)) and cudaPointerGetAttributes on every chunk and pool pointer. */
+kvx_status kvx_set_validation(kvx_ctx *ctx, int level);
+
+/* Default launch configuration of an operation (KVX_OP_*) on this context's GPU. */
+kvx_status kvx_default_launch_cfg(const kvx_ctx *ctx, int op, kvx_launch_cfg *cfg);
+
+/* ---------------------------------------------------------------- transfers */
+
+/* store: gather every covered (layer, kv, token) vector from the page pools into the
+ * chunks ("Strata Guide", section "Non-Intrusive Resource Sizing": eviction to host
+ * memory; "Tutti", section 7: store_layer(layer_id, block_ids)).  Chunks live in mapped
+ * pinned host memory.  cfg may be NULL (defaults).  Asynchronous on `stream`. */
+kvx_status kvx_store_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *reqs,
+                            int n_req, const kvx_chunk *chunks, int n_chunks,
+                            int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                            kvx_stream_t stream);
+
+/* load: scatter chunks from mapped pinned host memory into the pages named by the page
+ * tables ("Strata Guide", section "Step 1: High-Performance GPU-Assisted I/O CUDA
+ * Kernel"; "Tutti", section 7: retrieve_layer(layer_id, block_ids)).  Destination slots
+ * must be disjoint across the batch (checked at validation level 2).  Slots of a page
+ * past the request's last token are not written. */
+kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *reqs,
+                           int n_req, const kvx_chunk *chunks, int n_chunks,
+                           int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                           kvx_stream_t stream);
+
+/* transform: the same gather (dir = KVX_DIR_GATHER) or scatter (KVX_DIR_SCATTER) with
+ * the chunks in device memory: the explicit HBM-to-HBM layout pass that "Strata Guide",
+ * section "Two-Dimensional Memory Layout Decoupling", names as the conventional cost. */
+kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,
+                             const kvx_request *reqs, int n_req, const kvx_chunk *chunks,
+                             int n_chunks, int layer_begin, int layer_end,
+                             const kvx_launch_cfg *cfg, kvx_stream_t stream);
+
+/* Comparison baseline only: the same transfer as one cudaMemcpyAsync per contiguous
+ * (chunk, layer, kv, page) segment (cudaMemcpy2DAsync for token-major chunks), issued
+ * from this host thread ("Strata Guide", section "The Conflict Between PagedAttention
+ * and Transfer Efficiency": one DMA per page and layer).  Needs page_table_host on every
+ * request.  n_copies (may be NULL) receives the number of copies issued. */
+kvx_status kvx_dma_baseline(kvx_ctx *ctx, int dir, const kvx_pool *pool,
+                            const kvx_request *reqs, int n_req, const kvx_chunk *chunks,
+                            int n_chunks, int layer_begin, int layer_end,
+                            kvx_stream_t stream, int64_t *n_copies);
+
+/* Read the device status word (after synchronizing `stream`), clear it, and return
+ * KVX_ERR_DEVICE_STATUS if any bit was set.  flags may be NULL. */
+kvx_status kvx_get_status(kvx_ctx *ctx, kvx_stream_t stream, uint32_t *flags);
+
+/* Message describing the last error of this context ("" if none). */
+const char *kvx_last_error(const kvx_ctx *ctx);
+
+/* Shape of the context's last kernel launch: work items (page segments), CTAs, threads
+ * per CTA and bytes of descriptors copied to the device; zeros if the last call launched
+ * nothing.  Any output may be NULL. */
+kvx_status kvx_last_launch(const kvx_ctx *ctx, int64_t *items, int32_t *ctas,
+                           int32_t *threads, int64_t *descriptor_bytes);
+
+/* ---------------------------------------------------------------- host logic (no GPU) */
+
+/* Validate a transfer of kind `op` (KVX_OP_*) at `level` (1 or 2; level 2's pointer
+ * checks need a GPU and are skipped when none is present).  On failure a message is
+ * written to msg (if msg_len > 0). */
+kvx_status kvx_validate(const kvx_pool *pool, const kvx_request *reqs, int n_req,
+                        const kvx_chunk *chunks, int n_chunks, int layer_begin,
+                        int layer_end, int op, int level, char *msg, size_t msg_len);
+
+/* Count the page segments of a transfer -- one per (chunk, covered layer, kv, page the
+ * chunk touches); each is one copy of the DMA baseline (a 2D copy for a token-major
+ * chunk) and one work item of the kernel -- and its payload bytes (one direction).
+ * Either output may be NULL. */
+kvx_status kvx_plan_count(const kvx_pool *pool, const kvx_request *reqs, int n_req,
+                          const kvx_chunk *chunks, int n_chunks, int layer_begin,
+                          int layer_end, int64_t *n_segments, int64_t *n_bytes);
+
+/* Chunk-size policy: tokens and layers per chunk for a request's KV.
+ * layer_streaming != 0 asks for per-layer chunks (one layer per chunk, for transfers
+ * issued layer by layer); otherwise chunks hold all layers (page-first).  target_bytes
+ * is the wanted chunk size, 0 = the library default.  tokens_per_chunk is always a
+ * positive multiple of page_size, so no chunk boundary splits a page. */
+kvx_status kvx_chunk_policy(const kvx_pool *pool, int layer_streaming, int64_t target_bytes,
+                            int32_t *tokens_per_chunk, int32_t *layers_per_chunk);
+
+/* Pinned host memory, mapped into the device address space (allocate or register
+ * once, up front, never on the transfer path). */
+kvx_status kvx_host_alloc(void **ptr, size_t bytes);
+kvx_status kvx_host_free(void *ptr);
+kvx_status kvx_host_register(void *ptr, size_t bytes);
+kvx_status kvx_host_unregister(void *ptr);
+
+const char *kvx_status_string(kvx_status status);
+int kvx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVX_H */

@@ -93,7 +93,11 @@ def _lib():
 
 @dataclass
 class Pool:
-    """K/V page pools: ``pools[kv][layer]`` is a uint8 array [num_pages, page_size, token_bytes]."""
+    """K/V page pools: ``pools[kv][layer]`` is a uint8 array [num_pages, page_size, token_bytes].
+
+    A layer may be ``None`` (not materialised) when every call on the pool uses a layer
+    window that excludes it; the C loops never touch layers outside the window.
+    """
     pools: List[List[np.ndarray]]
     page_size: int
 
@@ -106,12 +110,20 @@ class Pool:
         return len(self.pools[0])
 
     @property
+    def layer_shape(self):
+        for per_kv in self.pools:
+            for a in per_kv:
+                if a is not None:
+                    return a.shape
+        raise ValueError("pool has no materialised layer")
+
+    @property
     def num_pages(self) -> int:
-        return self.pools[0][0].shape[0]
+        return self.layer_shape[0]
 
     @property
     def token_bytes(self) -> int:
-        return self.pools[0][0].shape[2]
+        return self.layer_shape[2]
 
 
 @dataclass
@@ -147,11 +159,14 @@ def _check_array(a: np.ndarray, what: str) -> None:
 def _marshal(pool: Pool, reqs: Sequence[Request], chunks: Sequence[Chunk]) -> _Marshalled:
     keep = []
     ptrs = (ctypes.c_void_p * (pool.kv_factor * pool.num_layers))()
+    shape = pool.layer_shape
     for k in range(pool.kv_factor):
         for l in range(pool.num_layers):
             a = pool.pools[k][l]
+            if a is None:  # layer not materialised: the call's layer window must skip it
+                continue
             _check_array(a, "pool")
-            if a.shape != (pool.num_pages, pool.page_size, pool.token_bytes):
+            if a.shape != shape:
                 raise ValueError("pool arrays must share one shape")
             ptrs[k * pool.num_layers + l] = a.ctypes.data
     cpool = _Pool(pool.num_layers, pool.kv_factor, pool.page_size, pool.num_pages,

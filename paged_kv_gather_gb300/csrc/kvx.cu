@@ -1,0 +1,641 @@
+// kvx.cu -- GB300 (sm_103a) kernels and C-ABI entry points of the paged KV gather/scatter
+// library.
+//
+// One kernel family moves every byte.  A persistent grid of warps walks the batch's work
+// items; an item is one (chunk, layer, kv, page) segment, contiguous on the page side
+// ("Strata Guide: Hierarchical Context Caching for Long LLMs", section "Two-Dimensional
+// Memory Layout Decoupling": the layout change is address arithmetic done by the moving
+// thread, not a separate pass).  Each lane moves 16-byte units ("Step 1:
+// High-Performance GPU-Assisted I/O CUDA Kernel": 128-bit vector accesses, a page-table
+// lookup per unit of work, streaming stores into HBM), with `unroll` independent loads in
+// flight per lane before its stores, because host-link reads need many bytes in flight
+// (section "The Physics of I/O Bandwidth and Little's Law": X = C * S / L).  The grid is
+// capped to a few SMs for host transfers so a concurrent compute stream keeps the rest
+// (section "Non-Intrusive Resource Sizing"); the HBM-only transform uses every SM.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kvx_internal.h"
+
+using kvx::DevChunk;
+using kvx::Plan;
+
+// ------------------------------------------------------------------------------- device
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+template <int HINT>
+__device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v)
+{
+    if (HINT == KVX_HINT_STREAMING)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+    else
+        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+}
+
+// Chunk owning `item`: the largest c with item_begin[c] <= item.  A 32-way search: each
+// step the warp probes 32 evenly spaced entries and keeps the last one not above `item`,
+// so 18k chunks take three coalesced probes.
+__device__ __forceinline__ int find_chunk(const int64_t *__restrict__ begin, int n, int64_t item,
+                                          int lane)
+{
+    int lo = 0, hi = n;  // begin[lo] <= item < begin[hi]
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int idx = lo + lane * step;
+        const bool ok = idx < hi && __ldg(begin + idx) <= item;
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        lo += (31 - __clz(m)) * step;
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
+
+// Contiguous copy of n16 16-byte units.  Lane i owns units i, i + 32, i + 64, ...; each
+// pass issues U independent loads before its U stores.
+template <int U, int HINT>
+__device__ __forceinline__ void copy_contig(const uint4 *__restrict__ s, uint4 *__restrict__ d,
+                                            int n16, int lane)
+{
+    s += lane;
+    d += lane;
+    int rem = n16 - lane;  // units of this lane's stride left, scaled by 32
+    for (; rem > 32 * (U - 1); rem -= 32 * U, s += 32 * U, d += 32 * U) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            r[u] = ld_nc_v4(s + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            st_v4<HINT>(d + 32 * u, r[u]);
+    }
+    if (rem > 0) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (32 * u < rem)
+                r[u] = ld_nc_v4(s + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (32 * u < rem)
+                st_v4<HINT>(d + 32 * u, r[u]);
+    }
+}
+
+// Warp per page segment.  DIR = KVX_DIR_GATHER copies page -> chunk, KVX_DIR_SCATTER the
+// reverse.
+template <int U, int DIR, int HINT>
+__global__ void __launch_bounds__(1024, U <= 4 ? 2 : 1) kvx_segment_kernel(const Plan p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int64_t v = p.token_bytes;
+    for (int64_t item = warp; item < p.total_items; item += n_warps) {
+        const int c = find_chunk(p.item_begin, p.n_chunks, item, lane);
+        const DevChunk &ch = p.chunks[c];
+        const int64_t i = item - p.item_begin[c];
+        const int32_t np = ch.np;
+        const int32_t slab = int32_t(i / np);
+        const int32_t j = int32_t(i - int64_t(slab) * np);
+        const int32_t kv = p.kv_factor == 2 ? (slab & 1) : 0;
+        const int32_t layer = ch.la + (p.kv_factor == 2 ? (slab >> 1) : slab);
+        const int32_t lpage = ch.pf + j;
+        const int32_t pt0 = lpage * p.page_size;
+        const int32_t tb = max(ch.t0, pt0);
+        const int32_t te = min(ch.t_end, pt0 + p.page_size);
+        const int32_t page = p.reqs[ch.request].page_table[lpage];
+        if (unsigned(page) >= unsigned(p.num_pages)) {
+            if (lane == 0)
+                atomicOr(p.status, KVX_DEV_PAGE_OUT_OF_RANGE);
+            continue;
+        }
+        char *pg = p.pools[kv * p.num_layers + layer] +
+                   (int64_t(page) * p.page_size + (tb - pt0)) * v;
+        char *ck = ch.ptr + int64_t(ch.slab0 + slab) * ch.slab_stride +
+                   int64_t(tb - ch.t0) * ch.row_stride;
+        const char *src = DIR == KVX_DIR_GATHER ? pg : ck;
+        char *dst = DIR == KVX_DIR_GATHER ? ck : pg;
+        const int rows = te - tb;
+        if (ch.row_stride == v) {
+            copy_contig<U, HINT>(reinterpret_cast<const uint4 *>(src),
+                                 reinterpret_cast<uint4 *>(dst), int((int64_t(rows) * v) >> 4),
+                                 lane);
+        } else {
+            // Token-major chunk: each token is its own run on the chunk side.
+            const int64_t s_pitch = DIR == KVX_DIR_GATHER ? v : ch.row_stride;
+            const int64_t d_pitch = DIR == KVX_DIR_GATHER ? ch.row_stride : v;
+            for (int r = 0; r < rows; ++r)
+                copy_contig<1, HINT>(reinterpret_cast<const uint4 *>(src + r * s_pitch),
+                                     reinterpret_cast<uint4 *>(dst + r * d_pitch), int(v >> 4),
+                                     lane);
+        }
+    }
+}
+
+typedef void (*KernelFn)(Plan);
+
+template <int U>
+KernelFn pick_hint_dir(int dir, int hint)
+{
+    if (dir == KVX_DIR_GATHER)
+        return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_GATHER, 1>
+                                          : kvx_segment_kernel<U, KVX_DIR_GATHER, 0>;
+    return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_SCATTER, 1>
+                                      : kvx_segment_kernel<U, KVX_DIR_SCATTER, 0>;
+}
+
+KernelFn pick_kernel(int unroll, int dir, int hint)
+{
+    switch (unroll) {
+    case 1: return pick_hint_dir<1>(dir, hint);
+    case 2: return pick_hint_dir<2>(dir, hint);
+    case 4: return pick_hint_dir<4>(dir, hint);
+    case 8: return pick_hint_dir<8>(dir, hint);
+    }
+    return nullptr;
+}
+
+}  // namespace
+
+// --------------------------------------------------------------------------------- host
+
+namespace {
+
+const int kSlots = 4;
+const size_t kDefaultDescriptorBytes = 8u << 20;
+
+struct Slot {
+    char *host = nullptr;
+    char *dev = nullptr;
+    cudaEvent_t done = nullptr;
+    bool used = false;
+};
+
+}  // namespace
+
+struct kvx_ctx {
+    int device = 0;
+    int num_sms = 0;
+    int validation = 1;
+    size_t slot_bytes = 0;
+    Slot slots[kSlots];
+    int next = 0;
+    unsigned int *status_dev = nullptr;
+    unsigned int *status_host = nullptr;
+    int64_t last_items = 0;
+    int32_t last_ctas = 0;
+    int32_t last_threads = 0;
+    int64_t last_desc_bytes = 0;
+    char err[512] = {0};
+};
+
+namespace {
+
+kvx_status set_err(kvx_ctx *ctx, kvx_status st, const char *fmt, ...)
+    __attribute__((format(printf, 3, 4)));
+
+kvx_status set_err(kvx_ctx *ctx, kvx_status st, const char *fmt, ...)
+{
+    if (ctx) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(ctx->err, sizeof ctx->err, fmt, ap);
+        va_end(ap);
+    }
+    return st;
+}
+
+kvx_status cuda_err(kvx_ctx *ctx, cudaError_t e, const char *what)
+{
+    return set_err(ctx, KVX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Keeps ctx->device current for the duration of a call and restores the caller's device.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            prev = -1;
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess)
+            ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+            cudaSetDevice(prev);
+    }
+};
+
+void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
+{
+    c->mapping = KVX_MAP_WARP_SEGMENT;
+    switch (op) {
+    case KVX_OP_STORE:
+        c->sm_cap = 16;
+        c->ctas_per_sm = 1;
+        c->threads = 1024;
+        c->unroll = 8;
+        c->store_hint = KVX_HINT_DEFAULT;
+        break;
+    case KVX_OP_LOAD:
+        c->sm_cap = 16;
+        c->ctas_per_sm = 1;
+        c->threads = 1024;
+        c->unroll = 8;
+        c->store_hint = KVX_HINT_STREAMING;
+        break;
+    default:  // HBM transform: the whole GPU
+        c->sm_cap = 0;
+        c->ctas_per_sm = 2;
+        c->threads = 1024;
+        c->unroll = 4;
+        c->store_hint = KVX_HINT_STREAMING;
+        break;
+    }
+    (void)ctx;
+}
+
+kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_launch_cfg *out)
+{
+    kvx_launch_cfg d;
+    defaults_for(ctx, op, &d);
+    *out = d;
+    if (!user)
+        return KVX_OK;
+    out->sm_cap = user->sm_cap;  // 0 means every SM
+    if (user->ctas_per_sm)
+        out->ctas_per_sm = user->ctas_per_sm;
+    if (user->threads)
+        out->threads = user->threads;
+    if (user->unroll)
+        out->unroll = user->unroll;
+    out->store_hint = user->store_hint;
+    out->mapping = user->mapping;
+    if (out->sm_cap < 0 || out->ctas_per_sm < 1 || out->ctas_per_sm > 32 ||
+        out->threads < 32 || out->threads > 1024 || out->threads % 32 != 0 ||
+        (out->store_hint != KVX_HINT_DEFAULT && out->store_hint != KVX_HINT_STREAMING) ||
+        out->mapping != KVX_MAP_WARP_SEGMENT || !pick_kernel(out->unroll, 0, 0))
+        return set_err(ctx, KVX_ERR_INVALID_ARG,
+                       "launch cfg: sm_cap %d ctas_per_sm %d threads %d unroll %d hint %d "
+                       "mapping %d", user->sm_cap, user->ctas_per_sm, user->threads,
+                       user->unroll, user->store_hint, user->mapping);
+    return KVX_OK;
+}
+
+kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request *reqs, int n_req,
+                  const kvx_chunk *chunks, int n_chunks, int layer_begin, int layer_end,
+                  const kvx_launch_cfg *user_cfg, kvx_stream_t stream)
+{
+    if (!ctx)
+        return KVX_ERR_INVALID_ARG;
+    ctx->last_items = 0;
+    ctx->last_ctas = 0;
+    ctx->last_threads = 0;
+    ctx->last_desc_bytes = 0;
+    kvx_launch_cfg cfg;
+    kvx_status st = resolve_cfg(ctx, op, user_cfg, &cfg);
+    if (st != KVX_OK)
+        return st;
+    st = kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, op,
+                       ctx->validation, true, ctx->err, sizeof ctx->err);
+    if (st != KVX_OK)
+        return st;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
+
+    const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
+    if (lay.total > ctx->slot_bytes)
+        return set_err(ctx, KVX_ERR_CAPACITY,
+                       "descriptors need %zu bytes, the context holds %zu per call; create it "
+                       "with a larger max_descriptor_bytes", lay.total, ctx->slot_bytes);
+    Slot &slot = ctx->slots[ctx->next];
+    if (slot.used) {
+        cudaError_t e = cudaEventSynchronize(slot.done);
+        if (e != cudaSuccess)
+            return cuda_err(ctx, e, "waiting for a descriptor buffer");
+    }
+    const int dir = (op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM) ? KVX_DIR_SCATTER
+                                                                    : KVX_DIR_GATHER;
+    Plan plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
+                          slot.host, slot.dev);
+    plan.status = ctx->status_dev;
+    if (plan.total_items == 0)
+        return KVX_OK;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, lay.total, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "descriptor copy");
+    const int64_t warps_per_cta = cfg.threads / 32;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
+    const int64_t needed = (plan.total_items + warps_per_cta - 1) / warps_per_cta;
+    if (ctas > needed)
+        ctas = needed;
+    KernelFn fn = pick_kernel(cfg.unroll, dir, cfg.store_hint);
+    void *args[] = {&plan};
+    e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
+                         dim3(unsigned(cfg.threads)), args, 0, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "kernel launch");
+    e = cudaEventRecord(slot.done, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "event record");
+    slot.used = true;
+    ctx->next = (ctx->next + 1) % kSlots;
+    ctx->last_items = plan.total_items;
+    ctx->last_ctas = int32_t(ctas);
+    ctx->last_threads = cfg.threads;
+    ctx->last_desc_bytes = int64_t(lay.total);
+    return KVX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvx_status kvx_create(kvx_ctx **out, int device, size_t max_descriptor_bytes)
+{
+    if (!out)
+        return KVX_ERR_INVALID_ARG;
+    *out = nullptr;
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) {
+        cudaGetLastError();
+        return KVX_ERR_CUDA;
+    }
+    kvx_ctx *ctx = new kvx_ctx();
+    ctx->device = device;
+    ctx->slot_bytes = max_descriptor_bytes ? max_descriptor_bytes : kDefaultDescriptorBytes;
+    DeviceGuard guard(device);
+    cudaError_t e = guard.ok ? cudaSuccess : cudaErrorInvalidDevice;
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
+    for (int i = 0; i < kSlots && e == cudaSuccess; ++i) {
+        e = cudaHostAlloc(reinterpret_cast<void **>(&ctx->slots[i].host), ctx->slot_bytes,
+                          cudaHostAllocDefault);
+        if (e == cudaSuccess)
+            e = cudaMalloc(reinterpret_cast<void **>(&ctx->slots[i].dev), ctx->slot_bytes);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&ctx->slots[i].done, cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&ctx->status_dev), 256);
+    if (e == cudaSuccess)
+        e = cudaMemset(ctx->status_dev, 0, 256);
+    if (e == cudaSuccess)
+        e = cudaHostAlloc(reinterpret_cast<void **>(&ctx->status_host), 64, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+        kvx_destroy(ctx);
+        return KVX_ERR_CUDA;
+    }
+    *out = ctx;
+    return KVX_OK;
+}
+
+void kvx_destroy(kvx_ctx *ctx)
+{
+    if (!ctx)
+        return;
+    {
+        DeviceGuard guard(ctx->device);
+        for (int i = 0; i < kSlots; ++i) {
+            Slot &s = ctx->slots[i];
+            if (s.done) {
+                if (s.used)
+                    cudaEventSynchronize(s.done);
+                cudaEventDestroy(s.done);
+            }
+            if (s.dev)
+                cudaFree(s.dev);
+            if (s.host)
+                cudaFreeHost(s.host);
+        }
+        if (ctx->status_dev)
+            cudaFree(ctx->status_dev);
+        if (ctx->status_host)
+            cudaFreeHost(ctx->status_host);
+    }
+    delete ctx;
+}
+
+kvx_status kvx_set_validation(kvx_ctx *ctx, int level)
+{
+    if (!ctx || level < 0 || level > 2)
+        return KVX_ERR_INVALID_ARG;
+    ctx->validation = level;
+    return KVX_OK;
+}
+
+kvx_status kvx_default_launch_cfg(const kvx_ctx *ctx, int op, kvx_launch_cfg *cfg)
+{
+    if (!ctx || !cfg || op < KVX_OP_STORE || op > KVX_OP_SCATTER_HBM)
+        return KVX_ERR_INVALID_ARG;
+    defaults_for(ctx, op, cfg);
+    return KVX_OK;
+}
+
+kvx_status kvx_store_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *reqs,
+                            int n_req, const kvx_chunk *chunks, int n_chunks, int layer_begin,
+                            int layer_end, const kvx_launch_cfg *cfg, kvx_stream_t stream)
+{
+    return launch(ctx, KVX_OP_STORE, pool, reqs, n_req, chunks, n_chunks, layer_begin,
+                  layer_end, cfg, stream);
+}
+
+kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *reqs,
+                           int n_req, const kvx_chunk *chunks, int n_chunks, int layer_begin,
+                           int layer_end, const kvx_launch_cfg *cfg, kvx_stream_t stream)
+{
+    return launch(ctx, KVX_OP_LOAD, pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                  cfg, stream);
+}
+
+kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,
+                             const kvx_request *reqs, int n_req, const kvx_chunk *chunks,
+                             int n_chunks, int layer_begin, int layer_end,
+                             const kvx_launch_cfg *cfg, kvx_stream_t stream)
+{
+    if (dir != KVX_DIR_GATHER && dir != KVX_DIR_SCATTER)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "transform direction %d", dir);
+    return launch(ctx, dir == KVX_DIR_GATHER ? KVX_OP_GATHER_HBM : KVX_OP_SCATTER_HBM, pool,
+                  reqs, n_req, chunks, n_chunks, layer_begin, layer_end, cfg, stream);
+}
+
+kvx_status kvx_dma_baseline(kvx_ctx *ctx, int dir, const kvx_pool *pool,
+                            const kvx_request *reqs, int n_req, const kvx_chunk *chunks,
+                            int n_chunks, int layer_begin, int layer_end, kvx_stream_t stream,
+                            int64_t *n_copies)
+{
+    if (!ctx)
+        return KVX_ERR_INVALID_ARG;
+    if (n_copies)
+        *n_copies = 0;
+    if (dir != KVX_DIR_GATHER && dir != KVX_DIR_SCATTER)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "baseline direction %d", dir);
+    // Chunks may sit in host or device memory here, so the pointer-type checks of level 2
+    // do not apply; sizes, ranges and alignment are checked as for the kernels.
+    const int level = ctx->validation < 1 ? ctx->validation : 1;
+    kvx_status st = kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                                  dir == KVX_DIR_GATHER ? KVX_OP_STORE : KVX_OP_LOAD, level,
+                                  false, ctx->err, sizeof ctx->err);
+    if (st != KVX_OK)
+        return st;
+    for (int r = 0; r < n_req; ++r)
+        if (reqs[r].n_tokens > 0 && !reqs[r].page_table_host)
+            return set_err(ctx, KVX_ERR_INVALID_ARG,
+                           "request %d: the DMA baseline needs page_table_host", r);
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t v = pool->token_bytes;
+    const int32_t P = pool->page_size;
+    int64_t copies = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+        const kvx_chunk &ch = chunks[c];
+        const int32_t *pt = reqs[ch.request].page_table_host;
+        int lo, hi;
+        kvx::chunk_layers(ch, layer_begin, layer_end, &lo, &hi);
+        if (lo >= hi || ch.n_tokens == 0)
+            continue;
+        const bool lm = ch.layout == KVX_CHUNK_LAYER_MAJOR;
+        const int64_t slab_stride = lm ? int64_t(ch.n_tokens) * v : v;
+        const int64_t row_stride = lm ? v : int64_t(ch.n_layers) * pool->kv_factor * v;
+        const int32_t t_end = ch.token_begin + ch.n_tokens;
+        for (int l = lo; l < hi; ++l)
+            for (int kv = 0; kv < pool->kv_factor; ++kv) {
+                char *base = static_cast<char *>((kv == 0 ? pool->k_pages : pool->v_pages)[l]);
+                const int64_t slab = int64_t(l - ch.layer_begin) * pool->kv_factor + kv;
+                for (int32_t lp = ch.token_begin / P; lp * P < t_end; ++lp) {
+                    const int32_t tb = lp * P > ch.token_begin ? lp * P : ch.token_begin;
+                    const int32_t te = (lp + 1) * P < t_end ? (lp + 1) * P : t_end;
+                    const int32_t page = pt[lp];
+                    if (page < 0 || page >= pool->num_pages)
+                        return set_err(ctx, KVX_ERR_PAGE_OUT_OF_RANGE, "page id %d", page);
+                    char *pg = base + (int64_t(page) * P + (tb - lp * P)) * v;
+                    char *ck = static_cast<char *>(ch.ptr) + slab * slab_stride +
+                               int64_t(tb - ch.token_begin) * row_stride;
+                    char *dst = dir == KVX_DIR_GATHER ? ck : pg;
+                    const char *src = dir == KVX_DIR_GATHER ? pg : ck;
+                    cudaError_t e;
+                    if (row_stride == v)
+                        e = cudaMemcpyAsync(dst, src, size_t(te - tb) * v, cudaMemcpyDefault, s);
+                    else
+                        e = cudaMemcpy2DAsync(dst, dir == KVX_DIR_GATHER ? row_stride : v, src,
+                                              dir == KVX_DIR_GATHER ? v : row_stride, v,
+                                              size_t(te - tb), cudaMemcpyDefault, s);
+                    if (e != cudaSuccess)
+                        return cuda_err(ctx, e, "baseline copy");
+                    ++copies;
+                }
+            }
+    }
+    if (n_copies)
+        *n_copies = copies;
+    return KVX_OK;
+}
+
+kvx_status kvx_get_status(kvx_ctx *ctx, kvx_stream_t stream, uint32_t *flags)
+{
+    if (!ctx)
+        return KVX_ERR_INVALID_ARG;
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(ctx->status_host, ctx->status_dev, sizeof(unsigned int),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(ctx->status_dev, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "reading the device status");
+    const uint32_t f = *ctx->status_host;
+    if (flags)
+        *flags = f;
+    if (f)
+        return set_err(ctx, KVX_ERR_DEVICE_STATUS, "device status 0x%x", f);
+    return KVX_OK;
+}
+
+const char *kvx_last_error(const kvx_ctx *ctx) { return ctx ? ctx->err : ""; }
+
+kvx_status kvx_last_launch(const kvx_ctx *ctx, int64_t *items, int32_t *ctas, int32_t *threads,
+                           int64_t *descriptor_bytes)
+{
+    if (!ctx)
+        return KVX_ERR_INVALID_ARG;
+    if (descriptor_bytes)
+        *descriptor_bytes = ctx->last_desc_bytes;
+    if (items)
+        *items = ctx->last_items;
+    if (ctas)
+        *ctas = ctx->last_ctas;
+    if (threads)
+        *threads = ctx->last_threads;
+    return KVX_OK;
+}
+
+kvx_status kvx_host_alloc(void **ptr, size_t bytes)
+{
+    if (!ptr || bytes == 0)
+        return KVX_ERR_INVALID_ARG;
+    cudaError_t e = cudaHostAlloc(ptr, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *ptr = nullptr;
+        return KVX_ERR_CUDA;
+    }
+    return KVX_OK;
+}
+
+kvx_status kvx_host_free(void *ptr)
+{
+    if (!ptr)
+        return KVX_OK;
+    return cudaFreeHost(ptr) == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
+}
+
+kvx_status kvx_host_register(void *ptr, size_t bytes)
+{
+    if (!ptr || bytes == 0)
+        return KVX_ERR_INVALID_ARG;
+    cudaError_t e =
+        cudaHostRegister(ptr, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return KVX_ERR_CUDA;
+    }
+    return KVX_OK;
+}
+
+kvx_status kvx_host_unregister(void *ptr)
+{
+    if (!ptr)
+        return KVX_ERR_INVALID_ARG;
+    return cudaHostUnregister(ptr) == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
+}
+
+}  // extern "C"

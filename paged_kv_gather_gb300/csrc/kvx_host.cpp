@@ -1,0 +1,392 @@
+// kvx_host.cpp -- host logic of the KV gather/scatter library: validation, descriptor
+// packing, segment counting, the chunk-size policy.  Runs without a GPU except for the
+// pointer-attribute checks of validation level 2.
+#include <cuda_runtime_api.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "kvx_internal.h"
+
+namespace kvx {
+namespace {
+
+kvx_status fail(kvx_status st, char *msg, size_t len, const char *fmt, ...)
+{
+    if (msg && len > 0) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(msg, len, fmt, ap);
+        va_end(ap);
+    }
+    return st;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool op_is_scatter(int op) { return op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM; }
+
+int64_t pages_of(int64_t n_tokens, int64_t page_size) { return (n_tokens + page_size - 1) / page_size; }
+
+// Level 2: the memory behind p must be reachable by the GPU at the same address.
+kvx_status check_pointer(const void *p, bool want_host, const char *what, int index, char *msg,
+                         size_t len)
+{
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(KVX_ERR_CUDA, msg, len, "%s %d: cudaPointerGetAttributes: %s", what, index,
+                    cudaGetErrorString(e));
+    }
+    if (a.type == cudaMemoryTypeUnregistered)
+        return fail(KVX_ERR_NOT_DEVICE_ACCESSIBLE, msg, len,
+                    "%s %d: pageable host memory; allocate with kvx_host_alloc or pin it with "
+                    "kvx_host_register", what, index);
+    if (a.devicePointer != p)
+        return fail(KVX_ERR_NOT_DEVICE_ACCESSIBLE, msg, len,
+                    "%s %d: not mapped at the same address on the device", what, index);
+    if (want_host && a.type == cudaMemoryTypeDevice)
+        return fail(KVX_ERR_INVALID_ARG, msg, len,
+                    "%s %d: device memory; store/load take host chunks (use kvx_transform_hbm)",
+                    what, index);
+    if (!want_host && a.type == cudaMemoryTypeHost)
+        return fail(KVX_ERR_INVALID_ARG, msg, len,
+                    "%s %d: host memory where device memory is required", what, index);
+    return KVX_OK;
+}
+
+struct SlotUse {
+    int64_t slot;  // page * page_size + token % page_size
+    int32_t lo, hi;  // layers written
+    int32_t chunk;
+};
+
+}  // namespace
+
+kvx_status validate(const kvx_pool *pool, const kvx_request *reqs, int n_req,
+                    const kvx_chunk *chunks, int n_chunks, int layer_begin, int layer_end,
+                    int op, int level, bool have_gpu, char *msg, size_t len)
+{
+    if (msg && len > 0)
+        msg[0] = '\0';
+    if (op < KVX_OP_STORE || op > KVX_OP_SCATTER_HBM)
+        return fail(KVX_ERR_INVALID_ARG, msg, len, "unknown operation %d", op);
+    // Always: what the packer itself relies on.
+    if (!pool)
+        return fail(KVX_ERR_INVALID_ARG, msg, len, "pool is NULL");
+    if (pool->num_layers <= 0 || (pool->kv_factor != 1 && pool->kv_factor != 2) ||
+        pool->page_size <= 0 || pool->num_pages <= 0 || pool->token_bytes <= 0)
+        return fail(KVX_ERR_INVALID_ARG, msg, len,
+                    "pool: num_layers %d, kv_factor %d, page_size %d, num_pages %d, "
+                    "token_bytes %lld", pool->num_layers, pool->kv_factor, pool->page_size,
+                    pool->num_pages, (long long)pool->token_bytes);
+    if (pool->token_bytes % 16 != 0)
+        return fail(KVX_ERR_ALIGNMENT, msg, len, "token_bytes %lld is not a multiple of 16",
+                    (long long)pool->token_bytes);
+    if (!pool->k_pages || (pool->kv_factor == 2 && !pool->v_pages))
+        return fail(KVX_ERR_INVALID_ARG, msg, len, "pool layer pointer array is NULL");
+    if (n_req < 0 || n_chunks < 0 || (n_req > 0 && !reqs) || (n_chunks > 0 && !chunks))
+        return fail(KVX_ERR_INVALID_ARG, msg, len, "bad request/chunk arrays (%d, %d)", n_req,
+                    n_chunks);
+    if (layer_begin < 0 || layer_end > pool->num_layers || layer_begin > layer_end)
+        return fail(KVX_ERR_INVALID_ARG, msg, len, "layer window [%d, %d) outside [0, %d)",
+                    layer_begin, layer_end, pool->num_layers);
+    // Every index the kernel derives from a descriptor (request, page-table entry, layer,
+    // pool) stays inside its array, whatever the level.
+    for (int r = 0; r < n_req; ++r) {
+        if (reqs[r].n_tokens < 0)
+            return fail(KVX_ERR_INVALID_ARG, msg, len, "request %d: n_tokens %d", r,
+                        reqs[r].n_tokens);
+        if (reqs[r].n_tokens > 0 && !reqs[r].page_table)
+            return fail(KVX_ERR_INVALID_ARG, msg, len, "request %d: page_table is NULL", r);
+    }
+    for (int c = 0; c < n_chunks; ++c) {
+        const kvx_chunk &ch = chunks[c];
+        if (ch.request < 0 || ch.request >= n_req)
+            return fail(KVX_ERR_INVALID_ARG, msg, len, "chunk %d: request %d of %d", c,
+                        ch.request, n_req);
+        if (ch.n_tokens < 0 || ch.n_layers < 0)
+            return fail(KVX_ERR_INVALID_ARG, msg, len, "chunk %d: negative size", c);
+        const kvx_request &rq = reqs[ch.request];
+        if (ch.token_begin < 0 || (int64_t)ch.token_begin + ch.n_tokens > rq.n_tokens)
+            return fail(KVX_ERR_INVALID_ARG, msg, len,
+                        "chunk %d: tokens [%d, %lld) outside request %d's %d tokens", c,
+                        ch.token_begin, (long long)ch.token_begin + ch.n_tokens, ch.request,
+                        rq.n_tokens);
+        if (ch.layer_begin < 0 || (int64_t)ch.layer_begin + ch.n_layers > pool->num_layers)
+            return fail(KVX_ERR_INVALID_ARG, msg, len, "chunk %d: layers [%d, %lld) outside "
+                        "[0, %d)", c, ch.layer_begin,
+                        (long long)ch.layer_begin + ch.n_layers, pool->num_layers);
+        if (ch.layout != KVX_CHUNK_LAYER_MAJOR && ch.layout != KVX_CHUNK_TOKEN_MAJOR)
+            return fail(KVX_ERR_INVALID_ARG, msg, len, "chunk %d: layout %d", c, ch.layout);
+    }
+    if (level <= 0)
+        return KVX_OK;
+
+    // Level 1: O(layers + chunks) pointer and alignment checks.
+    for (int k = 0; k < pool->kv_factor; ++k) {
+        void *const *arr = k == 0 ? pool->k_pages : pool->v_pages;
+        for (int l = 0; l < pool->num_layers; ++l) {
+            if (!arr[l])
+                return fail(KVX_ERR_INVALID_ARG, msg, len, "pool %c layer %d is NULL",
+                            k ? 'V' : 'K', l);
+            if (!aligned16(arr[l]))
+                return fail(KVX_ERR_ALIGNMENT, msg, len, "pool %c layer %d not 16-B aligned",
+                            k ? 'V' : 'K', l);
+        }
+    }
+    for (int c = 0; c < n_chunks; ++c) {
+        const kvx_chunk &ch = chunks[c];
+        if (!ch.ptr)
+            return fail(KVX_ERR_INVALID_ARG, msg, len, "chunk %d: ptr is NULL", c);
+        if (!aligned16(ch.ptr))
+            return fail(KVX_ERR_ALIGNMENT, msg, len, "chunk %d: ptr not 16-B aligned", c);
+    }
+    if (level <= 1)
+        return KVX_OK;
+
+    // Level 2: page ids against host copies, load-destination overlap, pointer attributes.
+    for (int r = 0; r < n_req; ++r) {
+        const int32_t *pt = reqs[r].page_table_host;
+        if (!pt)
+            continue;
+        int64_t n = pages_of(reqs[r].n_tokens, pool->page_size);
+        for (int64_t j = 0; j < n; ++j)
+            if (pt[j] < 0 || pt[j] >= pool->num_pages)
+                return fail(KVX_ERR_PAGE_OUT_OF_RANGE, msg, len,
+                            "request %d: page_table[%lld] = %d outside [0, %d)", r,
+                            (long long)j, pt[j], pool->num_pages);
+    }
+    if (op_is_scatter(op)) {
+        std::vector<SlotUse> uses;
+        for (int c = 0; c < n_chunks; ++c) {
+            const kvx_chunk &ch = chunks[c];
+            const int32_t *pt = reqs[ch.request].page_table_host;
+            int lo, hi;
+            chunk_layers(ch, layer_begin, layer_end, &lo, &hi);
+            if (!pt || lo >= hi)
+                continue;
+            for (int32_t t = ch.token_begin; t < ch.token_begin + ch.n_tokens; ++t)
+                uses.push_back({(int64_t)pt[t / pool->page_size] * pool->page_size +
+                                    t % pool->page_size, lo, hi, c});
+        }
+        std::sort(uses.begin(), uses.end(), [](const SlotUse &a, const SlotUse &b) {
+            return a.slot != b.slot ? a.slot < b.slot : a.lo < b.lo;
+        });
+        // Sorted by (slot, first layer): two uses of a slot overlap iff one starts below
+        // the running end of the earlier ones.
+        size_t i = 0;
+        while (i < uses.size()) {
+            size_t j = i + 1;
+            int32_t run_hi = uses[i].hi;
+            int32_t run_chunk = uses[i].chunk;
+            while (j < uses.size() && uses[j].slot == uses[i].slot) {
+                if (uses[j].lo < run_hi)
+                    return fail(KVX_ERR_OVERLAP, msg, len,
+                                "chunks %d and %d both write page slot %lld", run_chunk,
+                                uses[j].chunk, (long long)uses[j].slot);
+                if (uses[j].hi > run_hi) {
+                    run_hi = uses[j].hi;
+                    run_chunk = uses[j].chunk;
+                }
+                ++j;
+            }
+            i = j;
+        }
+    }
+    if (have_gpu) {
+        const bool chunks_on_host = op == KVX_OP_STORE || op == KVX_OP_LOAD;
+        const void *last = nullptr;
+        for (int c = 0; c < n_chunks; ++c) {
+            if (chunks[c].ptr == last)
+                continue;
+            last = chunks[c].ptr;
+            kvx_status st = check_pointer(chunks[c].ptr, chunks_on_host, "chunk", c, msg, len);
+            if (st != KVX_OK)
+                return st;
+        }
+        for (int k = 0; k < pool->kv_factor; ++k)
+            for (int l = 0; l < pool->num_layers; ++l) {
+                kvx_status st = check_pointer((k == 0 ? pool->k_pages : pool->v_pages)[l],
+                                              false, "pool layer", l, msg, len);
+                if (st != KVX_OK)
+                    return st;
+            }
+    }
+    return KVX_OK;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+PackedLayout packed_layout(const kvx_pool *pool, int n_req, int n_chunks)
+{
+    PackedLayout lay;
+    size_t off = 0;
+    lay.off_item_begin = off;
+    off = round_up(off + sizeof(int64_t) * (size_t)(n_chunks + 1), 128);
+    lay.off_chunks = off;
+    off = round_up(off + sizeof(DevChunk) * (size_t)n_chunks, 128);
+    lay.off_reqs = off;
+    off = round_up(off + sizeof(DevRequest) * (size_t)n_req, 128);
+    lay.off_pools = off;
+    off = round_up(off + sizeof(char *) * (size_t)pool->kv_factor * pool->num_layers, 128);
+    lay.total = off;
+    return lay;
+}
+
+Plan pack(const kvx_pool *pool, const kvx_request *reqs, int n_req, const kvx_chunk *chunks,
+          int n_chunks, int layer_begin, int layer_end, int dir, const PackedLayout &lay,
+          char *block, char *dev_block)
+{
+    int64_t *item_begin = reinterpret_cast<int64_t *>(block + lay.off_item_begin);
+    DevChunk *dch = reinterpret_cast<DevChunk *>(block + lay.off_chunks);
+    DevRequest *drq = reinterpret_cast<DevRequest *>(block + lay.off_reqs);
+    char **pools = reinterpret_cast<char **>(block + lay.off_pools);
+    const int64_t v = pool->token_bytes;
+    const int32_t KV = pool->kv_factor;
+    const int32_t P = pool->page_size;
+    int64_t item = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+        const kvx_chunk &ch = chunks[c];
+        DevChunk &d = dch[c];
+        int lo, hi;
+        chunk_layers(ch, layer_begin, layer_end, &lo, &hi);
+        d.ptr = static_cast<char *>(ch.ptr);
+        if (ch.layout == KVX_CHUNK_LAYER_MAJOR) {
+            d.slab_stride = (int64_t)ch.n_tokens * v;
+            d.row_stride = v;
+        } else {
+            d.slab_stride = v;
+            d.row_stride = (int64_t)ch.n_layers * KV * v;
+        }
+        d.request = ch.request;
+        d.t0 = ch.token_begin;
+        d.t_end = ch.token_begin + ch.n_tokens;
+        d.pf = ch.token_begin / P;
+        d.np = (ch.n_tokens > 0 && lo < hi)
+                   ? (ch.token_begin + ch.n_tokens - 1) / P - ch.token_begin / P + 1
+                   : 0;
+        d.la = lo;
+        d.slab0 = (lo - ch.layer_begin) * KV;
+        d.pad = 0;
+        item_begin[c] = item;
+        if (d.np > 0)
+            item += (int64_t)(hi - lo) * KV * d.np;
+    }
+    item_begin[n_chunks] = item;
+    for (int r = 0; r < n_req; ++r) {
+        drq[r].page_table = reqs[r].page_table;
+        drq[r].n_pages = (int32_t)pages_of(reqs[r].n_tokens, P);
+        drq[r].pad = 0;
+    }
+    for (int k = 0; k < KV; ++k)
+        for (int l = 0; l < pool->num_layers; ++l)
+            pools[k * pool->num_layers + l] =
+                static_cast<char *>((k == 0 ? pool->k_pages : pool->v_pages)[l]);
+
+    Plan p;
+    p.chunks = reinterpret_cast<const DevChunk *>(dev_block + lay.off_chunks);
+    p.item_begin = reinterpret_cast<const int64_t *>(dev_block + lay.off_item_begin);
+    p.reqs = reinterpret_cast<const DevRequest *>(dev_block + lay.off_reqs);
+    p.pools = reinterpret_cast<char *const *>(dev_block + lay.off_pools);
+    p.status = nullptr;
+    p.total_items = item;
+    p.token_bytes = v;
+    p.n_chunks = n_chunks;
+    p.kv_factor = KV;
+    p.page_size = P;
+    p.num_pages = pool->num_pages;
+    p.num_layers = pool->num_layers;
+    p.dir = dir;
+    return p;
+}
+
+}  // namespace kvx
+
+extern "C" {
+
+kvx_status kvx_validate(const kvx_pool *pool, const kvx_request *reqs, int n_req,
+                        const kvx_chunk *chunks, int n_chunks, int layer_begin, int layer_end,
+                        int op, int level, char *msg, size_t msg_len)
+{
+    int n_dev = 0;
+    bool have_gpu = cudaGetDeviceCount(&n_dev) == cudaSuccess && n_dev > 0;
+    if (!have_gpu)
+        cudaGetLastError();
+    return kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, op, level,
+                         have_gpu, msg, msg_len);
+}
+
+kvx_status kvx_plan_count(const kvx_pool *pool, const kvx_request *reqs, int n_req,
+                          const kvx_chunk *chunks, int n_chunks, int layer_begin, int layer_end,
+                          int64_t *n_segments, int64_t *n_bytes)
+{
+    kvx_status st = kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                                  KVX_OP_STORE, 0, false, nullptr, 0);
+    if (st != KVX_OK)
+        return st;
+    int64_t segs = 0, bytes = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+        int lo, hi;
+        kvx::chunk_layers(chunks[c], layer_begin, layer_end, &lo, &hi);
+        if (lo >= hi || chunks[c].n_tokens == 0)
+            continue;
+        int64_t np = (chunks[c].token_begin + chunks[c].n_tokens - 1) / pool->page_size -
+                     chunks[c].token_begin / pool->page_size + 1;
+        segs += (int64_t)(hi - lo) * pool->kv_factor * np;
+        bytes += (int64_t)(hi - lo) * pool->kv_factor * chunks[c].n_tokens * pool->token_bytes;
+    }
+    if (n_segments)
+        *n_segments = segs;
+    if (n_bytes)
+        *n_bytes = bytes;
+    return KVX_OK;
+}
+
+// Default chunk size of the policy (bytes).  Chosen from the page/chunk-size sweep of the
+// MLA-shaped workload: see kvx_chunk_policy.
+static const int64_t kDefaultChunkBytes = 2ll << 20;
+
+kvx_status kvx_chunk_policy(const kvx_pool *pool, int layer_streaming, int64_t target_bytes,
+                            int32_t *tokens_per_chunk, int32_t *layers_per_chunk)
+{
+    if (!pool || !tokens_per_chunk || !layers_per_chunk || pool->num_layers <= 0 ||
+        pool->page_size <= 0 || pool->token_bytes <= 0 ||
+        (pool->kv_factor != 1 && pool->kv_factor != 2) || target_bytes < 0)
+        return KVX_ERR_INVALID_ARG;
+    int64_t target = target_bytes > 0 ? target_bytes : kDefaultChunkBytes;
+    int32_t layers = layer_streaming ? 1 : pool->num_layers;
+    int64_t page_bytes = (int64_t)layers * pool->kv_factor * pool->page_size * pool->token_bytes;
+    int64_t pages = target / page_bytes;
+    if (pages < 1)
+        pages = 1;
+    if (pages * pool->page_size > INT32_MAX)
+        pages = INT32_MAX / pool->page_size;
+    *tokens_per_chunk = (int32_t)(pages * pool->page_size);
+    *layers_per_chunk = layers;
+    return KVX_OK;
+}
+
+const char *kvx_status_string(kvx_status s)
+{
+    switch (s) {
+    case KVX_OK: return "ok";
+    case KVX_ERR_INVALID_ARG: return "invalid argument";
+    case KVX_ERR_ALIGNMENT: return "misaligned pointer or size";
+    case KVX_ERR_NOT_DEVICE_ACCESSIBLE: return "memory not accessible by the device";
+    case KVX_ERR_PAGE_OUT_OF_RANGE: return "page id out of range";
+    case KVX_ERR_OVERLAP: return "overlapping load destinations";
+    case KVX_ERR_CUDA: return "CUDA error";
+    case KVX_ERR_DEVICE_STATUS: return "device reported an error";
+    case KVX_ERR_CAPACITY: return "descriptor buffer too small";
+    }
+    return "unknown status";
+}
+
+int kvx_version(void) { return KVX_VERSION; }
+
+}  // extern "C"

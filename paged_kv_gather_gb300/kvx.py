@@ -1,0 +1,412 @@
+"""Python binding of libkvx.so (include/kvx.h): the same entry points, argument marshalling only.
+
+Every byte of a transfer is moved by the library's CUDA kernels (or, for
+``kvx_dma_baseline``, by the driver copies it issues).  There is no Python or CPU
+fallback: importing this module fails if libkvx.so has not been built
+(``python -m paged_kv_gather_gb300.build``).
+
+Batches are passed as numpy structured arrays whose layout matches the C structs
+(``CHUNK_DTYPE`` = ``kvx_chunk``, ``REQUEST_DTYPE`` = ``kvx_request``), so building a
+batch of thousands of chunks stays cheap.  Streams are raw ``cudaStream_t`` handles
+(``torch.cuda.Stream().cuda_stream``), pointers are integers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvx.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                      "`python -m paged_kv_gather_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+# ---------------------------------------------------------------------------- constants
+
+KVX_OK = 0
+KVX_ERR_INVALID_ARG = 1
+KVX_ERR_ALIGNMENT = 2
+KVX_ERR_NOT_DEVICE_ACCESSIBLE = 3
+KVX_ERR_PAGE_OUT_OF_RANGE = 4
+KVX_ERR_OVERLAP = 5
+KVX_ERR_CUDA = 6
+KVX_ERR_DEVICE_STATUS = 7
+KVX_ERR_CAPACITY = 8
+
+KVX_DEV_PAGE_OUT_OF_RANGE = 0x1
+
+KVX_CHUNK_LAYER_MAJOR = 0
+KVX_CHUNK_TOKEN_MAJOR = 1
+
+KVX_DIR_GATHER = 0
+KVX_DIR_SCATTER = 1
+
+KVX_MAP_WARP_SEGMENT = 0
+
+KVX_HINT_DEFAULT = 0
+KVX_HINT_STREAMING = 1
+
+KVX_OP_STORE = 0
+KVX_OP_LOAD = 1
+KVX_OP_GATHER_HBM = 2
+KVX_OP_SCATTER_HBM = 3
+
+# ---------------------------------------------------------------------------- structs
+
+
+class kvx_pool(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("kv_factor", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("token_bytes", ctypes.c_int64),
+                ("k_pages", ctypes.POINTER(ctypes.c_void_p)),
+                ("v_pages", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class kvx_request(ctypes.Structure):
+    _fields_ = [("page_table", ctypes.c_void_p), ("page_table_host", ctypes.c_void_p),
+                ("n_tokens", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class kvx_chunk(ctypes.Structure):
+    _fields_ = [("request", ctypes.c_int32), ("token_begin", ctypes.c_int32),
+                ("n_tokens", ctypes.c_int32), ("layer_begin", ctypes.c_int32),
+                ("n_layers", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("ptr", ctypes.c_void_p)]
+
+
+class kvx_launch_cfg(ctypes.Structure):
+    _fields_ = [("sm_cap", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("unroll", ctypes.c_int32),
+                ("store_hint", ctypes.c_int32), ("mapping", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+CHUNK_DTYPE = np.dtype([("request", "<i4"), ("token_begin", "<i4"), ("n_tokens", "<i4"),
+                        ("layer_begin", "<i4"), ("n_layers", "<i4"), ("layout", "<i4"),
+                        ("ptr", "<u8")])
+REQUEST_DTYPE = np.dtype([("page_table", "<u8"), ("page_table_host", "<u8"),
+                          ("n_tokens", "<i4"), ("reserved", "<i4")])
+assert CHUNK_DTYPE.itemsize == ctypes.sizeof(kvx_chunk)
+assert REQUEST_DTYPE.itemsize == ctypes.sizeof(kvx_request)
+
+# ---------------------------------------------------------------------------- prototypes
+
+_c = ctypes
+_P = _c.POINTER
+_ctx_t = _c.c_void_p
+_batch = [_P(kvx_pool), _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int]
+
+
+def _proto(name, restype, argtypes):
+    fn = getattr(_lib, name)
+    fn.restype = restype
+    fn.argtypes = argtypes
+    return fn
+
+
+_proto("kvx_create", _c.c_int, [_P(_ctx_t), _c.c_int, _c.c_size_t])
+_proto("kvx_destroy", None, [_ctx_t])
+_proto("kvx_set_validation", _c.c_int, [_ctx_t, _c.c_int])
+_proto("kvx_default_launch_cfg", _c.c_int, [_ctx_t, _c.c_int, _P(kvx_launch_cfg)])
+_proto("kvx_store_chunks", _c.c_int, [_ctx_t, *_batch, _P(kvx_launch_cfg), _c.c_void_p])
+_proto("kvx_load_chunks", _c.c_int, [_ctx_t, *_batch, _P(kvx_launch_cfg), _c.c_void_p])
+_proto("kvx_transform_hbm", _c.c_int,
+       [_ctx_t, _c.c_int, *_batch, _P(kvx_launch_cfg), _c.c_void_p])
+_proto("kvx_dma_baseline", _c.c_int,
+       [_ctx_t, _c.c_int, *_batch, _c.c_void_p, _P(_c.c_int64)])
+_proto("kvx_get_status", _c.c_int, [_ctx_t, _c.c_void_p, _P(_c.c_uint32)])
+_proto("kvx_last_error", _c.c_char_p, [_ctx_t])
+_proto("kvx_last_launch", _c.c_int,
+       [_ctx_t, _P(_c.c_int64), _P(_c.c_int32), _P(_c.c_int32), _P(_c.c_int64)])
+_proto("kvx_validate", _c.c_int, [*_batch, _c.c_int, _c.c_int, _c.c_char_p, _c.c_size_t])
+_proto("kvx_plan_count", _c.c_int, [*_batch, _P(_c.c_int64), _P(_c.c_int64)])
+_proto("kvx_chunk_policy", _c.c_int,
+       [_P(kvx_pool), _c.c_int, _c.c_int64, _P(_c.c_int32), _P(_c.c_int32)])
+_proto("kvx_host_alloc", _c.c_int, [_P(_c.c_void_p), _c.c_size_t])
+_proto("kvx_host_free", _c.c_int, [_c.c_void_p])
+_proto("kvx_host_register", _c.c_int, [_c.c_void_p, _c.c_size_t])
+_proto("kvx_host_unregister", _c.c_int, [_c.c_void_p])
+_proto("kvx_status_string", _c.c_char_p, [_c.c_int])
+_proto("kvx_version", _c.c_int, [])
+
+EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_launch_cfg",
+            "kvx_store_chunks", "kvx_load_chunks", "kvx_transform_hbm", "kvx_dma_baseline",
+            "kvx_get_status", "kvx_last_error", "kvx_last_launch", "kvx_validate",
+            "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
+            "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version"]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def raw():
+    """The loaded ctypes library (for tests that probe symbols)."""
+    return _lib
+
+
+class KvxError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{kvx_status_string(status)} ({status}): {message}")
+        self.status = status
+        self.message = message
+
+
+def kvx_status_string(status: int) -> str:
+    return _lib.kvx_status_string(status).decode()
+
+
+def kvx_version() -> int:
+    return _lib.kvx_version()
+
+
+# ---------------------------------------------------------------------------- marshalling
+
+class Pool:
+    """A kvx_pool plus the host pointer arrays it references (kept alive with it)."""
+
+    def __init__(self, num_layers: int, kv_factor: int, page_size: int, num_pages: int,
+                 token_bytes: int, k_ptrs: Sequence[int], v_ptrs: Optional[Sequence[int]]):
+        self._k = (ctypes.c_void_p * num_layers)(*k_ptrs)
+        self._v = (ctypes.c_void_p * num_layers)(*(v_ptrs or [0] * num_layers))
+        self.c = kvx_pool(num_layers, kv_factor, page_size, num_pages, token_bytes,
+                          ctypes.cast(self._k, ctypes.POINTER(ctypes.c_void_p)),
+                          ctypes.cast(self._v, ctypes.POINTER(ctypes.c_void_p))
+                          if kv_factor == 2 else None)
+
+    @classmethod
+    def from_tensor(cls, pools, page_size: int) -> "Pool":
+        """pools: a contiguous uint8 tensor [kv_factor, num_layers, num_pages, page_size, token_bytes]."""
+        kv, L, n, P, v = pools.shape
+        assert P == page_size and pools.is_contiguous()
+        base = pools.data_ptr()
+        layer = n * P * v
+        k = [base + (0 * L + l) * layer for l in range(L)]
+        vv = [base + (1 * L + l) * layer for l in range(L)] if kv == 2 else None
+        return cls(L, kv, P, n, v, k, vv)
+
+
+def requests_array(entries) -> np.ndarray:
+    """entries: iterable of (page_table_ptr, page_table_host (np.int32 array or None), n_tokens)."""
+    entries = list(entries)
+    a = np.zeros(len(entries), REQUEST_DTYPE)
+    keep = []
+    for i, (ptr, host, n) in enumerate(entries):
+        a[i]["page_table"] = ptr
+        if host is not None:
+            h = np.ascontiguousarray(host, dtype=np.int32)
+            keep.append(h)
+            a[i]["page_table_host"] = h.ctypes.data
+        a[i]["n_tokens"] = n
+    return _Held(a, keep)
+
+
+class _Held(np.ndarray):
+    """A structured array that keeps the host buffers its pointers refer to alive."""
+
+    def __new__(cls, arr, keep):
+        obj = np.asarray(arr).view(cls)
+        obj._keep = keep
+        return obj
+
+    def __array_finalize__(self, obj):
+        self._keep = getattr(obj, "_keep", None)
+
+
+def chunks_array(specs, base_ptr: int) -> np.ndarray:
+    """specs: objects with request/token_begin/n_tokens/layer_begin/n_layers/layout/offset."""
+    a = np.zeros(len(specs), CHUNK_DTYPE)
+    if len(specs):
+        a["request"] = [c.request for c in specs]
+        a["token_begin"] = [c.token_begin for c in specs]
+        a["n_tokens"] = [c.n_tokens for c in specs]
+        a["layer_begin"] = [c.layer_begin for c in specs]
+        a["n_layers"] = [c.n_layers for c in specs]
+        a["layout"] = [c.layout for c in specs]
+        a["ptr"] = np.asarray([c.offset for c in specs], np.uint64) + np.uint64(base_ptr)
+    return a
+
+
+def _arr_ptr(a: Optional[np.ndarray], dtype) -> Tuple[int, int]:
+    if a is None or len(a) == 0:
+        return None, 0
+    assert a.dtype == dtype and a.flags["C_CONTIGUOUS"], "batch arrays must be contiguous"
+    return a.ctypes.data, len(a)
+
+
+def _batch_args(pool: Pool, reqs, chunks, layer_begin, layer_end):
+    rp, nr = _arr_ptr(reqs, REQUEST_DTYPE)
+    cp, nc = _arr_ptr(chunks, CHUNK_DTYPE)
+    if layer_end is None:
+        layer_end = pool.c.num_layers
+    return [ctypes.byref(pool.c), rp, nr, cp, nc, layer_begin, layer_end]
+
+
+def _cfg_ptr(cfg: Optional[kvx_launch_cfg]):
+    return ctypes.byref(cfg) if cfg is not None else None
+
+
+def _check(ctx, status: int):
+    if status != KVX_OK:
+        raise KvxError(status, kvx_last_error(ctx) if ctx else "")
+
+
+# ---------------------------------------------------------------------------- entry points
+
+def kvx_create(device: int = 0, max_descriptor_bytes: int = 0):
+    ctx = ctypes.c_void_p()
+    st = _lib.kvx_create(ctypes.byref(ctx), device, max_descriptor_bytes)
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_create failed")
+    return ctx
+
+
+def kvx_destroy(ctx) -> None:
+    _lib.kvx_destroy(ctx)
+
+
+def kvx_set_validation(ctx, level: int) -> None:
+    _check(ctx, _lib.kvx_set_validation(ctx, level))
+
+
+def kvx_default_launch_cfg(ctx, op: int) -> kvx_launch_cfg:
+    cfg = kvx_launch_cfg()
+    _check(ctx, _lib.kvx_default_launch_cfg(ctx, op, ctypes.byref(cfg)))
+    return cfg
+
+
+def kvx_store_chunks(ctx, pool: Pool, reqs, chunks, layer_begin: int = 0,
+                     layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
+                     stream: int = 0) -> None:
+    _check(ctx, _lib.kvx_store_chunks(ctx, *_batch_args(pool, reqs, chunks, layer_begin,
+                                                        layer_end), _cfg_ptr(cfg), stream))
+
+
+def kvx_load_chunks(ctx, pool: Pool, reqs, chunks, layer_begin: int = 0,
+                    layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
+                    stream: int = 0) -> None:
+    _check(ctx, _lib.kvx_load_chunks(ctx, *_batch_args(pool, reqs, chunks, layer_begin,
+                                                       layer_end), _cfg_ptr(cfg), stream))
+
+
+def kvx_transform_hbm(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,
+                      layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
+                      stream: int = 0) -> None:
+    _check(ctx, _lib.kvx_transform_hbm(ctx, direction,
+                                       *_batch_args(pool, reqs, chunks, layer_begin, layer_end),
+                                       _cfg_ptr(cfg), stream))
+
+
+def kvx_dma_baseline(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,
+                     layer_end: Optional[int] = None, stream: int = 0) -> int:
+    n = ctypes.c_int64(0)
+    _check(ctx, _lib.kvx_dma_baseline(ctx, direction,
+                                      *_batch_args(pool, reqs, chunks, layer_begin, layer_end),
+                                      stream, ctypes.byref(n)))
+    return n.value
+
+
+def kvx_get_status(ctx, stream: int = 0) -> int:
+    """Device status flags (0 = clean); reading clears them.  Never raises on flags."""
+    f = ctypes.c_uint32(0)
+    st = _lib.kvx_get_status(ctx, stream, ctypes.byref(f))
+    if st not in (KVX_OK, KVX_ERR_DEVICE_STATUS):
+        raise KvxError(st, kvx_last_error(ctx))
+    return f.value
+
+
+def kvx_last_error(ctx) -> str:
+    return _lib.kvx_last_error(ctx).decode()
+
+
+def kvx_last_launch(ctx) -> Tuple[int, int, int, int]:
+    """(work items, CTAs, threads per CTA, descriptor bytes) of the last launch."""
+    items, ctas, threads = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+    desc = ctypes.c_int64()
+    _check(ctx, _lib.kvx_last_launch(ctx, ctypes.byref(items), ctypes.byref(ctas),
+                                     ctypes.byref(threads), ctypes.byref(desc)))
+    return items.value, ctas.value, threads.value, desc.value
+
+
+def kvx_validate(pool: Pool, reqs, chunks, layer_begin: int = 0,
+                 layer_end: Optional[int] = None, op: int = KVX_OP_STORE,
+                 level: int = 1) -> Tuple[int, str]:
+    buf = ctypes.create_string_buffer(512)
+    st = _lib.kvx_validate(*_batch_args(pool, reqs, chunks, layer_begin, layer_end), op, level,
+                           buf, len(buf))
+    return st, buf.value.decode()
+
+
+def kvx_plan_count(pool: Pool, reqs, chunks, layer_begin: int = 0,
+                   layer_end: Optional[int] = None) -> Tuple[int, int]:
+    segs, nbytes = ctypes.c_int64(), ctypes.c_int64()
+    st = _lib.kvx_plan_count(*_batch_args(pool, reqs, chunks, layer_begin, layer_end),
+                             ctypes.byref(segs), ctypes.byref(nbytes))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_plan_count")
+    return segs.value, nbytes.value
+
+
+def kvx_chunk_policy(pool: Pool, layer_streaming: bool = False,
+                     target_bytes: int = 0) -> Tuple[int, int]:
+    t, l = ctypes.c_int32(), ctypes.c_int32()
+    st = _lib.kvx_chunk_policy(ctypes.byref(pool.c), int(layer_streaming), target_bytes,
+                               ctypes.byref(t), ctypes.byref(l))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_chunk_policy")
+    return t.value, l.value
+
+
+def kvx_host_alloc(nbytes: int) -> int:
+    p = ctypes.c_void_p()
+    st = _lib.kvx_host_alloc(ctypes.byref(p), nbytes)
+    if st != KVX_OK:
+        raise KvxError(st, f"kvx_host_alloc({nbytes})")
+    return p.value
+
+
+def kvx_host_free(ptr: int) -> None:
+    st = _lib.kvx_host_free(ptr)
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_host_free")
+
+
+def kvx_host_register(ptr: int, nbytes: int) -> None:
+    st = _lib.kvx_host_register(ptr, nbytes)
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_host_register")
+
+
+def kvx_host_unregister(ptr: int) -> None:
+    st = _lib.kvx_host_unregister(ptr)
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_host_unregister")
+
+
+class HostBuffer:
+    """Mapped pinned host memory from kvx_host_alloc, viewed as a numpy uint8 array."""
+
+    def __init__(self, nbytes: int):
+        self.nbytes = int(nbytes)
+        self.ptr = kvx_host_alloc(self.nbytes)
+        self.array = np.ctypeslib.as_array(
+            ctypes.cast(self.ptr, ctypes.POINTER(ctypes.c_uint8)), shape=(self.nbytes,))
+
+    def close(self) -> None:
+        if self.ptr:
+            self.array = None
+            kvx_host_free(self.ptr)
+            self.ptr = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

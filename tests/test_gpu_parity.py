@@ -1,0 +1,374 @@
+"""GPU parity: every kernel path against the CPU oracle, byte for byte (small and ragged).
+
+All transfers go through the C ABI (libkvx.so) via the ctypes binding; expected bytes come
+from the oracle run on host copies of the same seeded inputs.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU hosts too; every test here is gpu-marked
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from paged_kv_gather_gb300.build import build  # noqa: E402
+
+build()
+import oracle  # noqa: E402
+from paged_kv_gather_gb300 import kvx  # noqa: E402
+from paged_kv_gather_gb300 import workloads as wl  # noqa: E402
+from tests.gpu_common import (CANARY, Arena, DevicePool, Requests, assert_bytes_equal,  # noqa: E402
+                              assert_pool_equal, cfg, expected_load, expected_store,
+                              oracle_chunks, random_case)
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    c = kvx.kvx_create(0, 64 << 20)
+    yield c
+    kvx.kvx_destroy(c)
+
+
+@pytest.fixture
+def stream():
+    s = torch.cuda.Stream()
+    yield s
+    s.synchronize()
+
+
+def _store(ctx, op, dpool, reqs, specs, arena, lb, le, c, stream):
+    ch = kvx.chunks_array(specs, arena.ptr)
+    if op == "store":
+        kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, ch, lb, le, c, stream.cuda_stream)
+    elif op == "gather":
+        kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_GATHER, dpool.pool, reqs.array, ch, lb, le, c,
+                              stream.cuda_stream)
+    else:
+        kvx.kvx_dma_baseline(ctx, kvx.KVX_DIR_GATHER, dpool.pool, reqs.array, ch, lb, le,
+                             stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+
+
+def _load(ctx, op, dpool, reqs, specs, arena, lb, le, c, stream):
+    ch = kvx.chunks_array(specs, arena.ptr)
+    if op == "load":
+        kvx.kvx_load_chunks(ctx, dpool.pool, reqs.array, ch, lb, le, c, stream.cuda_stream)
+    elif op == "scatter":
+        kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_SCATTER, dpool.pool, reqs.array, ch, lb, le, c,
+                              stream.cuda_stream)
+    else:
+        kvx.kvx_dma_baseline(ctx, kvx.KVX_DIR_SCATTER, dpool.pool, reqs.array, ch, lb, le,
+                             stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+
+
+# ----------------------------------------------------------------------------- tiny workload
+
+@pytest.mark.parametrize("op_store,op_load,where", [("store", "load", "host"),
+                                                    ("gather", "scatter", "device"),
+                                                    ("dma", "dma", "host")])
+def test_tiny_workload_round_trip(ctx, stream, op_store, op_load, where):
+    """tiny: token-major chunk; store from one random page set, load into a disjoint one."""
+    w = wl.tiny()
+    s = w.shape
+    dpool = DevicePool.empty(s.num_layers, s.kv_factor, s.num_pages, s.page_size, s.token_bytes)
+    g = wl.values_generator(w.seed, "cuda")
+    wl.fill_values(dpool.tensor, s.dtype, g)
+    src = Requests([r.page_table for r in w.store_requests], [r.n_tokens for r in w.store_requests])
+    arena = Arena(w.store_arena_bytes, where)
+    _store(ctx, op_store, dpool, src, w.store_chunks, arena, 0, None, cfg(), stream)
+    exp = expected_store(dpool, src, w.store_chunks, w.store_arena_bytes)
+    assert_bytes_equal(arena.numpy(), exp, f"tiny {op_store}")
+
+    dst = Requests([r.page_table for r in w.load_requests], [r.n_tokens for r in w.load_requests])
+    pre = dpool.host_copy()
+    _load(ctx, op_load, dpool, dst, w.load_chunks, arena, 0, None, cfg(), stream)
+    exp_pool = expected_load(pre, dst, w.load_chunks, arena.numpy())
+    assert_pool_equal(dpool, exp_pool)
+    # The logical readback through the new page table equals the original.
+    for k in range(s.kv_factor):
+        for l in range(s.num_layers):
+            a = dpool.tensor[k, l][torch.from_numpy(src.host[0]).long().cuda()]
+            b = dpool.tensor[k, l][torch.from_numpy(dst.host[0]).long().cuda()]
+            assert torch.equal(a, b)
+    arena.close()
+
+
+# ----------------------------------------------------------------------------- random batches
+
+CONFIGS = [cfg(), cfg(1, 1, 32, 1, 0), cfg(2, 1, 64, 2, 1), cfg(3, 2, 256, 4, 0),
+           cfg(0, 1, 1024, 8, 1), cfg(1, 1, 1024, 8, 0), cfg(5, 3, 96, 4, 1)]
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_batches_all_paths(ctx, stream, seed):
+    rng = np.random.default_rng(5000 + seed)
+    shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
+    L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size, shape.token_bytes,
+                       shape.num_pages)
+    c = CONFIGS[seed % len(CONFIGS)]
+    arena_bytes = wl._arena_bytes(specs, shape)
+    src = Requests(tables, lens)
+    dst = Requests(load_tables, lens)
+    for op_store, op_load, where in (("store", "load", "host"), ("gather", "scatter", "device"),
+                                     ("dma", "dma", "host"), ("dma", "dma", "device")):
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        dpool.fill_random(seed * 31 + 1)
+        arena = Arena(arena_bytes, where)
+        _store(ctx, op_store, dpool, src, specs, arena, lb, le, c, stream)
+        exp = expected_store(dpool, src, specs, arena_bytes, lb, le)
+        assert_bytes_equal(arena.numpy(), exp, f"seed {seed} {op_store}/{where}")
+        # Load random chunk bytes into the disjoint page set of a random pool.
+        data = rng.integers(0, 256, arena_bytes + 4096, dtype=np.uint8)
+        arena.write(data)
+        pre = dpool.host_copy()
+        _load(ctx, op_load, dpool, dst, specs, arena, lb, le, c, stream)
+        exp_pool = expected_load(pre, dst, specs, data.copy(), lb, le)
+        assert_pool_equal(dpool, exp_pool)
+        arena.close()
+
+
+@pytest.mark.parametrize("unroll", [1, 2, 4, 8])
+@pytest.mark.parametrize("hint", [0, 1])
+def test_every_kernel_variant(ctx, stream, unroll, hint):
+    """Every (unroll, hint, direction) instantiation on a multi-tile ragged batch."""
+    rng = np.random.default_rng(77 + unroll * 10 + hint)
+    L, KV, P, v = 3, 2, 16, 2048
+    lens = [1000, 333, 17]
+    pages = [-(-n // P) for n in lens]
+    NP = sum(pages) * 2
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(perm[at:at + npg])
+        t_dst.append(perm[at + sum(pages):at + sum(pages) + npg])
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, 100, 0, L, wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    c = cfg(4, 1, 256, unroll, hint)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(unroll + 10 * hint)
+    arena = Arena(nbytes, "host")
+    _store(ctx, "store", dpool, src, specs, arena, 0, None, c, stream)
+    assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), "store")
+    pre = dpool.host_copy()
+    _load(ctx, "load", dpool, dst, specs, arena, 0, None, c, stream)
+    assert_pool_equal(dpool, expected_load(pre, dst, specs, arena.numpy().copy()))
+    arena.close()
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def test_empty_and_degenerate_batches(ctx, stream):
+    L, KV, P, v, NP = 2, 2, 4, 64, 16
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(3)
+    before = dpool.tensor.clone()
+    reqs = Requests([np.array([1, 2], np.int32), np.zeros(0, np.int32)], [7, 0])
+    arena = Arena(4096, "host")
+    empty = np.zeros(0, kvx.CHUNK_DTYPE)
+    kvx.kvx_load_chunks(ctx, dpool.pool, reqs.array, empty, 0, L, None, stream.cuda_stream)
+    assert kvx.kvx_last_launch(ctx)[0] == 0
+    # Zero-token chunk, chunk of the empty request, chunk outside the layer window.
+    specs = [wl.ChunkSpec(0, 3, 0, 0, L, 0, 0), wl.ChunkSpec(1, 0, 0, 0, L, 1, 256),
+             wl.ChunkSpec(0, 0, 7, 1, 1, 0, 512)]
+    ch = kvx.chunks_array(specs, arena.ptr)
+    kvx.kvx_load_chunks(ctx, dpool.pool, reqs.array, ch, 0, 1, None, stream.cuda_stream)
+    assert kvx.kvx_last_launch(ctx)[0] == 0
+    stream.synchronize()
+    assert torch.equal(before, dpool.tensor)
+    # Single token, one unit wide.
+    pool1 = DevicePool.empty(1, 1, 4, 1, 16)
+    pool1.fill_random(9)
+    r1 = Requests([np.array([3], np.int32)], [1])
+    a1 = Arena(16, "host")
+    _store(ctx, "store", pool1, r1, [wl.ChunkSpec(0, 0, 1, 0, 1, 1, 0)], a1, 0, None, cfg(), stream)
+    assert_bytes_equal(a1.numpy()[:16], pool1.tensor[0, 0, 3, 0].cpu().numpy(), "one token")
+    assert np.all(a1.numpy()[16:] == CANARY)
+    arena.close()
+    a1.close()
+
+
+def test_largest_segment_and_partial_pages(ctx, stream):
+    """64-token pages of 1152-B latents (72 KiB segments), chunks that split pages."""
+    L, KV, P, v = 2, 1, 64, 1152
+    T = 64 * 5 + 37
+    NP = 16
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(NP).astype(np.int32)
+    src, dst = Requests([perm[:6]], [T]), Requests([perm[6:12]], [T])
+    specs = wl.split_tokens(0, 0, T, 56, 0, L, wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(5)
+    arena = Arena(nbytes, "host")
+    _store(ctx, "store", dpool, src, specs, arena, 0, None, cfg(), stream)
+    assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), "store")
+    pre = dpool.host_copy()
+    _load(ctx, "load", dpool, dst, specs, arena, 0, None, cfg(), stream)
+    exp = expected_load(pre, dst, specs, arena.numpy().copy())
+    assert_pool_equal(dpool, exp)
+    # Slots past the last token of the last destination page keep their old bytes.
+    last = dst.host[0][-1]
+    assert torch.equal(dpool.tensor[0, :, last, 37:].cpu(),
+                       torch.from_numpy(np.stack([pre.pools[0][l][last, 37:]
+                                                  for l in range(L)])))
+    arena.close()
+
+
+def test_many_calls_in_flight_on_two_streams(ctx):
+    """More calls than descriptor buffers, alternating streams: each must see its own batch."""
+    rng = np.random.default_rng(8)
+    L, KV, P, v, T = 4, 2, 16, 256, 512
+    NP = 4 * (T // P) * 3
+    perm = rng.permutation(NP).astype(np.int32)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(11)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    arenas, cases = [], []
+    for i in range(10):
+        tab = perm[(i % 4) * (T // P):(i % 4 + 1) * (T // P)]
+        req = Requests([tab], [T])
+        specs = wl.split_tokens(0, 0, T, 64 + 16 * i, 0, L, i % 2)
+        shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+        wl.place_chunks(specs, shape)
+        nbytes = wl._arena_bytes(specs, shape)
+        arena = Arena(nbytes, "host")
+        ch = kvx.chunks_array(specs, arena.ptr)
+        kvx.kvx_store_chunks(ctx, dpool.pool, req.array, ch, 0, L, cfg(1 + i % 3),
+                             streams[i % 2].cuda_stream)
+        arenas.append(arena)
+        cases.append((req, specs, nbytes))
+    torch.cuda.synchronize()
+    for arena, (req, specs, nbytes) in zip(arenas, cases):
+        assert_bytes_equal(arena.numpy(), expected_store(dpool, req, specs, nbytes), "in flight")
+        arena.close()
+
+
+# ----------------------------------------------------------------------------- errors
+
+def test_in_kernel_page_check_skips_and_reports(ctx, stream):
+    """A device page table naming a page past the pool: that segment is skipped, flagged,
+    and everything else is still moved (validation level 1 does not read page tables)."""
+    L, KV, P, v, NP = 2, 2, 8, 64, 8
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(12)
+    good = np.array([5, 2], np.int32)
+    bad = np.array([5, NP + 1000], np.int32)
+    reqs = Requests([bad], [16], host_copy=False)
+    specs = [wl.ChunkSpec(0, 0, 8, 0, L, 0), wl.ChunkSpec(0, 8, 8, 0, L, 0)]
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    arena = Arena(nbytes, "host")
+    ch = kvx.chunks_array(specs, arena.ptr)
+    kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, ch, 0, L, None, stream.cuda_stream)
+    stream.synchronize()
+    flags = kvx.kvx_get_status(ctx, stream.cuda_stream)
+    assert flags == kvx.KVX_DEV_PAGE_OUT_OF_RANGE
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0  # reading cleared it
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(dpool.host_copy(), [oracle.Request(good, 16)], oracle_chunks(specs[:1], exp))
+    assert_bytes_equal(arena.numpy(), exp, "valid part moved, bad page skipped")
+    arena.close()
+
+
+def test_host_detected_errors_launch_nothing(ctx, stream):
+    L, KV, P, v, NP = 2, 2, 8, 64, 8
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(13)
+    before = dpool.tensor.clone()
+    tab = np.array([1, 2], np.int32)
+    reqs = Requests([tab], [16])
+    specs = [wl.ChunkSpec(0, 0, 16, 0, L, 0, 0)]
+    nbytes = 16 * L * KV * v
+    kvx.kvx_set_validation(ctx, 2)
+    try:
+        # Pageable host memory.
+        pageable = np.zeros(nbytes + 64, np.uint8)
+        base = pageable.ctypes.data + (-pageable.ctypes.data % 16)
+        ch = kvx.chunks_array(specs, base)
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, ch, 0, L, None, stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_NOT_DEVICE_ACCESSIBLE
+        # Device memory given to store, host memory given to the HBM transform.
+        dev = Arena(nbytes, "device")
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, kvx.chunks_array(specs, dev.ptr),
+                                 0, L, None, stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+        host = Arena(nbytes, "host")
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_SCATTER, dpool.pool, reqs.array,
+                                  kvx.chunks_array(specs, host.ptr), 0, L, None,
+                                  stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+        # Overlapping load destinations.
+        two = [wl.ChunkSpec(0, 0, 16, 0, L, 0, 0), wl.ChunkSpec(0, 8, 8, 1, 1, 0, 4096)]
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_load_chunks(ctx, dpool.pool, reqs.array, kvx.chunks_array(two, host.ptr), 0,
+                                L, None, stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_OVERLAP
+        # Page id out of range (host copy given).
+        badreq = Requests([np.array([1, 99], np.int32)], [16])
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_load_chunks(ctx, dpool.pool, badreq.array,
+                                kvx.chunks_array(specs, host.ptr), 0, L, None, stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_PAGE_OUT_OF_RANGE
+        assert "99" in kvx.kvx_last_error(ctx)
+        # Misaligned chunk pointer.
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_load_chunks(ctx, dpool.pool, reqs.array,
+                                kvx.chunks_array(specs, host.ptr + 8), 0, L, None,
+                                stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_ALIGNMENT
+        # Bad launch configuration.
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_load_chunks(ctx, dpool.pool, reqs.array, kvx.chunks_array(specs, host.ptr),
+                                0, L, cfg(threads=100), stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+        stream.synchronize()
+        assert torch.equal(before, dpool.tensor)
+        assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+        dev.close()
+        host.close()
+    finally:
+        kvx.kvx_set_validation(ctx, 1)
+
+
+def test_descriptor_capacity_error():
+    small = kvx.kvx_create(0, 1024)
+    try:
+        L, KV, P, v, NP = 1, 1, 1, 16, 512
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        reqs = Requests([np.arange(256, dtype=np.int32)], [256])
+        specs = wl.split_tokens(0, 0, 256, 1, 0, 1, 0)
+        shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+        wl.place_chunks(specs, shape, align=16)
+        arena = Arena(wl._arena_bytes(specs, shape), "host")
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_store_chunks(small, dpool.pool, reqs.array,
+                                 kvx.chunks_array(specs, arena.ptr), 0, 1, None, 0)
+        assert e.value.status == kvx.KVX_ERR_CAPACITY
+        arena.close()
+    finally:
+        kvx.kvx_destroy(small)
+
+
+def test_default_launch_configs(ctx):
+    for op in range(4):
+        c = kvx.kvx_default_launch_cfg(ctx, op)
+        assert c.threads % 32 == 0 and c.unroll in (1, 2, 4, 8)
+    assert kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD).sm_cap > 0
+    assert kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM).sm_cap == 0

@@ -1,0 +1,240 @@
+"""Host-side tests of libkvx.so that need no GPU: symbols, validation, counting, policy."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from paged_kv_gather_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+build()
+from paged_kv_gather_gb300 import kvx  # noqa: E402
+from paged_kv_gather_gb300 import workloads as wl  # noqa: E402
+
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "kvx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvx_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = header_symbols()
+    assert len(names) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", kvx.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kvx_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in names:
+        assert hasattr(kvx.raw(), n)
+    assert sorted(kvx.EXPORTED) == names, "binding and header disagree"
+
+
+def test_version_and_status_strings():
+    assert kvx.kvx_version() == 1
+    seen = set()
+    for st in range(9):
+        s = kvx.kvx_status_string(st)
+        assert s and s != "unknown status"
+        seen.add(s)
+    assert len(seen) == 9
+    assert kvx.kvx_status_string(99) == "unknown status"
+
+
+# ----------------------------------------------------------------------------- fixtures
+
+class FakeBatch:
+    """Pointers only: host logic never dereferences pool or chunk memory."""
+
+    def __init__(self, L=4, KV=2, P=16, num_pages=64, v=256):
+        self.L, self.KV, self.P, self.num_pages, self.v = L, KV, P, num_pages, v
+        base = 1 << 40
+        layer = num_pages * P * v
+        self.pool = kvx.Pool(L, KV, P, num_pages, v, [base + l * layer for l in range(L)],
+                             [base + (L + l) * layer for l in range(L)] if KV == 2 else None)
+
+    def reqs(self, tables, host=True):
+        return kvx.requests_array([(0x1000 + 0x100000 * i, t if host else None, n)
+                                   for i, (t, n) in enumerate(tables)])
+
+    @staticmethod
+    def chunks(specs, base=1 << 44):
+        a = np.zeros(len(specs), kvx.CHUNK_DTYPE)
+        for i, (r, t0, n, l0, nl, layout, off) in enumerate(specs):
+            a[i] = (r, t0, n, l0, nl, layout, base + off)
+        return a
+
+
+def _v(batch, reqs, chunks, lb=0, le=None, op=kvx.KVX_OP_STORE, level=1):
+    return kvx.kvx_validate(batch.pool, reqs, chunks, lb, le, op, level)
+
+
+def test_validate_accepts_a_good_batch():
+    b = FakeBatch()
+    reqs = b.reqs([(np.arange(8, dtype=np.int32), 128)])
+    ch = b.chunks([(0, 0, 64, 0, 4, 0, 0), (0, 64, 64, 0, 4, 1, 1 << 20)])
+    for op in range(4):
+        for level in (0, 1, 2):
+            assert _v(b, reqs, ch, op=op, level=level)[0] == kvx.KVX_OK
+
+
+@pytest.mark.parametrize("case,status", [
+    ("token_bytes", kvx.KVX_ERR_ALIGNMENT),
+    ("chunk_align", kvx.KVX_ERR_ALIGNMENT),
+    ("request_index", kvx.KVX_ERR_INVALID_ARG),
+    ("token_range", kvx.KVX_ERR_INVALID_ARG),
+    ("layer_range", kvx.KVX_ERR_INVALID_ARG),
+    ("window", kvx.KVX_ERR_INVALID_ARG),
+    ("layout", kvx.KVX_ERR_INVALID_ARG),
+    ("null_chunk", kvx.KVX_ERR_INVALID_ARG),
+    ("negative", kvx.KVX_ERR_INVALID_ARG),
+    ("null_table", kvx.KVX_ERR_INVALID_ARG),
+])
+def test_validate_rejects(case, status):
+    b = FakeBatch(v=40 if case == "token_bytes" else 256)
+    reqs = b.reqs([(np.arange(8, dtype=np.int32), 128)])
+    spec = [0, 0, 64, 0, 4, 0, 0]
+    lb, le = 0, None
+    if case == "chunk_align":
+        spec[6] = 8
+    elif case == "request_index":
+        spec[0] = 1
+    elif case == "token_range":
+        spec[1], spec[2] = 100, 64
+    elif case == "layer_range":
+        spec[3], spec[4] = 2, 3
+    elif case == "window":
+        lb, le = 3, 2
+    elif case == "layout":
+        spec[5] = 2
+    elif case == "negative":
+        spec[2] = -1
+    elif case == "null_table":
+        reqs = kvx.requests_array([(0, None, 128)])
+    ch = b.chunks([tuple(spec)])
+    if case == "null_chunk":
+        ch["ptr"] = 0
+    st, msg = _v(b, reqs, ch, lb, le)
+    assert st == status, msg
+    assert msg
+
+
+def test_validate_level2_page_ids_and_overlap():
+    b = FakeBatch()
+    bad = np.arange(8, dtype=np.int32)
+    bad[5] = 64
+    reqs = b.reqs([(bad, 128)])
+    ch = b.chunks([(0, 0, 128, 0, 4, 0, 0)])
+    assert _v(b, reqs, ch, level=1)[0] == kvx.KVX_OK  # level 1 does not read page tables
+    st, msg = _v(b, reqs, ch, level=2)
+    assert st == kvx.KVX_ERR_PAGE_OUT_OF_RANGE and "64" in msg
+
+    # Two requests sharing page 3 at the same slot: a load that writes both overlaps.
+    t1 = np.array([0, 1, 2, 3], np.int32)
+    t2 = np.array([3, 4], np.int32)
+    reqs = b.reqs([(t1, 64), (t2, 32)])
+    both = b.chunks([(0, 48, 16, 0, 4, 0, 0), (1, 0, 16, 0, 4, 0, 1 << 20)])
+    assert _v(b, reqs, both, op=kvx.KVX_OP_LOAD, level=2)[0] == kvx.KVX_ERR_OVERLAP
+    assert _v(b, reqs, both, op=kvx.KVX_OP_SCATTER_HBM, level=2)[0] == kvx.KVX_ERR_OVERLAP
+    # A store may read one slot twice.
+    assert _v(b, reqs, both, op=kvx.KVX_OP_STORE, level=2)[0] == kvx.KVX_OK
+    # Same slots but disjoint layers: per-layer chunks of a streamed load are fine.
+    per_layer = b.chunks([(0, 48, 16, 0, 2, 0, 0), (1, 0, 16, 2, 2, 0, 1 << 20)])
+    assert _v(b, reqs, per_layer, op=kvx.KVX_OP_LOAD, level=2)[0] == kvx.KVX_OK
+    # ... unless the call's layer windows make them meet: here they do not.
+    assert _v(b, reqs, per_layer, 1, 3, op=kvx.KVX_OP_LOAD, level=2)[0] == kvx.KVX_OK
+    # Overlap inside one chunk list of one request (two chunks over the same tokens).
+    dup = b.chunks([(0, 0, 32, 0, 4, 0, 0), (0, 16, 32, 3, 1, 1, 1 << 20)])
+    assert _v(b, reqs, dup, op=kvx.KVX_OP_LOAD, level=2)[0] == kvx.KVX_ERR_OVERLAP
+    assert _v(b, reqs, dup, 0, 3, op=kvx.KVX_OP_LOAD, level=2)[0] == kvx.KVX_OK
+
+
+def _golden(name):
+    rows = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        f = line.split("#")[0].split()
+        if f:
+            rows[f[0]] = [int(x) for x in f[1:]]
+    return rows
+
+
+def test_plan_count_reproduces_per_page_dma_example():
+    g = _golden("strata_dma_count.txt")
+    T, P, L = g["tokens"][0], g["page_size"][0], g["layers"][0]
+    b = FakeBatch(L=L, KV=1, P=P, num_pages=T // P, v=2048)
+    reqs = b.reqs([(np.arange(T // P, dtype=np.int32), T)])
+    one = b.chunks([(0, 0, T, 0, L, 0, 0)])
+    segs, nbytes = kvx.kvx_plan_count(b.pool, reqs, one)
+    assert segs == g["copies_per_request"][0]
+    assert nbytes == T * L * 2048
+    for layer in (0, 17, L - 1):
+        assert kvx.kvx_plan_count(b.pool, reqs, one, layer, layer + 1)[0] == \
+            g["copies_per_layer"][0]
+    # One chunk per page gives the same count: chunking at page boundaries adds no copy.
+    per_page = b.chunks([(0, p * P, P, 0, L, 0, p * L * P * 2048) for p in range(T // P)])
+    assert kvx.kvx_plan_count(b.pool, reqs, per_page)[0] == g["copies_per_request"][0]
+
+
+def _pool_for(shape):
+    return kvx.Pool(shape.num_layers, shape.kv_factor, shape.page_size, shape.num_pages,
+                    shape.token_bytes, [1 << 40] * shape.num_layers,
+                    [1 << 41] * shape.num_layers if shape.kv_factor == 2 else None)
+
+
+def test_plan_count_of_workloads():
+    w = wl.llama8b()
+    pool = _pool_for(w.shape)
+    reqs = kvx.requests_array([(0x1000, None, w.load_requests[0].n_tokens)])
+    ch = kvx.chunks_array(w.load_chunks, 1 << 44)
+    assert kvx.kvx_plan_count(pool, reqs, ch) == (131072, 4 << 30)
+    for P in wl.MLA_PAGE_SIZES:
+        for C in wl.MLA_CHUNK_BYTES:
+            w = wl.mla_sweep(P, C)
+            pool = _pool_for(w.shape)
+            reqs = kvx.requests_array([(0x1000, None, 16384)])
+            ch = kvx.chunks_array(w.load_chunks, 1 << 44)
+            segs, nbytes = kvx.kvx_plan_count(pool, reqs, ch)
+            assert nbytes == 1151336448
+            expect = 61 * sum((c.token_begin + c.n_tokens - 1) // P - c.token_begin // P + 1
+                              for c in w.load_chunks if c.layer_begin == 0)
+            assert segs == expect
+            if P == 1:
+                assert segs == 999424
+            if C % (P * 1152) == 0:
+                assert segs == 61 * (16384 // P)
+
+
+def test_chunk_policy_properties():
+    for w in (wl.tiny(), wl.llama8b(), wl.llama70b(), wl.qwen7b_batch(), wl.mla_sweep(1),
+              wl.mla_sweep(64)):
+        pool = _pool_for(w.shape)
+        s = w.shape
+        for streaming in (False, True):
+            for target in (0, 64 << 10, 1 << 20, 4 << 20, 64 << 20):
+                tpc, lpc = kvx.kvx_chunk_policy(pool, streaming, target)
+                assert tpc > 0 and tpc % s.page_size == 0
+                assert lpc == (1 if streaming else s.num_layers)
+                chunk = tpc * lpc * s.kv_factor * s.token_bytes
+                page = s.page_size * lpc * s.kv_factor * s.token_bytes
+                eff = target or (2 << 20)
+                if page <= eff:
+                    assert chunk <= eff < chunk + page
+                else:
+                    assert tpc == s.page_size
+    with pytest.raises(kvx.KvxError):
+        kvx.kvx_chunk_policy(_pool_for(wl.tiny().shape), False, -1)
+
+
+def test_chunk_and_request_dtypes_match_c_structs():
+    assert kvx.CHUNK_DTYPE.itemsize == ctypes.sizeof(kvx.kvx_chunk) == 32
+    assert kvx.REQUEST_DTYPE.itemsize == ctypes.sizeof(kvx.kvx_request) == 24
+    for name, _ in kvx.kvx_chunk._fields_:
+        assert kvx.CHUNK_DTYPE.fields[name][1] == getattr(kvx.kvx_chunk, name).offset
+    for name, _ in kvx.kvx_request._fields_:
+        assert kvx.REQUEST_DTYPE.fields[name][1] == getattr(kvx.kvx_request, name).offset
