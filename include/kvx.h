@@ -214,6 +214,42 @@ const char *kvx_last_error(const kvx_ctx *ctx);
 kvx_status kvx_last_launch(const kvx_ctx *ctx, int64_t *items, int32_t *ctas,
                            int32_t *threads, int64_t *descriptor_bytes);
 
+/* ---------------------------------------------------------------- allocation-free load */
+
+/* Size of the fixed scratch array behind kvx_load_chunks_noalloc: a 256-byte status
+ * header plus the packed descriptors (about 72 bytes per chunk, 16 per request, 8 per
+ * pool layer), so roughly 14,000 chunks per call. */
+#define KVX_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* kvx_load_chunks without a context and without allocating anything.  The pages have no
+ * counterpart of this call: it exists for callers that may not allocate device memory,
+ * such as a serving engine that has handed nearly all of HBM to its KV page pool at
+ * start-up (a later cudaMalloc fails or takes memory the pool was promised), or a plug-in
+ * the engine calls without a place to keep a kvx_ctx between calls.
+ *
+ * Scratch: the descriptors and the status word live in one file-scope device array of
+ * KVX_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds until the
+ * process exits.  A batch whose descriptors do not fit returns KVX_ERR_CAPACITY and
+ * launches nothing.  The call calls no cudaMalloc or cudaFree and allocates no host
+ * memory.
+ *
+ * Runs on the calling thread's current device.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Each call copies its descriptors into the array
+ * (from a static host image; the copy call returns once it has read it), which also
+ * clears the status word, then launches the load kernel on `stream`.  All calls share
+ * the one array and it keeps the last call's contents: calls whose work overlaps on the
+ * GPU (for example on two streams without ordering between them) race on it.  Issue
+ * them on one stream, or order them with events.
+ *
+ * Arguments are those of kvx_load_chunks (validation level 1 always).  device_flags,
+ * if not NULL, is a 4-byte aligned device-accessible word that the kernel ORs
+ * KVX_DEV_* bits into (the caller clears it); when NULL the bits are dropped. */
+kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_request *reqs, int n_req,
+                                   const kvx_chunk *chunks, int n_chunks, int layer_begin,
+                                   int layer_end, const kvx_launch_cfg *cfg,
+                                   kvx_stream_t stream, uint32_t *device_flags);
+
 /* ---------------------------------------------------------------- host logic (no GPU) */
 
 /* Validate a transfer of kind `op` (KVX_OP_*) at `level` (1 or 2; level 2's pointer

@@ -17,6 +17,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "kvx_internal.h"
 
@@ -639,3 +640,96 @@ kvx_status kvx_host_unregister(void *ptr)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free load
+//
+// kvx_load_chunks_noalloc is kvx_load_chunks for callers that may not allocate device
+// memory: a serving engine that hands nearly all of HBM to its KV page pool at start-up
+// (a later cudaMalloc fails, or eats into pages the engine already promised), or a
+// plug-in the engine calls with no place to keep a kvx_ctx between calls.  Its scratch
+// -- the status word and the packed descriptors that kvx_create would otherwise allocate
+// -- is the fixed array below.  Every GPU that loads this library holds that array until
+// the process exits.
+
+namespace {
+
+const size_t kNoallocScratchBytes = KVX_NOALLOC_SCRATCH_BYTES;
+const size_t kNoallocHeader = 256;  // status word, then zero padding
+const int kNoallocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVX_NOALLOC_SCRATCH_BYTES];
+
+// Host image of the scratch, filled under the mutex and copied from pageable memory:
+// cudaMemcpyAsync returns only after it has consumed a pageable source, so the image can
+// be refilled as soon as the copy call returns.
+unsigned char g_noalloc_stage[KVX_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[kNoallocMaxDevices];  // device address of the array, per device
+
+}  // namespace
+
+extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_request *reqs,
+                                              int n_req, const kvx_chunk *chunks, int n_chunks,
+                                              int layer_begin, int layer_end,
+                                              const kvx_launch_cfg *cfg, kvx_stream_t stream,
+                                              uint32_t *device_flags)
+{
+    kvx_launch_cfg c;
+    kvx_status st = resolve_cfg(nullptr, KVX_OP_LOAD, cfg, &c);
+    if (st != KVX_OK)
+        return st;
+    st = kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, KVX_OP_LOAD,
+                       1, false, nullptr, 0);
+    if (st != KVX_OK)
+        return st;
+    if (device_flags && (reinterpret_cast<uintptr_t>(device_flags) & 3u))
+        return KVX_ERR_ALIGNMENT;
+    const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
+    if (kNoallocHeader + lay.total > kNoallocScratchBytes)
+        return KVX_ERR_CAPACITY;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) {
+        cudaGetLastError();
+        return KVX_ERR_CUDA;
+    }
+    int sms = 0;
+    if (c.sm_cap == 0 &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return KVX_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        // First call on this device, with it current: look up the array's device address.
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) {
+            cudaGetLastError();
+            return KVX_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = addr;
+    }
+    char *dev_block = static_cast<char *>(g_noalloc_addr[dev]);
+    std::memset(g_noalloc_stage, 0, kNoallocHeader);  // the status word starts each call at 0
+    Plan plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                          KVX_DIR_SCATTER, lay,
+                          reinterpret_cast<char *>(g_noalloc_stage) + kNoallocHeader,
+                          dev_block + kNoallocHeader);
+    plan.status = device_flags ? device_flags : reinterpret_cast<unsigned int *>(dev_block);
+    if (plan.total_items == 0)
+        return KVX_OK;
+    if (cudaMemcpyAsync(dev_block, g_noalloc_stage, kNoallocHeader + lay.total,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return KVX_ERR_CUDA;
+    const int64_t warps_per_cta = c.threads / 32;
+    int64_t ctas = int64_t(c.sm_cap > 0 ? c.sm_cap : sms) * c.ctas_per_sm;
+    const int64_t needed = (plan.total_items + warps_per_cta - 1) / warps_per_cta;
+    if (ctas > needed)
+        ctas = needed;
+    void *args[] = {&plan};
+    if (cudaLaunchKernel(reinterpret_cast<const void *>(pick_kernel(c.unroll, KVX_DIR_SCATTER,
+                                                                    c.store_hint)),
+                         dim3(unsigned(ctas)), dim3(unsigned(c.threads)), args, 0, s) !=
+        cudaSuccess)
+        return KVX_ERR_CUDA;
+    return KVX_OK;
+}

@@ -135,12 +135,17 @@ _proto("kvx_host_register", _c.c_int, [_c.c_void_p, _c.c_size_t])
 _proto("kvx_host_unregister", _c.c_int, [_c.c_void_p])
 _proto("kvx_status_string", _c.c_char_p, [_c.c_int])
 _proto("kvx_version", _c.c_int, [])
+_proto("kvx_load_chunks_noalloc", _c.c_int, [*_batch, _P(kvx_launch_cfg), _c.c_void_p,
+                                             _c.c_void_p])
 
 EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_launch_cfg",
             "kvx_store_chunks", "kvx_load_chunks", "kvx_transform_hbm", "kvx_dma_baseline",
             "kvx_get_status", "kvx_last_error", "kvx_last_launch", "kvx_validate",
             "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
-            "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version"]
+            "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
+            "kvx_load_chunks_noalloc"]
+
+KVX_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 def library_path() -> str:
@@ -302,6 +307,22 @@ def kvx_transform_hbm(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin
     _check(ctx, _lib.kvx_transform_hbm(ctx, direction,
                                        *_batch_args(pool, reqs, chunks, layer_begin, layer_end),
                                        _cfg_ptr(cfg), stream))
+
+
+def kvx_load_chunks_noalloc(pool: Pool, reqs, chunks, layer_begin: int = 0,
+                            layer_end: Optional[int] = None,
+                            cfg: Optional[kvx_launch_cfg] = None, stream: int = 0,
+                            device_flags: int = 0) -> None:
+    """kvx_load_chunks without a context: for callers that may not allocate device memory.
+
+    Descriptors travel through one fixed device array inside the library (see
+    include/kvx.h), so calls must not overlap on the GPU.  device_flags: address of a
+    device word that collects KVX_DEV_* bits, or 0.
+    """
+    st = _lib.kvx_load_chunks_noalloc(*_batch_args(pool, reqs, chunks, layer_begin, layer_end),
+                                      _cfg_ptr(cfg), stream, device_flags or None)
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_load_chunks_noalloc")
 
 
 def kvx_dma_baseline(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,
