@@ -55,6 +55,16 @@ def parse():
     p.add_argument("--store-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--load-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
+    p.add_argument("--workload", default="llama8b",
+                   choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
+                            "transform_sweep", "profile_small"],
+                   help="llama8b is the headline line; the others print measurement lines of "
+                        "the other workloads (not the headline)")
+    p.add_argument("--profile-op", default="load",
+                   choices=["store", "load", "gather", "scatter"],
+                   help="operation of --workload profile_small")
+    p.add_argument("--sm-caps", default="1,2,4,8,16,32,0",
+                   help="SM caps of the llama70b overlap sweep (0 = all SMs)")
     return p.parse_args()
 
 
@@ -511,10 +521,365 @@ def run_ours(args):
     kvx.kvx_destroy(ctx)
 
 
+# ----------------------------------------------------------------------------- other workloads
+
+def _timed(stream, fn, reps, warm=2):
+    for _ in range(warm):
+        fn()
+    t = EventTimer(stream)
+    for _ in range(reps):
+        e = t.start()
+        fn()
+        t.stop(e)
+    stream.synchronize()
+    return statistics.median(t.ms())
+
+
+def _fill_host(arr, nbytes, shape, seed, stream_id, wl):
+    g = wl.values_generator(seed, "cuda", stream=stream_id)
+    step = 1 << 30
+    for s0 in range(0, nbytes, step):
+        e = min(nbytes, s0 + step)
+        tmp = torch.empty(e - s0, dtype=torch.uint8, device="cuda")
+        wl.fill_values(tmp, shape.dtype, g)
+        torch.from_numpy(arr[s0:e]).copy_(tmp)
+
+
+def _pool_tensor(shape, seed, wl):
+    t = torch.empty((shape.kv_factor, shape.num_layers, shape.num_pages, shape.page_size,
+                     shape.token_bytes), dtype=torch.uint8, device="cuda")
+    wl.fill_values(t, shape.dtype, wl.values_generator(seed, "cuda"))
+    return t
+
+
+def _emit(d):
+    print(json.dumps(d), flush=True)
+
+
+def run_llama70b(args, kvx, wl):
+    """Layer-streamed load of a 65536-token prefix (80 layers, 256 MiB per layer) while a
+    bf16 8192^3 GEMM per layer runs on a second stream; SM-cap sweep."""
+    w = wl.llama70b()
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    r = w.load_requests[0]
+    pt = torch.from_numpy(r.page_table).cuda()
+    reqs = kvx.requests_array([(pt.data_ptr(), r.page_table, r.n_tokens)])
+    arena = kvx.HostBuffer(w.load_arena_bytes)
+    _fill_host(arena.array, w.load_arena_bytes, s, w.seed, 1, wl)
+    per_layer = [kvx.chunks_array([c for c in w.load_chunks if c.layer_begin == l], arena.ptr)
+                 for l in range(s.num_layers)]
+    ctx = kvx.kvx_create(0)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    A = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16, generator=g)
+    B = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16, generator=g)
+    C = torch.empty(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    layer_bytes = w.load_bytes() // s.num_layers
+
+    def gemm():
+        torch.matmul(A, B, out=C)
+
+    with torch.cuda.stream(sb):
+        gemm_ms = _timed(sb, gemm, 20, warm=5)
+    for cap in [int(x) for x in args.sm_caps.split(",")]:
+        cfg = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD)
+        cfg.sm_cap = cap
+
+        def load_all():
+            for l in range(s.num_layers):
+                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, sa.cuda_stream)
+
+        alone_ms = _timed(sa, load_all, 3, warm=1)
+        # Overlapped: load(l) on stream A; GEMM(l) on stream B after load(l) is done.
+        for rep in range(2):
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            start.record(sa)
+            sb.wait_event(start)
+            gt = EventTimer(sb)
+            for l in range(s.num_layers):
+                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, sa.cuda_stream)
+                ev = torch.cuda.Event()
+                ev.record(sa)
+                sb.wait_event(ev)
+                with torch.cuda.stream(sb):
+                    e = gt.start()
+                    gemm()
+                    gt.stop(e)
+            end_a = torch.cuda.Event(enable_timing=True)
+            end_a.record(sa)
+            end_b = torch.cuda.Event(enable_timing=True)
+            end_b.record(sb)
+            torch.cuda.synchronize()
+        assert kvx.kvx_get_status(ctx, sa.cuda_stream) == 0
+        load_span = start.elapsed_time(end_a)
+        e2e = start.elapsed_time(end_b)
+        g_ms = statistics.mean(gt.ms())
+        _emit({"workload": "llama70b_layer_streaming", "sm_cap": cap,
+               "load_cfg": cfg.as_dict(),
+               "load_alone_ms": round(alone_ms, 3),
+               "load_alone_gbs": round(w.load_bytes() / (alone_ms * 1e-3) / GB, 2),
+               "load_overlap_span_ms": round(load_span, 3),
+               "load_overlap_gbs": round(w.load_bytes() / (load_span * 1e-3) / GB, 2),
+               "gemm_alone_ms": round(gemm_ms, 4), "gemm_overlap_ms": round(g_ms, 4),
+               "gemm_slowdown_pct": round(100 * (g_ms / gemm_ms - 1), 2),
+               "e2e_ms": round(e2e, 3),
+               "serial_ms": round(alone_ms + s.num_layers * gemm_ms, 3),
+               "layer_bytes": layer_bytes})
+    arena.close()
+    kvx.kvx_destroy(ctx)
+
+
+def run_qwen7b(args, kvx, wl):
+    """64 requests with partial prefix hits: one batched load (stream A) and one batched
+    store (stream B) at the same time."""
+    w = wl.qwen7b_batch()
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    dev_tables = [torch.from_numpy(r.page_table).cuda() for r in w.load_requests]
+    reqs = kvx.requests_array([(d.data_ptr(), r.page_table, r.n_tokens)
+                               for d, r in zip(dev_tables, w.load_requests)])
+    ld = kvx.HostBuffer(w.load_arena_bytes)
+    _fill_host(ld.array, w.load_arena_bytes, s, w.seed, 2, wl)
+    st = kvx.HostBuffer(w.store_arena_bytes)
+    st.array[:] = 0
+    ch_ld = kvx.chunks_array(w.load_chunks, ld.ptr)
+    ch_st = kvx.chunks_array(w.store_chunks, st.ptr)
+    ctx_a, ctx_b = kvx.kvx_create(0, 64 << 20), kvx.kvx_create(0, 64 << 20)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    Nl, Ns = w.load_bytes(), w.store_bytes()
+
+    def load():
+        kvx.kvx_load_chunks(ctx_a, pool, reqs, ch_ld, stream=sa.cuda_stream)
+
+    def store():
+        kvx.kvx_store_chunks(ctx_b, pool, reqs, ch_st, stream=sb.cuda_stream)
+
+    load_ms = _timed(sa, load, 5)
+    store_ms = _timed(sb, store, 5)
+    spans = []
+    for rep in range(5):
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(sa)
+        sb.wait_event(start)
+        load()
+        store()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(sa)
+        eb.record(sb)
+        torch.cuda.synchronize()
+        spans.append((start.elapsed_time(ea), start.elapsed_time(eb)))
+    assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
+    assert kvx.kvx_get_status(ctx_b, sb.cuda_stream) == 0
+    la = statistics.median(x[0] for x in spans)
+    sbm = statistics.median(x[1] for x in spans)
+    both = statistics.median(max(x) for x in spans)
+    # Bidirectional copy-engine peak for context: 4 GiB each way at once.
+    hp = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
+    hp2 = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
+    dp = torch.empty(4 << 30, dtype=torch.uint8, device="cuda")
+    dp2 = torch.empty(4 << 30, dtype=torch.uint8, device="cuda")
+    bid = []
+    for rep in range(4):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(sa):
+            dp.copy_(hp, non_blocking=True)
+        with torch.cuda.stream(sb):
+            hp2.copy_(dp2, non_blocking=True)
+        torch.cuda.synchronize()
+        bid.append(time.perf_counter() - t0)
+    _emit({"workload": "qwen7b_batched_partial_hits", "requests": len(w.load_requests),
+           "load_bytes": Nl, "store_bytes": Ns,
+           "load_chunks": len(w.load_chunks), "store_chunks": len(w.store_chunks),
+           "load_alone_gbs": round(Nl / (load_ms * 1e-3) / GB, 2),
+           "store_alone_gbs": round(Ns / (store_ms * 1e-3) / GB, 2),
+           "concurrent_load_gbs": round(Nl / (la * 1e-3) / GB, 2),
+           "concurrent_store_gbs": round(Ns / (sbm * 1e-3) / GB, 2),
+           "concurrent_aggregate_gbs": round((Nl + Ns) / (both * 1e-3) / GB, 2),
+           "concurrent_ms": round(both, 3),
+           "memcpy_bidirectional_gbs": round(2 * (4 << 30) / statistics.median(bid) / GB, 2)})
+    ld.close()
+    st.close()
+    kvx.kvx_destroy(ctx_a)
+    kvx.kvx_destroy(ctx_b)
+
+
+def run_mla_sweep(args, kvx, wl):
+    """MLA latent cache (61 layers x 1152 B per token), page size x chunk size grid, kernel
+    against the per-page DMA baseline, both directions."""
+    ctx = kvx.kvx_create(0, 64 << 20)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    for P in wl.MLA_PAGE_SIZES:
+        for Cb in wl.MLA_CHUNK_BYTES:
+            w = wl.mla_sweep(P, Cb)
+            s = w.shape
+            pools = _pool_tensor(s, w.seed, wl)
+            pool = kvx.Pool.from_tensor(pools, s.page_size)
+            src, dst = w.store_requests[0], w.load_requests[0]
+            ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+            rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+            rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+            arena = kvx.HostBuffer(w.store_arena_bytes)
+            arena.array[:] = 0
+            ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+            N = w.store_bytes()
+            st_ms = _timed(stream, lambda: kvx.kvx_store_chunks(ctx, pool, rs, ch, stream=sh), 5)
+            ld_ms = _timed(stream, lambda: kvx.kvx_load_chunks(ctx, pool, rd, ch, stream=sh), 5)
+            segs = kvx.kvx_last_launch(ctx)[0]
+            dma = {}
+            for name, d, rq in (("store", kvx.KVX_DIR_GATHER, rs), ("load", kvx.KVX_DIR_SCATTER, rd)):
+                kvx.kvx_dma_baseline(ctx, d, pool, rq, ch, stream=sh)
+                stream.synchronize()
+                t0 = time.perf_counter()
+                n = kvx.kvx_dma_baseline(ctx, d, pool, rq, ch, stream=sh)
+                stream.synchronize()
+                dma[name] = (N / (time.perf_counter() - t0) / GB, n)
+            assert kvx.kvx_get_status(ctx, sh) == 0
+            _emit({"workload": "mla_sweep", "page_size": P, "chunk_kib": Cb >> 10,
+                   "tokens_per_chunk": w.store_chunks[0].n_tokens, "chunks": len(w.store_chunks),
+                   "segments": segs, "bytes": N,
+                   "store_gbs": round(N / (st_ms * 1e-3) / GB, 2),
+                   "load_gbs": round(N / (ld_ms * 1e-3) / GB, 2),
+                   "dma_store_gbs": round(dma["store"][0], 2),
+                   "dma_load_gbs": round(dma["load"][0], 2), "dma_copies": dma["store"][1]})
+            arena.close()
+            del pools
+    kvx.kvx_destroy(ctx)
+
+
+def run_sm_sweep(args, kvx, wl):
+    """SM cap x unroll x threads for store and load of the Llama-3.1-8B-shaped request."""
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src, dst = w.store_requests[0], w.load_requests[0]
+    ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+    rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+    rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+    arena = kvx.HostBuffer(w.store_arena_bytes)
+    arena.array[:] = 0
+    ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+    ctx = kvx.kvx_create(0)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    N = w.store_bytes()
+    for cap in (1, 2, 4, 8, 12, 16, 24, 32, 64, 0):
+        for threads, unroll in ((1024, 8), (1024, 4), (512, 8), (256, 8)):
+            row = {"workload": "llama8b_sm_sweep", "sm_cap": cap, "threads": threads,
+                   "unroll": unroll}
+            for name, op, fn, rq in (("store", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs),
+                                     ("load", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd)):
+                c = kvx.kvx_default_launch_cfg(ctx, op)
+                c.sm_cap, c.threads, c.unroll, c.ctas_per_sm = cap, threads, unroll, 1
+                ms = _timed(stream, lambda: fn(ctx, pool, rq, ch, 0, s.num_layers, c, sh), 3, 1)
+                row[f"{name}_gbs"] = round(N / (ms * 1e-3) / GB, 2)
+            _emit(row)
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    arena.close()
+    kvx.kvx_destroy(ctx)
+
+
+def run_transform_sweep(args, kvx, wl):
+    """Launch shapes of the HBM transform (chunks in device memory), Llama-3.1-8B shape."""
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src, dst = w.store_requests[0], w.load_requests[0]
+    ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+    rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+    rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+    dchunk = torch.empty(w.store_arena_bytes, dtype=torch.uint8, device="cuda")
+    ch = kvx.chunks_array(w.store_chunks, dchunk.data_ptr())
+    ctx = kvx.kvx_create(0)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    N = w.store_bytes()
+    hbm, _ = peaks()
+    for ctas, threads, unroll in ((1, 1024, 8), (2, 1024, 4), (1, 1024, 4), (2, 512, 8),
+                                  (4, 512, 4), (4, 256, 8), (8, 256, 4), (2, 1024, 2),
+                                  (1, 512, 8), (3, 512, 4)):
+        for hint in (0, 1):
+            row = {"workload": "llama8b_transform_sweep", "ctas_per_sm": ctas,
+                   "threads": threads, "unroll": unroll, "store_hint": hint}
+            for name, d, rq in (("gather", kvx.KVX_DIR_GATHER, rs),
+                                ("scatter", kvx.KVX_DIR_SCATTER, rd)):
+                c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM)
+                c.sm_cap, c.ctas_per_sm, c.threads, c.unroll, c.store_hint = 0, ctas, threads, unroll, hint
+                ms = _timed(stream, lambda: kvx.kvx_transform_hbm(ctx, d, pool, rq, ch, 0,
+                                                                  s.num_layers, c, sh), 10, 3)
+                gbs = 2 * N / (ms * 1e-3) / GB
+                row[f"{name}_gbs_2n"] = round(gbs, 1)
+                row[f"{name}_frac"] = round(gbs / hbm, 4)
+            _emit(row)
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    kvx.kvx_destroy(ctx)
+
+
+def run_profile_small(args, kvx, wl):
+    """A small case for ncu captures: the Llama-3.1-8B shape cut to 8192 tokens (1 GiB per
+    direction, above the 129 MB L2) in a 1024-page pool (2 GiB), one operation 3 times
+    with the library's default launch configuration."""
+    w = wl.llama8b(num_pages=1024, n_tokens=8192)
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src, dst = w.store_requests[0], w.load_requests[0]
+    ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+    rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+    rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+    ctx = kvx.kvx_create(0)
+    sh = torch.cuda.current_stream().cuda_stream
+    if args.profile_op in ("store", "load"):
+        buf = kvx.HostBuffer(w.store_arena_bytes)
+        buf.array[:] = 0
+        ch = kvx.chunks_array(w.store_chunks, buf.ptr)
+    else:
+        dchunk = torch.zeros(w.store_arena_bytes, dtype=torch.uint8, device="cuda")
+        ch = kvx.chunks_array(w.store_chunks, dchunk.data_ptr())
+    for _ in range(3):
+        if args.profile_op == "store":
+            kvx.kvx_store_chunks(ctx, pool, rs, ch, stream=sh)
+        elif args.profile_op == "load":
+            kvx.kvx_load_chunks(ctx, pool, rd, ch, stream=sh)
+        else:
+            d = kvx.KVX_DIR_GATHER if args.profile_op == "gather" else kvx.KVX_DIR_SCATTER
+            kvx.kvx_transform_hbm(ctx, d, pool, rs if d == kvx.KVX_DIR_GATHER else rd, ch,
+                                  stream=sh)
+    torch.cuda.synchronize()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
+    _emit({"workload": "profile_small", "op": args.profile_op, "bytes": w.store_bytes(),
+           "items": items, "ctas": ctas, "threads": threads})
+    kvx.kvx_destroy(ctx)
+
+
+def run_workload(args):
+    torch.cuda.set_device(0)
+    from paged_kv_gather_gb300.build import build
+    build()
+    from paged_kv_gather_gb300 import kvx
+    from paged_kv_gather_gb300 import workloads as wl
+    {"llama70b": run_llama70b, "qwen7b_batch": run_qwen7b, "mla_sweep": run_mla_sweep,
+     "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
+     "profile_small": run_profile_small}[args.workload](
+        args, kvx, wl)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "llama8b":
+        run_workload(args)
     else:
         run_ours(args)
 

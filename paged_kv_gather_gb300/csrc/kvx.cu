@@ -268,11 +268,11 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
         c->unroll = 8;
         c->store_hint = KVX_HINT_STREAMING;
         break;
-    default:  // HBM transform: the whole GPU
+    default:  // HBM transform: the whole GPU, one 512-thread CTA per SM, 8 loads in flight
         c->sm_cap = 0;
-        c->ctas_per_sm = 2;
-        c->threads = 1024;
-        c->unroll = 4;
+        c->ctas_per_sm = 1;
+        c->threads = 512;
+        c->unroll = 8;
         c->store_hint = KVX_HINT_STREAMING;
         break;
     }

@@ -184,3 +184,44 @@ def random_case(rng: np.random.Generator, max_tokens=700):
     lb = int(rng.integers(0, L + 1)) if rng.random() < 0.4 else 0
     le = int(rng.integers(lb, L + 1)) if rng.random() < 0.4 else L
     return shape, lens, tables, load_tables, specs, lb, le
+
+
+def pinned_copy(t: torch.Tensor, out: Optional[torch.Tensor] = None) -> np.ndarray:
+    """Copy a device tensor into pinned host memory (fast D2H) and return a numpy view."""
+    if out is None:
+        out = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    out.copy_(t)
+    return out.numpy()
+
+
+class HostPool:
+    """Oracle pool over a copy of a whole device pool tensor in mapped pinned memory
+    (kvx_host_alloc, released by close(), unlike torch's caching host allocator)."""
+
+    def __init__(self, t: torch.Tensor, page_size: int):
+        self.hb = kvx.HostBuffer(t.numel())
+        h = torch.from_numpy(self.hb.array).view(t.shape)
+        h.copy_(t)
+        arr = self.hb.array.reshape(t.shape)
+        KV, L = t.shape[:2]
+        self.pool = oracle.Pool([[arr[k, l] for l in range(L)] for k in range(KV)], page_size)
+
+    def close(self):
+        self.pool = None
+        self.hb.close()
+
+
+def host_arena_view(hb, nbytes):
+    return hb.array[:nbytes]
+
+
+def slab_ranges(c, shape, layer):
+    """Byte ranges (offset, length) of one layer's slabs inside a layer-major chunk."""
+    out = []
+    if not (c.layer_begin <= layer < c.layer_begin + c.n_layers):
+        return out
+    slab = c.n_tokens * shape.token_bytes
+    for k in range(shape.kv_factor):
+        off = c.offset + ((layer - c.layer_begin) * shape.kv_factor + k) * slab
+        out.append((off, slab))
+    return out
