@@ -4,10 +4,12 @@
 One step = one full pass of the hot path over the Llama-3.1-8B-shaped request:
   kvx_store_chunks  32768 tokens x 32 layers x K/V (2048 random pages of a 16384-page
                     pool) gathered into 128 layer-major chunks of 256 tokens (32 MiB each)
-                    in mapped pinned host memory, then
-  kvx_load_chunks   those chunks scattered back into a disjoint set of 2048 fresh pages.
-Each direction moves N = 4 GiB over the host link; value = 2N per step / step time (GB/s).
-Inputs (4 GiB each way) are larger than L2 (129 MB), so no L2 flush is needed.
+                    in mapped pinned host memory, and
+  kvx_load_chunks   those chunks scattered back into a disjoint set of 2048 fresh pages,
+pipelined in chunk groups on two streams (group g's load after group g's store) so both
+directions of the host link carry data at once.  Each direction moves N = 4 GiB; value =
+2N per step / step time (GB/s).  Inputs (4 GiB each way) exceed L2 (129 MB): no flush.
+The same store and load run back to back on one stream give the per-direction rooflines.
 
 Also measured in the same run and printed on the same JSON line:
   host_link_peak  one 4 GiB pinned cudaMemcpyAsync per direction (the store/load roofline);
@@ -63,6 +65,8 @@ def parse():
     p.add_argument("--profile-op", default="load",
                    choices=["store", "load", "gather", "scatter"],
                    help="operation of --workload profile_small")
+    p.add_argument("--groups", type=int, default=8,
+                   help="chunk groups of the pipelined store/load round trip")
     p.add_argument("--sm-caps", default="1,2,4,8,16,32,0",
                    help="SM caps of the llama70b overlap sweep (0 = all SMs)")
     return p.parse_args()
@@ -308,6 +312,50 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- our arm
 
+class RoundTrip:
+    """The headline step: store the request's 128 chunks to host memory and load them back
+    into the fresh page set, pipelined in `groups` chunk groups on two streams so the two
+    directions of the host link run at once.  Group g's load waits for group g's store
+    (event); group g's next store waits for group g's previous load, so a chunk is never
+    overwritten while it is being read.  Each call is one kernel launch."""
+
+    def __init__(self, kvx, ctx_s, ctx_l, pool, reqs_src, reqs_dst, chunks, num_layers,
+                 cfg_s, cfg_l, groups, dev):
+        self.kvx, self.ctx_s, self.ctx_l, self.pool = kvx, ctx_s, ctx_l, pool
+        self.rs, self.rd, self.L = reqs_src, reqs_dst, num_layers
+        self.cfg_s, self.cfg_l = cfg_s, cfg_l
+        bounds = np.linspace(0, len(chunks), groups + 1).astype(int)
+        self.groups = [np.ascontiguousarray(chunks[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
+        self.ss = torch.cuda.Stream(device=dev)
+        self.sl = torch.cuda.Stream(device=dev)
+        self.loaded = [None] * groups
+
+    def step(self, t_store=None, t_load=None):
+        kvx = self.kvx
+        for g, ch in enumerate(self.groups):
+            if self.loaded[g] is not None:
+                self.ss.wait_event(self.loaded[g])
+            e = t_store.start() if t_store else None
+            kvx.kvx_store_chunks(self.ctx_s, self.pool, self.rs, ch, 0, self.L, self.cfg_s,
+                                 self.ss.cuda_stream)
+            if e is not None:
+                t_store.stop(e)
+            stored = torch.cuda.Event()
+            stored.record(self.ss)
+            self.sl.wait_event(stored)
+            e = t_load.start() if t_load else None
+            kvx.kvx_load_chunks(self.ctx_l, self.pool, self.rd, ch, 0, self.L, self.cfg_l,
+                                self.sl.cuda_stream)
+            if e is not None:
+                t_load.stop(e)
+            done = torch.cuda.Event()
+            done.record(self.sl)
+            self.loaded[g] = done
+
+    def launches_per_step(self):
+        return 2 * len(self.groups)
+
+
 def run_ours(args):
     world, rank, local = dist_setup(args)
     torch.cuda.set_device(local)
@@ -340,21 +388,14 @@ def run_ours(args):
     host.array[:] = 0  # fault in every page before timing
     chunks_host = kvx.chunks_array(w.store_chunks, host.ptr)
     ctx = kvx.kvx_create(local)
+    ctx_l = kvx.kvx_create(local)
     cfg_store = parse_cfg(kvx, ctx, kvx.KVX_OP_STORE, args.store_cfg)
     cfg_load = parse_cfg(kvx, ctx, kvx.KVX_OP_LOAD, args.load_cfg)
     cfg_tr = parse_cfg(kvx, ctx, kvx.KVX_OP_GATHER_HBM, args.transform_cfg)
+    rt = RoundTrip(kvx, ctx, ctx_l, pool, reqs_src, reqs_dst, chunks_host, s.num_layers,
+                   cfg_store, cfg_load, args.groups, dev)
 
-    def step(t_store=None, t_load=None):
-        e = t_store.start() if t_store else None
-        kvx.kvx_store_chunks(ctx, pool, reqs_src, chunks_host, 0, s.num_layers, cfg_store, sh)
-        if e is not None:
-            t_store.stop(e)
-        e = t_load.start() if t_load else None
-        kvx.kvx_load_chunks(ctx, pool, reqs_dst, chunks_host, 0, s.num_layers, cfg_load, sh)
-        if e is not None:
-            t_load.stop(e)
-
-    # ---- host-link peak: one 4 GiB pinned copy per direction
+    # ---- host-link peaks: one 4 GiB pinned copy per direction, then both at once
     link = {}
     hp = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
     dp = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
@@ -370,54 +411,106 @@ def run_ours(args):
                 t.stop(e)
             stream.synchronize()
             link[name] = round((4 << 30) / (statistics.median(t.ms()) * 1e-3) / GB, 1)
-    del hp, dp
-
-    # ---- warm-up, then the timed region (device clock)
-    for _ in range(args.warmup):
-        step()
-    stream.synchronize()
-    assert kvx.kvx_get_status(ctx, sh) == 0
-    ts, tl = EventTimer(stream), EventTimer(stream)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_all = EventTimer(stream)
-        e = t_all.start()
-        for _ in range(args.steps):
-            step(ts, tl)
-        t_all.stop(e)
+    hp2 = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
+    dp2 = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
+    s2 = torch.cuda.Stream(device=dev)
+    bid = []
+    for rep in range(5):
         torch.cuda.synchronize()
-    barrier(world)
-    total_ms = max_over_ranks(t_all.ms()[0], world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        s2.wait_event(e0)
+        with torch.cuda.stream(stream):
+            dp.copy_(hp, non_blocking=True)
+        with torch.cuda.stream(s2):
+            hp2.copy_(dp2, non_blocking=True)
+        e1, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e1.record(stream)
+        e2.record(s2)
+        torch.cuda.synchronize()
+        if rep:
+            bid.append(max(e0.elapsed_time(e1), e0.elapsed_time(e2)))
+    link["bidir"] = round(2 * (4 << 30) / (statistics.median(bid) * 1e-3) / GB, 1)
+    del hp, dp, hp2, dp2
+
+    # ---- sequential store then load on one stream (per-direction rooflines)
+    def seq_step(t_store=None, t_load=None):
+        e = t_store.start() if t_store else None
+        kvx.kvx_store_chunks(ctx, pool, reqs_src, chunks_host, 0, s.num_layers, cfg_store, sh)
+        if e is not None:
+            t_store.stop(e)
+        e = t_load.start() if t_load else None
+        kvx.kvx_load_chunks(ctx, pool, reqs_dst, chunks_host, 0, s.num_layers, cfg_load, sh)
+        if e is not None:
+            t_load.stop(e)
+
+    for _ in range(args.warmup):
+        seq_step()
+    ts, tl = EventTimer(stream), EventTimer(stream)
+    for _ in range(max(3, args.steps // 2)):
+        seq_step(ts, tl)
+    stream.synchronize()
     assert kvx.kvx_get_status(ctx, sh) == 0
     store_ms = statistics.mean(ts.ms())
     load_ms = statistics.mean(tl.ms())
-    items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
+    store_gbs = N / (store_ms * 1e-3) / GB
+    load_gbs = N / (load_ms * 1e-3) / GB
 
-    # ---- end to end through the C ABI on the host clock
+    # ---- the timed region: the pipelined round trip (device clock)
+    for _ in range(args.warmup):
+        rt.step()
+    torch.cuda.synchronize()
+    ps, pl = EventTimer(rt.ss), EventTimer(rt.sl)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_start.record(rt.ss)
+        rt.sl.wait_event(e_start)
+        for _ in range(args.steps):
+            rt.step(ps, pl)
+        e_end = torch.cuda.Event(enable_timing=True)
+        e_end.record(rt.sl)
+        torch.cuda.synchronize()
+    total_ms = max_over_ranks(e_start.elapsed_time(e_end), world)
+    barrier(world)
+    assert kvx.kvx_get_status(ctx, rt.ss.cuda_stream) == 0
+    assert kvx.kvx_get_status(ctx_l, rt.sl.cuda_stream) == 0
+    items, ctas, threads, _ = kvx.kvx_last_launch(ctx_l)
+    p_store_ms = statistics.mean(ps.ms())
+    p_load_ms = statistics.mean(pl.ms())
+    group_bytes = N / args.groups
+
+    # ---- end to end through the C ABI on the host clock (pipelined step + uploads/readback)
     pt_host = torch.from_numpy(np.concatenate([src_h, dst_h])).pin_memory()
     pt_dev = torch.empty_like(pt_host, device=dev)
     e2e_ms = []
+    desc = 0
     for i in range(args.warmup + max(3, args.steps // 2)):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
+        with torch.cuda.stream(rt.ss):
             pt_dev.copy_(pt_host, non_blocking=True)
-        r_src = kvx.requests_array([(pt_dev.data_ptr(), src_h, w.store_requests[0].n_tokens)])
-        r_dst = kvx.requests_array([(pt_dev.data_ptr() + 4 * len(src_h), dst_h,
+        up = torch.cuda.Event()
+        up.record(rt.ss)
+        rt.sl.wait_event(up)
+        rt.rs = kvx.requests_array([(pt_dev.data_ptr(), src_h, w.store_requests[0].n_tokens)])
+        rt.rd = kvx.requests_array([(pt_dev.data_ptr() + 4 * len(src_h), dst_h,
                                      w.load_requests[0].n_tokens)])
-        kvx.kvx_store_chunks(ctx, pool, r_src, chunks_host, 0, s.num_layers, cfg_store, sh)
-        kvx.kvx_load_chunks(ctx, pool, r_dst, chunks_host, 0, s.num_layers, cfg_load, sh)
-        flags = kvx.kvx_get_status(ctx, sh)  # D2H of the status word + stream sync
-        assert flags == 0
+        rt.step()
+        desc = kvx.kvx_last_launch(ctx)[3] + kvx.kvx_last_launch(ctx_l)[3]
+        assert kvx.kvx_get_status(ctx, rt.ss.cuda_stream) == 0   # D2H status word + sync
+        assert kvx.kvx_get_status(ctx_l, rt.sl.cuda_stream) == 0
         if i >= args.warmup:
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    desc_bytes = 2 * kvx.kvx_last_launch(ctx)[3]  # packed descriptors of both calls
+    rt.rs, rt.rd = reqs_src, reqs_dst
     e2e = {"value": round(2 * N / (statistics.median(e2e_ms) * 1e-3) / GB, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": int(pt_host.numel() * 4 + desc_bytes), "d2h_bytes_per_step": 4,
+           "h2d_bytes_per_step": int(pt_host.numel() * 4 + desc * args.groups),
+           "d2h_bytes_per_step": 8,
            "payload_link_bytes_per_step": 2 * N,
-           "note": "KV payload crosses the host link inside the kernels (zero-copy); the "
-                   "counted copies are the page tables, descriptors and status word"}
+           "note": "KV payload crosses the host link inside the kernels (zero-copy, mapped "
+                   "pinned memory); the counted copies are the page tables, descriptors and "
+                   "the two status words"}
 
     # ---- HBM transform on the same request (chunks in device memory)
     dchunk = torch.empty(w.store_arena_bytes, dtype=torch.uint8, device=dev)
@@ -446,13 +539,11 @@ def run_ours(args):
     transform = {
         "gather_ms": round(g_ms, 4), "scatter_ms": round(s_ms, 4),
         "gather_gbs_2n": round(tr_gbs["gather"], 1), "scatter_gbs_2n": round(tr_gbs["scatter"], 1),
-        "gather_gbs_n": round(tr_gbs["gather"] / 2, 1),
         "roofline": {"bound": "hbm", "achieved": round(tr_gbs[dom_tr], 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(tr_gbs[dom_tr] / hbm_peak, 4),
                      "traffic": recorded_traffic(f"transform_{dom_tr}", "llama8b"),
                      "kernel": f"kvx_segment_kernel ({dom_tr}, HBM chunks)",
-                     "peak_source": hbm_src,
-                     "algorithmic_bytes": 2 * N},
+                     "peak_source": hbm_src, "algorithmic_bytes": 2 * N},
         "cfg": cfg_tr.as_dict()}
     del dchunk
 
@@ -477,11 +568,7 @@ def run_ours(args):
         cpu = CpuSample(os.cpu_count() or 1).run(args.cpu_seconds)
 
     value = 2 * N * args.steps * world / (total_ms * 1e-3) / GB
-    store_gbs = N / (store_ms * 1e-3) / GB
-    load_gbs = N / (load_ms * 1e-3) / GB
-    dom = "load" if load_ms >= store_ms else "store"
-    dom_gbs = load_gbs if dom == "load" else store_gbs
-    dom_peak = link["h2d"] if dom == "load" else link["d2h"]
+    step_gbs = 2 * N / (total_ms / args.steps * 1e-3) / GB
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -490,35 +577,52 @@ def run_ours(args):
         "config": {"workload": "llama8b_kv: 32 layers, 8 KV heads x 128, bf16 N(0,1), "
                                "16-token pages, 32768 tokens on 2048 random pages of a "
                                "16384-page pool, 128 layer-major chunks of 256 tokens (32 MiB) "
-                               "in mapped pinned host memory; step = store + load",
+                               "in mapped pinned host memory; step = store all chunks + load "
+                               f"them into 2048 fresh pages, pipelined in {args.groups} chunk "
+                               "groups on two streams",
                    "bytes_per_direction": N, "l2": "inputs larger than L2 (4 GiB per "
                    "direction), no flush", "parallelism": f"replicas x{world}" if world > 1
                    else "single GPU"},
-        "roofline": {"bound": "host_link", "achieved": round(dom_gbs, 2), "peak": dom_peak,
-                     "unit": "GB/s", "frac": round(dom_gbs / dom_peak, 4),
-                     "traffic": recorded_traffic(dom, "llama8b"),
-                     "kernel": f"kvx_segment_kernel ({dom})",
-                     "peak_source": "measured in this run: one 4 GiB pinned cudaMemcpyAsync "
-                                    f"{'H2D' if dom == 'load' else 'D2H'}",
-                     "algorithmic_bytes": N, "items_per_launch": items},
-        "store": {"ms": round(store_ms, 4), "gbs": round(store_gbs, 2),
-                  "frac_of_link": round(store_gbs / link["d2h"], 4), "cfg": cfg_store.as_dict()},
-        "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
-                 "frac_of_link": round(load_gbs / link["h2d"], 4), "cfg": cfg_load.as_dict()},
+        "roofline": {"bound": "host_link", "achieved": round(step_gbs, 2),
+                     "peak": link["bidir"], "unit": "GB/s",
+                     "frac": round(step_gbs / link["bidir"], 4),
+                     "traffic": recorded_traffic("store", "llama8b"),
+                     "kernel": "kvx_segment_kernel store + load, concurrent on one link",
+                     "peak_source": "measured in this run: 4 GiB pinned cudaMemcpyAsync H2D "
+                                    "and D2H at once (both link directions)",
+                     "algorithmic_bytes": 2 * N,
+                     "per_launch": {"store_ms": round(p_store_ms, 4),
+                                    "store_gbs": round(group_bytes / (p_store_ms * 1e-3) / GB, 2),
+                                    "load_ms": round(p_load_ms, 4),
+                                    "load_gbs": round(group_bytes / (p_load_ms * 1e-3) / GB, 2),
+                                    "bytes_per_launch": int(group_bytes),
+                                    "items_per_launch": items}},
+        "sequential": {
+            "note": "store then load on one stream, no overlap: per-direction rooflines",
+            "step_gbs": round(2 * N / ((store_ms + load_ms) * 1e-3) / GB, 2),
+            "store": {"ms": round(store_ms, 4), "gbs": round(store_gbs, 2),
+                      "peak": link["d2h"], "frac": round(store_gbs / link["d2h"], 4),
+                      "traffic": recorded_traffic("store", "llama8b")},
+            "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
+                     "peak": link["h2d"], "frac": round(load_gbs / link["h2d"], 4),
+                     "traffic": recorded_traffic("load", "llama8b")}},
+        "cfg": {"store": cfg_store.as_dict(), "load": cfg_load.as_dict()},
         "host_link_peak": {"h2d_gbs": link["h2d"], "d2h_gbs": link["d2h"],
+                           "bidirectional_gbs": link["bidir"],
                            "nominal_gbs_per_direction": 450.0,
                            "nominal_note": "NVLink-C2C 900 GB/s bidirectional"},
         "transform": transform,
         "dma_baseline": dma,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": rt.launches_per_step() * args.steps,
         "clocks": clocks.summary(),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     host.close()
     kvx.kvx_destroy(ctx)
+    kvx.kvx_destroy(ctx_l)
 
 
 # ----------------------------------------------------------------------------- other workloads
@@ -571,7 +675,7 @@ def run_llama70b(args, kvx, wl):
     per_layer = [kvx.chunks_array([c for c in w.load_chunks if c.layer_begin == l], arena.ptr)
                  for l in range(s.num_layers)]
     ctx = kvx.kvx_create(0)
-    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sb = torch.cuda.Stream()
     g = torch.Generator(device="cuda")
     g.manual_seed(w.seed)
     A = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16, generator=g)
@@ -584,7 +688,10 @@ def run_llama70b(args, kvx, wl):
 
     with torch.cuda.stream(sb):
         gemm_ms = _timed(sb, gemm, 20, warm=5)
-    for cap in [int(x) for x in args.sm_caps.split(",")]:
+    caps = [int(x) for x in args.sm_caps.split(",")]
+    for cap, prio in [(c, p) for p in (-1, 0) for c in caps]:
+        # Loads on a high-priority stream (-1) get SMs as soon as GEMM CTAs retire.
+        sa = torch.cuda.Stream(priority=prio)
         cfg = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD)
         cfg.sm_cap = cap
 
@@ -619,6 +726,7 @@ def run_llama70b(args, kvx, wl):
         e2e = start.elapsed_time(end_b)
         g_ms = statistics.mean(gt.ms())
         _emit({"workload": "llama70b_layer_streaming", "sm_cap": cap,
+               "load_stream_priority": "high" if prio < 0 else "normal",
                "load_cfg": cfg.as_dict(),
                "load_alone_ms": round(alone_ms, 3),
                "load_alone_gbs": round(w.load_bytes() / (alone_ms * 1e-3) / GB, 2),

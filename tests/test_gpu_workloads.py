@@ -144,9 +144,46 @@ def test_llama8b_full_size_all_paths(ctx):
     hp.close()
 
 
+def test_llama8b_pipelined_round_trip_as_benchmarked(ctx):
+    """The headline step exactly as bench.py runs it: store and load pipelined in 8 chunk
+    groups on two streams, two steps back to back (the second step's stores wait for the
+    first step's loads of the same group)."""
+    import bench
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pools(s, w.seed)
+    hp = HostPool(pools, s.page_size)
+    src, dst = _requests(w.store_requests), _requests(w.load_requests)
+    arena = kvx.HostBuffer(w.store_arena_bytes + 4096)
+    arena.array[:] = CANARY
+    ctx_l = kvx.kvx_create(0)
+    try:
+        pool = kvx.Pool.from_tensor(pools, s.page_size)
+        rt = bench.RoundTrip(kvx, ctx, ctx_l, pool, src.array, dst.array,
+                             kvx.chunks_array(w.store_chunks, arena.ptr), s.num_layers,
+                             kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_STORE),
+                             kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD), 8,
+                             torch.device("cuda", 0))
+        rt.step()
+        rt.step()
+        torch.cuda.synchronize()
+        assert kvx.kvx_get_status(ctx, rt.ss.cuda_stream) == 0
+        assert kvx.kvx_get_status(ctx_l, rt.sl.cuda_stream) == 0
+    finally:
+        kvx.kvx_destroy(ctx_l)
+    expect = np.full(w.store_arena_bytes + 4096, CANARY, np.uint8)
+    oracle.store(hp.pool, src.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
+    assert_bytes_equal(arena.array, expect, "llama8b pipelined store")
+    oracle.load(hp.pool, dst.oracle(), oracle_chunks(w.load_chunks, expect), threads=16)
+    _compare_pool(pools, hp.pool, "llama8b pipelined load")
+    arena.close()
+    hp.close()
+
+
 # ----------------------------------------------------------------------------- llama70b
 
 def test_llama70b_layer_streamed_load_full_size(ctx):
+    """80 per-layer loads on a high-priority stream, as the streamed prefill issues them."""
     w = wl.llama70b()
     s = w.shape
     assert w.load_bytes() == 20 << 30
@@ -157,9 +194,9 @@ def test_llama70b_layer_streamed_load_full_size(ctx):
     _fill_host(arena.array, nbytes, s, w.seed, stream_id=1)
     per_layer = [[c for c in w.load_chunks if c.layer_begin == l] for l in range(s.num_layers)]
     arrays = [kvx.chunks_array(cs, arena.ptr) for cs in per_layer]
-    stream = torch.cuda.Stream()
+    stream = torch.cuda.Stream(priority=-1)
     pool = kvx.Pool.from_tensor(pools, s.page_size)
-    for l in range(s.num_layers):  # one call per layer, as the streamed prefill issues them
+    for l in range(s.num_layers):
         kvx.kvx_load_chunks(ctx, pool, dst.array, arrays[l], l, l + 1, stream=stream.cuda_stream)
     stream.synchronize()
     assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
