@@ -879,14 +879,19 @@ def run_sm_sweep(args, kvx, wl):
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
     N = w.store_bytes()
-    for cap in (1, 2, 4, 8, 12, 16, 24, 32, 64, 0):
-        for threads, unroll in ((1024, 8), (1024, 4), (512, 8), (256, 8)):
-            row = {"workload": "llama8b_sm_sweep", "sm_cap": cap, "threads": threads,
-                   "unroll": unroll}
+    shapes = [("segment", 1024, 8, 1, 0), ("segment", 512, 8, 1, 0),
+              ("bulk", 32, 6, 1, 32768), ("bulk", 32, 3, 2, 32768), ("bulk", 32, 4, 1, 49152)]
+    for cap in (1, 2, 4, 8, 12, 16, 32, 0):
+        for mapping, threads, unroll, ctas, stage in shapes:
+            row = {"workload": "llama8b_sm_sweep", "sm_cap": cap, "mapping": mapping,
+                   "threads": threads, "unroll": unroll, "ctas_per_sm": ctas,
+                   "stage_bytes": stage}
             for name, op, fn, rq in (("store", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs),
                                      ("load", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd)):
                 c = kvx.kvx_default_launch_cfg(ctx, op)
-                c.sm_cap, c.threads, c.unroll, c.ctas_per_sm = cap, threads, unroll, 1
+                c.sm_cap, c.threads, c.unroll, c.ctas_per_sm = cap, threads, unroll, ctas
+                c.mapping = kvx.KVX_MAP_BULK if mapping == "bulk" else kvx.KVX_MAP_WARP_SEGMENT
+                c.stage_bytes = stage
                 ms = _timed(stream, lambda: fn(ctx, pool, rq, ch, 0, s.num_layers, c, sh), 3, 1)
                 row[f"{name}_gbs"] = round(N / (ms * 1e-3) / GB, 2)
             _emit(row)
@@ -912,16 +917,22 @@ def run_transform_sweep(args, kvx, wl):
     sh = stream.cuda_stream
     N = w.store_bytes()
     hbm, _ = peaks()
-    for ctas, threads, unroll in ((1, 1024, 8), (2, 1024, 4), (1, 1024, 4), (2, 512, 8),
-                                  (4, 512, 4), (4, 256, 8), (8, 256, 4), (2, 1024, 2),
-                                  (1, 512, 8), (3, 512, 4)):
-        for hint in (0, 1):
-            row = {"workload": "llama8b_transform_sweep", "ctas_per_sm": ctas,
-                   "threads": threads, "unroll": unroll, "store_hint": hint}
+    shapes = [(0, 1, 512, 8, 1, 0), (0, 1, 512, 8, 0, 0), (0, 1, 1024, 8, 1, 0),
+              (0, 2, 512, 8, 1, 0), (0, 1, 256, 8, 1, 0), (0, 2, 256, 8, 1, 0),
+              (0, 1, 384, 8, 1, 0), (0, 2, 1024, 4, 1, 0),
+              (1, 1, 32, 6, 0, 32768), (1, 2, 32, 3, 0, 32768), (1, 1, 32, 4, 0, 49152),
+              (1, 3, 32, 2, 0, 32768), (1, 2, 32, 6, 0, 16384), (1, 4, 32, 3, 0, 16384)]
+    for mapping, ctas, threads, unroll, hint, stage in shapes:
+        if True:
+            row = {"workload": "llama8b_transform_sweep",
+                   "mapping": "bulk" if mapping else "segment", "ctas_per_sm": ctas,
+                   "threads": threads, "unroll": unroll, "store_hint": hint,
+                   "stage_bytes": stage}
             for name, d, rq in (("gather", kvx.KVX_DIR_GATHER, rs),
                                 ("scatter", kvx.KVX_DIR_SCATTER, rd)):
                 c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM)
                 c.sm_cap, c.ctas_per_sm, c.threads, c.unroll, c.store_hint = 0, ctas, threads, unroll, hint
+                c.mapping, c.stage_bytes = mapping, stage
                 ms = _timed(stream, lambda: kvx.kvx_transform_hbm(ctx, d, pool, rq, ch, 0,
                                                                   s.num_layers, c, sh), 10, 3)
                 gbs = 2 * N / (ms * 1e-3) / GB

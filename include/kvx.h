@@ -73,6 +73,8 @@ typedef enum kvx_status {
 
 /* Bits of the device status word (kvx_get_status). */
 #define KVX_DEV_PAGE_OUT_OF_RANGE 0x1u
+#define KVX_DEV_WAIT_TIMEOUT 0x2u       /* a bulk copy did not complete within ~1 s; the
+                                           kernel stopped early (output incomplete) */
 
 typedef enum kvx_chunk_layout {
     KVX_CHUNK_LAYER_MAJOR = 0,
@@ -118,7 +120,12 @@ typedef struct kvx_chunk {
 } kvx_chunk;
 
 /* Work mapping of the transfer kernel. */
-#define KVX_MAP_WARP_SEGMENT 0  /* one warp per (chunk, layer, kv, page) segment */
+#define KVX_MAP_WARP_SEGMENT 0  /* one warp per (chunk, layer, kv, page) segment; lanes move
+                                   16-byte units through registers */
+#define KVX_MAP_BULK 1          /* one warp per CTA streams segments through a ring of
+                                   shared-memory stages with bulk async copies
+                                   (cp.async.bulk, mbarrier completion); `unroll` is the
+                                   number of stages (2..8), `stage_bytes` their size */
 
 /* Store cache hint for the destination of each 16-byte unit. */
 #define KVX_HINT_DEFAULT 0      /* st.global (write-back) */
@@ -129,11 +136,15 @@ typedef struct kvx_launch_cfg {
                              less work); with ctas_per_sm = 1 the kernel occupies at most
                              sm_cap SMs.  0 = every SM */
     int32_t ctas_per_sm;  /* 0 = the operation's default */
-    int32_t threads;      /* threads per CTA, multiple of 32 in [32, 1024]; 0 = default */
-    int32_t unroll;       /* 16-byte loads in flight per lane before its stores: 1, 2, 4
-                             or 8; 0 = default */
-    int32_t store_hint;   /* KVX_HINT_* */
+    int32_t threads;      /* threads per CTA, multiple of 32 in [32, 1024]; 0 = default
+                             (the bulk mapping always runs one warp per CTA) */
+    int32_t unroll;       /* warp-segment mapping: 16-byte loads in flight per lane before
+                             its stores (1, 2, 4 or 8); bulk mapping: shared-memory stages
+                             (2..8).  0 = default */
+    int32_t store_hint;   /* KVX_HINT_* (warp-segment mapping) */
     int32_t mapping;      /* KVX_MAP_* */
+    int32_t stage_bytes;  /* bulk mapping: bytes per shared-memory stage, a multiple of 16;
+                             stages x stage_bytes <= 220 KiB.  0 = default (32 KiB) */
 } kvx_launch_cfg;
 
 typedef struct kvx_ctx kvx_ctx;

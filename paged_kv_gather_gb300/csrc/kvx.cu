@@ -99,6 +99,55 @@ __device__ __forceinline__ void copy_contig(const uint4 *__restrict__ s, uint4 *
     }
 }
 
+// One work item resolved to addresses: `rows` rows of row_bytes, contiguous on the page side
+// (pitch = token_bytes) and contiguous or strided on the chunk side.
+struct Segment {
+    const char *src;
+    char *dst;
+    int64_t s_pitch;
+    int64_t d_pitch;
+    int32_t rows;
+    bool contiguous;  // rows back to back on both sides: one run of rows * token_bytes
+};
+
+// Resolve item -> segment (warp-collective: every lane of the warp calls it with the same
+// item).  Returns false, after flagging the device status, if the page id is outside the
+// pool; the segment is then skipped.
+template <int DIR>
+__device__ __forceinline__ bool resolve_segment(const Plan &p, int64_t item, int lane,
+                                                Segment &sg)
+{
+    const int64_t v = p.token_bytes;
+    const int c = find_chunk(p.item_begin, p.n_chunks, item, lane);
+    const DevChunk &ch = p.chunks[c];
+    const int64_t i = item - p.item_begin[c];
+    const int32_t np = ch.np;
+    const int32_t slab = int32_t(i / np);
+    const int32_t j = int32_t(i - int64_t(slab) * np);
+    const int32_t kv = p.kv_factor == 2 ? (slab & 1) : 0;
+    const int32_t layer = ch.la + (p.kv_factor == 2 ? (slab >> 1) : slab);
+    const int32_t lpage = ch.pf + j;
+    const int32_t pt0 = lpage * p.page_size;
+    const int32_t tb = max(ch.t0, pt0);
+    const int32_t te = min(ch.t_end, pt0 + p.page_size);
+    const int32_t page = p.reqs[ch.request].page_table[lpage];
+    if (unsigned(page) >= unsigned(p.num_pages)) {
+        if (lane == 0)
+            atomicOr(p.status, KVX_DEV_PAGE_OUT_OF_RANGE);
+        return false;
+    }
+    char *pg = p.pools[kv * p.num_layers + layer] + (int64_t(page) * p.page_size + (tb - pt0)) * v;
+    char *ck = ch.ptr + int64_t(ch.slab0 + slab) * ch.slab_stride +
+               int64_t(tb - ch.t0) * ch.row_stride;
+    sg.src = DIR == KVX_DIR_GATHER ? pg : ck;
+    sg.dst = DIR == KVX_DIR_GATHER ? ck : pg;
+    sg.s_pitch = DIR == KVX_DIR_GATHER ? v : ch.row_stride;
+    sg.d_pitch = DIR == KVX_DIR_GATHER ? ch.row_stride : v;
+    sg.rows = te - tb;
+    sg.contiguous = ch.row_stride == v;
+    return true;
+}
+
 // Warp per page segment.  DIR = KVX_DIR_GATHER copies page -> chunk, KVX_DIR_SCATTER the
 // reverse.
 template <int U, int DIR, int HINT>
@@ -109,45 +158,203 @@ __global__ void __launch_bounds__(1024, U <= 4 ? 2 : 1) kvx_segment_kernel(const
     const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int64_t v = p.token_bytes;
     for (int64_t item = warp; item < p.total_items; item += n_warps) {
-        const int c = find_chunk(p.item_begin, p.n_chunks, item, lane);
-        const DevChunk &ch = p.chunks[c];
-        const int64_t i = item - p.item_begin[c];
-        const int32_t np = ch.np;
-        const int32_t slab = int32_t(i / np);
-        const int32_t j = int32_t(i - int64_t(slab) * np);
-        const int32_t kv = p.kv_factor == 2 ? (slab & 1) : 0;
-        const int32_t layer = ch.la + (p.kv_factor == 2 ? (slab >> 1) : slab);
-        const int32_t lpage = ch.pf + j;
-        const int32_t pt0 = lpage * p.page_size;
-        const int32_t tb = max(ch.t0, pt0);
-        const int32_t te = min(ch.t_end, pt0 + p.page_size);
-        const int32_t page = p.reqs[ch.request].page_table[lpage];
-        if (unsigned(page) >= unsigned(p.num_pages)) {
-            if (lane == 0)
-                atomicOr(p.status, KVX_DEV_PAGE_OUT_OF_RANGE);
+        Segment sg;
+        if (!resolve_segment<DIR>(p, item, lane, sg))
             continue;
-        }
-        char *pg = p.pools[kv * p.num_layers + layer] +
-                   (int64_t(page) * p.page_size + (tb - pt0)) * v;
-        char *ck = ch.ptr + int64_t(ch.slab0 + slab) * ch.slab_stride +
-                   int64_t(tb - ch.t0) * ch.row_stride;
-        const char *src = DIR == KVX_DIR_GATHER ? pg : ck;
-        char *dst = DIR == KVX_DIR_GATHER ? ck : pg;
-        const int rows = te - tb;
-        if (ch.row_stride == v) {
-            copy_contig<U, HINT>(reinterpret_cast<const uint4 *>(src),
-                                 reinterpret_cast<uint4 *>(dst), int((int64_t(rows) * v) >> 4),
-                                 lane);
+        if (sg.contiguous) {
+            copy_contig<U, HINT>(reinterpret_cast<const uint4 *>(sg.src),
+                                 reinterpret_cast<uint4 *>(sg.dst),
+                                 int((int64_t(sg.rows) * v) >> 4), lane);
         } else {
             // Token-major chunk: each token is its own run on the chunk side.
-            const int64_t s_pitch = DIR == KVX_DIR_GATHER ? v : ch.row_stride;
-            const int64_t d_pitch = DIR == KVX_DIR_GATHER ? ch.row_stride : v;
-            for (int r = 0; r < rows; ++r)
-                copy_contig<1, HINT>(reinterpret_cast<const uint4 *>(src + r * s_pitch),
-                                     reinterpret_cast<uint4 *>(dst + r * d_pitch), int(v >> 4),
-                                     lane);
+            for (int r = 0; r < sg.rows; ++r)
+                copy_contig<1, HINT>(reinterpret_cast<const uint4 *>(sg.src + r * sg.s_pitch),
+                                     reinterpret_cast<uint4 *>(sg.dst + r * sg.d_pitch),
+                                     int(v >> 4), lane);
         }
     }
+}
+
+// ------------------------------------------------------------------ bulk-copy (TMA) mapping
+//
+// One warp per CTA streams its items through a ring of shared-memory stages with the
+// Blackwell bulk-copy engine: cp.async.bulk global -> shared completes on an mbarrier
+// (transaction bytes), then cp.async.bulk shared -> global (bulk group) writes the stage
+// out.  Up to n_stages - 1 loads are in flight per CTA without holding them in registers,
+// and the SM's load/store pipes stay free for other work.  Every wait is bounded: past
+// about one second the kernel flags KVX_DEV_WAIT_TIMEOUT, drains what it issued and exits.
+
+constexpr int kBulkMaxStages = 8;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Warp-uniform bounded wait for the completion of phase `parity` of an mbarrier.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int lane)
+{
+    const uint32_t addr = smem_u32(bar);
+    const uint64_t deadline = global_ns() + kWaitLimitNs;
+    while (true) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(addr), "r"(parity)
+                     : "memory");
+        if (__any_sync(0xffffffffu, done))
+            return true;
+        const int late = lane == 0 ? int(global_ns() > deadline) : 0;
+        if (__shfl_sync(0xffffffffu, late, 0))
+            return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                 "[%0], [%1], %2, [%3];" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int DIR>
+__global__ void __launch_bounds__(32) kvx_bulk_kernel(const Plan p, int stage_bytes,
+                                                     int n_stages)
+{
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kBulkMaxStages];
+    __shared__ char *stage_dst[kBulkMaxStages];
+    __shared__ uint32_t stage_len[kBulkMaxStages];
+    const int lane = threadIdx.x;
+    const int64_t v = p.token_bytes;
+    if (lane == 0) {
+        for (int st = 0; st < n_stages; ++st)
+            mbar_init(&full[st], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+
+    // Piece stream: items of this CTA, cut into runs of at most stage_bytes.
+    int64_t item = blockIdx.x;
+    Segment sg;
+    bool have = false;
+    int32_t row = 0, n_rows = 0;
+    int64_t off = 0, row_bytes = 0;
+    auto next = [&](const char *&src, char *&dst, uint32_t &bytes) -> bool {
+        while (true) {
+            if (have) {
+                if (off < row_bytes) {
+                    const int64_t b = min(int64_t(stage_bytes), row_bytes - off);
+                    src = sg.src + row * sg.s_pitch + off;
+                    dst = sg.dst + row * sg.d_pitch + off;
+                    bytes = uint32_t(b);
+                    off += b;
+                    return true;
+                }
+                off = 0;
+                if (++row < n_rows)
+                    continue;
+                have = false;
+            }
+            if (item >= p.total_items)
+                return false;
+            if (resolve_segment<DIR>(p, item, lane, sg)) {
+                have = true;
+                row = 0;
+                off = 0;
+                n_rows = sg.contiguous ? 1 : sg.rows;
+                row_bytes = sg.contiguous ? int64_t(sg.rows) * v : v;
+            }
+            item += gridDim.x;
+        }
+    };
+
+    uint32_t issued = 0, retired = 0;
+    bool more = true, timed_out = false;
+    const char *src = nullptr;
+    char *dst = nullptr;
+    uint32_t bytes = 0;
+    auto issue = [&]() {
+        const uint32_t st = issued % n_stages;
+        if (lane == 0) {
+            stage_dst[st] = dst;
+            stage_len[st] = bytes;
+            mbar_expect_tx(&full[st], bytes);
+            bulk_load(ring + size_t(st) * stage_bytes, src, bytes, &full[st]);
+        }
+        ++issued;
+    };
+    while (issued + 1 < uint32_t(n_stages)) {
+        if (!next(src, dst, bytes)) {
+            more = false;
+            break;
+        }
+        issue();
+    }
+    while (retired < issued) {
+        const uint32_t st = retired % n_stages;
+        if (!mbar_wait(&full[st], (retired / n_stages) & 1u, lane)) {
+            timed_out = true;
+            break;
+        }
+        if (lane == 0)
+            bulk_store(stage_dst[st], ring + size_t(st) * stage_bytes, stage_len[st]);
+        ++retired;
+        if (more) {
+            if (!next(src, dst, bytes)) {
+                more = false;
+            } else {
+                // The stage about to be refilled was last written out by the store issued
+                // one iteration ago: wait until at most the newest store still reads.
+                if (lane == 0)
+                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                __syncwarp();
+                issue();
+            }
+        }
+    }
+    if (timed_out) {
+        if (lane == 0)
+            atomicOr(p.status, KVX_DEV_WAIT_TIMEOUT);
+        for (uint32_t r = retired; r < issued; ++r)  // drain the loads still in flight
+            mbar_wait(&full[r % n_stages], (r / n_stages) & 1u, lane);
+    }
+    if (lane == 0)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
 }
 
 typedef void (*KernelFn)(Plan);
@@ -181,6 +388,9 @@ namespace {
 
 const int kSlots = 4;
 const size_t kDefaultDescriptorBytes = 8u << 20;
+const int kDefaultStageBytes = 32 << 10;
+const int kDefaultStages = 6;
+const int64_t kMaxBulkSmem = 220 << 10;
 
 struct Slot {
     char *host = nullptr;
@@ -253,6 +463,7 @@ struct DeviceGuard {
 void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
 {
     c->mapping = KVX_MAP_WARP_SEGMENT;
+    c->stage_bytes = kDefaultStageBytes;
     switch (op) {
     case KVX_OP_STORE:
         c->sm_cap = 16;
@@ -289,20 +500,35 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
     out->sm_cap = user->sm_cap;  // 0 means every SM
     if (user->ctas_per_sm)
         out->ctas_per_sm = user->ctas_per_sm;
+    out->mapping = user->mapping;
     if (user->threads)
         out->threads = user->threads;
     if (user->unroll)
         out->unroll = user->unroll;
     out->store_hint = user->store_hint;
-    out->mapping = user->mapping;
-    if (out->sm_cap < 0 || out->ctas_per_sm < 1 || out->ctas_per_sm > 32 ||
-        out->threads < 32 || out->threads > 1024 || out->threads % 32 != 0 ||
-        (out->store_hint != KVX_HINT_DEFAULT && out->store_hint != KVX_HINT_STREAMING) ||
-        out->mapping != KVX_MAP_WARP_SEGMENT || !pick_kernel(out->unroll, 0, 0))
+    out->stage_bytes = user->stage_bytes ? user->stage_bytes : kDefaultStageBytes;
+    bool ok = out->sm_cap >= 0 && out->ctas_per_sm >= 1 && out->ctas_per_sm <= 32 &&
+              (out->store_hint == KVX_HINT_DEFAULT || out->store_hint == KVX_HINT_STREAMING);
+    if (out->mapping == KVX_MAP_WARP_SEGMENT) {
+        ok = ok && out->threads >= 32 && out->threads <= 1024 && out->threads % 32 == 0 &&
+             pick_kernel(out->unroll, 0, 0);
+    } else if (out->mapping == KVX_MAP_BULK) {
+        // One warp per CTA; `unroll` counts shared-memory stages.
+        if (!user->unroll)
+            out->unroll = kDefaultStages;
+        out->threads = 32;
+        ok = ok && out->unroll >= 2 && out->unroll <= kBulkMaxStages &&
+             out->stage_bytes >= 16 && out->stage_bytes % 16 == 0 &&
+             int64_t(out->unroll) * out->stage_bytes <= kMaxBulkSmem;
+    } else {
+        ok = false;
+    }
+    if (!ok)
         return set_err(ctx, KVX_ERR_INVALID_ARG,
                        "launch cfg: sm_cap %d ctas_per_sm %d threads %d unroll %d hint %d "
-                       "mapping %d", user->sm_cap, user->ctas_per_sm, user->threads,
-                       user->unroll, user->store_hint, user->mapping);
+                       "mapping %d stage_bytes %d", user->sm_cap, user->ctas_per_sm,
+                       user->threads, user->unroll, user->store_hint, user->mapping,
+                       user->stage_bytes);
     return KVX_OK;
 }
 
@@ -357,10 +583,23 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     const int64_t needed = (plan.total_items + warps_per_cta - 1) / warps_per_cta;
     if (ctas > needed)
         ctas = needed;
-    KernelFn fn = pick_kernel(cfg.unroll, dir, cfg.store_hint);
-    void *args[] = {&plan};
-    e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
-                         dim3(unsigned(cfg.threads)), args, 0, s);
+    if (cfg.mapping == KVX_MAP_BULK) {
+        const void *fn = dir == KVX_DIR_GATHER
+                             ? reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_GATHER>)
+                             : reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_SCATTER>);
+        const size_t smem = size_t(cfg.unroll) * cfg.stage_bytes;
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess)
+            return cuda_err(ctx, e, "bulk kernel shared memory");
+        int stage_bytes = cfg.stage_bytes, stages = cfg.unroll;
+        void *args[] = {&plan, &stage_bytes, &stages};
+        e = cudaLaunchKernel(fn, dim3(unsigned(ctas)), dim3(32u), args, smem, s);
+    } else {
+        KernelFn fn = pick_kernel(cfg.unroll, dir, cfg.store_hint);
+        void *args[] = {&plan};
+        e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
+                             dim3(unsigned(cfg.threads)), args, 0, s);
+    }
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
     e = cudaEventRecord(slot.done, s);
@@ -678,6 +917,8 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
     kvx_status st = resolve_cfg(nullptr, KVX_OP_LOAD, cfg, &c);
     if (st != KVX_OK)
         return st;
+    if (c.mapping != KVX_MAP_WARP_SEGMENT)
+        return KVX_ERR_INVALID_ARG;
     st = kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, KVX_OP_LOAD,
                        1, false, nullptr, 0);
     if (st != KVX_OK)

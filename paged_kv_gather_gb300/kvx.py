@@ -39,6 +39,7 @@ KVX_ERR_DEVICE_STATUS = 7
 KVX_ERR_CAPACITY = 8
 
 KVX_DEV_PAGE_OUT_OF_RANGE = 0x1
+KVX_DEV_WAIT_TIMEOUT = 0x2
 
 KVX_CHUNK_LAYER_MAJOR = 0
 KVX_CHUNK_TOKEN_MAJOR = 1
@@ -47,6 +48,7 @@ KVX_DIR_GATHER = 0
 KVX_DIR_SCATTER = 1
 
 KVX_MAP_WARP_SEGMENT = 0
+KVX_MAP_BULK = 1
 
 KVX_HINT_DEFAULT = 0
 KVX_HINT_STREAMING = 1
@@ -82,7 +84,8 @@ class kvx_chunk(ctypes.Structure):
 class kvx_launch_cfg(ctypes.Structure):
     _fields_ = [("sm_cap", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("unroll", ctypes.c_int32),
-                ("store_hint", ctypes.c_int32), ("mapping", ctypes.c_int32)]
+                ("store_hint", ctypes.c_int32), ("mapping", ctypes.c_int32),
+                ("stage_bytes", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

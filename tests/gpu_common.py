@@ -138,15 +138,21 @@ def assert_bytes_equal(got: np.ndarray, exp: np.ndarray, what: str):
                              f"(got {got[bad[0]]}, want {exp[bad[0]]})")
 
 
-def cfg(sm_cap=None, ctas_per_sm=0, threads=0, unroll=0, hint=0):
+def cfg(sm_cap=None, ctas_per_sm=0, threads=0, unroll=0, hint=0, mapping=0, stage_bytes=0):
     c = kvx.kvx_launch_cfg()
     c.sm_cap = 0 if sm_cap is None else sm_cap
     c.ctas_per_sm = ctas_per_sm
     c.threads = threads
     c.unroll = unroll
     c.store_hint = hint
-    c.mapping = kvx.KVX_MAP_WARP_SEGMENT
+    c.mapping = mapping
+    c.stage_bytes = stage_bytes
     return c
+
+
+def bulk(sm_cap=None, ctas_per_sm=0, stages=0, stage_bytes=0):
+    """Launch configuration of the bulk-copy (shared-memory stage) mapping."""
+    return cfg(sm_cap, ctas_per_sm, 0, stages, 0, kvx.KVX_MAP_BULK, stage_bytes)
 
 
 def random_case(rng: np.random.Generator, max_tokens=700):

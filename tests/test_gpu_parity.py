@@ -20,7 +20,7 @@ import oracle  # noqa: E402
 from paged_kv_gather_gb300 import kvx  # noqa: E402
 from paged_kv_gather_gb300 import workloads as wl  # noqa: E402
 from tests.gpu_common import (CANARY, Arena, DevicePool, Requests, assert_bytes_equal,  # noqa: E402
-                              assert_pool_equal, cfg, expected_load, expected_store,
+                              assert_pool_equal, bulk, cfg, expected_load, expected_store,
                               oracle_chunks, random_case)
 
 
@@ -101,10 +101,11 @@ def test_tiny_workload_round_trip(ctx, stream, op_store, op_load, where):
 # ----------------------------------------------------------------------------- random batches
 
 CONFIGS = [cfg(), cfg(1, 1, 32, 1, 0), cfg(2, 1, 64, 2, 1), cfg(3, 2, 256, 4, 0),
-           cfg(0, 1, 1024, 8, 1), cfg(1, 1, 1024, 8, 0), cfg(5, 3, 96, 4, 1)]
+           cfg(0, 1, 1024, 8, 1), cfg(1, 1, 1024, 8, 0), cfg(5, 3, 96, 4, 1),
+           bulk(), bulk(2, 1, 2, 64), bulk(3, 2, 3, 4096), bulk(0, 1, 8, 1040)]
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(33))
 def test_random_batches_all_paths(ctx, stream, seed):
     rng = np.random.default_rng(5000 + seed)
     shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
@@ -163,6 +164,54 @@ def test_every_kernel_variant(ctx, stream, unroll, hint):
     pre = dpool.host_copy()
     _load(ctx, "load", dpool, dst, specs, arena, 0, None, c, stream)
     assert_pool_equal(dpool, expected_load(pre, dst, specs, arena.numpy().copy()))
+    arena.close()
+
+
+@pytest.mark.parametrize("stages,stage_bytes,ctas", [(2, 16, 1), (3, 1040, 2), (6, 32768, 1),
+                                                    (8, 27648, 1), (3, 65536, 1)])
+def test_bulk_mapping_multi_tile_ragged(ctx, stream, stages, stage_bytes, ctas):
+    """The bulk-copy mapping on every direction: segments longer and shorter than a stage,
+    chunk cuts inside pages, both layouts, host and device chunks."""
+    rng = np.random.default_rng(900 + stages)
+    L, KV, P, v = 3, 2, 16, 1152
+    lens = [700, 129, 16]
+    pages = [-(-n // P) for n in lens]
+    NP = 2 * sum(pages) + 3
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(perm[at:at + npg])
+        t_dst.append(perm[at + sum(pages):at + sum(pages) + npg])
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, 77, 0, L, r % 2)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    c = bulk(5, ctas, stages, stage_bytes)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    for op_s, op_l, where in (("store", "load", "host"), ("gather", "scatter", "device")):
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        dpool.fill_random(stages * 7 + ctas)
+        arena = Arena(nbytes, where)
+        _store(ctx, op_s, dpool, src, specs, arena, 0, None, c, stream)
+        assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), op_s)
+        pre = dpool.host_copy()
+        _load(ctx, op_l, dpool, dst, specs, arena, 0, None, c, stream)
+        assert_pool_equal(dpool, expected_load(pre, dst, specs, arena.numpy().copy()))
+        arena.close()
+
+
+def test_bulk_mapping_rejects_bad_stage_shapes(ctx, stream):
+    dpool = DevicePool.empty(1, 1, 4, 1, 16)
+    reqs = Requests([np.array([0], np.int32)], [1])
+    arena = Arena(16, "host")
+    ch = kvx.chunks_array([wl.ChunkSpec(0, 0, 1, 0, 1, 0, 0)], arena.ptr)
+    for bad in (bulk(stages=1), bulk(stages=9), bulk(stage_bytes=24), bulk(stages=8, stage_bytes=65536)):
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, ch, 0, 1, bad, stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_INVALID_ARG
     arena.close()
 
 
