@@ -59,7 +59,7 @@ def parse():
     p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--workload", default="llama8b",
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
-                            "transform_sweep", "profile_small"],
+                            "transform_sweep", "profile_small", "batch_sweep"],
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
@@ -917,11 +917,11 @@ def run_transform_sweep(args, kvx, wl):
     sh = stream.cuda_stream
     N = w.store_bytes()
     hbm, _ = peaks()
-    shapes = [(0, 1, 512, 8, 1, 0), (0, 1, 512, 8, 0, 0), (0, 1, 1024, 8, 1, 0),
-              (0, 2, 512, 8, 1, 0), (0, 1, 256, 8, 1, 0), (0, 2, 256, 8, 1, 0),
-              (0, 1, 384, 8, 1, 0), (0, 2, 1024, 4, 1, 0),
-              (1, 1, 32, 6, 0, 32768), (1, 2, 32, 3, 0, 32768), (1, 1, 32, 4, 0, 49152),
-              (1, 3, 32, 2, 0, 32768), (1, 2, 32, 6, 0, 16384), (1, 4, 32, 3, 0, 16384)]
+    shapes = [(0, 1, 512, 8, 1, 0), (0, 2, 256, 8, 1, 0), (0, 1, 384, 8, 1, 0),
+              (0, 3, 256, 8, 1, 0), (0, 4, 128, 8, 1, 0), (0, 3, 128, 8, 1, 0),
+              (0, 2, 384, 8, 1, 0), (0, 6, 64, 8, 1, 0), (0, 2, 256, 8, 0, 0),
+              (0, 4, 256, 4, 1, 0), (0, 2, 192, 8, 1, 0),
+              (1, 3, 32, 2, 0, 32768), (1, 2, 32, 3, 0, 32768)] * 2
     for mapping, ctas, threads, unroll, hint, stage in shapes:
         if True:
             row = {"workload": "llama8b_transform_sweep",
@@ -939,6 +939,41 @@ def run_transform_sweep(args, kvx, wl):
                 row[f"{name}_gbs_2n"] = round(gbs, 1)
                 row[f"{name}_frac"] = round(gbs / hbm, 4)
             _emit(row)
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    kvx.kvx_destroy(ctx)
+
+
+def run_batch_sweep(args, kvx, wl):
+    """Segments resolved per warp at once, on the MLA latent shape with short segments."""
+    ctx = kvx.kvx_create(0, 64 << 20)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    for P in (1, 8):
+        w = wl.mla_sweep(P, 1 << 20)
+        s = w.shape
+        pools = _pool_tensor(s, w.seed, wl)
+        pool = kvx.Pool.from_tensor(pools, s.page_size)
+        src, dst = w.store_requests[0], w.load_requests[0]
+        ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+        rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+        rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+        arena = kvx.HostBuffer(w.store_arena_bytes)
+        arena.array[:] = 0
+        ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+        N = w.store_bytes()
+        for batch in (0, 1, 2, 4, 8, 16, 28, 32):
+            for cap in (16, 32):
+                row = {"workload": "mla_batch_sweep", "page_size": P, "batch": batch,
+                       "sm_cap": cap}
+                for name, op, fn, rq in (("store", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs),
+                                         ("load", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd)):
+                    c = kvx.kvx_default_launch_cfg(ctx, op)
+                    c.batch, c.sm_cap = batch, cap
+                    ms = _timed(stream, lambda: fn(ctx, pool, rq, ch, 0, s.num_layers, c, sh), 5)
+                    row[f"{name}_gbs"] = round(N / (ms * 1e-3) / GB, 2)
+                _emit(row)
+        arena.close()
+        del pools
     assert kvx.kvx_get_status(ctx, sh) == 0
     kvx.kvx_destroy(ctx)
 
@@ -989,7 +1024,7 @@ def run_workload(args):
     from paged_kv_gather_gb300 import workloads as wl
     {"llama70b": run_llama70b, "qwen7b_batch": run_qwen7b, "mla_sweep": run_mla_sweep,
      "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
-     "profile_small": run_profile_small}[args.workload](
+     "profile_small": run_profile_small, "batch_sweep": run_batch_sweep}[args.workload](
         args, kvx, wl)
 
 

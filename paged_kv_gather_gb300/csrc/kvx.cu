@@ -110,15 +110,29 @@ struct Segment {
     bool contiguous;  // rows back to back on both sides: one run of rows * token_bytes
 };
 
-// Resolve item -> segment (warp-collective: every lane of the warp calls it with the same
-// item).  Returns false, after flagging the device status, if the page id is outside the
-// pool; the segment is then skipped.
+// Chunk owning `item` for one lane alone (plain binary search): used when every lane
+// resolves a different item.
+__device__ __forceinline__ int find_chunk_lane(const int64_t *__restrict__ begin, int n,
+                                               int64_t item)
+{
+    int lo = 0, hi = n;  // begin[lo] <= item < begin[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(begin + mid) <= item)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Addresses of item `item` of chunk `c`.  Returns false, after flagging the device status
+// when `flag` is set, if the page id is outside the pool; the segment is then skipped.
 template <int DIR>
-__device__ __forceinline__ bool resolve_segment(const Plan &p, int64_t item, int lane,
-                                                Segment &sg)
+__device__ __forceinline__ bool segment_of(const Plan &p, int c, int64_t item, bool flag,
+                                           Segment &sg)
 {
     const int64_t v = p.token_bytes;
-    const int c = find_chunk(p.item_begin, p.n_chunks, item, lane);
     const DevChunk &ch = p.chunks[c];
     const int64_t i = item - p.item_begin[c];
     const int32_t np = ch.np;
@@ -132,7 +146,7 @@ __device__ __forceinline__ bool resolve_segment(const Plan &p, int64_t item, int
     const int32_t te = min(ch.t_end, pt0 + p.page_size);
     const int32_t page = p.reqs[ch.request].page_table[lpage];
     if (unsigned(page) >= unsigned(p.num_pages)) {
-        if (lane == 0)
+        if (flag)
             atomicOr(p.status, KVX_DEV_PAGE_OUT_OF_RANGE);
         return false;
     }
@@ -148,29 +162,84 @@ __device__ __forceinline__ bool resolve_segment(const Plan &p, int64_t item, int
     return true;
 }
 
+// Resolve item -> segment (warp-collective: every lane of the warp calls it with the same
+// item).
+template <int DIR>
+__device__ __forceinline__ bool resolve_segment(const Plan &p, int64_t item, int lane,
+                                                Segment &sg)
+{
+    const int c = find_chunk(p.item_begin, p.n_chunks, item, lane);
+    return segment_of<DIR>(p, c, item, lane == 0, sg);
+}
+
+__device__ __forceinline__ Segment shfl_segment(const Segment &s, int src_lane)
+{
+    Segment r;
+    r.src = reinterpret_cast<const char *>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(s.src), src_lane));
+    r.dst = reinterpret_cast<char *>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(s.dst), src_lane));
+    r.s_pitch = __shfl_sync(0xffffffffu, s.s_pitch, src_lane);
+    r.d_pitch = __shfl_sync(0xffffffffu, s.d_pitch, src_lane);
+    r.rows = __shfl_sync(0xffffffffu, s.rows, src_lane);
+    r.contiguous = __shfl_sync(0xffffffffu, int(s.contiguous), src_lane) != 0;
+    return r;
+}
+
+template <int U, int HINT>
+__device__ __forceinline__ void copy_segment(const Segment &sg, int64_t v, int lane)
+{
+    if (sg.contiguous) {
+        copy_contig<U, HINT>(reinterpret_cast<const uint4 *>(sg.src),
+                             reinterpret_cast<uint4 *>(sg.dst), int((int64_t(sg.rows) * v) >> 4),
+                             lane);
+    } else {
+        // Token-major chunk: each token is its own run on the chunk side.
+        for (int r = 0; r < sg.rows; ++r)
+            copy_contig<1, HINT>(reinterpret_cast<const uint4 *>(sg.src + r * sg.s_pitch),
+                                 reinterpret_cast<uint4 *>(sg.dst + r * sg.d_pitch),
+                                 int(v >> 4), lane);
+    }
+}
+
 // Warp per page segment.  DIR = KVX_DIR_GATHER copies page -> chunk, KVX_DIR_SCATTER the
-// reverse.
-template <int U, int DIR, int HINT>
-__global__ void __launch_bounds__(1024, U <= 4 ? 2 : 1) kvx_segment_kernel(const Plan p)
+// reverse.  BATCHED = false: a warp resolves one segment at a time (32-way search), for
+// page segments of 16 KiB and more.  BATCHED = true (short segments): each lane resolves
+// one of p.batch consecutive segments in parallel and the warp then copies them back to
+// back, so the lookup latency of short segments overlaps instead of adding up.
+template <int U, int DIR, int HINT, bool BATCHED>
+__global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int64_t v = p.token_bytes;
-    for (int64_t item = warp; item < p.total_items; item += n_warps) {
-        Segment sg;
-        if (!resolve_segment<DIR>(p, item, lane, sg))
-            continue;
-        if (sg.contiguous) {
-            copy_contig<U, HINT>(reinterpret_cast<const uint4 *>(sg.src),
-                                 reinterpret_cast<uint4 *>(sg.dst),
-                                 int((int64_t(sg.rows) * v) >> 4), lane);
-        } else {
-            // Token-major chunk: each token is its own run on the chunk side.
-            for (int r = 0; r < sg.rows; ++r)
-                copy_contig<1, HINT>(reinterpret_cast<const uint4 *>(sg.src + r * sg.s_pitch),
-                                     reinterpret_cast<uint4 *>(sg.dst + r * sg.d_pitch),
-                                     int(v >> 4), lane);
+    if (!BATCHED) {
+        for (int64_t item = warp; item < p.total_items; item += n_warps) {
+            Segment sg;
+            if (resolve_segment<DIR>(p, item, lane, sg))
+                copy_segment<U, HINT>(sg, v, lane);
+        }
+    } else {
+        const int B = p.batch;
+        for (int64_t base = warp * B; base < p.total_items; base += n_warps * B) {
+            const int64_t mine = base + lane;
+            Segment sg;
+            sg.src = nullptr;
+            sg.dst = nullptr;
+            sg.s_pitch = sg.d_pitch = 0;
+            sg.rows = 0;
+            sg.contiguous = true;
+            bool ok = false;
+            if (lane < B && mine < p.total_items)
+                ok = segment_of<DIR>(p, find_chunk_lane(p.item_begin, p.n_chunks, mine), mine,
+                                     true, sg);
+            const unsigned valid = __ballot_sync(0xffffffffu, ok);
+            for (int k = 0; k < B; ++k) {
+                const Segment s = shfl_segment(sg, k);
+                if (valid & (1u << k))
+                    copy_segment<U, HINT>(s, v, lane);
+            }
         }
     }
 }
@@ -359,25 +428,34 @@ __global__ void __launch_bounds__(32) kvx_bulk_kernel(const Plan p, int stage_by
 
 typedef void (*KernelFn)(Plan);
 
-template <int U>
+template <int U, bool BATCHED>
 KernelFn pick_hint_dir(int dir, int hint)
 {
     if (dir == KVX_DIR_GATHER)
-        return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_GATHER, 1>
-                                          : kvx_segment_kernel<U, KVX_DIR_GATHER, 0>;
-    return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_SCATTER, 1>
-                                      : kvx_segment_kernel<U, KVX_DIR_SCATTER, 0>;
+        return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_GATHER, 1, BATCHED>
+                                          : kvx_segment_kernel<U, KVX_DIR_GATHER, 0, BATCHED>;
+    return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_SCATTER, 1, BATCHED>
+                                      : kvx_segment_kernel<U, KVX_DIR_SCATTER, 0, BATCHED>;
 }
 
-KernelFn pick_kernel(int unroll, int dir, int hint)
+template <bool BATCHED>
+KernelFn pick_unroll(int unroll, int dir, int hint)
 {
     switch (unroll) {
-    case 1: return pick_hint_dir<1>(dir, hint);
-    case 2: return pick_hint_dir<2>(dir, hint);
-    case 4: return pick_hint_dir<4>(dir, hint);
-    case 8: return pick_hint_dir<8>(dir, hint);
+    case 1: return pick_hint_dir<1, BATCHED>(dir, hint);
+    case 2: return pick_hint_dir<2, BATCHED>(dir, hint);
+    case 4: return pick_hint_dir<4, BATCHED>(dir, hint);
+    case 8: return pick_hint_dir<8, BATCHED>(dir, hint);
     }
     return nullptr;
+}
+
+// The warp-segment kernel for (unroll, direction, hint), batched when more than one
+// segment is resolved per warp at once.
+KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1)
+{
+    return batch > 1 ? pick_unroll<true>(unroll, dir, hint)
+                     : pick_unroll<false>(unroll, dir, hint);
 }
 
 }  // namespace
@@ -464,6 +542,7 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
 {
     c->mapping = KVX_MAP_WARP_SEGMENT;
     c->stage_bytes = kDefaultStageBytes;
+    c->batch = 0;
     switch (op) {
     case KVX_OP_STORE:
         c->sm_cap = 16;
@@ -479,10 +558,10 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
         c->unroll = 8;
         c->store_hint = KVX_HINT_STREAMING;
         break;
-    default:  // HBM transform: the whole GPU, one 512-thread CTA per SM, 8 loads in flight
+    default:  // HBM transform: the whole GPU, two 256-thread CTAs per SM, 8 loads in flight
         c->sm_cap = 0;
-        c->ctas_per_sm = 1;
-        c->threads = 512;
+        c->ctas_per_sm = 2;
+        c->threads = 256;
         c->unroll = 8;
         c->store_hint = KVX_HINT_STREAMING;
         break;
@@ -507,7 +586,9 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
         out->unroll = user->unroll;
     out->store_hint = user->store_hint;
     out->stage_bytes = user->stage_bytes ? user->stage_bytes : kDefaultStageBytes;
+    out->batch = user->batch;
     bool ok = out->sm_cap >= 0 && out->ctas_per_sm >= 1 && out->ctas_per_sm <= 32 &&
+              out->batch >= 0 && out->batch <= 32 &&
               (out->store_hint == KVX_HINT_DEFAULT || out->store_hint == KVX_HINT_STREAMING);
     if (out->mapping == KVX_MAP_WARP_SEGMENT) {
         ok = ok && out->threads >= 32 && out->threads <= 1024 && out->threads % 32 == 0 &&
@@ -526,9 +607,9 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
     if (!ok)
         return set_err(ctx, KVX_ERR_INVALID_ARG,
                        "launch cfg: sm_cap %d ctas_per_sm %d threads %d unroll %d hint %d "
-                       "mapping %d stage_bytes %d", user->sm_cap, user->ctas_per_sm,
+                       "mapping %d stage_bytes %d batch %d", user->sm_cap, user->ctas_per_sm,
                        user->threads, user->unroll, user->store_hint, user->mapping,
-                       user->stage_bytes);
+                       user->stage_bytes, user->batch);
     return KVX_OK;
 }
 
@@ -570,6 +651,8 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     Plan plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
                           slot.host, slot.dev);
     plan.status = ctx->status_dev;
+    if (cfg.batch > 0)
+        plan.batch = cfg.batch;
     if (plan.total_items == 0)
         return KVX_OK;
 
@@ -580,7 +663,8 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     const int64_t warps_per_cta = cfg.threads / 32;
     const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
     int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
-    const int64_t needed = (plan.total_items + warps_per_cta - 1) / warps_per_cta;
+    const int64_t per_cta = warps_per_cta * (cfg.mapping == KVX_MAP_BULK ? 1 : plan.batch);
+    const int64_t needed = (plan.total_items + per_cta - 1) / per_cta;
     if (ctas > needed)
         ctas = needed;
     if (cfg.mapping == KVX_MAP_BULK) {
@@ -595,7 +679,7 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
         void *args[] = {&plan, &stage_bytes, &stages};
         e = cudaLaunchKernel(fn, dim3(unsigned(ctas)), dim3(32u), args, smem, s);
     } else {
-        KernelFn fn = pick_kernel(cfg.unroll, dir, cfg.store_hint);
+        KernelFn fn = pick_kernel(cfg.unroll, dir, cfg.store_hint, plan.batch);
         void *args[] = {&plan};
         e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
                              dim3(unsigned(cfg.threads)), args, 0, s);
@@ -968,7 +1052,7 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
         ctas = needed;
     void *args[] = {&plan};
     if (cudaLaunchKernel(reinterpret_cast<const void *>(pick_kernel(c.unroll, KVX_DIR_SCATTER,
-                                                                    c.store_hint)),
+                                                                    c.store_hint, plan.batch)),
                          dim3(unsigned(ctas)), dim3(unsigned(c.threads)), args, 0, s) !=
         cudaSuccess)
         return KVX_ERR_CUDA;

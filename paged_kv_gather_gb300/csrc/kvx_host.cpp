@@ -302,6 +302,8 @@ Plan pack(const kvx_pool *pool, const kvx_request *reqs, int n_req, const kvx_ch
     p.num_pages = pool->num_pages;
     p.num_layers = pool->num_layers;
     p.dir = dir;
+    p.batch = default_batch(P, v);
+    p.pad = 0;
     return p;
 }
 

@@ -54,7 +54,20 @@ struct Plan {
     int32_t num_pages;
     int32_t num_layers;
     int32_t dir;                // KVX_DIR_GATHER (pages -> chunks) or KVX_DIR_SCATTER
+    int32_t batch;              // segments a warp resolves at once (1..32)
+    int32_t pad;
 };
+
+// Segments a warp resolves in parallel by default: enough short segments to put ~32 KiB
+// in flight per warp (one segment when page segments are >= 16 KiB).
+inline int32_t default_batch(int64_t page_size, int64_t token_bytes)
+{
+    int64_t seg = page_size * token_bytes;
+    int64_t b = seg > 0 ? (32768 + seg - 1) / seg : 1;
+    if (seg >= 16384)
+        b = 1;
+    return int32_t(b < 1 ? 1 : (b > 32 ? 32 : b));
+}
 
 // Byte layout of one packed descriptor block (host staging == device copy).
 struct PackedLayout {

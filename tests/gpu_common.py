@@ -138,8 +138,10 @@ def assert_bytes_equal(got: np.ndarray, exp: np.ndarray, what: str):
                              f"(got {got[bad[0]]}, want {exp[bad[0]]})")
 
 
-def cfg(sm_cap=None, ctas_per_sm=0, threads=0, unroll=0, hint=0, mapping=0, stage_bytes=0):
+def cfg(sm_cap=None, ctas_per_sm=0, threads=0, unroll=0, hint=0, mapping=0, stage_bytes=0,
+        batch=0):
     c = kvx.kvx_launch_cfg()
+    c.batch = batch
     c.sm_cap = 0 if sm_cap is None else sm_cap
     c.ctas_per_sm = ctas_per_sm
     c.threads = threads

@@ -102,10 +102,11 @@ def test_tiny_workload_round_trip(ctx, stream, op_store, op_load, where):
 
 CONFIGS = [cfg(), cfg(1, 1, 32, 1, 0), cfg(2, 1, 64, 2, 1), cfg(3, 2, 256, 4, 0),
            cfg(0, 1, 1024, 8, 1), cfg(1, 1, 1024, 8, 0), cfg(5, 3, 96, 4, 1),
-           bulk(), bulk(2, 1, 2, 64), bulk(3, 2, 3, 4096), bulk(0, 1, 8, 1040)]
+           bulk(), bulk(2, 1, 2, 64), bulk(3, 2, 3, 4096), bulk(0, 1, 8, 1040),
+           cfg(3, 1, 256, 8, 0, batch=32), cfg(2, 2, 128, 2, 1, batch=5), cfg(0, 1, 64, 4, 0, batch=2)]
 
 
-@pytest.mark.parametrize("seed", range(33))
+@pytest.mark.parametrize("seed", range(42))
 def test_random_batches_all_paths(ctx, stream, seed):
     rng = np.random.default_rng(5000 + seed)
     shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
@@ -135,8 +136,10 @@ def test_random_batches_all_paths(ctx, stream, seed):
 
 @pytest.mark.parametrize("unroll", [1, 2, 4, 8])
 @pytest.mark.parametrize("hint", [0, 1])
-def test_every_kernel_variant(ctx, stream, unroll, hint):
-    """Every (unroll, hint, direction) instantiation on a multi-tile ragged batch."""
+@pytest.mark.parametrize("batch", [1, 7, 32])
+def test_every_kernel_variant(ctx, stream, unroll, hint, batch):
+    """Every (unroll, hint, direction) instantiation, one and several segments resolved per
+    warp, on a multi-tile ragged batch."""
     rng = np.random.default_rng(77 + unroll * 10 + hint)
     L, KV, P, v = 3, 2, 16, 2048
     lens = [1000, 333, 17]
@@ -154,10 +157,10 @@ def test_every_kernel_variant(ctx, stream, unroll, hint):
     shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
     wl.place_chunks(specs, shape)
     nbytes = wl._arena_bytes(specs, shape)
-    c = cfg(4, 1, 256, unroll, hint)
+    c = cfg(4, 1, 256, unroll, hint, batch=batch)
     src, dst = Requests(t_src, lens), Requests(t_dst, lens)
     dpool = DevicePool.empty(L, KV, NP, P, v)
-    dpool.fill_random(unroll + 10 * hint)
+    dpool.fill_random(unroll + 10 * hint + 100 * batch)
     arena = Arena(nbytes, "host")
     _store(ctx, "store", dpool, src, specs, arena, 0, None, c, stream)
     assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), "store")
@@ -208,7 +211,8 @@ def test_bulk_mapping_rejects_bad_stage_shapes(ctx, stream):
     reqs = Requests([np.array([0], np.int32)], [1])
     arena = Arena(16, "host")
     ch = kvx.chunks_array([wl.ChunkSpec(0, 0, 1, 0, 1, 0, 0)], arena.ptr)
-    for bad in (bulk(stages=1), bulk(stages=9), bulk(stage_bytes=24), bulk(stages=8, stage_bytes=65536)):
+    for bad in (bulk(stages=1), bulk(stages=9), bulk(stage_bytes=24), bulk(stages=8, stage_bytes=65536),
+                cfg(batch=33), cfg(batch=-1)):
         with pytest.raises(kvx.KvxError) as e:
             kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, ch, 0, 1, bad, stream.cuda_stream)
         assert e.value.status == kvx.KVX_ERR_INVALID_ARG
