@@ -59,7 +59,7 @@ def parse():
     p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--workload", default="llama8b",
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
-                            "transform_sweep", "profile_small", "batch_sweep"],
+                            "transform_sweep", "profile_small", "batch_sweep", "mla_blocks"],
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
@@ -978,6 +978,53 @@ def run_batch_sweep(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
+def run_mla_blocks(args, kvx, wl):
+    """Per-block object layout (STRIPED chunks, one per page, 61 layer objects each,
+    4096-aligned): one store of all layers, 61 per-layer loads, and the per-object DMA
+    baseline."""
+    ctx = kvx.kvx_create(0, 64 << 20)
+    stream = torch.cuda.Stream(priority=-1)
+    sh = stream.cuda_stream
+    for P in (16, 32, 64):
+        w = wl.mla_blocks(P)
+        s = w.shape
+        pools = _pool_tensor(s, w.seed, wl)
+        pool = kvx.Pool.from_tensor(pools, s.page_size)
+        src, dst = w.store_requests[0], w.load_requests[0]
+        ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+        rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+        rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+        arena = kvx.HostBuffer(w.store_arena_bytes)
+        arena.array[:] = 0
+        ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+        N = 16384 * s.num_layers * s.token_bytes
+        st_ms = _timed(stream, lambda: kvx.kvx_store_chunks(ctx, pool, rs, ch, stream=sh), 5)
+
+        def per_layer():
+            for l in range(s.num_layers):
+                kvx.kvx_load_chunks(ctx, pool, rd, ch, l, l + 1, stream=sh)
+
+        ld_ms = _timed(stream, per_layer, 5)
+        kvx.kvx_dma_baseline(ctx, kvx.KVX_DIR_GATHER, pool, rs, ch, stream=sh)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        n = kvx.kvx_dma_baseline(ctx, kvx.KVX_DIR_GATHER, pool, rs, ch, stream=sh)
+        stream.synchronize()
+        dma_s = time.perf_counter() - t0
+        assert kvx.kvx_get_status(ctx, sh) == 0
+        _emit({"workload": "mla_block_objects", "page_size": P, "blocks": len(w.store_chunks),
+               "object_bytes": P * s.token_bytes,
+               "object_stride": -(-P * s.token_bytes // 4096) * 4096,
+               "payload_bytes": N, "arena_bytes": w.store_arena_bytes,
+               "store_gbs": round(N / (st_ms * 1e-3) / GB, 2),
+               "per_layer_load_gbs": round(N / (ld_ms * 1e-3) / GB, 2),
+               "per_layer_load_ms": round(ld_ms / s.num_layers, 4),
+               "dma_store_gbs": round(N / dma_s / GB, 2), "dma_copies": n})
+        arena.close()
+        del pools
+    kvx.kvx_destroy(ctx)
+
+
 def run_profile_small(args, kvx, wl):
     """A small case for ncu captures: the Llama-3.1-8B shape cut to 8192 tokens (1 GiB per
     direction, above the 129 MB L2) in a 1024-page pool (2 GiB), one operation 3 times
@@ -1024,7 +1071,8 @@ def run_workload(args):
     from paged_kv_gather_gb300 import workloads as wl
     {"llama70b": run_llama70b, "qwen7b_batch": run_qwen7b, "mla_sweep": run_mla_sweep,
      "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
-     "profile_small": run_profile_small, "batch_sweep": run_batch_sweep}[args.workload](
+     "profile_small": run_profile_small, "batch_sweep": run_batch_sweep,
+     "mla_blocks": run_mla_blocks}[args.workload](
         args, kvx, wl)
 
 

@@ -27,6 +27,8 @@
  *     KVX_CHUNK_LAYER_MAJOR  [layer][kv][token][token_bytes]  (page-first, generalised to
  *                            a multi-page chunk)
  *     KVX_CHUNK_TOKEN_MAJOR  [token][layer][kv][token_bytes]
+ *     KVX_CHUNK_STRIPED      [layer][kv] objects of [token][token_bytes], each starting at
+ *                            a multiple of KVX_STRIPE_ALIGN from the chunk start
  *   A call moves only layers inside its window [layer_begin, layer_end) (half-open),
  *   intersected with each chunk's own layers; chunk offsets stay relative to the chunk's
  *   own layer_begin.
@@ -78,8 +80,17 @@ typedef enum kvx_status {
 
 typedef enum kvx_chunk_layout {
     KVX_CHUNK_LAYER_MAJOR = 0,
-    KVX_CHUNK_TOKEN_MAJOR = 1
+    KVX_CHUNK_TOKEN_MAJOR = 1,
+    KVX_CHUNK_STRIPED = 2
 } kvx_chunk_layout;
+
+/* KVX_CHUNK_STRIPED: one object per (layer, kv), in [layer][kv] order, each holding the
+ * chunk's tokens of that layer and kv back to back and each starting at a multiple of
+ * KVX_STRIPE_ALIGN bytes from the chunk start (stride = object bytes rounded up to
+ * KVX_STRIPE_ALIGN; the padding is never read or written).  A one-page chunk is the
+ * per-block "GPU file" of 2L objects of "Tutti: Making SSD-Backed KV Cache Practical",
+ * section 2 Design 1 and Figure 4, laid out for block-aligned (direct) storage I/O. */
+#define KVX_STRIPE_ALIGN 4096
 
 /* Direction of kvx_transform_hbm and kvx_dma_baseline. */
 #define KVX_DIR_GATHER 0   /* pages -> chunks (a store) */
@@ -115,7 +126,8 @@ typedef struct kvx_chunk {
     int32_t n_layers;     /* layers held, layer_begin + n_layers <= num_layers */
     int32_t layout;       /* kvx_chunk_layout */
     void *ptr;            /* chunk memory, 16-byte aligned, n_layers x kv_factor x n_tokens
-                             x token_bytes bytes: mapped pinned host memory for
+                             x token_bytes bytes (STRIPED: n_layers x kv_factor x the
+                             padded object stride): mapped pinned host memory for
                              store/load, device memory for kvx_transform_hbm */
 } kvx_chunk;
 

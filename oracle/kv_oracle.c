@@ -19,11 +19,18 @@
  *
  *   Chunks.  Host/storage memory keeps a transfer-friendly page-first layout [P, L, H, D]
  *   (same section, item 2): a chunk holds a run of tokens [t0, t0+n) of one request for a
- *   run of layers [l0, l0+nl).  Two orders are defined:
+ *   run of layers [l0, l0+nl).  Three layouts are defined:
  *     LAYER_MAJOR (0): [layer][kv][token][token_bytes]   -- page-first generalised to a
  *                      multi-page chunk; with one page per chunk and K/V folded it is the
  *                      page's host layout.
  *     TOKEN_MAJOR (1): [token][layer][kv][token_bytes]
+ *     STRIPED     (2): one object per (layer, kv) in [layer][kv] order, each holding the
+ *                      chunk's tokens of that layer and kv back to back, and each starting
+ *                      at a multiple of 4096 bytes from the chunk start (the object's
+ *                      length rounded up to 4096 is the stride).  This is the per-block
+ *                      object layout of "Tutti: Making SSD-Backed KV Cache Practical",
+ *                      section 2 Design 1 and Figure 4 (2L objects per KV block, stored
+ *                      aligned to the block granularity of the NVMe file).
  *
  *   store: every token vector of every covered (layer, kv, token) is copied from its page
  *          slot into its chunk position.
@@ -40,6 +47,8 @@
 
 #define ORA_LAYER_MAJOR 0
 #define ORA_TOKEN_MAJOR 1
+#define ORA_STRIPED 2
+#define ORA_STRIPE_ALIGN 4096
 
 #define ORA_OK 0
 #define ORA_EBADARG (-1)
@@ -90,6 +99,11 @@ static unsigned char *chunk_slot(const ora_pool *pool, const ora_chunk *c,
     int64_t lr = layer - c->layer_begin;
     int64_t tr = t - c->token_begin;
     int64_t index;
+    if (c->layout == ORA_STRIPED) {
+        int64_t object_bytes = (int64_t)c->n_tokens * v;
+        int64_t stride = (object_bytes + ORA_STRIPE_ALIGN - 1) / ORA_STRIPE_ALIGN * ORA_STRIPE_ALIGN;
+        return c->ptr + (lr * KV + kv) * stride + tr * v;
+    }
     if (c->layout == ORA_LAYER_MAJOR)
         index = (lr * KV + kv) * c->n_tokens + tr;
     else
@@ -111,7 +125,8 @@ static int check(const ora_pool *pool, const ora_request *reqs, int n_req,
     for (int i = 0; i < n_chunks; ++i) {
         const ora_chunk *c = &chunks[i];
         if (c->request < 0 || c->request >= n_req || !c->ptr ||
-            (c->layout != ORA_LAYER_MAJOR && c->layout != ORA_TOKEN_MAJOR))
+            (c->layout != ORA_LAYER_MAJOR && c->layout != ORA_TOKEN_MAJOR &&
+             c->layout != ORA_STRIPED))
             return ORA_EBADARG;
         const ora_request *r = &reqs[c->request];
         if (c->token_begin < 0 || c->n_tokens < 0 ||

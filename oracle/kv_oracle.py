@@ -35,6 +35,17 @@ _LIB = os.path.join(_HERE, "libkv_oracle.so")
 
 LAYER_MAJOR = 0
 TOKEN_MAJOR = 1
+STRIPED = 2
+STRIPE_ALIGN = 4096
+
+
+def chunk_bytes(n_layers: int, kv_factor: int, n_tokens: int, token_bytes: int,
+                layout: int) -> int:
+    """Bytes a chunk occupies in its layout (STRIPED pads each (layer, kv) object)."""
+    obj = n_tokens * token_bytes
+    if layout == STRIPED:
+        obj = -(-obj // STRIPE_ALIGN) * STRIPE_ALIGN
+    return n_layers * kv_factor * obj
 
 ERRORS = {0: "ok", -1: "bad argument", -2: "token range", -3: "page id out of range",
           -4: "layer range"}
@@ -180,7 +191,7 @@ def _marshal(pool: Pool, reqs: Sequence[Request], chunks: Sequence[Chunk]) -> _M
     cchunks = (_Chunk * max(1, len(chunks)))()
     for i, c in enumerate(chunks):
         _check_array(c.buf, "chunk buffer")
-        need = c.n_layers * pool.kv_factor * c.n_tokens * pool.token_bytes
+        need = chunk_bytes(c.n_layers, pool.kv_factor, c.n_tokens, pool.token_bytes, c.layout)
         if c.buf.nbytes < need:
             raise ValueError(f"chunk {i} buffer holds {c.buf.nbytes} B, needs {need}")
         cchunks[i] = _Chunk(c.request, c.token_begin, c.n_tokens, c.layer_begin, c.n_layers,

@@ -121,7 +121,8 @@ kvx_status validate(const kvx_pool *pool, const kvx_request *reqs, int n_req,
             return fail(KVX_ERR_INVALID_ARG, msg, len, "chunk %d: layers [%d, %lld) outside "
                         "[0, %d)", c, ch.layer_begin,
                         (long long)ch.layer_begin + ch.n_layers, pool->num_layers);
-        if (ch.layout != KVX_CHUNK_LAYER_MAJOR && ch.layout != KVX_CHUNK_TOKEN_MAJOR)
+        if (ch.layout != KVX_CHUNK_LAYER_MAJOR && ch.layout != KVX_CHUNK_TOKEN_MAJOR &&
+            ch.layout != KVX_CHUNK_STRIPED)
             return fail(KVX_ERR_INVALID_ARG, msg, len, "chunk %d: layout %d", c, ch.layout);
     }
     if (level <= 0)
@@ -258,6 +259,10 @@ Plan pack(const kvx_pool *pool, const kvx_request *reqs, int n_req, const kvx_ch
         d.ptr = static_cast<char *>(ch.ptr);
         if (ch.layout == KVX_CHUNK_LAYER_MAJOR) {
             d.slab_stride = (int64_t)ch.n_tokens * v;
+            d.row_stride = v;
+        } else if (ch.layout == KVX_CHUNK_STRIPED) {
+            const int64_t obj = (int64_t)ch.n_tokens * v;
+            d.slab_stride = (obj + KVX_STRIPE_ALIGN - 1) / KVX_STRIPE_ALIGN * KVX_STRIPE_ALIGN;
             d.row_stride = v;
         } else {
             d.slab_stride = v;

@@ -43,6 +43,8 @@ KVX_DEV_WAIT_TIMEOUT = 0x2
 
 KVX_CHUNK_LAYER_MAJOR = 0
 KVX_CHUNK_TOKEN_MAJOR = 1
+KVX_CHUNK_STRIPED = 2
+KVX_STRIPE_ALIGN = 4096
 
 KVX_DIR_GATHER = 0
 KVX_DIR_SCATTER = 1

@@ -34,6 +34,8 @@ import torch
 
 LAYER_MAJOR = 0
 TOKEN_MAJOR = 1
+STRIPED = 2          # layer-major objects, each starting at a 4096-byte multiple
+STRIPE_ALIGN = 4096
 
 DTYPE_BYTES = {"fp16": 2, "bf16": 2, "fp8_e4m3": 1}
 TORCH_DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
@@ -82,7 +84,10 @@ class ChunkSpec:
     offset: int = 0          # byte offset of the chunk in its arena
 
     def nbytes(self, shape: KVShape) -> int:
-        return self.n_layers * shape.kv_factor * self.n_tokens * shape.token_bytes
+        obj = self.n_tokens * shape.token_bytes
+        if self.layout == STRIPED:
+            obj = -(-obj // STRIPE_ALIGN) * STRIPE_ALIGN
+        return self.n_layers * shape.kv_factor * obj
 
 
 @dataclass
@@ -255,8 +260,23 @@ def mla_sweep(page_size: int = 16, chunk_bytes: int = 1 << 20, seed: int = 1004,
                     f"per-layer chunks of {tpc} tokens ({chunk_bytes >> 10} KiB budget)")
 
 
+def mla_blocks(page_size: int = 16, seed: int = 1004, n_tokens: int = 16384,
+               num_layers: int = 61) -> Workload:
+    """The MLA request stored as per-block objects: one STRIPED chunk per page (block) holding
+    that block's 61 layer objects, each 4096-byte aligned (Tutti's 2L objects per KV block,
+    with kv_factor 1)."""
+    w = mla_sweep(page_size, 1 << 20, seed, n_tokens, num_layers)
+    chunks = split_tokens(0, 0, n_tokens, page_size, 0, num_layers, STRIPED)
+    place_chunks(chunks, w.shape, align=STRIPE_ALIGN)
+    w.name = f"mla_blocks_p{page_size}"
+    w.store_chunks = chunks
+    w.load_chunks = [ChunkSpec(**vars(c)) for c in chunks]
+    w.notes = "one 4096-aligned object per (block, layer)"
+    return w
+
+
 WORKLOADS = {"tiny": tiny, "llama8b": llama8b, "llama70b": llama70b,
-             "qwen7b_batch": qwen7b_batch, "mla_sweep": mla_sweep}
+             "qwen7b_batch": qwen7b_batch, "mla_sweep": mla_sweep, "mla_blocks": mla_blocks}
 
 
 # ----------------------------------------------------------------------------- values

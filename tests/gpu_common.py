@@ -182,7 +182,7 @@ def random_case(rng: np.random.Generator, max_tokens=700):
         for a, b in zip(cuts[:-1], cuts[1:]):
             l0 = int(rng.integers(0, L))
             nl = int(rng.integers(1, L - l0 + 1))
-            specs.append(wl.ChunkSpec(r, a, b - a, l0, nl, int(rng.integers(0, 2))))
+            specs.append(wl.ChunkSpec(r, a, b - a, l0, nl, int(rng.integers(0, 3))))
     if rng.random() < 0.2:  # an empty chunk now and then
         specs.append(wl.ChunkSpec(0, 0, 0, 0, L, 0))
     order = rng.permutation(len(specs))

@@ -296,3 +296,36 @@ def test_mla_sweep_cell_full_size(ctx, page_size, chunk_bytes):
         _compare_pool(pools, host_pool, f"mla P={page_size} C={chunk_bytes} {how} load")
     arena.close()
     hp.close()
+
+
+# ----------------------------------------------------------------------------- mla_blocks
+
+def test_mla_block_objects_store_and_per_layer_load(ctx):
+    """Per-block STRIPED chunks (one 4096-aligned object per layer): one store of every
+    layer, then one load call per layer (layer window [l, l+1)), as a per-layer retrieve of
+    block objects issues them."""
+    w = wl.mla_blocks(16)
+    s = w.shape
+    pools = _pools(s, w.seed)
+    hp = HostPool(pools, s.page_size)
+    src, dst = _requests(w.store_requests), _requests(w.load_requests)
+    nbytes = w.store_arena_bytes
+    arena = kvx.HostBuffer(nbytes + 4096)
+    arena.array[:] = CANARY
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    stream = torch.cuda.Stream(priority=-1)
+    sh = stream.cuda_stream
+    ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+    kvx.kvx_store_chunks(ctx, pool, src.array, ch, stream=sh)
+    stream.synchronize()
+    expect = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(hp.pool, src.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
+    assert_bytes_equal(arena.array, expect, "mla block objects store")
+    for l in range(s.num_layers):
+        kvx.kvx_load_chunks(ctx, pool, dst.array, ch, l, l + 1, stream=sh)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    oracle.load(hp.pool, dst.oracle(), oracle_chunks(w.load_chunks, arena.array), threads=16)
+    _compare_pool(pools, hp.pool, "mla block objects per-layer load")
+    arena.close()
+    hp.close()

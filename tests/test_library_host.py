@@ -112,7 +112,7 @@ def test_validate_rejects(case, status):
     elif case == "window":
         lb, le = 3, 2
     elif case == "layout":
-        spec[5] = 2
+        spec[5] = 3
     elif case == "negative":
         spec[2] = -1
     elif case == "null_table":

@@ -32,6 +32,8 @@ MUTATIONS = {
     "window_ignored": ("int32_t l_lo = c->layer_begin > layer_begin ? c->layer_begin : layer_begin;",
                        "int32_t l_lo = c->layer_begin;"),
     "token_offset_sign": ("int64_t tr = t - c->token_begin;", "int64_t tr = c->token_begin - t + c->n_tokens - 1;"),
+    "stripe_not_padded": ("int64_t stride = (object_bytes + ORA_STRIPE_ALIGN - 1) / ORA_STRIPE_ALIGN * ORA_STRIPE_ALIGN;",
+                          "int64_t stride = object_bytes;"),
 }
 
 PIN_CASES = [

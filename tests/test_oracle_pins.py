@@ -23,7 +23,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import LAYER_MAJOR, TOKEN_MAJOR, Chunk, Pool, Request
+from oracle import LAYER_MAJOR, STRIPED, TOKEN_MAJOR, Chunk, Pool, Request
 from paged_kv_gather_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -57,7 +57,8 @@ def fill_pool_with_tags(pool, reqs, Tmax):
 
 
 def expected_chunk_words(c, r, L, KV, W, Tmax, lb, le):
-    """Chunk contents by the layout definition, CANARY32 outside the layer window."""
+    """Chunk contents by the layout definition, CANARY32 outside the layer window (and in
+    the padding after each object of a STRIPED chunk)."""
     lr = np.arange(c.n_layers)[:, None, None, None]
     k = np.arange(KV)[None, :, None, None]
     tr = np.arange(c.n_tokens)[None, None, :, None]
@@ -69,19 +70,26 @@ def expected_chunk_words(c, r, L, KV, W, Tmax, lb, le):
     e = np.where(np.broadcast_to(in_window, e.shape), e, CANARY32)
     if c.layout == TOKEN_MAJOR:
         e = e.transpose(2, 0, 1, 3)  # [layer][kv][token] -> [token][layer][kv]
+    if c.layout == STRIPED:
+        # Each (layer, kv) object padded with canaries up to the next 4096-byte multiple.
+        obj_words = c.n_tokens * W
+        stride_words = -(-obj_words * 4 // 4096) * 4096 // 4
+        padded = np.full((c.n_layers, KV, stride_words), CANARY32, np.int32)
+        padded[:, :, :obj_words] = e.reshape(c.n_layers, KV, obj_words)
+        e = padded
     return e.reshape(-1)
 
 
 def make_chunks(specs, KV, v, pad=16):
     out = []
     for (r, t0, n, l0, nl, layout) in specs:
-        buf = np.full(nl * KV * n * v + pad, 0xA5, np.uint8)
+        buf = np.full(oracle.chunk_bytes(nl, KV, n, v, layout) + pad, 0xA5, np.uint8)
         out.append(Chunk(r, t0, n, l0, nl, layout, buf))
     return out
 
 
 def chunk_words(c, KV, v):
-    return c.buf[: c.n_layers * KV * c.n_tokens * v].view(np.int32)
+    return c.buf[: oracle.chunk_bytes(c.n_layers, KV, c.n_tokens, v, c.layout)].view(np.int32)
 
 
 def random_table(rng, n_pages_needed, num_pages):
@@ -137,7 +145,7 @@ def test_bruteforce_all_injective_page_maps(P):
         for perm in itertools.permutations(range(num_pages), n_pages):
             pt = np.array(perm, np.int32)
             reqs = [Request(pt, T)]
-            for layout in (LAYER_MAJOR, TOKEN_MAJOR):
+            for layout in (LAYER_MAJOR, TOKEN_MAJOR, STRIPED):
                 pool = empty_pool(L, KV, num_pages, P, v)
                 fill_pool_with_tags(pool, reqs, T)
                 check_store(pool, reqs, [(0, 0, T, 0, L, layout)], 0, L, T)
@@ -158,9 +166,9 @@ def test_bruteforce_every_cut_and_layer_window(KV, v):
     layer_ranges = [(a, b - a) for a in range(L) for b in range(a + 1, L + 1)]
     windows = [(a, b) for a in range(L + 1) for b in range(a, L + 1)]
     for cut in range(T + 1):
-        layout = cut % 2
+        layout = cut % 3
         l0, nl = layer_ranges[cut % len(layer_ranges)]
-        specs = [(0, 0, cut, l0, nl, layout), (0, cut, T - cut, 0, L, 1 - layout)]
+        specs = [(0, 0, cut, l0, nl, layout), (0, cut, T - cut, 0, L, (layout + 1) % 3)]
         for lb, le in windows:
             check_store(pool, reqs, specs, lb, le, T)
             check_load(L, KV, P, v, num_pages, reqs, specs, lb, le, T)
@@ -190,7 +198,7 @@ def test_bruteforce_random_multi_request_mixes():
             for a, b in zip(cuts[:-1], cuts[1:]):
                 l0 = int(rng.integers(0, L))
                 nl = int(rng.integers(1, L - l0 + 1))
-                specs.append((r, a, b - a, l0, nl, int(rng.integers(0, 2))))
+                specs.append((r, a, b - a, l0, nl, int(rng.integers(0, 3))))
         lb = int(rng.integers(0, L + 1))
         le = int(rng.integers(lb, L + 1))
         pool = empty_pool(L, KV, num_pages, P, v)
@@ -252,7 +260,7 @@ def test_partial_last_page_slots_untouched():
 
 # ----------------------------------------------------------------------------- P-c
 
-@pytest.mark.parametrize("layout", [LAYER_MAJOR, TOKEN_MAJOR])
+@pytest.mark.parametrize("layout", [LAYER_MAJOR, TOKEN_MAJOR, STRIPED])
 def test_round_trip_store_then_load_disjoint_pages(layout):
     rng = np.random.default_rng(99 + layout)
     L, KV, P, v, T = 3, 2, 16, 64, 200
@@ -444,6 +452,26 @@ def test_strata_index_formula_randomised():
             np.testing.assert_array_equal(dst[d], host[s])
             touched[d] = True
         assert np.all(dst[~touched] == 0)
+
+
+def test_striped_object_offsets_closed_form():
+    """One block of the MLA latent cache (16 tokens x 1152 B = 18,432 B per object) in the
+    STRIPED layout: objects start at 0, 20480, 40960, ... and hold the block's bytes of
+    that layer; the 2,048 padding bytes after each object are never written."""
+    L, KV, P, v = 61, 1, 16, 1152
+    assert oracle.chunk_bytes(L, KV, P, v, STRIPED) == L * 20480
+    assert oracle.chunk_bytes(L, KV, P, v, LAYER_MAJOR) == L * 18432
+    rng = np.random.default_rng(12)
+    pool = Pool([[rng.integers(0, 256, (4, P, v), dtype=np.uint8) for _ in range(L)]], P)
+    chunks = make_chunks([(0, 0, P, 0, L, STRIPED)], KV, v, pad=0)
+    oracle.store(pool, [Request(np.array([2], np.int32), P)], chunks)
+    buf = chunks[0].buf
+    for l in range(L):
+        assert buf[l * 20480:l * 20480 + 18432].tobytes() == pool.pools[0][l][2].tobytes()
+        assert np.all(buf[l * 20480 + 18432:(l + 1) * 20480] == 0xA5)
+    # A 4 KiB-multiple object needs no padding: STRIPED and LAYER_MAJOR coincide.
+    assert oracle.chunk_bytes(32, 2, 16, 2048, STRIPED) == oracle.chunk_bytes(32, 2, 16, 2048,
+                                                                               LAYER_MAJOR)
 
 
 # ----------------------------------------------------------------------------- errors
