@@ -725,8 +725,13 @@ def run_llama70b(args, kvx, wl):
         load_span = start.elapsed_time(end_a)
         e2e = start.elapsed_time(end_b)
         g_ms = statistics.mean(gt.ms())
+        model = kvx.kvx_default_link_model()
+        pred_io = kvx.kvx_estimate_us(model, kvx.KVX_OP_LOAD, layer_bytes, cfg)
+        pred_e2e, pred_bubble = kvx.kvx_estimate_stream_us(pred_io, gemm_ms * 1e3, s.num_layers)
         _emit({"workload": "llama70b_layer_streaming", "sm_cap": cap,
                "load_stream_priority": "high" if prio < 0 else "normal",
+               "model_e2e_ms": round(pred_e2e * 1e-3, 3),
+               "model_bubble_ms": round(pred_bubble * 1e-3, 3),
                "load_cfg": cfg.as_dict(),
                "load_alone_ms": round(alone_ms, 3),
                "load_alone_gbs": round(w.load_bytes() / (alone_ms * 1e-3) / GB, 2),

@@ -301,6 +301,44 @@ kvx_status kvx_plan_count(const kvx_pool *pool, const kvx_request *reqs, int n_r
 kvx_status kvx_chunk_policy(const kvx_pool *pool, int layer_streaming, int64_t target_bytes,
                             int32_t *tokens_per_chunk, int32_t *layers_per_chunk);
 
+/* ---------------------------------------------------------------- I/O-time estimator */
+
+/* A measured description of one GPU's data paths, for kvx_estimate_us.  Fill it from
+ * measurements (bench.py prints them); kvx_default_link_model gives the GB300 + Grace
+ * NVLink-C2C figures measured by this library's benchmark. */
+typedef struct kvx_link_model {
+    double h2d_gbs;      /* host -> device peak, GB/s (one 4 GiB pinned copy) */
+    double d2h_gbs;      /* device -> host peak, GB/s */
+    double hbm_gbs;      /* HBM copy peak, GB/s counting read + write */
+    double latency_us;   /* round trip of one host-memory access from an SM */
+    double launch_us;    /* fixed cost of one call: host packing, descriptor copy, launch */
+    int32_t num_sms;
+    int32_t reserved;
+} kvx_link_model;
+
+kvx_status kvx_default_link_model(kvx_link_model *model);
+
+/* Predicted duration (microseconds) of one store/load/transform call of the warp-segment
+ * mapping moving `bytes` in each direction with launch configuration cfg (NULL = the
+ * operation's defaults).  Little's law, as "Strata Guide: Hierarchical Context Caching for
+ * Long LLMs", section "The Physics of I/O Bandwidth and Little's Law", states it
+ * (X = C * S / L): each CTA keeps threads x unroll 16-byte units in flight, so the
+ * CTAs sustain ctas x threads x unroll x 16 / latency, capped by the link's peak in that
+ * direction; the HBM transform is capped by the HBM peak (2 x bytes of traffic).
+ * t = launch_us + bytes / min(peak, in_flight / latency). */
+kvx_status kvx_estimate_us(const kvx_link_model *model, int op, int64_t bytes,
+                           const kvx_launch_cfg *cfg, double *us);
+
+/* Layer-streamed prefill: layer l + 1's KV is loaded while layer l computes (as "Strata
+ * Guide", section "The Loading-Bound Scheduling Dilemma and Delay Hits", and the
+ * step list "Layer-Overlapped Prefill" describe).  With per-layer load time io_us and
+ * compute time compute_us, the predicted end-to-end time is
+ *   io_us + (n_layers - 1) * max(io_us, compute_us) + compute_us
+ * and the I/O bubble (time the compute stream waits) is n_layers' worth of
+ * max(0, io_us - compute_us) after the first layer plus the first load itself. */
+kvx_status kvx_estimate_stream_us(double io_us, double compute_us, int n_layers,
+                                  double *e2e_us, double *bubble_us);
+
 /* Pinned host memory, mapped into the device address space (allocate or register
  * once, up front, never on the transfer path). */
 kvx_status kvx_host_alloc(void **ptr, size_t bytes);

@@ -378,6 +378,73 @@ kvx_status kvx_chunk_policy(const kvx_pool *pool, int layer_streaming, int64_t t
     return KVX_OK;
 }
 
+kvx_status kvx_default_link_model(kvx_link_model *m)
+{
+    if (!m)
+        return KVX_ERR_INVALID_ARG;
+    // GB300 with a Grace host over NVLink-C2C, as measured by the benchmark: pinned copies
+    // 211.6 GB/s H2D and 193.7 GB/s D2H; copy peak 6791.7 GB/s; one SM with 128 KiB of
+    // host reads in flight sustains ~50 GB/s (2.6 us round trip); ~10 us per call.
+    m->h2d_gbs = 211.6;
+    m->d2h_gbs = 193.7;
+    m->hbm_gbs = 6791.7;
+    m->latency_us = 2.6;
+    m->launch_us = 10.0;
+    m->num_sms = 152;
+    m->reserved = 0;
+    return KVX_OK;
+}
+
+kvx_status kvx_estimate_us(const kvx_link_model *m, int op, int64_t bytes,
+                           const kvx_launch_cfg *cfg, double *us)
+{
+    if (!m || !us || bytes < 0 || op < KVX_OP_STORE || op > KVX_OP_SCATTER_HBM ||
+        m->latency_us <= 0 || m->num_sms <= 0)
+        return KVX_ERR_INVALID_ARG;
+    // The operation's defaults when no configuration is given (kept in step with the
+    // library's kvx_default_launch_cfg).
+    int sm_cap = op <= KVX_OP_LOAD ? 16 : 0, ctas = op <= KVX_OP_LOAD ? 1 : 2;
+    int threads = op <= KVX_OP_LOAD ? 1024 : 256, unroll = 8;
+    if (cfg) {
+        sm_cap = cfg->sm_cap;
+        if (cfg->ctas_per_sm)
+            ctas = cfg->ctas_per_sm;
+        if (cfg->threads)
+            threads = cfg->threads;
+        if (cfg->unroll)
+            unroll = cfg->unroll;
+    }
+    const double sms = sm_cap > 0 && sm_cap < m->num_sms ? sm_cap : m->num_sms;
+    const double in_flight = sms * ctas * threads * (double)unroll * 16.0;  // bytes
+    const double little_gbs = in_flight / (m->latency_us * 1e3);           // B/ns = GB/s
+    double peak;
+    double moved = (double)bytes;
+    if (op == KVX_OP_STORE)
+        peak = m->d2h_gbs;
+    else if (op == KVX_OP_LOAD)
+        peak = m->h2d_gbs;
+    else {
+        peak = m->hbm_gbs;
+        moved = 2.0 * bytes;  // read + write in HBM
+    }
+    const double gbs = op <= KVX_OP_LOAD ? (little_gbs < peak ? little_gbs : peak) : peak;
+    *us = m->launch_us + (gbs > 0 ? moved / (gbs * 1e3) : 0.0);
+    return KVX_OK;
+}
+
+kvx_status kvx_estimate_stream_us(double io_us, double compute_us, int n_layers,
+                                  double *e2e_us, double *bubble_us)
+{
+    if (n_layers <= 0 || io_us < 0 || compute_us < 0)
+        return KVX_ERR_INVALID_ARG;
+    const double step = io_us > compute_us ? io_us : compute_us;
+    if (e2e_us)
+        *e2e_us = io_us + (n_layers - 1) * step + compute_us;
+    if (bubble_us)
+        *bubble_us = io_us + (n_layers - 1) * (io_us > compute_us ? io_us - compute_us : 0.0);
+    return KVX_OK;
+}
+
 const char *kvx_status_string(kvx_status s)
 {
     switch (s) {

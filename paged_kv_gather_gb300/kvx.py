@@ -93,6 +93,13 @@ class kvx_launch_cfg(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class kvx_link_model(ctypes.Structure):
+    _fields_ = [("h2d_gbs", ctypes.c_double), ("d2h_gbs", ctypes.c_double),
+                ("hbm_gbs", ctypes.c_double), ("latency_us", ctypes.c_double),
+                ("launch_us", ctypes.c_double), ("num_sms", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 CHUNK_DTYPE = np.dtype([("request", "<i4"), ("token_begin", "<i4"), ("n_tokens", "<i4"),
                         ("layer_begin", "<i4"), ("n_layers", "<i4"), ("layout", "<i4"),
                         ("ptr", "<u8")])
@@ -140,6 +147,11 @@ _proto("kvx_host_register", _c.c_int, [_c.c_void_p, _c.c_size_t])
 _proto("kvx_host_unregister", _c.c_int, [_c.c_void_p])
 _proto("kvx_status_string", _c.c_char_p, [_c.c_int])
 _proto("kvx_version", _c.c_int, [])
+_proto("kvx_default_link_model", _c.c_int, [_P(kvx_link_model)])
+_proto("kvx_estimate_us", _c.c_int, [_P(kvx_link_model), _c.c_int, _c.c_int64,
+                                     _P(kvx_launch_cfg), _P(_c.c_double)])
+_proto("kvx_estimate_stream_us", _c.c_int, [_c.c_double, _c.c_double, _c.c_int,
+                                            _P(_c.c_double), _P(_c.c_double)])
 _proto("kvx_load_chunks_noalloc", _c.c_int, [*_batch, _P(kvx_launch_cfg), _c.c_void_p,
                                              _c.c_void_p])
 
@@ -148,7 +160,8 @@ EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_laun
             "kvx_get_status", "kvx_last_error", "kvx_last_launch", "kvx_validate",
             "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
-            "kvx_load_chunks_noalloc"]
+            "kvx_load_chunks_noalloc", "kvx_default_link_model", "kvx_estimate_us",
+            "kvx_estimate_stream_us"]
 
 KVX_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -388,6 +401,32 @@ def kvx_chunk_policy(pool: Pool, layer_streaming: bool = False,
     if st != KVX_OK:
         raise KvxError(st, "kvx_chunk_policy")
     return t.value, l.value
+
+
+def kvx_default_link_model() -> kvx_link_model:
+    m = kvx_link_model()
+    st = _lib.kvx_default_link_model(ctypes.byref(m))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_default_link_model")
+    return m
+
+
+def kvx_estimate_us(model: kvx_link_model, op: int, nbytes: int,
+                    cfg: Optional[kvx_launch_cfg] = None) -> float:
+    us = ctypes.c_double()
+    st = _lib.kvx_estimate_us(ctypes.byref(model), op, nbytes, _cfg_ptr(cfg), ctypes.byref(us))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_estimate_us")
+    return us.value
+
+
+def kvx_estimate_stream_us(io_us: float, compute_us: float, n_layers: int) -> Tuple[float, float]:
+    e2e, bubble = ctypes.c_double(), ctypes.c_double()
+    st = _lib.kvx_estimate_stream_us(io_us, compute_us, n_layers, ctypes.byref(e2e),
+                                     ctypes.byref(bubble))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_estimate_stream_us")
+    return e2e.value, bubble.value
 
 
 def kvx_host_alloc(nbytes: int) -> int:

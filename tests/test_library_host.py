@@ -238,3 +238,48 @@ def test_chunk_and_request_dtypes_match_c_structs():
         assert kvx.CHUNK_DTYPE.fields[name][1] == getattr(kvx.kvx_chunk, name).offset
     for name, _ in kvx.kvx_request._fields_:
         assert kvx.REQUEST_DTYPE.fields[name][1] == getattr(kvx.kvx_request, name).offset
+
+
+# ----------------------------------------------------------------------------- estimator
+
+def test_estimator_littles_law_and_link_cap():
+    m = kvx.kvx_default_link_model()
+    N = 4 << 30
+    prev = 0.0
+    for cap in (1, 2, 4, 8, 16, 32, 0):
+        c = kvx.kvx_launch_cfg()
+        c.sm_cap, c.ctas_per_sm, c.threads, c.unroll = cap, 1, 1024, 8
+        us = kvx.kvx_estimate_us(m, kvx.KVX_OP_LOAD, N, c)
+        gbs = N / ((us - m.launch_us) * 1e3)
+        sms = cap if cap else m.num_sms
+        # X = C * S / L with 1024 threads x 8 units x 16 B in flight per SM, capped by the link.
+        assert gbs == pytest.approx(min(m.h2d_gbs, sms * 1024 * 8 * 16 / (m.latency_us * 1e3)))
+        assert gbs >= prev
+        prev = gbs
+    # Halving the bytes in flight halves the Little's-law rate below the cap.
+    c = kvx.kvx_launch_cfg()
+    c.sm_cap, c.ctas_per_sm, c.threads, c.unroll = 2, 1, 1024, 4
+    us = kvx.kvx_estimate_us(m, kvx.KVX_OP_STORE, N, c)
+    assert N / ((us - m.launch_us) * 1e3) == pytest.approx(2 * 1024 * 4 * 16 / 2600.0)
+    # The HBM transform moves 2N through HBM at the copy peak, whatever the SM cap.
+    us = kvx.kvx_estimate_us(m, kvx.KVX_OP_GATHER_HBM, N, None)
+    assert us == pytest.approx(m.launch_us + 2 * N / (m.hbm_gbs * 1e3))
+    with pytest.raises(kvx.KvxError):
+        kvx.kvx_estimate_us(m, 7, N, None)
+
+
+def test_estimator_layer_streaming_bounds():
+    # Loading-bound (io > compute): e2e = L * io + compute; the compute stream waits for
+    # the first load and then io - compute per layer.
+    e2e, bubble = kvx.kvx_estimate_stream_us(1290.0, 560.0, 80)
+    assert e2e == pytest.approx(1290 + 79 * 1290 + 560)
+    assert bubble == pytest.approx(1290 + 79 * 730)
+    assert e2e >= max(80 * 1290, 80 * 560)
+    # Compute-bound: only the first load is exposed.
+    e2e, bubble = kvx.kvx_estimate_stream_us(300.0, 560.0, 80)
+    assert e2e == pytest.approx(300 + 79 * 560 + 560)
+    assert bubble == pytest.approx(300)
+    # One layer: load then compute.
+    assert kvx.kvx_estimate_stream_us(5.0, 7.0, 1) == (12.0, 5.0)
+    with pytest.raises(kvx.KvxError):
+        kvx.kvx_estimate_stream_us(1.0, 1.0, 0)
