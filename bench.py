@@ -59,7 +59,8 @@ def parse():
     p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--workload", default="llama8b",
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
-                            "transform_sweep", "profile_small", "batch_sweep", "mla_blocks"],
+                            "transform_sweep", "profile_small", "batch_sweep", "mla_blocks",
+                            "eviction"],
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
@@ -1030,6 +1031,75 @@ def run_mla_blocks(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
+def run_eviction(args, kvx, wl):
+    """Background eviction: the llama8b request stored to host memory by a 1-, 2- or 4-SM
+    kernel on a low-priority stream while a decode-like, HBM-bound bf16 GEMV loop runs on
+    a high-priority stream; decode step time alone vs with the eviction running."""
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src = w.store_requests[0]
+    ps = torch.from_numpy(src.page_table).cuda()
+    rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+    arena = kvx.HostBuffer(w.store_arena_bytes)
+    arena.array[:] = 0
+    ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+    ctx = kvx.kvx_create(0)
+    N = w.store_bytes()
+    low = torch.cuda.Stream(priority=0)
+    high = torch.cuda.Stream(priority=-1)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    Wm = torch.randn(16384, 32768, device="cuda", dtype=torch.bfloat16, generator=g)  # 1 GiB
+    x = torch.randn(32768, 1, device="cuda", dtype=torch.bfloat16, generator=g)
+    y = torch.empty(16384, 1, device="cuda", dtype=torch.bfloat16)
+
+    def decode(n):
+        with torch.cuda.stream(high):
+            for _ in range(n):
+                torch.matmul(Wm, x, out=y)
+
+    decode(20)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(high)
+    decode(200)
+    e1.record(high)
+    torch.cuda.synchronize()
+    step_alone = e0.elapsed_time(e1) / 200
+    for cap in (1, 2, 4):
+        cfg = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_STORE)
+        cfg.sm_cap = cap
+        cfg.store_hint = kvx.KVX_HINT_DEFAULT
+        # Store alone on the low-priority stream.
+        st_ms = _timed(low, lambda: kvx.kvx_store_chunks(ctx, pool, rs, ch, 0, s.num_layers,
+                                                         cfg, low.cuda_stream), 2, 1)
+        n_steps = max(50, int(st_ms / step_alone))
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(low)
+        kvx.kvx_store_chunks(ctx, pool, rs, ch, 0, s.num_layers, cfg, low.cuda_stream)
+        a1.record(low)
+        d0.record(high)
+        decode(n_steps)
+        d1.record(high)
+        torch.cuda.synchronize()
+        assert kvx.kvx_get_status(ctx, low.cuda_stream) == 0
+        step_with = d0.elapsed_time(d1) / n_steps
+        _emit({"workload": "background_eviction", "sm_cap": cap,
+               "store_alone_gbs": round(N / (st_ms * 1e-3) / GB, 2),
+               "store_under_decode_gbs": round(N / (a0.elapsed_time(a1) * 1e-3) / GB, 2),
+               "decode_step_alone_ms": round(step_alone, 4),
+               "decode_step_with_eviction_ms": round(step_with, 4),
+               "decode_slowdown_pct": round(100 * (step_with / step_alone - 1), 2),
+               "decode_steps": n_steps,
+               "decode_gemv": "bf16 [16384 x 32768] x [32768], 1 GiB of weights per step"})
+    arena.close()
+    kvx.kvx_destroy(ctx)
+
+
 def run_profile_small(args, kvx, wl):
     """A small case for ncu captures: the Llama-3.1-8B shape cut to 8192 tokens (1 GiB per
     direction, above the 129 MB L2) in a 1024-page pool (2 GiB), one operation 3 times
@@ -1077,7 +1147,7 @@ def run_workload(args):
     {"llama70b": run_llama70b, "qwen7b_batch": run_qwen7b, "mla_sweep": run_mla_sweep,
      "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
      "profile_small": run_profile_small, "batch_sweep": run_batch_sweep,
-     "mla_blocks": run_mla_blocks}[args.workload](
+     "mla_blocks": run_mla_blocks, "eviction": run_eviction}[args.workload](
         args, kvx, wl)
 
 
