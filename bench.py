@@ -743,6 +743,68 @@ def run_llama70b(args, kvx, wl):
                "e2e_ms": round(e2e, 3),
                "serial_ms": round(alone_ms + s.num_layers * gemm_ms, 3),
                "layer_bytes": layer_bytes})
+    # Hard SM partitions (green contexts): the loads on an I/O partition, the GEMM on the
+    # rest of the GPU.
+    for io_sms in (8, 16):
+        try:
+            part = kvx.kvx_partition_create(0, io_sms, -1, 0)
+        except kvx.KvxError as e:
+            _emit({"workload": "llama70b_layer_streaming", "partition": "unavailable",
+                   "reason": str(e)})
+            break
+        sa = torch.cuda.ExternalStream(part.io_stream)
+        sc = torch.cuda.ExternalStream(part.compute_stream)
+        cfg = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD)
+        cfg.sm_cap = 0  # the partition bounds the SMs
+
+        def gemm_c():
+            with torch.cuda.stream(sc):
+                torch.matmul(A, B, out=C)
+
+        g_part = _timed(sc, gemm_c, 20, warm=5)
+
+        def load_all():
+            for l in range(s.num_layers):
+                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, part.io_stream)
+
+        alone_ms = _timed(sa, load_all, 3, warm=1)
+        for rep in range(2):
+            torch.cuda.synchronize()
+            start = torch.cuda.Event(enable_timing=True)
+            start.record(sa)
+            sc.wait_event(start)
+            gt = EventTimer(sc)
+            for l in range(s.num_layers):
+                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, part.io_stream)
+                ev = torch.cuda.Event()
+                ev.record(sa)
+                sc.wait_event(ev)
+                with torch.cuda.stream(sc):
+                    e = gt.start()
+                    torch.matmul(A, B, out=C)
+                    gt.stop(e)
+            end_a = torch.cuda.Event(enable_timing=True)
+            end_a.record(sa)
+            end_b = torch.cuda.Event(enable_timing=True)
+            end_b.record(sc)
+            torch.cuda.synchronize()
+        assert kvx.kvx_get_status(ctx, part.io_stream) == 0
+        g_ms = statistics.mean(gt.ms())
+        load_span = start.elapsed_time(end_a)
+        _emit({"workload": "llama70b_layer_streaming", "partition": "green contexts",
+               "io_sms": part.io_sms, "compute_sms": part.compute_sms,
+               "load_alone_ms": round(alone_ms, 3),
+               "load_alone_gbs": round(w.load_bytes() / (alone_ms * 1e-3) / GB, 2),
+               "load_overlap_span_ms": round(load_span, 3),
+               "load_overlap_gbs": round(w.load_bytes() / (load_span * 1e-3) / GB, 2),
+               "gemm_alone_ms": round(gemm_ms, 4),
+               "gemm_on_compute_partition_ms": round(g_part, 4),
+               "gemm_overlap_ms": round(g_ms, 4),
+               "gemm_slowdown_pct": round(100 * (g_ms / gemm_ms - 1), 2),
+               "e2e_ms": round(start.elapsed_time(end_b), 3),
+               "serial_ms": round(alone_ms + s.num_layers * gemm_ms, 3)})
+        torch.cuda.synchronize()
+        part.close()
     arena.close()
     kvx.kvx_destroy(ctx)
 

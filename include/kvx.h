@@ -301,6 +301,29 @@ kvx_status kvx_plan_count(const kvx_pool *pool, const kvx_request *reqs, int n_r
 kvx_status kvx_chunk_policy(const kvx_pool *pool, int layer_streaming, int64_t target_bytes,
                             int32_t *tokens_per_chunk, int32_t *layers_per_chunk);
 
+/* ---------------------------------------------------------------- SM partitioning */
+
+/* Hard split of one GPU's SMs into an I/O partition and a compute partition, each a green
+ * context with one non-blocking stream ("Tutti: Making SSD-Backed KV Cache Practical",
+ * section 2 Design 2: SM partitioning into a compute domain and an I/O domain with green
+ * contexts).  Transfers launched on the I/O stream run only on the I/O SMs; work launched
+ * on the compute stream (wrap it with torch.cuda.ExternalStream, for instance) runs only
+ * on the rest, so neither waits for the other's SMs.  io_sms is a minimum: the driver
+ * rounds it up to its partition granularity (8 SMs on this GPU).  Priorities follow CUDA's
+ * convention (lower = higher; 0 = default).  On failure msg (if msg_len > 0) holds the
+ * failing driver step.  Requires a GPU and a driver with green-context support. */
+typedef struct kvx_partition kvx_partition;
+
+kvx_status kvx_partition_create(int device, int io_sms, int io_priority, int compute_priority,
+                                kvx_partition **out, char *msg, size_t msg_len);
+
+/* The partition's streams and SM counts; any output may be NULL. */
+kvx_status kvx_partition_info(const kvx_partition *partition, kvx_stream_t *io_stream,
+                              kvx_stream_t *compute_stream, int *io_sms, int *compute_sms);
+
+/* Synchronize the device, then destroy the streams and green contexts. */
+void kvx_partition_destroy(kvx_partition *partition);
+
 /* ---------------------------------------------------------------- I/O-time estimator */
 
 /* A measured description of one GPU's data paths, for kvx_estimate_us.  Fill it from

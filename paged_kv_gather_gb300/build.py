@@ -1,7 +1,8 @@
 """Build libkvx.so (the C-ABI library) in-tree for sm_103a with nvcc.
 
-Two translation units, compiled in parallel: the CUDA kernels + entry points (kvx.cu, by
-nvcc) and the host logic (kvx_host.cpp, by the host C++ compiler).  The CUDA runtime is
+Three translation units, compiled in parallel: the CUDA kernels + entry points (kvx.cu, by
+nvcc), the host logic (kvx_host.cpp) and the SM partitioning (kvx_partition.cpp), the last
+two by the host C++ compiler.  The CUDA runtime is
 linked statically so the library loads on machines without a GPU (its host logic and
 exported symbols stay usable there).
 """
@@ -19,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libkvx.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = [os.path.join(CSRC, f) for f in ("kvx.cu", "kvx_host.cpp", "kvx_internal.h")]
+SOURCES = [os.path.join(CSRC, f) for f in ("kvx.cu", "kvx_host.cpp", "kvx_partition.cpp",
+                                             "kvx_internal.h")]
 HEADER = os.path.join(ROOT, "include", "kvx.h")
 
 
@@ -57,18 +59,22 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     tag = f"{os.getpid()}"
     obj_cu = os.path.join(BUILD_DIR, f"kvx.{tag}.o")
-    obj_host = os.path.join(BUILD_DIR, f"kvx_host.{tag}.o")
     cu = [nvcc, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
           "-c", os.path.join(CSRC, "kvx.cu"), "-o", obj_cu]
     cxx = shutil.which("g++") or shutil.which("c++")
-    host = [cxx, "-O2", "-std=c++17", "-fPIC", f"-I{inc}", "-c",
-            os.path.join(CSRC, "kvx_host.cpp"), "-o", obj_host]
-    with ThreadPoolExecutor(2) as ex:
-        logs = list(ex.map(_run, [cu, host]))
+    objs = [obj_cu]
+    cmds = [cu]
+    for src in ("kvx_host.cpp", "kvx_partition.cpp"):
+        obj = os.path.join(BUILD_DIR, f"{src[:-4]}.{tag}.o")
+        objs.append(obj)
+        cmds.append([cxx, "-O2", "-std=c++17", "-fPIC", f"-I{inc}", "-c",
+                     os.path.join(CSRC, src), "-o", obj])
+    with ThreadPoolExecutor(len(cmds)) as ex:
+        logs = list(ex.map(_run, cmds))
     tmp = LIB + f".tmp{tag}"
-    _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, obj_cu, obj_host])
+    _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
     os.replace(tmp, LIB)
-    for o in (obj_cu, obj_host):
+    for o in objs:
         os.remove(o)
     if verbose:
         sys.stdout.write(logs[0])

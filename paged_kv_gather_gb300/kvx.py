@@ -152,6 +152,11 @@ _proto("kvx_estimate_us", _c.c_int, [_P(kvx_link_model), _c.c_int, _c.c_int64,
                                      _P(kvx_launch_cfg), _P(_c.c_double)])
 _proto("kvx_estimate_stream_us", _c.c_int, [_c.c_double, _c.c_double, _c.c_int,
                                             _P(_c.c_double), _P(_c.c_double)])
+_proto("kvx_partition_create", _c.c_int, [_c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                                          _P(_c.c_void_p), _c.c_char_p, _c.c_size_t])
+_proto("kvx_partition_info", _c.c_int, [_c.c_void_p, _P(_c.c_void_p), _P(_c.c_void_p),
+                                        _P(_c.c_int), _P(_c.c_int)])
+_proto("kvx_partition_destroy", None, [_c.c_void_p])
 _proto("kvx_load_chunks_noalloc", _c.c_int, [*_batch, _P(kvx_launch_cfg), _c.c_void_p,
                                              _c.c_void_p])
 
@@ -161,7 +166,8 @@ EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_laun
             "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
             "kvx_load_chunks_noalloc", "kvx_default_link_model", "kvx_estimate_us",
-            "kvx_estimate_stream_us"]
+            "kvx_estimate_stream_us", "kvx_partition_create", "kvx_partition_info",
+            "kvx_partition_destroy"]
 
 KVX_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -427,6 +433,48 @@ def kvx_estimate_stream_us(io_us: float, compute_us: float, n_layers: int) -> Tu
     if st != KVX_OK:
         raise KvxError(st, "kvx_estimate_stream_us")
     return e2e.value, bubble.value
+
+
+class Partition:
+    """An I/O / compute split of the GPU's SMs (green contexts); see kvx_partition_create."""
+
+    def __init__(self, handle, io_stream: int, compute_stream: int, io_sms: int,
+                 compute_sms: int):
+        self.handle = handle
+        self.io_stream = io_stream
+        self.compute_stream = compute_stream
+        self.io_sms = io_sms
+        self.compute_sms = compute_sms
+
+    def close(self):
+        if self.handle:
+            kvx_partition_destroy(self.handle)
+            self.handle = None
+
+
+def kvx_partition_create(device: int, io_sms: int, io_priority: int = -1,
+                         compute_priority: int = 0) -> Partition:
+    h = ctypes.c_void_p()
+    msg = ctypes.create_string_buffer(256)
+    st = _lib.kvx_partition_create(device, io_sms, io_priority, compute_priority,
+                                   ctypes.byref(h), msg, len(msg))
+    if st != KVX_OK:
+        raise KvxError(st, msg.value.decode())
+    io_s, co_s = ctypes.c_void_p(), ctypes.c_void_p()
+    n_io, n_co = ctypes.c_int(), ctypes.c_int()
+    st = _lib.kvx_partition_info(h, ctypes.byref(io_s), ctypes.byref(co_s), ctypes.byref(n_io),
+                                 ctypes.byref(n_co))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_partition_info")
+    return Partition(h, io_s.value or 0, co_s.value or 0, n_io.value, n_co.value)
+
+
+def kvx_partition_info(p: Partition):
+    return p.io_stream, p.compute_stream, p.io_sms, p.compute_sms
+
+
+def kvx_partition_destroy(handle) -> None:
+    _lib.kvx_partition_destroy(handle)
 
 
 def kvx_host_alloc(nbytes: int) -> int:
