@@ -6,8 +6,8 @@ One step = one full pass of the hot path over the Llama-3.1-8B-shaped request:
                     pool) gathered into 128 layer-major chunks of 256 tokens (32 MiB each)
                     in mapped pinned host memory, and
   kvx_load_chunks   those chunks scattered back into a disjoint set of 2048 fresh pages,
-pipelined in chunk groups on two streams (group g's load after group g's store) so both
-directions of the host link carry data at once.  Each direction moves N = 4 GiB; value =
+pipelined in chunk groups: each kvx_exchange_chunks launch stores group g and loads group
+g - 1, so both directions of the host link carry data at once.  Each direction moves N = 4 GiB; value =
 2N per step / step time (GB/s).  Inputs (4 GiB each way) exceed L2 (129 MB): no flush.
 The same store and load run back to back on one stream give the per-direction rooflines.
 
@@ -57,6 +57,7 @@ def parse():
     p.add_argument("--store-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--load-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
+    p.add_argument("--exchange-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--workload", default="llama8b",
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
                             "transform_sweep", "profile_small", "batch_sweep", "mla_blocks",
@@ -66,7 +67,7 @@ def parse():
     p.add_argument("--profile-op", default="load",
                    choices=["store", "load", "gather", "scatter"],
                    help="operation of --workload profile_small")
-    p.add_argument("--groups", type=int, default=8,
+    p.add_argument("--groups", type=int, default=16,
                    help="chunk groups of the pipelined store/load round trip")
     p.add_argument("--sm-caps", default="1,2,4,8,16,32,0",
                    help="SM caps of the llama70b overlap sweep (0 = all SMs)")
@@ -315,46 +316,43 @@ def run_reference(args):
 
 class RoundTrip:
     """The headline step: store the request's 128 chunks to host memory and load them back
-    into the fresh page set, pipelined in `groups` chunk groups on two streams so the two
-    directions of the host link run at once.  Group g's load waits for group g's store
-    (event); group g's next store waits for group g's previous load, so a chunk is never
-    overwritten while it is being read.  Each call is one kernel launch."""
+    into the fresh page set, pipelined in `groups` chunk groups.  Every launch is one
+    kvx_exchange_chunks call on one stream that stores group g and loads group g - 1 (the
+    group the previous launch stored), so both directions of the host link carry data at
+    once and stream order alone keeps each load after its store.  The pipeline runs on
+    across steps: a step's first launch loads the previous step's last group; flush()
+    issues the last load."""
 
-    def __init__(self, kvx, ctx_s, ctx_l, pool, reqs_src, reqs_dst, chunks, num_layers,
-                 cfg_s, cfg_l, groups, dev):
-        self.kvx, self.ctx_s, self.ctx_l, self.pool = kvx, ctx_s, ctx_l, pool
-        self.rs, self.rd, self.L = reqs_src, reqs_dst, num_layers
-        self.cfg_s, self.cfg_l = cfg_s, cfg_l
+    def __init__(self, kvx, ctx, pool, reqs_src, reqs_dst, chunks, num_layers, cfg, groups,
+                 dev):
+        self.kvx, self.ctx, self.pool = kvx, ctx, pool
+        self.rs, self.rd, self.L, self.cfg = reqs_src, reqs_dst, num_layers, cfg
         bounds = np.linspace(0, len(chunks), groups + 1).astype(int)
         self.groups = [np.ascontiguousarray(chunks[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
-        self.ss = torch.cuda.Stream(device=dev)
-        self.sl = torch.cuda.Stream(device=dev)
-        self.loaded = [None] * groups
+        self.empty = np.zeros(0, dtype=chunks.dtype)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.pending = None
 
-    def step(self, t_store=None, t_load=None):
-        kvx = self.kvx
-        for g, ch in enumerate(self.groups):
-            if self.loaded[g] is not None:
-                self.ss.wait_event(self.loaded[g])
-            e = t_store.start() if t_store else None
-            kvx.kvx_store_chunks(self.ctx_s, self.pool, self.rs, ch, 0, self.L, self.cfg_s,
-                                 self.ss.cuda_stream)
-            if e is not None:
-                t_store.stop(e)
-            stored = torch.cuda.Event()
-            stored.record(self.ss)
-            self.sl.wait_event(stored)
-            e = t_load.start() if t_load else None
-            kvx.kvx_load_chunks(self.ctx_l, self.pool, self.rd, ch, 0, self.L, self.cfg_l,
-                                self.sl.cuda_stream)
-            if e is not None:
-                t_load.stop(e)
-            done = torch.cuda.Event()
-            done.record(self.sl)
-            self.loaded[g] = done
+    def _launch(self, store, load, timer=None):
+        e = timer.start() if timer else None
+        self.kvx.kvx_exchange_chunks(self.ctx, self.pool, self.rs, store, self.rd,
+                                     self.empty if load is None else load, 0, self.L,
+                                     self.cfg, self.stream.cuda_stream)
+        if e is not None:
+            timer.stop(e)
+
+    def step(self, timer=None):
+        for ch in self.groups:
+            self._launch(ch, self.pending, timer)
+            self.pending = ch
+
+    def flush(self, timer=None):
+        if self.pending is not None:
+            self._launch(self.empty, self.pending, timer)
+            self.pending = None
 
     def launches_per_step(self):
-        return 2 * len(self.groups)
+        return len(self.groups)
 
 
 def run_ours(args):
@@ -389,12 +387,12 @@ def run_ours(args):
     host.array[:] = 0  # fault in every page before timing
     chunks_host = kvx.chunks_array(w.store_chunks, host.ptr)
     ctx = kvx.kvx_create(local)
-    ctx_l = kvx.kvx_create(local)
     cfg_store = parse_cfg(kvx, ctx, kvx.KVX_OP_STORE, args.store_cfg)
     cfg_load = parse_cfg(kvx, ctx, kvx.KVX_OP_LOAD, args.load_cfg)
     cfg_tr = parse_cfg(kvx, ctx, kvx.KVX_OP_GATHER_HBM, args.transform_cfg)
-    rt = RoundTrip(kvx, ctx, ctx_l, pool, reqs_src, reqs_dst, chunks_host, s.num_layers,
-                   cfg_store, cfg_load, args.groups, dev)
+    cfg_x = parse_cfg(kvx, ctx, kvx.KVX_OP_EXCHANGE, args.exchange_cfg)
+    rt = RoundTrip(kvx, ctx, pool, reqs_src, reqs_dst, chunks_host, s.num_layers, cfg_x,
+                   args.groups, dev)
 
     # ---- host-link peaks: one 4 GiB pinned copy per direction, then both at once
     link = {}
@@ -457,29 +455,28 @@ def run_ours(args):
     store_gbs = N / (store_ms * 1e-3) / GB
     load_gbs = N / (load_ms * 1e-3) / GB
 
-    # ---- the timed region: the pipelined round trip (device clock)
+    # ---- the timed region: the pipelined round trip (device clock).  The warm-up leaves
+    # one group's load pending, so the K timed steps move exactly K x N each way.
     for _ in range(args.warmup):
         rt.step()
     torch.cuda.synchronize()
-    ps, pl = EventTimer(rt.ss), EventTimer(rt.sl)
+    px = EventTimer(rt.stream)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         e_start = torch.cuda.Event(enable_timing=True)
-        e_start.record(rt.ss)
-        rt.sl.wait_event(e_start)
+        e_start.record(rt.stream)
         for _ in range(args.steps):
-            rt.step(ps, pl)
+            rt.step(px)
         e_end = torch.cuda.Event(enable_timing=True)
-        e_end.record(rt.sl)
+        e_end.record(rt.stream)
         torch.cuda.synchronize()
     total_ms = max_over_ranks(e_start.elapsed_time(e_end), world)
     barrier(world)
-    assert kvx.kvx_get_status(ctx, rt.ss.cuda_stream) == 0
-    assert kvx.kvx_get_status(ctx_l, rt.sl.cuda_stream) == 0
-    items, ctas, threads, _ = kvx.kvx_last_launch(ctx_l)
-    p_store_ms = statistics.mean(ps.ms())
-    p_load_ms = statistics.mean(pl.ms())
+    rt.flush()
+    assert kvx.kvx_get_status(ctx, rt.stream.cuda_stream) == 0
+    items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
+    p_x_ms = statistics.mean(px.ms())
     group_bytes = N / args.groups
 
     # ---- end to end through the C ABI on the host clock (pipelined step + uploads/readback)
@@ -490,24 +487,21 @@ def run_ours(args):
     for i in range(args.warmup + max(3, args.steps // 2)):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        with torch.cuda.stream(rt.ss):
+        with torch.cuda.stream(rt.stream):
             pt_dev.copy_(pt_host, non_blocking=True)
-        up = torch.cuda.Event()
-        up.record(rt.ss)
-        rt.sl.wait_event(up)
         rt.rs = kvx.requests_array([(pt_dev.data_ptr(), src_h, w.store_requests[0].n_tokens)])
         rt.rd = kvx.requests_array([(pt_dev.data_ptr() + 4 * len(src_h), dst_h,
                                      w.load_requests[0].n_tokens)])
         rt.step()
-        desc = kvx.kvx_last_launch(ctx)[3] + kvx.kvx_last_launch(ctx_l)[3]
-        assert kvx.kvx_get_status(ctx, rt.ss.cuda_stream) == 0   # D2H status word + sync
-        assert kvx.kvx_get_status(ctx_l, rt.sl.cuda_stream) == 0
+        rt.flush()  # each end-to-end step completes its own round trip
+        desc = kvx.kvx_last_launch(ctx)[3]
+        assert kvx.kvx_get_status(ctx, rt.stream.cuda_stream) == 0   # D2H status word + sync
         if i >= args.warmup:
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
     rt.rs, rt.rd = reqs_src, reqs_dst
     e2e = {"value": round(2 * N / (statistics.median(e2e_ms) * 1e-3) / GB, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": int(pt_host.numel() * 4 + desc * args.groups),
-           "d2h_bytes_per_step": 8,
+           "h2d_bytes_per_step": int(pt_host.numel() * 4 + desc * (args.groups + 1)),
+           "d2h_bytes_per_step": 4,
            "payload_link_bytes_per_step": 2 * N,
            "note": "KV payload crosses the host link inside the kernels (zero-copy, mapped "
                    "pinned memory); the counted copies are the page tables, descriptors and "
@@ -580,7 +574,8 @@ def run_ours(args):
                                "16384-page pool, 128 layer-major chunks of 256 tokens (32 MiB) "
                                "in mapped pinned host memory; step = store all chunks + load "
                                f"them into 2048 fresh pages, pipelined in {args.groups} chunk "
-                               "groups on two streams",
+                               "groups, each launch storing one group and loading the "
+                               "previous one",
                    "bytes_per_direction": N, "l2": "inputs larger than L2 (4 GiB per "
                    "direction), no flush", "parallelism": f"replicas x{world}" if world > 1
                    else "single GPU"},
@@ -588,16 +583,16 @@ def run_ours(args):
                      "peak": link["bidir"], "unit": "GB/s",
                      "frac": round(step_gbs / link["bidir"], 4),
                      "traffic": recorded_traffic("store", "llama8b"),
-                     "kernel": "kvx_segment_kernel store + load, concurrent on one link",
+                     "kernel": "kvx_exchange_kernel (store group g + load group g-1 in "
+                               "one launch)",
                      "peak_source": "measured in this run: 4 GiB pinned cudaMemcpyAsync H2D "
                                     "and D2H at once (both link directions)",
                      "algorithmic_bytes": 2 * N,
-                     "per_launch": {"store_ms": round(p_store_ms, 4),
-                                    "store_gbs": round(group_bytes / (p_store_ms * 1e-3) / GB, 2),
-                                    "load_ms": round(p_load_ms, 4),
-                                    "load_gbs": round(group_bytes / (p_load_ms * 1e-3) / GB, 2),
-                                    "bytes_per_launch": int(group_bytes),
-                                    "items_per_launch": items}},
+                     "per_launch": {"ms": round(p_x_ms, 4),
+                                    "gbs": round(2 * group_bytes / (p_x_ms * 1e-3) / GB, 2),
+                                    "bytes_per_launch": int(2 * group_bytes),
+                                    "items_per_launch": items, "ctas": ctas,
+                                    "threads": threads}},
         "sequential": {
             "note": "store then load on one stream, no overlap: per-direction rooflines",
             "step_gbs": round(2 * N / ((store_ms + load_ms) * 1e-3) / GB, 2),
@@ -607,7 +602,8 @@ def run_ours(args):
             "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
                      "peak": link["h2d"], "frac": round(load_gbs / link["h2d"], 4),
                      "traffic": recorded_traffic("load", "llama8b")}},
-        "cfg": {"store": cfg_store.as_dict(), "load": cfg_load.as_dict()},
+        "cfg": {"exchange": cfg_x.as_dict(), "store": cfg_store.as_dict(),
+                "load": cfg_load.as_dict()},
         "host_link_peak": {"h2d_gbs": link["h2d"], "d2h_gbs": link["d2h"],
                            "bidirectional_gbs": link["bidir"],
                            "nominal_gbs_per_direction": 450.0,
@@ -623,7 +619,6 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     host.close()
     kvx.kvx_destroy(ctx)
-    kvx.kvx_destroy(ctx_l)
 
 
 # ----------------------------------------------------------------------------- other workloads

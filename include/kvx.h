@@ -169,6 +169,7 @@ typedef struct kvx_ctx kvx_ctx;
 #define KVX_OP_LOAD 1         /* chunks in mapped pinned host memory -> pages */
 #define KVX_OP_GATHER_HBM 2   /* pages -> chunks in device memory */
 #define KVX_OP_SCATTER_HBM 3  /* chunks in device memory -> pages */
+#define KVX_OP_EXCHANGE 4     /* a store batch and a load batch in one launch (defaults only) */
 
 /* ---------------------------------------------------------------- context */
 
@@ -208,6 +209,22 @@ kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
                            int n_req, const kvx_chunk *chunks, int n_chunks,
                            int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
                            kvx_stream_t stream);
+
+/* exchange: a store batch and a load batch moved by ONE kernel launch, half of its CTAs
+ * on each direction, so both directions of the host link carry data at once (an eviction
+ * and a prefetch issued together: "Strata Guide", section "Implementation: GPU-Assisted
+ * I/O Kernels and Bubble-Filling Scheduler", steps "Dispatch Asynchronous Transfer" and
+ * "Asynchronous Eviction").  Each batch follows the rules of kvx_store_chunks /
+ * kvx_load_chunks; either may be empty.  The store's source slots and the load's
+ * destination slots must not meet for a common layer (checked at validation level 2).
+ * cfg->sm_cap counts the SMs of both directions together (default 32: 16 each). */
+kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
+                               const kvx_request *store_reqs, int n_store_req,
+                               const kvx_chunk *store_chunks, int n_store_chunks,
+                               const kvx_request *load_reqs, int n_load_req,
+                               const kvx_chunk *load_chunks, int n_load_chunks,
+                               int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                               kvx_stream_t stream);
 
 /* transform: the same gather (dir = KVX_DIR_GATHER) or scatter (KVX_DIR_SCATTER) with
  * the chunks in device memory: the explicit HBM-to-HBM layout pass that "Strata Guide",
@@ -303,23 +320,27 @@ kvx_status kvx_chunk_policy(const kvx_pool *pool, int layer_streaming, int64_t t
 
 /* ---------------------------------------------------------------- SM partitioning */
 
-/* Hard split of one GPU's SMs into an I/O partition and a compute partition, each a green
- * context with one non-blocking stream ("Tutti: Making SSD-Backed KV Cache Practical",
- * section 2 Design 2: SM partitioning into a compute domain and an I/O domain with green
- * contexts).  Transfers launched on the I/O stream run only on the I/O SMs; work launched
- * on the compute stream (wrap it with torch.cuda.ExternalStream, for instance) runs only
- * on the rest, so neither waits for the other's SMs.  io_sms is a minimum: the driver
- * rounds it up to its partition granularity (8 SMs on this GPU).  Priorities follow CUDA's
- * convention (lower = higher; 0 = default).  On failure msg (if msg_len > 0) holds the
- * failing driver step.  Requires a GPU and a driver with green-context support. */
+/* Hard split of one GPU's SMs into io_groups I/O partitions and one compute partition,
+ * each a green context with one non-blocking stream ("Tutti: Making SSD-Backed KV Cache
+ * Practical", section 2 Design 2: SM partitioning into a compute domain and an I/O domain
+ * with green contexts).  Transfers launched on an I/O stream run only on that partition's
+ * SMs; work launched on the compute stream (wrap it with torch.cuda.ExternalStream, for
+ * instance) runs only on the rest, so neither waits for the other's SMs.  Two I/O
+ * partitions give a store and a load that run at once fixed, disjoint SM sets.  io_sms is
+ * a minimum per I/O partition: the driver rounds it up to its partition granularity (8 SMs
+ * on this GPU).  Priorities follow CUDA's convention (lower = higher; 0 = default).  On
+ * failure msg (if msg_len > 0) holds the failing driver step.  Requires a GPU and a driver
+ * with green-context support. */
 typedef struct kvx_partition kvx_partition;
 
-kvx_status kvx_partition_create(int device, int io_sms, int io_priority, int compute_priority,
-                                kvx_partition **out, char *msg, size_t msg_len);
+kvx_status kvx_partition_create(int device, int io_groups, int io_sms, int io_priority,
+                                int compute_priority, kvx_partition **out, char *msg,
+                                size_t msg_len);
 
-/* The partition's streams and SM counts; any output may be NULL. */
-kvx_status kvx_partition_info(const kvx_partition *partition, kvx_stream_t *io_stream,
-                              kvx_stream_t *compute_stream, int *io_sms, int *compute_sms);
+/* Stream and SM count of partition `group`: 0 .. io_groups-1 are the I/O partitions,
+ * io_groups is the compute partition.  Either output may be NULL. */
+kvx_status kvx_partition_info(const kvx_partition *partition, int group, kvx_stream_t *stream,
+                              int *sms);
 
 /* Synchronize the device, then destroy the streams and green contexts. */
 void kvx_partition_destroy(kvx_partition *partition);

@@ -14,6 +14,7 @@
 // (section "Non-Intrusive Resource Sizing"); the HBM-only transform uses every SM.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -208,11 +209,9 @@ __device__ __forceinline__ void copy_segment(const Segment &sg, int64_t v, int l
 // one of p.batch consecutive segments in parallel and the warp then copies them back to
 // back, so the lookup latency of short segments overlaps instead of adding up.
 template <int U, int DIR, int HINT, bool BATCHED>
-__global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
+__device__ __forceinline__ void run_segments(const Plan &p, int64_t warp, int64_t n_warps,
+                                             int lane)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int64_t v = p.token_bytes;
     if (!BATCHED) {
         for (int64_t item = warp; item < p.total_items; item += n_warps) {
@@ -241,6 +240,37 @@ __global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
                     copy_segment<U, HINT>(s, v, lane);
             }
         }
+    }
+}
+
+template <int U, int DIR, int HINT, bool BATCHED>
+__global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    run_segments<U, DIR, HINT, BATCHED>(p, warp, n_warps, lane);
+}
+
+// Exchange: one launch moves a store batch (pages -> host chunks) and a load batch (host
+// chunks -> pages) at once.  Even CTAs run the store plan, odd CTAs the load plan, so the
+// block scheduler spreads both directions evenly over the SMs the launch gets instead of
+// giving each direction its own contiguous block of SMs (two separate kernels), which
+// lets the two directions of the host link run at full rate together.
+template <int U, bool BATCHED_S, bool BATCHED_L>
+__global__ void __launch_bounds__(1024, 1) kvx_exchange_kernel(const Plan ps, const Plan pl)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t wpc = blockDim.x >> 5;
+    const int64_t role_cta = blockIdx.x >> 1;
+    const int64_t warp = role_cta * wpc + (threadIdx.x >> 5);
+    if ((blockIdx.x & 1) == 0) {
+        const int64_t ctas = (int64_t(gridDim.x) + 1) >> 1;
+        run_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S>(ps, warp, ctas * wpc, lane);
+    } else {
+        const int64_t ctas = int64_t(gridDim.x) >> 1;
+        run_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L>(pl, warp, ctas * wpc,
+                                                                        lane);
     }
 }
 
@@ -458,6 +488,27 @@ KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1)
                      : pick_unroll<false>(unroll, dir, hint);
 }
 
+typedef void (*ExchangeFn)(Plan, Plan);
+
+template <int U>
+ExchangeFn pick_exchange_u(bool bs, bool bl)
+{
+    if (bs)
+        return bl ? kvx_exchange_kernel<U, true, true> : kvx_exchange_kernel<U, true, false>;
+    return bl ? kvx_exchange_kernel<U, false, true> : kvx_exchange_kernel<U, false, false>;
+}
+
+ExchangeFn pick_exchange(int unroll, int batch_s, int batch_l)
+{
+    switch (unroll) {
+    case 1: return pick_exchange_u<1>(batch_s > 1, batch_l > 1);
+    case 2: return pick_exchange_u<2>(batch_s > 1, batch_l > 1);
+    case 4: return pick_exchange_u<4>(batch_s > 1, batch_l > 1);
+    case 8: return pick_exchange_u<8>(batch_s > 1, batch_l > 1);
+    }
+    return nullptr;
+}
+
 }  // namespace
 
 // --------------------------------------------------------------------------------- host
@@ -557,6 +608,13 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
         c->threads = 1024;
         c->unroll = 8;
         c->store_hint = KVX_HINT_STREAMING;
+        break;
+    case KVX_OP_EXCHANGE:  // 16 SMs per direction, as for store and load alone
+        c->sm_cap = 32;
+        c->ctas_per_sm = 1;
+        c->threads = 1024;
+        c->unroll = 8;
+        c->store_hint = KVX_HINT_DEFAULT;
         break;
     default:  // HBM transform: the whole GPU, two 256-thread CTAs per SM, 8 loads in flight
         c->sm_cap = 0;
@@ -698,6 +756,88 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     return KVX_OK;
 }
 
+kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *sreqs,
+                           int n_sreq, const kvx_chunk *schunks, int n_schunks,
+                           const kvx_request *lreqs, int n_lreq, const kvx_chunk *lchunks,
+                           int n_lchunks, int layer_begin, int layer_end,
+                           const kvx_launch_cfg *user_cfg, kvx_stream_t stream)
+{
+    if (!ctx)
+        return KVX_ERR_INVALID_ARG;
+    ctx->last_items = 0;
+    ctx->last_ctas = 0;
+    ctx->last_threads = 0;
+    ctx->last_desc_bytes = 0;
+    kvx_launch_cfg cfg;
+    kvx_status st = resolve_cfg(ctx, KVX_OP_EXCHANGE, user_cfg, &cfg);
+    if (st != KVX_OK)
+        return st;
+    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "exchange runs the warp-segment mapping only");
+    st = kvx::validate_exchange(pool, sreqs, n_sreq, schunks, n_schunks, lreqs, n_lreq, lchunks,
+                                n_lchunks, layer_begin, layer_end, ctx->validation, true,
+                                ctx->err, sizeof ctx->err);
+    if (st != KVX_OK)
+        return st;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
+    const kvx::PackedLayout ls = kvx::packed_layout(pool, n_sreq, n_schunks);
+    const kvx::PackedLayout ll = kvx::packed_layout(pool, n_lreq, n_lchunks);
+    const size_t total = ls.total + ll.total;
+    if (total > ctx->slot_bytes)
+        return set_err(ctx, KVX_ERR_CAPACITY,
+                       "descriptors need %zu bytes, the context holds %zu per call; create it "
+                       "with a larger max_descriptor_bytes", total, ctx->slot_bytes);
+    Slot &slot = ctx->slots[ctx->next];
+    if (slot.used) {
+        cudaError_t e = cudaEventSynchronize(slot.done);
+        if (e != cudaSuccess)
+            return cuda_err(ctx, e, "waiting for a descriptor buffer");
+    }
+    Plan ps = kvx::pack(pool, sreqs, n_sreq, schunks, n_schunks, layer_begin, layer_end,
+                        KVX_DIR_GATHER, ls, slot.host, slot.dev);
+    Plan pl = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
+                        KVX_DIR_SCATTER, ll, slot.host + ls.total, slot.dev + ls.total);
+    ps.status = pl.status = ctx->status_dev;
+    if (cfg.batch > 0)
+        ps.batch = pl.batch = cfg.batch;
+    if (ps.total_items + pl.total_items == 0)
+        return KVX_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, total, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "descriptor copy");
+    // sm_cap covers both directions: half of the CTAs per direction.
+    const int64_t warps_per_cta = cfg.threads / 32;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    const int64_t per_dir = (int64_t(sms) * cfg.ctas_per_sm + 1) / 2;
+    auto needed = [&](const Plan &p) {
+        const int64_t per_cta = warps_per_cta * p.batch;
+        return (p.total_items + per_cta - 1) / per_cta;
+    };
+    int64_t role = std::max(needed(ps), needed(pl));
+    if (role > per_dir)
+        role = per_dir;
+    const int64_t ctas = 2 * role;
+    ExchangeFn fn = pick_exchange(cfg.unroll, ps.batch, pl.batch);
+    void *args[] = {&ps, &pl};
+    e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
+                         dim3(unsigned(cfg.threads)), args, 0, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "kernel launch");
+    e = cudaEventRecord(slot.done, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "event record");
+    slot.used = true;
+    ctx->next = (ctx->next + 1) % kSlots;
+    ctx->last_items = ps.total_items + pl.total_items;
+    ctx->last_ctas = int32_t(ctas);
+    ctx->last_threads = cfg.threads;
+    ctx->last_desc_bytes = int64_t(total);
+    return KVX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -777,7 +917,7 @@ kvx_status kvx_set_validation(kvx_ctx *ctx, int level)
 
 kvx_status kvx_default_launch_cfg(const kvx_ctx *ctx, int op, kvx_launch_cfg *cfg)
 {
-    if (!ctx || !cfg || op < KVX_OP_STORE || op > KVX_OP_SCATTER_HBM)
+    if (!ctx || !cfg || op < KVX_OP_STORE || op > KVX_OP_EXCHANGE)
         return KVX_ERR_INVALID_ARG;
     defaults_for(ctx, op, cfg);
     return KVX_OK;
@@ -797,6 +937,19 @@ kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
 {
     return launch(ctx, KVX_OP_LOAD, pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                   cfg, stream);
+}
+
+kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
+                               const kvx_request *store_reqs, int n_store_req,
+                               const kvx_chunk *store_chunks, int n_store_chunks,
+                               const kvx_request *load_reqs, int n_load_req,
+                               const kvx_chunk *load_chunks, int n_load_chunks,
+                               int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                               kvx_stream_t stream)
+{
+    return launch_exchange(ctx, pool, store_reqs, n_store_req, store_chunks, n_store_chunks,
+                           load_reqs, n_load_req, load_chunks, n_load_chunks, layer_begin,
+                           layer_end, cfg, stream);
 }
 
 kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,

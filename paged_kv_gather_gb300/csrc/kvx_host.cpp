@@ -221,6 +221,54 @@ kvx_status validate(const kvx_pool *pool, const kvx_request *reqs, int n_req,
     return KVX_OK;
 }
 
+kvx_status validate_exchange(const kvx_pool *pool, const kvx_request *sreqs, int n_sreq,
+                             const kvx_chunk *schunks, int n_schunks, const kvx_request *lreqs,
+                             int n_lreq, const kvx_chunk *lchunks, int n_lchunks,
+                             int layer_begin, int layer_end, int level, bool have_gpu,
+                             char *msg, size_t len)
+{
+    kvx_status st = validate(pool, sreqs, n_sreq, schunks, n_schunks, layer_begin, layer_end,
+                             KVX_OP_STORE, level, have_gpu, msg, len);
+    if (st != KVX_OK)
+        return st;
+    st = validate(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end, KVX_OP_LOAD,
+                  level, have_gpu, msg, len);
+    if (st != KVX_OK || level < 2)
+        return st;
+    // A slot the store reads must not be one the load writes, for any common layer.
+    auto slots = [&](const kvx_request *reqs, const kvx_chunk *chunks, int n) {
+        std::vector<SlotUse> out;
+        for (int c = 0; c < n; ++c) {
+            const int32_t *pt = reqs[chunks[c].request].page_table_host;
+            int lo, hi;
+            chunk_layers(chunks[c], layer_begin, layer_end, &lo, &hi);
+            if (!pt || lo >= hi)
+                continue;
+            for (int32_t t = chunks[c].token_begin;
+                 t < chunks[c].token_begin + chunks[c].n_tokens; ++t)
+                out.push_back({(int64_t)pt[t / pool->page_size] * pool->page_size +
+                                   t % pool->page_size, lo, hi, c});
+        }
+        std::sort(out.begin(), out.end(), [](const SlotUse &a, const SlotUse &b) {
+            return a.slot < b.slot;
+        });
+        return out;
+    };
+    const std::vector<SlotUse> reads = slots(sreqs, schunks, n_schunks);
+    const std::vector<SlotUse> writes = slots(lreqs, lchunks, n_lchunks);
+    size_t w = 0;
+    for (const SlotUse &r : reads) {
+        while (w < writes.size() && writes[w].slot < r.slot)
+            ++w;
+        for (size_t k = w; k < writes.size() && writes[k].slot == r.slot; ++k)
+            if (writes[k].lo < r.hi && r.lo < writes[k].hi)
+                return fail(KVX_ERR_OVERLAP, msg, len,
+                            "store chunk %d reads page slot %lld that load chunk %d writes",
+                            r.chunk, (long long)r.slot, writes[k].chunk);
+    }
+    return KVX_OK;
+}
+
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 PackedLayout packed_layout(const kvx_pool *pool, int n_req, int n_chunks)

@@ -79,6 +79,15 @@ kvx_status validate(const kvx_pool *pool, const kvx_request *reqs, int n_req,
                     const kvx_chunk *chunks, int n_chunks, int layer_begin, int layer_end,
                     int op, int level, bool have_gpu, char *msg, size_t msg_len);
 
+// An exchange (store batch + load batch in one launch): each batch validated as its own
+// operation, and, at level 2, no page slot read by the store and written by the load for a
+// common layer.
+kvx_status validate_exchange(const kvx_pool *pool, const kvx_request *sreqs, int n_sreq,
+                             const kvx_chunk *schunks, int n_schunks, const kvx_request *lreqs,
+                             int n_lreq, const kvx_chunk *lchunks, int n_lchunks,
+                             int layer_begin, int layer_end, int level, bool have_gpu,
+                             char *msg, size_t msg_len);
+
 PackedLayout packed_layout(const kvx_pool *pool, int n_req, int n_chunks);
 
 // Fill `block` (host memory of at least layout.total bytes) with descriptors whose device

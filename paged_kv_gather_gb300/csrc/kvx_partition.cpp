@@ -3,11 +3,12 @@
 // "Tutti: Making SSD-Backed KV Cache Practical for Long-Context LLM Serving", section 2
 // Design 2, splits the GPU's SMs into a compute domain and an I/O domain with NVIDIA green
 // contexts so that the I/O kernel never competes with compute for SMs.  Here the device's
-// SM resource is split into an I/O partition of at least `io_sms` SMs (the driver rounds
-// up to its partition granularity) and a compute partition with the rest; each becomes a
-// green context with one non-blocking stream.  Transfers launched on the I/O stream run
-// only on the I/O SMs; anything launched on the compute stream (a GEMM, attention) runs
-// only on the others.
+// SM resource is split into `io_groups` I/O partitions of at least `io_sms` SMs each (the
+// driver rounds up to its partition granularity) and a compute partition with the rest;
+// each becomes a green context with one non-blocking stream.  Transfers launched on an
+// I/O stream run only on that partition's SMs; anything launched on the compute stream (a
+// GEMM, attention) runs only on the others.  Two I/O partitions keep a store and a load
+// that run at once on fixed, disjoint SM sets.
 //
 // The driver entry points are looked up at run time through the CUDA runtime, so the
 // library still loads on machines without a GPU driver.
@@ -21,13 +22,12 @@
 #include "kvx_internal.h"
 
 struct kvx_partition {
+    static const int kMaxGroups = 8;
     int device = 0;
-    CUgreenCtx io_ctx = nullptr;
-    CUgreenCtx compute_ctx = nullptr;
-    CUstream io_stream = nullptr;
-    CUstream compute_stream = nullptr;
-    int io_sms = 0;
-    int compute_sms = 0;
+    int groups = 0;  // I/O groups; the compute partition is index `groups`
+    CUgreenCtx ctx[kMaxGroups + 1] = {};
+    CUstream stream[kMaxGroups + 1] = {};
+    int sms[kMaxGroups + 1] = {};
 };
 
 namespace {
@@ -93,26 +93,27 @@ kvx_status fail(char *msg, size_t len, const char *fmt, ...)
 
 void release(const Driver &d, kvx_partition *p)
 {
-    if (p->io_stream)
-        d.stream_destroy(p->io_stream);
-    if (p->compute_stream)
-        d.stream_destroy(p->compute_stream);
-    if (p->io_ctx)
-        d.green_destroy(p->io_ctx);
-    if (p->compute_ctx)
-        d.green_destroy(p->compute_ctx);
+    for (int g = 0; g <= kvx_partition::kMaxGroups; ++g) {
+        if (p->stream[g])
+            d.stream_destroy(p->stream[g]);
+        if (p->ctx[g])
+            d.green_destroy(p->ctx[g]);
+        p->stream[g] = nullptr;
+        p->ctx[g] = nullptr;
+    }
 }
 
 }  // namespace
 
 extern "C" {
 
-kvx_status kvx_partition_create(int device, int io_sms, int io_priority, int compute_priority,
-                                kvx_partition **out, char *msg, size_t msg_len)
+kvx_status kvx_partition_create(int device, int io_groups, int io_sms, int io_priority,
+                                int compute_priority, kvx_partition **out, char *msg,
+                                size_t msg_len)
 {
     if (msg && msg_len)
         msg[0] = '\0';
-    if (!out || io_sms <= 0)
+    if (!out || io_sms <= 0 || io_groups <= 0 || io_groups > kvx_partition::kMaxGroups)
         return KVX_ERR_INVALID_ARG;
     *out = nullptr;
     Driver d;
@@ -126,49 +127,45 @@ kvx_status kvx_partition_create(int device, int io_sms, int io_priority, int com
     }
     kvx_partition *p = new kvx_partition();
     p->device = device;
+    p->groups = io_groups;
     CUdevice dev;
-    CUdevResource all, io, rest;
+    CUdevResource all, io[kvx_partition::kMaxGroups], rest;
     std::memset(&all, 0, sizeof all);
-    std::memset(&io, 0, sizeof io);
+    std::memset(io, 0, sizeof io);
     std::memset(&rest, 0, sizeof rest);
-    unsigned int groups = 1;
-    CUdevResourceDesc io_desc = nullptr, rest_desc = nullptr;
-    CUresult r = d.device_get(&dev, device);
+    unsigned int groups = unsigned(io_groups);
     const char *step = "cuDeviceGet";
+    CUresult r = d.device_get(&dev, device);
     if (r == CUDA_SUCCESS) {
         step = "cuDeviceGetDevResource";
         r = d.get_dev_resource(dev, &all, CU_DEV_RESOURCE_TYPE_SM);
     }
     if (r == CUDA_SUCCESS) {
         step = "cuDevSmResourceSplitByCount";
-        r = d.split_by_count(&io, &groups, &all, &rest, 0, unsigned(io_sms));
+        r = d.split_by_count(io, &groups, &all, &rest, 0, unsigned(io_sms));
     }
-    if (r == CUDA_SUCCESS && (groups != 1 || rest.sm.smCount == 0)) {
-        release(d, p);
+    if (r == CUDA_SUCCESS && (groups != unsigned(io_groups) || rest.sm.smCount == 0)) {
         delete p;
         if (prev >= 0)
             cudaSetDevice(prev);
-        return fail(msg, msg_len, "cannot split %u SMs into %d I/O SMs and a remainder",
-                    all.sm.smCount, io_sms);
+        return fail(msg, msg_len, "cannot split %u SMs into %d groups of %d I/O SMs and a "
+                    "remainder", all.sm.smCount, io_groups, io_sms);
     }
-    if (r == CUDA_SUCCESS) {
+    for (int g = 0; g <= io_groups && r == CUDA_SUCCESS; ++g) {
+        CUdevResource *res = g < io_groups ? &io[g] : &rest;
+        CUdevResourceDesc desc = nullptr;
         step = "cuDevResourceGenerateDesc";
-        r = d.generate_desc(&io_desc, &io, 1);
-        if (r == CUDA_SUCCESS)
-            r = d.generate_desc(&rest_desc, &rest, 1);
-    }
-    if (r == CUDA_SUCCESS) {
-        step = "cuGreenCtxCreate";
-        r = d.green_create(&p->io_ctx, io_desc, dev, CU_GREEN_CTX_DEFAULT_STREAM);
-        if (r == CUDA_SUCCESS)
-            r = d.green_create(&p->compute_ctx, rest_desc, dev, CU_GREEN_CTX_DEFAULT_STREAM);
-    }
-    if (r == CUDA_SUCCESS) {
-        step = "cuGreenCtxStreamCreate";
-        r = d.green_stream_create(&p->io_stream, p->io_ctx, CU_STREAM_NON_BLOCKING, io_priority);
-        if (r == CUDA_SUCCESS)
-            r = d.green_stream_create(&p->compute_stream, p->compute_ctx, CU_STREAM_NON_BLOCKING,
-                                      compute_priority);
+        r = d.generate_desc(&desc, res, 1);
+        if (r == CUDA_SUCCESS) {
+            step = "cuGreenCtxCreate";
+            r = d.green_create(&p->ctx[g], desc, dev, CU_GREEN_CTX_DEFAULT_STREAM);
+        }
+        if (r == CUDA_SUCCESS) {
+            step = "cuGreenCtxStreamCreate";
+            r = d.green_stream_create(&p->stream[g], p->ctx[g], CU_STREAM_NON_BLOCKING,
+                                      g < io_groups ? io_priority : compute_priority);
+        }
+        p->sms[g] = int(res->sm.smCount);
     }
     if (prev >= 0)
         cudaSetDevice(prev);
@@ -177,25 +174,19 @@ kvx_status kvx_partition_create(int device, int io_sms, int io_priority, int com
         delete p;
         return fail(msg, msg_len, "%s failed with CUresult %d", step, int(r));
     }
-    p->io_sms = int(io.sm.smCount);
-    p->compute_sms = int(rest.sm.smCount);
     *out = p;
     return KVX_OK;
 }
 
-kvx_status kvx_partition_info(const kvx_partition *p, kvx_stream_t *io_stream,
-                              kvx_stream_t *compute_stream, int *io_sms, int *compute_sms)
+kvx_status kvx_partition_info(const kvx_partition *p, int group, kvx_stream_t *stream,
+                              int *sms)
 {
-    if (!p)
+    if (!p || group < 0 || group > p->groups)
         return KVX_ERR_INVALID_ARG;
-    if (io_stream)
-        *io_stream = reinterpret_cast<kvx_stream_t>(p->io_stream);
-    if (compute_stream)
-        *compute_stream = reinterpret_cast<kvx_stream_t>(p->compute_stream);
-    if (io_sms)
-        *io_sms = p->io_sms;
-    if (compute_sms)
-        *compute_sms = p->compute_sms;
+    if (stream)
+        *stream = reinterpret_cast<kvx_stream_t>(p->stream[group]);
+    if (sms)
+        *sms = p->sms[group];
     return KVX_OK;
 }
 

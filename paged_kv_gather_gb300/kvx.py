@@ -59,6 +59,7 @@ KVX_OP_STORE = 0
 KVX_OP_LOAD = 1
 KVX_OP_GATHER_HBM = 2
 KVX_OP_SCATTER_HBM = 3
+KVX_OP_EXCHANGE = 4
 
 # ---------------------------------------------------------------------------- structs
 
@@ -129,6 +130,9 @@ _proto("kvx_set_validation", _c.c_int, [_ctx_t, _c.c_int])
 _proto("kvx_default_launch_cfg", _c.c_int, [_ctx_t, _c.c_int, _P(kvx_launch_cfg)])
 _proto("kvx_store_chunks", _c.c_int, [_ctx_t, *_batch, _P(kvx_launch_cfg), _c.c_void_p])
 _proto("kvx_load_chunks", _c.c_int, [_ctx_t, *_batch, _P(kvx_launch_cfg), _c.c_void_p])
+_proto("kvx_exchange_chunks", _c.c_int,
+       [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int,
+        _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _P(kvx_launch_cfg), _c.c_void_p])
 _proto("kvx_transform_hbm", _c.c_int,
        [_ctx_t, _c.c_int, *_batch, _P(kvx_launch_cfg), _c.c_void_p])
 _proto("kvx_dma_baseline", _c.c_int,
@@ -152,16 +156,16 @@ _proto("kvx_estimate_us", _c.c_int, [_P(kvx_link_model), _c.c_int, _c.c_int64,
                                      _P(kvx_launch_cfg), _P(_c.c_double)])
 _proto("kvx_estimate_stream_us", _c.c_int, [_c.c_double, _c.c_double, _c.c_int,
                                             _P(_c.c_double), _P(_c.c_double)])
-_proto("kvx_partition_create", _c.c_int, [_c.c_int, _c.c_int, _c.c_int, _c.c_int,
+_proto("kvx_partition_create", _c.c_int, [_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
                                           _P(_c.c_void_p), _c.c_char_p, _c.c_size_t])
-_proto("kvx_partition_info", _c.c_int, [_c.c_void_p, _P(_c.c_void_p), _P(_c.c_void_p),
-                                        _P(_c.c_int), _P(_c.c_int)])
+_proto("kvx_partition_info", _c.c_int, [_c.c_void_p, _c.c_int, _P(_c.c_void_p),
+                                        _P(_c.c_int)])
 _proto("kvx_partition_destroy", None, [_c.c_void_p])
 _proto("kvx_load_chunks_noalloc", _c.c_int, [*_batch, _P(kvx_launch_cfg), _c.c_void_p,
                                              _c.c_void_p])
 
 EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_launch_cfg",
-            "kvx_store_chunks", "kvx_load_chunks", "kvx_transform_hbm", "kvx_dma_baseline",
+            "kvx_store_chunks", "kvx_load_chunks", "kvx_exchange_chunks", "kvx_transform_hbm", "kvx_dma_baseline",
             "kvx_get_status", "kvx_last_error", "kvx_last_launch", "kvx_validate",
             "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
@@ -325,6 +329,21 @@ def kvx_load_chunks(ctx, pool: Pool, reqs, chunks, layer_begin: int = 0,
                                                        layer_end), _cfg_ptr(cfg), stream))
 
 
+def kvx_exchange_chunks(ctx, pool: Pool, store_reqs, store_chunks, load_reqs, load_chunks,
+                        layer_begin: int = 0, layer_end: Optional[int] = None,
+                        cfg: Optional[kvx_launch_cfg] = None, stream: int = 0) -> None:
+    """One launch that stores store_chunks and loads load_chunks (either may be empty)."""
+    srp, nsr = _arr_ptr(store_reqs, REQUEST_DTYPE)
+    scp, nsc = _arr_ptr(store_chunks, CHUNK_DTYPE)
+    lrp, nlr = _arr_ptr(load_reqs, REQUEST_DTYPE)
+    lcp, nlc = _arr_ptr(load_chunks, CHUNK_DTYPE)
+    if layer_end is None:
+        layer_end = pool.c.num_layers
+    _check(ctx, _lib.kvx_exchange_chunks(ctx, ctypes.byref(pool.c), srp, nsr, scp, nsc, lrp, nlr,
+                                         lcp, nlc, layer_begin, layer_end, _cfg_ptr(cfg),
+                                         stream))
+
+
 def kvx_transform_hbm(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,
                       layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
                       stream: int = 0) -> None:
@@ -436,15 +455,25 @@ def kvx_estimate_stream_us(io_us: float, compute_us: float, n_layers: int) -> Tu
 
 
 class Partition:
-    """An I/O / compute split of the GPU's SMs (green contexts); see kvx_partition_create."""
+    """I/O partitions plus one compute partition of the GPU's SMs (green contexts).
 
-    def __init__(self, handle, io_stream: int, compute_stream: int, io_sms: int,
-                 compute_sms: int):
+    io_streams[g] / io_sms[g] for g < io_groups; compute_stream / compute_sms for the rest.
+    """
+
+    def __init__(self, handle, streams, sms):
         self.handle = handle
-        self.io_stream = io_stream
-        self.compute_stream = compute_stream
-        self.io_sms = io_sms
-        self.compute_sms = compute_sms
+        self.io_streams = streams[:-1]
+        self.io_sms_list = sms[:-1]
+        self.compute_stream = streams[-1]
+        self.compute_sms = sms[-1]
+
+    @property
+    def io_stream(self) -> int:
+        return self.io_streams[0]
+
+    @property
+    def io_sms(self) -> int:
+        return self.io_sms_list[0]
 
     def close(self):
         if self.handle:
@@ -453,24 +482,29 @@ class Partition:
 
 
 def kvx_partition_create(device: int, io_sms: int, io_priority: int = -1,
-                         compute_priority: int = 0) -> Partition:
+                         compute_priority: int = 0, io_groups: int = 1) -> Partition:
     h = ctypes.c_void_p()
     msg = ctypes.create_string_buffer(256)
-    st = _lib.kvx_partition_create(device, io_sms, io_priority, compute_priority,
+    st = _lib.kvx_partition_create(device, io_groups, io_sms, io_priority, compute_priority,
                                    ctypes.byref(h), msg, len(msg))
     if st != KVX_OK:
         raise KvxError(st, msg.value.decode())
-    io_s, co_s = ctypes.c_void_p(), ctypes.c_void_p()
-    n_io, n_co = ctypes.c_int(), ctypes.c_int()
-    st = _lib.kvx_partition_info(h, ctypes.byref(io_s), ctypes.byref(co_s), ctypes.byref(n_io),
-                                 ctypes.byref(n_co))
-    if st != KVX_OK:
-        raise KvxError(st, "kvx_partition_info")
-    return Partition(h, io_s.value or 0, co_s.value or 0, n_io.value, n_co.value)
+    streams, sms = [], []
+    for g in range(io_groups + 1):
+        s_ = ctypes.c_void_p()
+        n = ctypes.c_int()
+        st = _lib.kvx_partition_info(h, g, ctypes.byref(s_), ctypes.byref(n))
+        if st != KVX_OK:
+            raise KvxError(st, "kvx_partition_info")
+        streams.append(s_.value or 0)
+        sms.append(n.value)
+    return Partition(h, streams, sms)
 
 
-def kvx_partition_info(p: Partition):
-    return p.io_stream, p.compute_stream, p.io_sms, p.compute_sms
+def kvx_partition_info(p: Partition, group: int):
+    if group < len(p.io_streams):
+        return p.io_streams[group], p.io_sms_list[group]
+    return p.compute_stream, p.compute_sms
 
 
 def kvx_partition_destroy(handle) -> None:

