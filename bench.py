@@ -65,7 +65,7 @@ def parse():
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
-                   choices=["store", "load", "gather", "scatter"],
+                   choices=["store", "load", "gather", "scatter", "exchange"],
                    help="operation of --workload profile_small")
     p.add_argument("--groups", type=int, default=16,
                    help="chunk groups of the pipelined store/load round trip")
@@ -199,8 +199,11 @@ def source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on this source."""
+def recorded_traffic(kernel: str, workload: str, groups: int = 1):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this source.
+
+    Exchange launches of the headline move 1/groups of the request each way; the recorded
+    figure is for a launch moving 4 GiB each way and scales with the bytes moved."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -209,7 +212,7 @@ def recorded_traffic(kernel: str, workload: str):
         f = dict(x.split("=", 1) for x in line.split() if "=" in x)
         if f.get("kernel") == kernel and f.get("workload") == workload and \
                 f.get("source_sha") == sha:
-            return float(f["dram_bytes_per_launch"])
+            return float(f["dram_bytes_per_launch"]) / groups
     return None
 
 
@@ -582,7 +585,7 @@ def run_ours(args):
         "roofline": {"bound": "host_link", "achieved": round(step_gbs, 2),
                      "peak": link["bidir"], "unit": "GB/s",
                      "frac": round(step_gbs / link["bidir"], 4),
-                     "traffic": recorded_traffic("store", "llama8b"),
+                     "traffic": recorded_traffic("exchange", "llama8b", args.groups),
                      "kernel": "kvx_exchange_kernel (store group g + load group g-1 in "
                                "one launch)",
                      "peak_source": "measured in this run: 4 GiB pinned cudaMemcpyAsync H2D "
@@ -1171,15 +1174,19 @@ def run_profile_small(args, kvx, wl):
     rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
     ctx = kvx.kvx_create(0)
     sh = torch.cuda.current_stream().cuda_stream
-    if args.profile_op in ("store", "load"):
+    if args.profile_op in ("store", "load", "exchange"):
         buf = kvx.HostBuffer(w.store_arena_bytes)
         buf.array[:] = 0
         ch = kvx.chunks_array(w.store_chunks, buf.ptr)
     else:
         dchunk = torch.zeros(w.store_arena_bytes, dtype=torch.uint8, device="cuda")
         ch = kvx.chunks_array(w.store_chunks, dchunk.data_ptr())
+    half = len(w.store_chunks) // 2
     for _ in range(3):
-        if args.profile_op == "store":
+        if args.profile_op == "exchange":  # store the first half, load the second half
+            kvx.kvx_exchange_chunks(ctx, pool, rs, np.ascontiguousarray(ch[:half]), rd,
+                                    np.ascontiguousarray(ch[half:]), stream=sh)
+        elif args.profile_op == "store":
             kvx.kvx_store_chunks(ctx, pool, rs, ch, stream=sh)
         elif args.profile_op == "load":
             kvx.kvx_load_chunks(ctx, pool, rd, ch, stream=sh)

@@ -217,7 +217,7 @@ kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
  * "Asynchronous Eviction").  Each batch follows the rules of kvx_store_chunks /
  * kvx_load_chunks; either may be empty.  The store's source slots and the load's
  * destination slots must not meet for a common layer (checked at validation level 2).
- * cfg->sm_cap counts the SMs of both directions together (default 32: 16 each). */
+ * cfg->sm_cap counts the SMs of both directions together (default 40: 20 each). */
 kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
                                const kvx_request *store_reqs, int n_store_req,
                                const kvx_chunk *store_chunks, int n_store_chunks,

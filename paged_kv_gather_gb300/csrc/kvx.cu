@@ -609,8 +609,8 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
         c->unroll = 8;
         c->store_hint = KVX_HINT_STREAMING;
         break;
-    case KVX_OP_EXCHANGE:  // 16 SMs per direction, as for store and load alone
-        c->sm_cap = 32;
+    case KVX_OP_EXCHANGE:  // 20 SMs per direction
+        c->sm_cap = 40;
         c->ctas_per_sm = 1;
         c->threads = 1024;
         c->unroll = 8;
