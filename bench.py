@@ -850,6 +850,11 @@ def run_qwen7b(args, kvx, wl):
         spans.append((start.elapsed_time(ea), start.elapsed_time(eb)))
     assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
     assert kvx.kvx_get_status(ctx_b, sb.cuda_stream) == 0
+    # The same two batches in one exchange launch.
+    xcfg = kvx.kvx_default_launch_cfg(ctx_a, kvx.KVX_OP_EXCHANGE)
+    x_ms = _timed(sa, lambda: kvx.kvx_exchange_chunks(ctx_a, pool, reqs, ch_st, reqs, ch_ld,
+                                                       cfg=xcfg, stream=sa.cuda_stream), 5)
+    assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
     la = statistics.median(x[0] for x in spans)
     sbm = statistics.median(x[1] for x in spans)
     both = statistics.median(max(x) for x in spans)
@@ -877,6 +882,8 @@ def run_qwen7b(args, kvx, wl):
            "concurrent_store_gbs": round(Ns / (sbm * 1e-3) / GB, 2),
            "concurrent_aggregate_gbs": round((Nl + Ns) / (both * 1e-3) / GB, 2),
            "concurrent_ms": round(both, 3),
+           "exchange_one_launch_ms": round(x_ms, 3),
+           "exchange_one_launch_aggregate_gbs": round((Nl + Ns) / (x_ms * 1e-3) / GB, 2),
            "memcpy_bidirectional_gbs": round(2 * (4 << 30) / statistics.median(bid) / GB, 2)})
     ld.close()
     st.close()
@@ -983,22 +990,21 @@ def run_transform_sweep(args, kvx, wl):
     sh = stream.cuda_stream
     N = w.store_bytes()
     hbm, _ = peaks()
-    shapes = [(0, 1, 512, 8, 1, 0), (0, 2, 256, 8, 1, 0), (0, 1, 384, 8, 1, 0),
-              (0, 3, 256, 8, 1, 0), (0, 4, 128, 8, 1, 0), (0, 3, 128, 8, 1, 0),
-              (0, 2, 384, 8, 1, 0), (0, 6, 64, 8, 1, 0), (0, 2, 256, 8, 0, 0),
-              (0, 4, 256, 4, 1, 0), (0, 2, 192, 8, 1, 0),
-              (1, 3, 32, 2, 0, 32768), (1, 2, 32, 3, 0, 32768)] * 2
-    for mapping, ctas, threads, unroll, hint, stage in shapes:
+    shapes = [(0, 2, 256, 8, 1, 0, 1), (0, 2, 256, 8, 1, 0, 2), (0, 2, 256, 8, 1, 0, 4),
+              (0, 1, 512, 8, 1, 0, 1), (0, 1, 512, 8, 1, 0, 2), (0, 4, 128, 8, 1, 0, 1),
+              (0, 4, 128, 8, 1, 0, 2), (0, 2, 256, 4, 1, 0, 2), (0, 3, 256, 8, 1, 0, 2),
+              (1, 3, 32, 2, 0, 32768, 0), (1, 2, 32, 3, 0, 32768, 0)] * 2
+    for mapping, ctas, threads, unroll, hint, stage, batch in shapes:
         if True:
             row = {"workload": "llama8b_transform_sweep",
                    "mapping": "bulk" if mapping else "segment", "ctas_per_sm": ctas,
                    "threads": threads, "unroll": unroll, "store_hint": hint,
-                   "stage_bytes": stage}
+                   "stage_bytes": stage, "batch": batch}
             for name, d, rq in (("gather", kvx.KVX_DIR_GATHER, rs),
                                 ("scatter", kvx.KVX_DIR_SCATTER, rd)):
                 c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM)
                 c.sm_cap, c.ctas_per_sm, c.threads, c.unroll, c.store_hint = 0, ctas, threads, unroll, hint
-                c.mapping, c.stage_bytes = mapping, stage
+                c.mapping, c.stage_bytes, c.batch = mapping, stage, batch
                 ms = _timed(stream, lambda: kvx.kvx_transform_hbm(ctx, d, pool, rq, ch, 0,
                                                                   s.num_layers, c, sh), 10, 3)
                 gbs = 2 * N / (ms * 1e-3) / GB

@@ -158,8 +158,9 @@ typedef struct kvx_launch_cfg {
     int32_t stage_bytes;  /* bulk mapping: bytes per shared-memory stage, a multiple of 16;
                              stages x stage_bytes <= 220 KiB.  0 = default (32 KiB) */
     int32_t batch;        /* warp-segment mapping: page segments a warp resolves at once,
-                             one per lane (1..32); 0 = automatic (about 32 KiB of segments,
-                             1 when a page segment is >= 16 KiB) */
+                             one per lane (1..32); 0 = automatic (about 32 KiB of segments;
+                             for page segments >= 16 KiB, 1 for host transfers and 2 for
+                             the HBM transform) */
 } kvx_launch_cfg;
 
 typedef struct kvx_ctx kvx_ctx;

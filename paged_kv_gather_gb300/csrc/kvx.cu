@@ -711,6 +711,8 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     plan.status = ctx->status_dev;
     if (cfg.batch > 0)
         plan.batch = cfg.batch;
+    else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && plan.batch == 1)
+        plan.batch = 2;  // HBM transform: overlap the lookup of two long segments per warp
     if (plan.total_items == 0)
         return KVX_OK;
 

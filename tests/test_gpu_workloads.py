@@ -246,6 +246,33 @@ def test_qwen7b_batched_concurrent_load_and_store_full_size(ctx):
     hp.close()
 
 
+def test_qwen7b_batched_partial_hits_in_one_exchange_launch(ctx):
+    """The batched load and store of the 64 partial-hit requests in one exchange launch."""
+    w = wl.qwen7b_batch()
+    s = w.shape
+    pools = _pools(s, w.seed)
+    hp = HostPool(pools, s.page_size)
+    reqs = _requests(w.load_requests)
+    ld = kvx.HostBuffer(w.load_arena_bytes)
+    _fill_host(ld.array, w.load_arena_bytes, s, w.seed, stream_id=2)
+    st = kvx.HostBuffer(w.store_arena_bytes + 4096)
+    st.array[:] = CANARY
+    sh = torch.cuda.current_stream().cuda_stream
+    kvx.kvx_exchange_chunks(ctx, kvx.Pool.from_tensor(pools, s.page_size), reqs.array,
+                            kvx.chunks_array(w.store_chunks, st.ptr), reqs.array,
+                            kvx.chunks_array(w.load_chunks, ld.ptr), stream=sh)
+    torch.cuda.synchronize()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    expect = np.full(w.store_arena_bytes + 4096, CANARY, np.uint8)
+    oracle.store(hp.pool, reqs.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
+    assert_bytes_equal(st.array, expect, "qwen7b exchange store")
+    oracle.load(hp.pool, reqs.oracle(), oracle_chunks(w.load_chunks, ld.array), threads=16)
+    _compare_pool(pools, hp.pool, "qwen7b exchange load")
+    ld.close()
+    st.close()
+    hp.close()
+
+
 # ----------------------------------------------------------------------------- mla_sweep
 
 @pytest.mark.parametrize("page_size", wl.MLA_PAGE_SIZES)
