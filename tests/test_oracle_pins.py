@@ -489,3 +489,27 @@ def test_oracle_rejects_bad_inputs():
         oracle.store(pool, [Request(good, 8)], make_chunks([(0, 0, 8, 1, 2, 0)], KV, v))
     with pytest.raises(ValueError, match="layer range"):
         oracle.store(pool, [Request(good, 8)], make_chunks([(0, 0, 8, 0, 2, 0)], KV, v), 0, 3)
+
+
+def test_chunk_parallel_timing_wrapper_matches_single_thread():
+    """The CPU baseline runs the oracle over disjoint chunk ranges on host threads; the bytes
+    must be those of the single-threaded loops."""
+    rng = np.random.default_rng(21)
+    L, KV, P, v, T = 3, 2, 8, 64, 500
+    n = -(-T // P)
+    pt = rng.permutation(2 * n)[:n].astype(np.int32)
+    pool = Pool([[rng.integers(0, 256, (2 * n, P, v), dtype=np.uint8) for _ in range(L)]
+                 for _ in range(KV)], P)
+    specs = [(0, a, min(37, T - a), 0, L, (a // 37) % 3) for a in range(0, T, 37)]
+    one = make_chunks(specs, KV, v)
+    many = make_chunks(specs, KV, v)
+    oracle.store(pool, [Request(pt, T)], one)
+    oracle.store(pool, [Request(pt, T)], many, threads=5)
+    for a, b in zip(one, many):
+        np.testing.assert_array_equal(a.buf, b.buf)
+    p1, p2 = empty_pool(L, KV, 2 * n, P, v), empty_pool(L, KV, 2 * n, P, v)
+    oracle.load(p1, [Request(pt, T)], one, 1, 3)
+    oracle.load(p2, [Request(pt, T)], one, 1, 3, threads=4)
+    for k in range(KV):
+        for l in range(L):
+            np.testing.assert_array_equal(p1.pools[k][l], p2.pools[k][l])
