@@ -1099,6 +1099,28 @@ def run_mla_blocks(args, kvx, wl):
                 kvx.kvx_load_chunks(ctx, pool, rd, ch, l, l + 1, stream=sh)
 
         ld_ms = _timed(stream, per_layer, 5)
+        # The same per-layer loads as prepared plans, launched one by one and as one graph.
+        plans = [kvx.kvx_plan_create(ctx, kvx.KVX_OP_LOAD, pool, rd, ch, l, l + 1, None, sh)
+                 for l in range(s.num_layers)]
+
+        def per_layer_plans():
+            for pl in plans:
+                kvx.kvx_plan_launch(pl, sh)
+
+        plan_ms = _timed(stream, per_layer_plans, 5)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            cs = torch.cuda.current_stream().cuda_stream
+            for pl in plans:
+                kvx.kvx_plan_launch(pl, cs)
+        def replay():
+            with torch.cuda.stream(stream):
+                graph.replay()
+
+        graph_ms = _timed(stream, replay, 5)
+        torch.cuda.synchronize()
+        for pl in plans:
+            kvx.kvx_plan_destroy(pl)
         kvx.kvx_dma_baseline(ctx, kvx.KVX_DIR_GATHER, pool, rs, ch, stream=sh)
         stream.synchronize()
         t0 = time.perf_counter()
@@ -1113,6 +1135,8 @@ def run_mla_blocks(args, kvx, wl):
                "store_gbs": round(N / (st_ms * 1e-3) / GB, 2),
                "per_layer_load_gbs": round(N / (ld_ms * 1e-3) / GB, 2),
                "per_layer_load_ms": round(ld_ms / s.num_layers, 4),
+               "per_layer_plans_gbs": round(N / (plan_ms * 1e-3) / GB, 2),
+               "per_layer_graph_gbs": round(N / (graph_ms * 1e-3) / GB, 2),
                "dma_store_gbs": round(N / dma_s / GB, 2), "dma_copies": n})
         arena.close()
         del pools

@@ -235,6 +235,26 @@ kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,
                              int n_chunks, int layer_begin, int layer_end,
                              const kvx_launch_cfg *cfg, kvx_stream_t stream);
 
+/* ---------------------------------------------------------------- prepared plans */
+
+/* A store, load or transform (op = KVX_OP_STORE .. KVX_OP_SCATTER_HBM) validated and
+ * packed once.  kvx_plan_create allocates device memory of its own for the descriptors,
+ * copies them there on `stream` and waits for the copy.  kvx_plan_launch then only
+ * enqueues the kernel: no validation, no host packing, no descriptor copy, no slot wait,
+ * so repeated transfers (the same per-layer batches every prefill, for instance) cost one
+ * launch each, and a sequence of launches can be captured into a CUDA graph.  The plan
+ * keeps the addresses of the pools, page tables and chunks it was made with: their
+ * contents may change between launches, their addresses may not.  Launches report to the
+ * context's status word; destroy a plan (it synchronizes the device) before its context. */
+typedef struct kvx_plan kvx_plan;
+
+kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request *reqs,
+                           int n_req, const kvx_chunk *chunks, int n_chunks, int layer_begin,
+                           int layer_end, const kvx_launch_cfg *cfg, kvx_stream_t stream,
+                           kvx_plan **out);
+kvx_status kvx_plan_launch(const kvx_plan *plan, kvx_stream_t stream);
+void kvx_plan_destroy(kvx_plan *plan);
+
 /* Comparison baseline only: the same transfer as one cudaMemcpyAsync per contiguous
  * (chunk, layer, kv, page) segment (cudaMemcpy2DAsync for token-major chunks), issued
  * from this host thread ("Strata Guide", section "The Conflict Between PagedAttention

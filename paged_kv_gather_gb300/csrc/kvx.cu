@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <cstdarg>
+#include <vector>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -671,6 +672,61 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
     return KVX_OK;
 }
 
+// Kernel, grid and shared memory of one transfer launch.
+struct LaunchShape {
+    const void *fn = nullptr;
+    int64_t ctas = 0;
+    int threads = 0;
+    size_t smem = 0;
+    int bulk = 0;
+    int stage_bytes = 0;
+    int stages = 0;
+};
+
+LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &plan, int dir)
+{
+    LaunchShape sh;
+    const int64_t warps_per_cta = cfg.threads / 32;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
+    const int64_t per_cta = warps_per_cta * (cfg.mapping == KVX_MAP_BULK ? 1 : plan.batch);
+    const int64_t needed = (plan.total_items + per_cta - 1) / per_cta;
+    if (ctas > needed)
+        ctas = needed;
+    sh.ctas = ctas;
+    if (cfg.mapping == KVX_MAP_BULK) {
+        sh.fn = dir == KVX_DIR_GATHER
+                    ? reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_GATHER>)
+                    : reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_SCATTER>);
+        sh.threads = 32;
+        sh.bulk = 1;
+        sh.stage_bytes = cfg.stage_bytes;
+        sh.stages = cfg.unroll;
+        sh.smem = size_t(cfg.unroll) * cfg.stage_bytes;
+    } else {
+        sh.fn = reinterpret_cast<const void *>(pick_kernel(cfg.unroll, dir, cfg.store_hint,
+                                                           plan.batch));
+        sh.threads = cfg.threads;
+    }
+    return sh;
+}
+
+cudaError_t launch_kernel(const LaunchShape &sh, Plan plan, cudaStream_t s)
+{
+    if (sh.bulk) {
+        cudaError_t e = cudaFuncSetAttribute(sh.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(sh.smem));
+        if (e != cudaSuccess)
+            return e;
+        int stage_bytes = sh.stage_bytes, stages = sh.stages;
+        void *args[] = {&plan, &stage_bytes, &stages};
+        return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(32u), args, sh.smem, s);
+    }
+    void *args[] = {&plan};
+    return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args, 0,
+                            s);
+}
+
 kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request *reqs, int n_req,
                   const kvx_chunk *chunks, int n_chunks, int layer_begin, int layer_end,
                   const kvx_launch_cfg *user_cfg, kvx_stream_t stream)
@@ -720,32 +776,11 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, lay.total, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
-    const int64_t warps_per_cta = cfg.threads / 32;
-    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
-    int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
-    const int64_t per_cta = warps_per_cta * (cfg.mapping == KVX_MAP_BULK ? 1 : plan.batch);
-    const int64_t needed = (plan.total_items + per_cta - 1) / per_cta;
-    if (ctas > needed)
-        ctas = needed;
-    if (cfg.mapping == KVX_MAP_BULK) {
-        const void *fn = dir == KVX_DIR_GATHER
-                             ? reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_GATHER>)
-                             : reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_SCATTER>);
-        const size_t smem = size_t(cfg.unroll) * cfg.stage_bytes;
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess)
-            return cuda_err(ctx, e, "bulk kernel shared memory");
-        int stage_bytes = cfg.stage_bytes, stages = cfg.unroll;
-        void *args[] = {&plan, &stage_bytes, &stages};
-        e = cudaLaunchKernel(fn, dim3(unsigned(ctas)), dim3(32u), args, smem, s);
-    } else {
-        KernelFn fn = pick_kernel(cfg.unroll, dir, cfg.store_hint, plan.batch);
-        void *args[] = {&plan};
-        e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
-                             dim3(unsigned(cfg.threads)), args, 0, s);
-    }
+    const LaunchShape shape = launch_shape(ctx, cfg, plan, dir);
+    e = launch_kernel(shape, plan, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
+    const int64_t ctas = shape.ctas;
     e = cudaEventRecord(slot.done, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "event record");
@@ -842,7 +877,92 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
 
 }  // namespace
 
+// A transfer validated and packed once, its descriptors in device memory of its own.
+struct kvx_plan {
+    kvx_ctx *ctx = nullptr;
+    char *dev = nullptr;
+    Plan plan;
+    LaunchShape shape;
+};
+
 extern "C" {
+
+kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request *reqs,
+                           int n_req, const kvx_chunk *chunks, int n_chunks, int layer_begin,
+                           int layer_end, const kvx_launch_cfg *user_cfg, kvx_stream_t stream,
+                           kvx_plan **out)
+{
+    if (!ctx || !out)
+        return KVX_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (op < KVX_OP_STORE || op > KVX_OP_SCATTER_HBM)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "plans take store, load or transform ops");
+    kvx_launch_cfg cfg;
+    kvx_status st = resolve_cfg(ctx, op, user_cfg, &cfg);
+    if (st != KVX_OK)
+        return st;
+    st = kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, op,
+                       ctx->validation, true, ctx->err, sizeof ctx->err);
+    if (st != KVX_OK)
+        return st;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
+    const int dir = (op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM) ? KVX_DIR_SCATTER
+                                                                    : KVX_DIR_GATHER;
+    const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
+    kvx_plan *p = new kvx_plan();
+    p->ctx = ctx;
+    std::vector<char> host(lay.total);
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->dev), lay.total);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_err(ctx, e, "plan descriptor buffer");
+    }
+    p->plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
+                        host.data(), p->dev);
+    p->plan.status = ctx->status_dev;
+    if (cfg.batch > 0)
+        p->plan.batch = cfg.batch;
+    else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && p->plan.batch == 1)
+        p->plan.batch = 2;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaMemcpyAsync(p->dev, host.data(), lay.total, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);  // the host image dies with this call
+    if (e != cudaSuccess) {
+        cudaFree(p->dev);
+        delete p;
+        return cuda_err(ctx, e, "plan descriptor copy");
+    }
+    p->shape = launch_shape(ctx, cfg, p->plan, dir);
+    *out = p;
+    return KVX_OK;
+}
+
+kvx_status kvx_plan_launch(const kvx_plan *p, kvx_stream_t stream)
+{
+    if (!p)
+        return KVX_ERR_INVALID_ARG;
+    if (p->plan.total_items == 0)
+        return KVX_OK;
+    cudaError_t e = launch_kernel(p->shape, p->plan, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_err(p->ctx, e, "plan launch");
+    return KVX_OK;
+}
+
+void kvx_plan_destroy(kvx_plan *p)
+{
+    if (!p)
+        return;
+    if (p->dev) {
+        DeviceGuard guard(p->ctx->device);
+        cudaDeviceSynchronize();
+        cudaFree(p->dev);
+    }
+    delete p;
+}
 
 kvx_status kvx_create(kvx_ctx **out, int device, size_t max_descriptor_bytes)
 {

@@ -133,6 +133,10 @@ _proto("kvx_load_chunks", _c.c_int, [_ctx_t, *_batch, _P(kvx_launch_cfg), _c.c_v
 _proto("kvx_exchange_chunks", _c.c_int,
        [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int,
         _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _P(kvx_launch_cfg), _c.c_void_p])
+_proto("kvx_plan_create", _c.c_int, [_ctx_t, _c.c_int, *_batch, _P(kvx_launch_cfg), _c.c_void_p,
+                                     _P(_c.c_void_p)])
+_proto("kvx_plan_launch", _c.c_int, [_c.c_void_p, _c.c_void_p])
+_proto("kvx_plan_destroy", None, [_c.c_void_p])
 _proto("kvx_transform_hbm", _c.c_int,
        [_ctx_t, _c.c_int, *_batch, _P(kvx_launch_cfg), _c.c_void_p])
 _proto("kvx_dma_baseline", _c.c_int,
@@ -165,7 +169,8 @@ _proto("kvx_load_chunks_noalloc", _c.c_int, [*_batch, _P(kvx_launch_cfg), _c.c_v
                                              _c.c_void_p])
 
 EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_launch_cfg",
-            "kvx_store_chunks", "kvx_load_chunks", "kvx_exchange_chunks", "kvx_transform_hbm", "kvx_dma_baseline",
+            "kvx_store_chunks", "kvx_load_chunks", "kvx_exchange_chunks", "kvx_plan_create",
+            "kvx_plan_launch", "kvx_plan_destroy", "kvx_transform_hbm", "kvx_dma_baseline",
             "kvx_get_status", "kvx_last_error", "kvx_last_launch", "kvx_validate",
             "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
@@ -342,6 +347,27 @@ def kvx_exchange_chunks(ctx, pool: Pool, store_reqs, store_chunks, load_reqs, lo
     _check(ctx, _lib.kvx_exchange_chunks(ctx, ctypes.byref(pool.c), srp, nsr, scp, nsc, lrp, nlr,
                                          lcp, nlc, layer_begin, layer_end, _cfg_ptr(cfg),
                                          stream))
+
+
+def kvx_plan_create(ctx, op: int, pool: Pool, reqs, chunks, layer_begin: int = 0,
+                    layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
+                    stream: int = 0):
+    """Validate and pack a transfer once; returns the plan handle for kvx_plan_launch."""
+    h = ctypes.c_void_p()
+    _check(ctx, _lib.kvx_plan_create(ctx, op, *_batch_args(pool, reqs, chunks, layer_begin,
+                                                           layer_end), _cfg_ptr(cfg), stream,
+                                     ctypes.byref(h)))
+    return h
+
+
+def kvx_plan_launch(plan, stream: int = 0) -> None:
+    st = _lib.kvx_plan_launch(plan, stream)
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_plan_launch")
+
+
+def kvx_plan_destroy(plan) -> None:
+    _lib.kvx_plan_destroy(plan)
 
 
 def kvx_transform_hbm(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,

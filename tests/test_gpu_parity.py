@@ -487,3 +487,138 @@ def test_default_launch_configs(ctx):
         assert c.threads % 32 == 0 and c.unroll in (1, 2, 4, 8)
     assert kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD).sm_cap > 0
     assert kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM).sm_cap == 0
+
+
+def test_offsets_beyond_4_gib(ctx, stream):
+    """64-bit address arithmetic: one layer pool of 4.5 GiB with the request on its last
+    pages (page offsets past 2^32), and an HBM chunk of 4.25 GiB (chunk offsets past 2^32),
+    checked byte for byte on host copies."""
+    L, KV, P, v = 1, 1, 16, 4096
+    num_pages = 73728                      # 73728 x 16 x 4096 B = 4.5 GiB
+    n_tok = 1114112                        # 69632 pages, chunk 1114112 x 4096 B = 4.25 GiB
+    pages = n_tok // P
+    table = np.arange(num_pages - pages, num_pages, dtype=np.int32)[::-1].copy()
+    dpool = DevicePool.empty(L, KV, num_pages, P, v, fill=0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4242)
+    tail = dpool.tensor[0, 0, num_pages - pages:]
+    tail.copy_(torch.randint(0, 256, tail.shape, generator=g, device="cuda",
+                             dtype=torch.int16).to(torch.uint8))
+    reqs = Requests([table], [n_tok])
+    spec = [wl.ChunkSpec(0, 0, n_tok, 0, 1, wl.LAYER_MAJOR, 0)]
+    chunk = torch.full((n_tok * v,), CANARY, dtype=torch.uint8, device="cuda")
+    assert chunk.numel() > (1 << 32)
+    kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_GATHER, dpool.pool, reqs.array,
+                          kvx.chunks_array(spec, chunk.data_ptr()), stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    # Oracle on host copies of the whole 4.5 GiB layer.
+    host_layer = torch.empty(dpool.tensor.shape[2:], dtype=torch.uint8, pin_memory=True)
+    host_layer.copy_(dpool.tensor[0, 0])
+    opool = oracle.Pool([[host_layer.numpy()]], P)
+    expect = np.empty(n_tok * v, np.uint8)
+    oracle.store(opool, reqs.oracle(), oracle_chunks(spec, expect), threads=8)
+    got = torch.empty(chunk.shape, dtype=torch.uint8, pin_memory=True)
+    got.copy_(chunk)
+    assert_bytes_equal(got.numpy(), expect, "gather with offsets past 4 GiB")
+    # Scatter it back into the first pages of the pool, in order (table2 = 0, 1, 2, ...),
+    # and check those pages against the oracle's load.
+    table2 = np.arange(0, pages, dtype=np.int32)
+    reqs2 = Requests([table2], [n_tok])
+    kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_SCATTER, dpool.pool, reqs2.array,
+                          kvx.chunks_array(spec, chunk.data_ptr()), stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    oracle.load(opool, reqs2.oracle(), oracle_chunks(spec, expect), threads=8)
+    host_layer2 = torch.empty(dpool.tensor.shape[2:], dtype=torch.uint8, pin_memory=True)
+    host_layer2.copy_(dpool.tensor[0, 0])
+    assert_bytes_equal(host_layer2.numpy().reshape(-1), host_layer.numpy().reshape(-1),
+                       "scatter with chunk offsets past 4 GiB")
+    del chunk
+
+
+def _blocks_case(rng, L=4, KV=2, P=16, v=1024, n_tok=900):
+    pages = -(-n_tok // P)
+    NP = 2 * pages + 3
+    table = rng.permutation(NP)[:pages].astype(np.int32)
+    specs = wl.split_tokens(0, 0, n_tok, P, 0, L, wl.STRIPED)  # one block object set per page
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape, align=wl.STRIPE_ALIGN)
+    return shape, table, specs, wl._arena_bytes(specs, shape)
+
+
+def test_prepared_plans_reuse_descriptors_and_see_new_contents(ctx, stream):
+    """Per-layer load plans made once, launched twice with different chunk contents."""
+    rng = np.random.default_rng(606)
+    shape, table, specs, nbytes = _blocks_case(rng)
+    L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size, shape.token_bytes,
+                       shape.num_pages)
+    reqs = Requests([table], [900])
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    arena = Arena(nbytes, "host")
+    ch = kvx.chunks_array(specs, arena.ptr)
+    plans = [kvx.kvx_plan_create(ctx, kvx.KVX_OP_LOAD, dpool.pool, reqs.array, ch, l, l + 1,
+                                 None, stream.cuda_stream) for l in range(L)]
+    try:
+        for round_ in range(2):
+            data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+            arena.write(data)
+            pre = dpool.host_copy()
+            for p in plans:
+                kvx.kvx_plan_launch(p, stream.cuda_stream)
+            stream.synchronize()
+            assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+            assert_pool_equal(dpool, expected_load(pre, reqs, specs, data.copy()))
+    finally:
+        for p in plans:
+            kvx.kvx_plan_destroy(p)
+        arena.close()
+
+
+def test_prepared_plans_in_a_cuda_graph(ctx):
+    """A store plan and per-layer load plans captured into one CUDA graph and replayed."""
+    rng = np.random.default_rng(707)
+    shape, table, specs, nbytes = _blocks_case(rng, L=3, KV=1, v=1152)
+    L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size, shape.token_bytes,
+                       shape.num_pages)
+    src = Requests([table], [900])
+    dst_table = np.setdiff1d(np.arange(NP, dtype=np.int32), table)[:len(table)]
+    dst = Requests([rng.permutation(dst_table).astype(np.int32)], [900])
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    arena = Arena(nbytes, "host")
+    ch = kvx.chunks_array(specs, arena.ptr)
+    s = torch.cuda.Stream()
+    store = kvx.kvx_plan_create(ctx, kvx.KVX_OP_STORE, dpool.pool, src.array, ch, 0, L, None,
+                                s.cuda_stream)
+    loads = [kvx.kvx_plan_create(ctx, kvx.KVX_OP_LOAD, dpool.pool, dst.array, ch, l, l + 1,
+                                 None, s.cuda_stream) for l in range(L)]
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            cs = torch.cuda.current_stream().cuda_stream
+            kvx.kvx_plan_launch(store, cs)
+            for p in loads:
+                kvx.kvx_plan_launch(p, cs)
+        for round_ in range(2):
+            dpool.fill_random(808 + round_)
+            pre = dpool.host_copy()
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert kvx.kvx_get_status(ctx, 0) == 0
+            exp_chunks = np.full(nbytes + 4096, CANARY, np.uint8)
+            oracle.store(pre, src.oracle(), oracle_chunks(specs, exp_chunks))
+            got = arena.numpy()
+            for c in specs:  # compare the objects (padding is never written)
+                stride = -(-c.n_tokens * v // wl.STRIPE_ALIGN) * wl.STRIPE_ALIGN
+                for l in range(L):
+                    off = c.offset + l * stride
+                    assert_bytes_equal(got[off:off + c.n_tokens * v],
+                                       exp_chunks[off:off + c.n_tokens * v], "graph store")
+            oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp_chunks))
+            assert_pool_equal(dpool, pre)
+    finally:
+        kvx.kvx_plan_destroy(store)
+        for p in loads:
+            kvx.kvx_plan_destroy(p)
+        arena.close()
