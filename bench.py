@@ -58,17 +58,23 @@ def parse():
     p.add_argument("--load-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--exchange-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
+    p.add_argument("--roundtrip-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--workload", default="llama8b",
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
                             "transform_sweep", "profile_small", "batch_sweep", "mla_blocks",
-                            "eviction"],
+                            "roundtrip_sweep", "eviction"],
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
-                   choices=["store", "load", "gather", "scatter", "exchange"],
+                   choices=["store", "load", "gather", "scatter", "exchange", "roundtrip"],
                    help="operation of --workload profile_small")
     p.add_argument("--groups", type=int, default=16,
                    help="chunk groups of the pipelined store/load round trip")
+    p.add_argument("--group-list", default="8,16,32,64",
+                   help="group counts of --workload roundtrip_sweep")
+    p.add_argument("--fused-cfgs", default="40:8:1024,32:8:1024,48:8:1024,80:8:512",
+                   help="sm_cap:unroll:threads launch shapes of the one-launch round trip in "
+                        "--workload roundtrip_sweep")
     p.add_argument("--sm-caps", default="1,2,4,8,16,32,0",
                    help="SM caps of the llama70b overlap sweep (0 = all SMs)")
     return p.parse_args()
@@ -267,7 +273,19 @@ class CpuSample:
         self.oracle.store(self.psrc, self.src, self.chunks, threads=self.threads)
         self.oracle.load(self.pdst, self.dst, self.chunks, threads=self.threads)
 
-    def run(self, seconds: float):
+    def run(self, seconds: float, single_thread_seconds: float = 0.0):
+        single = None
+        if single_thread_seconds > 0:
+            threads, self.threads = self.threads, 1
+            single = self._timed(single_thread_seconds)
+            self.threads = threads
+        out = self._timed(seconds)
+        if single is not None:
+            out["single_thread"] = {"value": single["value"], "unit": "GB/s", "cores": 1,
+                                    "sample": single["sample"]}
+        return out
+
+    def _timed(self, seconds: float):
         passes, t0 = 0, time.perf_counter()
         while True:
             self.one_pass()
@@ -394,6 +412,7 @@ def run_ours(args):
     cfg_load = parse_cfg(kvx, ctx, kvx.KVX_OP_LOAD, args.load_cfg)
     cfg_tr = parse_cfg(kvx, ctx, kvx.KVX_OP_GATHER_HBM, args.transform_cfg)
     cfg_x = parse_cfg(kvx, ctx, kvx.KVX_OP_EXCHANGE, args.exchange_cfg)
+    cfg_rt = parse_cfg(kvx, ctx, kvx.KVX_OP_ROUNDTRIP, args.roundtrip_cfg)
     rt = RoundTrip(kvx, ctx, pool, reqs_src, reqs_dst, chunks_host, s.num_layers, cfg_x,
                    args.groups, dev)
 
@@ -466,57 +485,73 @@ def run_ours(args):
     store_gbs = N / (store_ms * 1e-3) / GB
     load_gbs = N / (load_ms * 1e-3) / GB
 
-    # ---- the timed region: the pipelined round trip (device clock).  The warm-up leaves
-    # one group's load pending, so the K timed steps move exactly K x N each way.
+    # ---- the timed region: one kvx_roundtrip_chunks launch per step (device clock)
+    def roundtrip(rs=reqs_src, rd=reqs_dst):
+        kvx.kvx_roundtrip_chunks(ctx, pool, rs, rd, chunks_host, 0, s.num_layers, cfg_rt, sh)
+
     for _ in range(args.warmup):
-        rt.step()
+        roundtrip()
     torch.cuda.synchronize()
-    px = EventTimer(rt.stream)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         e_start = torch.cuda.Event(enable_timing=True)
-        e_start.record(rt.stream)
+        e_start.record(stream)
+        step_events = [e_start]
         for _ in range(args.steps):
-            rt.step(px)
-        e_end = torch.cuda.Event(enable_timing=True)
-        e_end.record(rt.stream)
+            roundtrip()
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            step_events.append(ev)
+        e_end = step_events[-1]
         torch.cuda.synchronize()
     total_ms = max_over_ranks(e_start.elapsed_time(e_end), world)
+    step_ms = [a.elapsed_time(b) for a, b in zip(step_events, step_events[1:])]
     barrier(world)
-    rt.flush()
-    assert kvx.kvx_get_status(ctx, rt.stream.cuda_stream) == 0
-    items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
-    p_x_ms = statistics.mean(px.ms())
-    group_bytes = N / args.groups
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    items, ctas, threads, desc = kvx.kvx_last_launch(ctx)
 
-    # ---- end to end through the C ABI on the host clock (pipelined step + uploads/readback)
+    # ---- end to end through the C ABI on the host clock: page tables up, the round trip,
+    # the status word back (which waits for the launch)
     pt_host = torch.from_numpy(np.concatenate([src_h, dst_h])).pin_memory()
     pt_dev = torch.empty_like(pt_host, device=dev)
+    rs_e2e = kvx.requests_array([(pt_dev.data_ptr(), src_h, w.store_requests[0].n_tokens)])
+    rd_e2e = kvx.requests_array([(pt_dev.data_ptr() + 4 * len(src_h), dst_h,
+                                  w.load_requests[0].n_tokens)])
     e2e_ms = []
-    desc = 0
     for i in range(args.warmup + max(3, args.steps // 2)):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        with torch.cuda.stream(rt.stream):
+        with torch.cuda.stream(stream):
             pt_dev.copy_(pt_host, non_blocking=True)
-        rt.rs = kvx.requests_array([(pt_dev.data_ptr(), src_h, w.store_requests[0].n_tokens)])
-        rt.rd = kvx.requests_array([(pt_dev.data_ptr() + 4 * len(src_h), dst_h,
-                                     w.load_requests[0].n_tokens)])
-        rt.step()
-        rt.flush()  # each end-to-end step completes its own round trip
-        desc = kvx.kvx_last_launch(ctx)[3]
-        assert kvx.kvx_get_status(ctx, rt.stream.cuda_stream) == 0   # D2H status word + sync
+        roundtrip(rs_e2e, rd_e2e)
+        assert kvx.kvx_get_status(ctx, sh) == 0   # D2H status word + sync
         if i >= args.warmup:
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    rt.rs, rt.rd = reqs_src, reqs_dst
     e2e = {"value": round(2 * N / (statistics.median(e2e_ms) * 1e-3) / GB, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": int(pt_host.numel() * 4 + desc * (args.groups + 1)),
+           "h2d_bytes_per_step": int(pt_host.numel() * 4 + desc),
            "d2h_bytes_per_step": 4,
            "payload_link_bytes_per_step": 2 * N,
-           "note": "KV payload crosses the host link inside the kernels (zero-copy, mapped "
-                   "pinned memory); the counted copies are the page tables, descriptors and "
-                   "the two status words"}
+           "note": "KV payload crosses the host link inside the kernel (zero-copy, mapped "
+                   "pinned memory); the counted copies are the page tables, the descriptors "
+                   "and the status word"}
+
+    # ---- context: the same step as a pipeline of exchange launches (store group g + load
+    # group g - 1 per launch), carried across steps
+    for _ in range(2):
+        rt.step()
+    px = EventTimer(rt.stream)
+    for _ in range(max(3, args.steps // 2)):
+        e = px.start()
+        rt.step()
+        px.stop(e)
+    rt.flush()
+    torch.cuda.synchronize()
+    assert kvx.kvx_get_status(ctx, rt.stream.cuda_stream) == 0
+    x_ms = statistics.median(px.ms())
+    exchange_pipeline = {"groups": args.groups, "launches_per_step": rt.launches_per_step(),
+                         "gbs": round(2 * N / (x_ms * 1e-3) / GB, 2),
+                         "kernel": "kvx_exchange_kernel", "cfg": cfg_x.as_dict()}
 
     # ---- HBM transform on the same request (chunks in device memory)
     dchunk = torch.empty(w.store_arena_bytes, dtype=torch.uint8, device=dev)
@@ -571,40 +606,51 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = CpuSample(os.cpu_count() or 1).run(args.cpu_seconds)
+        cpu = CpuSample(os.cpu_count() or 1).run(args.cpu_seconds,
+                                                 single_thread_seconds=args.cpu_seconds / 3)
 
     value = 2 * N * args.steps * world / (total_ms * 1e-3) / GB
     step_gbs = 2 * N / (total_ms / args.steps * 1e-3) / GB
+    launch_gbs = step_gbs  # one launch per step
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "step_ms": {"median": round(statistics.median(step_ms), 4),
+                    "min": round(min(step_ms), 4), "max": round(max(step_ms), 4),
+                    "note": "this rank's steps, device clock"},
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": "llama8b_kv: 32 layers, 8 KV heads x 128, bf16 N(0,1), "
                                "16-token pages, 32768 tokens on 2048 random pages of a "
                                "16384-page pool, 128 layer-major chunks of 256 tokens (32 MiB) "
                                "in mapped pinned host memory; step = store all chunks + load "
-                               f"them into 2048 fresh pages, pipelined in {args.groups} chunk "
-                               "groups, each launch storing one group and loading the "
-                               "previous one",
+                               "them into 2048 fresh pages in one kvx_roundtrip_chunks launch "
+                               "(each page segment is loaded once its store has reached host "
+                               "memory)",
                    "bytes_per_direction": N, "l2": "inputs larger than L2 (4 GiB per "
                    "direction), no flush", "parallelism": f"replicas x{world}" if world > 1
                    else "single GPU"},
-        "roofline": {"bound": "host_link", "achieved": round(step_gbs, 2),
+        "roofline": {"bound": "host_link", "achieved": round(launch_gbs, 2),
                      "peak": link["bidir"], "unit": "GB/s",
-                     "frac": round(step_gbs / link["bidir"], 4),
-                     "traffic": recorded_traffic("exchange", "llama8b", args.groups),
-                     "kernel": "kvx_exchange_kernel (store group g + load group g-1 in "
-                               "one launch)",
+                     "frac": round(launch_gbs / link["bidir"], 4),
+                     "step_gbs": round(step_gbs, 2),
+                     "achieved_note": "bytes per round-trip launch (both directions) / "
+                                      "mean launch duration on the launching stream (one "
+                                      "launch per step; the events also hold its descriptor "
+                                      "copy and completion-word reset)",
+                     "traffic": recorded_traffic("roundtrip", "llama8b"),
+                     "kernel": "kvx_roundtrip_kernel (store + load of every segment in one "
+                               "launch)",
                      "peak_source": "measured in this run: best of 8 pairs of 4 GiB pinned "
                                     "cudaMemcpyAsync, H2D and D2H at once (both link "
                                     "directions)",
                      "algorithmic_bytes": 2 * N,
-                     "per_launch": {"ms": round(p_x_ms, 4),
-                                    "gbs": round(2 * group_bytes / (p_x_ms * 1e-3) / GB, 2),
-                                    "bytes_per_launch": int(2 * group_bytes),
+                     "per_launch": {"ms": round(total_ms / args.steps, 4),
+                                    "gbs": round(launch_gbs, 2), "bytes_per_launch": 2 * N,
                                     "items_per_launch": items, "ctas": ctas,
                                     "threads": threads}},
+        "exchange_pipeline": exchange_pipeline,
         "sequential": {
             "note": "store then load on one stream, no overlap: per-direction rooflines",
             "step_gbs": round(2 * N / ((store_ms + load_ms) * 1e-3) / GB, 2),
@@ -614,7 +660,7 @@ def run_ours(args):
             "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
                      "peak": link["h2d"], "frac": round(load_gbs / link["h2d"], 4),
                      "traffic": recorded_traffic("load", "llama8b")}},
-        "cfg": {"exchange": cfg_x.as_dict(), "store": cfg_store.as_dict(),
+        "cfg": {"roundtrip": cfg_rt.as_dict(), "store": cfg_store.as_dict(),
                 "load": cfg_load.as_dict()},
         "host_link_peak": {"h2d_gbs": link["h2d"], "d2h_gbs": link["d2h"],
                            "bidirectional_gbs": link["bidir"], "samples_gbs": samples,
@@ -626,7 +672,7 @@ def run_ours(args):
         "dma_baseline": dma,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": rt.launches_per_step() * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }
     if rank == 0:
@@ -862,7 +908,7 @@ def run_qwen7b(args, kvx, wl):
     assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
     assert kvx.kvx_get_status(ctx_b, sb.cuda_stream) == 0
     # The same two batches in one exchange launch.
-    xcfg = kvx.kvx_default_launch_cfg(ctx_a, kvx.KVX_OP_EXCHANGE)
+    xcfg = parse_cfg(kvx, ctx_a, kvx.KVX_OP_EXCHANGE, args.exchange_cfg)
     x_ms = _timed(sa, lambda: kvx.kvx_exchange_chunks(ctx_a, pool, reqs, ch_st, reqs, ch_ld,
                                                        cfg=xcfg, stream=sa.cuda_stream), 5)
     assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
@@ -1226,7 +1272,7 @@ def run_profile_small(args, kvx, wl):
     rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
     ctx = kvx.kvx_create(0)
     sh = torch.cuda.current_stream().cuda_stream
-    if args.profile_op in ("store", "load", "exchange"):
+    if args.profile_op in ("store", "load", "exchange", "roundtrip"):
         buf = kvx.HostBuffer(w.store_arena_bytes)
         buf.array[:] = 0
         ch = kvx.chunks_array(w.store_chunks, buf.ptr)
@@ -1235,7 +1281,9 @@ def run_profile_small(args, kvx, wl):
         ch = kvx.chunks_array(w.store_chunks, dchunk.data_ptr())
     half = len(w.store_chunks) // 2
     for _ in range(3):
-        if args.profile_op == "exchange":  # store the first half, load the second half
+        if args.profile_op == "roundtrip":  # store every chunk and load it into other pages
+            kvx.kvx_roundtrip_chunks(ctx, pool, rs, rd, ch, stream=sh)
+        elif args.profile_op == "exchange":  # store the first half, load the second half
             kvx.kvx_exchange_chunks(ctx, pool, rs, np.ascontiguousarray(ch[:half]), rd,
                                     np.ascontiguousarray(ch[half:]), stream=sh)
         elif args.profile_op == "store":
@@ -1254,6 +1302,142 @@ def run_profile_small(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
+def run_roundtrip_sweep(args, kvx, wl):
+    """The headline round trip (llama8b, store all chunks + load them into fresh pages) in
+    G chunk groups, issued three ways: one kvx_exchange_chunks call per launch, prepared
+    exchange plans, and the plans captured in one CUDA graph per step.  Two step shapes:
+    pipelined (a step's first launch loads the previous step's last group) and
+    self-contained (first launch stores only, last launch loads only)."""
+    w = wl.llama8b()
+    s = w.shape
+    N = w.store_bytes()
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src_h, dst_h = w.store_requests[0].page_table, w.load_requests[0].page_table
+    src_d, dst_d = torch.from_numpy(src_h).cuda(), torch.from_numpy(dst_h).cuda()
+    rs = kvx.requests_array([(src_d.data_ptr(), src_h, w.store_requests[0].n_tokens)])
+    rd = kvx.requests_array([(dst_d.data_ptr(), dst_h, w.load_requests[0].n_tokens)])
+    host = kvx.HostBuffer(w.store_arena_bytes)
+    host.array[:] = 0
+    chunks = kvx.chunks_array(w.store_chunks, host.ptr)
+    ctx = kvx.kvx_create(0)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    empty = np.zeros(0, dtype=chunks.dtype)
+    reps = max(5, args.steps // 2)
+    # One kvx_roundtrip_chunks launch per step, over a few launch shapes.
+    for cap, unroll, threads in [tuple(int(v) for v in x.split(":"))
+                                 for x in args.fused_cfgs.split(",") if x]:
+        c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_ROUNDTRIP)
+        c.sm_cap, c.unroll, c.threads = cap, unroll, threads
+
+        def fused():
+            kvx.kvx_roundtrip_chunks(ctx, pool, rs, rd, chunks, cfg=c, stream=sh)
+
+        for _ in range(3):
+            fused()
+        t = EventTimer(stream)
+        host_ms = []
+        for _ in range(reps):
+            stream.synchronize()
+            t0 = time.perf_counter()
+            e = t.start()
+            fused()
+            t.stop(e)
+            stream.synchronize()
+            host_ms.append((time.perf_counter() - t0) * 1e3)
+        assert kvx.kvx_get_status(ctx, sh) == 0
+        ms = statistics.median(t.ms())
+        _emit({"workload": "llama8b_roundtrip_fused", "cfg": c.as_dict(),
+               "ctas": kvx.kvx_last_launch(ctx)[1],
+               "step_ms": round(ms, 4), "gbs": round(2 * N / (ms * 1e-3) / GB, 2),
+               "min_gbs": round(2 * N / (min(t.ms()) * 1e-3) / GB, 2),
+               "host_gbs": round(2 * N / (statistics.median(host_ms) * 1e-3) / GB, 2)})
+    for G in [int(x) for x in args.group_list.split(",") if x]:
+        bounds = np.linspace(0, len(chunks), G + 1).astype(int)
+        groups = [np.ascontiguousarray(chunks[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
+        # launch list of one step: (store, load) pairs
+        pipelined = [(groups[0], groups[-1])] + [(groups[k], groups[k - 1]) for k in range(1, G)]
+        selfc = ([(groups[0], empty)] + [(groups[k], groups[k - 1]) for k in range(1, G)] +
+                 [(empty, groups[-1])])
+        plans = {}
+
+        def plan_of(pair):
+            key = (id(pair[0]), id(pair[1]))
+            if key not in plans:
+                plans[key] = kvx.kvx_plan_create_exchange(ctx, pool, rs, pair[0], rd, pair[1],
+                                                          stream=sh)
+            return plans[key]
+
+        def by_call(seq):
+            for st, ld in seq:
+                kvx.kvx_exchange_chunks(ctx, pool, rs, st, rd, ld, stream=sh)
+
+        def by_plan(seq):
+            for pair in seq:
+                kvx.kvx_plan_launch(plan_of(pair), sh)
+
+        for pair in selfc + pipelined:
+            plan_of(pair)  # all plans exist before any graph capture
+        graphs = {}
+        for name, seq in (("pipelined", pipelined), ("self_contained", selfc)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                cs = torch.cuda.current_stream().cuda_stream
+                for pair in seq:
+                    kvx.kvx_plan_launch(plan_of(pair), cs)
+            graphs[name] = g
+
+        def by_graph(name):
+            def run(_seq):
+                with torch.cuda.stream(stream):
+                    graphs[name].replay()
+            return run
+
+        row = {"workload": "llama8b_roundtrip_sweep", "groups": G,
+               "group_bytes_each_way": int(N // G)}
+        for mode, fn_p, fn_s in (("call", by_call, by_call), ("plan", by_plan, by_plan),
+                                 ("graph", by_graph("pipelined"), by_graph("self_contained"))):
+            # pipelined: prime with a self-contained step minus its flush
+            fn_s(selfc[:-1]) if mode != "graph" else by_call(selfc[:-1])
+            for _ in range(2):
+                fn_p(pipelined)
+            t = EventTimer(stream)
+            for _ in range(reps):
+                e = t.start()
+                fn_p(pipelined)
+                t.stop(e)
+            by_call(selfc[-1:])
+            stream.synchronize()
+            pip_ms = statistics.median(t.ms())
+            # self-contained, device clock and host clock (sync after each step)
+            for _ in range(2):
+                fn_s(selfc)
+            t = EventTimer(stream)
+            host_ms = []
+            for _ in range(reps):
+                stream.synchronize()
+                t0 = time.perf_counter()
+                e = t.start()
+                fn_s(selfc)
+                t.stop(e)
+                stream.synchronize()
+                host_ms.append((time.perf_counter() - t0) * 1e3)
+            sc_ms = statistics.median(t.ms())
+            row[mode] = {"pipelined_gbs": round(2 * N / (pip_ms * 1e-3) / GB, 2),
+                         "self_contained_gbs": round(2 * N / (sc_ms * 1e-3) / GB, 2),
+                         "self_contained_host_gbs": round(
+                             2 * N / (statistics.median(host_ms) * 1e-3) / GB, 2)}
+        assert kvx.kvx_get_status(ctx, sh) == 0
+        _emit(row)
+        del graphs
+        torch.cuda.synchronize()
+        for h in plans.values():
+            kvx.kvx_plan_destroy(h)
+    host.close()
+    kvx.kvx_destroy(ctx)
+
+
 def run_workload(args):
     torch.cuda.set_device(0)
     from paged_kv_gather_gb300.build import build
@@ -1263,7 +1447,8 @@ def run_workload(args):
     {"llama70b": run_llama70b, "qwen7b_batch": run_qwen7b, "mla_sweep": run_mla_sweep,
      "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
      "profile_small": run_profile_small, "batch_sweep": run_batch_sweep,
-     "mla_blocks": run_mla_blocks, "eviction": run_eviction}[args.workload](
+     "mla_blocks": run_mla_blocks, "eviction": run_eviction,
+     "roundtrip_sweep": run_roundtrip_sweep}[args.workload](
         args, kvx, wl)
 
 

@@ -75,8 +75,9 @@ typedef enum kvx_status {
 
 /* Bits of the device status word (kvx_get_status). */
 #define KVX_DEV_PAGE_OUT_OF_RANGE 0x1u
-#define KVX_DEV_WAIT_TIMEOUT 0x2u       /* a bulk copy did not complete within ~1 s; the
-                                           kernel stopped early (output incomplete) */
+#define KVX_DEV_WAIT_TIMEOUT 0x2u       /* a bulk copy, or the store a round-trip load
+                                           waits for, did not complete within ~1 s; the
+                                           kernel skipped work (output incomplete) */
 
 typedef enum kvx_chunk_layout {
     KVX_CHUNK_LAYER_MAJOR = 0,
@@ -171,6 +172,8 @@ typedef struct kvx_ctx kvx_ctx;
 #define KVX_OP_GATHER_HBM 2   /* pages -> chunks in device memory */
 #define KVX_OP_SCATTER_HBM 3  /* chunks in device memory -> pages */
 #define KVX_OP_EXCHANGE 4     /* a store batch and a load batch in one launch (defaults only) */
+#define KVX_OP_ROUNDTRIP 5    /* store to chunks, then load them elsewhere, in one launch
+                                 (defaults only) */
 
 /* ---------------------------------------------------------------- context */
 
@@ -211,14 +214,17 @@ kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
                            int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
                            kvx_stream_t stream);
 
-/* exchange: a store batch and a load batch moved by ONE kernel launch, half of its CTAs
- * on each direction, so both directions of the host link carry data at once (an eviction
+/* exchange: a store batch and a load batch moved by ONE kernel launch, so both
+ * directions of the host link carry data at once (an eviction
  * and a prefetch issued together: "Strata Guide", section "Implementation: GPU-Assisted
  * I/O Kernels and Bubble-Filling Scheduler", steps "Dispatch Asynchronous Transfer" and
  * "Asynchronous Eviction").  Each batch follows the rules of kvx_store_chunks /
  * kvx_load_chunks; either may be empty.  The store's source slots and the load's
  * destination slots must not meet for a common layer (checked at validation level 2).
- * cfg->sm_cap counts the SMs of both directions together (default 40: 20 each). */
+ * cfg->sm_cap counts the SMs of both directions together (default 40).  Batches of
+ * similar size (within 1.5x in segments) split the CTAs by direction, half each; otherwise
+ * every warp takes units of both batches, so the larger one keeps the whole grid after the
+ * smaller one is done.  Either way, nothing in the launch waits on anything else. */
 kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
                                const kvx_request *store_reqs, int n_store_req,
                                const kvx_chunk *store_chunks, int n_store_chunks,
@@ -226,6 +232,27 @@ kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
                                const kvx_chunk *load_chunks, int n_load_chunks,
                                int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
                                kvx_stream_t stream);
+
+/* round trip: store the pages of src_reqs into the chunks and load the chunks into the
+ * pages of dst_reqs, in ONE launch: a swap-out to host memory followed by a swap-in to
+ * another page set (a preempted request resumed on new pages).  The pages describe the
+ * two transfers ("Strata Guide", section "Implementation: GPU-Assisted I/O Kernels and
+ * Bubble-Filling Scheduler": asynchronous eviction and transfer dispatch) but no call
+ * that orders one after the other inside a launch; this one does so per unit of work:
+ * each (chunk, layer, kv, page) segment is loaded once its own store has reached host
+ * memory, so both link directions carry data from the first finished store to the last
+ * load, with no launch boundary in between.  Chunk c belongs to request
+ * chunks[c].request of BOTH arrays (n_req entries each); the two page sets must not
+ * share a slot for a common layer (checked at validation level 2), and each batch
+ * follows the rules of kvx_store_chunks / kvx_load_chunks.  Its waits are bounded: a
+ * unit whose store has not finished within about a second is skipped and
+ * KVX_DEV_WAIT_TIMEOUT is set.  The descriptor buffer holds both plans plus 4 bytes per
+ * unit (a unit is `batch` segments).  cfg->sm_cap counts all SMs (default 16). */
+kvx_status kvx_roundtrip_chunks(kvx_ctx *ctx, const kvx_pool *pool,
+                                const kvx_request *src_reqs, const kvx_request *dst_reqs,
+                                int n_req, const kvx_chunk *chunks, int n_chunks,
+                                int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                                kvx_stream_t stream);
 
 /* transform: the same gather (dir = KVX_DIR_GATHER) or scatter (KVX_DIR_SCATTER) with
  * the chunks in device memory: the explicit HBM-to-HBM layout pass that "Strata Guide",
@@ -252,6 +279,16 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
                            int n_req, const kvx_chunk *chunks, int n_chunks, int layer_begin,
                            int layer_end, const kvx_launch_cfg *cfg, kvx_stream_t stream,
                            kvx_plan **out);
+/* The exchange of kvx_exchange_chunks (a store batch and a load batch in one launch),
+ * validated and packed once; launched with kvx_plan_launch like any plan.  Same rules on
+ * what may change between launches. */
+kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
+                                    const kvx_request *store_reqs, int n_store_req,
+                                    const kvx_chunk *store_chunks, int n_store_chunks,
+                                    const kvx_request *load_reqs, int n_load_req,
+                                    const kvx_chunk *load_chunks, int n_load_chunks,
+                                    int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                                    kvx_stream_t stream, kvx_plan **out);
 kvx_status kvx_plan_launch(const kvx_plan *plan, kvx_stream_t stream);
 void kvx_plan_destroy(kvx_plan *plan);
 

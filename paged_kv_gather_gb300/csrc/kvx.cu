@@ -39,6 +39,24 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p)
     return r;
 }
 
+// Coherent 16-byte load, cached in L2 only: for bytes another warp of the same launch wrote
+// (the read-only .nc path is valid only for data no thread writes during the launch).
+__device__ __forceinline__ uint4 ld_cg_v4(const uint4 *p)
+{
+    uint4 r;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
+
+template <bool NC>
+__device__ __forceinline__ uint4 ld_v4(const uint4 *p)
+{
+    return NC ? ld_nc_v4(p) : ld_cg_v4(p);
+}
+
 template <int HINT>
 __device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v)
 {
@@ -71,8 +89,9 @@ __device__ __forceinline__ int find_chunk(const int64_t *__restrict__ begin, int
 }
 
 // Contiguous copy of n16 16-byte units.  Lane i owns units i, i + 32, i + 64, ...; each
-// pass issues U independent loads before its U stores.
-template <int U, int HINT>
+// pass issues U independent loads before its U stores.  NC = false reads through the
+// coherent path.
+template <int U, int HINT, bool NC = true>
 __device__ __forceinline__ void copy_contig(const uint4 *__restrict__ s, uint4 *__restrict__ d,
                                             int n16, int lane)
 {
@@ -83,7 +102,7 @@ __device__ __forceinline__ void copy_contig(const uint4 *__restrict__ s, uint4 *
         uint4 r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            r[u] = ld_nc_v4(s + 32 * u);
+            r[u] = ld_v4<NC>(s + 32 * u);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             st_v4<HINT>(d + 32 * u, r[u]);
@@ -93,7 +112,7 @@ __device__ __forceinline__ void copy_contig(const uint4 *__restrict__ s, uint4 *
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (32 * u < rem)
-                r[u] = ld_nc_v4(s + 32 * u);
+                r[u] = ld_v4<NC>(s + 32 * u);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (32 * u < rem)
@@ -188,19 +207,19 @@ __device__ __forceinline__ Segment shfl_segment(const Segment &s, int src_lane)
     return r;
 }
 
-template <int U, int HINT>
+template <int U, int HINT, bool NC = true>
 __device__ __forceinline__ void copy_segment(const Segment &sg, int64_t v, int lane)
 {
     if (sg.contiguous) {
-        copy_contig<U, HINT>(reinterpret_cast<const uint4 *>(sg.src),
-                             reinterpret_cast<uint4 *>(sg.dst), int((int64_t(sg.rows) * v) >> 4),
-                             lane);
+        copy_contig<U, HINT, NC>(reinterpret_cast<const uint4 *>(sg.src),
+                                 reinterpret_cast<uint4 *>(sg.dst),
+                                 int((int64_t(sg.rows) * v) >> 4), lane);
     } else {
         // Token-major chunk: each token is its own run on the chunk side.
         for (int r = 0; r < sg.rows; ++r)
-            copy_contig<1, HINT>(reinterpret_cast<const uint4 *>(sg.src + r * sg.s_pitch),
-                                 reinterpret_cast<uint4 *>(sg.dst + r * sg.d_pitch),
-                                 int(v >> 4), lane);
+            copy_contig<1, HINT, NC>(reinterpret_cast<const uint4 *>(sg.src + r * sg.s_pitch),
+                                     reinterpret_cast<uint4 *>(sg.dst + r * sg.d_pitch),
+                                     int(v >> 4), lane);
     }
 }
 
@@ -457,6 +476,251 @@ __global__ void __launch_bounds__(32) kvx_bulk_kernel(const Plan p, int stage_by
     __syncwarp();
 }
 
+// ------------------------------------------------------------------------- round trip
+//
+// Store a batch to host chunks and load the same chunks into other pages in one launch
+// (a swap-out followed by a swap-in elsewhere).  The store and load plans enumerate the
+// same items, so load unit u reads exactly the host bytes store unit u writes.  Units
+// (unit_items consecutive items) are handed out by two fetch-and-add counters, one per
+// direction.  A warp takes a store unit while the loads handed out are within `lag`
+// units (one per warp of the grid by default) of the stores handed out, and a load unit
+// otherwise,
+// so each load usually starts well after its store finished.  A warp that holds a load
+// unit whose store has not been handed out yet hands out (and does) store units until it
+// has; only then does it wait for that store.  Every wait is therefore on a unit held by a
+// running warp that waits on nothing, whatever the residency of the grid, so the waits
+// end; each is still bounded (about one second, then KVX_DEV_WAIT_TIMEOUT and the unit is
+// skipped).  Both directions of the host link run from the first completed store to the
+// last load, in a single launch.
+
+struct RoundTripSync {
+    unsigned int *next;  // [0] next store unit, [1] next load unit; zero at launch
+    unsigned int *done;  // [units]: 1 once the store unit's bytes are in host memory
+    int64_t units;
+    int unit_items;
+    unsigned lag;        // loads handed out may trail stores handed out by this many units
+};
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Lane 0: bounded wait for a store unit to finish.
+__device__ __forceinline__ bool wait_unit(const RoundTripSync &sy, int64_t unit)
+{
+    const uint64_t deadline = global_ns() + kWaitLimitNs;
+    while (ld_acquire_u32(sy.done + unit) == 0u) {
+        if (global_ns() > deadline)
+            return false;
+        __nanosleep(200);
+    }
+    return true;
+}
+
+enum : int { kUnitStore = 1, kUnitLoad = 2, kUnitSkip = 3 };
+
+// Lane 0: the warp's next unit (-1: nothing left for this warp) and what to do with it.
+// `pending` carries a load unit taken before its store was handed out.
+__device__ __forceinline__ long long next_unit(const RoundTripSync &sy, unsigned lag,
+                                               long long &pending, int &what)
+{
+    const unsigned n = unsigned(sy.units);
+    if (pending < 0) {
+        const unsigned si = ld_relaxed_u32(sy.next);
+        const unsigned li = ld_relaxed_u32(sy.next + 1);
+        if (si < n && li + lag >= si) {
+            const unsigned s = atomicAdd(sy.next, 1u);
+            if (s < n) {
+                what = kUnitStore;
+                return s;
+            }
+        }
+        const unsigned t = atomicAdd(sy.next + 1, 1u);
+        if (t >= n)
+            return -1;  // every load is handed out; their holders finish the stores
+        pending = t;
+    }
+    if (ld_relaxed_u32(sy.next) <= unsigned(pending)) {
+        // The store this load needs is not handed out yet: hand out the next one.
+        const unsigned s = atomicAdd(sy.next, 1u);
+        if (s < n) {
+            what = kUnitStore;
+            return s;
+        }
+    }
+    const long long u = pending;
+    pending = -1;
+    what = wait_unit(sy, u) ? kUnitLoad : kUnitSkip;
+    return u;
+}
+
+// Items [first, first + count) of plan p, warp-collective (count is 1 unless BATCHED).
+// NC = false for bytes written earlier in the same launch.
+template <int U, int DIR, int HINT, bool BATCHED, bool NC>
+__device__ __forceinline__ void copy_items(const Plan &p, int64_t first, int count, int lane)
+{
+    const int64_t v = p.token_bytes;
+    if (!BATCHED) {  // one item per unit
+        Segment sg;
+        if (resolve_segment<DIR>(p, first, lane, sg))
+            copy_segment<U, HINT, NC>(sg, v, lane);
+        return;
+    }
+    Segment sg;
+    sg.src = nullptr;
+    sg.dst = nullptr;
+    sg.s_pitch = sg.d_pitch = 0;
+    sg.rows = 0;
+    sg.contiguous = true;
+    bool ok = false;
+    if (lane < count) {
+        const int64_t mine = first + lane;
+        ok = segment_of<DIR>(p, find_chunk_lane(p.item_begin, p.n_chunks, mine), mine, true,
+                             sg);
+    }
+    const unsigned valid = __ballot_sync(0xffffffffu, ok);
+    for (int k = 0; k < count; ++k) {
+        const Segment sk = shfl_segment(sg, k);
+        if (valid & (1u << k))
+            copy_segment<U, HINT, NC>(sk, v, lane);
+    }
+}
+
+template <int U, bool BATCHED>
+__global__ void __launch_bounds__(1024, 1)
+    kvx_roundtrip_kernel(const Plan ps, const Plan pl, const RoundTripSync sy)
+{
+    const int lane = threadIdx.x & 31;
+    long long pending = -1;  // lane 0's
+    for (;;) {
+        long long unit = -1;
+        int what = 0;
+        if (lane == 0) {
+            unit = next_unit(sy, sy.lag, pending, what);
+            if (what == kUnitSkip)
+                atomicOr(ps.status, KVX_DEV_WAIT_TIMEOUT);
+        }
+        unit = __shfl_sync(0xffffffffu, unit, 0);
+        what = __shfl_sync(0xffffffffu, what, 0);
+        if (unit < 0)
+            break;
+        if (what == kUnitSkip)
+            continue;  // its store never finished: leave the unit alone
+        __syncwarp();  // lane 0's acquire orders every lane's loads below
+        const int64_t first = unit * sy.unit_items;
+        const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
+        if (what == kUnitLoad) {
+            copy_items<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED, false>(pl, first, count,
+                                                                             lane);
+        } else {
+            // HBM reads need fewer bytes in flight than host reads: four loads per lane.
+            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
+                ps, first, count, lane);
+            __syncwarp();  // every lane's writes happen before lane 0's release
+            if (lane == 0)
+                st_release_u32(sy.done + unit, 1u);
+        }
+    }
+}
+
+// Exchange with shared work: a store batch and an independent load batch, each warp taking
+// its next unit from whichever direction is further behind in proportion to its size, so
+// both directions finish together and every warp works until the last unit, whatever the
+// ratio of the two batches.  No unit waits on another.
+struct DuplexSync {
+    unsigned int *next;  // [0] next store unit, [1] next load unit; zero at launch
+    int64_t units_s;
+    int64_t units_l;
+    int unit_items;
+};
+
+// Lane 0: the next unit (-1: none left) and its direction.
+__device__ __forceinline__ long long next_duplex_unit(const DuplexSync &sy, int &what)
+{
+    const unsigned ns = unsigned(sy.units_s), nl = unsigned(sy.units_l);
+    const unsigned si = ld_relaxed_u32(sy.next);
+    const unsigned li = ld_relaxed_u32(sy.next + 1);
+    // store progress si / ns against load progress li / nl
+    const bool store_first = si < ns && (li >= nl || uint64_t(si) * nl <= uint64_t(li) * ns);
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const bool store = (attempt == 0) == store_first;
+        const unsigned u = atomicAdd(sy.next + (store ? 0 : 1), 1u);
+        if (u < (store ? ns : nl)) {
+            what = store ? kUnitStore : kUnitLoad;
+            return u;
+        }
+    }
+    return -1;
+}
+
+template <int U, bool BATCHED>
+__global__ void __launch_bounds__(1024, 1)
+    kvx_duplex_kernel(const Plan ps, const Plan pl, const DuplexSync sy)
+{
+    const int lane = threadIdx.x & 31;
+    for (;;) {
+        long long unit = -1;
+        int what = 0;
+        if (lane == 0)
+            unit = next_duplex_unit(sy, what);
+        unit = __shfl_sync(0xffffffffu, unit, 0);
+        what = __shfl_sync(0xffffffffu, what, 0);
+        if (unit < 0)
+            break;
+        const int64_t first = unit * sy.unit_items;
+        if (what == kUnitLoad) {
+            const int count = int(min(int64_t(sy.unit_items), pl.total_items - first));
+            copy_items<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED, true>(pl, first, count,
+                                                                            lane);
+        } else {
+            const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
+            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
+                ps, first, count, lane);
+        }
+    }
+}
+
+typedef void (*DuplexFn)(Plan, Plan, DuplexSync);
+
+DuplexFn pick_duplex(int unroll, bool batched)
+{
+    switch (unroll) {
+    case 1: return batched ? kvx_duplex_kernel<1, true> : kvx_duplex_kernel<1, false>;
+    case 2: return batched ? kvx_duplex_kernel<2, true> : kvx_duplex_kernel<2, false>;
+    case 4: return batched ? kvx_duplex_kernel<4, true> : kvx_duplex_kernel<4, false>;
+    case 8: return batched ? kvx_duplex_kernel<8, true> : kvx_duplex_kernel<8, false>;
+    }
+    return nullptr;
+}
+
+typedef void (*RoundTripFn)(Plan, Plan, RoundTripSync);
+
+RoundTripFn pick_roundtrip(int unroll, bool batched)
+{
+    switch (unroll) {
+    case 1: return batched ? kvx_roundtrip_kernel<1, true> : kvx_roundtrip_kernel<1, false>;
+    case 2: return batched ? kvx_roundtrip_kernel<2, true> : kvx_roundtrip_kernel<2, false>;
+    case 4: return batched ? kvx_roundtrip_kernel<4, true> : kvx_roundtrip_kernel<4, false>;
+    case 8: return batched ? kvx_roundtrip_kernel<8, true> : kvx_roundtrip_kernel<8, false>;
+    }
+    return nullptr;
+}
+
 typedef void (*KernelFn)(Plan);
 
 template <int U, bool BATCHED>
@@ -612,6 +876,13 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
         break;
     case KVX_OP_EXCHANGE:  // 20 SMs per direction
         c->sm_cap = 40;
+        c->ctas_per_sm = 1;
+        c->threads = 1024;
+        c->unroll = 8;
+        c->store_hint = KVX_HINT_DEFAULT;
+        break;
+    case KVX_OP_ROUNDTRIP:  // both directions mixed on 16 SMs
+        c->sm_cap = 16;
         c->ctas_per_sm = 1;
         c->threads = 1024;
         c->unroll = 8;
@@ -793,6 +1064,77 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     return KVX_OK;
 }
 
+// An exchange whose batches differ in size by more than this factor (in segments) shares its
+// units between all warps (kvx_duplex_kernel): with the role split the smaller batch's half
+// of the grid would finish early and leave the larger batch on half the CTAs.  Batches of
+// similar size keep the role split, which measured 2-5 % faster for them.
+constexpr double kExchangeShareRatio = 1.5;
+
+bool exchange_shared(const Plan &ps, const Plan &pl)
+{
+    const double a = double(ps.total_items), b = double(pl.total_items);
+    return a > kExchangeShareRatio * b || b > kExchangeShareRatio * a;
+}
+
+// Work counters and grid of a shared exchange; `next` is a zeroed 256-byte device word.
+bool duplex_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, const Plan &pl,
+                  unsigned *next, DuplexSync *sy, LaunchShape *sh)
+{
+    sy->unit_items = ps.batch;
+    sy->units_s = (ps.total_items + sy->unit_items - 1) / sy->unit_items;
+    sy->units_l = (pl.total_items + sy->unit_items - 1) / sy->unit_items;
+    sy->next = next;
+    if (ps.batch != pl.batch || sy->units_s >= (int64_t(1) << 31) ||
+        sy->units_l >= (int64_t(1) << 31))
+        return false;
+    const int64_t warps_per_cta = cfg.threads / 32;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
+    const int64_t needed = (sy->units_s + sy->units_l + warps_per_cta - 1) / warps_per_cta;
+    if (ctas > needed)
+        ctas = needed;
+    sh->ctas = ctas;
+    sh->threads = cfg.threads;
+    sh->fn = reinterpret_cast<const void *>(pick_duplex(cfg.unroll, ps.batch > 1));
+    return true;
+}
+
+cudaError_t launch_duplex_kernel(const LaunchShape &sh, Plan ps, Plan pl, DuplexSync sy,
+                                 cudaStream_t s)
+{
+    void *args[] = {&ps, &pl, &sy};
+    return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args, 0,
+                            s);
+}
+
+// Exchange grid: sm_cap covers both directions, half of the CTAs per direction.
+LaunchShape exchange_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps,
+                           const Plan &pl)
+{
+    LaunchShape sh;
+    const int64_t warps_per_cta = cfg.threads / 32;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    const int64_t per_dir = (int64_t(sms) * cfg.ctas_per_sm + 1) / 2;
+    auto needed = [&](const Plan &p) {
+        const int64_t per_cta = warps_per_cta * p.batch;
+        return (p.total_items + per_cta - 1) / per_cta;
+    };
+    int64_t role = std::max(needed(ps), needed(pl));
+    if (role > per_dir)
+        role = per_dir;
+    sh.ctas = 2 * role;
+    sh.threads = cfg.threads;
+    sh.fn = reinterpret_cast<const void *>(pick_exchange(cfg.unroll, ps.batch, pl.batch));
+    return sh;
+}
+
+cudaError_t launch_exchange_kernel(const LaunchShape &sh, Plan ps, Plan pl, cudaStream_t s)
+{
+    void *args[] = {&ps, &pl};
+    return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args, 0,
+                            s);
+}
+
 kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *sreqs,
                            int n_sreq, const kvx_chunk *schunks, int n_schunks,
                            const kvx_request *lreqs, int n_lreq, const kvx_chunk *lchunks,
@@ -842,25 +1184,35 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
     if (ps.total_items + pl.total_items == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, total, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess)
-        return cuda_err(ctx, e, "descriptor copy");
-    // sm_cap covers both directions: half of the CTAs per direction.
-    const int64_t warps_per_cta = cfg.threads / 32;
-    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
-    const int64_t per_dir = (int64_t(sms) * cfg.ctas_per_sm + 1) / 2;
-    auto needed = [&](const Plan &p) {
-        const int64_t per_cta = warps_per_cta * p.batch;
-        return (p.total_items + per_cta - 1) / per_cta;
-    };
-    int64_t role = std::max(needed(ps), needed(pl));
-    if (role > per_dir)
-        role = per_dir;
-    const int64_t ctas = 2 * role;
-    ExchangeFn fn = pick_exchange(cfg.unroll, ps.batch, pl.batch);
-    void *args[] = {&ps, &pl};
-    e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
-                         dim3(unsigned(cfg.threads)), args, 0, s);
+    cudaError_t e;
+    int64_t ctas;
+    if (exchange_shared(ps, pl)) {
+        if (total + 256 > ctx->slot_bytes)
+            return set_err(ctx, KVX_ERR_CAPACITY, "descriptors need %zu bytes, the context "
+                           "holds %zu per call", total + 256, ctx->slot_bytes);
+        DuplexSync sy;
+        LaunchShape shape;
+        if (!duplex_setup(ctx, cfg, ps, pl, reinterpret_cast<unsigned *>(slot.dev + total), &sy,
+                          &shape))
+            return set_err(ctx, KVX_ERR_CAPACITY, "exchange batches of %lld and %lld segments "
+                           "(%d and %d per warp) do not fit one shared launch",
+                           (long long)ps.total_items, (long long)pl.total_items, ps.batch,
+                           pl.batch);
+        e = cudaMemcpyAsync(slot.dev, slot.host, total, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(slot.dev + total, 0, 256, s);
+        if (e != cudaSuccess)
+            return cuda_err(ctx, e, "descriptor copy");
+        e = launch_duplex_kernel(shape, ps, pl, sy, s);
+        ctas = shape.ctas;
+    } else {
+        e = cudaMemcpyAsync(slot.dev, slot.host, total, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess)
+            return cuda_err(ctx, e, "descriptor copy");
+        const LaunchShape shape = exchange_shape(ctx, cfg, ps, pl);
+        e = launch_exchange_kernel(shape, ps, pl, s);
+        ctas = shape.ctas;
+    }
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
     e = cudaEventRecord(slot.done, s);
@@ -875,13 +1227,110 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
     return KVX_OK;
 }
 
+// Descriptor slot of a round trip: the store plan, the load plan (same chunks, other page
+// tables), then the work counters and one completion word per unit, zeroed per launch.
+kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *src_reqs,
+                            const kvx_request *dst_reqs, int n_req, const kvx_chunk *chunks,
+                            int n_chunks, int layer_begin, int layer_end,
+                            const kvx_launch_cfg *user_cfg, kvx_stream_t stream)
+{
+    if (!ctx)
+        return KVX_ERR_INVALID_ARG;
+    ctx->last_items = 0;
+    ctx->last_ctas = 0;
+    ctx->last_threads = 0;
+    ctx->last_desc_bytes = 0;
+    kvx_launch_cfg cfg;
+    kvx_status st = resolve_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
+    if (st != KVX_OK)
+        return st;
+    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "round trip runs the warp-segment mapping only");
+    st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
+                                n_chunks, layer_begin, layer_end, ctx->validation, true,
+                                ctx->err, sizeof ctx->err);
+    if (st != KVX_OK)
+        return st;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
+    const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
+    // Units from the packed item count (known after packing); bound the sync area first by
+    // the largest count the slot could describe.
+    Slot &slot = ctx->slots[ctx->next];
+    if (2 * lay.total + 256 > ctx->slot_bytes)
+        return set_err(ctx, KVX_ERR_CAPACITY,
+                       "descriptors need %zu bytes, the context holds %zu per call; create it "
+                       "with a larger max_descriptor_bytes", 2 * lay.total + 256,
+                       ctx->slot_bytes);
+    if (slot.used) {
+        cudaError_t e = cudaEventSynchronize(slot.done);
+        if (e != cudaSuccess)
+            return cuda_err(ctx, e, "waiting for a descriptor buffer");
+    }
+    Plan ps = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                        KVX_DIR_GATHER, lay, slot.host, slot.dev);
+    Plan pl = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                        KVX_DIR_SCATTER, lay, slot.host + lay.total, slot.dev + lay.total);
+    ps.status = pl.status = ctx->status_dev;
+    if (cfg.batch > 0)
+        ps.batch = pl.batch = cfg.batch;
+    if (ps.total_items == 0)
+        return KVX_OK;
+    RoundTripSync sy;
+    sy.unit_items = ps.batch;
+    sy.units = (ps.total_items + sy.unit_items - 1) / sy.unit_items;
+    const size_t sync_off = 2 * lay.total;
+    const size_t sync_bytes = 256 + sizeof(unsigned) * size_t(sy.units);
+    if (sy.units >= (int64_t(1) << 31) || sync_off + sync_bytes > ctx->slot_bytes)
+        return set_err(ctx, KVX_ERR_CAPACITY,
+                       "round trip of %lld units needs %zu bytes of descriptors and "
+                       "completion words, the context holds %zu per call",
+                       (long long)sy.units, sync_off + sync_bytes, ctx->slot_bytes);
+    sy.next = reinterpret_cast<unsigned *>(slot.dev + sync_off);
+    sy.done = reinterpret_cast<unsigned *>(slot.dev + sync_off + 256);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, sync_off, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(slot.dev + sync_off, 0, sync_bytes, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "descriptor copy");
+    const int64_t warps_per_cta = cfg.threads / 32;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
+    const int64_t needed = (2 * sy.units + warps_per_cta - 1) / warps_per_cta;
+    if (ctas > needed)
+        ctas = needed;
+    sy.lag = unsigned(ctas * warps_per_cta);  // one unit per warp of the grid
+    RoundTripFn fn = pick_roundtrip(cfg.unroll, ps.batch > 1);
+    void *args[] = {&ps, &pl, &sy};
+    e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
+                         dim3(unsigned(cfg.threads)), args, 0, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "kernel launch");
+    e = cudaEventRecord(slot.done, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "event record");
+    slot.used = true;
+    ctx->next = (ctx->next + 1) % kSlots;
+    ctx->last_items = 2 * ps.total_items;
+    ctx->last_ctas = int32_t(ctas);
+    ctx->last_threads = cfg.threads;
+    ctx->last_desc_bytes = int64_t(sync_off);
+    return KVX_OK;
+}
+
 }  // namespace
 
 // A transfer validated and packed once, its descriptors in device memory of its own.
 struct kvx_plan {
     kvx_ctx *ctx = nullptr;
     char *dev = nullptr;
-    Plan plan;
+    Plan plan;       // the transfer; the store half of an exchange
+    Plan load;       // the load half of an exchange
+    bool exchange = false;
+    bool shared = false;  // shared-work exchange: its counters are zeroed before each launch
+    DuplexSync sync;
     LaunchShape shape;
 };
 
@@ -940,13 +1389,88 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
     return KVX_OK;
 }
 
+kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
+                                    const kvx_request *sreqs, int n_sreq,
+                                    const kvx_chunk *schunks, int n_schunks,
+                                    const kvx_request *lreqs, int n_lreq,
+                                    const kvx_chunk *lchunks, int n_lchunks, int layer_begin,
+                                    int layer_end, const kvx_launch_cfg *user_cfg,
+                                    kvx_stream_t stream, kvx_plan **out)
+{
+    if (!ctx || !out)
+        return KVX_ERR_INVALID_ARG;
+    *out = nullptr;
+    kvx_launch_cfg cfg;
+    kvx_status st = resolve_cfg(ctx, KVX_OP_EXCHANGE, user_cfg, &cfg);
+    if (st != KVX_OK)
+        return st;
+    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "exchange runs the warp-segment mapping only");
+    st = kvx::validate_exchange(pool, sreqs, n_sreq, schunks, n_schunks, lreqs, n_lreq, lchunks,
+                                n_lchunks, layer_begin, layer_end, ctx->validation, true,
+                                ctx->err, sizeof ctx->err);
+    if (st != KVX_OK)
+        return st;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
+    const kvx::PackedLayout ls = kvx::packed_layout(pool, n_sreq, n_schunks);
+    const kvx::PackedLayout ll = kvx::packed_layout(pool, n_lreq, n_lchunks);
+    const size_t total = ls.total + ll.total;
+    kvx_plan *p = new kvx_plan();
+    p->ctx = ctx;
+    p->exchange = true;
+    std::vector<char> host(total);
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->dev), total + 256);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_err(ctx, e, "plan descriptor buffer");
+    }
+    p->plan = kvx::pack(pool, sreqs, n_sreq, schunks, n_schunks, layer_begin, layer_end,
+                        KVX_DIR_GATHER, ls, host.data(), p->dev);
+    p->load = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
+                        KVX_DIR_SCATTER, ll, host.data() + ls.total, p->dev + ls.total);
+    p->plan.status = p->load.status = ctx->status_dev;
+    if (cfg.batch > 0)
+        p->plan.batch = p->load.batch = cfg.batch;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaMemcpyAsync(p->dev, host.data(), total, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);  // the host image dies with this call
+    if (e != cudaSuccess) {
+        cudaFree(p->dev);
+        delete p;
+        return cuda_err(ctx, e, "plan descriptor copy");
+    }
+    p->shared = exchange_shared(p->plan, p->load);
+    if (!p->shared) {
+        p->shape = exchange_shape(ctx, cfg, p->plan, p->load);
+    } else if (!duplex_setup(ctx, cfg, p->plan, p->load,
+                             reinterpret_cast<unsigned *>(p->dev + total), &p->sync, &p->shape)) {
+        cudaFree(p->dev);
+        delete p;
+        return set_err(ctx, KVX_ERR_CAPACITY, "exchange batches do not fit one shared launch");
+    }
+    *out = p;
+    return KVX_OK;
+}
+
 kvx_status kvx_plan_launch(const kvx_plan *p, kvx_stream_t stream)
 {
     if (!p)
         return KVX_ERR_INVALID_ARG;
-    if (p->plan.total_items == 0)
+    if (p->plan.total_items + (p->exchange ? p->load.total_items : 0) == 0)
         return KVX_OK;
-    cudaError_t e = launch_kernel(p->shape, p->plan, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (p->shared) {
+        e = cudaMemsetAsync(p->sync.next, 0, 256, s);
+        if (e == cudaSuccess)
+            e = launch_duplex_kernel(p->shape, p->plan, p->load, p->sync, s);
+    } else {
+        e = p->exchange ? launch_exchange_kernel(p->shape, p->plan, p->load, s)
+                        : launch_kernel(p->shape, p->plan, s);
+    }
     if (e != cudaSuccess)
         return cuda_err(p->ctx, e, "plan launch");
     return KVX_OK;
@@ -1039,7 +1563,7 @@ kvx_status kvx_set_validation(kvx_ctx *ctx, int level)
 
 kvx_status kvx_default_launch_cfg(const kvx_ctx *ctx, int op, kvx_launch_cfg *cfg)
 {
-    if (!ctx || !cfg || op < KVX_OP_STORE || op > KVX_OP_EXCHANGE)
+    if (!ctx || !cfg || op < KVX_OP_STORE || op > KVX_OP_ROUNDTRIP)
         return KVX_ERR_INVALID_ARG;
     defaults_for(ctx, op, cfg);
     return KVX_OK;
@@ -1072,6 +1596,16 @@ kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
     return launch_exchange(ctx, pool, store_reqs, n_store_req, store_chunks, n_store_chunks,
                            load_reqs, n_load_req, load_chunks, n_load_chunks, layer_begin,
                            layer_end, cfg, stream);
+}
+
+kvx_status kvx_roundtrip_chunks(kvx_ctx *ctx, const kvx_pool *pool,
+                                const kvx_request *src_reqs, const kvx_request *dst_reqs,
+                                int n_req, const kvx_chunk *chunks, int n_chunks,
+                                int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                                kvx_stream_t stream)
+{
+    return launch_roundtrip(ctx, pool, src_reqs, dst_reqs, n_req, chunks, n_chunks, layer_begin,
+                            layer_end, cfg, stream);
 }
 
 kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,

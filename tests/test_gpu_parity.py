@@ -242,6 +242,8 @@ def test_exchange_store_and_load_in_one_launch(ctx, stream, seed):
     inp.write(data)
     store_specs = [] if seed % 6 == 5 else specs
     load_specs = [] if seed % 6 == 4 else specs
+    if seed % 6 == 3:  # a small load beside a large store: the shared-work kernel
+        load_specs = specs[:max(1, len(specs) // 4)]
     pre = dpool.host_copy()
     kvx.kvx_exchange_chunks(ctx, dpool.pool, src.array, kvx.chunks_array(store_specs, out.ptr),
                             dst.array, kvx.chunks_array(load_specs, inp.ptr), lb, le, c,
@@ -621,4 +623,114 @@ def test_prepared_plans_in_a_cuda_graph(ctx):
         kvx.kvx_plan_destroy(store)
         for p in loads:
             kvx.kvx_plan_destroy(p)
+        arena.close()
+
+
+@pytest.mark.parametrize("n_s,n_l", [(700, 500), (900, 120), (64, 1100)])
+def test_exchange_plans_match_the_oracle(ctx, stream, n_s, n_l):
+    """Exchange plans: store one batch and load another in one prepared launch, twice, with
+    new pool and chunk contents in between; also captured in a CUDA graph.  Similar batch
+    sizes run the role-split kernel, unequal ones the shared-work kernel."""
+    rng = np.random.default_rng(909 + n_s)
+    L, KV, P, v, NP = 3, 2, 16, 512, 200
+    pages_s, pages_l = -(-n_s // P), -(-n_l // P)
+    perm = rng.permutation(NP).astype(np.int32)
+    st_req = Requests([perm[:pages_s]], [n_s])
+    ld_req = Requests([perm[pages_s:pages_s + pages_l]], [n_l])
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    s_specs = wl.split_tokens(0, 0, n_s, 96, 0, L, wl.LAYER_MAJOR)
+    l_specs = wl.split_tokens(0, 0, n_l, 80, 0, L, wl.TOKEN_MAJOR)
+    wl.place_chunks(s_specs + l_specs, shape)
+    nbytes = wl._arena_bytes(s_specs + l_specs, shape)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    arena = Arena(nbytes, "host")
+    sch = kvx.chunks_array(s_specs, arena.ptr)
+    lch = kvx.chunks_array(l_specs, arena.ptr)
+    plan = kvx.kvx_plan_create_exchange(ctx, dpool.pool, st_req.array, sch, ld_req.array, lch,
+                                        stream=stream.cuda_stream)
+    s2 = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s2):
+        kvx.kvx_plan_launch(plan, torch.cuda.current_stream().cuda_stream)
+    try:
+        for round_ in range(3):
+            dpool.fill_random(910 + round_)
+            data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+            arena.write(data)
+            pre = dpool.host_copy()
+            torch.cuda.synchronize()
+            if round_ < 2:
+                kvx.kvx_plan_launch(plan, stream.cuda_stream)
+            else:
+                with torch.cuda.stream(s2):
+                    graph.replay()
+            torch.cuda.synchronize()
+            assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+            exp = data.copy()
+            oracle.store(pre, st_req.oracle(), oracle_chunks(s_specs, exp))
+            oracle.load(pre, ld_req.oracle(), oracle_chunks(l_specs, exp))
+            assert_bytes_equal(arena.numpy()[:nbytes + 4096], exp, "exchange plan chunks")
+            assert_pool_equal(dpool, pre)
+    finally:
+        del graph
+        kvx.kvx_plan_destroy(plan)
+        arena.close()
+
+
+RT_CONFIGS = [None, cfg(1, 1, 32, 1, 0), cfg(1, 1, 64, 8, 0), cfg(2, 1, 1024, 8, 0),
+              cfg(3, 1, 256, 4, 0, batch=5), cfg(1, 1, 32, 2, 0, batch=32),
+              cfg(0, 1, 1024, 8, 0), cfg(4, 2, 128, 2, 0, batch=3)]
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_roundtrip_in_one_launch(ctx, stream, seed):
+    """Store to host chunks and load them into the other page set in one launch; the
+    arena must hold the oracle's store and the pool the oracle's load of it."""
+    rng = np.random.default_rng(7100 + seed)
+    shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
+    L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size, shape.token_bytes,
+                       shape.num_pages)
+    c = RT_CONFIGS[seed % len(RT_CONFIGS)]
+    arena_bytes = wl._arena_bytes(specs, shape)
+    src = Requests(tables, lens)
+    dst = Requests(load_tables, lens)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(seed * 17 + 3)
+    arena = Arena(arena_bytes, "host")
+    pre = dpool.host_copy()
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                             kvx.chunks_array(specs, arena.ptr), lb, le, c, stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    exp = np.full(arena_bytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp), lb, le)
+    assert_bytes_equal(arena.numpy(), exp, f"seed {seed} round-trip chunks")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp), lb, le)
+    assert_pool_equal(dpool, pre)
+    arena.close()
+
+
+def test_roundtrip_rejects_overlapping_page_sets(ctx, stream):
+    """A load page set that meets the store's sources is refused (validation level 2)."""
+    rng = np.random.default_rng(7200)
+    L, KV, P, v, NP = 2, 2, 16, 256, 64
+    table = rng.permutation(NP)[:8].astype(np.int32)
+    other = table.copy()
+    other[3] = table[3]  # same page: overlap
+    other[:3] = rng.permutation(np.setdiff1d(np.arange(NP), table))[:3]
+    src, dst = Requests([table], [128]), Requests([other], [128])
+    specs = wl.split_tokens(0, 0, 128, 64, 0, L, wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    arena = Arena(wl._arena_bytes(specs, shape), "host")
+    kvx.kvx_set_validation(ctx, 2)
+    try:
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                                     kvx.chunks_array(specs, arena.ptr),
+                                     stream=stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_OVERLAP
+    finally:
+        kvx.kvx_set_validation(ctx, 1)
         arena.close()

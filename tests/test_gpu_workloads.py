@@ -175,6 +175,34 @@ def test_llama8b_pipelined_round_trip_as_benchmarked(ctx):
     hp.close()
 
 
+def test_llama8b_roundtrip_in_one_launch_as_benchmarked(ctx):
+    """The headline step exactly as bench.py runs it: one kvx_roundtrip_chunks launch that
+    stores every chunk and loads it into the fresh page set, twice in a row, in the
+    library's default launch configuration."""
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pools(s, w.seed)
+    hp = HostPool(pools, s.page_size)
+    src, dst = _requests(w.store_requests), _requests(w.load_requests)
+    arena = kvx.HostBuffer(w.store_arena_bytes + 4096)
+    arena.array[:] = CANARY
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    chunks = kvx.chunks_array(w.store_chunks, arena.ptr)
+    stream = torch.cuda.Stream()
+    for _ in range(2):
+        kvx.kvx_roundtrip_chunks(ctx, pool, src.array, dst.array, chunks,
+                                 stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    expect = np.full(w.store_arena_bytes + 4096, CANARY, np.uint8)
+    oracle.store(hp.pool, src.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
+    assert_bytes_equal(arena.array, expect, "llama8b round-trip store")
+    oracle.load(hp.pool, dst.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
+    _compare_pool(pools, hp.pool, "llama8b round-trip load")
+    arena.close()
+    hp.close()
+
+
 # ----------------------------------------------------------------------------- llama70b
 
 def test_llama70b_layer_streamed_load_full_size(ctx):
