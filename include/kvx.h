@@ -289,6 +289,15 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
                                     const kvx_chunk *load_chunks, int n_load_chunks,
                                     int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
                                     kvx_stream_t stream, kvx_plan **out);
+/* The round trip of kvx_roundtrip_chunks, validated and packed once.  Each launch first
+ * zeroes the plan's work counters and completion words (a memset on `stream`, captured
+ * with the kernel in a CUDA graph), so launches of one such plan must not overlap in time;
+ * the same holds for an exchange plan whose batches differ by more than 1.5x. */
+kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
+                                     const kvx_request *src_reqs, const kvx_request *dst_reqs,
+                                     int n_req, const kvx_chunk *chunks, int n_chunks,
+                                     int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
+                                     kvx_stream_t stream, kvx_plan **out);
 kvx_status kvx_plan_launch(const kvx_plan *plan, kvx_stream_t stream);
 void kvx_plan_destroy(kvx_plan *plan);
 

@@ -1227,6 +1227,44 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
     return KVX_OK;
 }
 
+// Units, lag and grid of a round trip whose work counters and completion words start at
+// `sync` (sync_bytes(), zeroed before each launch).
+void roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, char *sync,
+                     RoundTripSync *sy, LaunchShape *sh)
+{
+    sy->unit_items = ps.batch;
+    sy->units = (ps.total_items + sy->unit_items - 1) / sy->unit_items;
+    sy->next = reinterpret_cast<unsigned *>(sync);
+    sy->done = reinterpret_cast<unsigned *>(sync + 256);
+    const int64_t warps_per_cta = cfg.threads / 32;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
+    const int64_t needed = (2 * sy->units + warps_per_cta - 1) / warps_per_cta;
+    if (ctas > needed)
+        ctas = needed;
+    sy->lag = unsigned(ctas * warps_per_cta);  // one unit per warp of the grid
+    sh->ctas = ctas;
+    sh->threads = cfg.threads;
+    sh->fn = reinterpret_cast<const void *>(pick_roundtrip(cfg.unroll, ps.batch > 1));
+}
+
+size_t roundtrip_sync_bytes(const Plan &ps)
+{
+    const int64_t units = (ps.total_items + ps.batch - 1) / ps.batch;
+    return 256 + sizeof(unsigned) * size_t(units);
+}
+
+cudaError_t launch_roundtrip_kernel(const LaunchShape &sh, Plan ps, Plan pl, RoundTripSync sy,
+                                    size_t sync_bytes, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(sy.next, 0, sync_bytes, s);
+    if (e != cudaSuccess)
+        return e;
+    void *args[] = {&ps, &pl, &sy};
+    return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args, 0,
+                            s);
+}
+
 // Descriptor slot of a round trip: the store plan, the load plan (same chunks, other page
 // tables), then the work counters and one completion word per unit, zeroed per launch.
 kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *src_reqs,
@@ -1277,37 +1315,24 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
         ps.batch = pl.batch = cfg.batch;
     if (ps.total_items == 0)
         return KVX_OK;
-    RoundTripSync sy;
-    sy.unit_items = ps.batch;
-    sy.units = (ps.total_items + sy.unit_items - 1) / sy.unit_items;
     const size_t sync_off = 2 * lay.total;
-    const size_t sync_bytes = 256 + sizeof(unsigned) * size_t(sy.units);
-    if (sy.units >= (int64_t(1) << 31) || sync_off + sync_bytes > ctx->slot_bytes)
+    const size_t sync_bytes = roundtrip_sync_bytes(ps);
+    if (sync_bytes > (size_t(1) << 33) || sync_off + sync_bytes > ctx->slot_bytes)
         return set_err(ctx, KVX_ERR_CAPACITY,
-                       "round trip of %lld units needs %zu bytes of descriptors and "
+                       "round trip of %lld segments needs %zu bytes of descriptors and "
                        "completion words, the context holds %zu per call",
-                       (long long)sy.units, sync_off + sync_bytes, ctx->slot_bytes);
-    sy.next = reinterpret_cast<unsigned *>(slot.dev + sync_off);
-    sy.done = reinterpret_cast<unsigned *>(slot.dev + sync_off + 256);
+                       (long long)ps.total_items, sync_off + sync_bytes, ctx->slot_bytes);
+    RoundTripSync sy;
+    LaunchShape shape;
+    roundtrip_setup(ctx, cfg, ps, slot.dev + sync_off, &sy, &shape);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, sync_off, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemsetAsync(slot.dev + sync_off, 0, sync_bytes, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
-    const int64_t warps_per_cta = cfg.threads / 32;
-    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
-    int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
-    const int64_t needed = (2 * sy.units + warps_per_cta - 1) / warps_per_cta;
-    if (ctas > needed)
-        ctas = needed;
-    sy.lag = unsigned(ctas * warps_per_cta);  // one unit per warp of the grid
-    RoundTripFn fn = pick_roundtrip(cfg.unroll, ps.batch > 1);
-    void *args[] = {&ps, &pl, &sy};
-    e = cudaLaunchKernel(reinterpret_cast<const void *>(fn), dim3(unsigned(ctas)),
-                         dim3(unsigned(cfg.threads)), args, 0, s);
+    e = launch_roundtrip_kernel(shape, ps, pl, sy, sync_bytes, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
+    const int64_t ctas = shape.ctas;
     e = cudaEventRecord(slot.done, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "event record");
@@ -1329,8 +1354,11 @@ struct kvx_plan {
     Plan plan;       // the transfer; the store half of an exchange
     Plan load;       // the load half of an exchange
     bool exchange = false;
-    bool shared = false;  // shared-work exchange: its counters are zeroed before each launch
+    bool shared = false;     // shared-work exchange: its counters are zeroed before each launch
+    bool roundtrip = false;  // round trip: counters and completion words zeroed per launch
     DuplexSync sync;
+    RoundTripSync rsync;
+    size_t sync_bytes = 0;
     LaunchShape shape;
 };
 
@@ -1455,15 +1483,80 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
     return KVX_OK;
 }
 
+kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
+                                     const kvx_request *src_reqs, const kvx_request *dst_reqs,
+                                     int n_req, const kvx_chunk *chunks, int n_chunks,
+                                     int layer_begin, int layer_end,
+                                     const kvx_launch_cfg *user_cfg, kvx_stream_t stream,
+                                     kvx_plan **out)
+{
+    if (!ctx || !out)
+        return KVX_ERR_INVALID_ARG;
+    *out = nullptr;
+    kvx_launch_cfg cfg;
+    kvx_status st = resolve_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
+    if (st != KVX_OK)
+        return st;
+    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "round trip runs the warp-segment mapping only");
+    st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
+                                n_chunks, layer_begin, layer_end, ctx->validation, true,
+                                ctx->err, sizeof ctx->err);
+    if (st != KVX_OK)
+        return st;
+    DeviceGuard guard(ctx->device);
+    if (!guard.ok)
+        return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
+    const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
+    std::vector<char> host(2 * lay.total);
+    kvx_plan *p = new kvx_plan();
+    p->ctx = ctx;
+    p->exchange = true;
+    p->roundtrip = true;
+    // Pack once to learn the item count (device addresses not final), then size the
+    // allocation and pack again.
+    p->plan = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                        KVX_DIR_GATHER, lay, host.data(), host.data());
+    if (cfg.batch > 0)
+        p->plan.batch = cfg.batch;
+    p->sync_bytes = roundtrip_sync_bytes(p->plan);
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->dev), 2 * lay.total + p->sync_bytes);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_err(ctx, e, "plan descriptor buffer");
+    }
+    p->plan = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                        KVX_DIR_GATHER, lay, host.data(), p->dev);
+    p->load = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
+                        KVX_DIR_SCATTER, lay, host.data() + lay.total, p->dev + lay.total);
+    p->plan.status = p->load.status = ctx->status_dev;
+    if (cfg.batch > 0)
+        p->plan.batch = p->load.batch = cfg.batch;
+    roundtrip_setup(ctx, cfg, p->plan, p->dev + 2 * lay.total, &p->rsync, &p->shape);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaMemcpyAsync(p->dev, host.data(), 2 * lay.total, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);  // the host image dies with this call
+    if (e != cudaSuccess) {
+        cudaFree(p->dev);
+        delete p;
+        return cuda_err(ctx, e, "plan descriptor copy");
+    }
+    *out = p;
+    return KVX_OK;
+}
+
 kvx_status kvx_plan_launch(const kvx_plan *p, kvx_stream_t stream)
 {
     if (!p)
         return KVX_ERR_INVALID_ARG;
-    if (p->plan.total_items + (p->exchange ? p->load.total_items : 0) == 0)
+    if (p->plan.total_items + (p->exchange && !p->roundtrip ? p->load.total_items : 0) == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (p->shared) {
+    if (p->roundtrip) {
+        e = launch_roundtrip_kernel(p->shape, p->plan, p->load, p->rsync, p->sync_bytes, s);
+    } else if (p->shared) {
         e = cudaMemsetAsync(p->sync.next, 0, 256, s);
         if (e == cudaSuccess)
             e = launch_duplex_kernel(p->shape, p->plan, p->load, p->sync, s);

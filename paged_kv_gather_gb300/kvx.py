@@ -143,6 +143,9 @@ _proto("kvx_plan_create_exchange", _c.c_int,
        [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int,
         _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _P(kvx_launch_cfg), _c.c_void_p,
         _P(_c.c_void_p)])
+_proto("kvx_plan_create_roundtrip", _c.c_int,
+       [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_int,
+        _c.c_int, _P(kvx_launch_cfg), _c.c_void_p, _P(_c.c_void_p)])
 _proto("kvx_plan_launch", _c.c_int, [_c.c_void_p, _c.c_void_p])
 _proto("kvx_plan_destroy", None, [_c.c_void_p])
 _proto("kvx_transform_hbm", _c.c_int,
@@ -179,7 +182,7 @@ _proto("kvx_load_chunks_noalloc", _c.c_int, [*_batch, _P(kvx_launch_cfg), _c.c_v
 EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_launch_cfg",
             "kvx_store_chunks", "kvx_load_chunks", "kvx_exchange_chunks", "kvx_roundtrip_chunks",
             "kvx_plan_create",
-            "kvx_plan_create_exchange", "kvx_plan_launch", "kvx_plan_destroy", "kvx_transform_hbm", "kvx_dma_baseline",
+            "kvx_plan_create_exchange", "kvx_plan_create_roundtrip", "kvx_plan_launch", "kvx_plan_destroy", "kvx_transform_hbm", "kvx_dma_baseline",
             "kvx_get_status", "kvx_last_error", "kvx_last_launch", "kvx_validate",
             "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
@@ -398,6 +401,24 @@ def kvx_plan_create_exchange(ctx, pool: Pool, store_reqs, store_chunks, load_req
     _check(ctx, _lib.kvx_plan_create_exchange(ctx, ctypes.byref(pool.c), srp, nsr, scp, nsc,
                                               lrp, nlr, lcp, nlc, layer_begin, layer_end,
                                               _cfg_ptr(cfg), stream, ctypes.byref(h)))
+    return h
+
+
+def kvx_plan_create_roundtrip(ctx, pool: Pool, src_reqs, dst_reqs, chunks, layer_begin: int = 0,
+                              layer_end: Optional[int] = None,
+                              cfg: Optional[kvx_launch_cfg] = None, stream: int = 0):
+    """kvx_roundtrip_chunks validated and packed once; launch it with kvx_plan_launch."""
+    srp, nsr = _arr_ptr(src_reqs, REQUEST_DTYPE)
+    drp, ndr = _arr_ptr(dst_reqs, REQUEST_DTYPE)
+    if nsr != ndr:
+        raise ValueError("src_reqs and dst_reqs need the same number of requests")
+    cp, nc = _arr_ptr(chunks, CHUNK_DTYPE)
+    if layer_end is None:
+        layer_end = pool.c.num_layers
+    h = ctypes.c_void_p()
+    _check(ctx, _lib.kvx_plan_create_roundtrip(ctx, ctypes.byref(pool.c), srp, drp, nsr, cp, nc,
+                                               layer_begin, layer_end, _cfg_ptr(cfg), stream,
+                                               ctypes.byref(h)))
     return h
 
 

@@ -734,3 +734,77 @@ def test_roundtrip_rejects_overlapping_page_sets(ctx, stream):
     finally:
         kvx.kvx_set_validation(ctx, 1)
         arena.close()
+
+
+def test_roundtrip_plan_and_graph(ctx):
+    """A round-trip plan launched directly and from a CUDA graph, each time on fresh pool
+    contents; counters and completion words are reset by the launch itself."""
+    rng = np.random.default_rng(7300)
+    shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
+    L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size, shape.token_bytes,
+                       shape.num_pages)
+    arena_bytes = wl._arena_bytes(specs, shape)
+    src, dst = Requests(tables, lens), Requests(load_tables, lens)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    arena = Arena(arena_bytes, "host")
+    s = torch.cuda.Stream()
+    plan = kvx.kvx_plan_create_roundtrip(ctx, dpool.pool, src.array, dst.array,
+                                         kvx.chunks_array(specs, arena.ptr), lb, le,
+                                         cfg(3, 1, 128, 8, 0, batch=3), s.cuda_stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        kvx.kvx_plan_launch(plan, torch.cuda.current_stream().cuda_stream)
+    try:
+        for round_ in range(4):
+            dpool.fill_random(7301 + round_)
+            pre = dpool.host_copy()
+            torch.cuda.synchronize()
+            if round_ % 2 == 0:
+                kvx.kvx_plan_launch(plan, s.cuda_stream)
+            else:
+                with torch.cuda.stream(s):
+                    graph.replay()
+            torch.cuda.synchronize()
+            assert kvx.kvx_get_status(ctx, s.cuda_stream) == 0
+            # Every round writes the same chunk bytes, so the arena holds exactly this round's
+            # store over the canary fill.
+            exp = np.full(arena_bytes + 4096, CANARY, np.uint8)
+            oracle.store(pre, src.oracle(), oracle_chunks(specs, exp), lb, le)
+            assert_bytes_equal(arena.numpy(), exp, f"round {round_} chunk bytes")
+            oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp), lb, le)
+            assert_pool_equal(dpool, pre)
+    finally:
+        del graph
+        kvx.kvx_plan_destroy(plan)
+        arena.close()
+
+
+def test_roundtrip_with_more_ctas_than_can_be_resident(ctx, stream):
+    """608 CTAs of 1024 threads on 152 SMs: most start only after others finish, so a warp
+    may wait on a store held by any running warp but never on one not yet started."""
+    rng = np.random.default_rng(7400)
+    L, KV, P, v, n_tok = 32, 2, 16, 2048, 4096        # 16,384 segments of 32 KiB each way
+    pages = n_tok // P
+    NP = 2 * pages + 5
+    perm = rng.permutation(NP).astype(np.int32)
+    src, dst = Requests([perm[:pages]], [n_tok]), Requests([perm[pages:2 * pages]], [n_tok])
+    specs = wl.split_tokens(0, 0, n_tok, 256, 0, L, wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(7401)
+    arena = Arena(nbytes, "host")
+    pre = dpool.host_copy()
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                             kvx.chunks_array(specs, arena.ptr), 0, L, cfg(0, 4, 1024, 8, 0),
+                             stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    assert kvx.kvx_last_launch(ctx)[1] == 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+    assert_bytes_equal(arena.numpy(), exp, "round trip, oversubscribed grid")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
+    assert_pool_equal(dpool, pre)
+    arena.close()
