@@ -205,11 +205,14 @@ def test_llama8b_roundtrip_in_one_launch_as_benchmarked(ctx):
 
 # ----------------------------------------------------------------------------- llama70b
 
-def test_llama70b_layer_streamed_load_full_size(ctx):
-    """80 per-layer loads on a high-priority stream, as the streamed prefill issues them."""
-    w = wl.llama70b()
+@pytest.mark.parametrize("tokens_per_chunk", [256, 512])
+def test_llama70b_layer_streamed_load_full_size(ctx, tokens_per_chunk):
+    """80 per-layer loads on a high-priority stream, as the streamed prefill issues them;
+    per-layer chunks of 256 tokens (1 MiB, the closed form) and of 512 tokens (2 MiB)."""
+    w = wl.llama70b(tokens_per_chunk=tokens_per_chunk)
     s = w.shape
     assert w.load_bytes() == 20 << 30
+    assert all(c.nbytes(s) == tokens_per_chunk * 4096 for c in w.load_chunks)
     pools = _pools(s, w.seed, fill=CANARY)
     dst = _requests(w.load_requests)
     nbytes = w.load_arena_bytes
