@@ -179,7 +179,10 @@ typedef struct kvx_ctx kvx_ctx;
 
 /* Create a context on `device` whose descriptor buffers hold up to
  * max_descriptor_bytes each (0 = 8 MiB; about 72 bytes per chunk).  Allocates four
- * pinned host + device descriptor buffers and a device status word.  Requires a GPU. */
+ * pinned host + device descriptor buffers, a device status word and a non-blocking stream
+ * on which each call copies its descriptors (the caller's stream waits for that copy with
+ * an event, so the copy overlaps the previous kernel).  Calls therefore cannot be captured
+ * into a CUDA graph; prepared plans (below) can.  Requires a GPU. */
 kvx_status kvx_create(kvx_ctx **out, int device, size_t max_descriptor_bytes);
 
 /* Synchronize with every kernel the context launched, then free its buffers. */

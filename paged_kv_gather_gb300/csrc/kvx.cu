@@ -789,7 +789,8 @@ const int64_t kMaxBulkSmem = 220 << 10;
 struct Slot {
     char *host = nullptr;
     char *dev = nullptr;
-    cudaEvent_t done = nullptr;
+    cudaEvent_t done = nullptr;    // recorded on the caller's stream after the kernel
+    cudaEvent_t staged = nullptr;  // recorded on the copy stream after the descriptor copy
     bool used = false;
 };
 
@@ -802,6 +803,9 @@ struct kvx_ctx {
     size_t slot_bytes = 0;
     Slot slots[kSlots];
     int next = 0;
+    // Descriptor copies run here, beside the caller's stream, so that a call's copy overlaps
+    // the previous call's kernel instead of sitting between two kernels.
+    cudaStream_t copy_stream = nullptr;
     unsigned int *status_dev = nullptr;
     unsigned int *status_host = nullptr;
     int64_t last_items = 0;
@@ -830,6 +834,22 @@ kvx_status set_err(kvx_ctx *ctx, kvx_status st, const char *fmt, ...)
 kvx_status cuda_err(kvx_ctx *ctx, cudaError_t e, const char *what)
 {
     return set_err(ctx, KVX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Copy a call's packed descriptors into its slot on the context's copy stream (zeroing
+// `zero_bytes` at `zero_off` after them), and make the caller's stream wait for that.
+cudaError_t stage(kvx_ctx *ctx, Slot &slot, size_t bytes, size_t zero_off, size_t zero_bytes,
+                  cudaStream_t s)
+{
+    cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, bytes, cudaMemcpyHostToDevice,
+                                    ctx->copy_stream);
+    if (e == cudaSuccess && zero_bytes)
+        e = cudaMemsetAsync(slot.dev + zero_off, 0, zero_bytes, ctx->copy_stream);
+    if (e == cudaSuccess)
+        e = cudaEventRecord(slot.staged, ctx->copy_stream);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(s, slot.staged, 0);
+    return e;
 }
 
 // Keeps ctx->device current for the duration of a call and restores the caller's device.
@@ -1044,7 +1064,7 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
         return KVX_OK;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, lay.total, cudaMemcpyHostToDevice, s);
+    cudaError_t e = stage(ctx, slot, lay.total, 0, 0, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
     const LaunchShape shape = launch_shape(ctx, cfg, plan, dir);
@@ -1198,15 +1218,13 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
                            "(%d and %d per warp) do not fit one shared launch",
                            (long long)ps.total_items, (long long)pl.total_items, ps.batch,
                            pl.batch);
-        e = cudaMemcpyAsync(slot.dev, slot.host, total, cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess)
-            e = cudaMemsetAsync(slot.dev + total, 0, 256, s);
+        e = stage(ctx, slot, total, total, 256, s);
         if (e != cudaSuccess)
             return cuda_err(ctx, e, "descriptor copy");
         e = launch_duplex_kernel(shape, ps, pl, sy, s);
         ctas = shape.ctas;
     } else {
-        e = cudaMemcpyAsync(slot.dev, slot.host, total, cudaMemcpyHostToDevice, s);
+        e = stage(ctx, slot, total, 0, 0, s);
         if (e != cudaSuccess)
             return cuda_err(ctx, e, "descriptor copy");
         const LaunchShape shape = exchange_shape(ctx, cfg, ps, pl);
@@ -1254,12 +1272,16 @@ size_t roundtrip_sync_bytes(const Plan &ps)
     return 256 + sizeof(unsigned) * size_t(units);
 }
 
+// sync_bytes > 0: zero the counters and completion words on `s` first (plans; calls zero
+// them with their descriptor copy).
 cudaError_t launch_roundtrip_kernel(const LaunchShape &sh, Plan ps, Plan pl, RoundTripSync sy,
                                     size_t sync_bytes, cudaStream_t s)
 {
-    cudaError_t e = cudaMemsetAsync(sy.next, 0, sync_bytes, s);
-    if (e != cudaSuccess)
-        return e;
+    if (sync_bytes) {
+        cudaError_t e = cudaMemsetAsync(sy.next, 0, sync_bytes, s);
+        if (e != cudaSuccess)
+            return e;
+    }
     void *args[] = {&ps, &pl, &sy};
     return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args, 0,
                             s);
@@ -1326,10 +1348,10 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
     LaunchShape shape;
     roundtrip_setup(ctx, cfg, ps, slot.dev + sync_off, &sy, &shape);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, sync_off, cudaMemcpyHostToDevice, s);
+    cudaError_t e = stage(ctx, slot, sync_off, sync_off, sync_bytes, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
-    e = launch_roundtrip_kernel(shape, ps, pl, sy, sync_bytes, s);
+    e = launch_roundtrip_kernel(shape, ps, pl, sy, 0, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
     const int64_t ctas = shape.ctas;
@@ -1605,7 +1627,11 @@ kvx_status kvx_create(kvx_ctx **out, int device, size_t max_descriptor_bytes)
             e = cudaMalloc(reinterpret_cast<void **>(&ctx->slots[i].dev), ctx->slot_bytes);
         if (e == cudaSuccess)
             e = cudaEventCreateWithFlags(&ctx->slots[i].done, cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&ctx->slots[i].staged, cudaEventDisableTiming);
     }
+    if (e == cudaSuccess)
+        e = cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess)
         e = cudaMalloc(reinterpret_cast<void **>(&ctx->status_dev), 256);
     if (e == cudaSuccess)
@@ -1633,10 +1659,16 @@ void kvx_destroy(kvx_ctx *ctx)
                     cudaEventSynchronize(s.done);
                 cudaEventDestroy(s.done);
             }
+            if (s.staged)
+                cudaEventDestroy(s.staged);
             if (s.dev)
                 cudaFree(s.dev);
             if (s.host)
                 cudaFreeHost(s.host);
+        }
+        if (ctx->copy_stream) {
+            cudaStreamSynchronize(ctx->copy_stream);
+            cudaStreamDestroy(ctx->copy_stream);
         }
         if (ctx->status_dev)
             cudaFree(ctx->status_dev);
