@@ -80,6 +80,8 @@ def parse():
                            "0:2:256:8:1:0:4,0:1:256:8:1:0:2,0:2:128:8:1:0:2,0:2:256:4:1:0:2",
                    help="mapping:ctas_per_sm:threads:unroll:hint:stage_bytes:batch launch "
                         "shapes of --workload transform_sweep")
+    p.add_argument("--mla-pages", default="1,16,64",
+                   help="page sizes of the MLA round trip in --workload roundtrip_sweep")
     p.add_argument("--chunk-tokens", type=int, default=256,
                    help="tokens per per-layer chunk of --workload llama70b (256 = 1 MiB, the "
                         "closed form; 512 = 2 MiB)")
@@ -1478,6 +1480,31 @@ def run_roundtrip_sweep(args, kvx, wl):
         for h in plans.values():
             kvx.kvx_plan_destroy(h)
     host.close()
+    del pools
+    torch.cuda.empty_cache()
+    # The one-launch round trip on the MLA latent (61 layers, 1152-byte tokens, per-layer
+    # chunks of 1 MiB): short page segments use the batched lookup.
+    for P in [int(x) for x in args.mla_pages.split(",") if x]:
+        m = wl.mla_sweep(page_size=P, chunk_bytes=1 << 20)
+        ms_ = m.shape
+        Nm = m.store_bytes()
+        mp = _pool_tensor(ms_, m.seed, wl)
+        mpool = kvx.Pool.from_tensor(mp, P)
+        a, b = m.store_requests[0], m.load_requests[0]
+        ad, bd = torch.from_numpy(a.page_table).cuda(), torch.from_numpy(b.page_table).cuda()
+        mrs = kvx.requests_array([(ad.data_ptr(), a.page_table, a.n_tokens)])
+        mrd = kvx.requests_array([(bd.data_ptr(), b.page_table, b.n_tokens)])
+        mh = kvx.HostBuffer(m.store_arena_bytes)
+        mh.array[:] = 0
+        mch = kvx.chunks_array(m.store_chunks, mh.ptr)
+        ms = _timed(stream, lambda: kvx.kvx_roundtrip_chunks(ctx, mpool, mrs, mrd, mch,
+                                                             stream=sh), reps)
+        assert kvx.kvx_get_status(ctx, sh) == 0
+        _emit({"workload": "mla_roundtrip_one_launch", "page_size": P, "chunk_bytes": 1 << 20,
+               "bytes_each_way": Nm, "segments_each_way": kvx.kvx_last_launch(ctx)[0] // 2,
+               "ms": round(ms, 4), "gbs": round(2 * Nm / (ms * 1e-3) / GB, 2)})
+        mh.close()
+        del mp
     kvx.kvx_destroy(ctx)
 
 
