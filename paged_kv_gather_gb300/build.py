@@ -20,8 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libkvx.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = [os.path.join(CSRC, f) for f in ("kvx.cu", "kvx_host.cpp", "kvx_partition.cpp",
-                                             "kvx_internal.h")]
+SOURCES = [os.path.join(CSRC, f) for f in ("kvx.cu", "kvx_kernels.cuh", "kvx_host.cpp",
+                                             "kvx_partition.cpp", "kvx_internal.h")]
 HEADER = os.path.join(ROOT, "include", "kvx.h")
 
 

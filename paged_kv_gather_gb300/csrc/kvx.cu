@@ -1,17 +1,7 @@
-// kvx.cu -- GB300 (sm_103a) kernels and C-ABI entry points of the paged KV gather/scatter
-// library.
-//
-// One kernel family moves every byte.  A persistent grid of warps walks the batch's work
-// items; an item is one (chunk, layer, kv, page) segment, contiguous on the page side
-// ("Strata Guide: Hierarchical Context Caching for Long LLMs", section "Two-Dimensional
-// Memory Layout Decoupling": the layout change is address arithmetic done by the moving
-// thread, not a separate pass).  Each lane moves 16-byte units ("Step 1:
-// High-Performance GPU-Assisted I/O CUDA Kernel": 128-bit vector accesses, a page-table
-// lookup per unit of work, streaming stores into HBM), with `unroll` independent loads in
-// flight per lane before its stores, because host-link reads need many bytes in flight
-// (section "The Physics of I/O Bandwidth and Little's Law": X = C * S / L).  The grid is
-// capped to a few SMs for host transfers so a concurrent compute stream keeps the rest
-// (section "Non-Intrusive Resource Sizing"); the HBM-only transform uses every SM.
+// kvx.cu -- C-ABI entry points of the paged KV gather/scatter library: contexts,
+// descriptor staging, launch shapes, prepared plans, the per-page DMA baseline and the
+// allocation-free load.  The kernels are in kvx_kernels.cuh; host-only validation and
+// packing are in kvx_host.cpp.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -22,759 +12,7 @@
 #include <mutex>
 
 #include "kvx_internal.h"
-
-using kvx::DevChunk;
-using kvx::Plan;
-
-// ------------------------------------------------------------------------------- device
-
-namespace {
-
-__device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p)
-{
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
-
-// Coherent 16-byte load, cached in L2 only: for bytes another warp of the same launch wrote
-// (the read-only .nc path is valid only for data no thread writes during the launch).
-__device__ __forceinline__ uint4 ld_cg_v4(const uint4 *p)
-{
-    uint4 r;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p)
-                 : "memory");
-    return r;
-}
-
-template <bool NC>
-__device__ __forceinline__ uint4 ld_v4(const uint4 *p)
-{
-    return NC ? ld_nc_v4(p) : ld_cg_v4(p);
-}
-
-template <int HINT>
-__device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v)
-{
-    if (HINT == KVX_HINT_STREAMING)
-        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                     "r"(v.z), "r"(v.w)
-                     : "memory");
-    else
-        asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                     "r"(v.z), "r"(v.w)
-                     : "memory");
-}
-
-// Chunk owning `item`: the largest c with item_begin[c] <= item.  A 32-way search: each
-// step the warp probes 32 evenly spaced entries and keeps the last one not above `item`,
-// so 18k chunks take three coalesced probes.
-__device__ __forceinline__ int find_chunk(const int64_t *__restrict__ begin, int n, int64_t item,
-                                          int lane)
-{
-    int lo = 0, hi = n;  // begin[lo] <= item < begin[hi]
-    while (hi - lo > 1) {
-        const int step = (hi - lo + 31) >> 5;
-        const int idx = lo + lane * step;
-        const bool ok = idx < hi && __ldg(begin + idx) <= item;
-        const unsigned m = __ballot_sync(0xffffffffu, ok);
-        lo += (31 - __clz(m)) * step;
-        hi = min(hi, lo + step);
-    }
-    return lo;
-}
-
-// Contiguous copy of n16 16-byte units.  Lane i owns units i, i + 32, i + 64, ...; each
-// pass issues U independent loads before its U stores.  NC = false reads through the
-// coherent path.
-template <int U, int HINT, bool NC = true>
-__device__ __forceinline__ void copy_contig(const uint4 *__restrict__ s, uint4 *__restrict__ d,
-                                            int n16, int lane)
-{
-    s += lane;
-    d += lane;
-    int rem = n16 - lane;  // units of this lane's stride left, scaled by 32
-    for (; rem > 32 * (U - 1); rem -= 32 * U, s += 32 * U, d += 32 * U) {
-        uint4 r[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            r[u] = ld_v4<NC>(s + 32 * u);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            st_v4<HINT>(d + 32 * u, r[u]);
-    }
-    if (rem > 0) {
-        uint4 r[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (32 * u < rem)
-                r[u] = ld_v4<NC>(s + 32 * u);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (32 * u < rem)
-                st_v4<HINT>(d + 32 * u, r[u]);
-    }
-}
-
-// One work item resolved to addresses: `rows` rows of row_bytes, contiguous on the page side
-// (pitch = token_bytes) and contiguous or strided on the chunk side.
-struct Segment {
-    const char *src;
-    char *dst;
-    int64_t s_pitch;
-    int64_t d_pitch;
-    int32_t rows;
-    bool contiguous;  // rows back to back on both sides: one run of rows * token_bytes
-};
-
-// Chunk owning `item` for one lane alone (plain binary search): used when every lane
-// resolves a different item.
-__device__ __forceinline__ int find_chunk_lane(const int64_t *__restrict__ begin, int n,
-                                               int64_t item)
-{
-    int lo = 0, hi = n;  // begin[lo] <= item < begin[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(begin + mid) <= item)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    return lo;
-}
-
-// Addresses of item `item` of chunk `c`.  Returns false, after flagging the device status
-// when `flag` is set, if the page id is outside the pool; the segment is then skipped.
-template <int DIR>
-__device__ __forceinline__ bool segment_of(const Plan &p, int c, int64_t item, bool flag,
-                                           Segment &sg)
-{
-    const int64_t v = p.token_bytes;
-    const DevChunk &ch = p.chunks[c];
-    const int64_t i = item - p.item_begin[c];
-    const int32_t np = ch.np;
-    const int32_t slab = int32_t(i / np);
-    const int32_t j = int32_t(i - int64_t(slab) * np);
-    const int32_t kv = p.kv_factor == 2 ? (slab & 1) : 0;
-    const int32_t layer = ch.la + (p.kv_factor == 2 ? (slab >> 1) : slab);
-    const int32_t lpage = ch.pf + j;
-    const int32_t pt0 = lpage * p.page_size;
-    const int32_t tb = max(ch.t0, pt0);
-    const int32_t te = min(ch.t_end, pt0 + p.page_size);
-    const int32_t page = p.reqs[ch.request].page_table[lpage];
-    if (unsigned(page) >= unsigned(p.num_pages)) {
-        if (flag)
-            atomicOr(p.status, KVX_DEV_PAGE_OUT_OF_RANGE);
-        return false;
-    }
-    char *pg = p.pools[kv * p.num_layers + layer] + (int64_t(page) * p.page_size + (tb - pt0)) * v;
-    char *ck = ch.ptr + int64_t(ch.slab0 + slab) * ch.slab_stride +
-               int64_t(tb - ch.t0) * ch.row_stride;
-    sg.src = DIR == KVX_DIR_GATHER ? pg : ck;
-    sg.dst = DIR == KVX_DIR_GATHER ? ck : pg;
-    sg.s_pitch = DIR == KVX_DIR_GATHER ? v : ch.row_stride;
-    sg.d_pitch = DIR == KVX_DIR_GATHER ? ch.row_stride : v;
-    sg.rows = te - tb;
-    sg.contiguous = ch.row_stride == v;
-    return true;
-}
-
-// Resolve item -> segment (warp-collective: every lane of the warp calls it with the same
-// item).
-template <int DIR>
-__device__ __forceinline__ bool resolve_segment(const Plan &p, int64_t item, int lane,
-                                                Segment &sg)
-{
-    const int c = find_chunk(p.item_begin, p.n_chunks, item, lane);
-    return segment_of<DIR>(p, c, item, lane == 0, sg);
-}
-
-__device__ __forceinline__ Segment shfl_segment(const Segment &s, int src_lane)
-{
-    Segment r;
-    r.src = reinterpret_cast<const char *>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(s.src), src_lane));
-    r.dst = reinterpret_cast<char *>(
-        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(s.dst), src_lane));
-    r.s_pitch = __shfl_sync(0xffffffffu, s.s_pitch, src_lane);
-    r.d_pitch = __shfl_sync(0xffffffffu, s.d_pitch, src_lane);
-    r.rows = __shfl_sync(0xffffffffu, s.rows, src_lane);
-    r.contiguous = __shfl_sync(0xffffffffu, int(s.contiguous), src_lane) != 0;
-    return r;
-}
-
-template <int U, int HINT, bool NC = true>
-__device__ __forceinline__ void copy_segment(const Segment &sg, int64_t v, int lane)
-{
-    if (sg.contiguous) {
-        copy_contig<U, HINT, NC>(reinterpret_cast<const uint4 *>(sg.src),
-                                 reinterpret_cast<uint4 *>(sg.dst),
-                                 int((int64_t(sg.rows) * v) >> 4), lane);
-    } else {
-        // Token-major chunk: each token is its own run on the chunk side.
-        for (int r = 0; r < sg.rows; ++r)
-            copy_contig<1, HINT, NC>(reinterpret_cast<const uint4 *>(sg.src + r * sg.s_pitch),
-                                     reinterpret_cast<uint4 *>(sg.dst + r * sg.d_pitch),
-                                     int(v >> 4), lane);
-    }
-}
-
-// Warp per page segment.  DIR = KVX_DIR_GATHER copies page -> chunk, KVX_DIR_SCATTER the
-// reverse.  BATCHED = false: a warp resolves one segment at a time (32-way search), for
-// page segments of 16 KiB and more.  BATCHED = true (short segments): each lane resolves
-// one of p.batch consecutive segments in parallel and the warp then copies them back to
-// back, so the lookup latency of short segments overlaps instead of adding up.
-template <int U, int DIR, int HINT, bool BATCHED>
-__device__ __forceinline__ void run_segments(const Plan &p, int64_t warp, int64_t n_warps,
-                                             int lane)
-{
-    const int64_t v = p.token_bytes;
-    if (!BATCHED) {
-        for (int64_t item = warp; item < p.total_items; item += n_warps) {
-            Segment sg;
-            if (resolve_segment<DIR>(p, item, lane, sg))
-                copy_segment<U, HINT>(sg, v, lane);
-        }
-    } else {
-        const int B = p.batch;
-        for (int64_t base = warp * B; base < p.total_items; base += n_warps * B) {
-            const int64_t mine = base + lane;
-            Segment sg;
-            sg.src = nullptr;
-            sg.dst = nullptr;
-            sg.s_pitch = sg.d_pitch = 0;
-            sg.rows = 0;
-            sg.contiguous = true;
-            bool ok = false;
-            if (lane < B && mine < p.total_items)
-                ok = segment_of<DIR>(p, find_chunk_lane(p.item_begin, p.n_chunks, mine), mine,
-                                     true, sg);
-            const unsigned valid = __ballot_sync(0xffffffffu, ok);
-            for (int k = 0; k < B; ++k) {
-                const Segment s = shfl_segment(sg, k);
-                if (valid & (1u << k))
-                    copy_segment<U, HINT>(s, v, lane);
-            }
-        }
-    }
-}
-
-template <int U, int DIR, int HINT, bool BATCHED>
-__global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
-{
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    run_segments<U, DIR, HINT, BATCHED>(p, warp, n_warps, lane);
-}
-
-// Exchange: one launch moves a store batch (pages -> host chunks) and a load batch (host
-// chunks -> pages) at once.  Even CTAs run the store plan, odd CTAs the load plan, so the
-// block scheduler spreads both directions evenly over the SMs the launch gets instead of
-// giving each direction its own contiguous block of SMs (two separate kernels), which
-// lets the two directions of the host link run at full rate together.
-template <int U, bool BATCHED_S, bool BATCHED_L>
-__global__ void __launch_bounds__(1024, 1) kvx_exchange_kernel(const Plan ps, const Plan pl)
-{
-    const int lane = threadIdx.x & 31;
-    const int64_t wpc = blockDim.x >> 5;
-    const int64_t role_cta = blockIdx.x >> 1;
-    const int64_t warp = role_cta * wpc + (threadIdx.x >> 5);
-    if ((blockIdx.x & 1) == 0) {
-        const int64_t ctas = (int64_t(gridDim.x) + 1) >> 1;
-        run_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S>(ps, warp, ctas * wpc, lane);
-    } else {
-        const int64_t ctas = int64_t(gridDim.x) >> 1;
-        run_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L>(pl, warp, ctas * wpc,
-                                                                        lane);
-    }
-}
-
-// ------------------------------------------------------------------ bulk-copy (TMA) mapping
-//
-// One warp per CTA streams its items through a ring of shared-memory stages with the
-// Blackwell bulk-copy engine: cp.async.bulk global -> shared completes on an mbarrier
-// (transaction bytes), then cp.async.bulk shared -> global (bulk group) writes the stage
-// out.  Up to n_stages - 1 loads are in flight per CTA without holding them in registers,
-// and the SM's load/store pipes stay free for other work.  Every wait is bounded: past
-// about one second the kernel flags KVX_DEV_WAIT_TIMEOUT, drains what it issued and exits.
-
-constexpr int kBulkMaxStages = 8;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-// Warp-uniform bounded wait for the completion of phase `parity` of an mbarrier.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int lane)
-{
-    const uint32_t addr = smem_u32(bar);
-    const uint64_t deadline = global_ns() + kWaitLimitNs;
-    while (true) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done)
-                     : "r"(addr), "r"(parity)
-                     : "memory");
-        if (__any_sync(0xffffffffu, done))
-            return true;
-        const int late = lane == 0 ? int(global_ns() > deadline) : 0;
-        if (__shfl_sync(0xffffffffu, late, 0))
-            return false;
-    }
-}
-
-__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
-                                          uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-                 "[%0], [%1], %2, [%3];" ::"r"(smem_u32(smem_dst)),
-                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_u32(smem_src)), "r"(bytes)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-template <int DIR>
-__global__ void __launch_bounds__(32) kvx_bulk_kernel(const Plan p, int stage_bytes,
-                                                     int n_stages)
-{
-    extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ __align__(8) uint64_t full[kBulkMaxStages];
-    __shared__ char *stage_dst[kBulkMaxStages];
-    __shared__ uint32_t stage_len[kBulkMaxStages];
-    const int lane = threadIdx.x;
-    const int64_t v = p.token_bytes;
-    if (lane == 0) {
-        for (int st = 0; st < n_stages; ++st)
-            mbar_init(&full[st], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-
-    // Piece stream: items of this CTA, cut into runs of at most stage_bytes.
-    int64_t item = blockIdx.x;
-    Segment sg;
-    bool have = false;
-    int32_t row = 0, n_rows = 0;
-    int64_t off = 0, row_bytes = 0;
-    auto next = [&](const char *&src, char *&dst, uint32_t &bytes) -> bool {
-        while (true) {
-            if (have) {
-                if (off < row_bytes) {
-                    const int64_t b = min(int64_t(stage_bytes), row_bytes - off);
-                    src = sg.src + row * sg.s_pitch + off;
-                    dst = sg.dst + row * sg.d_pitch + off;
-                    bytes = uint32_t(b);
-                    off += b;
-                    return true;
-                }
-                off = 0;
-                if (++row < n_rows)
-                    continue;
-                have = false;
-            }
-            if (item >= p.total_items)
-                return false;
-            if (resolve_segment<DIR>(p, item, lane, sg)) {
-                have = true;
-                row = 0;
-                off = 0;
-                n_rows = sg.contiguous ? 1 : sg.rows;
-                row_bytes = sg.contiguous ? int64_t(sg.rows) * v : v;
-            }
-            item += gridDim.x;
-        }
-    };
-
-    uint32_t issued = 0, retired = 0;
-    bool more = true, timed_out = false;
-    const char *src = nullptr;
-    char *dst = nullptr;
-    uint32_t bytes = 0;
-    auto issue = [&]() {
-        const uint32_t st = issued % n_stages;
-        if (lane == 0) {
-            stage_dst[st] = dst;
-            stage_len[st] = bytes;
-            mbar_expect_tx(&full[st], bytes);
-            bulk_load(ring + size_t(st) * stage_bytes, src, bytes, &full[st]);
-        }
-        ++issued;
-    };
-    while (issued + 1 < uint32_t(n_stages)) {
-        if (!next(src, dst, bytes)) {
-            more = false;
-            break;
-        }
-        issue();
-    }
-    while (retired < issued) {
-        const uint32_t st = retired % n_stages;
-        if (!mbar_wait(&full[st], (retired / n_stages) & 1u, lane)) {
-            timed_out = true;
-            break;
-        }
-        if (lane == 0)
-            bulk_store(stage_dst[st], ring + size_t(st) * stage_bytes, stage_len[st]);
-        ++retired;
-        if (more) {
-            if (!next(src, dst, bytes)) {
-                more = false;
-            } else {
-                // The stage about to be refilled was last written out by the store issued
-                // one iteration ago: wait until at most the newest store still reads.
-                if (lane == 0)
-                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                __syncwarp();
-                issue();
-            }
-        }
-    }
-    if (timed_out) {
-        if (lane == 0)
-            atomicOr(p.status, KVX_DEV_WAIT_TIMEOUT);
-        for (uint32_t r = retired; r < issued; ++r)  // drain the loads still in flight
-            mbar_wait(&full[r % n_stages], (r / n_stages) & 1u, lane);
-    }
-    if (lane == 0)
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    __syncwarp();
-}
-
-// ------------------------------------------------------------------------- round trip
-//
-// Store a batch to host chunks and load the same chunks into other pages in one launch
-// (a swap-out followed by a swap-in elsewhere).  The store and load plans enumerate the
-// same items, so load unit u reads exactly the host bytes store unit u writes.  Units
-// (unit_items consecutive items) are handed out by two fetch-and-add counters, one per
-// direction.  A warp takes a store unit while the loads handed out are within `lag`
-// units (one per warp of the grid by default) of the stores handed out, and a load unit
-// otherwise,
-// so each load usually starts well after its store finished.  A warp that holds a load
-// unit whose store has not been handed out yet hands out (and does) store units until it
-// has; only then does it wait for that store.  Every wait is therefore on a unit held by a
-// running warp that waits on nothing, whatever the residency of the grid, so the waits
-// end; each is still bounded (about one second, then KVX_DEV_WAIT_TIMEOUT and the unit is
-// skipped).  Both directions of the host link run from the first completed store to the
-// last load, in a single launch.
-
-struct RoundTripSync {
-    unsigned int *next;  // [0] next store unit, [1] next load unit; zero at launch
-    unsigned int *done;  // [units]: 1 once the store unit's bytes are in host memory
-    int64_t units;
-    int unit_items;
-    unsigned lag;        // loads handed out may trail stores handed out by this many units
-};
-
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Lane 0: bounded wait for a store unit to finish.
-__device__ __forceinline__ bool wait_unit(const RoundTripSync &sy, int64_t unit)
-{
-    const uint64_t deadline = global_ns() + kWaitLimitNs;
-    while (ld_acquire_u32(sy.done + unit) == 0u) {
-        if (global_ns() > deadline)
-            return false;
-        __nanosleep(200);
-    }
-    return true;
-}
-
-enum : int { kUnitStore = 1, kUnitLoad = 2, kUnitSkip = 3 };
-
-// Lane 0: the warp's next unit (-1: nothing left for this warp) and what to do with it.
-// `pending` carries a load unit taken before its store was handed out.
-__device__ __forceinline__ long long next_unit(const RoundTripSync &sy, unsigned lag,
-                                               long long &pending, int &what)
-{
-    const unsigned n = unsigned(sy.units);
-    if (pending < 0) {
-        const unsigned si = ld_relaxed_u32(sy.next);
-        const unsigned li = ld_relaxed_u32(sy.next + 1);
-        if (si < n && li + lag >= si) {
-            const unsigned s = atomicAdd(sy.next, 1u);
-            if (s < n) {
-                what = kUnitStore;
-                return s;
-            }
-        }
-        const unsigned t = atomicAdd(sy.next + 1, 1u);
-        if (t >= n)
-            return -1;  // every load is handed out; their holders finish the stores
-        pending = t;
-    }
-    if (ld_relaxed_u32(sy.next) <= unsigned(pending)) {
-        // The store this load needs is not handed out yet: hand out the next one.
-        const unsigned s = atomicAdd(sy.next, 1u);
-        if (s < n) {
-            what = kUnitStore;
-            return s;
-        }
-    }
-    const long long u = pending;
-    pending = -1;
-    what = wait_unit(sy, u) ? kUnitLoad : kUnitSkip;
-    return u;
-}
-
-// Items [first, first + count) of plan p, warp-collective (count is 1 unless BATCHED).
-// NC = false for bytes written earlier in the same launch.
-template <int U, int DIR, int HINT, bool BATCHED, bool NC>
-__device__ __forceinline__ void copy_items(const Plan &p, int64_t first, int count, int lane)
-{
-    const int64_t v = p.token_bytes;
-    if (!BATCHED) {  // one item per unit
-        Segment sg;
-        if (resolve_segment<DIR>(p, first, lane, sg))
-            copy_segment<U, HINT, NC>(sg, v, lane);
-        return;
-    }
-    Segment sg;
-    sg.src = nullptr;
-    sg.dst = nullptr;
-    sg.s_pitch = sg.d_pitch = 0;
-    sg.rows = 0;
-    sg.contiguous = true;
-    bool ok = false;
-    if (lane < count) {
-        const int64_t mine = first + lane;
-        ok = segment_of<DIR>(p, find_chunk_lane(p.item_begin, p.n_chunks, mine), mine, true,
-                             sg);
-    }
-    const unsigned valid = __ballot_sync(0xffffffffu, ok);
-    for (int k = 0; k < count; ++k) {
-        const Segment sk = shfl_segment(sg, k);
-        if (valid & (1u << k))
-            copy_segment<U, HINT, NC>(sk, v, lane);
-    }
-}
-
-template <int U, bool BATCHED>
-__global__ void __launch_bounds__(1024, 1)
-    kvx_roundtrip_kernel(const Plan ps, const Plan pl, const RoundTripSync sy)
-{
-    const int lane = threadIdx.x & 31;
-    long long pending = -1;  // lane 0's
-    for (;;) {
-        long long unit = -1;
-        int what = 0;
-        if (lane == 0) {
-            unit = next_unit(sy, sy.lag, pending, what);
-            if (what == kUnitSkip)
-                atomicOr(ps.status, KVX_DEV_WAIT_TIMEOUT);
-        }
-        unit = __shfl_sync(0xffffffffu, unit, 0);
-        what = __shfl_sync(0xffffffffu, what, 0);
-        if (unit < 0)
-            break;
-        if (what == kUnitSkip)
-            continue;  // its store never finished: leave the unit alone
-        __syncwarp();  // lane 0's acquire orders every lane's loads below
-        const int64_t first = unit * sy.unit_items;
-        const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
-        if (what == kUnitLoad) {
-            copy_items<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED, false>(pl, first, count,
-                                                                             lane);
-        } else {
-            // HBM reads need fewer bytes in flight than host reads: four loads per lane.
-            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
-                ps, first, count, lane);
-            __syncwarp();  // every lane's writes happen before lane 0's release
-            if (lane == 0)
-                st_release_u32(sy.done + unit, 1u);
-        }
-    }
-}
-
-// Exchange with shared work: a store batch and an independent load batch, each warp taking
-// its next unit from whichever direction is further behind in proportion to its size, so
-// both directions finish together and every warp works until the last unit, whatever the
-// ratio of the two batches.  No unit waits on another.
-struct DuplexSync {
-    unsigned int *next;  // [0] next store unit, [1] next load unit; zero at launch
-    int64_t units_s;
-    int64_t units_l;
-    int unit_items;
-};
-
-// Lane 0: the next unit (-1: none left) and its direction.
-__device__ __forceinline__ long long next_duplex_unit(const DuplexSync &sy, int &what)
-{
-    const unsigned ns = unsigned(sy.units_s), nl = unsigned(sy.units_l);
-    const unsigned si = ld_relaxed_u32(sy.next);
-    const unsigned li = ld_relaxed_u32(sy.next + 1);
-    // store progress si / ns against load progress li / nl
-    const bool store_first = si < ns && (li >= nl || uint64_t(si) * nl <= uint64_t(li) * ns);
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        const bool store = (attempt == 0) == store_first;
-        const unsigned u = atomicAdd(sy.next + (store ? 0 : 1), 1u);
-        if (u < (store ? ns : nl)) {
-            what = store ? kUnitStore : kUnitLoad;
-            return u;
-        }
-    }
-    return -1;
-}
-
-template <int U, bool BATCHED>
-__global__ void __launch_bounds__(1024, 1)
-    kvx_duplex_kernel(const Plan ps, const Plan pl, const DuplexSync sy)
-{
-    const int lane = threadIdx.x & 31;
-    for (;;) {
-        long long unit = -1;
-        int what = 0;
-        if (lane == 0)
-            unit = next_duplex_unit(sy, what);
-        unit = __shfl_sync(0xffffffffu, unit, 0);
-        what = __shfl_sync(0xffffffffu, what, 0);
-        if (unit < 0)
-            break;
-        const int64_t first = unit * sy.unit_items;
-        if (what == kUnitLoad) {
-            const int count = int(min(int64_t(sy.unit_items), pl.total_items - first));
-            copy_items<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED, true>(pl, first, count,
-                                                                            lane);
-        } else {
-            const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
-            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
-                ps, first, count, lane);
-        }
-    }
-}
-
-typedef void (*DuplexFn)(Plan, Plan, DuplexSync);
-
-DuplexFn pick_duplex(int unroll, bool batched)
-{
-    switch (unroll) {
-    case 1: return batched ? kvx_duplex_kernel<1, true> : kvx_duplex_kernel<1, false>;
-    case 2: return batched ? kvx_duplex_kernel<2, true> : kvx_duplex_kernel<2, false>;
-    case 4: return batched ? kvx_duplex_kernel<4, true> : kvx_duplex_kernel<4, false>;
-    case 8: return batched ? kvx_duplex_kernel<8, true> : kvx_duplex_kernel<8, false>;
-    }
-    return nullptr;
-}
-
-typedef void (*RoundTripFn)(Plan, Plan, RoundTripSync);
-
-RoundTripFn pick_roundtrip(int unroll, bool batched)
-{
-    switch (unroll) {
-    case 1: return batched ? kvx_roundtrip_kernel<1, true> : kvx_roundtrip_kernel<1, false>;
-    case 2: return batched ? kvx_roundtrip_kernel<2, true> : kvx_roundtrip_kernel<2, false>;
-    case 4: return batched ? kvx_roundtrip_kernel<4, true> : kvx_roundtrip_kernel<4, false>;
-    case 8: return batched ? kvx_roundtrip_kernel<8, true> : kvx_roundtrip_kernel<8, false>;
-    }
-    return nullptr;
-}
-
-typedef void (*KernelFn)(Plan);
-
-template <int U, bool BATCHED>
-KernelFn pick_hint_dir(int dir, int hint)
-{
-    if (dir == KVX_DIR_GATHER)
-        return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_GATHER, 1, BATCHED>
-                                          : kvx_segment_kernel<U, KVX_DIR_GATHER, 0, BATCHED>;
-    return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_SCATTER, 1, BATCHED>
-                                      : kvx_segment_kernel<U, KVX_DIR_SCATTER, 0, BATCHED>;
-}
-
-template <bool BATCHED>
-KernelFn pick_unroll(int unroll, int dir, int hint)
-{
-    switch (unroll) {
-    case 1: return pick_hint_dir<1, BATCHED>(dir, hint);
-    case 2: return pick_hint_dir<2, BATCHED>(dir, hint);
-    case 4: return pick_hint_dir<4, BATCHED>(dir, hint);
-    case 8: return pick_hint_dir<8, BATCHED>(dir, hint);
-    }
-    return nullptr;
-}
-
-// The warp-segment kernel for (unroll, direction, hint), batched when more than one
-// segment is resolved per warp at once.
-KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1)
-{
-    return batch > 1 ? pick_unroll<true>(unroll, dir, hint)
-                     : pick_unroll<false>(unroll, dir, hint);
-}
-
-typedef void (*ExchangeFn)(Plan, Plan);
-
-template <int U>
-ExchangeFn pick_exchange_u(bool bs, bool bl)
-{
-    if (bs)
-        return bl ? kvx_exchange_kernel<U, true, true> : kvx_exchange_kernel<U, true, false>;
-    return bl ? kvx_exchange_kernel<U, false, true> : kvx_exchange_kernel<U, false, false>;
-}
-
-ExchangeFn pick_exchange(int unroll, int batch_s, int batch_l)
-{
-    switch (unroll) {
-    case 1: return pick_exchange_u<1>(batch_s > 1, batch_l > 1);
-    case 2: return pick_exchange_u<2>(batch_s > 1, batch_l > 1);
-    case 4: return pick_exchange_u<4>(batch_s > 1, batch_l > 1);
-    case 8: return pick_exchange_u<8>(batch_s > 1, batch_l > 1);
-    }
-    return nullptr;
-}
-
-}  // namespace
+#include "kvx_kernels.cuh"
 
 // --------------------------------------------------------------------------------- host
 
