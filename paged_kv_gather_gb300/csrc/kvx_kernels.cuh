@@ -41,16 +41,13 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p)
     return r;
 }
 
-// Coherent 16-byte load, cached in L2 only: for bytes another warp of the same launch wrote
-// (the read-only .nc path is valid only for data no thread writes during the launch).
+// Coherent 16-byte load, cached in L2 only (ld.global.cg through the compiler's own
+// intrinsic, so it stays ordered after fences and warp barriers like any load): for bytes
+// another warp of the same launch wrote (the read-only .nc path is valid only for data no
+// thread writes during the launch).
 __device__ __forceinline__ uint4 ld_cg_v4(const uint4 *p)
 {
-    uint4 r;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p)
-                 : "memory");
-    return r;
+    return __ldcg(p);
 }
 
 template <bool NC>
@@ -537,9 +534,10 @@ __device__ __forceinline__ bool wait_unit(const RoundTripSync &sy, int64_t unit)
 enum : int { kUnitStore = 1, kUnitLoad = 2, kUnitSkip = 3 };
 
 // Lane 0: the warp's next unit (-1: nothing left for this warp) and what to do with it.
-// `pending` carries a load unit taken before its store was handed out.
-__device__ __forceinline__ long long next_unit(const RoundTripSync &sy, unsigned lag,
-                                               long long &pending, int &what)
+// `pending` carries a load unit taken before its store was handed out.  Units stay below
+// 2^31 (the host checks), so 32-bit indices hold them.
+__device__ __forceinline__ int next_unit(const RoundTripSync &sy, unsigned lag, int &pending,
+                                         int &what)
 {
     const unsigned n = unsigned(sy.units);
     if (pending < 0) {
@@ -549,23 +547,23 @@ __device__ __forceinline__ long long next_unit(const RoundTripSync &sy, unsigned
             const unsigned s = atomicAdd(sy.next, 1u);
             if (s < n) {
                 what = kUnitStore;
-                return s;
+                return int(s);
             }
         }
         const unsigned t = atomicAdd(sy.next + 1, 1u);
         if (t >= n)
             return -1;  // every load is handed out; their holders finish the stores
-        pending = t;
+        pending = int(t);
     }
     if (ld_relaxed_u32(sy.next) <= unsigned(pending)) {
         // The store this load needs is not handed out yet: hand out the next one.
         const unsigned s = atomicAdd(sy.next, 1u);
         if (s < n) {
             what = kUnitStore;
-            return s;
+            return int(s);
         }
     }
-    const long long u = pending;
+    const int u = pending;
     pending = -1;
     what = wait_unit(sy, u) ? kUnitLoad : kUnitSkip;
     return u;
@@ -608,9 +606,9 @@ __global__ void __launch_bounds__(1024, 1)
     kvx_roundtrip_kernel(const Plan ps, const Plan pl, const RoundTripSync sy)
 {
     const int lane = threadIdx.x & 31;
-    long long pending = -1;  // lane 0's
+    int pending = -1;  // lane 0's
     for (;;) {
-        long long unit = -1;
+        int unit = -1;
         int what = 0;
         if (lane == 0) {
             unit = next_unit(sy, sy.lag, pending, what);
@@ -624,11 +622,12 @@ __global__ void __launch_bounds__(1024, 1)
         if (what == kUnitSkip)
             continue;  // its store never finished: leave the unit alone
         __syncwarp();  // lane 0's acquire orders every lane's loads below
-        const int64_t first = unit * sy.unit_items;
+        const int64_t first = int64_t(unit) * sy.unit_items;
         const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
         if (what == kUnitLoad) {
-            copy_items<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED, false>(pl, first, count,
-                                                                             lane);
+            // Short (batched) segments fill at most a few loads per lane: four are enough.
+            copy_items<(BATCHED && U > 4 ? 4 : U), KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED,
+                       false>(pl, first, count, lane);
         } else {
             // HBM reads need fewer bytes in flight than host reads: four loads per lane.
             copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
@@ -687,8 +686,9 @@ __global__ void __launch_bounds__(1024, 1)
         const int64_t first = unit * sy.unit_items;
         if (what == kUnitLoad) {
             const int count = int(min(int64_t(sy.unit_items), pl.total_items - first));
-            copy_items<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED, true>(pl, first, count,
-                                                                            lane);
+            // Short (batched) segments fill at most a few loads per lane: four are enough.
+            copy_items<(BATCHED && U > 4 ? 4 : U), KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED,
+                       true>(pl, first, count, lane);
         } else {
             const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
             copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
