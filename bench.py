@@ -1109,7 +1109,7 @@ def run_transform_sweep(args, kvx, wl):
     for mapping, ctas, threads, unroll, hint, stage, batch in shapes:
         if True:
             row = {"workload": "llama8b_transform_sweep",
-                   "mapping": "bulk" if mapping else "segment", "ctas_per_sm": ctas,
+                   "mapping": ["segment", "bulk", "cta"][mapping], "ctas_per_sm": ctas,
                    "threads": threads, "unroll": unroll, "store_hint": hint,
                    "stage_bytes": stage, "batch": batch}
             for name, d, rq in (("gather", kvx.KVX_DIR_GATHER, rs),

@@ -139,6 +139,9 @@ typedef struct kvx_chunk {
                                    shared-memory stages with bulk async copies
                                    (cp.async.bulk, mbarrier completion); `unroll` is the
                                    number of stages (2..8), `stage_bytes` their size */
+#define KVX_MAP_CTA 2           /* all threads of a CTA move one segment together (thread t
+                                   takes units t, t + threads, ...), 32 segments resolved
+                                   per batch by one warp; store, load and transform only */
 
 /* Store cache hint for the destination of each 16-byte unit. */
 #define KVX_HINT_DEFAULT 0      /* st.global (write-back) */
@@ -151,10 +154,10 @@ typedef struct kvx_launch_cfg {
     int32_t ctas_per_sm;  /* 0 = the operation's default */
     int32_t threads;      /* threads per CTA, multiple of 32 in [32, 1024]; 0 = default
                              (the bulk mapping always runs one warp per CTA) */
-    int32_t unroll;       /* warp-segment mapping: 16-byte loads in flight per lane before
-                             its stores (1, 2, 4 or 8); bulk mapping: shared-memory stages
-                             (2..8).  0 = default */
-    int32_t store_hint;   /* KVX_HINT_* (warp-segment mapping) */
+    int32_t unroll;       /* warp-segment and CTA mappings: 16-byte loads in flight per
+                             thread before its stores (1, 2, 4 or 8); bulk mapping:
+                             shared-memory stages (2..8).  0 = default */
+    int32_t store_hint;   /* KVX_HINT_* (warp-segment and CTA mappings) */
     int32_t mapping;      /* KVX_MAP_* */
     int32_t stage_bytes;  /* bulk mapping: bytes per shared-memory stage, a multiple of 16;
                              stages x stage_bytes <= 220 KiB.  0 = default (32 KiB) */

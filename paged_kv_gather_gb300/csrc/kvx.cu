@@ -178,7 +178,7 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
     bool ok = out->sm_cap >= 0 && out->ctas_per_sm >= 1 && out->ctas_per_sm <= 32 &&
               out->batch >= 0 && out->batch <= 32 &&
               (out->store_hint == KVX_HINT_DEFAULT || out->store_hint == KVX_HINT_STREAMING);
-    if (out->mapping == KVX_MAP_WARP_SEGMENT) {
+    if (out->mapping == KVX_MAP_WARP_SEGMENT || out->mapping == KVX_MAP_CTA) {
         ok = ok && out->threads >= 32 && out->threads <= 1024 && out->threads % 32 == 0 &&
              pick_kernel(out->unroll, 0, 0);
     } else if (out->mapping == KVX_MAP_BULK) {
@@ -218,7 +218,9 @@ LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Pl
     const int64_t warps_per_cta = cfg.threads / 32;
     const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
     int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
-    const int64_t per_cta = warps_per_cta * (cfg.mapping == KVX_MAP_BULK ? 1 : plan.batch);
+    const int64_t per_cta = cfg.mapping == KVX_MAP_CTA    ? 32
+                            : cfg.mapping == KVX_MAP_BULK ? warps_per_cta
+                                                          : warps_per_cta * plan.batch;
     const int64_t needed = (plan.total_items + per_cta - 1) / per_cta;
     if (ctas > needed)
         ctas = needed;
@@ -232,6 +234,9 @@ LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Pl
         sh.stage_bytes = cfg.stage_bytes;
         sh.stages = cfg.unroll;
         sh.smem = size_t(cfg.unroll) * cfg.stage_bytes;
+    } else if (cfg.mapping == KVX_MAP_CTA) {
+        sh.fn = reinterpret_cast<const void *>(pick_cta(cfg.unroll, dir, cfg.store_hint));
+        sh.threads = cfg.threads;
     } else {
         sh.fn = reinterpret_cast<const void *>(pick_kernel(cfg.unroll, dir, cfg.store_hint,
                                                            plan.batch));

@@ -293,6 +293,121 @@ __global__ void __launch_bounds__(1024, 1) kvx_exchange_kernel(const Plan ps, co
     }
 }
 
+// ------------------------------------------------------------------ CTA-per-segment mapping
+//
+// Every thread of a CTA moves part of the same segment: thread t takes 16-byte units t,
+// t + T, t + 2T, ... (T threads), U of them in flight before their stores.  Warp 0
+// resolves 32 consecutive segments at once, one per lane, into shared memory; the CTA then
+// walks them without further synchronisation.  Per SM this keeps the bytes in flight of
+// many warps while touching only a few segments (DRAM streams) at a time.
+
+// Units [0, n16) of one segment, strided over the CTA.
+template <int U, int HINT>
+__device__ __forceinline__ void copy_contig_cta(const uint4 *__restrict__ s,
+                                                uint4 *__restrict__ d, int n16, int tid, int T)
+{
+    int i = tid;
+    for (; i + (U - 1) * T < n16; i += U * T) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            r[u] = ld_nc_v4(s + i + u * T);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            st_v4<HINT>(d + i + u * T, r[u]);
+    }
+    if (i < n16) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i + u * T < n16)
+                r[u] = ld_nc_v4(s + i + u * T);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i + u * T < n16)
+                st_v4<HINT>(d + i + u * T, r[u]);
+    }
+}
+
+template <int U, int DIR, int HINT>
+__global__ void __launch_bounds__(1024, 1) kvx_cta_kernel(const Plan p)
+{
+    __shared__ Segment segs[32];
+    __shared__ unsigned valid;
+    const int tid = threadIdx.x;
+    const int T = blockDim.x;
+    const int64_t v = p.token_bytes;
+    const int units_per_row = int(v >> 4);
+    for (int64_t base = int64_t(blockIdx.x) * 32; base < p.total_items;
+         base += int64_t(gridDim.x) * 32) {
+        __syncthreads();  // the previous batch's segments are no longer read
+        if (tid < 32) {
+            Segment sg;
+            sg.src = nullptr;
+            sg.dst = nullptr;
+            sg.s_pitch = sg.d_pitch = 0;
+            sg.rows = 0;
+            sg.contiguous = true;
+            const int64_t mine = base + tid;
+            bool ok = false;
+            if (mine < p.total_items)
+                ok = segment_of<DIR>(p, find_chunk_lane(p.item_begin, p.n_chunks, mine), mine,
+                                     true, sg);
+            segs[tid] = sg;
+            const unsigned m = __ballot_sync(0xffffffffu, ok);
+            if (tid == 0)
+                valid = m;
+        }
+        __syncthreads();
+        const unsigned m = valid;
+        const int n = int(min(int64_t(32), p.total_items - base));
+        for (int k = 0; k < n; ++k) {
+            if (!((m >> k) & 1u))
+                continue;
+            const Segment sg = segs[k];
+            if (sg.contiguous) {
+                copy_contig_cta<U, HINT>(reinterpret_cast<const uint4 *>(sg.src),
+                                         reinterpret_cast<uint4 *>(sg.dst),
+                                         int((int64_t(sg.rows) * v) >> 4), tid, T);
+            } else {
+                // Token-major chunk: unit j of the segment is unit j % units_per_row of row
+                // j / units_per_row, each row at its own pitch on the chunk side.
+                const int total = sg.rows * units_per_row;
+                for (int j = tid; j < total; j += T) {
+                    const int r = j / units_per_row, u = j - r * units_per_row;
+                    const uint4 x = ld_nc_v4(reinterpret_cast<const uint4 *>(
+                                                 sg.src + r * sg.s_pitch) + u);
+                    st_v4<HINT>(reinterpret_cast<uint4 *>(sg.dst + r * sg.d_pitch) + u, x);
+                }
+            }
+        }
+    }
+}
+
+typedef void (*CtaFn)(Plan);
+
+template <int U>
+CtaFn pick_cta_u(int dir, int hint)
+{
+    if (dir == KVX_DIR_GATHER)
+        return hint == KVX_HINT_STREAMING ? kvx_cta_kernel<U, KVX_DIR_GATHER, 1>
+                                          : kvx_cta_kernel<U, KVX_DIR_GATHER, 0>;
+    return hint == KVX_HINT_STREAMING ? kvx_cta_kernel<U, KVX_DIR_SCATTER, 1>
+                                      : kvx_cta_kernel<U, KVX_DIR_SCATTER, 0>;
+}
+
+// The CTA-per-segment kernel for (unroll, direction, hint); nullptr for another unroll.
+CtaFn pick_cta(int unroll, int dir, int hint)
+{
+    switch (unroll) {
+    case 1: return pick_cta_u<1>(dir, hint);
+    case 2: return pick_cta_u<2>(dir, hint);
+    case 4: return pick_cta_u<4>(dir, hint);
+    case 8: return pick_cta_u<8>(dir, hint);
+    }
+    return nullptr;
+}
+
 // ------------------------------------------------------------------ bulk-copy (TMA) mapping
 //
 // One warp per CTA streams its items through a ring of shared-memory stages with the

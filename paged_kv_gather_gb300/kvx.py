@@ -51,6 +51,7 @@ KVX_DIR_SCATTER = 1
 
 KVX_MAP_WARP_SEGMENT = 0
 KVX_MAP_BULK = 1
+KVX_MAP_CTA = 2
 
 KVX_HINT_DEFAULT = 0
 KVX_HINT_STREAMING = 1

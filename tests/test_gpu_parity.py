@@ -98,12 +98,18 @@ def test_tiny_workload_round_trip(ctx, stream, op_store, op_load, where):
     arena.close()
 
 
+def cta(sm_cap, ctas_per_sm, threads, unroll, hint):
+    """Launch configuration of the CTA-per-segment mapping."""
+    return cfg(sm_cap, ctas_per_sm, threads, unroll, hint, kvx.KVX_MAP_CTA)
+
+
 # ----------------------------------------------------------------------------- random batches
 
 CONFIGS = [cfg(), cfg(1, 1, 32, 1, 0), cfg(2, 1, 64, 2, 1), cfg(3, 2, 256, 4, 0),
            cfg(0, 1, 1024, 8, 1), cfg(1, 1, 1024, 8, 0), cfg(5, 3, 96, 4, 1),
            bulk(), bulk(2, 1, 2, 64), bulk(3, 2, 3, 4096), bulk(0, 1, 8, 1040),
-           cfg(3, 1, 256, 8, 0, batch=32), cfg(2, 2, 128, 2, 1, batch=5), cfg(0, 1, 64, 4, 0, batch=2)]
+           cfg(3, 1, 256, 8, 0, batch=32), cfg(2, 2, 128, 2, 1, batch=5), cfg(0, 1, 64, 4, 0, batch=2),
+           cta(2, 1, 256, 8, 1), cta(1, 1, 32, 1, 0), cta(0, 2, 512, 4, 0), cta(3, 1, 96, 2, 1)]
 
 
 @pytest.mark.parametrize("seed", range(42))
@@ -168,6 +174,44 @@ def test_every_kernel_variant(ctx, stream, unroll, hint, batch):
     _load(ctx, "load", dpool, dst, specs, arena, 0, None, c, stream)
     assert_pool_equal(dpool, expected_load(pre, dst, specs, arena.numpy().copy()))
     arena.close()
+
+
+@pytest.mark.parametrize("unroll", [1, 2, 4, 8])
+@pytest.mark.parametrize("hint", [0, 1])
+@pytest.mark.parametrize("layout", [wl.LAYER_MAJOR, wl.TOKEN_MAJOR])
+def test_cta_mapping_every_variant(ctx, stream, unroll, hint, layout):
+    """CTA-per-segment mapping: every (unroll, hint, direction) instantiation, more segments
+    than one batch of 32 per CTA, a ragged last batch, partial pages and both contiguous and
+    token-major chunk rows; store, load and the HBM transform."""
+    rng = np.random.default_rng(91 + unroll * 10 + hint + 100 * layout)
+    L, KV, P, v = 3, 2, 16, 1024
+    lens = [1000, 333, 17]
+    pages = [-(-n // P) for n in lens]
+    NP = sum(pages) * 2
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(perm[at:at + npg])
+        t_dst.append(perm[at + sum(pages):at + sum(pages) + npg])
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, 90, 0, L, layout)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    c = cta(2, 1, 160, unroll, hint)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    for op_store, op_load, where in (("store", "load", "host"), ("gather", "scatter", "device")):
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        dpool.fill_random(unroll + 10 * hint + 1000 * layout)
+        arena = Arena(nbytes, where)
+        _store(ctx, op_store, dpool, src, specs, arena, 0, None, c, stream)
+        assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), op_store)
+        pre = dpool.host_copy()
+        _load(ctx, op_load, dpool, dst, specs, arena, 0, None, c, stream)
+        assert_pool_equal(dpool, expected_load(pre, dst, specs, arena.numpy().copy()))
+        arena.close()
 
 
 @pytest.mark.parametrize("stages,stage_bytes,ctas", [(2, 16, 1), (3, 1040, 2), (6, 32768, 1),
