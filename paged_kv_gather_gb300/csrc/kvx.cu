@@ -261,16 +261,81 @@ cudaError_t launch_kernel(const LaunchShape &sh, Plan plan, cudaStream_t s)
                             s);
 }
 
+// Every call starts with an empty last-launch record, so a call that fails or moves
+// nothing reports zeros.
+void begin_call(kvx_ctx *ctx)
+{
+    ctx->last_items = 0;
+    ctx->last_ctas = 0;
+    ctx->last_threads = 0;
+    ctx->last_desc_bytes = 0;
+}
+
+// The context's next descriptor slot, once the launch that last used it has finished.
+kvx_status acquire_slot(kvx_ctx *ctx, size_t bytes, Slot **out)
+{
+    if (bytes > ctx->slot_bytes)
+        return set_err(ctx, KVX_ERR_CAPACITY,
+                       "descriptors need %zu bytes, the context holds %zu per call; create it "
+                       "with a larger max_descriptor_bytes", bytes, ctx->slot_bytes);
+    Slot &slot = ctx->slots[ctx->next];
+    if (slot.used) {
+        cudaError_t e = cudaEventSynchronize(slot.done);
+        if (e != cudaSuccess)
+            return cuda_err(ctx, e, "waiting for a descriptor buffer");
+    }
+    *out = &slot;
+    return KVX_OK;
+}
+
+// After a launch: the slot stays busy until `s` passes this point; record the launch.
+kvx_status finish_call(kvx_ctx *ctx, Slot &slot, cudaStream_t s, int64_t items, int64_t ctas,
+                       int threads, size_t desc_bytes)
+{
+    cudaError_t e = cudaEventRecord(slot.done, s);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "event record");
+    slot.used = true;
+    ctx->next = (ctx->next + 1) % kSlots;
+    ctx->last_items = items;
+    ctx->last_ctas = int32_t(ctas);
+    ctx->last_threads = threads;
+    ctx->last_desc_bytes = int64_t(desc_bytes);
+    return KVX_OK;
+}
+
+// Launch configuration of an exchange or round trip: warp-segment mapping only.
+kvx_status resolve_pair_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_launch_cfg *cfg)
+{
+    kvx_status st = resolve_cfg(ctx, op, user, cfg);
+    if (st == KVX_OK && cfg->mapping != KVX_MAP_WARP_SEGMENT)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "%s runs the warp-segment mapping only",
+                       op == KVX_OP_EXCHANGE ? "exchange" : "round trip");
+    return st;
+}
+
+// Segments a warp resolves at once: the configured batch, else the packed default, with two
+// long segments per warp for the HBM transform (their lookups then overlap).
+void apply_batch(int op, const kvx_launch_cfg &cfg, Plan *plan)
+{
+    if (cfg.batch > 0)
+        plan->batch = cfg.batch;
+    else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && plan->batch == 1)
+        plan->batch = 2;
+}
+
+int op_dir(int op)
+{
+    return (op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM) ? KVX_DIR_SCATTER : KVX_DIR_GATHER;
+}
+
 kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request *reqs, int n_req,
                   const kvx_chunk *chunks, int n_chunks, int layer_begin, int layer_end,
                   const kvx_launch_cfg *user_cfg, kvx_stream_t stream)
 {
     if (!ctx)
         return KVX_ERR_INVALID_ARG;
-    ctx->last_items = 0;
-    ctx->last_ctas = 0;
-    ctx->last_threads = 0;
-    ctx->last_desc_bytes = 0;
+    begin_call(ctx);
     kvx_launch_cfg cfg;
     kvx_status st = resolve_cfg(ctx, op, user_cfg, &cfg);
     if (st != KVX_OK)
@@ -282,49 +347,26 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     DeviceGuard guard(ctx->device);
     if (!guard.ok)
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
-
     const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
-    if (lay.total > ctx->slot_bytes)
-        return set_err(ctx, KVX_ERR_CAPACITY,
-                       "descriptors need %zu bytes, the context holds %zu per call; create it "
-                       "with a larger max_descriptor_bytes", lay.total, ctx->slot_bytes);
-    Slot &slot = ctx->slots[ctx->next];
-    if (slot.used) {
-        cudaError_t e = cudaEventSynchronize(slot.done);
-        if (e != cudaSuccess)
-            return cuda_err(ctx, e, "waiting for a descriptor buffer");
-    }
-    const int dir = (op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM) ? KVX_DIR_SCATTER
-                                                                    : KVX_DIR_GATHER;
+    Slot *slot = nullptr;
+    if ((st = acquire_slot(ctx, lay.total, &slot)) != KVX_OK)
+        return st;
+    const int dir = op_dir(op);
     Plan plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
-                          slot.host, slot.dev);
+                          slot->host, slot->dev);
     plan.status = ctx->status_dev;
-    if (cfg.batch > 0)
-        plan.batch = cfg.batch;
-    else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && plan.batch == 1)
-        plan.batch = 2;  // HBM transform: overlap the lookup of two long segments per warp
+    apply_batch(op, cfg, &plan);
     if (plan.total_items == 0)
         return KVX_OK;
-
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = stage(ctx, slot, lay.total, 0, 0, s);
+    cudaError_t e = stage(ctx, *slot, lay.total, 0, 0, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
     const LaunchShape shape = launch_shape(ctx, cfg, plan, dir);
     e = launch_kernel(shape, plan, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
-    const int64_t ctas = shape.ctas;
-    e = cudaEventRecord(slot.done, s);
-    if (e != cudaSuccess)
-        return cuda_err(ctx, e, "event record");
-    slot.used = true;
-    ctx->next = (ctx->next + 1) % kSlots;
-    ctx->last_items = plan.total_items;
-    ctx->last_ctas = int32_t(ctas);
-    ctx->last_threads = cfg.threads;
-    ctx->last_desc_bytes = int64_t(lay.total);
-    return KVX_OK;
+    return finish_call(ctx, *slot, s, plan.total_items, shape.ctas, shape.threads, lay.total);
 }
 
 // An exchange whose batches differ in size by more than this factor (in segments) shares its
@@ -406,16 +448,11 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
 {
     if (!ctx)
         return KVX_ERR_INVALID_ARG;
-    ctx->last_items = 0;
-    ctx->last_ctas = 0;
-    ctx->last_threads = 0;
-    ctx->last_desc_bytes = 0;
+    begin_call(ctx);
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_cfg(ctx, KVX_OP_EXCHANGE, user_cfg, &cfg);
+    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_EXCHANGE, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
-    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
-        return set_err(ctx, KVX_ERR_INVALID_ARG, "exchange runs the warp-segment mapping only");
     st = kvx::validate_exchange(pool, sreqs, n_sreq, schunks, n_schunks, lreqs, n_lreq, lchunks,
                                 n_lchunks, layer_begin, layer_end, ctx->validation, true,
                                 ctx->err, sizeof ctx->err);
@@ -426,66 +463,45 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
     const kvx::PackedLayout ls = kvx::packed_layout(pool, n_sreq, n_schunks);
     const kvx::PackedLayout ll = kvx::packed_layout(pool, n_lreq, n_lchunks);
-    const size_t total = ls.total + ll.total;
-    if (total > ctx->slot_bytes)
-        return set_err(ctx, KVX_ERR_CAPACITY,
-                       "descriptors need %zu bytes, the context holds %zu per call; create it "
-                       "with a larger max_descriptor_bytes", total, ctx->slot_bytes);
-    Slot &slot = ctx->slots[ctx->next];
-    if (slot.used) {
-        cudaError_t e = cudaEventSynchronize(slot.done);
-        if (e != cudaSuccess)
-            return cuda_err(ctx, e, "waiting for a descriptor buffer");
-    }
+    const size_t total = ls.total + ll.total;  // then 256 bytes of work counters
+    Slot *slot = nullptr;
+    if ((st = acquire_slot(ctx, total + 256, &slot)) != KVX_OK)
+        return st;
     Plan ps = kvx::pack(pool, sreqs, n_sreq, schunks, n_schunks, layer_begin, layer_end,
-                        KVX_DIR_GATHER, ls, slot.host, slot.dev);
+                        KVX_DIR_GATHER, ls, slot->host, slot->dev);
     Plan pl = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
-                        KVX_DIR_SCATTER, ll, slot.host + ls.total, slot.dev + ls.total);
+                        KVX_DIR_SCATTER, ll, slot->host + ls.total, slot->dev + ls.total);
     ps.status = pl.status = ctx->status_dev;
-    if (cfg.batch > 0)
-        ps.batch = pl.batch = cfg.batch;
+    apply_batch(KVX_OP_EXCHANGE, cfg, &ps);
+    apply_batch(KVX_OP_EXCHANGE, cfg, &pl);
     if (ps.total_items + pl.total_items == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    int64_t ctas;
+    LaunchShape shape;
     if (exchange_shared(ps, pl)) {
-        if (total + 256 > ctx->slot_bytes)
-            return set_err(ctx, KVX_ERR_CAPACITY, "descriptors need %zu bytes, the context "
-                           "holds %zu per call", total + 256, ctx->slot_bytes);
         DuplexSync sy;
-        LaunchShape shape;
-        if (!duplex_setup(ctx, cfg, ps, pl, reinterpret_cast<unsigned *>(slot.dev + total), &sy,
+        if (!duplex_setup(ctx, cfg, ps, pl, reinterpret_cast<unsigned *>(slot->dev + total), &sy,
                           &shape))
             return set_err(ctx, KVX_ERR_CAPACITY, "exchange batches of %lld and %lld segments "
                            "(%d and %d per warp) do not fit one shared launch",
                            (long long)ps.total_items, (long long)pl.total_items, ps.batch,
                            pl.batch);
-        e = stage(ctx, slot, total, total, 256, s);
+        e = stage(ctx, *slot, total, total, 256, s);
         if (e != cudaSuccess)
             return cuda_err(ctx, e, "descriptor copy");
         e = launch_duplex_kernel(shape, ps, pl, sy, s);
-        ctas = shape.ctas;
     } else {
-        e = stage(ctx, slot, total, 0, 0, s);
+        e = stage(ctx, *slot, total, 0, 0, s);
         if (e != cudaSuccess)
             return cuda_err(ctx, e, "descriptor copy");
-        const LaunchShape shape = exchange_shape(ctx, cfg, ps, pl);
+        shape = exchange_shape(ctx, cfg, ps, pl);
         e = launch_exchange_kernel(shape, ps, pl, s);
-        ctas = shape.ctas;
     }
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
-    e = cudaEventRecord(slot.done, s);
-    if (e != cudaSuccess)
-        return cuda_err(ctx, e, "event record");
-    slot.used = true;
-    ctx->next = (ctx->next + 1) % kSlots;
-    ctx->last_items = ps.total_items + pl.total_items;
-    ctx->last_ctas = int32_t(ctas);
-    ctx->last_threads = cfg.threads;
-    ctx->last_desc_bytes = int64_t(total);
-    return KVX_OK;
+    return finish_call(ctx, *slot, s, ps.total_items + pl.total_items, shape.ctas, shape.threads,
+                       total);
 }
 
 // Units, lag and grid of a round trip whose work counters and completion words start at
@@ -539,16 +555,11 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
 {
     if (!ctx)
         return KVX_ERR_INVALID_ARG;
-    ctx->last_items = 0;
-    ctx->last_ctas = 0;
-    ctx->last_threads = 0;
-    ctx->last_desc_bytes = 0;
+    begin_call(ctx);
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
+    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
-    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
-        return set_err(ctx, KVX_ERR_INVALID_ARG, "round trip runs the warp-segment mapping only");
     st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
                                 n_chunks, layer_begin, layer_end, ctx->validation, true,
                                 ctx->err, sizeof ctx->err);
@@ -558,56 +569,37 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
     if (!guard.ok)
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
     const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
-    // Units from the packed item count (known after packing); bound the sync area first by
-    // the largest count the slot could describe.
-    Slot &slot = ctx->slots[ctx->next];
-    if (2 * lay.total + 256 > ctx->slot_bytes)
-        return set_err(ctx, KVX_ERR_CAPACITY,
-                       "descriptors need %zu bytes, the context holds %zu per call; create it "
-                       "with a larger max_descriptor_bytes", 2 * lay.total + 256,
-                       ctx->slot_bytes);
-    if (slot.used) {
-        cudaError_t e = cudaEventSynchronize(slot.done);
-        if (e != cudaSuccess)
-            return cuda_err(ctx, e, "waiting for a descriptor buffer");
-    }
+    const size_t sync_off = 2 * lay.total;
+    Slot *slot = nullptr;
+    if ((st = acquire_slot(ctx, sync_off + 256, &slot)) != KVX_OK)
+        return st;
     Plan ps = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
-                        KVX_DIR_GATHER, lay, slot.host, slot.dev);
+                        KVX_DIR_GATHER, lay, slot->host, slot->dev);
     Plan pl = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
-                        KVX_DIR_SCATTER, lay, slot.host + lay.total, slot.dev + lay.total);
+                        KVX_DIR_SCATTER, lay, slot->host + lay.total, slot->dev + lay.total);
     ps.status = pl.status = ctx->status_dev;
-    if (cfg.batch > 0)
-        ps.batch = pl.batch = cfg.batch;
+    apply_batch(KVX_OP_ROUNDTRIP, cfg, &ps);
+    apply_batch(KVX_OP_ROUNDTRIP, cfg, &pl);
     if (ps.total_items == 0)
         return KVX_OK;
-    const size_t sync_off = 2 * lay.total;
+    // The completion words (4 bytes per unit) are known only now that the plan is packed.
     const size_t sync_bytes = roundtrip_sync_bytes(ps);
-    if (sync_bytes > (size_t(1) << 33) || sync_off + sync_bytes > ctx->slot_bytes)
+    if (sync_off + sync_bytes > ctx->slot_bytes)
         return set_err(ctx, KVX_ERR_CAPACITY,
                        "round trip of %lld segments needs %zu bytes of descriptors and "
                        "completion words, the context holds %zu per call",
                        (long long)ps.total_items, sync_off + sync_bytes, ctx->slot_bytes);
     RoundTripSync sy;
     LaunchShape shape;
-    roundtrip_setup(ctx, cfg, ps, slot.dev + sync_off, &sy, &shape);
+    roundtrip_setup(ctx, cfg, ps, slot->dev + sync_off, &sy, &shape);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = stage(ctx, slot, sync_off, sync_off, sync_bytes, s);
+    cudaError_t e = stage(ctx, *slot, sync_off, sync_off, sync_bytes, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
     e = launch_roundtrip_kernel(shape, ps, pl, sy, 0, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");
-    const int64_t ctas = shape.ctas;
-    e = cudaEventRecord(slot.done, s);
-    if (e != cudaSuccess)
-        return cuda_err(ctx, e, "event record");
-    slot.used = true;
-    ctx->next = (ctx->next + 1) % kSlots;
-    ctx->last_items = 2 * ps.total_items;
-    ctx->last_ctas = int32_t(ctas);
-    ctx->last_threads = cfg.threads;
-    ctx->last_desc_bytes = int64_t(sync_off);
-    return KVX_OK;
+    return finish_call(ctx, *slot, s, 2 * ps.total_items, shape.ctas, shape.threads, sync_off);
 }
 
 }  // namespace
@@ -650,8 +642,7 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
     DeviceGuard guard(ctx->device);
     if (!guard.ok)
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
-    const int dir = (op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM) ? KVX_DIR_SCATTER
-                                                                    : KVX_DIR_GATHER;
+    const int dir = op_dir(op);
     const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);
     kvx_plan *p = new kvx_plan();
     p->ctx = ctx;
@@ -664,10 +655,7 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
     p->plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
                         host.data(), p->dev);
     p->plan.status = ctx->status_dev;
-    if (cfg.batch > 0)
-        p->plan.batch = cfg.batch;
-    else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && p->plan.batch == 1)
-        p->plan.batch = 2;
+    apply_batch(op, cfg, &p->plan);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), lay.total, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
@@ -694,11 +682,9 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
         return KVX_ERR_INVALID_ARG;
     *out = nullptr;
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_cfg(ctx, KVX_OP_EXCHANGE, user_cfg, &cfg);
+    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_EXCHANGE, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
-    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
-        return set_err(ctx, KVX_ERR_INVALID_ARG, "exchange runs the warp-segment mapping only");
     st = kvx::validate_exchange(pool, sreqs, n_sreq, schunks, n_schunks, lreqs, n_lreq, lchunks,
                                 n_lchunks, layer_begin, layer_end, ctx->validation, true,
                                 ctx->err, sizeof ctx->err);
@@ -724,8 +710,8 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
     p->load = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, ll, host.data() + ls.total, p->dev + ls.total);
     p->plan.status = p->load.status = ctx->status_dev;
-    if (cfg.batch > 0)
-        p->plan.batch = p->load.batch = cfg.batch;
+    apply_batch(KVX_OP_EXCHANGE, cfg, &p->plan);
+    apply_batch(KVX_OP_EXCHANGE, cfg, &p->load);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), total, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
@@ -759,11 +745,9 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
         return KVX_ERR_INVALID_ARG;
     *out = nullptr;
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
+    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
-    if (cfg.mapping != KVX_MAP_WARP_SEGMENT)
-        return set_err(ctx, KVX_ERR_INVALID_ARG, "round trip runs the warp-segment mapping only");
     st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
                                 n_chunks, layer_begin, layer_end, ctx->validation, true,
                                 ctx->err, sizeof ctx->err);
@@ -782,8 +766,7 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     // allocation and pack again.
     p->plan = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_GATHER, lay, host.data(), host.data());
-    if (cfg.batch > 0)
-        p->plan.batch = cfg.batch;
+    apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->plan);
     p->sync_bytes = roundtrip_sync_bytes(p->plan);
     cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->dev), 2 * lay.total + p->sync_bytes);
     if (e != cudaSuccess) {
@@ -795,8 +778,8 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     p->load = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, lay, host.data() + lay.total, p->dev + lay.total);
     p->plan.status = p->load.status = ctx->status_dev;
-    if (cfg.batch > 0)
-        p->plan.batch = p->load.batch = cfg.batch;
+    apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->plan);
+    apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->load);
     roundtrip_setup(ctx, cfg, p->plan, p->dev + 2 * lay.total, &p->rsync, &p->shape);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), 2 * lay.total, cudaMemcpyHostToDevice, s);
