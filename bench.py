@@ -209,7 +209,7 @@ class EventTimer:
 
 def source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("kvx_kernels.cuh", "kvx.cu", "kvx_internal.h"):
+    for f in ("kvx_kernels.cuh", "kvx_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_gather_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
