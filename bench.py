@@ -648,6 +648,11 @@ def run_ours(args):
     value = 2 * N * args.steps * world / (total_ms * 1e-3) / GB
     step_gbs = 2 * N / (total_ms / args.steps * 1e-3) / GB
     launch_gbs = step_gbs  # one launch per step
+    # The I/O-time model with this run's measured link peaks (kvx_estimate_pair_us).
+    model = kvx.kvx_default_link_model()
+    model.h2d_gbs, model.d2h_gbs, model.bidir_gbs = link["h2d"], link["d2h"], link["bidir"]
+    model_ms = kvx.kvx_estimate_pair_us(model, kvx.KVX_OP_ROUNDTRIP, N, N,
+                                        s.page_size * s.token_bytes, cfg_rt) * 1e-3
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -676,6 +681,10 @@ def run_ours(args):
                                       "launch per step; the events also hold its descriptor "
                                       "copy and completion-word reset)",
                      "traffic": recorded_traffic("roundtrip", "llama8b"),
+                     "model_ms": round(model_ms, 4),
+                     "model_note": "kvx_estimate_pair_us with this run's link peaks: fill and "
+                                   "drain of one 32 KiB unit per warp at the one-way rates, "
+                                   "the rest at the bidirectional peak, plus 10 us per call",
                      "kernel": "kvx_roundtrip_kernel (store + load of every segment in one "
                                "launch)",
                      "peak_source": "measured in this run: best of 8 pairs of 4 GiB pinned "
@@ -979,6 +988,8 @@ def run_qwen7b(args, kvx, wl):
            "concurrent_ms": round(both, 3),
            "exchange_one_launch_ms": round(x_ms, 3),
            "exchange_one_launch_aggregate_gbs": round((Nl + Ns) / (x_ms * 1e-3) / GB, 2),
+           "model_exchange_ms": round(kvx.kvx_estimate_pair_us(
+               kvx.kvx_default_link_model(), kvx.KVX_OP_EXCHANGE, Ns, Nl, 0, xcfg) * 1e-3, 3),
            "memcpy_bidirectional_gbs": round(2 * (4 << 30) / statistics.median(bid) / GB, 2)})
     ld.close()
     st.close()

@@ -427,6 +427,8 @@ typedef struct kvx_link_model {
     double h2d_gbs;      /* host -> device peak, GB/s (one 4 GiB pinned copy) */
     double d2h_gbs;      /* device -> host peak, GB/s */
     double hbm_gbs;      /* HBM copy peak, GB/s counting read + write */
+    double bidir_gbs;    /* host link, both directions at once (H2D + D2H pinned copies on
+                            two streams), GB/s counting both directions */
     double latency_us;   /* round trip of one host-memory access from an SM */
     double launch_us;    /* fixed cost of one call: host packing, descriptor copy, launch */
     int32_t num_sms;
@@ -445,6 +447,20 @@ kvx_status kvx_default_link_model(kvx_link_model *model);
  * t = launch_us + bytes / min(peak, in_flight / latency). */
 kvx_status kvx_estimate_us(const kvx_link_model *model, int op, int64_t bytes,
                            const kvx_launch_cfg *cfg, double *us);
+
+/* Predicted duration (microseconds) of one exchange (op = KVX_OP_EXCHANGE) or round trip
+ * (KVX_OP_ROUNDTRIP) moving store_bytes to the host and load_bytes to the device in one
+ * launch with cfg (NULL = defaults).  Both directions share the link: each is capped by
+ * its own peak, together they are capped by the bidirectional peak and by Little's law
+ * on the launch's bytes in flight (as in kvx_estimate_us):
+ *   t = launch_us + max(store / d2h, load / h2d, (store + load) / min(bidir, in_flight / L))
+ * A round trip (store_bytes = load_bytes) first stores, and last loads, one unit of
+ * unit_bytes per warp of its grid on its own at the one-way rates (its fill and drain):
+ *   t = launch_us + F / d2h + (2 x bytes - 2 F) / min(bidir, ...) + F / h2d,
+ *   F = min(bytes, warps x unit_bytes). */
+kvx_status kvx_estimate_pair_us(const kvx_link_model *model, int op, int64_t store_bytes,
+                                int64_t load_bytes, int64_t unit_bytes,
+                                const kvx_launch_cfg *cfg, double *us);
 
 /* Layer-streamed prefill: layer l + 1's KV is loaded while layer l computes (as "Strata
  * Guide", section "The Loading-Bound Scheduling Dilemma and Delay Hits", and the

@@ -431,11 +431,13 @@ kvx_status kvx_default_link_model(kvx_link_model *m)
     if (!m)
         return KVX_ERR_INVALID_ARG;
     // GB300 with a Grace host over NVLink-C2C, as measured by the benchmark: pinned copies
-    // 211.6 GB/s H2D and 193.7 GB/s D2H; copy peak 6791.7 GB/s; one SM with 128 KiB of
+    // 211.6 GB/s H2D and 193.7 GB/s D2H, 343.1 GB/s both at once; copy peak 6791.7 GB/s;
+    // one SM with 128 KiB of
     // host reads in flight sustains ~50 GB/s (2.6 us round trip); ~10 us per call.
     m->h2d_gbs = 211.6;
     m->d2h_gbs = 193.7;
     m->hbm_gbs = 6791.7;
+    m->bidir_gbs = 343.1;
     m->latency_us = 2.6;
     m->launch_us = 10.0;
     m->num_sms = 152;
@@ -477,6 +479,50 @@ kvx_status kvx_estimate_us(const kvx_link_model *m, int op, int64_t bytes,
     }
     const double gbs = op <= KVX_OP_LOAD ? (little_gbs < peak ? little_gbs : peak) : peak;
     *us = m->launch_us + (gbs > 0 ? moved / (gbs * 1e3) : 0.0);
+    return KVX_OK;
+}
+
+kvx_status kvx_estimate_pair_us(const kvx_link_model *m, int op, int64_t store_bytes,
+                                int64_t load_bytes, int64_t unit_bytes,
+                                const kvx_launch_cfg *cfg, double *us)
+{
+    if (!m || !us || store_bytes < 0 || load_bytes < 0 || unit_bytes < 0 ||
+        (op != KVX_OP_EXCHANGE && op != KVX_OP_ROUNDTRIP) || m->latency_us <= 0 ||
+        m->num_sms <= 0 || m->h2d_gbs <= 0 || m->d2h_gbs <= 0 || m->bidir_gbs <= 0 ||
+        (op == KVX_OP_ROUNDTRIP && store_bytes != load_bytes))
+        return KVX_ERR_INVALID_ARG;
+    // Defaults in step with kvx_default_launch_cfg: exchange 40 SMs, round trip 16, both one
+    // CTA of 1024 threads per SM with 8 loads in flight per lane.
+    int sm_cap = op == KVX_OP_EXCHANGE ? 40 : 16, ctas = 1, threads = 1024, unroll = 8;
+    if (cfg) {
+        sm_cap = cfg->sm_cap;
+        if (cfg->ctas_per_sm)
+            ctas = cfg->ctas_per_sm;
+        if (cfg->threads)
+            threads = cfg->threads;
+        if (cfg->unroll)
+            unroll = cfg->unroll;
+    }
+    const double sms = sm_cap > 0 && sm_cap < m->num_sms ? sm_cap : m->num_sms;
+    const double in_flight = sms * ctas * threads * (double)unroll * 16.0;
+    const double little_gbs = in_flight / (m->latency_us * 1e3);
+    const double both = little_gbs < m->bidir_gbs ? little_gbs : m->bidir_gbs;
+    const double S = (double)store_bytes, Lb = (double)load_bytes;
+    double t_ns;
+    if (op == KVX_OP_EXCHANGE) {
+        t_ns = S / m->d2h_gbs;
+        if (Lb / m->h2d_gbs > t_ns)
+            t_ns = Lb / m->h2d_gbs;
+        if ((S + Lb) / both > t_ns)
+            t_ns = (S + Lb) / both;
+    } else {
+        const double warps = sms * ctas * (threads / 32);
+        double F = warps * (double)unit_bytes;
+        if (F > S)
+            F = S;
+        t_ns = F / m->d2h_gbs + (2.0 * S - 2.0 * F) / both + F / m->h2d_gbs;
+    }
+    *us = m->launch_us + t_ns * 1e-3;
     return KVX_OK;
 }
 

@@ -98,7 +98,8 @@ class kvx_launch_cfg(ctypes.Structure):
 
 class kvx_link_model(ctypes.Structure):
     _fields_ = [("h2d_gbs", ctypes.c_double), ("d2h_gbs", ctypes.c_double),
-                ("hbm_gbs", ctypes.c_double), ("latency_us", ctypes.c_double),
+                ("hbm_gbs", ctypes.c_double), ("bidir_gbs", ctypes.c_double),
+                ("latency_us", ctypes.c_double),
                 ("launch_us", ctypes.c_double), ("num_sms", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
 
@@ -170,6 +171,8 @@ _proto("kvx_version", _c.c_int, [])
 _proto("kvx_default_link_model", _c.c_int, [_P(kvx_link_model)])
 _proto("kvx_estimate_us", _c.c_int, [_P(kvx_link_model), _c.c_int, _c.c_int64,
                                      _P(kvx_launch_cfg), _P(_c.c_double)])
+_proto("kvx_estimate_pair_us", _c.c_int, [_P(kvx_link_model), _c.c_int, _c.c_int64, _c.c_int64,
+                                          _c.c_int64, _P(kvx_launch_cfg), _P(_c.c_double)])
 _proto("kvx_estimate_stream_us", _c.c_int, [_c.c_double, _c.c_double, _c.c_int,
                                             _P(_c.c_double), _P(_c.c_double)])
 _proto("kvx_partition_create", _c.c_int, [_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
@@ -182,14 +185,14 @@ _proto("kvx_load_chunks_noalloc", _c.c_int, [*_batch, _P(kvx_launch_cfg), _c.c_v
 
 EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_launch_cfg",
             "kvx_store_chunks", "kvx_load_chunks", "kvx_exchange_chunks", "kvx_roundtrip_chunks",
-            "kvx_plan_create",
-            "kvx_plan_create_exchange", "kvx_plan_create_roundtrip", "kvx_plan_launch", "kvx_plan_destroy", "kvx_transform_hbm", "kvx_dma_baseline",
+            "kvx_plan_create", "kvx_plan_create_exchange", "kvx_plan_create_roundtrip",
+            "kvx_plan_launch", "kvx_plan_destroy", "kvx_transform_hbm", "kvx_dma_baseline",
             "kvx_get_status", "kvx_last_error", "kvx_last_launch", "kvx_validate",
             "kvx_plan_count", "kvx_chunk_policy", "kvx_host_alloc", "kvx_host_free",
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
             "kvx_load_chunks_noalloc", "kvx_default_link_model", "kvx_estimate_us",
-            "kvx_estimate_stream_us", "kvx_partition_create", "kvx_partition_info",
-            "kvx_partition_destroy"]
+            "kvx_estimate_pair_us", "kvx_estimate_stream_us", "kvx_partition_create",
+            "kvx_partition_info", "kvx_partition_destroy"]
 
 KVX_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -531,6 +534,16 @@ def kvx_estimate_us(model: kvx_link_model, op: int, nbytes: int,
     st = _lib.kvx_estimate_us(ctypes.byref(model), op, nbytes, _cfg_ptr(cfg), ctypes.byref(us))
     if st != KVX_OK:
         raise KvxError(st, "kvx_estimate_us")
+    return us.value
+
+
+def kvx_estimate_pair_us(model: kvx_link_model, op: int, store_bytes: int, load_bytes: int,
+                         unit_bytes: int = 0, cfg: Optional[kvx_launch_cfg] = None) -> float:
+    us = ctypes.c_double()
+    st = _lib.kvx_estimate_pair_us(ctypes.byref(model), op, store_bytes, load_bytes, unit_bytes,
+                                   _cfg_ptr(cfg), ctypes.byref(us))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_estimate_pair_us")
     return us.value
 
 

@@ -445,6 +445,36 @@ def test_in_kernel_page_check_skips_and_reports(ctx, stream):
     arena.close()
 
 
+def test_roundtrip_page_check_skips_and_reports(ctx, stream):
+    """Round trip whose source table names a page past the pool: that store segment is
+    skipped and flagged, its load still runs after it (reading the untouched chunk bytes),
+    and every other segment makes the full round trip."""
+    L, KV, P, v, NP = 2, 2, 8, 64, 8
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(13)
+    bad_src = np.array([5, NP + 1000], np.int32)
+    dst_table = np.array([1, 3], np.int32)
+    src = Requests([bad_src], [16], host_copy=False)
+    dst = Requests([dst_table], [16])
+    specs = [wl.ChunkSpec(0, 0, 8, 0, L, 0), wl.ChunkSpec(0, 8, 8, 0, L, 0)]
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    arena = Arena(nbytes, "host")
+    pre = dpool.host_copy()
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                             kvx.chunks_array(specs, arena.ptr), stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == kvx.KVX_DEV_PAGE_OUT_OF_RANGE
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, [oracle.Request(np.array([5, 0], np.int32), 16)],
+                 oracle_chunks(specs[:1], exp))
+    assert_bytes_equal(arena.numpy(), exp, "valid chunk stored, bad page's chunk untouched")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
+    assert_pool_equal(dpool, pre)
+    arena.close()
+
+
 def test_host_detected_errors_launch_nothing(ctx, stream):
     L, KV, P, v, NP = 2, 2, 8, 64, 8
     dpool = DevicePool.empty(L, KV, NP, P, v)

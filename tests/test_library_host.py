@@ -283,3 +283,37 @@ def test_estimator_layer_streaming_bounds():
     assert kvx.kvx_estimate_stream_us(5.0, 7.0, 1) == (12.0, 5.0)
     with pytest.raises(kvx.KvxError):
         kvx.kvx_estimate_stream_us(1.0, 1.0, 0)
+
+
+def test_estimator_exchange_and_round_trip():
+    m = kvx.kvx_default_link_model()
+    X, R = kvx.KVX_OP_EXCHANGE, kvx.KVX_OP_ROUNDTRIP
+    G = 1 << 30
+    launch = m.launch_us
+    # Exchange: each direction capped by its own peak, both by the bidirectional peak.
+    assert kvx.kvx_estimate_pair_us(m, X, 4 * G, 4 * G) == pytest.approx(
+        launch + 8 * G / m.bidir_gbs * 1e-3)
+    assert kvx.kvx_estimate_pair_us(m, X, 4 * G, 0) == pytest.approx(
+        launch + 4 * G / m.d2h_gbs * 1e-3)
+    assert kvx.kvx_estimate_pair_us(m, X, 0, 4 * G) == pytest.approx(
+        launch + 4 * G / m.h2d_gbs * 1e-3)
+    # A small store beside a large load: the load's own peak decides.
+    assert kvx.kvx_estimate_pair_us(m, X, G, 10 * G) == pytest.approx(
+        launch + 10 * G / m.h2d_gbs * 1e-3)
+    # Round trip: fill and drain of one unit per warp (16 SMs x 32 warps x 32 KiB = 16 MiB).
+    F = 16 * 32 * (32 << 10)
+    want = launch + (F / m.d2h_gbs + (8 * G - 2 * F) / m.bidir_gbs + F / m.h2d_gbs) * 1e-3
+    assert kvx.kvx_estimate_pair_us(m, R, 4 * G, 4 * G, 32 << 10) == pytest.approx(want)
+    # The fill never exceeds the transfer: a tiny round trip is one store then one load.
+    tiny = 1 << 20
+    assert kvx.kvx_estimate_pair_us(m, R, tiny, tiny, 32 << 10) == pytest.approx(
+        launch + (tiny / m.d2h_gbs + tiny / m.h2d_gbs) * 1e-3)
+    # Too few bytes in flight: Little's law caps both directions together.
+    c = kvx.kvx_launch_cfg()
+    c.sm_cap, c.ctas_per_sm, c.threads, c.unroll = 1, 1, 32, 1
+    little = 32 * 16 / (m.latency_us * 1e3)
+    assert kvx.kvx_estimate_pair_us(m, X, G, G, 0, c) == pytest.approx(
+        launch + 2 * G / little * 1e-3)
+    for bad in ((kvx.KVX_OP_STORE, G, G), (R, G, 2 * G), (X, -1, G)):
+        with pytest.raises(kvx.KvxError):
+            kvx.kvx_estimate_pair_us(m, *bad)
