@@ -34,17 +34,19 @@
  *   own layer_begin.
  *
  * Ownership.  The caller owns the pools, page tables, chunk memory and streams.  A
- * kvx_ctx owns only a small ring of descriptor buffers (pinned host + device) and a
- * device status word.  Nothing on the transfer path allocates.
+ * kvx_ctx owns only a small ring of descriptor buffers (pinned host + device), a device
+ * status word and a stream for descriptor copies.  Nothing on the transfer path
+ * allocates; prepared plans allocate once, when created.
  *
  * Asynchrony and errors.  Every transfer call validates on the host, packs O(chunks)
- * descriptors, copies them to the device and launches ONE kernel on the given stream,
- * then returns.  A host-detected error returns a non-zero kvx_status and launches
- * nothing; kvx_last_error() then holds a message.  Errors the kernel meets (a page id
- * outside the pool) set a bit in the device status word and skip that page, without
- * trapping; kvx_get_status() reads and clears it.  A kvx_ctx must not be used from two
- * host threads at once.  Descriptor buffers are reused round-robin; before reusing one
- * the call waits for the kernel that last used it.
+ * descriptors, copies them to the device (on the context's copy stream, which the given
+ * stream then waits for) and launches ONE kernel on the given stream, then returns.  A
+ * host-detected error returns a non-zero kvx_status and launches nothing;
+ * kvx_last_error() then holds a message.  Errors the kernel meets (a page id outside the
+ * pool, a bounded wait that ran out) set a bit in the device status word and skip that
+ * work, without trapping; kvx_get_status() reads and clears it.  A kvx_ctx must not be
+ * used from two host threads at once.  Descriptor buffers are reused round-robin; before
+ * reusing one the call waits for the kernel that last used it.
  */
 #ifndef KVX_H
 #define KVX_H
@@ -324,9 +326,10 @@ kvx_status kvx_get_status(kvx_ctx *ctx, kvx_stream_t stream, uint32_t *flags);
 /* Message describing the last error of this context ("" if none). */
 const char *kvx_last_error(const kvx_ctx *ctx);
 
-/* Shape of the context's last kernel launch: work items (page segments), CTAs, threads
- * per CTA and bytes of descriptors copied to the device; zeros if the last call launched
- * nothing.  Any output may be NULL. */
+/* Shape of the context's last kernel launch by a call (not by a plan): work items (page
+ * segments; an exchange or round trip counts both directions), CTAs, threads per CTA and
+ * bytes of descriptors copied to the device; zeros if the last call launched nothing.
+ * Any output may be NULL. */
 kvx_status kvx_last_launch(const kvx_ctx *ctx, int64_t *items, int32_t *ctas,
                            int32_t *threads, int64_t *descriptor_bytes);
 

@@ -345,7 +345,25 @@ def test_empty_and_degenerate_batches(ctx, stream):
     ch = kvx.chunks_array(specs, arena.ptr)
     kvx.kvx_load_chunks(ctx, dpool.pool, reqs.array, ch, 0, 1, None, stream.cuda_stream)
     assert kvx.kvx_last_launch(ctx)[0] == 0
+    # The same nothing through the exchange, the round trip and their plans.
+    kvx.kvx_exchange_chunks(ctx, dpool.pool, reqs.array, empty, reqs.array, ch, 0, 1,
+                            stream=stream.cuda_stream)
+    assert kvx.kvx_last_launch(ctx)[0] == 0
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, reqs.array, reqs.array, empty,
+                             stream=stream.cuda_stream)
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, reqs.array, reqs.array, ch, 0, 1,
+                             stream=stream.cuda_stream)
+    assert kvx.kvx_last_launch(ctx)[0] == 0
+    for plan in (kvx.kvx_plan_create(ctx, kvx.KVX_OP_LOAD, dpool.pool, reqs.array, ch, 0, 1,
+                                     stream=stream.cuda_stream),
+                 kvx.kvx_plan_create_exchange(ctx, dpool.pool, reqs.array, empty, reqs.array,
+                                              empty, stream=stream.cuda_stream),
+                 kvx.kvx_plan_create_roundtrip(ctx, dpool.pool, reqs.array, reqs.array, ch, 0, 1,
+                                               stream=stream.cuda_stream)):
+        kvx.kvx_plan_launch(plan, stream.cuda_stream)
+        kvx.kvx_plan_destroy(plan)
     stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
     assert torch.equal(before, dpool.tensor)
     # Single token, one unit wide.
     pool1 = DevicePool.empty(1, 1, 4, 1, 16)
