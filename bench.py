@@ -310,6 +310,19 @@ class CpuSample:
                           f"workload on {self.threads} host threads, {el:.1f} s"}
 
 
+def headline_config(world: int, bytes_per_direction: int) -> dict:
+    """The headline workload, shared by both arms of the benchmark."""
+    return {"workload": "llama8b_kv: 32 layers, 8 KV heads x 128, bf16 N(0,1), 16-token pages, "
+                        "32768 tokens on 2048 random pages of a 16384-page pool, 128 "
+                        "layer-major chunks of 256 tokens (32 MiB) in mapped pinned host "
+                        "memory; step = store all chunks + load them into 2048 fresh pages "
+                        "in one kvx_roundtrip_chunks launch (each page segment is loaded once "
+                        "its store has reached host memory)",
+            "bytes_per_direction": bytes_per_direction,
+            "l2": "inputs larger than L2 (4 GiB per direction), no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     world, rank, local = dist_setup(args)
     if rank != 0:
@@ -326,17 +339,14 @@ def run_reference(args):
     step_ms = statistics.median(ms)
     value = round(sample.bytes_per_pass / (step_ms * 1e-3) / GB, 3)
     base = {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"each step: oracle store+load over 32 chunks (8192 tokens x 32 layers x "
-                      f"K/V = 1 GiB per direction) of the Llama-3.1-8B-shaped workload on "
-                      f"{threads} host threads"}
+            "sample": f"each step: oracle store+load over 32 of the workload's chunks (8192 "
+                      f"tokens x 32 layers x K/V = 1 GiB per direction, a quarter of the "
+                      f"workload) on {threads} host threads; GB/s is scaled by bytes moved"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(step_ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": "llama8b_kv: 32 layers, 8 KV heads x 128, bf16, 16-token "
-                                   "pages, 256-token layer-major chunks; step = store + load "
-                                   "(CPU oracle on a 1 GiB-per-direction sample)",
-                       "parallelism": "none (CPU oracle)"},
+            "config": headline_config(1, 4 << 30),
             "cpu_baseline": base,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -662,16 +672,7 @@ def run_ours(args):
                     "note": "this rank's steps, device clock"},
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": "llama8b_kv: 32 layers, 8 KV heads x 128, bf16 N(0,1), "
-                               "16-token pages, 32768 tokens on 2048 random pages of a "
-                               "16384-page pool, 128 layer-major chunks of 256 tokens (32 MiB) "
-                               "in mapped pinned host memory; step = store all chunks + load "
-                               "them into 2048 fresh pages in one kvx_roundtrip_chunks launch "
-                               "(each page segment is loaded once its store has reached host "
-                               "memory)",
-                   "bytes_per_direction": N, "l2": "inputs larger than L2 (4 GiB per "
-                   "direction), no flush", "parallelism": f"replicas x{world}" if world > 1
-                   else "single GPU"},
+        "config": headline_config(world, N),
         "roofline": {"bound": "host_link", "achieved": round(launch_gbs, 2),
                      "peak": link["bidir"], "unit": "GB/s",
                      "frac": round(launch_gbs / link["bidir"], 4),
