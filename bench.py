@@ -66,7 +66,8 @@ def parse():
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
-                   choices=["store", "load", "gather", "scatter", "exchange", "roundtrip"],
+                   choices=["store", "load", "gather", "scatter", "exchange", "roundtrip",
+                            "exchange_shared", "gather_cta"],
                    help="operation of --workload profile_small")
     p.add_argument("--groups", type=int, default=16,
                    help="chunk groups of the pipelined store/load round trip")
@@ -1329,7 +1330,7 @@ def run_profile_small(args, kvx, wl):
     rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
     ctx = kvx.kvx_create(0)
     sh = torch.cuda.current_stream().cuda_stream
-    if args.profile_op in ("store", "load", "exchange", "roundtrip"):
+    if args.profile_op in ("store", "load", "exchange", "roundtrip", "exchange_shared"):
         buf = kvx.HostBuffer(w.store_arena_bytes)
         buf.array[:] = 0
         ch = kvx.chunks_array(w.store_chunks, buf.ptr)
@@ -1340,6 +1341,14 @@ def run_profile_small(args, kvx, wl):
     for _ in range(3):
         if args.profile_op == "roundtrip":  # store every chunk and load it into other pages
             kvx.kvx_roundtrip_chunks(ctx, pool, rs, rd, ch, stream=sh)
+        elif args.profile_op == "exchange_shared":  # store a quarter, load three quarters
+            q = len(w.store_chunks) // 4
+            kvx.kvx_exchange_chunks(ctx, pool, rs, np.ascontiguousarray(ch[:q]), rd,
+                                    np.ascontiguousarray(ch[q:]), stream=sh)
+        elif args.profile_op == "gather_cta":  # the HBM gather, CTA-per-segment mapping
+            c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM)
+            c.mapping, c.ctas_per_sm, c.threads, c.unroll = kvx.KVX_MAP_CTA, 2, 512, 8
+            kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_GATHER, pool, rs, ch, cfg=c, stream=sh)
         elif args.profile_op == "exchange":  # store the first half, load the second half
             kvx.kvx_exchange_chunks(ctx, pool, rs, np.ascontiguousarray(ch[:half]), rd,
                                     np.ascontiguousarray(ch[half:]), stream=sh)
