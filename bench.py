@@ -208,11 +208,36 @@ class EventTimer:
         return [a.elapsed_time(b) for a, b in self.pairs]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and blank-line or indentation differences."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':  # string literal, kept whole
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return "\n".join(" ".join(line.split()) for line in "".join(out).splitlines()
+                     if line.strip())
+
+
 def source_sha() -> str:
+    """Hash of the kernel sources' code (comments and layout ignored): recorded ncu traffic
+    is reported only while it still matches."""
     h = hashlib.sha256()
     for f in ("kvx_kernels.cuh", "kvx_internal.h"):
-        with open(os.path.join(ROOT, "paged_kv_gather_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_gather_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

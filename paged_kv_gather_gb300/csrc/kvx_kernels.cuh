@@ -1,8 +1,8 @@
 // kvx_kernels.cuh -- the sm_103a kernels of the paged KV gather/scatter library, and the
 // functions that pick a kernel instantiation for a launch.  Included by kvx.cu only.
 //
-// One kernel family moves every byte.  A persistent grid of warps walks the batch's work
-// items; an item is one (chunk, layer, kv, page) segment, contiguous on the page side
+// By default a persistent grid of warps walks the batch's work items; an item is one
+// (chunk, layer, kv, page) segment, contiguous on the page side
 // ("Strata Guide: Hierarchical Context Caching for Long LLMs", section "Two-Dimensional
 // Memory Layout Decoupling": the layout change is address arithmetic done by the moving
 // thread, not a separate pass).  Each lane moves 16-byte units ("Step 1:
@@ -13,10 +13,11 @@
 // capped to a few SMs for host transfers so a concurrent compute stream keeps the rest
 // (section "Non-Intrusive Resource Sizing"); the HBM-only transform uses every SM.
 //
-// Kernels: kvx_segment_kernel (store, load, HBM gather/scatter), kvx_exchange_kernel and
-// kvx_duplex_kernel (a store batch and a load batch in one launch), kvx_roundtrip_kernel
-// (store, then load the same chunks elsewhere, ordered per unit inside the launch) and
-// kvx_bulk_kernel (the bulk-copy staging mapping).
+// Kernels: kvx_segment_kernel (store, load, HBM gather/scatter; the default mapping),
+// kvx_exchange_kernel and kvx_duplex_kernel (a store batch and a load batch in one launch),
+// kvx_roundtrip_kernel (store, then load the same chunks elsewhere, ordered per unit inside
+// the launch), and two alternative mappings of a single transfer: kvx_cta_kernel (a whole
+// CTA per segment) and kvx_bulk_kernel (bulk-copy staging through shared memory).
 #pragma once
 
 #include <cuda_runtime.h>
