@@ -443,6 +443,7 @@ def run_ours(args):
     pools = torch.empty((s.kv_factor, s.num_layers, s.num_pages, s.page_size, s.token_bytes),
                         dtype=torch.uint8, device=dev)
     wl.fill_values(pools, s.dtype, wl.values_generator(w.seed, str(dev)))
+    torch.cuda.synchronize()  # filled on the current stream; the transfers use others
     pool = kvx.Pool.from_tensor(pools, s.page_size)
     src_h = w.store_requests[0].page_table
     dst_h = w.load_requests[0].page_table
@@ -781,6 +782,7 @@ def _pool_tensor(shape, seed, wl):
     t = torch.empty((shape.kv_factor, shape.num_layers, shape.num_pages, shape.page_size,
                      shape.token_bytes), dtype=torch.uint8, device="cuda")
     wl.fill_values(t, shape.dtype, wl.values_generator(seed, "cuda"))
+    torch.cuda.synchronize()  # filled on the current stream; the transfers use others
     return t
 
 

@@ -1,5 +1,8 @@
 """Helpers shared by the GPU parity tests: device pools, chunk arenas, oracle comparison.
 
+Every helper that writes device memory with torch (on the current stream) synchronizes
+before returning, because the tests launch the library's kernels on other streams.
+
 Inputs come from the seeded generators of paged_kv_gather_gb300.workloads (or a seeded
 numpy generator for the small random cases); expected values come only from the CPU
 oracle run on host copies of the same inputs.
@@ -28,6 +31,7 @@ class DevicePool:
     @classmethod
     def empty(cls, L, KV, num_pages, P, v, fill=CANARY):
         t = torch.full((KV, L, num_pages, P, v), fill, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()  # the tests launch on other streams
         return cls(t, kvx.Pool.from_tensor(t, P), P)
 
     def fill_random(self, seed: int):
@@ -39,6 +43,7 @@ class DevicePool:
             e = min(flat.numel(), s + step)
             flat[s:e] = torch.randint(0, 256, (e - s,), generator=g, device="cuda",
                                       dtype=torch.int16).to(torch.uint8)
+        torch.cuda.synchronize()  # the tests launch on other streams
 
     def host_copy(self, layers=None) -> oracle.Pool:
         """Oracle pool holding host copies of the given layers (None = all)."""
@@ -81,6 +86,7 @@ class Arena:
             self.ptr = self.hb.ptr
         else:
             self.t = torch.full((total,), CANARY, dtype=torch.uint8, device="cuda")
+            torch.cuda.synchronize()  # the tests launch on other streams
             self.ptr = self.t.data_ptr()
 
     def numpy(self) -> np.ndarray:
@@ -93,6 +99,7 @@ class Arena:
             self.view[:len(data)] = data
         else:
             self.t[:len(data)] = torch.from_numpy(data).cuda()
+            torch.cuda.synchronize()
 
     def close(self):
         if self.where == "host":

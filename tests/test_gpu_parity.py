@@ -602,6 +602,7 @@ def test_offsets_beyond_4_gib(ctx, stream):
     spec = [wl.ChunkSpec(0, 0, n_tok, 0, 1, wl.LAYER_MAJOR, 0)]
     chunk = torch.full((n_tok * v,), CANARY, dtype=torch.uint8, device="cuda")
     assert chunk.numel() > (1 << 32)
+    torch.cuda.synchronize()  # the pool and chunk fills ran on the current stream
     kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_GATHER, dpool.pool, reqs.array,
                           kvx.chunks_array(spec, chunk.data_ptr()), stream=stream.cuda_stream)
     stream.synchronize()

@@ -99,6 +99,7 @@ def test_llama8b_full_size_all_paths(ctx):
 
     # HBM gather into device chunks
     dchunk = torch.full((nbytes + 4096,), CANARY, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()  # filled on the current stream; the transform runs on another
     kvx.kvx_transform_hbm(ctx, kvx.KVX_DIR_GATHER, kvx.Pool.from_tensor(pools, s.page_size),
                           src.array, kvx.chunks_array(w.store_chunks, dchunk.data_ptr()),
                           stream=sh)

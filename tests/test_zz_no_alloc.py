@@ -71,6 +71,7 @@ def test_noalloc_load_matches_context_load_two_calls_in_a_row():
             chunks = kvx.chunks_array(specs, host.ptr)
             ref = kvx.Pool.from_tensor(ref_pool, shape.page_size)
             new = kvx.Pool.from_tensor(new_pool, shape.page_size)
+            torch.cuda.synchronize()  # pools and flags were written on the current stream
             kvx.kvx_load_chunks(ctx, ref, reqs, chunks, 0, shape.num_layers, None,
                                 stream.cuda_stream)
             kvx.kvx_load_chunks_noalloc(new, reqs, chunks, 0, shape.num_layers, None,
