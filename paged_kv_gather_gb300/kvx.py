@@ -238,8 +238,15 @@ class Pool:
     @classmethod
     def from_tensor(cls, pools, page_size: int) -> "Pool":
         """pools: a contiguous uint8 tensor [kv_factor, num_layers, num_pages, page_size, token_bytes]."""
+        if pools.dim() != 5 or pools.element_size() != 1 or not pools.is_contiguous():
+            raise ValueError("pools must be a contiguous byte tensor "
+                             "[kv_factor, num_layers, num_pages, page_size, token_bytes]")
+        if not pools.is_cuda:
+            raise ValueError("pools must be in device memory")
         kv, L, n, P, v = pools.shape
-        assert P == page_size and pools.is_contiguous()
+        if P != page_size or kv not in (1, 2):
+            raise ValueError(f"pools shape {tuple(pools.shape)} does not match page_size "
+                             f"{page_size} and kv_factor 1 or 2")
         base = pools.data_ptr()
         layer = n * P * v
         k = [base + (0 * L + l) * layer for l in range(L)]
@@ -291,7 +298,9 @@ def chunks_array(specs, base_ptr: int) -> np.ndarray:
 def _arr_ptr(a: Optional[np.ndarray], dtype) -> Tuple[int, int]:
     if a is None or len(a) == 0:
         return None, 0
-    assert a.dtype == dtype and a.flags["C_CONTIGUOUS"], "batch arrays must be contiguous"
+    if a.dtype != dtype or not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("batch arrays must be contiguous arrays of the C struct's dtype "
+                         "(use requests_array / chunks_array)")
     return a.ctypes.data, len(a)
 
 

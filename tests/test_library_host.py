@@ -317,3 +317,18 @@ def test_estimator_exchange_and_round_trip():
     for bad in ((kvx.KVX_OP_STORE, G, G), (R, G, 2 * G), (X, -1, G)):
         with pytest.raises(kvx.KvxError):
             kvx.kvx_estimate_pair_us(m, *bad)
+
+
+def test_binding_rejects_malformed_inputs():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):  # not in device memory
+        kvx.Pool.from_tensor(torch.zeros((2, 1, 4, 16, 64), dtype=torch.uint8), 16)
+    with pytest.raises(ValueError):  # wrong rank
+        kvx.Pool.from_tensor(torch.zeros((1, 4, 16, 64), dtype=torch.uint8), 16)
+    with pytest.raises(ValueError):  # wrong element size
+        kvx.Pool.from_tensor(torch.zeros((2, 1, 4, 16, 64), dtype=torch.float32), 16)
+    pool = kvx.Pool(1, 1, 16, 4, 64, [0x1000], None)
+    reqs = kvx.requests_array([(0x2000, None, 16)])
+    bad = np.zeros(2, dtype=np.int64)  # not the chunk struct dtype
+    with pytest.raises(ValueError):
+        kvx.kvx_validate(pool, reqs, bad)
