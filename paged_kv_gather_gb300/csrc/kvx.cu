@@ -800,6 +800,9 @@ kvx_status kvx_plan_launch(const kvx_plan *p, kvx_stream_t stream)
         return KVX_ERR_INVALID_ARG;
     if (p->plan.total_items + (p->exchange && !p->roundtrip ? p->load.total_items : 0) == 0)
         return KVX_OK;
+    DeviceGuard guard(p->ctx->device);  // the plan's memory lives on its context's GPU
+    if (!guard.ok)
+        return set_err(p->ctx, KVX_ERR_CUDA, "cannot make device %d current", p->ctx->device);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (p->roundtrip) {
