@@ -435,6 +435,54 @@ def test_many_calls_in_flight_on_two_streams(ctx):
         arena.close()
 
 
+def test_round_trips_and_exchanges_in_flight_on_two_streams(ctx):
+    """Eight round trips and exchanges, more than the descriptor buffers, alternating two
+    streams so that launches overlap on the GPU: each keeps its own work counters and
+    completion words, and each result matches the oracle."""
+    rng = np.random.default_rng(18)
+    L, KV, P, v, T = 3, 2, 16, 512, 640
+    pages = T // P
+    NP = pages * 17
+    perm = rng.permutation(NP).astype(np.int32)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(19)
+    pre = dpool.host_copy()  # every source page set is read-only below
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    cases = []
+    for i in range(8):
+        src = Requests([perm[(2 * i) * pages:(2 * i + 1) * pages]], [T])
+        dst = Requests([perm[(2 * i + 1) * pages:(2 * i + 2) * pages]], [T])
+        specs = wl.split_tokens(0, 0, T, 32 + 16 * i, 0, L, i % 3)
+        wl.place_chunks(specs, shape)
+        nbytes = wl._arena_bytes(specs, shape)
+        out = Arena(nbytes, "host")
+        ch = kvx.chunks_array(specs, out.ptr)
+        s = streams[i % 2].cuda_stream
+        if i % 2 == 0:
+            kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array, ch, 0, L,
+                                     cfg(2 + i % 3, 1, 128), s)
+            inp = None
+        else:  # an exchange: store src into `out`, load `inp` (random bytes) into dst
+            inp = Arena(nbytes, "host")
+            inp.write(rng.integers(0, 256, nbytes + 4096, dtype=np.uint8))
+            kvx.kvx_exchange_chunks(ctx, dpool.pool, src.array, ch, dst.array,
+                                    kvx.chunks_array(specs, inp.ptr), 0, L, None, s)
+        cases.append((src, dst, specs, nbytes, out, inp))
+    torch.cuda.synchronize()
+    assert kvx.kvx_get_status(ctx, 0) == 0
+    for src, dst, specs, nbytes, out, inp in cases:
+        exp = np.full(nbytes + 4096, CANARY, np.uint8)
+        oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+        assert_bytes_equal(out.numpy(), exp, "store half in flight")
+        oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp if inp is None
+                                                     else inp.numpy().copy()))
+        out.close()
+        if inp is not None:
+            inp.close()
+    assert_pool_equal(dpool, pre)
+
+
 # ----------------------------------------------------------------------------- errors
 
 def test_in_kernel_page_check_skips_and_reports(ctx, stream):
