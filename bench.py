@@ -62,7 +62,7 @@ def parse():
     p.add_argument("--workload", default="llama8b",
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
                             "transform_sweep", "profile_small", "batch_sweep", "mla_blocks",
-                            "roundtrip_sweep", "eviction"],
+                            "roundtrip_sweep", "size_sweep", "eviction"],
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
@@ -1556,6 +1556,45 @@ def run_roundtrip_sweep(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
+def run_size_sweep(args, kvx, wl):
+    """Store and load of 1 to 2048 one-page chunks (all 32 layers, 2 MiB each) of the
+    Llama-3.1-8B-shaped request, per call on the device clock, next to the I/O-time model's
+    prediction (kvx_estimate_us) for the same bytes."""
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src, dst = w.store_requests[0], w.load_requests[0]
+    ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+    rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+    rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+    specs = wl.split_tokens(0, 0, src.n_tokens, s.page_size, 0, s.num_layers, wl.LAYER_MAJOR)
+    wl.place_chunks(specs, s)
+    arena = kvx.HostBuffer(wl._arena_bytes(specs, s))
+    arena.array[:] = 0
+    ch = kvx.chunks_array(specs, arena.ptr)
+    ctx = kvx.kvx_create(0)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    model = kvx.kvx_default_link_model()
+    n = 1
+    while n <= len(specs):
+        part = np.ascontiguousarray(ch[:n])
+        nbytes = n * specs[0].nbytes(s)
+        row = {"workload": "llama8b_size_sweep", "chunks": n, "bytes": nbytes}
+        for name, op, fn, rq in (("store", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs),
+                                 ("load", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd)):
+            ms = _timed(stream, lambda: fn(ctx, pool, rq, part, stream=sh), 10, 3)
+            row[f"{name}_us"] = round(ms * 1e3, 2)
+            row[f"{name}_gbs"] = round(nbytes / (ms * 1e-3) / GB, 2)
+            row[f"{name}_model_us"] = round(kvx.kvx_estimate_us(model, op, nbytes), 2)
+        _emit(row)
+        n *= 2
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    arena.close()
+    kvx.kvx_destroy(ctx)
+
+
 def run_workload(args):
     torch.cuda.set_device(0)
     from paged_kv_gather_gb300.build import build
@@ -1566,7 +1605,7 @@ def run_workload(args):
      "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
      "profile_small": run_profile_small, "batch_sweep": run_batch_sweep,
      "mla_blocks": run_mla_blocks, "eviction": run_eviction,
-     "roundtrip_sweep": run_roundtrip_sweep}[args.workload](
+     "roundtrip_sweep": run_roundtrip_sweep, "size_sweep": run_size_sweep}[args.workload](
         args, kvx, wl)
 
 
