@@ -212,16 +212,35 @@ struct LaunchShape {
     int stages = 0;
 };
 
+// Row slices per segment for a warp-segment launch of one segment per warp: when the batch
+// has fewer segments than the grid has warps, each segment is cut into enough slices (at
+// most 8, at most its page's rows) to give the spare warps work.
+void choose_split(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, Plan *plan)
+{
+    plan->split = 1;
+    if (cfg.mapping != KVX_MAP_WARP_SEGMENT || plan->batch != 1 || plan->total_items <= 0)
+        return;
+    const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+    const int64_t warps = int64_t(sms) * cfg.ctas_per_sm * (cfg.threads / 32);
+    if (plan->total_items >= warps)
+        return;
+    int64_t split = (warps + plan->total_items - 1) / plan->total_items;
+    split = std::min<int64_t>(split, std::min<int64_t>(8, plan->page_size));
+    plan->split = int32_t(std::max<int64_t>(split, 1));
+}
+
 LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &plan, int dir)
 {
     LaunchShape sh;
     const int64_t warps_per_cta = cfg.threads / 32;
     const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
     int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
+    const bool split = cfg.mapping == KVX_MAP_WARP_SEGMENT && plan.split > 1;
     const int64_t per_cta = cfg.mapping == KVX_MAP_CTA    ? 32
                             : cfg.mapping == KVX_MAP_BULK ? warps_per_cta
                                                           : warps_per_cta * plan.batch;
-    const int64_t needed = (plan.total_items + per_cta - 1) / per_cta;
+    const int64_t work = split ? plan.total_items * plan.split : plan.total_items;
+    const int64_t needed = (work + per_cta - 1) / per_cta;
     if (ctas > needed)
         ctas = needed;
     sh.ctas = ctas;
@@ -236,6 +255,9 @@ LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Pl
         sh.smem = size_t(cfg.unroll) * cfg.stage_bytes;
     } else if (cfg.mapping == KVX_MAP_CTA) {
         sh.fn = reinterpret_cast<const void *>(pick_cta(cfg.unroll, dir, cfg.store_hint));
+        sh.threads = cfg.threads;
+    } else if (split) {
+        sh.fn = reinterpret_cast<const void *>(pick_split(cfg.unroll, dir, cfg.store_hint));
         sh.threads = cfg.threads;
     } else {
         sh.fn = reinterpret_cast<const void *>(pick_kernel(cfg.unroll, dir, cfg.store_hint,
@@ -356,6 +378,7 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
                           slot->host, slot->dev);
     plan.status = ctx->status_dev;
     apply_batch(op, cfg, &plan);
+    choose_split(ctx, cfg, &plan);
     if (plan.total_items == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -656,6 +679,7 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
                         host.data(), p->dev);
     p->plan.status = ctx->status_dev;
     apply_batch(op, cfg, &p->plan);
+    choose_split(ctx, cfg, &p->plan);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), lay.total, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)

@@ -356,7 +356,7 @@ Plan pack(const kvx_pool *pool, const kvx_request *reqs, int n_req, const kvx_ch
     p.num_layers = pool->num_layers;
     p.dir = dir;
     p.batch = default_batch(P, v);
-    p.pad = 0;
+    p.split = 1;
     return p;
 }
 

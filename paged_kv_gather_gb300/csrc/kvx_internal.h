@@ -55,7 +55,8 @@ struct Plan {
     int32_t num_layers;
     int32_t dir;                // KVX_DIR_GATHER (pages -> chunks) or KVX_DIR_SCATTER
     int32_t batch;              // segments a warp resolves at once (1..32)
-    int32_t pad;
+    int32_t split;              // row slices per segment, one per warp (kvx_split_kernel);
+                                // 1 = whole segments
 };
 
 // Segments a warp resolves in parallel by default: enough short segments to put ~32 KiB

@@ -272,6 +272,34 @@ __global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
     run_segments<U, DIR, HINT, BATCHED>(p, warp, n_warps, lane);
 }
 
+// Few segments, many warps: each segment is cut into p.split slices of its rows, one warp
+// per slice, so a small transfer still puts the whole grid's bytes in flight.  Slice k of
+// a segment of r rows holds rows [k r / split, (k + 1) r / split); a slice may be empty
+// when a partial page has fewer rows than split.
+template <int U, int DIR, int HINT>
+__global__ void __launch_bounds__(1024, 1) kvx_split_kernel(const Plan p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int S = p.split;
+    const int64_t v = p.token_bytes;
+    for (int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         w < p.total_items * S; w += n_warps) {
+        const int64_t item = w / S;
+        const int k = int(w - item * S);
+        Segment sg;
+        if (!resolve_segment<DIR>(p, item, lane, sg))
+            continue;
+        const int r0 = k * sg.rows / S, r1 = (k + 1) * sg.rows / S;
+        if (r1 <= r0)
+            continue;
+        sg.src += int64_t(r0) * sg.s_pitch;
+        sg.dst += int64_t(r0) * sg.d_pitch;
+        sg.rows = r1 - r0;
+        copy_segment<U, HINT>(sg, v, lane);
+    }
+}
+
 // Exchange: one launch moves a store batch (pages -> host chunks) and a load batch (host
 // chunks -> pages) at once.  Even CTAs run the store plan, odd CTAs the load plan, so the
 // block scheduler spreads both directions evenly over the SMs the launch gets instead of
@@ -869,6 +897,28 @@ KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1)
 {
     return batch > 1 ? pick_unroll<true>(unroll, dir, hint)
                      : pick_unroll<false>(unroll, dir, hint);
+}
+
+template <int U>
+KernelFn pick_split_u(int dir, int hint)
+{
+    if (dir == KVX_DIR_GATHER)
+        return hint == KVX_HINT_STREAMING ? kvx_split_kernel<U, KVX_DIR_GATHER, 1>
+                                          : kvx_split_kernel<U, KVX_DIR_GATHER, 0>;
+    return hint == KVX_HINT_STREAMING ? kvx_split_kernel<U, KVX_DIR_SCATTER, 1>
+                                      : kvx_split_kernel<U, KVX_DIR_SCATTER, 0>;
+}
+
+// The row-slice kernel for (unroll, direction, hint).
+KernelFn pick_split(int unroll, int dir, int hint)
+{
+    switch (unroll) {
+    case 1: return pick_split_u<1>(dir, hint);
+    case 2: return pick_split_u<2>(dir, hint);
+    case 4: return pick_split_u<4>(dir, hint);
+    case 8: return pick_split_u<8>(dir, hint);
+    }
+    return nullptr;
 }
 
 typedef void (*ExchangeFn)(Plan, Plan);

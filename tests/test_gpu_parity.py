@@ -214,6 +214,51 @@ def test_cta_mapping_every_variant(ctx, stream, unroll, hint, layout):
         arena.close()
 
 
+@pytest.mark.parametrize("layout", [wl.LAYER_MAJOR, wl.TOKEN_MAJOR, wl.STRIPED])
+@pytest.mark.parametrize("unroll", [1, 8])
+def test_small_transfers_cut_segments_into_row_slices(ctx, stream, layout, unroll):
+    """A batch with fewer page segments than the grid has warps: each segment is cut into
+    row slices, one per warp; partial pages leave some slices empty.  Store, load and a
+    prepared plan, each against the oracle."""
+    rng = np.random.default_rng(1300 + layout * 10 + unroll)
+    L, KV, P, v = 2, 2, 16, 2048
+    lens = [37, 19]  # 3 and 2 pages, the last ones partial (5 and 3 rows)
+    pages = [-(-n // P) for n in lens]
+    NP = 4 * sum(pages)
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src = [perm[:3], perm[3:5]]
+    t_dst = [perm[5:8], perm[8:10]]
+    specs = [wl.ChunkSpec(0, 0, 37, 0, L, layout), wl.ChunkSpec(1, 0, 19, 0, L, layout)]
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape, align=wl.STRIPE_ALIGN)
+    nbytes = wl._arena_bytes(specs, shape)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    c = cfg(4, 1, 1024, unroll, 0)  # 128 warps for 20 segments
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(1301 + layout)
+    arena = Arena(nbytes, "host")
+    _store(ctx, "store", dpool, src, specs, arena, 0, None, c, stream)
+    segments = (3 + 2) * L * KV
+    assert kvx.kvx_last_launch(ctx)[0] == segments
+    assert kvx.kvx_last_launch(ctx)[1] * 32 > segments  # more warps than segments
+    assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), "split store")
+    pre = dpool.host_copy()
+    _load(ctx, "load", dpool, dst, specs, arena, 0, None, c, stream)
+    assert_pool_equal(dpool, expected_load(pre, dst, specs, arena.numpy().copy()))
+    # The same load as a plan, into a third page set.
+    third = Requests([perm[10:13], perm[13:15]], lens)
+    plan = kvx.kvx_plan_create(ctx, kvx.KVX_OP_LOAD, dpool.pool, third.array,
+                               kvx.chunks_array(specs, arena.ptr), cfg=c,
+                               stream=stream.cuda_stream)
+    pre = dpool.host_copy()
+    kvx.kvx_plan_launch(plan, stream.cuda_stream)
+    stream.synchronize()
+    kvx.kvx_plan_destroy(plan)
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    assert_pool_equal(dpool, expected_load(pre, third, specs, arena.numpy().copy()))
+    arena.close()
+
+
 @pytest.mark.parametrize("stages,stage_bytes,ctas", [(2, 16, 1), (3, 1040, 2), (6, 32768, 1),
                                                     (8, 27648, 1), (3, 65536, 1)])
 def test_bulk_mapping_multi_tile_ragged(ctx, stream, stages, stage_bytes, ctas):
