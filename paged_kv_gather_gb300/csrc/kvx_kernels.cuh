@@ -14,6 +14,7 @@
 // (section "Non-Intrusive Resource Sizing"); the HBM-only transform uses every SM.
 //
 // Kernels: kvx_segment_kernel (store, load, HBM gather/scatter; the default mapping),
+// kvx_split_kernel (the same for batches with fewer segments than warps, in row slices),
 // kvx_exchange_kernel and kvx_duplex_kernel (a store batch and a load batch in one launch),
 // kvx_roundtrip_kernel (store, then load the same chunks elsewhere, ordered per unit inside
 // the launch), and two alternative mappings of a single transfer: kvx_cta_kernel (a whole
