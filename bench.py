@@ -67,7 +67,7 @@ def parse():
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
                    choices=["store", "load", "gather", "scatter", "exchange", "roundtrip",
-                            "exchange_shared", "gather_cta"],
+                            "exchange_shared", "gather_cta", "load_bulk"],
                    help="operation of --workload profile_small")
     p.add_argument("--groups", type=int, default=16,
                    help="chunk groups of the pipelined store/load round trip")
@@ -1357,7 +1357,8 @@ def run_profile_small(args, kvx, wl):
     rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
     ctx = kvx.kvx_create(0)
     sh = torch.cuda.current_stream().cuda_stream
-    if args.profile_op in ("store", "load", "exchange", "roundtrip", "exchange_shared"):
+    if args.profile_op in ("store", "load", "exchange", "roundtrip", "exchange_shared",
+                           "load_bulk"):
         buf = kvx.HostBuffer(w.store_arena_bytes)
         buf.array[:] = 0
         ch = kvx.chunks_array(w.store_chunks, buf.ptr)
@@ -1372,6 +1373,10 @@ def run_profile_small(args, kvx, wl):
             q = len(w.store_chunks) // 4
             kvx.kvx_exchange_chunks(ctx, pool, rs, np.ascontiguousarray(ch[:q]), rd,
                                     np.ascontiguousarray(ch[q:]), stream=sh)
+        elif args.profile_op == "load_bulk":  # the load, bulk-copy staging mapping
+            c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD)
+            c.mapping, c.unroll, c.stage_bytes = kvx.KVX_MAP_BULK, 6, 32768
+            kvx.kvx_load_chunks(ctx, pool, rd, ch, cfg=c, stream=sh)
         elif args.profile_op == "gather_cta":  # the HBM gather, CTA-per-segment mapping
             c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM)
             c.mapping, c.ctas_per_sm, c.threads, c.unroll = kvx.KVX_MAP_CTA, 2, 512, 8
