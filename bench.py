@@ -62,7 +62,8 @@ def parse():
     p.add_argument("--workload", default="llama8b",
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
                             "transform_sweep", "profile_small", "batch_sweep", "mla_blocks",
-                            "roundtrip_sweep", "size_sweep", "eviction"],
+                            "roundtrip_sweep", "size_sweep", "roundtrip_under_gemm",
+                            "eviction"],
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
@@ -1600,6 +1601,82 @@ def run_size_sweep(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
+def run_roundtrip_under_gemm(args, kvx, wl):
+    """The headline round trip (llama8b, one launch) beside a stream of bf16 8192^3 GEMMs:
+    round-trip GB/s and GEMM slowdown, on a high-priority stream with the default 16-SM
+    grid, and on a 16-SM green-context partition with the GEMMs on the rest."""
+    w = wl.llama8b()
+    s = w.shape
+    N = w.store_bytes()
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src_h, dst_h = w.store_requests[0].page_table, w.load_requests[0].page_table
+    src_d, dst_d = torch.from_numpy(src_h).cuda(), torch.from_numpy(dst_h).cuda()
+    rs = kvx.requests_array([(src_d.data_ptr(), src_h, w.store_requests[0].n_tokens)])
+    rd = kvx.requests_array([(dst_d.data_ptr(), dst_h, w.load_requests[0].n_tokens)])
+    host = kvx.HostBuffer(w.store_arena_bytes)
+    host.array[:] = 0
+    chunks = kvx.chunks_array(w.store_chunks, host.ptr)
+    ctx = kvx.kvx_create(0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    A = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16, generator=g)
+    B = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16, generator=g)
+    C = torch.empty(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    n_gemm = 60  # about 33 ms of GEMMs, longer than one round trip
+
+    def measure(io_stream, gemm_stream):
+        def rt():
+            kvx.kvx_roundtrip_chunks(ctx, pool, rs, rd, chunks, stream=io_stream.cuda_stream)
+
+        def gemms():
+            with torch.cuda.stream(gemm_stream):
+                for _ in range(n_gemm):
+                    torch.matmul(A, B, out=C)
+
+        rt_alone = _timed(io_stream, rt, 3, 1)
+        with torch.cuda.stream(gemm_stream):
+            g_alone = _timed(gemm_stream, gemms, 3, 1)
+        both = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(gemm_stream)
+            io_stream.wait_event(e0)
+            a0 = torch.cuda.Event(enable_timing=True)
+            a0.record(io_stream)
+            rt()
+            a1 = torch.cuda.Event(enable_timing=True)
+            a1.record(io_stream)
+            gemms()
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(gemm_stream)
+            torch.cuda.synchronize()
+            both.append((a0.elapsed_time(a1), e0.elapsed_time(e1)))
+        rt_ms = statistics.median(x[0] for x in both)
+        g_ms = statistics.median(x[1] for x in both)
+        assert kvx.kvx_get_status(ctx, io_stream.cuda_stream) == 0
+        return {"roundtrip_alone_gbs": round(2 * N / (rt_alone * 1e-3) / GB, 2),
+                "roundtrip_beside_gemm_gbs": round(2 * N / (rt_ms * 1e-3) / GB, 2),
+                "gemm_alone_ms": round(g_alone, 3), "gemm_beside_roundtrip_ms": round(g_ms, 3),
+                "gemm_slowdown_pct": round(100 * (g_ms / g_alone - 1), 2)}
+
+    row = {"workload": "llama8b_roundtrip_under_gemm", "gemms": n_gemm,
+           "gemm": "bf16 8192^3 torch.matmul"}
+    row["high_priority_stream"] = measure(torch.cuda.Stream(priority=-1), torch.cuda.Stream())
+    try:
+        part = kvx.kvx_partition_create(0, 16, -1, 0)
+        row["green_contexts_16_io_sms"] = measure(torch.cuda.ExternalStream(part.io_stream),
+                                                  torch.cuda.ExternalStream(part.compute_stream))
+        torch.cuda.synchronize()
+        part.close()
+    except kvx.KvxError as e:
+        row["green_contexts_16_io_sms"] = {"unavailable": str(e)}
+    _emit(row)
+    host.close()
+    kvx.kvx_destroy(ctx)
+
+
 def run_workload(args):
     torch.cuda.set_device(0)
     from paged_kv_gather_gb300.build import build
@@ -1610,7 +1687,8 @@ def run_workload(args):
      "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
      "profile_small": run_profile_small, "batch_sweep": run_batch_sweep,
      "mla_blocks": run_mla_blocks, "eviction": run_eviction,
-     "roundtrip_sweep": run_roundtrip_sweep, "size_sweep": run_size_sweep}[args.workload](
+     "roundtrip_sweep": run_roundtrip_sweep, "size_sweep": run_size_sweep,
+     "roundtrip_under_gemm": run_roundtrip_under_gemm}[args.workload](
         args, kvx, wl)
 
 
