@@ -332,3 +332,37 @@ def test_binding_rejects_malformed_inputs():
     bad = np.zeros(2, dtype=np.int64)  # not the chunk struct dtype
     with pytest.raises(ValueError):
         kvx.kvx_validate(pool, reqs, bad)
+
+
+def test_oracle_and_library_share_nothing():
+    """The CUDA path and the oracle are independent: neither imports, includes or links the
+    other, and the package's source never names the oracle."""
+    import pathlib
+    import re
+    root = pathlib.Path(__file__).resolve().parents[1]
+    pkg = root / "paged_kv_gather_gb300"
+    for f in list(pkg.rglob("*.py")) + list(pkg.rglob("*.cu")) + list(pkg.rglob("*.cuh")) + \
+            list(pkg.rglob("*.cpp")) + list(pkg.rglob("*.h")) + [root / "include" / "kvx.h"]:
+        text = f.read_text()
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+        assert "kv_oracle" not in text, f
+    for f in (root / "oracle").glob("*"):
+        if f.suffix in (".py", ".c"):
+            text = f.read_text()
+            assert not re.search(r"^\s*(import|from)\s+paged_kv_gather_gb300", text, re.M), f
+            assert "libkvx" not in text and '#include "kvx' not in text, f
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """The binding, away from its built library, refuses to import (no CPU fallback)."""
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "paged_kv_gather_gb300", "kvx.py")
+    shutil.copy(src, tmp_path / "kvx_copy.py")
+    code = ("import importlib.util as u; "
+            "s = u.spec_from_file_location('kvx_copy', %r); "
+            "m = u.module_from_spec(s); s.loader.exec_module(m)") % str(tmp_path / "kvx_copy.py")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert r.returncode != 0 and "is missing" in r.stderr, r.stderr[-500:]
