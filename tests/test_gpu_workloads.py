@@ -3,9 +3,12 @@ uses (the library defaults), every output byte checked against the CPU oracle.
 
 Verification copies device tensors into pinned host memory and runs the oracle on them:
   llama8b       store, load, HBM gather/scatter and the per-page DMA baseline, all layers;
-  llama70b      80 layer-streamed loads (1 MiB per-layer chunks), every layer;
-  qwen7b_batch  one batched load and one batched store running concurrently on two streams;
-  mla_sweep     every page size x chunk size cell, store and load, kernel and DMA baseline.
+                the headline round trip in one launch, and the exchange pipeline;
+  llama70b      80 layer-streamed loads, 1 MiB and 2 MiB per-layer chunks, every layer;
+  qwen7b_batch  one batched load and one batched store concurrently on two streams, and
+                both in one exchange launch;
+  mla_sweep     every page size x chunk size cell, store and load, kernel and DMA baseline;
+  mla_blocks    per-block STRIPED objects: one store, then per-layer loads.
 """
 import numpy as np
 import pytest
