@@ -568,7 +568,8 @@ def kvx_estimate_stream_us(io_us: float, compute_us: float, n_layers: int) -> Tu
 class Partition:
     """I/O partitions plus one compute partition of the GPU's SMs (green contexts).
 
-    io_streams[g] / io_sms[g] for g < io_groups; compute_stream / compute_sms for the rest.
+    io_streams[g] / io_sms_list[g] for g < io_groups (io_stream / io_sms: group 0);
+    compute_stream / compute_sms for the rest.
     """
 
     def __init__(self, handle, streams, sms):

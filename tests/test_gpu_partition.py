@@ -15,8 +15,10 @@ from paged_kv_gather_gb300.build import build  # noqa: E402
 build()
 from paged_kv_gather_gb300 import kvx  # noqa: E402
 from paged_kv_gather_gb300 import workloads as wl  # noqa: E402
-from tests.gpu_common import (Arena, DevicePool, Requests, assert_pool_equal,  # noqa: E402
-                              expected_load)
+import oracle  # noqa: E402
+from tests.gpu_common import (CANARY, Arena, DevicePool, Requests,  # noqa: E402
+                              assert_bytes_equal, assert_pool_equal, expected_load,
+                              oracle_chunks)
 
 
 def test_partition_load_and_concurrent_gemm():
@@ -54,6 +56,7 @@ def test_partition_load_and_concurrent_gemm():
         A = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
         B = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
         ref = A @ B
+        torch.cuda.synchronize()  # A and B were made on the current stream
         compute = torch.cuda.ExternalStream(part.compute_stream)
         with torch.cuda.stream(compute):
             C = A @ B
@@ -67,6 +70,49 @@ def test_partition_load_and_concurrent_gemm():
         kvx.kvx_destroy(ctx)
         arena.close()
     finally:
+        part.close()
+
+
+def test_two_io_partitions_store_and_load_at_once():
+    """Two I/O partitions plus compute: a store on one and a load on the other run at the
+    same time on disjoint SM sets, both bit-exact."""
+    part = kvx.kvx_partition_create(0, 8, io_groups=2)
+    try:
+        assert len(part.io_streams) == 2 and all(part.io_sms_list[g] >= 8 for g in range(2))
+        rng = np.random.default_rng(41)
+        L, KV, P, v, T = 3, 2, 16, 2048, 900
+        pages = -(-T // P)
+        NP = 2 * pages + 4
+        perm = rng.permutation(NP).astype(np.int32)
+        src, dst = Requests([perm[:pages]], [T]), Requests([perm[pages:2 * pages]], [T])
+        specs = wl.split_tokens(0, 0, T, 256, 0, L, wl.LAYER_MAJOR)
+        shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+        wl.place_chunks(specs, shape)
+        nbytes = wl._arena_bytes(specs, shape)
+        out, inp = Arena(nbytes, "host"), Arena(nbytes, "host")
+        data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+        inp.write(data)
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        dpool.fill_random(42)
+        pre = dpool.host_copy()
+        ctx_a, ctx_b = kvx.kvx_create(0), kvx.kvx_create(0)
+        kvx.kvx_store_chunks(ctx_a, dpool.pool, src.array, kvx.chunks_array(specs, out.ptr),
+                             stream=part.io_streams[0])
+        kvx.kvx_load_chunks(ctx_b, dpool.pool, dst.array, kvx.chunks_array(specs, inp.ptr),
+                            stream=part.io_streams[1])
+        torch.cuda.synchronize()
+        assert kvx.kvx_get_status(ctx_a, part.io_streams[0]) == 0
+        assert kvx.kvx_get_status(ctx_b, part.io_streams[1]) == 0
+        exp = np.full(nbytes + 4096, CANARY, np.uint8)
+        oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+        assert_bytes_equal(out.numpy(), exp, "store on I/O partition 0")
+        assert_pool_equal(dpool, expected_load(pre, dst, specs, data.copy()))
+        kvx.kvx_destroy(ctx_a)
+        kvx.kvx_destroy(ctx_b)
+        out.close()
+        inp.close()
+    finally:
+        torch.cuda.synchronize()
         part.close()
 
 
