@@ -1,25 +1,32 @@
 #!/usr/bin/env python3
 """Benchmark of the paged KV gather/scatter path on one GB300 (or N independent replicas).
 
-One step = one full pass of the hot path over the Llama-3.1-8B-shaped request:
-  kvx_store_chunks  32768 tokens x 32 layers x K/V (2048 random pages of a 16384-page
-                    pool) gathered into 128 layer-major chunks of 256 tokens (32 MiB each)
-                    in mapped pinned host memory, and
-  kvx_load_chunks   those chunks scattered back into a disjoint set of 2048 fresh pages,
-pipelined in chunk groups: each kvx_exchange_chunks launch stores group g and loads group
-g - 1, so both directions of the host link carry data at once.  Each direction moves N = 4 GiB; value =
-2N per step / step time (GB/s).  Inputs (4 GiB each way) exceed L2 (129 MB): no flush.
-The same store and load run back to back on one stream give the per-direction rooflines.
+One step = one full pass of the hot path over the Llama-3.1-8B-shaped request, in ONE
+kvx_roundtrip_chunks launch:
+  store  32768 tokens x 32 layers x K/V (2048 random pages of a 16384-page pool) gathered
+         into 128 layer-major chunks of 256 tokens (32 MiB each) in mapped pinned host
+         memory, and
+  load   those chunks scattered into a disjoint set of 2048 fresh pages, each page segment
+         once its own store has reached host memory,
+so both directions of the host link carry data at once.  Each direction moves N = 4 GiB;
+value = 2N per step / step time (GB/s).  Inputs (4 GiB each way) exceed L2 (129 MB): no
+flush.  The same store and load run back to back on one stream give the per-direction
+rooflines.
 
 Also measured in the same run and printed on the same JSON line:
-  host_link_peak  one 4 GiB pinned cudaMemcpyAsync per direction (the store/load roofline);
-  transform       kvx_transform_hbm gather + scatter of the same request with the chunks in
-                  HBM, against the measured HBM copy peak;
-  dma_baseline    one cudaMemcpyAsync per (chunk, layer, kv, page) segment, both ways;
-  cpu_baseline    the CPU oracle on a bounded sample of the same workload, all host cores;
-  e2e             the same step timed on the host clock through the C ABI, with the page
-                  tables uploaded from pinned host memory and the status word read back.
+  host_link_peak     pinned cudaMemcpyAsync per direction and both at once (the rooflines);
+  exchange_pipeline  the same step as 16 kvx_exchange_chunks launches (context);
+  transform          kvx_transform_hbm gather + scatter of the same request with the chunks
+                     in HBM, against the measured HBM copy peak and a same-run copy;
+  dma_baseline       one cudaMemcpyAsync per (chunk, layer, kv, page) segment, both ways;
+  cpu_baseline       the CPU oracle on a bounded sample of the same workload, all host cores
+                     and one;
+  e2e                the same step timed on the host clock through the C ABI, with the page
+                     tables uploaded from pinned host memory and the status word read back.
 
+--workload selects the other measurement modes (layer streaming, batched partial hits, the
+MLA sweeps, launch-shape sweeps, transfer sizes, the round trip beside GEMMs, background
+eviction, small cases for ncu); each prints one JSON line per measured configuration.
 --impl reference times the CPU oracle alone (the reference arm of this comparison).
 """
 from __future__ import annotations
