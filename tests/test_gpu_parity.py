@@ -896,6 +896,46 @@ def test_roundtrip_in_one_launch(ctx, stream, seed):
     arena.close()
 
 
+def test_roundtrip_many_requests_and_chunks(ctx, stream):
+    """64 requests of mixed length cut into about 540 chunks of all three layouts: the
+    round trip's unit search runs several probe levels deep."""
+    rng = np.random.default_rng(7500)
+    L, KV, P, v = 4, 2, 16, 512
+    lens = [int(x) for x in rng.integers(1, 2000, 64)]
+    pages = [-(-n // P) for n in lens]
+    NP = 2 * sum(pages) + 7
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(perm[at:at + npg])
+        t_dst.append(perm[sum(pages) + at:sum(pages) + at + npg])
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, int(rng.choice([48, 160, 256])), 0, L, r % 3)
+    order = rng.permutation(len(specs))
+    specs = [specs[i] for i in order]
+    assert len(specs) > 500
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape, align=wl.STRIPE_ALIGN)
+    nbytes = wl._arena_bytes(specs, shape)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(7501)
+    pre = dpool.host_copy()
+    arena = Arena(nbytes, "host")
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                             kvx.chunks_array(specs, arena.ptr), stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+    assert_bytes_equal(arena.numpy(), exp, "many-request round trip chunks")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
+    assert_pool_equal(dpool, pre)
+    arena.close()
+
+
 def test_roundtrip_rejects_overlapping_page_sets(ctx, stream):
     """A load page set that meets the store's sources is refused (validation level 2)."""
     rng = np.random.default_rng(7200)
