@@ -777,7 +777,11 @@ __global__ void __launch_bounds__(1024, 1)
             // HBM reads need fewer bytes in flight than host reads: four loads per lane.
             copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
                 ps, first, count, lane);
-            __syncwarp();  // every lane's writes happen before lane 0's release
+            // Each lane's host writes are performed at GPU scope, then lane 0 publishes the
+            // unit with a release (the fence costs nothing measurable, and it keeps the
+            // publication correct without leaning on the warp barrier's ordering).
+            __threadfence();
+            __syncwarp();
             if (lane == 0)
                 st_release_u32(sy.done + unit, 1u);
         }
