@@ -198,6 +198,7 @@ KVX_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 def library_path() -> str:
+    """Path of the loaded libkvx.so."""
     return _LIB_PATH
 
 
@@ -214,10 +215,12 @@ class KvxError(RuntimeError):
 
 
 def kvx_status_string(status: int) -> str:
+    """Name of a kvx_status code."""
     return _lib.kvx_status_string(status).decode()
 
 
 def kvx_version() -> int:
+    """KVX_VERSION of the loaded library."""
     return _lib.kvx_version()
 
 
@@ -237,7 +240,8 @@ class Pool:
 
     @classmethod
     def from_tensor(cls, pools, page_size: int) -> "Pool":
-        """pools: a contiguous uint8 tensor [kv_factor, num_layers, num_pages, page_size, token_bytes]."""
+        """pools: a contiguous uint8 CUDA tensor
+        [kv_factor, num_layers, num_pages, page_size, token_bytes]."""
         if pools.dim() != 5 or pools.element_size() != 1 or not pools.is_contiguous():
             raise ValueError("pools must be a contiguous byte tensor "
                              "[kv_factor, num_layers, num_pages, page_size, token_bytes]")
@@ -324,6 +328,7 @@ def _check(ctx, status: int):
 # ---------------------------------------------------------------------------- entry points
 
 def kvx_create(device: int = 0, max_descriptor_bytes: int = 0):
+    """A context on `device` (descriptor ring, status word, copy stream); raises on failure."""
     ctx = ctypes.c_void_p()
     st = _lib.kvx_create(ctypes.byref(ctx), device, max_descriptor_bytes)
     if st != KVX_OK:
@@ -332,14 +337,17 @@ def kvx_create(device: int = 0, max_descriptor_bytes: int = 0):
 
 
 def kvx_destroy(ctx) -> None:
+    """Wait for the context's launches, then free it."""
     _lib.kvx_destroy(ctx)
 
 
 def kvx_set_validation(ctx, level: int) -> None:
+    """Host validation level: 0, 1 (default) or 2 (page ids, overlap, pointer attributes)."""
     _check(ctx, _lib.kvx_set_validation(ctx, level))
 
 
 def kvx_default_launch_cfg(ctx, op: int) -> kvx_launch_cfg:
+    """The default launch configuration of an operation (KVX_OP_*)."""
     cfg = kvx_launch_cfg()
     _check(ctx, _lib.kvx_default_launch_cfg(ctx, op, ctypes.byref(cfg)))
     return cfg
@@ -348,6 +356,7 @@ def kvx_default_launch_cfg(ctx, op: int) -> kvx_launch_cfg:
 def kvx_store_chunks(ctx, pool: Pool, reqs, chunks, layer_begin: int = 0,
                      layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
                      stream: int = 0) -> None:
+    """Gather the requests' pages into the chunks (mapped pinned host memory); async on `stream`."""
     _check(ctx, _lib.kvx_store_chunks(ctx, *_batch_args(pool, reqs, chunks, layer_begin,
                                                         layer_end), _cfg_ptr(cfg), stream))
 
@@ -355,6 +364,7 @@ def kvx_store_chunks(ctx, pool: Pool, reqs, chunks, layer_begin: int = 0,
 def kvx_load_chunks(ctx, pool: Pool, reqs, chunks, layer_begin: int = 0,
                     layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
                     stream: int = 0) -> None:
+    """Scatter the chunks (mapped pinned host memory) into the requests' pages; async."""
     _check(ctx, _lib.kvx_load_chunks(ctx, *_batch_args(pool, reqs, chunks, layer_begin,
                                                        layer_end), _cfg_ptr(cfg), stream))
 
@@ -436,18 +446,21 @@ def kvx_plan_create_roundtrip(ctx, pool: Pool, src_reqs, dst_reqs, chunks, layer
 
 
 def kvx_plan_launch(plan, stream: int = 0) -> None:
+    """Launch a prepared plan on `stream` (may be captured in a CUDA graph)."""
     st = _lib.kvx_plan_launch(plan, stream)
     if st != KVX_OK:
         raise KvxError(st, "kvx_plan_launch")
 
 
 def kvx_plan_destroy(plan) -> None:
+    """Wait for the device, then free a plan (before its context)."""
     _lib.kvx_plan_destroy(plan)
 
 
 def kvx_transform_hbm(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,
                       layer_end: Optional[int] = None, cfg: Optional[kvx_launch_cfg] = None,
                       stream: int = 0) -> None:
+    """The same gather (KVX_DIR_GATHER) or scatter (KVX_DIR_SCATTER) with chunks in HBM."""
     _check(ctx, _lib.kvx_transform_hbm(ctx, direction,
                                        *_batch_args(pool, reqs, chunks, layer_begin, layer_end),
                                        _cfg_ptr(cfg), stream))
@@ -471,6 +484,7 @@ def kvx_load_chunks_noalloc(pool: Pool, reqs, chunks, layer_begin: int = 0,
 
 def kvx_dma_baseline(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,
                      layer_end: Optional[int] = None, stream: int = 0) -> int:
+    """Comparison only: one cudaMemcpyAsync per segment; returns the number of copies."""
     n = ctypes.c_int64(0)
     _check(ctx, _lib.kvx_dma_baseline(ctx, direction,
                                       *_batch_args(pool, reqs, chunks, layer_begin, layer_end),
@@ -488,6 +502,7 @@ def kvx_get_status(ctx, stream: int = 0) -> int:
 
 
 def kvx_last_error(ctx) -> str:
+    """Message of the context's last error ("" if none)."""
     return _lib.kvx_last_error(ctx).decode()
 
 
@@ -503,6 +518,7 @@ def kvx_last_launch(ctx) -> Tuple[int, int, int, int]:
 def kvx_validate(pool: Pool, reqs, chunks, layer_begin: int = 0,
                  layer_end: Optional[int] = None, op: int = KVX_OP_STORE,
                  level: int = 1) -> Tuple[int, str]:
+    """Host validation alone, no launch: (status, message)."""
     buf = ctypes.create_string_buffer(512)
     st = _lib.kvx_validate(*_batch_args(pool, reqs, chunks, layer_begin, layer_end), op, level,
                            buf, len(buf))
@@ -511,6 +527,7 @@ def kvx_validate(pool: Pool, reqs, chunks, layer_begin: int = 0,
 
 def kvx_plan_count(pool: Pool, reqs, chunks, layer_begin: int = 0,
                    layer_end: Optional[int] = None) -> Tuple[int, int]:
+    """Work of a transfer without running it: (page segments, payload bytes one way)."""
     segs, nbytes = ctypes.c_int64(), ctypes.c_int64()
     st = _lib.kvx_plan_count(*_batch_args(pool, reqs, chunks, layer_begin, layer_end),
                              ctypes.byref(segs), ctypes.byref(nbytes))
@@ -521,6 +538,7 @@ def kvx_plan_count(pool: Pool, reqs, chunks, layer_begin: int = 0,
 
 def kvx_chunk_policy(pool: Pool, layer_streaming: bool = False,
                      target_bytes: int = 0) -> Tuple[int, int]:
+    """Chunk-size policy: (tokens per chunk, layers per chunk) for a pool."""
     t, l = ctypes.c_int32(), ctypes.c_int32()
     st = _lib.kvx_chunk_policy(ctypes.byref(pool.c), int(layer_streaming), target_bytes,
                                ctypes.byref(t), ctypes.byref(l))
@@ -530,6 +548,7 @@ def kvx_chunk_policy(pool: Pool, layer_streaming: bool = False,
 
 
 def kvx_default_link_model() -> kvx_link_model:
+    """The measured GB300 + NVLink-C2C link model used by the estimators."""
     m = kvx_link_model()
     st = _lib.kvx_default_link_model(ctypes.byref(m))
     if st != KVX_OK:
@@ -539,6 +558,7 @@ def kvx_default_link_model() -> kvx_link_model:
 
 def kvx_estimate_us(model: kvx_link_model, op: int, nbytes: int,
                     cfg: Optional[kvx_launch_cfg] = None) -> float:
+    """Predicted microseconds of one store, load or transform call (Little's law)."""
     us = ctypes.c_double()
     st = _lib.kvx_estimate_us(ctypes.byref(model), op, nbytes, _cfg_ptr(cfg), ctypes.byref(us))
     if st != KVX_OK:
@@ -548,6 +568,7 @@ def kvx_estimate_us(model: kvx_link_model, op: int, nbytes: int,
 
 def kvx_estimate_pair_us(model: kvx_link_model, op: int, store_bytes: int, load_bytes: int,
                          unit_bytes: int = 0, cfg: Optional[kvx_launch_cfg] = None) -> float:
+    """Predicted microseconds of one exchange or round trip (both link directions)."""
     us = ctypes.c_double()
     st = _lib.kvx_estimate_pair_us(ctypes.byref(model), op, store_bytes, load_bytes, unit_bytes,
                                    _cfg_ptr(cfg), ctypes.byref(us))
@@ -557,6 +578,7 @@ def kvx_estimate_pair_us(model: kvx_link_model, op: int, store_bytes: int, load_
 
 
 def kvx_estimate_stream_us(io_us: float, compute_us: float, n_layers: int) -> Tuple[float, float]:
+    """Layer-streaming model: (end-to-end us, I/O bubble us)."""
     e2e, bubble = ctypes.c_double(), ctypes.c_double()
     st = _lib.kvx_estimate_stream_us(io_us, compute_us, n_layers, ctypes.byref(e2e),
                                      ctypes.byref(bubble))
@@ -595,6 +617,7 @@ class Partition:
 
 def kvx_partition_create(device: int, io_sms: int, io_priority: int = -1,
                          compute_priority: int = 0, io_groups: int = 1) -> Partition:
+    """Green-context SM partitions: io_groups I/O partitions of >= io_sms SMs and the rest."""
     h = ctypes.c_void_p()
     msg = ctypes.create_string_buffer(256)
     st = _lib.kvx_partition_create(device, io_groups, io_sms, io_priority, compute_priority,
@@ -614,16 +637,19 @@ def kvx_partition_create(device: int, io_sms: int, io_priority: int = -1,
 
 
 def kvx_partition_info(p: Partition, group: int):
+    """(stream handle, SMs) of partition `group` (io_groups = the compute partition)."""
     if group < len(p.io_streams):
         return p.io_streams[group], p.io_sms_list[group]
     return p.compute_stream, p.compute_sms
 
 
 def kvx_partition_destroy(handle) -> None:
+    """Wait for the device, then free the partitions and their streams."""
     _lib.kvx_partition_destroy(handle)
 
 
 def kvx_host_alloc(nbytes: int) -> int:
+    """Mapped pinned host memory of `nbytes`; returns its address."""
     p = ctypes.c_void_p()
     st = _lib.kvx_host_alloc(ctypes.byref(p), nbytes)
     if st != KVX_OK:
@@ -632,18 +658,21 @@ def kvx_host_alloc(nbytes: int) -> int:
 
 
 def kvx_host_free(ptr: int) -> None:
+    """Free memory from kvx_host_alloc."""
     st = _lib.kvx_host_free(ptr)
     if st != KVX_OK:
         raise KvxError(st, "kvx_host_free")
 
 
 def kvx_host_register(ptr: int, nbytes: int) -> None:
+    """Pin and map existing host memory for the device."""
     st = _lib.kvx_host_register(ptr, nbytes)
     if st != KVX_OK:
         raise KvxError(st, "kvx_host_register")
 
 
 def kvx_host_unregister(ptr: int) -> None:
+    """Undo kvx_host_register."""
     st = _lib.kvx_host_unregister(ptr)
     if st != KVX_OK:
         raise KvxError(st, "kvx_host_unregister")
