@@ -1047,7 +1047,8 @@ def run_mla_sweep(args, kvx, wl):
             pools = _pool_tensor(s, w.seed, wl)
             pool = kvx.Pool.from_tensor(pools, s.page_size)
             src, dst = w.store_requests[0], w.load_requests[0]
-            ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+            ps = torch.from_numpy(src.page_table).cuda()
+            pd = torch.from_numpy(dst.page_table).cuda()
             rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
             rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
             arena = kvx.HostBuffer(w.store_arena_bytes)
@@ -1067,7 +1068,8 @@ def run_mla_sweep(args, kvx, wl):
                 host_us.append((time.perf_counter() - t0) * 1e6)
                 stream.synchronize()
             dma = {}
-            for name, d, rq in (("store", kvx.KVX_DIR_GATHER, rs), ("load", kvx.KVX_DIR_SCATTER, rd)):
+            for name, d, rq in (("store", kvx.KVX_DIR_GATHER, rs),
+                                ("load", kvx.KVX_DIR_SCATTER, rd)):
                 kvx.kvx_dma_baseline(ctx, d, pool, rq, ch, stream=sh)
                 stream.synchronize()
                 t0 = time.perf_counter()
@@ -1163,7 +1165,8 @@ def run_transform_sweep(args, kvx, wl):
             for name, d, rq in (("gather", kvx.KVX_DIR_GATHER, rs),
                                 ("scatter", kvx.KVX_DIR_SCATTER, rd)):
                 c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM)
-                c.sm_cap, c.ctas_per_sm, c.threads, c.unroll, c.store_hint = 0, ctas, threads, unroll, hint
+                c.sm_cap, c.ctas_per_sm, c.threads = 0, ctas, threads
+                c.unroll, c.store_hint = unroll, hint
                 c.mapping, c.stage_bytes, c.batch = mapping, stage, batch
                 ms = _timed(stream, lambda: kvx.kvx_transform_hbm(ctx, d, pool, rq, ch, 0,
                                                                   s.num_layers, c, sh), 10, 3)

@@ -169,7 +169,8 @@ def tiny(seed: int = 1000) -> Workload:
     dst = RequestSpec(perm[n:2 * n].copy(), T)
     chunks = [ChunkSpec(0, 0, T, 0, shape.num_layers, TOKEN_MAJOR)]
     place_chunks(chunks, shape)
-    return Workload("tiny", seed, shape, [src], chunks, [dst], [ChunkSpec(**vars(c)) for c in chunks],
+    return Workload("tiny", seed, shape, [src], chunks, [dst],
+                    [ChunkSpec(**vars(c)) for c in chunks],
                     True, "one token-major chunk, load into a disjoint random page set")
 
 

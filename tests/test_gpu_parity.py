@@ -108,7 +108,8 @@ def cta(sm_cap, ctas_per_sm, threads, unroll, hint):
 CONFIGS = [cfg(), cfg(1, 1, 32, 1, 0), cfg(2, 1, 64, 2, 1), cfg(3, 2, 256, 4, 0),
            cfg(0, 1, 1024, 8, 1), cfg(1, 1, 1024, 8, 0), cfg(5, 3, 96, 4, 1),
            bulk(), bulk(2, 1, 2, 64), bulk(3, 2, 3, 4096), bulk(0, 1, 8, 1040),
-           cfg(3, 1, 256, 8, 0, batch=32), cfg(2, 2, 128, 2, 1, batch=5), cfg(0, 1, 64, 4, 0, batch=2),
+           cfg(3, 1, 256, 8, 0, batch=32), cfg(2, 2, 128, 2, 1, batch=5),
+           cfg(0, 1, 64, 4, 0, batch=2),
            cta(2, 1, 256, 8, 1), cta(1, 1, 32, 1, 0), cta(0, 2, 512, 4, 0), cta(3, 1, 96, 2, 1)]
 
 
@@ -300,8 +301,8 @@ def test_bulk_mapping_rejects_bad_stage_shapes(ctx, stream):
     reqs = Requests([np.array([0], np.int32)], [1])
     arena = Arena(16, "host")
     ch = kvx.chunks_array([wl.ChunkSpec(0, 0, 1, 0, 1, 0, 0)], arena.ptr)
-    for bad in (bulk(stages=1), bulk(stages=9), bulk(stage_bytes=24), bulk(stages=8, stage_bytes=65536),
-                cfg(batch=33), cfg(batch=-1)):
+    for bad in (bulk(stages=1), bulk(stages=9), bulk(stage_bytes=24),
+                bulk(stages=8, stage_bytes=65536), cfg(batch=33), cfg(batch=-1)):
         with pytest.raises(kvx.KvxError) as e:
             kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, ch, 0, 1, bad, stream.cuda_stream)
         assert e.value.status == kvx.KVX_ERR_INVALID_ARG
@@ -1027,7 +1028,8 @@ def test_roundtrip_with_more_ctas_than_can_be_resident(ctx, stream):
                              stream.cuda_stream)
     stream.synchronize()
     assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
-    assert kvx.kvx_last_launch(ctx)[1] == 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert kvx.kvx_last_launch(ctx)[1] == 4 * n_sms
     exp = np.full(nbytes + 4096, CANARY, np.uint8)
     oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
     assert_bytes_equal(arena.numpy(), exp, "round trip, oversubscribed grid")
