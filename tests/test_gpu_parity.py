@@ -141,6 +141,59 @@ def test_random_batches_all_paths(ctx, stream, seed):
         arena.close()
 
 
+def test_random_launch_shapes(ctx, stream):
+    """150 random batches, each under a random launch shape (SM cap, CTAs per SM, threads,
+    unroll, hint, batch, sometimes the CTA mapping) through a store then load, a round trip
+    or an exchange with a random share of the batch loaded."""
+    for seed in range(150):
+        rng = np.random.default_rng(90000 + seed)
+        shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
+        L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size,
+                           shape.token_bytes, shape.num_pages)
+        c = cfg(int(rng.integers(0, 9)), int(rng.integers(1, 4)), 32 * int(rng.integers(1, 33)),
+                int(rng.choice([1, 2, 4, 8])), int(rng.integers(0, 2)),
+                batch=int(rng.choice([0, 0, 1, 2, 3, 7, 16, 32])))
+        op = int(rng.integers(0, 3))  # 0 store + load, 1 round trip, 2 exchange
+        if op == 0 and rng.random() < 0.3:
+            c.mapping = kvx.KVX_MAP_CTA
+        nbytes = wl._arena_bytes(specs, shape)
+        src, dst = Requests(tables, lens), Requests(load_tables, lens)
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        dpool.fill_random(seed)
+        pre = dpool.host_copy()
+        out = Arena(nbytes, "host")
+        ch = kvx.chunks_array(specs, out.ptr)
+        exp = np.full(nbytes + 4096, CANARY, np.uint8)
+        oracle.store(pre, src.oracle(), oracle_chunks(specs, exp), lb, le)
+        what = f"seed {seed} op {op} cfg {c.as_dict()}"
+        if op == 0:
+            kvx.kvx_store_chunks(ctx, dpool.pool, src.array, ch, lb, le, c, stream.cuda_stream)
+            stream.synchronize()
+            assert_bytes_equal(out.numpy(), exp, what)
+            kvx.kvx_load_chunks(ctx, dpool.pool, dst.array, ch, lb, le, c, stream.cuda_stream)
+            oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp), lb, le)
+        elif op == 1:
+            kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array, ch, lb, le, c,
+                                     stream.cuda_stream)
+            oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp), lb, le)
+        else:
+            inp = Arena(nbytes, "host")
+            data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+            inp.write(data)
+            lspecs = specs[:int(rng.integers(0, len(specs) + 1))]
+            kvx.kvx_exchange_chunks(ctx, dpool.pool, src.array, ch, dst.array,
+                                    kvx.chunks_array(lspecs, inp.ptr), lb, le, c,
+                                    stream.cuda_stream)
+            stream.synchronize()
+            inp.close()
+            oracle.load(pre, dst.oracle(), oracle_chunks(lspecs, data), lb, le)
+        stream.synchronize()
+        assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0, what
+        assert_bytes_equal(out.numpy(), exp, what)
+        assert_pool_equal(dpool, pre)
+        out.close()
+
+
 @pytest.mark.parametrize("unroll", [1, 2, 4, 8])
 @pytest.mark.parametrize("hint", [0, 1])
 @pytest.mark.parametrize("batch", [1, 7, 32])
