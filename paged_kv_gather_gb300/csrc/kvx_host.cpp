@@ -454,7 +454,7 @@ kvx_status kvx_estimate_us(const kvx_link_model *m, int op, int64_t bytes,
     // The operation's defaults when no configuration is given (kept in step with the
     // library's kvx_default_launch_cfg).
     int sm_cap = op <= KVX_OP_LOAD ? 16 : 0, ctas = op <= KVX_OP_LOAD ? 1 : 2;
-    int threads = op <= KVX_OP_LOAD ? 1024 : 256, unroll = 8;
+    int threads = op <= KVX_OP_LOAD ? 1024 : 256, unroll = op <= KVX_OP_LOAD ? 8 : 4;
     if (cfg) {
         sm_cap = cfg->sm_cap;
         if (cfg->ctas_per_sm)

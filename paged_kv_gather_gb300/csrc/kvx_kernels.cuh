@@ -121,6 +121,67 @@ __device__ __forceinline__ void copy_contig(const uint4 *__restrict__ s, uint4 *
     }
 }
 
+// 32-byte accesses (sm_100 and later): one vector of eight 32-bit words per lane, so each
+// warp instruction moves 1 KiB.  Used by the HBM transform when every address it touches
+// is 32-byte aligned (the host checks the pool, the chunks and token_bytes).
+struct V8 {
+    unsigned a, b, c, d, e, f, g, h;
+};
+
+__device__ __forceinline__ V8 ld_nc_v8(const V8 *p)
+{
+    V8 r;
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r.a), "=r"(r.b), "=r"(r.c), "=r"(r.d), "=r"(r.e), "=r"(r.f), "=r"(r.g), "=r"(r.h)
+        : "l"(p));
+    return r;
+}
+
+template <int HINT>
+__device__ __forceinline__ void st_v8(V8 *p, const V8 &v)
+{
+    if (HINT == KVX_HINT_STREAMING)
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+                     "r"(v.a), "r"(v.b), "r"(v.c), "r"(v.d), "r"(v.e), "r"(v.f), "r"(v.g),
+                     "r"(v.h)
+                     : "memory");
+    else
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+                     "r"(v.a), "r"(v.b), "r"(v.c), "r"(v.d), "r"(v.e), "r"(v.f), "r"(v.g),
+                     "r"(v.h)
+                     : "memory");
+}
+
+// Contiguous copy of n32 32-byte units: lane i owns units i, i + 32, ...; U loads in flight.
+template <int U, int HINT>
+__device__ __forceinline__ void copy_contig32(const V8 *__restrict__ s, V8 *__restrict__ d,
+                                              int n32, int lane)
+{
+    s += lane;
+    d += lane;
+    int rem = n32 - lane;
+    for (; rem > 32 * (U - 1); rem -= 32 * U, s += 32 * U, d += 32 * U) {
+        V8 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            r[u] = ld_nc_v8(s + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            st_v8<HINT>(d + 32 * u, r[u]);
+    }
+    if (rem > 0) {
+        V8 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (32 * u < rem)
+                r[u] = ld_nc_v8(s + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (32 * u < rem)
+                st_v8<HINT>(d + 32 * u, r[u]);
+    }
+}
+
 // One work item resolved to addresses: `rows` rows of row_bytes, contiguous on the page side
 // (pitch = token_bytes) and contiguous or strided on the chunk side.
 struct Segment {
@@ -208,9 +269,25 @@ __device__ __forceinline__ Segment shfl_segment(const Segment &s, int src_lane)
     return r;
 }
 
-template <int U, int HINT, bool NC = true>
+// W32: 32-byte accesses, U / 2 of them in flight per lane (the same bytes as U 16-byte ones);
+// only for segments whose addresses and sizes are all multiples of 32 bytes.
+template <int U, int HINT, bool NC = true, bool W32 = false>
 __device__ __forceinline__ void copy_segment(const Segment &sg, int64_t v, int lane)
 {
+    if (W32) {
+        constexpr int U32 = U > 1 ? U / 2 : 1;
+        if (sg.contiguous) {
+            copy_contig32<U32, HINT>(reinterpret_cast<const V8 *>(sg.src),
+                                     reinterpret_cast<V8 *>(sg.dst),
+                                     int((int64_t(sg.rows) * v) >> 5), lane);
+        } else {
+            for (int r = 0; r < sg.rows; ++r)
+                copy_contig32<1, HINT>(reinterpret_cast<const V8 *>(sg.src + r * sg.s_pitch),
+                                       reinterpret_cast<V8 *>(sg.dst + r * sg.d_pitch),
+                                       int(v >> 5), lane);
+        }
+        return;
+    }
     if (sg.contiguous) {
         copy_contig<U, HINT, NC>(reinterpret_cast<const uint4 *>(sg.src),
                                  reinterpret_cast<uint4 *>(sg.dst),
@@ -229,7 +306,7 @@ __device__ __forceinline__ void copy_segment(const Segment &sg, int64_t v, int l
 // page segments of 16 KiB and more.  BATCHED = true (short segments): each lane resolves
 // one of p.batch consecutive segments in parallel and the warp then copies them back to
 // back, so the lookup latency of short segments overlaps instead of adding up.
-template <int U, int DIR, int HINT, bool BATCHED>
+template <int U, int DIR, int HINT, bool BATCHED, bool W32 = false>
 __device__ __forceinline__ void run_segments(const Plan &p, int64_t warp, int64_t n_warps,
                                              int lane)
 {
@@ -238,7 +315,7 @@ __device__ __forceinline__ void run_segments(const Plan &p, int64_t warp, int64_
         for (int64_t item = warp; item < p.total_items; item += n_warps) {
             Segment sg;
             if (resolve_segment<DIR>(p, item, lane, sg))
-                copy_segment<U, HINT>(sg, v, lane);
+                copy_segment<U, HINT, true, W32>(sg, v, lane);
         }
     } else {
         const int B = p.batch;
@@ -258,19 +335,19 @@ __device__ __forceinline__ void run_segments(const Plan &p, int64_t warp, int64_
             for (int k = 0; k < B; ++k) {
                 const Segment s = shfl_segment(sg, k);
                 if (valid & (1u << k))
-                    copy_segment<U, HINT>(s, v, lane);
+                    copy_segment<U, HINT, true, W32>(s, v, lane);
             }
         }
     }
 }
 
-template <int U, int DIR, int HINT, bool BATCHED>
+template <int U, int DIR, int HINT, bool BATCHED, bool W32 = false>
 __global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    run_segments<U, DIR, HINT, BATCHED>(p, warp, n_warps, lane);
+    run_segments<U, DIR, HINT, BATCHED, W32>(p, warp, n_warps, lane);
 }
 
 // Few segments, many warps: each segment is cut into p.split slices of its rows, one warp
@@ -874,34 +951,38 @@ RoundTripFn pick_roundtrip(int unroll, bool batched)
 
 typedef void (*KernelFn)(Plan);
 
-template <int U, bool BATCHED>
+template <int U, bool BATCHED, bool W32>
 KernelFn pick_hint_dir(int dir, int hint)
 {
     if (dir == KVX_DIR_GATHER)
-        return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_GATHER, 1, BATCHED>
-                                          : kvx_segment_kernel<U, KVX_DIR_GATHER, 0, BATCHED>;
-    return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_SCATTER, 1, BATCHED>
-                                      : kvx_segment_kernel<U, KVX_DIR_SCATTER, 0, BATCHED>;
+        return hint == KVX_HINT_STREAMING
+                   ? kvx_segment_kernel<U, KVX_DIR_GATHER, 1, BATCHED, W32>
+                   : kvx_segment_kernel<U, KVX_DIR_GATHER, 0, BATCHED, W32>;
+    return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_SCATTER, 1, BATCHED, W32>
+                                      : kvx_segment_kernel<U, KVX_DIR_SCATTER, 0, BATCHED, W32>;
 }
 
-template <bool BATCHED>
+template <bool BATCHED, bool W32>
 KernelFn pick_unroll(int unroll, int dir, int hint)
 {
     switch (unroll) {
-    case 1: return pick_hint_dir<1, BATCHED>(dir, hint);
-    case 2: return pick_hint_dir<2, BATCHED>(dir, hint);
-    case 4: return pick_hint_dir<4, BATCHED>(dir, hint);
-    case 8: return pick_hint_dir<8, BATCHED>(dir, hint);
+    case 1: return pick_hint_dir<1, BATCHED, W32>(dir, hint);
+    case 2: return pick_hint_dir<2, BATCHED, W32>(dir, hint);
+    case 4: return pick_hint_dir<4, BATCHED, W32>(dir, hint);
+    case 8: return pick_hint_dir<8, BATCHED, W32>(dir, hint);
     }
     return nullptr;
 }
 
 // The warp-segment kernel for (unroll, direction, hint), batched when more than one
-// segment is resolved per warp at once.
-KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1)
+// segment is resolved per warp at once, with 32-byte accesses when w32.
+KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1, bool w32 = false)
 {
-    return batch > 1 ? pick_unroll<true>(unroll, dir, hint)
-                     : pick_unroll<false>(unroll, dir, hint);
+    if (w32)
+        return batch > 1 ? pick_unroll<true, true>(unroll, dir, hint)
+                         : pick_unroll<false, true>(unroll, dir, hint);
+    return batch > 1 ? pick_unroll<true, false>(unroll, dir, hint)
+                     : pick_unroll<false, false>(unroll, dir, hint);
 }
 
 template <int U>

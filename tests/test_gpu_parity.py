@@ -722,6 +722,45 @@ def test_descriptor_capacity_error():
         kvx.kvx_destroy(small)
 
 
+@pytest.mark.parametrize("v,shift,layout", [(64, 0, wl.LAYER_MAJOR), (64, 0, wl.TOKEN_MAJOR),
+                                             (2048, 0, wl.STRIPED), (48, 0, wl.LAYER_MAJOR),
+                                             (64, 16, wl.LAYER_MAJOR)])
+@pytest.mark.parametrize("unroll", [1, 2, 4, 8])
+def test_transform_32_byte_accesses_and_fallbacks(ctx, stream, v, shift, layout, unroll):
+    """The HBM transform takes 32-byte accesses when token_bytes, the pool and every chunk are
+    32-byte aligned (v = 64, 2048), and 16-byte ones otherwise (v = 48; chunks 16 bytes off
+    a 32-byte boundary).  Both, for every unroll and row layout, against the oracle."""
+    rng = np.random.default_rng(1500 + v + shift + layout * 7 + unroll)
+    L, KV, P = 3, 2, 16
+    lens = [700, 230]
+    pages = [-(-n // P) for n in lens]
+    NP = 2 * sum(pages) + 3
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(perm[at:at + npg])
+        t_dst.append(perm[sum(pages) + at:sum(pages) + at + npg])
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, 96, 0, L, layout)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape, align=wl.STRIPE_ALIGN)
+    nbytes = wl._arena_bytes(specs, shape)
+    for c in specs:
+        c.offset += shift
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    c = cfg(0, 2, 256, unroll, 1)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(1501 + unroll)
+    arena = Arena(nbytes + shift, "device")
+    _store(ctx, "gather", dpool, src, specs, arena, 0, None, c, stream)
+    assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes + shift), "gather")
+    pre = dpool.host_copy()
+    _load(ctx, "scatter", dpool, dst, specs, arena, 0, None, c, stream)
+    assert_pool_equal(dpool, expected_load(pre, dst, specs, arena.numpy().copy()))
+
+
 def test_default_launch_configs(ctx):
     for op in range(5):
         c = kvx.kvx_default_launch_cfg(ctx, op)
