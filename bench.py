@@ -1600,10 +1600,43 @@ def run_size_sweep(args, kvx, wl):
         row = {"workload": "llama8b_size_sweep", "chunks": n, "bytes": nbytes}
         for name, op, fn, rq in (("store", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs),
                                  ("load", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd)):
-            ms = _timed(stream, lambda: fn(ctx, pool, rq, part, stream=sh), 10, 3)
+            def call():
+                fn(ctx, pool, rq, part, stream=sh)
+
+            ms = _timed(stream, call, 10, 3)
             row[f"{name}_us"] = round(ms * 1e3, 2)
             row[f"{name}_gbs"] = round(nbytes / (ms * 1e-3) / GB, 2)
             row[f"{name}_model_us"] = round(kvx.kvx_estimate_us(model, op, nbytes), 2)
+            if nbytes > (64 << 20):
+                continue
+            # Where a small call's fixed cost goes: host time of the call alone, calls issued
+            # back to back (the host runs ahead), a prepared plan, and that plan as a graph.
+            host = []
+            for _ in range(20):
+                stream.synchronize()
+                t0 = time.perf_counter()
+                call()
+                host.append(time.perf_counter() - t0)
+            stream.synchronize()
+            reps = 20
+            row[f"{name}_host_us"] = round(statistics.median(host) * 1e6, 2)
+            row[f"{name}_back_to_back_us"] = round(
+                _timed(stream, lambda: [call() for _ in range(reps)], 5, 2) * 1e3 / reps, 2)
+            plan = kvx.kvx_plan_create(ctx, op, pool, rq, part, 0, None, None, sh)
+            row[f"{name}_plan_us"] = round(
+                _timed(stream, lambda: kvx.kvx_plan_launch(plan, sh), 10, 3) * 1e3, 2)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                kvx.kvx_plan_launch(plan, torch.cuda.current_stream().cuda_stream)
+
+            def replay():
+                with torch.cuda.stream(stream):
+                    graph.replay()
+
+            row[f"{name}_graph_us"] = round(_timed(stream, replay, 10, 3) * 1e3, 2)
+            torch.cuda.synchronize()
+            del graph
+            kvx.kvx_plan_destroy(plan)
         _emit(row)
         n *= 2
     assert kvx.kvx_get_status(ctx, sh) == 0
