@@ -136,7 +136,8 @@ typedef struct kvx_chunk {
 
 /* Work mapping of the transfer kernel. */
 #define KVX_MAP_WARP_SEGMENT 0  /* one warp per (chunk, layer, kv, page) segment; lanes move
-                                   16-byte units through registers */
+                                   16-byte units through registers (32-byte units for an
+                                   HBM transform on 32-byte-aligned memory) */
 #define KVX_MAP_BULK 1          /* one warp per CTA streams segments through a ring of
                                    shared-memory stages with bulk async copies
                                    (cp.async.bulk, mbarrier completion); `unroll` is the
@@ -157,8 +158,10 @@ typedef struct kvx_launch_cfg {
     int32_t threads;      /* threads per CTA, multiple of 32 in [32, 1024]; 0 = default
                              (the bulk mapping always runs one warp per CTA) */
     int32_t unroll;       /* warp-segment and CTA mappings: 16-byte loads in flight per
-                             thread before its stores (1, 2, 4 or 8); bulk mapping:
-                             shared-memory stages (2..8).  0 = default */
+                             thread before its stores (1, 2, 4 or 8; where
+                             kvx_transform_hbm moves 32-byte units, max(unroll / 2, 1)
+                             32-byte loads); bulk mapping: shared-memory stages (2..8).
+                             0 = default */
     int32_t store_hint;   /* KVX_HINT_* (warp-segment and CTA mappings) */
     int32_t mapping;      /* KVX_MAP_* */
     int32_t stage_bytes;  /* bulk mapping: bytes per shared-memory stage, a multiple of 16;
@@ -264,7 +267,10 @@ kvx_status kvx_roundtrip_chunks(kvx_ctx *ctx, const kvx_pool *pool,
 
 /* transform: the same gather (dir = KVX_DIR_GATHER) or scatter (KVX_DIR_SCATTER) with
  * the chunks in device memory: the explicit HBM-to-HBM layout pass that "Strata Guide",
- * section "Two-Dimensional Memory Layout Decoupling", names as the conventional cost. */
+ * section "Two-Dimensional Memory Layout Decoupling", names as the conventional cost.
+ * With the warp-segment mapping, when token_bytes, every pool layer and every chunk pointer
+ * are multiples of 32 bytes, lanes move 32-byte units (max(unroll / 2, 1) loads in
+ * flight); otherwise 16-byte units.  The result is the same either way. */
 kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,
                              const kvx_request *reqs, int n_req, const kvx_chunk *chunks,
                              int n_chunks, int layer_begin, int layer_end,
