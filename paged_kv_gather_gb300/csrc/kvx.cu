@@ -557,12 +557,15 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
 }
 
 // Units, lag and grid of a round trip whose work counters and completion words start at
-// `sync` (sync_bytes(), zeroed before each launch).
-void roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, char *sync,
+// `sync` (sync_bytes(), zeroed before each launch).  False when the units do not fit the
+// kernel's 32-bit unit indices.
+bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, char *sync,
                      RoundTripSync *sy, LaunchShape *sh)
 {
     sy->unit_items = ps.batch;
     sy->units = (ps.total_items + sy->unit_items - 1) / sy->unit_items;
+    if (sy->units >= (int64_t(1) << 31))
+        return false;
     sy->next = reinterpret_cast<unsigned *>(sync);
     sy->done = reinterpret_cast<unsigned *>(sync + 256);
     const int64_t warps_per_cta = cfg.threads / 32;
@@ -575,6 +578,7 @@ void roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &
     sh->ctas = ctas;
     sh->threads = cfg.threads;
     sh->fn = reinterpret_cast<const void *>(pick_roundtrip(cfg.unroll, ps.batch > 1));
+    return true;
 }
 
 size_t roundtrip_sync_bytes(const Plan &ps)
@@ -643,7 +647,9 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
                        (long long)ps.total_items, sync_off + sync_bytes, ctx->slot_bytes);
     RoundTripSync sy;
     LaunchShape shape;
-    roundtrip_setup(ctx, cfg, ps, slot->dev + sync_off, &sy, &shape);
+    if (!roundtrip_setup(ctx, cfg, ps, slot->dev + sync_off, &sy, &shape))
+        return set_err(ctx, KVX_ERR_CAPACITY, "round trip of %lld segments (%d per unit) has "
+                       "2^31 units or more", (long long)ps.total_items, ps.batch);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = stage(ctx, *slot, sync_off, sync_off, sync_bytes, s);
     if (e != cudaSuccess)
@@ -820,6 +826,11 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     p->plan = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_GATHER, lay, host.data(), host.data());
     apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->plan);
+    if ((p->plan.total_items + p->plan.batch - 1) / p->plan.batch >= (int64_t(1) << 31)) {
+        delete p;
+        return set_err(ctx, KVX_ERR_CAPACITY, "round trip of %lld segments (%d per unit) has "
+                       "2^31 units or more", (long long)p->plan.total_items, p->plan.batch);
+    }
     p->sync_bytes = roundtrip_sync_bytes(p->plan);
     cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->dev), 2 * lay.total + p->sync_bytes);
     if (e != cudaSuccess) {
@@ -833,6 +844,7 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     p->plan.status = p->load.status = ctx->status_dev;
     apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->plan);
     apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->load);
+    // The unit count was checked above, so the setup cannot fail here.
     roundtrip_setup(ctx, cfg, p->plan, p->dev + 2 * lay.total, &p->rsync, &p->shape);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), 2 * lay.total, cudaMemcpyHostToDevice, s);
