@@ -491,6 +491,22 @@ kvx_status kvx_host_unregister(void *ptr);
 const char *kvx_status_string(kvx_status status);
 int kvx_version(void);
 
+/* ---------------------------------------------------------------- test support */
+
+/* Makes the round trip's bounded wait run out, so that a test can check the timeout path
+ * without faulting or hanging the GPU.  It launches the round trip of kvx_roundtrip_chunks
+ * (same arguments and validation, all layers, default launch configuration) with every
+ * store unit counted as handed out but none performed.  Each load unit's wait for its
+ * store then ends after wait_ns nanoseconds (1 ms to 1 s; a transfer waits about 1 s).
+ * The kernel sets KVX_DEV_WAIT_TIMEOUT in the context's device status word, skips that
+ * load unit and returns; no page and no chunk is written.  The launch takes about
+ * ceil(units / warps of the grid) x wait_ns.  Read the flag with kvx_get_status.  Not a
+ * transfer: for tests of failure handling only. */
+kvx_status kvx_test_roundtrip_timeout(kvx_ctx *ctx, const kvx_pool *pool,
+                                      const kvx_request *src_reqs, const kvx_request *dst_reqs,
+                                      int n_req, const kvx_chunk *chunks, int n_chunks,
+                                      uint64_t wait_ns, kvx_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

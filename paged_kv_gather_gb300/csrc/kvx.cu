@@ -575,6 +575,7 @@ bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &
     if (ctas > needed)
         ctas = needed;
     sy->lag = unsigned(ctas * warps_per_cta);  // one unit per warp of the grid
+    sy->wait_ns = kWaitLimitNs;
     sh->ctas = ctas;
     sh->threads = cfg.threads;
     sh->fn = reinterpret_cast<const void *>(pick_roundtrip(cfg.unroll, ps.batch > 1));
@@ -604,10 +605,14 @@ cudaError_t launch_roundtrip_kernel(const LaunchShape &sh, Plan ps, Plan pl, Rou
 
 // Descriptor slot of a round trip: the store plan, the load plan (same chunks, other page
 // tables), then the work counters and one completion word per unit, zeroed per launch.
+// test_wait_ns > 0 (kvx_test_roundtrip_timeout): the store counter starts at the unit count,
+// so every store counts as handed out and none is done, and each load unit's wait ends
+// after test_wait_ns without its store.
 kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *src_reqs,
                             const kvx_request *dst_reqs, int n_req, const kvx_chunk *chunks,
                             int n_chunks, int layer_begin, int layer_end,
-                            const kvx_launch_cfg *user_cfg, kvx_stream_t stream)
+                            const kvx_launch_cfg *user_cfg, kvx_stream_t stream,
+                            uint64_t test_wait_ns = 0)
 {
     if (!ctx)
         return KVX_ERR_INVALID_ARG;
@@ -652,6 +657,13 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
                        "2^31 units or more", (long long)ps.total_items, ps.batch);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = stage(ctx, *slot, sync_off, sync_off, sync_bytes, s);
+    if (e == cudaSuccess && test_wait_ns) {
+        sy.wait_ns = test_wait_ns;
+        const unsigned all_stores = unsigned(sy.units);
+        std::memcpy(slot->host + sync_off, &all_stores, sizeof all_stores);
+        e = cudaMemcpyAsync(sy.next, slot->host + sync_off, sizeof all_stores,
+                            cudaMemcpyHostToDevice, s);
+    }
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
     e = launch_roundtrip_kernel(shape, ps, pl, sy, 0, s);
@@ -1025,6 +1037,20 @@ kvx_status kvx_roundtrip_chunks(kvx_ctx *ctx, const kvx_pool *pool,
 {
     return launch_roundtrip(ctx, pool, src_reqs, dst_reqs, n_req, chunks, n_chunks, layer_begin,
                             layer_end, cfg, stream);
+}
+
+kvx_status kvx_test_roundtrip_timeout(kvx_ctx *ctx, const kvx_pool *pool,
+                                      const kvx_request *src_reqs, const kvx_request *dst_reqs,
+                                      int n_req, const kvx_chunk *chunks, int n_chunks,
+                                      uint64_t wait_ns, kvx_stream_t stream)
+{
+    if (!ctx || !pool)
+        return KVX_ERR_INVALID_ARG;
+    if (wait_ns < 1000000ull || wait_ns > kWaitLimitNs)
+        return set_err(ctx, KVX_ERR_INVALID_ARG, "wait_ns %llu outside [1 ms, 1 s]",
+                       (unsigned long long)wait_ns);
+    return launch_roundtrip(ctx, pool, src_reqs, dst_reqs, n_req, chunks, n_chunks, 0,
+                            pool->num_layers, nullptr, stream, wait_ns);
 }
 
 kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,

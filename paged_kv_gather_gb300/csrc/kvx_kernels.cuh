@@ -705,8 +705,7 @@ __global__ void __launch_bounds__(32) kvx_bulk_kernel(const Plan p, int stage_by
 // (unit_items consecutive items) are handed out by two fetch-and-add counters, one per
 // direction.  A warp takes a store unit while the loads handed out are within `lag`
 // units (one per warp of the grid by default) of the stores handed out, and a load unit
-// otherwise,
-// so each load usually starts well after its store finished.  A warp that holds a load
+// otherwise, so each load usually starts well after its store finished.  A warp that holds a load
 // unit whose store has not been handed out yet hands out (and does) store units until it
 // has; only then does it wait for that store.  Every wait is therefore on a unit held by a
 // running warp that waits on nothing, whatever the residency of the grid, so the waits
@@ -720,6 +719,7 @@ struct RoundTripSync {
     int64_t units;
     int unit_items;
     unsigned lag;        // loads handed out may trail stores handed out by this many units
+    uint64_t wait_ns;    // limit of one wait for a store unit (about one second)
 };
 
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p)
@@ -744,7 +744,7 @@ __device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v)
 // Lane 0: bounded wait for a store unit to finish.
 __device__ __forceinline__ bool wait_unit(const RoundTripSync &sy, int64_t unit)
 {
-    const uint64_t deadline = global_ns() + kWaitLimitNs;
+    const uint64_t deadline = global_ns() + sy.wait_ns;
     while (ld_acquire_u32(sy.done + unit) == 0u) {
         if (global_ns() > deadline)
             return false;

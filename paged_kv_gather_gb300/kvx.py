@@ -141,6 +141,9 @@ _proto("kvx_plan_create", _c.c_int, [_ctx_t, _c.c_int, *_batch, _P(kvx_launch_cf
 _proto("kvx_roundtrip_chunks", _c.c_int,
        [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_int,
         _c.c_int, _P(kvx_launch_cfg), _c.c_void_p])
+_proto("kvx_test_roundtrip_timeout", _c.c_int,
+       [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int,
+        _c.c_uint64, _c.c_void_p])
 _proto("kvx_plan_create_exchange", _c.c_int,
        [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int,
         _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _P(kvx_launch_cfg), _c.c_void_p,
@@ -192,7 +195,7 @@ EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_laun
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
             "kvx_load_chunks_noalloc", "kvx_default_link_model", "kvx_estimate_us",
             "kvx_estimate_pair_us", "kvx_estimate_stream_us", "kvx_partition_create",
-            "kvx_partition_info", "kvx_partition_destroy"]
+            "kvx_partition_info", "kvx_partition_destroy", "kvx_test_roundtrip_timeout"]
 
 KVX_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -455,6 +458,18 @@ def kvx_plan_launch(plan, stream: int = 0) -> None:
 def kvx_plan_destroy(plan) -> None:
     """Wait for the device, then free a plan (before its context)."""
     _lib.kvx_plan_destroy(plan)
+
+
+def kvx_test_roundtrip_timeout(ctx, pool: Pool, src_reqs, dst_reqs, chunks, wait_ns: int,
+                               stream: int = 0) -> None:
+    """Test support: a round trip whose stores never run, so every load's wait runs out."""
+    srp, nsr = _arr_ptr(src_reqs, REQUEST_DTYPE)
+    drp, ndr = _arr_ptr(dst_reqs, REQUEST_DTYPE)
+    if nsr != ndr:
+        raise ValueError("src_reqs and dst_reqs need the same number of requests")
+    cp, nc = _arr_ptr(chunks, CHUNK_DTYPE)
+    _check(ctx, _lib.kvx_test_roundtrip_timeout(ctx, ctypes.byref(pool.c), srp, drp, nsr, cp, nc,
+                                                wait_ns, stream))
 
 
 def kvx_transform_hbm(ctx, direction: int, pool: Pool, reqs, chunks, layer_begin: int = 0,

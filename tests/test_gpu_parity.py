@@ -3,6 +3,8 @@
 All transfers go through the C ABI (libkvx.so) via the ctypes binding; expected bytes come
 from the oracle run on host copies of the same seeded inputs.
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -635,6 +637,53 @@ def test_roundtrip_page_check_skips_and_reports(ctx, stream):
     oracle.store(pre, [oracle.Request(np.array([5, 0], np.int32), 16)],
                  oracle_chunks(specs[:1], exp))
     assert_bytes_equal(arena.numpy(), exp, "valid chunk stored, bad page's chunk untouched")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
+    assert_pool_equal(dpool, pre)
+    arena.close()
+
+
+def test_roundtrip_wait_runs_out_and_reports(ctx, stream):
+    """The round trip's bounded wait, made to run out without faulting the GPU: a round trip
+    whose stores never run (kvx_test_roundtrip_timeout) ends after about one wait limit,
+    sets KVX_DEV_WAIT_TIMEOUT and writes nothing; the same context then carries a normal
+    round trip bit-exactly."""
+    L, KV, P, v, NP = 2, 2, 16, 256, 40
+    perm = np.random.default_rng(7900).permutation(NP).astype(np.int32)
+    src, dst = Requests([perm[:8]], [128]), Requests([perm[8:16]], [128])
+    specs = wl.split_tokens(0, 0, 128, 32, 0, L, wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(7901)
+    pre = dpool.host_copy()
+    arena = Arena(nbytes, "host")
+    ch = kvx.chunks_array(specs, arena.ptr)
+    for bad in (0, 999_999, 1_000_000_001):
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.kvx_test_roundtrip_timeout(ctx, dpool.pool, src.array, dst.array, ch, bad,
+                                           stream.cuda_stream)
+        assert e.value.status == kvx.KVX_ERR_INVALID_ARG
+    wait_ns = 20_000_000
+    stream.synchronize()
+    t0 = time.perf_counter()
+    kvx.kvx_test_roundtrip_timeout(ctx, dpool.pool, src.array, dst.array, ch, wait_ns,
+                                   stream.cuda_stream)
+    stream.synchronize()
+    elapsed = time.perf_counter() - t0
+    # 32 segments of 4 KiB in units of 8: four load units, one per warp, waiting together.
+    assert 0.9 * wait_ns * 1e-9 <= elapsed < 1.0, elapsed
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == kvx.KVX_DEV_WAIT_TIMEOUT
+    assert_bytes_equal(arena.numpy(), np.full(nbytes + 4096, CANARY, np.uint8),
+                       "no store ran, so no chunk byte changed")
+    assert_pool_equal(dpool, pre)
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array, ch,
+                             stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+    assert_bytes_equal(arena.numpy(), exp, "round trip after the timeout")
     oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
     assert_pool_equal(dpool, pre)
     arena.close()
