@@ -1102,7 +1102,8 @@ kvx_status kvx_dma_baseline(kvx_ctx *ctx, int dir, const kvx_pool *pool,
         const bool lm = ch.layout != KVX_CHUNK_TOKEN_MAJOR;
         int64_t slab_stride = lm ? int64_t(ch.n_tokens) * v : v;
         if (ch.layout == KVX_CHUNK_STRIPED)
-            slab_stride = (slab_stride + KVX_STRIPE_ALIGN - 1) / KVX_STRIPE_ALIGN * KVX_STRIPE_ALIGN;
+            slab_stride =
+                (slab_stride + KVX_STRIPE_ALIGN - 1) / KVX_STRIPE_ALIGN * KVX_STRIPE_ALIGN;
         const int64_t row_stride = lm ? v : int64_t(ch.n_layers) * pool->kv_factor * v;
         const int32_t t_end = ch.token_begin + ch.n_tokens;
         for (int l = lo; l < hi; ++l)

@@ -29,7 +29,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool op_is_scatter(int op) { return op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM; }
 
-int64_t pages_of(int64_t n_tokens, int64_t page_size) { return (n_tokens + page_size - 1) / page_size; }
+int64_t pages_of(int64_t n_tokens, int64_t page_size)
+{
+    return (n_tokens + page_size - 1) / page_size;
+}
 
 // Level 2: the memory behind p must be reachable by the GPU at the same address.
 kvx_status check_pointer(const void *p, bool want_host, const char *what, int index, char *msg,
