@@ -190,7 +190,14 @@ typedef struct kvx_ctx kvx_ctx;
  * pinned host + device descriptor buffers, a device status word and a non-blocking stream
  * on which each call copies its descriptors (the caller's stream waits for that copy with
  * an event, so the copy overlaps the previous kernel).  Calls therefore cannot be captured
- * into a CUDA graph; prepared plans (below) can.  Requires a GPU. */
+ * into a CUDA graph; prepared plans (below) can.  Requires a GPU.
+ *
+ * Threads: a context is not thread-safe.  Its descriptor ring, last-launch record and
+ * error text belong to whichever call is running, so calls on one context must not
+ * overlap in time; give each host thread its own context.  Streams are independent of
+ * this: one thread may issue calls on any number of streams.  kvx_plan_launch touches its
+ * context only to report an error, and kvx_load_chunks_noalloc uses no context (it
+ * serialises its own calls). */
 kvx_status kvx_create(kvx_ctx **out, int device, size_t max_descriptor_bytes);
 
 /* Synchronize with every kernel the context launched, then free its buffers. */
