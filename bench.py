@@ -91,6 +91,9 @@ def parse():
                         "shapes of --workload transform_sweep")
     p.add_argument("--mla-pages", default="1,16,64",
                    help="page sizes of the MLA round trip in --workload roundtrip_sweep")
+    p.add_argument("--mla-cfgs", default="0:0:0:0",
+                   help="sm_cap:unroll:threads:batch launch shapes of the MLA round trip in "
+                        "--workload roundtrip_sweep (0 = the default of each field)")
     p.add_argument("--chunk-tokens", type=int, default=256,
                    help="tokens per per-layer chunk of --workload llama70b (256 = 1 MiB, the "
                         "closed form; 512 = 2 MiB)")
@@ -1561,12 +1564,22 @@ def run_roundtrip_sweep(args, kvx, wl):
         mh = kvx.HostBuffer(m.store_arena_bytes)
         mh.array[:] = 0
         mch = kvx.chunks_array(m.store_chunks, mh.ptr)
-        ms = _timed(stream, lambda: kvx.kvx_roundtrip_chunks(ctx, mpool, mrs, mrd, mch,
-                                                             stream=sh), reps)
-        assert kvx.kvx_get_status(ctx, sh) == 0
-        _emit({"workload": "mla_roundtrip_one_launch", "page_size": P, "chunk_bytes": 1 << 20,
-               "bytes_each_way": Nm, "segments_each_way": kvx.kvx_last_launch(ctx)[0] // 2,
-               "ms": round(ms, 4), "gbs": round(2 * Nm / (ms * 1e-3) / GB, 2)})
+        for shape_ in [tuple(int(v) for v in x.split(":")) for x in args.mla_cfgs.split(",") if x]:
+            c = None  # all fields 0: the library's defaults (cfg = NULL)
+            if any(shape_):
+                c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_ROUNDTRIP)
+                for field, val in zip(("sm_cap", "unroll", "threads", "batch"), shape_):
+                    if val:
+                        setattr(c, field, val)
+            ms = _timed(stream, lambda: kvx.kvx_roundtrip_chunks(ctx, mpool, mrs, mrd, mch, cfg=c,
+                                                                 stream=sh), reps)
+            assert kvx.kvx_get_status(ctx, sh) == 0
+            items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
+            _emit({"workload": "mla_roundtrip_one_launch", "page_size": P,
+                   "chunk_bytes": 1 << 20, "cfg": c.as_dict() if c else "defaults",
+                   "ctas": ctas, "threads": threads, "bytes_each_way": Nm,
+                   "segments_each_way": items // 2,
+                   "ms": round(ms, 4), "gbs": round(2 * Nm / (ms * 1e-3) / GB, 2)})
         mh.close()
         del mp
     kvx.kvx_destroy(ctx)

@@ -169,7 +169,7 @@ typedef struct kvx_launch_cfg {
     int32_t batch;        /* warp-segment mapping: page segments a warp resolves at once,
                              one per lane (1..32); 0 = automatic (about 32 KiB of segments;
                              for page segments >= 16 KiB, 1 for host transfers and 2 for
-                             the HBM transform) */
+                             the HBM transform; round trips: see kvx_roundtrip_chunks) */
 } kvx_launch_cfg;
 
 typedef struct kvx_ctx kvx_ctx;
@@ -265,7 +265,10 @@ kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
  * follows the rules of kvx_store_chunks / kvx_load_chunks.  Its waits are bounded: a
  * unit whose store has not finished within about a second is skipped and
  * KVX_DEV_WAIT_TIMEOUT is set.  The descriptor buffer holds both plans plus 4 bytes per
- * unit (a unit is `batch` segments).  cfg->sm_cap counts all SMs (default 16). */
+ * unit (a unit is `batch` segments; by default one segment when page segments are 8 KiB
+ * or longer, else about 8 KiB of segments on 32 SMs or more and about 32 KiB on fewer).
+ * cfg->sm_cap counts all SMs (default 16; with cfg = NULL and page segments shorter than
+ * 16 KiB, 32, because a warp then has at most one short segment in flight). */
 kvx_status kvx_roundtrip_chunks(kvx_ctx *ctx, const kvx_pool *pool,
                                 const kvx_request *src_reqs, const kvx_request *dst_reqs,
                                 int n_req, const kvx_chunk *chunks, int n_chunks,

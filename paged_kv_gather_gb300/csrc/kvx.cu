@@ -364,14 +364,56 @@ kvx_status resolve_pair_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kv
     return st;
 }
 
-// Segments a warp resolves at once: the configured batch, else the packed default, with two
-// long segments per warp for the HBM transform (their lookups then overlap).
-void apply_batch(int op, const kvx_launch_cfg &cfg, Plan *plan)
+// Round-trip units.  A load unit waits for its own store unit, and the grid's warps hold
+// one unit each at the start (stores only) and at the end (loads only), so smaller units
+// shorten that one-way fill and drain; but every unit also pays its hand-out, completion
+// and wait, which only enough warps hide.  Measured on the MLA latent (1152-byte tokens,
+// GB/s of both directions, 1.15 GB each way):
+//  - 1, 2 and 4 tokens per page: 340.3-340.7 in units of about kRoundTripUnitBytes on 32
+//    SMs, against 332.2-336.9 in 32 KiB units on 16 SMs; 8 KiB units on 16 SMs lose
+//    (285-330), so fewer SMs keep 32 KiB units;
+//  - 8 tokens per page (9 KiB segments, one per unit): 340.9 on 32 SMs in two runs, 333.2
+//    and 341.9 on 16;
+//  - 16 tokens and more (18 KiB segments and longer): 16 SMs is best (340.7 against 338.5).
+// Hence, with no configuration given, kRoundTripShortSms SMs for page segments shorter than
+// kRoundTripShortSegment.
+constexpr int64_t kRoundTripUnitBytes = 8192;
+constexpr int64_t kRoundTripShortSegment = 16384;
+constexpr int kRoundTripShortSms = 32;
+// Page segments longer than this travel as row slices of at most this size, one unit each,
+// for the same fill and drain reason (72 KiB segments: 334.7 GB/s whole).
+constexpr int64_t kRoundTripMaxUnitBytes = 32768;
+
+// Segments a warp resolves at once: the configured batch, else the packed default (about
+// 32 KiB of segments), with two long segments per warp for the HBM transform (their
+// lookups then overlap) and the round-trip units above.
+void apply_batch(const kvx_ctx *ctx, int op, const kvx_launch_cfg &cfg, Plan *plan)
 {
-    if (cfg.batch > 0)
+    if (cfg.batch > 0) {
         plan->batch = cfg.batch;
-    else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && plan->batch == 1)
+    } else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && plan->batch == 1) {
         plan->batch = 2;
+    } else if (op == KVX_OP_ROUNDTRIP) {
+        const int64_t seg = int64_t(plan->page_size) * plan->token_bytes;
+        const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
+        if (seg >= kRoundTripUnitBytes)
+            plan->batch = 1;
+        else if (sms >= kRoundTripShortSms)
+            plan->batch = int32_t(std::min<int64_t>((kRoundTripUnitBytes + seg - 1) / seg, 32));
+    }
+}
+
+// Launch configuration of a round trip: as resolve_pair_cfg, and with no configuration
+// given, kRoundTripShortSms SMs for short page segments.
+kvx_status resolve_roundtrip_cfg(kvx_ctx *ctx, const kvx_pool *pool,
+                                 const kvx_launch_cfg *user, kvx_launch_cfg *cfg)
+{
+    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user, cfg);
+    if (st == KVX_OK && !user && pool && pool->page_size > 0 && pool->token_bytes > 0 &&
+        pool->token_bytes < kRoundTripShortSegment &&
+        int64_t(pool->page_size) * pool->token_bytes < kRoundTripShortSegment)
+        cfg->sm_cap = kRoundTripShortSms;
+    return st;
 }
 
 int op_dir(int op)
@@ -405,7 +447,7 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     Plan plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
                           slot->host, slot->dev);
     plan.status = ctx->status_dev;
-    apply_batch(op, cfg, &plan);
+    apply_batch(ctx, op, cfg, &plan);
     choose_split(ctx, cfg, &plan);
     if (plan.total_items == 0)
         return KVX_OK;
@@ -524,8 +566,8 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
     Plan pl = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, ll, slot->host + ls.total, slot->dev + ls.total);
     ps.status = pl.status = ctx->status_dev;
-    apply_batch(KVX_OP_EXCHANGE, cfg, &ps);
-    apply_batch(KVX_OP_EXCHANGE, cfg, &pl);
+    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &ps);
+    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &pl);
     if (ps.total_items + pl.total_items == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -556,14 +598,32 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
                        total);
 }
 
+// Row slices per round-trip unit: with one segment per unit by default, a page segment
+// longer than kRoundTripMaxUnitBytes is cut into slices of at most that (and at least one
+// row), each its own unit.  An explicit batch keeps whole segments.
+int roundtrip_slices(const kvx_launch_cfg &cfg, const Plan &ps)
+{
+    if (cfg.batch > 0 || ps.batch != 1)
+        return 1;
+    const int64_t seg = int64_t(ps.page_size) * ps.token_bytes;
+    const int64_t k = (seg + kRoundTripMaxUnitBytes - 1) / kRoundTripMaxUnitBytes;
+    return int(std::min<int64_t>(std::max<int64_t>(k, 1), ps.page_size));
+}
+
+int64_t roundtrip_units(const Plan &ps, int slices)
+{
+    return slices > 1 ? ps.total_items * slices : (ps.total_items + ps.batch - 1) / ps.batch;
+}
+
 // Units, lag and grid of a round trip whose work counters and completion words start at
 // `sync` (sync_bytes(), zeroed before each launch).  False when the units do not fit the
 // kernel's 32-bit unit indices.
 bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, char *sync,
                      RoundTripSync *sy, LaunchShape *sh)
 {
-    sy->unit_items = ps.batch;
-    sy->units = (ps.total_items + sy->unit_items - 1) / sy->unit_items;
+    sy->slices = roundtrip_slices(cfg, ps);
+    sy->unit_items = sy->slices > 1 ? 1 : ps.batch;
+    sy->units = roundtrip_units(ps, sy->slices);
     if (sy->units >= (int64_t(1) << 31))
         return false;
     sy->next = reinterpret_cast<unsigned *>(sync);
@@ -582,10 +642,9 @@ bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &
     return true;
 }
 
-size_t roundtrip_sync_bytes(const Plan &ps)
+size_t roundtrip_sync_bytes(const kvx_launch_cfg &cfg, const Plan &ps)
 {
-    const int64_t units = (ps.total_items + ps.batch - 1) / ps.batch;
-    return 256 + sizeof(unsigned) * size_t(units);
+    return 256 + sizeof(unsigned) * size_t(roundtrip_units(ps, roundtrip_slices(cfg, ps)));
 }
 
 // sync_bytes > 0: zero the counters and completion words on `s` first (plans; calls zero
@@ -618,7 +677,7 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
         return KVX_ERR_INVALID_ARG;
     begin_call(ctx);
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
+    kvx_status st = resolve_roundtrip_cfg(ctx, pool, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
     st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
@@ -639,12 +698,12 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
     Plan pl = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, lay, slot->host + lay.total, slot->dev + lay.total);
     ps.status = pl.status = ctx->status_dev;
-    apply_batch(KVX_OP_ROUNDTRIP, cfg, &ps);
-    apply_batch(KVX_OP_ROUNDTRIP, cfg, &pl);
+    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &ps);
+    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &pl);
     if (ps.total_items == 0)
         return KVX_OK;
     // The completion words (4 bytes per unit) are known only now that the plan is packed.
-    const size_t sync_bytes = roundtrip_sync_bytes(ps);
+    const size_t sync_bytes = roundtrip_sync_bytes(cfg, ps);
     if (sync_off + sync_bytes > ctx->slot_bytes)
         return set_err(ctx, KVX_ERR_CAPACITY,
                        "round trip of %lld segments needs %zu bytes of descriptors and "
@@ -725,7 +784,7 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
     p->plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
                         host.data(), p->dev);
     p->plan.status = ctx->status_dev;
-    apply_batch(op, cfg, &p->plan);
+    apply_batch(ctx, op, cfg, &p->plan);
     choose_split(ctx, cfg, &p->plan);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), lay.total, cudaMemcpyHostToDevice, s);
@@ -781,8 +840,8 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
     p->load = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, ll, host.data() + ls.total, p->dev + ls.total);
     p->plan.status = p->load.status = ctx->status_dev;
-    apply_batch(KVX_OP_EXCHANGE, cfg, &p->plan);
-    apply_batch(KVX_OP_EXCHANGE, cfg, &p->load);
+    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &p->plan);
+    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &p->load);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), total, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
@@ -816,7 +875,7 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
         return KVX_ERR_INVALID_ARG;
     *out = nullptr;
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
+    kvx_status st = resolve_roundtrip_cfg(ctx, pool, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
     st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
@@ -837,13 +896,13 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     // allocation and pack again.
     p->plan = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_GATHER, lay, host.data(), host.data());
-    apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->plan);
-    if ((p->plan.total_items + p->plan.batch - 1) / p->plan.batch >= (int64_t(1) << 31)) {
+    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &p->plan);
+    if (roundtrip_units(p->plan, roundtrip_slices(cfg, p->plan)) >= (int64_t(1) << 31)) {
         delete p;
         return set_err(ctx, KVX_ERR_CAPACITY, "round trip of %lld segments (%d per unit) has "
                        "2^31 units or more", (long long)p->plan.total_items, p->plan.batch);
     }
-    p->sync_bytes = roundtrip_sync_bytes(p->plan);
+    p->sync_bytes = roundtrip_sync_bytes(cfg, p->plan);
     cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->dev), 2 * lay.total + p->sync_bytes);
     if (e != cudaSuccess) {
         delete p;
@@ -854,8 +913,8 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     p->load = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, lay, host.data() + lay.total, p->dev + lay.total);
     p->plan.status = p->load.status = ctx->status_dev;
-    apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->plan);
-    apply_batch(KVX_OP_ROUNDTRIP, cfg, &p->load);
+    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &p->plan);
+    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &p->load);
     // The unit count was checked above, so the setup cannot fail here.
     roundtrip_setup(ctx, cfg, p->plan, p->dev + 2 * lay.total, &p->rsync, &p->shape);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -718,6 +718,7 @@ struct RoundTripSync {
     unsigned int *done;  // [units]: 1 once the store unit's bytes are in host memory
     int64_t units;
     int unit_items;
+    int slices;          // > 1: unit u is row slice u % slices of item u / slices
     unsigned lag;        // loads handed out may trail stores handed out by this many units
     uint64_t wait_ns;    // limit of one wait for a store unit (about one second)
 };
@@ -792,15 +793,26 @@ __device__ __forceinline__ int next_unit(const RoundTripSync &sy, unsigned lag, 
 }
 
 // Items [first, first + count) of plan p, warp-collective (count is 1 unless BATCHED).
-// NC = false for bytes written earlier in the same launch.
+// With slices > 1 (not BATCHED), only rows [k r / slices, (k + 1) r / slices) of the one
+// item's r rows, k = slice.  NC = false for bytes written earlier in the same launch.
 template <int U, int DIR, int HINT, bool BATCHED, bool NC>
-__device__ __forceinline__ void copy_items(const Plan &p, int64_t first, int count, int lane)
+__device__ __forceinline__ void copy_items(const Plan &p, int64_t first, int count, int lane,
+                                           int slices = 1, int slice = 0)
 {
     const int64_t v = p.token_bytes;
     if (!BATCHED) {  // one item per unit
         Segment sg;
-        if (resolve_segment<DIR>(p, first, lane, sg))
-            copy_segment<U, HINT, NC>(sg, v, lane);
+        if (resolve_segment<DIR>(p, first, lane, sg)) {
+            if (slices > 1) {
+                const int r0 = int(int64_t(slice) * sg.rows / slices);
+                const int r1 = int(int64_t(slice + 1) * sg.rows / slices);
+                sg.src += int64_t(r0) * sg.s_pitch;
+                sg.dst += int64_t(r0) * sg.d_pitch;
+                sg.rows = r1 - r0;
+            }
+            if (sg.rows > 0)
+                copy_segment<U, HINT, NC>(sg, v, lane);
+        }
         return;
     }
     Segment sg;
@@ -844,16 +856,24 @@ __global__ void __launch_bounds__(1024, 1)
         if (what == kUnitSkip)
             continue;  // its store never finished: leave the unit alone
         __syncwarp();  // lane 0's acquire orders every lane's loads below
-        const int64_t first = int64_t(unit) * sy.unit_items;
-        const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
+        int64_t first;
+        int count, slice = 0;
+        if (sy.slices > 1) {  // a row slice of one long segment
+            first = unit / sy.slices;
+            slice = int(unit - first * sy.slices);
+            count = 1;
+        } else {
+            first = int64_t(unit) * sy.unit_items;
+            count = int(min(int64_t(sy.unit_items), ps.total_items - first));
+        }
         if (what == kUnitLoad) {
             // Short (batched) segments fill at most a few loads per lane: four are enough.
             copy_items<(BATCHED && U > 4 ? 4 : U), KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED,
-                       false>(pl, first, count, lane);
+                       false>(pl, first, count, lane, sy.slices, slice);
         } else {
             // HBM reads need fewer bytes in flight than host reads: four loads per lane.
             copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
-                ps, first, count, lane);
+                ps, first, count, lane, sy.slices, slice);
             // Each lane's host writes are performed at GPU scope, then lane 0 publishes the
             // unit with a release (the fence costs nothing measurable, and it keeps the
             // publication correct without leaning on the warp barrier's ordering).

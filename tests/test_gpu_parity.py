@@ -671,7 +671,8 @@ def test_roundtrip_wait_runs_out_and_reports(ctx, stream):
                                    stream.cuda_stream)
     stream.synchronize()
     elapsed = time.perf_counter() - t0
-    # 32 segments of 4 KiB in units of 8: four load units, one per warp, waiting together.
+    # 32 segments of 4 KiB in units of two (8 KiB): 16 load units, one per warp of the one
+    # CTA the launch needs, all waiting at once.
     assert 0.9 * wait_ns * 1e-9 <= elapsed < 1.0, elapsed
     assert kvx.kvx_get_status(ctx, stream.cuda_stream) == kvx.KVX_DEV_WAIT_TIMEOUT
     assert_bytes_equal(arena.numpy(), np.full(nbytes + 4096, CANARY, np.uint8),
@@ -1034,6 +1035,50 @@ def test_roundtrip_in_one_launch(ctx, stream, seed):
     oracle.store(pre, src.oracle(), oracle_chunks(specs, exp), lb, le)
     assert_bytes_equal(arena.numpy(), exp, f"seed {seed} round-trip chunks")
     oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp), lb, le)
+    assert_pool_equal(dpool, pre)
+    arena.close()
+
+
+@pytest.mark.parametrize("v,P,layout", [(1152, 64, 0), (1152, 64, 1), (1152, 64, 2),
+                                         (4096, 16, 0), (2048, 32, 1), (1152, 29, 2)])
+def test_roundtrip_long_segments_in_row_slices(ctx, stream, v, P, layout):
+    """Page segments longer than 32 KiB make the round trip's units row slices of one
+    segment (72 KiB: three slices; 64 KiB: two).  Partial last pages (one row, so some
+    slices are empty) and chunk cuts inside pages shorten segments; everything is compared
+    with the oracle's store and load."""
+    rng = np.random.default_rng(8100 + v + P + layout)
+    L, KV = 2, 2
+    lens = [700, 65, 1, 3 * P + 1]
+    pages = [-(-n // P) for n in lens]
+    NP = 2 * sum(pages) + 5
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(perm[at:at + npg])
+        t_dst.append(perm[sum(pages) + at:sum(pages) + at + npg])
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, 100, 0, L, layout)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape, align=wl.STRIPE_ALIGN)
+    nbytes = wl._arena_bytes(specs, shape)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(8101 + P)
+    pre = dpool.host_copy()
+    arena = Arena(nbytes, "host")
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                             kvx.chunks_array(specs, arena.ptr), stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    items, _, _, _ = kvx.kvx_last_launch(ctx)
+    segments = kvx.kvx_plan_count(dpool.pool, src.array, kvx.chunks_array(specs, arena.ptr))[0]
+    assert items == 2 * segments
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+    assert_bytes_equal(arena.numpy(), exp, "sliced round trip chunks")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
     assert_pool_equal(dpool, pre)
     arena.close()
 
