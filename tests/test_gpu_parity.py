@@ -1083,6 +1083,41 @@ def test_roundtrip_long_segments_in_row_slices(ctx, stream, v, P, layout):
     arena.close()
 
 
+@pytest.mark.parametrize("v,P,cfg_given,ctas", [(256, 16, False, 32), (256, 16, True, 16),
+                                                 (1024, 16, False, 16)])
+def test_roundtrip_default_grid_follows_segment_size(ctx, stream, v, P, cfg_given, ctas):
+    """With no configuration, a round trip of page segments shorter than 16 KiB runs on 32
+    SMs (one CTA each), longer ones on 16; an explicit configuration keeps its own SM cap.
+    The transfer is checked against the oracle either way."""
+    rng = np.random.default_rng(8300 + v + int(cfg_given))
+    L, KV, T = 4, 2, 4096
+    npg = T // P
+    NP = 2 * npg + 3
+    perm = rng.permutation(NP).astype(np.int32)
+    src, dst = Requests([perm[:npg]], [T]), Requests([perm[npg:2 * npg]], [T])
+    specs = wl.split_tokens(0, 0, T, 256, 0, L, wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(8301)
+    pre = dpool.host_copy()
+    arena = Arena(nbytes, "host")
+    c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_ROUNDTRIP) if cfg_given else None
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                             kvx.chunks_array(specs, arena.ptr), cfg=c,
+                             stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    assert kvx.kvx_last_launch(ctx)[1] == ctas
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+    assert_bytes_equal(arena.numpy(), exp, "round trip chunks")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
+    assert_pool_equal(dpool, pre)
+    arena.close()
+
+
 def test_roundtrip_many_requests_and_chunks(ctx, stream):
     """64 requests of mixed length cut into about 540 chunks of all three layouts: the
     round trip's unit search runs several probe levels deep."""
