@@ -58,7 +58,8 @@
 extern "C" {
 #endif
 
-#define KVX_VERSION 1
+/* ABI version: bumped whenever a struct's layout changes (2: kvx_launch_cfg.overlap). */
+#define KVX_VERSION 2
 
 /* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
 typedef struct CUstream_st *kvx_stream_t;
@@ -170,6 +171,14 @@ typedef struct kvx_launch_cfg {
                              one per lane (1..32); 0 = automatic (about 32 KiB of segments;
                              for page segments >= 16 KiB, 1 for host transfers and 2 for
                              the HBM transform; round trips: see kvx_roundtrip_chunks) */
+    int32_t overlap;      /* 1: the launch may start while the previous kernel on its stream
+                             is still running (programmatic dependent launch), so that its
+                             ramp overlaps that kernel's drain; it still completes after that
+                             kernel, so events recorded after it keep their meaning.  Use it
+                             only when this transfer touches no memory the previous kernel
+                             writes and writes none it reads (for example consecutive
+                             per-layer loads).  Store, load and transform with the
+                             warp-segment mapping; 0 elsewhere.  0 = off (default) */
 } kvx_launch_cfg;
 
 typedef struct kvx_ctx kvx_ctx;

@@ -117,6 +117,7 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
     c->mapping = KVX_MAP_WARP_SEGMENT;
     c->stage_bytes = kDefaultStageBytes;
     c->batch = 0;
+    c->overlap = 0;
     switch (op) {
     case KVX_OP_STORE:
         c->sm_cap = 16;
@@ -176,9 +177,14 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
     out->store_hint = user->store_hint;
     out->stage_bytes = user->stage_bytes ? user->stage_bytes : kDefaultStageBytes;
     out->batch = user->batch;
+    out->overlap = user->overlap;
     bool ok = out->sm_cap >= 0 && out->ctas_per_sm >= 1 && out->ctas_per_sm <= 32 &&
               out->batch >= 0 && out->batch <= 32 &&
               (out->store_hint == KVX_HINT_DEFAULT || out->store_hint == KVX_HINT_STREAMING);
+    // Overlapped launches: single transfers on the warp-segment mapping only.
+    if (out->overlap != 0)
+        ok = ok && out->overlap == 1 && out->mapping == KVX_MAP_WARP_SEGMENT &&
+             op >= KVX_OP_STORE && op <= KVX_OP_SCATTER_HBM;
     if (out->mapping == KVX_MAP_WARP_SEGMENT || out->mapping == KVX_MAP_CTA) {
         ok = ok && out->threads >= 32 && out->threads <= 1024 && out->threads % 32 == 0 &&
              pick_kernel(out->unroll, 0, 0);
@@ -196,9 +202,10 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
     if (!ok)
         return set_err(ctx, KVX_ERR_INVALID_ARG,
                        "launch cfg: sm_cap %d ctas_per_sm %d threads %d unroll %d hint %d "
-                       "mapping %d stage_bytes %d batch %d", user->sm_cap, user->ctas_per_sm,
-                       user->threads, user->unroll, user->store_hint, user->mapping,
-                       user->stage_bytes, user->batch);
+                       "mapping %d stage_bytes %d batch %d overlap %d (overlap: store, load "
+                       "and transform on the warp-segment mapping only)", user->sm_cap,
+                       user->ctas_per_sm, user->threads, user->unroll, user->store_hint,
+                       user->mapping, user->stage_bytes, user->batch, user->overlap);
     return KVX_OK;
 }
 
@@ -211,6 +218,7 @@ struct LaunchShape {
     int bulk = 0;
     int stage_bytes = 0;
     int stages = 0;
+    bool overlap = false;  // programmatic dependent launch (kvx_launch_cfg.overlap)
 };
 
 // Row slices per segment for a warp-segment launch of one segment per warp: when the batch
@@ -284,12 +292,15 @@ LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Pl
     } else if (cfg.mapping == KVX_MAP_CTA) {
         sh.fn = reinterpret_cast<const void *>(pick_cta(cfg.unroll, dir, cfg.store_hint));
         sh.threads = cfg.threads;
-    } else if (split) {
-        sh.fn = reinterpret_cast<const void *>(pick_split(cfg.unroll, dir, cfg.store_hint));
+    }
+    sh.overlap = cfg.overlap == 1 && cfg.mapping == KVX_MAP_WARP_SEGMENT;
+    if (cfg.mapping == KVX_MAP_WARP_SEGMENT && split) {
+        sh.fn = reinterpret_cast<const void *>(
+            pick_split(cfg.unroll, dir, cfg.store_hint, sh.overlap));
         sh.threads = cfg.threads;
-    } else {
-        sh.fn = reinterpret_cast<const void *>(pick_kernel(cfg.unroll, dir, cfg.store_hint,
-                                                           plan.batch, w32));
+    } else if (cfg.mapping == KVX_MAP_WARP_SEGMENT) {
+        sh.fn = reinterpret_cast<const void *>(
+            pick_kernel(cfg.unroll, dir, cfg.store_hint, plan.batch, w32, sh.overlap));
         sh.threads = cfg.threads;
     }
     return sh;
@@ -307,8 +318,22 @@ cudaError_t launch_kernel(const LaunchShape &sh, Plan plan, cudaStream_t s)
         return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(32u), args, sh.smem, s);
     }
     void *args[] = {&plan};
-    return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args, 0,
-                            s);
+    if (!sh.overlap)
+        return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args,
+                                0, s);
+    // May start once every CTA of the previous kernel on s has started; the kernel waits for
+    // that kernel's completion before it exits.
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(unsigned(sh.ctas));
+    lc.blockDim = dim3(unsigned(sh.threads));
+    lc.dynamicSmemBytes = 0;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelExC(&lc, sh.fn, args);
 }
 
 // Every call starts with an empty last-launch record, so a call that fails or moves
@@ -1317,7 +1342,7 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
     kvx_status st = resolve_cfg(nullptr, KVX_OP_LOAD, cfg, &c);
     if (st != KVX_OK)
         return st;
-    if (c.mapping != KVX_MAP_WARP_SEGMENT)
+    if (c.mapping != KVX_MAP_WARP_SEGMENT || c.overlap)
         return KVX_ERR_INVALID_ARG;
     st = kvx::validate(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, KVX_OP_LOAD,
                        1, false, nullptr, 0);

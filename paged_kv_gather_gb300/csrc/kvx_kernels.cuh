@@ -15,6 +15,7 @@
 //
 // Kernels: kvx_segment_kernel (store, load, HBM gather/scatter; the default mapping),
 // kvx_split_kernel (the same for batches with fewer segments than warps, in row slices),
+// their overlapped variants kvx_segment_overlap_kernel and kvx_split_overlap_kernel,
 // kvx_exchange_kernel and kvx_duplex_kernel (a store batch and a load batch in one launch),
 // kvx_roundtrip_kernel (store, then load the same chunks elsewhere, ordered per unit inside
 // the launch), and two alternative mappings of a single transfer: kvx_cta_kernel (a whole
@@ -350,12 +351,39 @@ __global__ void __launch_bounds__(1024, 1) kvx_segment_kernel(const Plan p)
     run_segments<U, DIR, HINT, BATCHED, W32>(p, warp, n_warps, lane);
 }
 
+// Programmatic dependent launch (kvx_launch_cfg.overlap).  An overlapped transfer kernel
+// lets the next kernel on its stream launch as soon as all its CTAs have started (when that
+// kernel is launched to overlap too), and before it exits waits until the kernel before it
+// on the stream has completed, so kernels on a stream still complete in order.  These
+// instructions live only in the overlapped kernels: their mere presence adds about a third
+// to the warp instructions of the copy loop (the durations are the same).
+__device__ __forceinline__ void allow_next_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_previous_grid()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <int U, int DIR, int HINT, bool BATCHED, bool W32 = false>
+__global__ void __launch_bounds__(1024, 1) kvx_segment_overlap_kernel(const Plan p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    allow_next_launch();
+    run_segments<U, DIR, HINT, BATCHED, W32>(p, warp, n_warps, lane);
+    wait_previous_grid();
+}
+
 // Few segments, many warps: each segment is cut into p.split slices of its rows, one warp
 // per slice, so a small transfer still puts the whole grid's bytes in flight.  Slice k of
 // a segment of r rows holds rows [k r / split, (k + 1) r / split); a slice may be empty
 // when a partial page has fewer rows than split.
 template <int U, int DIR, int HINT>
-__global__ void __launch_bounds__(1024, 1) kvx_split_kernel(const Plan p)
+__device__ __forceinline__ void split_segments(const Plan &p)
 {
     const int lane = threadIdx.x & 31;
     const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -376,6 +404,20 @@ __global__ void __launch_bounds__(1024, 1) kvx_split_kernel(const Plan p)
         sg.rows = r1 - r0;
         copy_segment<U, HINT>(sg, v, lane);
     }
+}
+
+template <int U, int DIR, int HINT>
+__global__ void __launch_bounds__(1024, 1) kvx_split_kernel(const Plan p)
+{
+    split_segments<U, DIR, HINT>(p);
+}
+
+template <int U, int DIR, int HINT>
+__global__ void __launch_bounds__(1024, 1) kvx_split_overlap_kernel(const Plan p)
+{
+    allow_next_launch();
+    split_segments<U, DIR, HINT>(p);
+    wait_previous_grid();
 }
 
 // Exchange: one launch moves a store batch (pages -> host chunks) and a load batch (host
@@ -971,58 +1013,73 @@ RoundTripFn pick_roundtrip(int unroll, bool batched)
 
 typedef void (*KernelFn)(Plan);
 
+template <int U, int DIR, int HINT, bool BATCHED, bool W32>
+KernelFn segment_fn(bool overlap)
+{
+    return overlap ? kvx_segment_overlap_kernel<U, DIR, HINT, BATCHED, W32>
+                   : kvx_segment_kernel<U, DIR, HINT, BATCHED, W32>;
+}
+
 template <int U, bool BATCHED, bool W32>
-KernelFn pick_hint_dir(int dir, int hint)
+KernelFn pick_hint_dir(int dir, int hint, bool overlap)
 {
     if (dir == KVX_DIR_GATHER)
         return hint == KVX_HINT_STREAMING
-                   ? kvx_segment_kernel<U, KVX_DIR_GATHER, 1, BATCHED, W32>
-                   : kvx_segment_kernel<U, KVX_DIR_GATHER, 0, BATCHED, W32>;
-    return hint == KVX_HINT_STREAMING ? kvx_segment_kernel<U, KVX_DIR_SCATTER, 1, BATCHED, W32>
-                                      : kvx_segment_kernel<U, KVX_DIR_SCATTER, 0, BATCHED, W32>;
+                   ? segment_fn<U, KVX_DIR_GATHER, 1, BATCHED, W32>(overlap)
+                   : segment_fn<U, KVX_DIR_GATHER, 0, BATCHED, W32>(overlap);
+    return hint == KVX_HINT_STREAMING ? segment_fn<U, KVX_DIR_SCATTER, 1, BATCHED, W32>(overlap)
+                                      : segment_fn<U, KVX_DIR_SCATTER, 0, BATCHED, W32>(overlap);
 }
 
 template <bool BATCHED, bool W32>
-KernelFn pick_unroll(int unroll, int dir, int hint)
+KernelFn pick_unroll(int unroll, int dir, int hint, bool overlap)
 {
     switch (unroll) {
-    case 1: return pick_hint_dir<1, BATCHED, W32>(dir, hint);
-    case 2: return pick_hint_dir<2, BATCHED, W32>(dir, hint);
-    case 4: return pick_hint_dir<4, BATCHED, W32>(dir, hint);
-    case 8: return pick_hint_dir<8, BATCHED, W32>(dir, hint);
+    case 1: return pick_hint_dir<1, BATCHED, W32>(dir, hint, overlap);
+    case 2: return pick_hint_dir<2, BATCHED, W32>(dir, hint, overlap);
+    case 4: return pick_hint_dir<4, BATCHED, W32>(dir, hint, overlap);
+    case 8: return pick_hint_dir<8, BATCHED, W32>(dir, hint, overlap);
     }
     return nullptr;
 }
 
 // The warp-segment kernel for (unroll, direction, hint), batched when more than one
-// segment is resolved per warp at once, with 32-byte accesses when w32.
-KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1, bool w32 = false)
+// segment is resolved per warp at once, with 32-byte accesses when w32, and the overlapped
+// variant when overlap.
+KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1, bool w32 = false,
+                     bool overlap = false)
 {
     if (w32)
-        return batch > 1 ? pick_unroll<true, true>(unroll, dir, hint)
-                         : pick_unroll<false, true>(unroll, dir, hint);
-    return batch > 1 ? pick_unroll<true, false>(unroll, dir, hint)
-                     : pick_unroll<false, false>(unroll, dir, hint);
+        return batch > 1 ? pick_unroll<true, true>(unroll, dir, hint, overlap)
+                         : pick_unroll<false, true>(unroll, dir, hint, overlap);
+    return batch > 1 ? pick_unroll<true, false>(unroll, dir, hint, overlap)
+                     : pick_unroll<false, false>(unroll, dir, hint, overlap);
+}
+
+template <int U, int DIR, int HINT>
+KernelFn split_fn(bool overlap)
+{
+    return overlap ? kvx_split_overlap_kernel<U, DIR, HINT> : kvx_split_kernel<U, DIR, HINT>;
 }
 
 template <int U>
-KernelFn pick_split_u(int dir, int hint)
+KernelFn pick_split_u(int dir, int hint, bool overlap)
 {
     if (dir == KVX_DIR_GATHER)
-        return hint == KVX_HINT_STREAMING ? kvx_split_kernel<U, KVX_DIR_GATHER, 1>
-                                          : kvx_split_kernel<U, KVX_DIR_GATHER, 0>;
-    return hint == KVX_HINT_STREAMING ? kvx_split_kernel<U, KVX_DIR_SCATTER, 1>
-                                      : kvx_split_kernel<U, KVX_DIR_SCATTER, 0>;
+        return hint == KVX_HINT_STREAMING ? split_fn<U, KVX_DIR_GATHER, 1>(overlap)
+                                          : split_fn<U, KVX_DIR_GATHER, 0>(overlap);
+    return hint == KVX_HINT_STREAMING ? split_fn<U, KVX_DIR_SCATTER, 1>(overlap)
+                                      : split_fn<U, KVX_DIR_SCATTER, 0>(overlap);
 }
 
-// The row-slice kernel for (unroll, direction, hint).
-KernelFn pick_split(int unroll, int dir, int hint)
+// The row-slice kernel for (unroll, direction, hint), overlapped when overlap.
+KernelFn pick_split(int unroll, int dir, int hint, bool overlap = false)
 {
     switch (unroll) {
-    case 1: return pick_split_u<1>(dir, hint);
-    case 2: return pick_split_u<2>(dir, hint);
-    case 4: return pick_split_u<4>(dir, hint);
-    case 8: return pick_split_u<8>(dir, hint);
+    case 1: return pick_split_u<1>(dir, hint, overlap);
+    case 2: return pick_split_u<2>(dir, hint, overlap);
+    case 4: return pick_split_u<4>(dir, hint, overlap);
+    case 8: return pick_split_u<8>(dir, hint, overlap);
     }
     return nullptr;
 }

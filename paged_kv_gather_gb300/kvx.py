@@ -90,7 +90,8 @@ class kvx_launch_cfg(ctypes.Structure):
     _fields_ = [("sm_cap", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("unroll", ctypes.c_int32),
                 ("store_hint", ctypes.c_int32), ("mapping", ctypes.c_int32),
-                ("stage_bytes", ctypes.c_int32), ("batch", ctypes.c_int32)]
+                ("stage_bytes", ctypes.c_int32), ("batch", ctypes.c_int32),
+                ("overlap", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_version_and_status_strings():
-    assert kvx.kvx_version() == 1
+    assert kvx.kvx_version() == 2
     seen = set()
     for st in range(9):
         s = kvx.kvx_status_string(st)
