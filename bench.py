@@ -1664,6 +1664,15 @@ def run_size_sweep(args, kvx, wl):
             plan = kvx.kvx_plan_create(ctx, op, pool, rq, part, 0, None, None, sh)
             row[f"{name}_plan_us"] = round(
                 _timed(stream, lambda: kvx.kvx_plan_launch(plan, sh), 10, 3) * 1e3, 2)
+            # The same plan, overlapped (programmatic dependent launch), launched back to back:
+            # the repeated transfer moves the same bytes, so each launch may overlap the last.
+            oc = kvx.kvx_default_launch_cfg(ctx, op)
+            oc.overlap = 1
+            oplan = kvx.kvx_plan_create(ctx, op, pool, rq, part, 0, None, oc, sh)
+            row[f"{name}_plan_overlap_back_to_back_us"] = round(
+                _timed(stream, lambda: [kvx.kvx_plan_launch(oplan, sh) for _ in range(reps)], 5,
+                       2) * 1e3 / reps, 2)
+            kvx.kvx_plan_destroy(oplan)
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 kvx.kvx_plan_launch(plan, torch.cuda.current_stream().cuda_stream)
