@@ -743,13 +743,14 @@ __global__ void __launch_bounds__(32) kvx_bulk_kernel(const Plan p, int stage_by
 //
 // Store a batch to host chunks and load the same chunks into other pages in one launch
 // (a swap-out followed by a swap-in elsewhere).  The store and load plans enumerate the
-// same items, so load unit u reads exactly the host bytes store unit u writes.  Units
-// (unit_items consecutive items) are handed out by two fetch-and-add counters, one per
-// direction.  A warp takes a store unit while the loads handed out are within `lag`
-// units (one per warp of the grid by default) of the stores handed out, and a load unit
-// otherwise, so each load usually starts well after its store finished.  A warp that holds a load
-// unit whose store has not been handed out yet hands out (and does) store units until it
-// has; only then does it wait for that store.  Every wait is therefore on a unit held by a
+// same items, so load unit u reads exactly the host bytes store unit u writes.  A unit is
+// unit_items consecutive items, or one row slice of a long item (slices > 1); units are
+// handed out by two fetch-and-add counters, one per direction.  A warp takes a store unit
+// while the loads handed out are within `lag` units (one per warp of the grid by default)
+// of the stores handed out, and a load unit otherwise, so each load usually starts well
+// after its store finished.  A warp that holds a load unit whose store has not been
+// handed out yet hands out (and does) store units until it has; only then does it wait
+// for that store.  Every wait is therefore on a unit held by a
 // running warp that waits on nothing, whatever the residency of the grid, so the waits
 // end; each is still bounded (about one second, then KVX_DEV_WAIT_TIMEOUT and the unit is
 // skipped).  Both directions of the host link run from the first completed store to the
