@@ -1601,11 +1601,19 @@ def run_roundtrip_sweep(args, kvx, wl):
                                                                  stream=sh), reps)
             assert kvx.kvx_get_status(ctx, sh) == 0
             items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
+            # The time model with the unit and SM cap the library picked (default link model).
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            unit, cap = kvx.kvx_roundtrip_unit(P, ms_.token_bytes, c, sms)
+            mc = c if c is not None else kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_ROUNDTRIP)
+            mc.sm_cap = cap
+            model_ms = kvx.kvx_estimate_pair_us(kvx.kvx_default_link_model(),
+                                                kvx.KVX_OP_ROUNDTRIP, Nm, Nm, unit, mc) * 1e-3
             _emit({"workload": "mla_roundtrip_one_launch", "page_size": P,
                    "chunk_bytes": 1 << 20, "cfg": c.as_dict() if c else "defaults",
                    "ctas": ctas, "threads": threads, "bytes_each_way": Nm,
-                   "segments_each_way": items // 2,
-                   "ms": round(ms, 4), "gbs": round(2 * Nm / (ms * 1e-3) / GB, 2)})
+                   "segments_each_way": items // 2, "unit_bytes": unit,
+                   "ms": round(ms, 4), "gbs": round(2 * Nm / (ms * 1e-3) / GB, 2),
+                   "model_ms": round(model_ms, 4)})
         mh.close()
         del mp
     kvx.kvx_destroy(ctx)

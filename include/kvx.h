@@ -490,6 +490,14 @@ kvx_status kvx_estimate_pair_us(const kvx_link_model *model, int op, int64_t sto
                                 int64_t load_bytes, int64_t unit_bytes,
                                 const kvx_launch_cfg *cfg, double *us);
 
+/* The unit and SM cap kvx_roundtrip_chunks uses for page segments of page_size tokens of
+ * token_bytes each, on a device of num_sms SMs, with cfg (NULL = no configuration given):
+ * unit_bytes = segments per unit x the segment, or the largest row slice when long segments
+ * are cut.  Pass them to kvx_estimate_pair_us (unit_bytes, and sm_cap in its cfg).  Host
+ * only; KVX_ERR_INVALID_ARG for non-positive sizes or an invalid SM cap or batch. */
+kvx_status kvx_roundtrip_unit(int32_t page_size, int64_t token_bytes, const kvx_launch_cfg *cfg,
+                              int32_t num_sms, int64_t *unit_bytes, int32_t *sm_cap);
+
 /* Layer-streamed prefill: layer l + 1's KV is loaded while layer l computes (as "Strata
  * Guide", section "The Loading-Bound Scheduling Dilemma and Delay Hits", and the
  * step list "Layer-Overlapped Prefill" describe).  With per-layer load time io_us and

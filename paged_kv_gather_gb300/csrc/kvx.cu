@@ -13,6 +13,7 @@
 
 #include "kvx_internal.h"
 #include "kvx_kernels.cuh"
+#include "kvx_rules.h"
 
 // --------------------------------------------------------------------------------- host
 
@@ -389,56 +390,15 @@ kvx_status resolve_pair_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kv
     return st;
 }
 
-// Round-trip units.  A load unit waits for its own store unit, and the grid's warps hold
-// one unit each at the start (stores only) and at the end (loads only), so smaller units
-// shorten that one-way fill and drain; but every unit also pays its hand-out, completion
-// and wait, which only enough warps hide.  Measured on the MLA latent (1152-byte tokens,
-// GB/s of both directions, 1.15 GB each way):
-//  - 1, 2 and 4 tokens per page: 340.3-340.7 in units of about kRoundTripUnitBytes on 32
-//    SMs, against 332.2-336.9 in 32 KiB units on 16 SMs; 8 KiB units on 16 SMs lose
-//    (285-330), so fewer SMs keep 32 KiB units;
-//  - 8 tokens per page (9 KiB segments, one per unit): 340.9 on 32 SMs in two runs, 333.2
-//    and 341.9 on 16;
-//  - 16 tokens and more (18 KiB segments and longer): 16 SMs is best (340.7 against 338.5).
-// Hence, with no configuration given, kRoundTripShortSms SMs for page segments shorter than
-// kRoundTripShortSegment.
-constexpr int64_t kRoundTripUnitBytes = 8192;
-constexpr int64_t kRoundTripShortSegment = 16384;
-constexpr int kRoundTripShortSms = 32;
-// Page segments longer than this travel as row slices of at most this size, one unit each,
-// for the same fill and drain reason (72 KiB segments: 334.7 GB/s whole).
-constexpr int64_t kRoundTripMaxUnitBytes = 32768;
-
 // Segments a warp resolves at once: the configured batch, else the packed default (about
 // 32 KiB of segments), with two long segments per warp for the HBM transform (their
-// lookups then overlap) and the round-trip units above.
-void apply_batch(const kvx_ctx *ctx, int op, const kvx_launch_cfg &cfg, Plan *plan)
+// lookups then overlap).  Round trips take theirs from kvx::roundtrip_rule.
+void apply_batch(int op, const kvx_launch_cfg &cfg, Plan *plan)
 {
-    if (cfg.batch > 0) {
+    if (cfg.batch > 0)
         plan->batch = cfg.batch;
-    } else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && plan->batch == 1) {
+    else if ((op == KVX_OP_GATHER_HBM || op == KVX_OP_SCATTER_HBM) && plan->batch == 1)
         plan->batch = 2;
-    } else if (op == KVX_OP_ROUNDTRIP) {
-        const int64_t seg = int64_t(plan->page_size) * plan->token_bytes;
-        const int sms = cfg.sm_cap > 0 ? cfg.sm_cap : ctx->num_sms;
-        if (seg >= kRoundTripUnitBytes)
-            plan->batch = 1;
-        else if (sms >= kRoundTripShortSms)
-            plan->batch = int32_t(std::min<int64_t>((kRoundTripUnitBytes + seg - 1) / seg, 32));
-    }
-}
-
-// Launch configuration of a round trip: as resolve_pair_cfg, and with no configuration
-// given, kRoundTripShortSms SMs for short page segments.
-kvx_status resolve_roundtrip_cfg(kvx_ctx *ctx, const kvx_pool *pool,
-                                 const kvx_launch_cfg *user, kvx_launch_cfg *cfg)
-{
-    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user, cfg);
-    if (st == KVX_OK && !user && pool && pool->page_size > 0 && pool->token_bytes > 0 &&
-        pool->token_bytes < kRoundTripShortSegment &&
-        int64_t(pool->page_size) * pool->token_bytes < kRoundTripShortSegment)
-        cfg->sm_cap = kRoundTripShortSms;
-    return st;
 }
 
 int op_dir(int op)
@@ -472,7 +432,7 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     Plan plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
                           slot->host, slot->dev);
     plan.status = ctx->status_dev;
-    apply_batch(ctx, op, cfg, &plan);
+    apply_batch(op, cfg, &plan);
     choose_split(ctx, cfg, &plan);
     if (plan.total_items == 0)
         return KVX_OK;
@@ -591,8 +551,8 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
     Plan pl = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, ll, slot->host + ls.total, slot->dev + ls.total);
     ps.status = pl.status = ctx->status_dev;
-    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &ps);
-    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &pl);
+    apply_batch(KVX_OP_EXCHANGE, cfg, &ps);
+    apply_batch(KVX_OP_EXCHANGE, cfg, &pl);
     if (ps.total_items + pl.total_items == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -623,18 +583,6 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
                        total);
 }
 
-// Row slices per round-trip unit: with one segment per unit by default, a page segment
-// longer than kRoundTripMaxUnitBytes is cut into slices of at most that (and at least one
-// row), each its own unit.  An explicit batch keeps whole segments.
-int roundtrip_slices(const kvx_launch_cfg &cfg, const Plan &ps)
-{
-    if (cfg.batch > 0 || ps.batch != 1)
-        return 1;
-    const int64_t seg = int64_t(ps.page_size) * ps.token_bytes;
-    const int64_t k = (seg + kRoundTripMaxUnitBytes - 1) / kRoundTripMaxUnitBytes;
-    return int(std::min<int64_t>(std::max<int64_t>(k, 1), ps.page_size));
-}
-
 int64_t roundtrip_units(const Plan &ps, int slices)
 {
     return slices > 1 ? ps.total_items * slices : (ps.total_items + ps.batch - 1) / ps.batch;
@@ -643,10 +591,10 @@ int64_t roundtrip_units(const Plan &ps, int slices)
 // Units, lag and grid of a round trip whose work counters and completion words start at
 // `sync` (sync_bytes(), zeroed before each launch).  False when the units do not fit the
 // kernel's 32-bit unit indices.
-bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, char *sync,
-                     RoundTripSync *sy, LaunchShape *sh)
+bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, int slices,
+                     char *sync, RoundTripSync *sy, LaunchShape *sh)
 {
-    sy->slices = roundtrip_slices(cfg, ps);
+    sy->slices = slices;
     sy->unit_items = sy->slices > 1 ? 1 : ps.batch;
     sy->units = roundtrip_units(ps, sy->slices);
     if (sy->units >= (int64_t(1) << 31))
@@ -667,9 +615,21 @@ bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &
     return true;
 }
 
-size_t roundtrip_sync_bytes(const kvx_launch_cfg &cfg, const Plan &ps)
+size_t roundtrip_sync_bytes(const Plan &ps, int slices)
 {
-    return 256 + sizeof(unsigned) * size_t(roundtrip_units(ps, roundtrip_slices(cfg, ps)));
+    return 256 + sizeof(unsigned) * size_t(roundtrip_units(ps, slices));
+}
+
+// The round trip's units and SM cap (kvx::roundtrip_rule) for a validated pool; sets the
+// SM cap in cfg and returns the rule.
+kvx::RoundTripRule roundtrip_rule_for(const kvx_ctx *ctx, const kvx_pool *pool,
+                                      const kvx_launch_cfg *user_cfg, kvx_launch_cfg *cfg)
+{
+    const kvx::RoundTripRule r = kvx::roundtrip_rule(pool->page_size, pool->token_bytes,
+                                                     user_cfg != nullptr, cfg->sm_cap,
+                                                     cfg->batch, ctx->num_sms);
+    cfg->sm_cap = r.sm_cap;
+    return r;
 }
 
 // sync_bytes > 0: zero the counters and completion words on `s` first (plans; calls zero
@@ -702,7 +662,7 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
         return KVX_ERR_INVALID_ARG;
     begin_call(ctx);
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_roundtrip_cfg(ctx, pool, user_cfg, &cfg);
+    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
     st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
@@ -710,6 +670,7 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
                                 ctx->err, sizeof ctx->err);
     if (st != KVX_OK)
         return st;
+    const kvx::RoundTripRule rule = roundtrip_rule_for(ctx, pool, user_cfg, &cfg);
     DeviceGuard guard(ctx->device);
     if (!guard.ok)
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
@@ -723,12 +684,11 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
     Plan pl = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, lay, slot->host + lay.total, slot->dev + lay.total);
     ps.status = pl.status = ctx->status_dev;
-    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &ps);
-    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &pl);
+    ps.batch = pl.batch = rule.batch;
     if (ps.total_items == 0)
         return KVX_OK;
     // The completion words (4 bytes per unit) are known only now that the plan is packed.
-    const size_t sync_bytes = roundtrip_sync_bytes(cfg, ps);
+    const size_t sync_bytes = roundtrip_sync_bytes(ps, rule.slices);
     if (sync_off + sync_bytes > ctx->slot_bytes)
         return set_err(ctx, KVX_ERR_CAPACITY,
                        "round trip of %lld segments needs %zu bytes of descriptors and "
@@ -736,7 +696,7 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
                        (long long)ps.total_items, sync_off + sync_bytes, ctx->slot_bytes);
     RoundTripSync sy;
     LaunchShape shape;
-    if (!roundtrip_setup(ctx, cfg, ps, slot->dev + sync_off, &sy, &shape))
+    if (!roundtrip_setup(ctx, cfg, ps, rule.slices, slot->dev + sync_off, &sy, &shape))
         return set_err(ctx, KVX_ERR_CAPACITY, "round trip of %lld segments (%d per unit) has "
                        "2^31 units or more", (long long)ps.total_items, ps.batch);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -809,7 +769,7 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
     p->plan = kvx::pack(pool, reqs, n_req, chunks, n_chunks, layer_begin, layer_end, dir, lay,
                         host.data(), p->dev);
     p->plan.status = ctx->status_dev;
-    apply_batch(ctx, op, cfg, &p->plan);
+    apply_batch(op, cfg, &p->plan);
     choose_split(ctx, cfg, &p->plan);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), lay.total, cudaMemcpyHostToDevice, s);
@@ -865,8 +825,8 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
     p->load = kvx::pack(pool, lreqs, n_lreq, lchunks, n_lchunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, ll, host.data() + ls.total, p->dev + ls.total);
     p->plan.status = p->load.status = ctx->status_dev;
-    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &p->plan);
-    apply_batch(ctx, KVX_OP_EXCHANGE, cfg, &p->load);
+    apply_batch(KVX_OP_EXCHANGE, cfg, &p->plan);
+    apply_batch(KVX_OP_EXCHANGE, cfg, &p->load);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), total, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
@@ -900,7 +860,7 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
         return KVX_ERR_INVALID_ARG;
     *out = nullptr;
     kvx_launch_cfg cfg;
-    kvx_status st = resolve_roundtrip_cfg(ctx, pool, user_cfg, &cfg);
+    kvx_status st = resolve_pair_cfg(ctx, KVX_OP_ROUNDTRIP, user_cfg, &cfg);
     if (st != KVX_OK)
         return st;
     st = kvx::validate_exchange(pool, src_reqs, n_req, chunks, n_chunks, dst_reqs, n_req, chunks,
@@ -908,6 +868,7 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
                                 ctx->err, sizeof ctx->err);
     if (st != KVX_OK)
         return st;
+    const kvx::RoundTripRule rule = roundtrip_rule_for(ctx, pool, user_cfg, &cfg);
     DeviceGuard guard(ctx->device);
     if (!guard.ok)
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
@@ -921,13 +882,13 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     // allocation and pack again.
     p->plan = kvx::pack(pool, src_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_GATHER, lay, host.data(), host.data());
-    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &p->plan);
-    if (roundtrip_units(p->plan, roundtrip_slices(cfg, p->plan)) >= (int64_t(1) << 31)) {
+    p->plan.batch = rule.batch;
+    if (roundtrip_units(p->plan, rule.slices) >= (int64_t(1) << 31)) {
         delete p;
         return set_err(ctx, KVX_ERR_CAPACITY, "round trip of %lld segments (%d per unit) has "
                        "2^31 units or more", (long long)p->plan.total_items, p->plan.batch);
     }
-    p->sync_bytes = roundtrip_sync_bytes(cfg, p->plan);
+    p->sync_bytes = roundtrip_sync_bytes(p->plan, rule.slices);
     cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->dev), 2 * lay.total + p->sync_bytes);
     if (e != cudaSuccess) {
         delete p;
@@ -938,10 +899,10 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     p->load = kvx::pack(pool, dst_reqs, n_req, chunks, n_chunks, layer_begin, layer_end,
                         KVX_DIR_SCATTER, lay, host.data() + lay.total, p->dev + lay.total);
     p->plan.status = p->load.status = ctx->status_dev;
-    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &p->plan);
-    apply_batch(ctx, KVX_OP_ROUNDTRIP, cfg, &p->load);
+    p->plan.batch = p->load.batch = rule.batch;
     // The unit count was checked above, so the setup cannot fail here.
-    roundtrip_setup(ctx, cfg, p->plan, p->dev + 2 * lay.total, &p->rsync, &p->shape);
+    roundtrip_setup(ctx, cfg, p->plan, rule.slices, p->dev + 2 * lay.total, &p->rsync,
+                    &p->shape);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), 2 * lay.total, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "kvx_internal.h"
+#include "kvx_rules.h"
 
 namespace kvx {
 namespace {
@@ -363,6 +364,53 @@ Plan pack(const kvx_pool *pool, const kvx_request *reqs, int n_req, const kvx_ch
     return p;
 }
 
+// Round-trip units.  A load unit waits for its own store unit, and the grid's warps hold
+// one unit each at the start (stores only) and at the end (loads only), so smaller units
+// shorten that one-way fill and drain; but every unit also pays its hand-out, completion
+// and wait, which only enough warps hide.  Measured on the MLA latent (1152-byte tokens,
+// GB/s of both directions, 1.15 GB each way):
+//  - 1, 2 and 4 tokens per page: 340.3-340.7 in units of about kRoundTripUnitBytes on 32
+//    SMs, against 332.2-336.9 in 32 KiB units on 16 SMs; 8 KiB units on 16 SMs lose
+//    (285-330), so fewer SMs keep 32 KiB units;
+//  - 8 tokens per page (9 KiB segments, one per unit): 340.9 on 32 SMs in two runs, 333.2
+//    and 341.9 on 16;
+//  - 16 tokens and more (18 KiB segments and longer): 16 SMs is best (340.7 against 338.5);
+//  - segments longer than kRoundTripMaxUnitBytes travel as row slices of at most that size
+//    (72 KiB segments: 340.0 in three slices, 330.7-334.7 whole).
+// Hence, with no configuration given, kRoundTripShortSms SMs for page segments shorter than
+// kRoundTripShortSegment.
+constexpr int64_t kRoundTripUnitBytes = 8192;
+constexpr int64_t kRoundTripShortSegment = 16384;
+constexpr int32_t kRoundTripShortSms = 32;
+constexpr int64_t kRoundTripMaxUnitBytes = 32768;
+
+RoundTripRule roundtrip_rule(int32_t page_size, int64_t token_bytes, bool user_cfg,
+                             int32_t sm_cap, int32_t batch, int num_sms)
+{
+    RoundTripRule r{1, 1, sm_cap};
+    if (page_size <= 0 || token_bytes <= 0)
+        return r;
+    const int64_t seg = token_bytes < kRoundTripMaxUnitBytes * 64
+                            ? int64_t(page_size) * token_bytes
+                            : kRoundTripMaxUnitBytes * 64;  // long enough for any rule
+    if (!user_cfg && seg < kRoundTripShortSegment)
+        r.sm_cap = kRoundTripShortSms;
+    const int sms = r.sm_cap > 0 ? r.sm_cap : num_sms;
+    if (batch > 0) {
+        r.batch = batch;
+    } else if (seg >= kRoundTripUnitBytes) {
+        r.batch = 1;
+        const int64_t k = (seg + kRoundTripMaxUnitBytes - 1) / kRoundTripMaxUnitBytes;
+        r.slices = int32_t(std::min<int64_t>(std::max<int64_t>(k, 1), page_size));
+    } else if (sms >= kRoundTripShortSms) {
+        r.batch = int32_t(std::min<int64_t>((kRoundTripUnitBytes + seg - 1) / seg, 32));
+    } else {
+        r.batch = default_batch(page_size, token_bytes);
+    }
+    return r;
+}
+
+
 }  // namespace kvx
 
 extern "C" {
@@ -482,6 +530,25 @@ kvx_status kvx_estimate_us(const kvx_link_model *m, int op, int64_t bytes,
     }
     const double gbs = op <= KVX_OP_LOAD ? (little_gbs < peak ? little_gbs : peak) : peak;
     *us = m->launch_us + (gbs > 0 ? moved / (gbs * 1e3) : 0.0);
+    return KVX_OK;
+}
+
+
+kvx_status kvx_roundtrip_unit(int32_t page_size, int64_t token_bytes, const kvx_launch_cfg *cfg,
+                              int32_t num_sms, int64_t *unit_bytes, int32_t *sm_cap)
+{
+    if (page_size <= 0 || token_bytes <= 0 || num_sms <= 0 || (cfg && cfg->sm_cap < 0) ||
+        (cfg && (cfg->batch < 0 || cfg->batch > 32)))
+        return KVX_ERR_INVALID_ARG;
+    const kvx::RoundTripRule r = kvx::roundtrip_rule(page_size, token_bytes, cfg != nullptr,
+                                                     cfg ? cfg->sm_cap : 16,
+                                                     cfg ? cfg->batch : 0, num_sms);
+    if (unit_bytes)
+        *unit_bytes = r.slices > 1
+                          ? (int64_t(page_size) + r.slices - 1) / r.slices * token_bytes
+                          : int64_t(r.batch) * page_size * token_bytes;
+    if (sm_cap)
+        *sm_cap = r.sm_cap;
     return KVX_OK;
 }
 

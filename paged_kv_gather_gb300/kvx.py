@@ -142,6 +142,9 @@ _proto("kvx_plan_create", _c.c_int, [_ctx_t, _c.c_int, *_batch, _P(kvx_launch_cf
 _proto("kvx_roundtrip_chunks", _c.c_int,
        [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int, _c.c_int,
         _c.c_int, _P(kvx_launch_cfg), _c.c_void_p])
+_proto("kvx_roundtrip_unit", _c.c_int,
+       [_c.c_int32, _c.c_int64, _P(kvx_launch_cfg), _c.c_int32, _P(_c.c_int64),
+        _P(_c.c_int32)])
 _proto("kvx_test_roundtrip_timeout", _c.c_int,
        [_ctx_t, _P(kvx_pool), _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int,
         _c.c_uint64, _c.c_void_p])
@@ -196,7 +199,8 @@ EXPORTED = ["kvx_create", "kvx_destroy", "kvx_set_validation", "kvx_default_laun
             "kvx_host_register", "kvx_host_unregister", "kvx_status_string", "kvx_version",
             "kvx_load_chunks_noalloc", "kvx_default_link_model", "kvx_estimate_us",
             "kvx_estimate_pair_us", "kvx_estimate_stream_us", "kvx_partition_create",
-            "kvx_partition_info", "kvx_partition_destroy", "kvx_test_roundtrip_timeout"]
+            "kvx_partition_info", "kvx_partition_destroy", "kvx_test_roundtrip_timeout",
+            "kvx_roundtrip_unit"]
 
 KVX_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -459,6 +463,17 @@ def kvx_plan_launch(plan, stream: int = 0) -> None:
 def kvx_plan_destroy(plan) -> None:
     """Wait for the device, then free a plan (before its context)."""
     _lib.kvx_plan_destroy(plan)
+
+
+def kvx_roundtrip_unit(page_size: int, token_bytes: int, cfg: Optional[kvx_launch_cfg] = None,
+                       num_sms: int = 152) -> Tuple[int, int]:
+    """(unit bytes, SM cap) kvx_roundtrip_chunks uses for these page segments (host only)."""
+    unit, sms = ctypes.c_int64(), ctypes.c_int32()
+    st = _lib.kvx_roundtrip_unit(page_size, token_bytes, _cfg_ptr(cfg), num_sms,
+                                 ctypes.byref(unit), ctypes.byref(sms))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_roundtrip_unit")
+    return unit.value, sms.value
 
 
 def kvx_test_roundtrip_timeout(ctx, pool: Pool, src_reqs, dst_reqs, chunks, wait_ns: int,

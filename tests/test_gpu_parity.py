@@ -1110,6 +1110,8 @@ def test_roundtrip_default_grid_follows_segment_size(ctx, stream, v, P, cfg_give
     stream.synchronize()
     assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
     assert kvx.kvx_last_launch(ctx)[1] == ctas
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert kvx.kvx_roundtrip_unit(P, v, c, sms)[1] == ctas  # the query the time model uses
     exp = np.full(nbytes + 4096, CANARY, np.uint8)
     oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
     assert_bytes_equal(arena.numpy(), exp, "round trip chunks")

@@ -366,3 +366,36 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             "m = u.module_from_spec(s); s.loader.exec_module(m)") % str(tmp_path / "kvx_copy.py")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
     assert r.returncode != 0 and "is missing" in r.stderr, r.stderr[-500:]
+
+
+def test_roundtrip_unit_follows_segment_size():
+    """kvx_roundtrip_unit reports the round trip's own unit rule: about 8 KiB units on 32 SMs
+    for segments under 8 KiB, one segment per unit up to 32 KiB (32 SMs under 16 KiB), row
+    slices of at most 32 KiB beyond; an explicit configuration keeps its SM cap, and its
+    batch if it gives one."""
+    u = kvx.kvx_roundtrip_unit
+    assert u(1, 1152) == (8 * 1152, 32)       # 8 one-token segments per unit
+    assert u(2, 1152) == (4 * 2304, 32)
+    assert u(4, 1152) == (2 * 4608, 32)
+    assert u(8, 1152) == (9216, 32)            # one 9 KiB segment, still short: 32 SMs
+    assert u(16, 1152) == (18432, 16)          # 18 KiB: one per unit on 16 SMs
+    assert u(16, 2048) == (32768, 16)          # llama8b pages
+    assert u(32, 1152) == (16 * 1152, 16)      # 36 KiB: two slices of 16 rows
+    assert u(64, 1152) == (22 * 1152, 16)      # 72 KiB: three slices of at most 22 rows
+    assert u(4, 65536) == (65536, 16)          # rows longer than 32 KiB: one row per slice
+    c = kvx.kvx_launch_cfg()
+    c.sm_cap, c.ctas_per_sm, c.threads, c.unroll = 16, 1, 1024, 8
+    assert u(16, 256, c) == (8 * 4096, 16)     # given 16 SMs: the 32 KiB units of one-way
+    assert u(1, 1152, c) == (29 * 1152, 16)
+    c.batch = 3
+    assert u(16, 256, c) == (3 * 4096, 16)
+    assert u(64, 1152, c) == (3 * 73728, 16)   # an explicit batch keeps whole segments
+    c.batch, c.sm_cap = 0, 0                   # every SM
+    assert u(1, 1152, c, num_sms=152) == (8 * 1152, 0)
+    assert u(1, 1152, c, num_sms=16) == (29 * 1152, 0)
+    for bad in [(0, 1152), (16, 0), (-1, 64)]:
+        with pytest.raises(kvx.KvxError):
+            u(*bad)
+    with pytest.raises(kvx.KvxError):
+        u(16, 1152, None, 0)
+
