@@ -483,7 +483,8 @@ kvx_status kvx_estimate_us(const kvx_link_model *model, int op, int64_t bytes,
  * on the launch's bytes in flight (as in kvx_estimate_us):
  *   t = launch_us + max(store / d2h, load / h2d, (store + load) / min(bidir, in_flight / L))
  * A round trip (store_bytes = load_bytes) first stores, and last loads, one unit of
- * unit_bytes per warp of its grid on its own at the one-way rates (its fill and drain):
+ * unit_bytes per warp of its grid on its own at the one-way rates (its fill and drain;
+ * kvx_roundtrip_unit gives the unit and SM cap kvx_roundtrip_chunks uses):
  *   t = launch_us + F / d2h + (2 x bytes - 2 F) / min(bidir, ...) + F / h2d,
  *   F = min(bytes, warps x unit_bytes). */
 kvx_status kvx_estimate_pair_us(const kvx_link_model *model, int op, int64_t store_bytes,
