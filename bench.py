@@ -654,6 +654,8 @@ def run_ours(args):
     transform = {
         "gather_ms": round(g_ms, 4), "scatter_ms": round(s_ms, 4),
         "gather_gbs_2n": round(tr_gbs["gather"], 1), "scatter_gbs_2n": round(tr_gbs["scatter"], 1),
+        "gather_gbs_n": round(tr_gbs["gather"] / 2, 1),  # payload N / t, one way
+        "scatter_gbs_n": round(tr_gbs["scatter"] / 2, 1),
         "roofline": {"bound": "hbm", "achieved": round(tr_gbs[dom_tr], 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(tr_gbs[dom_tr] / hbm_peak, 4),
                      "traffic": recorded_traffic(f"transform_{dom_tr}", "llama8b"),
