@@ -4,6 +4,7 @@
  * (validation, work counts, chunk policy, time model), one "name value" pair per line,
  * for tests/test_c_abi.py to compare with the Python binding and the closed forms.
  */
+#include <stddef.h>
 #include <stdint.h>
 #include <stdio.h>
 
@@ -35,6 +36,22 @@ int main(void)
     printf("sizeof_cfg %zu\n", sizeof(kvx_launch_cfg));
     printf("sizeof_link_model %zu\n", sizeof(kvx_link_model));
     printf("version %d\n", kvx_version());
+#define OFF(type, field) printf("off_%s_%s %zu\n", #type, #field, offsetof(type, field))
+    OFF(kvx_pool, num_layers); OFF(kvx_pool, kv_factor); OFF(kvx_pool, page_size);
+    OFF(kvx_pool, num_pages); OFF(kvx_pool, token_bytes); OFF(kvx_pool, k_pages);
+    OFF(kvx_pool, v_pages);
+    OFF(kvx_request, page_table); OFF(kvx_request, page_table_host);
+    OFF(kvx_request, n_tokens); OFF(kvx_request, reserved);
+    OFF(kvx_chunk, request); OFF(kvx_chunk, token_begin); OFF(kvx_chunk, n_tokens);
+    OFF(kvx_chunk, layer_begin); OFF(kvx_chunk, n_layers); OFF(kvx_chunk, layout);
+    OFF(kvx_chunk, ptr);
+    OFF(kvx_launch_cfg, sm_cap); OFF(kvx_launch_cfg, ctas_per_sm); OFF(kvx_launch_cfg, threads);
+    OFF(kvx_launch_cfg, unroll); OFF(kvx_launch_cfg, store_hint); OFF(kvx_launch_cfg, mapping);
+    OFF(kvx_launch_cfg, stage_bytes); OFF(kvx_launch_cfg, batch); OFF(kvx_launch_cfg, overlap);
+    OFF(kvx_link_model, h2d_gbs); OFF(kvx_link_model, d2h_gbs); OFF(kvx_link_model, hbm_gbs);
+    OFF(kvx_link_model, bidir_gbs); OFF(kvx_link_model, latency_us);
+    OFF(kvx_link_model, launch_us); OFF(kvx_link_model, num_sms); OFF(kvx_link_model, reserved);
+#undef OFF
 
     char msg[256];
     printf("validate_ok %d\n",

@@ -38,6 +38,19 @@ def test_struct_sizes_match_the_binding(abi_values):
     assert int(abi_values["version"]) == kvx.kvx_version()
 
 
+def test_field_offsets_match_the_binding(abi_values):
+    """Every field of every ABI struct sits where the binding puts it (sizes alone would not
+    catch two swapped fields of the same size)."""
+    offs = {k[len("off_"):]: int(v) for k, v in abi_values.items() if k.startswith("off_")}
+    for struct in (kvx.kvx_pool, kvx.kvx_launch_cfg, kvx.kvx_link_model):
+        for name, _ in struct._fields_:
+            assert offs.pop(f"{struct.__name__}_{name}") == getattr(struct, name).offset, name
+    for cname, dtype in (("kvx_request", kvx.REQUEST_DTYPE), ("kvx_chunk", kvx.CHUNK_DTYPE)):
+        for name in dtype.names:
+            assert offs.pop(f"{cname}_{name}") == dtype.fields[name][1], name
+    assert not offs, f"fields the binding does not have: {sorted(offs)}"
+
+
 def test_host_entry_points_from_c(abi_values):
     assert int(abi_values["validate_ok"]) == kvx.KVX_OK
     assert int(abi_values["validate_misaligned"]) == kvx.KVX_ERR_ALIGNMENT
