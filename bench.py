@@ -97,6 +97,15 @@ def parse():
     p.add_argument("--chunk-tokens", type=int, default=256,
                    help="tokens per per-layer chunk of --workload llama70b (256 = 1 MiB, the "
                         "closed form; 512 = 2 MiB)")
+    p.add_argument("--mapping", default="segment", choices=["segment", "bulk"],
+                   help="llama70b: mapping of the per-layer loads")
+    p.add_argument("--stages", type=int, default=0, help="bulk mapping: stages per ring")
+    p.add_argument("--stage-bytes", type=int, default=0, help="bulk mapping: bytes per stage")
+    p.add_argument("--layers", type=int, default=80, help="llama70b: layers streamed")
+    p.add_argument("--priorities", default="-1,0",
+                   help="llama70b: load stream priorities (-1 high, 0 normal)")
+    p.add_argument("--partition-sms", default="8,16",
+                   help="llama70b: I/O partition sizes (green contexts) to run; empty: none")
     p.add_argument("--sm-caps", default="1,2,4,8,16,32,0",
                    help="SM caps of the llama70b overlap sweep (0 = all SMs)")
     return p.parse_args()
@@ -803,10 +812,84 @@ def _emit(d):
     print(json.dumps(d), flush=True)
 
 
-def run_llama70b(args, kvx, wl):
-    """Layer-streamed load of a 65536-token prefix (80 layers, 256 MiB per layer) while a
-    bf16 8192^3 GEMM per layer runs on a second stream; SM-cap sweep."""
-    w = wl.llama70b(tokens_per_chunk=args.chunk_tokens)
+def io_cfg(kvx, ctx, op, cap, mapping="segment", stages=0, stage_bytes=0):
+    """Launch configuration of a store or load: the default register mapping, or the bulk
+    mapping (two bulk-copy rings per CTA) with `stages` stages of `stage_bytes` each."""
+    c = kvx.kvx_default_launch_cfg(ctx, op)
+    c.sm_cap = cap
+    if mapping == "bulk":
+        c.mapping, c.threads = kvx.KVX_MAP_BULK, 0
+        c.unroll, c.stage_bytes = stages, stage_bytes
+    return c
+
+
+def layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes, cfg, io_stream,
+                    gemm_stream, gemm, gemm_alone_ms, reps=2):
+    """Per-layer loads on io_stream; GEMM(l) on gemm_stream once load(l) is done (an event).
+    Returns load GB/s alone and overlapped, the GEMM's mean time beside the loads against
+    gemm_alone_ms, end to end, and the I/O-time model's prediction for the same launches."""
+    io_h = io_stream.cuda_stream
+
+    def load_all():
+        for l in range(n_layers):
+            kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, io_h)
+
+    total = layer_bytes * n_layers
+    alone_ms = _timed(io_stream, load_all, 3, warm=1)
+    spans, e2es, gms = [], [], []
+    for rep in range(reps):
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(io_stream)
+        gemm_stream.wait_event(start)
+        gt = EventTimer(gemm_stream)
+        for l in range(n_layers):
+            kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, io_h)
+            ev = torch.cuda.Event()
+            ev.record(io_stream)
+            gemm_stream.wait_event(ev)
+            with torch.cuda.stream(gemm_stream):
+                e = gt.start()
+                gemm()
+                gt.stop(e)
+        end_a = torch.cuda.Event(enable_timing=True)
+        end_a.record(io_stream)
+        end_b = torch.cuda.Event(enable_timing=True)
+        end_b.record(gemm_stream)
+        torch.cuda.synchronize()
+        spans.append(start.elapsed_time(end_a))
+        e2es.append(start.elapsed_time(end_b))
+        gms.append(statistics.mean(gt.ms()))
+    assert kvx.kvx_get_status(ctx, io_h) == 0
+    g_ms = statistics.median(gms)
+    model = kvx.kvx_default_link_model()
+    pred_io = kvx.kvx_estimate_us(model, kvx.KVX_OP_LOAD, layer_bytes, cfg)
+    pred_e2e, pred_bubble = kvx.kvx_estimate_stream_us(pred_io, gemm_alone_ms * 1e3, n_layers)
+    # The same model fed with this run's own per-layer load time (alone) and GEMM time.
+    meas_e2e, _ = kvx.kvx_estimate_stream_us(alone_ms * 1e3 / n_layers, gemm_alone_ms * 1e3,
+                                             n_layers)
+    e2e = statistics.median(e2es)
+    return {"layers": n_layers, "layer_bytes": layer_bytes,
+            "load_cfg": cfg.as_dict(),
+            "load_alone_ms": round(alone_ms, 3),
+            "load_alone_gbs": round(total / (alone_ms * 1e-3) / GB, 2),
+            "load_overlap_span_ms": round(statistics.median(spans), 3),
+            "load_overlap_gbs": round(total / (statistics.median(spans) * 1e-3) / GB, 2),
+            "gemm_alone_ms": round(gemm_alone_ms, 4), "gemm_overlap_ms": round(g_ms, 4),
+            "gemm_slowdown_pct": round(100 * (g_ms / gemm_alone_ms - 1), 2),
+            "e2e_ms": round(e2e, 3),
+            "serial_ms": round(alone_ms + n_layers * gemm_alone_ms, 3),
+            "model_e2e_ms": round(pred_e2e * 1e-3, 3),
+            "model_bubble_ms": round(pred_bubble * 1e-3, 3),
+            "e2e_vs_model": round(e2e / (pred_e2e * 1e-3), 4),
+            "model_from_measured_e2e_ms": round(meas_e2e * 1e-3, 3),
+            "e2e_vs_model_from_measured": round(e2e / (meas_e2e * 1e-3), 4)}
+
+
+def llama70b_setup(kvx, wl, n_layers, chunk_tokens=256):
+    """Pool, page table, host arena and per-layer chunk arrays of the Llama-3.1-70B-shaped
+    prefix, for its first n_layers layers (80 = the whole model)."""
+    w = wl.llama70b(tokens_per_chunk=chunk_tokens, num_layers=n_layers)
     s = w.shape
     pools = _pool_tensor(s, w.seed, wl)
     pool = kvx.Pool.from_tensor(pools, s.page_size)
@@ -817,13 +900,28 @@ def run_llama70b(args, kvx, wl):
     _fill_host(arena.array, w.load_arena_bytes, s, w.seed, 1, wl)
     per_layer = [kvx.chunks_array([c for c in w.load_chunks if c.layer_begin == l], arena.ptr)
                  for l in range(s.num_layers)]
-    ctx = kvx.kvx_create(0)
-    sb = torch.cuda.Stream()
+    return w, pools, pool, pt, reqs, arena, per_layer
+
+
+def gemm_operands(seed):
     g = torch.Generator(device="cuda")
-    g.manual_seed(w.seed)
+    g.manual_seed(seed)
     A = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16, generator=g)
     B = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16, generator=g)
     C = torch.empty(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    return A, B, C
+
+
+def run_llama70b(args, kvx, wl):
+    """Layer-streamed load of a 65536-token prefix (80 layers, 256 MiB per layer) while a
+    bf16 8192^3 GEMM per layer runs on a second stream: SM caps and stream priorities for the
+    chosen mapping (--mapping segment|bulk), then hard SM partitions (green contexts)."""
+    w, pools, pool, pt, reqs, arena, per_layer = llama70b_setup(kvx, wl, args.layers,
+                                                               args.chunk_tokens)
+    s = w.shape
+    ctx = kvx.kvx_create(0)
+    sb = torch.cuda.Stream()
+    A, B, C = gemm_operands(w.seed)
     layer_bytes = w.load_bytes() // s.num_layers
 
     def gemm():
@@ -832,63 +930,20 @@ def run_llama70b(args, kvx, wl):
     with torch.cuda.stream(sb):
         gemm_ms = _timed(sb, gemm, 20, warm=5)
     caps = [int(x) for x in args.sm_caps.split(",")]
-    for cap, prio in [(c, p) for p in (-1, 0) for c in caps]:
+    prios = [int(x) for x in args.priorities.split(",")]
+    for cap, prio in [(c, p) for p in prios for c in caps]:
         # Loads on a high-priority stream (-1) get SMs as soon as GEMM CTAs retire.
         sa = torch.cuda.Stream(priority=prio)
-        cfg = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD)
-        cfg.sm_cap = cap
-
-        def load_all():
-            for l in range(s.num_layers):
-                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, sa.cuda_stream)
-
-        alone_ms = _timed(sa, load_all, 3, warm=1)
-        # Overlapped: load(l) on stream A; GEMM(l) on stream B after load(l) is done.
-        for rep in range(2):
-            torch.cuda.synchronize()
-            start = torch.cuda.Event(enable_timing=True)
-            start.record(sa)
-            sb.wait_event(start)
-            gt = EventTimer(sb)
-            for l in range(s.num_layers):
-                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, sa.cuda_stream)
-                ev = torch.cuda.Event()
-                ev.record(sa)
-                sb.wait_event(ev)
-                with torch.cuda.stream(sb):
-                    e = gt.start()
-                    gemm()
-                    gt.stop(e)
-            end_a = torch.cuda.Event(enable_timing=True)
-            end_a.record(sa)
-            end_b = torch.cuda.Event(enable_timing=True)
-            end_b.record(sb)
-            torch.cuda.synchronize()
-        assert kvx.kvx_get_status(ctx, sa.cuda_stream) == 0
-        load_span = start.elapsed_time(end_a)
-        e2e = start.elapsed_time(end_b)
-        g_ms = statistics.mean(gt.ms())
-        model = kvx.kvx_default_link_model()
-        pred_io = kvx.kvx_estimate_us(model, kvx.KVX_OP_LOAD, layer_bytes, cfg)
-        pred_e2e, pred_bubble = kvx.kvx_estimate_stream_us(pred_io, gemm_ms * 1e3, s.num_layers)
+        cfg = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, cap, args.mapping, args.stages,
+                     args.stage_bytes)
+        r = layer_streaming(kvx, ctx, pool, reqs, per_layer, s.num_layers, layer_bytes, cfg,
+                            sa, sb, gemm, gemm_ms)
         _emit({"workload": "llama70b_layer_streaming", "chunk_tokens": args.chunk_tokens,
-               "sm_cap": cap,
-               "load_stream_priority": "high" if prio < 0 else "normal",
-               "model_e2e_ms": round(pred_e2e * 1e-3, 3),
-               "model_bubble_ms": round(pred_bubble * 1e-3, 3),
-               "load_cfg": cfg.as_dict(),
-               "load_alone_ms": round(alone_ms, 3),
-               "load_alone_gbs": round(w.load_bytes() / (alone_ms * 1e-3) / GB, 2),
-               "load_overlap_span_ms": round(load_span, 3),
-               "load_overlap_gbs": round(w.load_bytes() / (load_span * 1e-3) / GB, 2),
-               "gemm_alone_ms": round(gemm_ms, 4), "gemm_overlap_ms": round(g_ms, 4),
-               "gemm_slowdown_pct": round(100 * (g_ms / gemm_ms - 1), 2),
-               "e2e_ms": round(e2e, 3),
-               "serial_ms": round(alone_ms + s.num_layers * gemm_ms, 3),
-               "layer_bytes": layer_bytes})
+               "mapping": args.mapping, "sm_cap": cap,
+               "load_stream_priority": "high" if prio < 0 else "normal", **r})
     # Hard SM partitions (green contexts): the loads on an I/O partition, the GEMM on the
     # rest of the GPU.
-    for io_sms in (8, 16):
+    for io_sms in [int(x) for x in args.partition_sms.split(",") if x]:
         try:
             part = kvx.kvx_partition_create(0, io_sms, -1, 0)
         except kvx.KvxError as e:
@@ -897,56 +952,19 @@ def run_llama70b(args, kvx, wl):
             break
         sa = torch.cuda.ExternalStream(part.io_stream)
         sc = torch.cuda.ExternalStream(part.compute_stream)
-        cfg = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD)
-        cfg.sm_cap = 0  # the partition bounds the SMs
+        cfg = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, 0, args.mapping, args.stages, args.stage_bytes)
 
         def gemm_c():
             with torch.cuda.stream(sc):
                 torch.matmul(A, B, out=C)
 
         g_part = _timed(sc, gemm_c, 20, warm=5)
-
-        def load_all():
-            for l in range(s.num_layers):
-                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, part.io_stream)
-
-        alone_ms = _timed(sa, load_all, 3, warm=1)
-        for rep in range(2):
-            torch.cuda.synchronize()
-            start = torch.cuda.Event(enable_timing=True)
-            start.record(sa)
-            sc.wait_event(start)
-            gt = EventTimer(sc)
-            for l in range(s.num_layers):
-                kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, part.io_stream)
-                ev = torch.cuda.Event()
-                ev.record(sa)
-                sc.wait_event(ev)
-                with torch.cuda.stream(sc):
-                    e = gt.start()
-                    torch.matmul(A, B, out=C)
-                    gt.stop(e)
-            end_a = torch.cuda.Event(enable_timing=True)
-            end_a.record(sa)
-            end_b = torch.cuda.Event(enable_timing=True)
-            end_b.record(sc)
-            torch.cuda.synchronize()
-        assert kvx.kvx_get_status(ctx, part.io_stream) == 0
-        g_ms = statistics.mean(gt.ms())
-        load_span = start.elapsed_time(end_a)
+        r = layer_streaming(kvx, ctx, pool, reqs, per_layer, s.num_layers, layer_bytes, cfg,
+                            sa, sc, gemm, gemm_ms)
         _emit({"workload": "llama70b_layer_streaming", "chunk_tokens": args.chunk_tokens,
-               "partition": "green contexts",
+               "mapping": args.mapping, "partition": "green contexts",
                "io_sms": part.io_sms, "compute_sms": part.compute_sms,
-               "load_alone_ms": round(alone_ms, 3),
-               "load_alone_gbs": round(w.load_bytes() / (alone_ms * 1e-3) / GB, 2),
-               "load_overlap_span_ms": round(load_span, 3),
-               "load_overlap_gbs": round(w.load_bytes() / (load_span * 1e-3) / GB, 2),
-               "gemm_alone_ms": round(gemm_ms, 4),
-               "gemm_on_compute_partition_ms": round(g_part, 4),
-               "gemm_overlap_ms": round(g_ms, 4),
-               "gemm_slowdown_pct": round(100 * (g_ms / gemm_ms - 1), 2),
-               "e2e_ms": round(start.elapsed_time(end_b), 3),
-               "serial_ms": round(alone_ms + s.num_layers * gemm_ms, 3)})
+               "gemm_on_compute_partition_ms": round(g_part, 4), **r})
         torch.cuda.synchronize()
         part.close()
     arena.close()
@@ -1114,8 +1132,9 @@ def run_sm_sweep(args, kvx, wl):
     sh = stream.cuda_stream
     N = w.store_bytes()
     shapes = [("segment", 1024, 8, 1, 0), ("segment", 512, 8, 1, 0),
-              ("bulk", 32, 6, 1, 32768), ("bulk", 32, 3, 2, 32768), ("bulk", 32, 4, 1, 49152)]
-    for cap in (1, 2, 4, 8, 12, 16, 32, 0):
+              ("bulk", 96, 3, 1, 32768), ("bulk", 96, 2, 1, 49152), ("bulk", 96, 6, 1, 16384),
+              ("bulk", 96, 2, 1, 32768)]
+    for cap in [int(x) for x in args.sm_caps.split(",")]:
         for mapping, threads, unroll, ctas, stage in shapes:
             row = {"workload": "llama8b_sm_sweep", "sm_cap": cap, "mapping": mapping,
                    "threads": threads, "unroll": unroll, "ctas_per_sm": ctas,

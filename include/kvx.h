@@ -139,10 +139,14 @@ typedef struct kvx_chunk {
 #define KVX_MAP_WARP_SEGMENT 0  /* one warp per (chunk, layer, kv, page) segment; lanes move
                                    16-byte units through registers (32-byte units for an
                                    HBM transform on 32-byte-aligned memory) */
-#define KVX_MAP_BULK 1          /* one warp per CTA streams segments through a ring of
+#define KVX_MAP_BULK 1          /* three warps per CTA: one resolves segments 32 at a
+                                   time, and one lane of each of the other two streams
+                                   alternate batches of them through its own ring of
                                    shared-memory stages with bulk async copies
                                    (cp.async.bulk, mbarrier completion); `unroll` is the
-                                   number of stages (2..8), `stage_bytes` their size */
+                                   number of stages per ring (2..8), `stage_bytes` their
+                                   size.  Loads reach the host link's peak on the fewest
+                                   SMs (4 on GB300) */
 #define KVX_MAP_CTA 2           /* all threads of a CTA move one segment together (thread t
                                    takes units t, t + threads, ...), 32 segments resolved
                                    per batch by one warp; store, load and transform only */
@@ -157,16 +161,16 @@ typedef struct kvx_launch_cfg {
                              sm_cap SMs.  0 = every SM */
     int32_t ctas_per_sm;  /* 0 = the operation's default */
     int32_t threads;      /* threads per CTA, multiple of 32 in [32, 1024]; 0 = default
-                             (the bulk mapping always runs one warp per CTA) */
+                             (the bulk mapping always runs three warps per CTA) */
     int32_t unroll;       /* warp-segment and CTA mappings: 16-byte loads in flight per
                              thread before its stores (1, 2, 4 or 8; where
                              kvx_transform_hbm moves 32-byte units, max(unroll / 2, 1)
-                             32-byte loads); bulk mapping: shared-memory stages (2..8).
-                             0 = default */
+                             32-byte loads); bulk mapping: shared-memory stages of each of
+                             its two rings (2..8).  0 = default (bulk: 3) */
     int32_t store_hint;   /* KVX_HINT_* (warp-segment and CTA mappings) */
     int32_t mapping;      /* KVX_MAP_* */
     int32_t stage_bytes;  /* bulk mapping: bytes per shared-memory stage, a multiple of 16;
-                             stages x stage_bytes <= 220 KiB.  0 = default (32 KiB) */
+                             2 x stages x stage_bytes <= 208 KiB.  0 = default (32 KiB) */
     int32_t batch;        /* warp-segment mapping: page segments a warp resolves at once,
                              one per lane (1..32); 0 = automatic (about 32 KiB of segments;
                              for page segments >= 16 KiB, 1 for host transfers and 2 for
@@ -469,9 +473,10 @@ kvx_status kvx_default_link_model(kvx_link_model *model);
  * mapping moving `bytes` in each direction with launch configuration cfg (NULL = the
  * operation's defaults).  Little's law, as "Strata Guide: Hierarchical Context Caching for
  * Long LLMs", section "The Physics of I/O Bandwidth and Little's Law", states it
- * (X = C * S / L): each CTA keeps threads x unroll 16-byte units in flight, so the
- * CTAs sustain ctas x threads x unroll x 16 / latency, capped by the link's peak in that
- * direction; the HBM transform is capped by the HBM peak (2 x bytes of traffic).
+ * (X = C * S / L): each CTA keeps threads x unroll 16-byte units in flight (the bulk
+ * mapping: 2 x (unroll - 1) x stage_bytes, the loading stages of its two rings), so the
+ * CTAs sustain ctas x that / latency, capped by the link's peak in that direction; the HBM
+ * transform is capped by the HBM peak (2 x bytes of traffic).
  * t = launch_us + bytes / min(peak, in_flight / latency). */
 kvx_status kvx_estimate_us(const kvx_link_model *model, int op, int64_t bytes,
                            const kvx_launch_cfg *cfg, double *us);

@@ -22,8 +22,8 @@ namespace {
 const int kSlots = 4;
 const size_t kDefaultDescriptorBytes = 8u << 20;
 const int kDefaultStageBytes = 32 << 10;
-const int kDefaultStages = 6;
-const int64_t kMaxBulkSmem = 220 << 10;
+const int kDefaultStages = 3;  // per copy lane of the bulk mapping
+const int64_t kMaxBulkSmem = 208 << 10;  // the rings; the CTA's other shared state is ~14 KiB
 
 struct Slot {
     char *host = nullptr;
@@ -190,13 +190,14 @@ kvx_status resolve_cfg(kvx_ctx *ctx, int op, const kvx_launch_cfg *user, kvx_lau
         ok = ok && out->threads >= 32 && out->threads <= 1024 && out->threads % 32 == 0 &&
              pick_kernel(out->unroll, 0, 0);
     } else if (out->mapping == KVX_MAP_BULK) {
-        // One warp per CTA; `unroll` counts shared-memory stages.
+        // Three warps per CTA (segment lookups, two copy lanes); `unroll` counts the
+        // shared-memory stages of each copy lane's ring.
         if (!user->unroll)
             out->unroll = kDefaultStages;
-        out->threads = 32;
+        out->threads = 32 * (1 + kBulkLanes);
         ok = ok && out->unroll >= 2 && out->unroll <= kBulkMaxStages &&
              out->stage_bytes >= 16 && out->stage_bytes % 16 == 0 &&
-             int64_t(out->unroll) * out->stage_bytes <= kMaxBulkSmem;
+             int64_t(kBulkLanes) * out->unroll * out->stage_bytes <= kMaxBulkSmem;
     } else {
         ok = false;
     }
@@ -274,7 +275,7 @@ LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Pl
     int64_t ctas = int64_t(sms) * cfg.ctas_per_sm;
     const bool split = cfg.mapping == KVX_MAP_WARP_SEGMENT && plan.split > 1;
     const int64_t per_cta = cfg.mapping == KVX_MAP_CTA    ? 32
-                            : cfg.mapping == KVX_MAP_BULK ? warps_per_cta
+                            : cfg.mapping == KVX_MAP_BULK ? 1
                                                           : warps_per_cta * plan.batch;
     const int64_t work = split ? plan.total_items * plan.split : plan.total_items;
     const int64_t needed = (work + per_cta - 1) / per_cta;
@@ -285,11 +286,11 @@ LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Pl
         sh.fn = dir == KVX_DIR_GATHER
                     ? reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_GATHER>)
                     : reinterpret_cast<const void *>(kvx_bulk_kernel<KVX_DIR_SCATTER>);
-        sh.threads = 32;
+        sh.threads = 32 * (1 + kBulkLanes);
         sh.bulk = 1;
         sh.stage_bytes = cfg.stage_bytes;
         sh.stages = cfg.unroll;
-        sh.smem = size_t(cfg.unroll) * cfg.stage_bytes;
+        sh.smem = size_t(kBulkLanes) * cfg.unroll * cfg.stage_bytes;
     } else if (cfg.mapping == KVX_MAP_CTA) {
         sh.fn = reinterpret_cast<const void *>(pick_cta(cfg.unroll, dir, cfg.store_hint));
         sh.threads = cfg.threads;
@@ -316,7 +317,8 @@ cudaError_t launch_kernel(const LaunchShape &sh, Plan plan, cudaStream_t s)
             return e;
         int stage_bytes = sh.stage_bytes, stages = sh.stages;
         void *args[] = {&plan, &stage_bytes, &stages};
-        return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(32u), args, sh.smem, s);
+        return cudaLaunchKernel(sh.fn, dim3(unsigned(sh.ctas)), dim3(unsigned(sh.threads)), args,
+                                sh.smem, s);
     }
     void *args[] = {&plan};
     if (!sh.overlap)

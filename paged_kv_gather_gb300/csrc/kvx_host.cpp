@@ -506,17 +506,29 @@ kvx_status kvx_estimate_us(const kvx_link_model *m, int op, int64_t bytes,
     // library's kvx_default_launch_cfg).
     int sm_cap = op <= KVX_OP_LOAD ? 16 : 0, ctas = op <= KVX_OP_LOAD ? 1 : 2;
     int threads = op <= KVX_OP_LOAD ? 1024 : 256, unroll = op <= KVX_OP_LOAD ? 8 : 4;
+    bool bulk = false;
+    double stage_bytes = 32768.0;
     if (cfg) {
         sm_cap = cfg->sm_cap;
         if (cfg->ctas_per_sm)
             ctas = cfg->ctas_per_sm;
-        if (cfg->threads)
-            threads = cfg->threads;
-        if (cfg->unroll)
-            unroll = cfg->unroll;
+        bulk = cfg->mapping == KVX_MAP_BULK;
+        if (bulk) {
+            unroll = cfg->unroll ? cfg->unroll : 3;
+            if (cfg->stage_bytes)
+                stage_bytes = cfg->stage_bytes;
+        } else {
+            if (cfg->threads)
+                threads = cfg->threads;
+            if (cfg->unroll)
+                unroll = cfg->unroll;
+        }
     }
     const double sms = sm_cap > 0 && sm_cap < m->num_sms ? sm_cap : m->num_sms;
-    const double in_flight = sms * ctas * threads * (double)unroll * 16.0;  // bytes
+    // Bytes in flight per CTA: threads x unroll 16-byte units (registers), or for the bulk
+    // mapping its two rings' loading stages, 2 x (stages - 1) x stage_bytes.
+    const double per_cta = bulk ? 2.0 * (unroll - 1) * stage_bytes : threads * (double)unroll * 16.0;
+    const double in_flight = sms * ctas * per_cta;  // bytes
     const double little_gbs = in_flight / (m->latency_us * 1e3);           // B/ns = GB/s
     double peak;
     double moved = (double)bytes;

@@ -559,14 +559,29 @@ CtaFn pick_cta(int unroll, int dir, int hint)
 
 // ------------------------------------------------------------------ bulk-copy (TMA) mapping
 //
-// One warp per CTA streams its items through a ring of shared-memory stages with the
-// Blackwell bulk-copy engine: cp.async.bulk global -> shared completes on an mbarrier
-// (transaction bytes), then cp.async.bulk shared -> global (bulk group) writes the stage
-// out.  Up to n_stages - 1 loads are in flight per CTA without holding them in registers,
-// and the SM's load/store pipes stay free for other work.  Every wait is bounded: past
-// about one second the kernel flags KVX_DEV_WAIT_TIMEOUT, drains what it issued and exits.
+// Host-link bandwidth per SM is capped on GB300 at about 50 GB/s however the bytes in
+// flight are held (registers, cp.async into shared memory or bulk copies), and host reads
+// reach that cap only with about 128 KiB in flight per SM: less is latency-bound, more
+// queues up and runs slower.  So the fewest SMs that reach the link's peak are the ones
+// that keep exactly that much in flight without stalls between copies.  Each CTA here is
+// three warps.  Warp 0 resolves the CTA's segments 32 at a time, one per lane (chunk search
+// and page-table read in parallel), into a queue of kBulkQueue batches in shared memory.
+// Lane 0 of warps 1 and 2 (the copy lanes) take alternate batches and each drives the
+// Blackwell bulk-copy engine on its own ring of n_stages shared-memory stages: it packs
+// segments into stages back to back, cutting a segment where a stage ends, loads each full
+// stage (cp.async.bulk global -> shared, completing on the stage's mbarrier with transaction
+// bytes) and writes it out (cp.async.bulk shared -> global, one bulk group per stage), with
+// one copy per run of pieces that lie back to back on that side: a stage's host side is
+// then usually one copy, and only its page side needs one copy per page segment.  Each lane keeps n_stages - 1 stages loading while the next fills; two lanes keep
+// their issue costs (a bulk copy occupies its issuing thread for a few hundred cycles) from
+// adding up.  Every wait is bounded (about one second): on expiry the kernel flags
+// KVX_DEV_WAIT_TIMEOUT, issues nothing more, waits (again bounded) for the copies it issued
+// and exits.
 
-constexpr int kBulkMaxStages = 8;
+constexpr int kBulkLanes = 2;         // copy lanes per CTA, each with its own ring
+constexpr int kBulkMaxStages = 8;     // stages per ring
+constexpr int kBulkQueue = 4;         // resolved batches of 32 segments between the warps
+constexpr int kBulkStagePieces = 32;  // bulk copies per stage at most
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -587,31 +602,49 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
                  : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+// One arrival (release at CTA scope: the caller's earlier shared-memory writes are visible
+// to whoever waits on the completed phase).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Warp-uniform bounded wait for the completion of phase `parity` of an mbarrier.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int lane)
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 {
-    const uint32_t addr = smem_u32(bar);
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+
+// One thread: bounded wait for the completion of phase `parity` of an mbarrier.
+__device__ __forceinline__ bool mbar_wait1(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_test(bar, parity))
+        return true;
+    const uint64_t deadline = global_ns() + kWaitLimitNs;
+    while (!mbar_test(bar, parity))
+        if (global_ns() > deadline)
+            return false;
+    return true;
+}
+
+// Warp-uniform bounded wait (every lane returns the same answer); sleeps between polls so
+// that a waiting warp leaves the shared-memory pipe to the copy lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int lane)
+{
     const uint64_t deadline = global_ns() + kWaitLimitNs;
     while (true) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done)
-                     : "r"(addr), "r"(parity)
-                     : "memory");
-        if (__any_sync(0xffffffffu, done))
+        if (__any_sync(0xffffffffu, mbar_test(bar, parity)))
             return true;
         const int late = lane == 0 ? int(global_ns() > deadline) : 0;
         if (__shfl_sync(0xffffffffu, late, 0))
             return false;
+        __nanosleep(500);
     }
 }
 
@@ -629,114 +662,246 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uin
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
                  "r"(smem_u32(smem_src)), "r"(bytes)
                  : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-template <int DIR>
-__global__ void __launch_bounds__(32) kvx_bulk_kernel(const Plan p, int stage_bytes,
-                                                     int n_stages)
-{
-    extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ __align__(8) uint64_t full[kBulkMaxStages];
-    __shared__ char *stage_dst[kBulkMaxStages];
-    __shared__ uint32_t stage_len[kBulkMaxStages];
-    const int lane = threadIdx.x;
-    const int64_t v = p.token_bytes;
-    if (lane == 0) {
-        for (int st = 0; st < n_stages; ++st)
-            mbar_init(&full[st], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
+// One copy lane's ring bookkeeping.
+struct BulkLaneState {
+    uint64_t full[kBulkMaxStages];  // stage loaded: one arrival + its bytes
+    const char *psrc[kBulkMaxStages][kBulkStagePieces];
+    char *pdst[kBulkMaxStages][kBulkStagePieces];
+    uint32_t poff[kBulkMaxStages][kBulkStagePieces];
+    uint32_t plen[kBulkMaxStages][kBulkStagePieces];
+    uint32_t npieces[kBulkMaxStages];
+};
 
-    // Piece stream: items of this CTA, cut into runs of at most stage_bytes.
-    int64_t item = blockIdx.x;
-    Segment sg;
-    bool have = false;
-    int32_t row = 0, n_rows = 0;
-    int64_t off = 0, row_bytes = 0;
-    auto next = [&](const char *&src, char *&dst, uint32_t &bytes) -> bool {
-        while (true) {
-            if (have) {
-                if (off < row_bytes) {
-                    const int64_t b = min(int64_t(stage_bytes), row_bytes - off);
-                    src = sg.src + row * sg.s_pitch + off;
-                    dst = sg.dst + row * sg.d_pitch + off;
-                    bytes = uint32_t(b);
-                    off += b;
-                    return true;
-                }
-                off = 0;
-                if (++row < n_rows)
-                    continue;
-                have = false;
-            }
-            if (item >= p.total_items)
-                return false;
-            if (resolve_segment<DIR>(p, item, lane, sg)) {
-                have = true;
-                row = 0;
-                off = 0;
-                n_rows = sg.contiguous ? 1 : sg.rows;
-                row_bytes = sg.contiguous ? int64_t(sg.rows) * v : v;
-            }
-            item += gridDim.x;
-        }
-    };
+// Shared state of one bulk CTA (the rings of stages are the dynamic shared memory).
+struct BulkShared {
+    uint64_t qfull[kBulkQueue];   // batch resolved: 32 arrivals (every lane of warp 0)
+    uint64_t qempty[kBulkQueue];  // batch consumed: one arrival (its copy lane)
+    Segment seg[kBulkQueue][32];
+    unsigned valid[kBulkQueue];
+    BulkLaneState lane[kBulkLanes];
+};
 
+// A copy lane's ring: stages [retired, issued) are loading (their loads issued, their
+// stores not yet), and stage `issued` is being filled when `open`.
+struct BulkRing {
+    BulkLaneState &ls;
+    unsigned char *ring;
+    uint32_t stage_bytes;
+    uint32_t n_stages;
     uint32_t issued = 0, retired = 0;
-    bool more = true, timed_out = false;
-    const char *src = nullptr;
-    char *dst = nullptr;
-    uint32_t bytes = 0;
-    auto issue = [&]() {
+    uint32_t fill = 0, np = 0;
+    bool open = false;
+
+    __device__ BulkRing(BulkLaneState &s, unsigned char *r, uint32_t sb, uint32_t ns)
+        : ls(s), ring(r), stage_bytes(sb), n_stages(ns)
+    {
+    }
+
+    __device__ unsigned char *stage(uint32_t st) { return ring + size_t(st) * stage_bytes; }
+
+    // Oldest loading stage: wait for its bytes, then write it out (one bulk group), one bulk
+    // copy per run of pieces that are back to back at their destination.
+    __device__ bool retire_one()
+    {
+        const uint32_t st = retired % n_stages;
+        if (!mbar_wait1(&ls.full[st], (retired / n_stages) & 1u))
+            return false;
+        const uint32_t n = ls.npieces[st];
+        for (uint32_t i = 0; i < n;) {
+            char *d = ls.pdst[st][i];
+            uint32_t bytes = ls.plen[st][i];
+            uint32_t j = i + 1;
+            for (; j < n && ls.pdst[st][j] == d + bytes; ++j)
+                bytes += ls.plen[st][j];
+            bulk_store(d, stage(st) + ls.poff[st][i], bytes);
+            i = j;
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        ++retired;
+        return true;
+    }
+
+    // The open stage is complete: expect its bytes (with the stage's one arrival), then load
+    // it, one bulk copy per run of pieces that are back to back at their source.
+    __device__ void close_stage()
+    {
         const uint32_t st = issued % n_stages;
-        if (lane == 0) {
-            stage_dst[st] = dst;
-            stage_len[st] = bytes;
-            mbar_expect_tx(&full[st], bytes);
-            bulk_load(ring + size_t(st) * stage_bytes, src, bytes, &full[st]);
+        ls.npieces[st] = np;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                         smem_u32(&ls.full[st])),
+                     "r"(fill)
+                     : "memory");
+        for (uint32_t i = 0; i < np;) {
+            const char *s = ls.psrc[st][i];
+            uint32_t bytes = ls.plen[st][i];
+            uint32_t j = i + 1;
+            for (; j < np && ls.psrc[st][j] == s + bytes; ++j)
+                bytes += ls.plen[st][j];
+            bulk_load(stage(st) + ls.poff[st][i], s, bytes, &ls.full[st]);
+            i = j;
         }
         ++issued;
-    };
-    while (issued + 1 < uint32_t(n_stages)) {
-        if (!next(src, dst, bytes)) {
-            more = false;
+        open = false;
+    }
+
+    __device__ bool open_stage()
+    {
+        if (issued - retired == n_stages - 1 && !retire_one())
+            return false;
+        // The stage about to be filled was last written out n_stages stages ago; at most one
+        // newer store group may still be reading shared memory.
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        open = true;
+        fill = 0;
+        np = 0;
+        return true;
+    }
+
+    // A contiguous run of `bytes` (a multiple of 16): recorded as pieces cut at stage
+    // boundaries, so every stage but the last is filled completely whatever the segment size.
+    __device__ bool add_run(const char *src, char *dst, int64_t bytes)
+    {
+        while (bytes > 0) {
+            if (!open && !open_stage())
+                return false;
+            const uint32_t st = issued % n_stages;
+            const uint32_t take = uint32_t(min(bytes, int64_t(stage_bytes - fill)));
+            ls.psrc[st][np] = src;
+            ls.pdst[st][np] = dst;
+            ls.poff[st][np] = fill;
+            ls.plen[st][np] = take;
+            ++np;
+            fill += take;
+            src += take;
+            dst += take;
+            bytes -= take;
+            if (fill == stage_bytes || np == kBulkStagePieces)
+                close_stage();
+        }
+        return true;
+    }
+
+    // After a timeout: issue no more stores, but wait (bounded) until the loads already
+    // issued have landed, so that no bulk copy still targets this CTA's shared memory when
+    // it exits.  False if one of them did not land within its limit either.
+    __device__ bool drain_loads()
+    {
+        open = false;  // the open stage's loads are issued only when it closes: none yet
+        bool ok = true;
+        for (; retired < issued; ++retired)
+            ok = mbar_wait1(&ls.full[retired % n_stages], (retired / n_stages) & 1u) && ok;
+        return ok;
+    }
+};
+
+// The CTA's items are first, first + 1, ..., first + n_mine - 1 (a contiguous block, so
+// that consecutive segments of a chunk stay back to back on its side); batch k holds items
+// first + 32 k .. first + 32 k + 31.
+template <int DIR>
+__device__ __forceinline__ void bulk_resolver(const Plan &p, BulkShared &sh, int64_t first,
+                                              int64_t n_mine, int64_t n_batches, int lane)
+{
+    for (int64_t k = 0; k < n_batches; ++k) {
+        const int q = int(k % kBulkQueue);
+        if (k >= kBulkQueue &&
+            !mbar_wait_warp(&sh.qempty[q], uint32_t((k / kBulkQueue - 1) & 1), lane)) {
+            if (lane == 0)
+                atomicOr(p.status, KVX_DEV_WAIT_TIMEOUT);
+            return;  // the copy lane's wait for this batch then runs out too
+        }
+        Segment sg;
+        sg.src = nullptr;
+        sg.dst = nullptr;
+        sg.s_pitch = sg.d_pitch = 0;
+        sg.rows = 0;
+        sg.contiguous = true;
+        bool ok = false;
+        const int64_t idx = k * 32 + lane;
+        if (idx < n_mine) {
+            const int64_t item = first + idx;
+            ok = segment_of<DIR>(p, find_chunk_lane(p.item_begin, p.n_chunks, item), item, true,
+                                 sg);
+        }
+        sh.seg[q][lane] = sg;
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0)
+            sh.valid[q] = m;
+        mbar_arrive(&sh.qfull[q]);  // each lane releases its own entry (and lane 0 the mask)
+    }
+}
+
+// Copy lane `which`: batches which, which + kBulkLanes, ...
+template <int DIR>
+__device__ __forceinline__ void bulk_copier(const Plan &p, BulkShared &sh, unsigned char *ring,
+                                            int stage_bytes, int n_stages, int64_t n_batches,
+                                            int which)
+{
+    BulkRing r(sh.lane[which], ring + size_t(which) * n_stages * stage_bytes,
+               uint32_t(stage_bytes), uint32_t(n_stages));
+    const int64_t v = p.token_bytes;
+    bool ok = true;
+    for (int64_t k = which; k < n_batches && ok; k += kBulkLanes) {
+        const int q = int(k % kBulkQueue);
+        if (!mbar_wait1(&sh.qfull[q], uint32_t((k / kBulkQueue) & 1))) {
+            ok = false;
             break;
         }
-        issue();
-    }
-    while (retired < issued) {
-        const uint32_t st = retired % n_stages;
-        if (!mbar_wait(&full[st], (retired / n_stages) & 1u, lane)) {
-            timed_out = true;
-            break;
+        const unsigned m = sh.valid[q];
+        for (int i = 0; i < 32 && ok; ++i) {
+            if (!((m >> i) & 1u))
+                continue;
+            const Segment sg = sh.seg[q][i];
+            const int n_runs = sg.contiguous ? 1 : sg.rows;
+            const int64_t run = sg.contiguous ? int64_t(sg.rows) * v : v;
+            for (int rr = 0; rr < n_runs && ok; ++rr)
+                ok = r.add_run(sg.src + rr * sg.s_pitch, sg.dst + rr * sg.d_pitch, run);
         }
-        if (lane == 0)
-            bulk_store(stage_dst[st], ring + size_t(st) * stage_bytes, stage_len[st]);
-        ++retired;
-        if (more) {
-            if (!next(src, dst, bytes)) {
-                more = false;
-            } else {
-                // The stage about to be refilled was last written out by the store issued
-                // one iteration ago: wait until at most the newest store still reads.
-                if (lane == 0)
-                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                __syncwarp();
-                issue();
-            }
+        mbar_arrive(&sh.qempty[q]);  // the batch's entries are no longer read
+    }
+    if (ok) {
+        if (r.open)
+            r.close_stage();
+        while (ok && r.retired < r.issued)
+            ok = r.retire_one();
+    }
+    if (!ok) {
+        atomicOr(p.status, KVX_DEV_WAIT_TIMEOUT);
+        r.drain_loads();
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// n_stages stages of stage_bytes per copy lane: dynamic shared memory of
+// kBulkLanes x n_stages x stage_bytes.
+template <int DIR>
+__global__ void __launch_bounds__(32 * (1 + kBulkLanes), 1)
+    kvx_bulk_kernel(const Plan p, int stage_bytes, int n_stages)
+{
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ BulkShared sh;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t per_cta = (p.total_items + gridDim.x - 1) / gridDim.x;
+    const int64_t first = min(p.total_items, int64_t(blockIdx.x) * per_cta);
+    const int64_t n_mine = min(p.total_items - first, per_cta);
+    const int64_t n_batches = (n_mine + 31) / 32;
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < kBulkLanes; ++j)
+            for (int st = 0; st < n_stages; ++st)
+                mbar_init(&sh.lane[j].full[st], 1);
+        for (int q = 0; q < kBulkQueue; ++q) {
+            mbar_init(&sh.qfull[q], 32);
+            mbar_init(&sh.qempty[q], 1);
         }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (timed_out) {
-        if (lane == 0)
-            atomicOr(p.status, KVX_DEV_WAIT_TIMEOUT);
-        for (uint32_t r = retired; r < issued; ++r)  // drain the loads still in flight
-            mbar_wait(&full[r % n_stages], (r / n_stages) & 1u, lane);
-    }
-    if (lane == 0)
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-    __syncwarp();
+    __syncthreads();
+    if (warp == 0)
+        bulk_resolver<DIR>(p, sh, first, n_mine, n_batches, lane);
+    else if (lane == 0)
+        bulk_copier<DIR>(p, sh, ring, stage_bytes, n_stages, n_batches, warp - 1);
 }
 
 // ------------------------------------------------------------------------- round trip

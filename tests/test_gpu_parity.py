@@ -315,8 +315,8 @@ def test_small_transfers_cut_segments_into_row_slices(ctx, stream, layout, unrol
     arena.close()
 
 
-@pytest.mark.parametrize("stages,stage_bytes,ctas", [(2, 16, 1), (3, 1040, 2), (6, 32768, 1),
-                                                    (8, 27648, 1), (3, 65536, 1)])
+@pytest.mark.parametrize("stages,stage_bytes,ctas", [(2, 16, 1), (3, 1040, 2), (3, 32768, 1),
+                                                    (8, 13312, 1), (2, 53248, 1)])
 def test_bulk_mapping_multi_tile_ragged(ctx, stream, stages, stage_bytes, ctas):
     """The bulk-copy mapping on every direction: segments longer and shorter than a stage,
     chunk cuts inside pages, both layouts, host and device chunks."""
@@ -357,7 +357,8 @@ def test_bulk_mapping_rejects_bad_stage_shapes(ctx, stream):
     arena = Arena(16, "host")
     ch = kvx.chunks_array([wl.ChunkSpec(0, 0, 1, 0, 1, 0, 0)], arena.ptr)
     for bad in (bulk(stages=1), bulk(stages=9), bulk(stage_bytes=24),
-                bulk(stages=8, stage_bytes=65536), cfg(batch=33), cfg(batch=-1)):
+                bulk(stages=8, stage_bytes=65536), bulk(stages=4, stage_bytes=32768),
+                cfg(batch=33), cfg(batch=-1)):
         with pytest.raises(kvx.KvxError) as e:
             kvx.kvx_store_chunks(ctx, dpool.pool, reqs.array, ch, 0, 1, bad, stream.cuda_stream)
         assert e.value.status == kvx.KVX_ERR_INVALID_ARG

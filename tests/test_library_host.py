@@ -261,6 +261,17 @@ def test_estimator_littles_law_and_link_cap():
     c.sm_cap, c.ctas_per_sm, c.threads, c.unroll = 2, 1, 1024, 4
     us = kvx.kvx_estimate_us(m, kvx.KVX_OP_STORE, N, c)
     assert N / ((us - m.launch_us) * 1e3) == pytest.approx(2 * 1024 * 4 * 16 / 2600.0)
+    # The bulk mapping keeps its two rings' loading stages in flight: 2 x (stages - 1) x
+    # stage_bytes per CTA, whatever the thread count.
+    c = kvx.kvx_launch_cfg()
+    c.sm_cap, c.ctas_per_sm, c.mapping, c.unroll, c.stage_bytes = 1, 1, kvx.KVX_MAP_BULK, 3, 32768
+    us = kvx.kvx_estimate_us(m, kvx.KVX_OP_LOAD, N, c)
+    assert N / ((us - m.launch_us) * 1e3) == pytest.approx(2 * 2 * 32768 / 2600.0)
+    c.unroll, c.stage_bytes = 0, 0  # the bulk defaults: 3 stages of 32 KiB
+    assert kvx.kvx_estimate_us(m, kvx.KVX_OP_LOAD, N, c) == pytest.approx(us)
+    c.sm_cap = 4
+    us = kvx.kvx_estimate_us(m, kvx.KVX_OP_LOAD, N, c)
+    assert N / ((us - m.launch_us) * 1e3) == pytest.approx(min(m.h2d_gbs, 4 * 4 * 32768 / 2600.0))
     # The HBM transform moves 2N through HBM at the copy peak, whatever the SM cap.
     us = kvx.kvx_estimate_us(m, kvx.KVX_OP_GATHER_HBM, N, None)
     assert us == pytest.approx(m.launch_us + 2 * N / (m.hbm_gbs * 1e3))
