@@ -61,6 +61,8 @@ def parse():
                    help="target CPU time of the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-dma-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the 4-SM, MLA, batched and layer-streaming legs of the default run")
     p.add_argument("--store-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--load-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
     p.add_argument("--transform-cfg", default="", help="sm_cap,ctas,threads,unroll,hint")
@@ -106,6 +108,8 @@ def parse():
                    help="llama70b: load stream priorities (-1 high, 0 normal)")
     p.add_argument("--partition-sms", default="8,16",
                    help="llama70b: I/O partition sizes (green contexts) to run; empty: none")
+    p.add_argument("--partition-sms-qwen", type=int, default=16,
+                   help="qwen7b_batch: SMs of each of the two I/O partitions")
     p.add_argument("--sm-caps", default="1,2,4,8,16,32,0",
                    help="SM caps of the llama70b overlap sweep (0 = all SMs)")
     return p.parse_args()
@@ -442,6 +446,116 @@ class RoundTrip:
         return len(self.groups)
 
 
+def few_sm_legs(kvx, ctx, stream, pool, rs, rd, chunks, num_layers, N, link, cap=4):
+    """The same store and load of the Llama-3.1-8B-shaped request on `cap` SMs: the bulk
+    mapping (two bulk-copy rings per CTA) and the register mapping, each against its
+    one-way peak."""
+    sh = stream.cuda_stream
+    out = {"sm_cap": cap}
+    for name, op, fn, rq, mapping, stages, sb in (
+            ("load_bulk", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd, "bulk", 3, 32768),
+            ("store_bulk", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs, "bulk", 6, 16384),
+            ("load_segment", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd, "segment", 0, 0),
+            ("store_segment", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs, "segment", 0, 0)):
+        c = io_cfg(kvx, ctx, op, cap, mapping, stages, sb)
+        ms = _timed(stream, lambda: fn(ctx, pool, rq, chunks, 0, num_layers, c, sh), 3, 1)
+        peak = link["h2d"] if op == kvx.KVX_OP_LOAD else link["d2h"]
+        gbs = N / (ms * 1e-3) / GB
+        out[name] = {"gbs": round(gbs, 2), "frac": round(gbs / peak, 4), "cfg": c.as_dict()}
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    return out
+
+
+def mla_legs(kvx, wl, link, pages=(1, 16), chunk_bytes=1 << 20, reps=3):
+    """The MLA latent (61 layers, 1152-byte tokens, 16384 tokens) stored and loaded with the
+    library defaults at the given page sizes, per-layer chunks of chunk_bytes."""
+    ctx = kvx.kvx_create(0, 64 << 20)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    out = {}
+    for P in pages:
+        w = wl.mla_sweep(P, chunk_bytes)
+        s = w.shape
+        pools = _pool_tensor(s, w.seed, wl)
+        pool = kvx.Pool.from_tensor(pools, s.page_size)
+        src, dst = w.store_requests[0], w.load_requests[0]
+        ps = torch.from_numpy(src.page_table).cuda()
+        pd = torch.from_numpy(dst.page_table).cuda()
+        rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+        rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+        arena = kvx.HostBuffer(w.store_arena_bytes)
+        arena.array[:] = 0
+        ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+        N = w.store_bytes()
+        st_ms = _timed(stream, lambda: kvx.kvx_store_chunks(ctx, pool, rs, ch, stream=sh), reps)
+        ld_ms = _timed(stream, lambda: kvx.kvx_load_chunks(ctx, pool, rd, ch, stream=sh), reps)
+        assert kvx.kvx_get_status(ctx, sh) == 0
+        sg, lg = N / (st_ms * 1e-3) / GB, N / (ld_ms * 1e-3) / GB
+        out[f"p{P}"] = {"page_tokens": P, "chunk_kib": chunk_bytes >> 10, "bytes": N,
+                        "chunks": len(w.store_chunks),
+                        "store_gbs": round(sg, 2), "store_frac": round(sg / link["d2h"], 4),
+                        "load_gbs": round(lg, 2), "load_frac": round(lg / link["h2d"], 4)}
+        arena.close()
+        del pools
+    kvx.kvx_destroy(ctx)
+    return out
+
+
+def llama70b_legs(kvx, wl, n_layers=16, reps=2):
+    """Layer streaming of the Llama-3.1-70B-shaped prefix over its first n_layers layers
+    under one bf16 8192^3 GEMM per layer: the bulk mapping on 5 and 4 SMs and the register
+    mapping on its default 16 SMs, each on a high-priority load stream."""
+    w, pools, pool, pt, reqs, arena, per_layer = llama70b_setup(kvx, wl, n_layers)
+    ctx = kvx.kvx_create(0)
+    sb = torch.cuda.Stream()
+    A, B, C = gemm_operands(w.seed)
+    layer_bytes = w.load_bytes() // n_layers
+
+    def gemm():
+        torch.matmul(A, B, out=C)
+
+    with torch.cuda.stream(sb):
+        gemm_ms = _timed(sb, gemm, 20, warm=5)
+    out = {"layers": n_layers, "layer_bytes": layer_bytes, "gemm_alone_ms": round(gemm_ms, 4)}
+    for name, mapping, cap in (("bulk_5sm", "bulk", 5), ("bulk_4sm", "bulk", 4),
+                               ("segment_16sm", "segment", 16)):
+        sa = torch.cuda.Stream(priority=-1)
+        cfg = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, cap, mapping)
+        out[name] = layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes,
+                                    cfg, sa, sb, gemm, gemm_ms, reps)
+    arena.close()
+    kvx.kvx_destroy(ctx)
+    del pools, A, B, C
+    return out
+
+
+def flat_extras(seq, few, mla, qwen, l70, link):
+    """Scalar summaries of the extra legs, for the roofline object of the JSON line."""
+    f = {"store_gbs": seq["store"]["gbs"], "store_frac": seq["store"]["frac"],
+         "load_gbs": seq["load"]["gbs"], "load_frac": seq["load"]["frac"]}
+    if few:
+        for k in ("load_bulk", "store_bulk", "load_segment", "store_segment"):
+            f[f"sm4_{k}_frac"] = few[k]["frac"]
+    if mla:
+        for k, v in mla.items():
+            f[f"cfg5_mla_{k}_store_frac"] = v["store_frac"]
+            f[f"cfg5_mla_{k}_load_frac"] = v["load_frac"]
+    if qwen:
+        f["cfg4_qwen7b_bound_ms"] = qwen["bound_ms"]
+        f["cfg4_exchange_frac_of_bound"] = qwen["exchange_one_launch"]["frac_of_bound"]
+        f["cfg4_two_streams_frac_of_bound"] = qwen["two_streams"]["frac_of_bound"]
+        tp = qwen.get("two_partitions", {})
+        if "frac_of_bound" in tp:
+            f["cfg4_two_partitions_frac_of_bound"] = tp["frac_of_bound"]
+    if l70:
+        for k in ("bulk_5sm", "bulk_4sm", "segment_16sm"):
+            r = l70[k]
+            f[f"cfg3_{k}_load_overlap_frac"] = round(r["load_overlap_gbs"] / link["h2d"], 4)
+            f[f"cfg3_{k}_gemm_slowdown_pct"] = r["gemm_slowdown_pct"]
+            f[f"cfg3_{k}_e2e_vs_model"] = r["e2e_vs_model"]
+    return f
+
+
 def run_ours(args):
     world, rank, local = dist_setup(args)
     torch.cuda.set_device(local)
@@ -485,49 +599,7 @@ def run_ours(args):
 
     # ---- host-link peaks: one 4 GiB pinned copy per direction, then both at once.  A peak
     # is the best of 8 timed copies (the copy engines' concurrent rate varies by run).
-    link, samples = {}, {}
-    hp = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
-    dp = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
-    with torch.cuda.stream(stream):
-        for name, fn in (("h2d", lambda: dp.copy_(hp, non_blocking=True)),
-                         ("d2h", lambda: hp.copy_(dp, non_blocking=True))):
-            for _ in range(2):
-                fn()
-            t = EventTimer(stream)
-            for _ in range(8):
-                e = t.start()
-                fn()
-                t.stop(e)
-            stream.synchronize()
-            gbs = [(4 << 30) / (ms * 1e-3) / GB for ms in t.ms()]
-            link[name] = round(max(gbs), 1)
-            samples[name] = [round(x, 1) for x in gbs]
-    hp2 = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
-    dp2 = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
-    s2 = torch.cuda.Stream(device=dev)
-    bid = []
-    for rep in range(9):
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        s2.wait_event(e0)
-        first, second = (stream, s2) if rep % 2 else (s2, stream)
-        with torch.cuda.stream(first):
-            (dp.copy_(hp, non_blocking=True) if first is stream else
-             hp2.copy_(dp2, non_blocking=True))
-        with torch.cuda.stream(second):
-            (dp.copy_(hp, non_blocking=True) if second is stream else
-             hp2.copy_(dp2, non_blocking=True))
-        e1, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e1.record(stream)
-        e2.record(s2)
-        torch.cuda.synchronize()
-        if rep:
-            ms = max(e0.elapsed_time(e1), e0.elapsed_time(e2))
-            bid.append(2 * (4 << 30) / (ms * 1e-3) / GB)
-    link["bidir"] = round(max(bid), 1)
-    samples["bidir"] = [round(x, 1) for x in bid]
-    del hp, dp, hp2, dp2
+    link, samples = measure_link(dev, stream)
 
     # ---- sequential store then load on one stream (per-direction rooflines)
     def seq_step(t_store=None, t_load=None):
@@ -704,6 +776,33 @@ def run_ours(args):
         cpu = CpuSample(os.cpu_count() or 1).run(args.cpu_seconds,
                                                  single_thread_seconds=args.cpu_seconds / 3)
 
+    # ---- the other workloads of the scope, compactly (1 GPU only): the same request on 4
+    # SMs, the MLA latent at 1- and 16-token pages, the batched partial hits, and layer
+    # streaming of the 70B-shaped prefix under GEMMs.  Outside the timed region.
+    seq = {"note": "store then load on one stream, no overlap: per-direction rooflines",
+           "step_gbs": round(2 * N / ((store_ms + load_ms) * 1e-3) / GB, 2),
+           "store": {"ms": round(store_ms, 4), "gbs": round(store_gbs, 2),
+                     "peak": link["d2h"], "frac": round(store_gbs / link["d2h"], 4),
+                     "traffic": recorded_traffic("store", "llama8b")},
+           "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
+                    "peak": link["h2d"], "frac": round(load_gbs / link["h2d"], 4),
+                    "traffic": recorded_traffic("load", "llama8b")}}
+    few = mla = qwen = l70 = None
+    extra_clocks = None
+    if world == 1 and not args.no_extras:
+        few = few_sm_legs(kvx, ctx, stream, pool, reqs_src, reqs_dst, chunks_host,
+                          s.num_layers, N, link)
+        del pools
+        torch.cuda.empty_cache()
+        with ClockSampler(local) as ec:
+            mla = mla_legs(kvx, wl, link)
+            torch.cuda.empty_cache()
+            qwen = qwen7b_measure(args, kvx, wl, link, reps=3)
+            torch.cuda.empty_cache()
+            l70 = llama70b_legs(kvx, wl)
+            torch.cuda.synchronize()
+        extra_clocks = ec.summary()
+
     value = 2 * N * args.steps * world / (total_ms * 1e-3) / GB
     step_gbs = 2 * N / (total_ms / args.steps * 1e-3) / GB
     launch_gbs = step_gbs  # one launch per step
@@ -744,17 +843,17 @@ def run_ours(args):
                      "per_launch": {"ms": round(total_ms / args.steps, 4),
                                     "gbs": round(launch_gbs, 2), "bytes_per_launch": 2 * N,
                                     "items_per_launch": items, "ctas": ctas,
-                                    "threads": threads}},
+                                    "threads": threads},
+                     **flat_extras(seq, few, mla, qwen, l70, link),
+                     "flat_note": "store_/load_: the request stored, then loaded, alone on "
+                                  "one stream (library defaults) against the one-way peaks; "
+                                  "sm4_: the same on 4 SMs; cfg3_/cfg4_/cfg5_: the 70B "
+                                  "layer streaming, batched partial hits and MLA legs of "
+                                  "extra_workloads"},
+        "extra_workloads": {"few_sms": few, "mla_latent": mla, "qwen7b_batched": qwen,
+                            "llama70b_layer_streaming": l70, "clocks": extra_clocks},
         "exchange_pipeline": exchange_pipeline,
-        "sequential": {
-            "note": "store then load on one stream, no overlap: per-direction rooflines",
-            "step_gbs": round(2 * N / ((store_ms + load_ms) * 1e-3) / GB, 2),
-            "store": {"ms": round(store_ms, 4), "gbs": round(store_gbs, 2),
-                      "peak": link["d2h"], "frac": round(store_gbs / link["d2h"], 4),
-                      "traffic": recorded_traffic("store", "llama8b")},
-            "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
-                     "peak": link["h2d"], "frac": round(load_gbs / link["h2d"], 4),
-                     "traffic": recorded_traffic("load", "llama8b")}},
+        "sequential": seq,
         "cfg": {"roundtrip": cfg_rt.as_dict(), "store": cfg_store.as_dict(),
                 "load": cfg_load.as_dict()},
         "host_link_peak": {"h2d_gbs": link["h2d"], "d2h_gbs": link["d2h"],
@@ -971,9 +1070,8 @@ def run_llama70b(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
-def run_qwen7b(args, kvx, wl):
-    """64 requests with partial prefix hits: one batched load (stream A) and one batched
-    store (stream B) at the same time."""
+def qwen7b_setup(kvx, wl):
+    """Pool, page tables and host arenas of the 64-request batched partial-hit workload."""
     w = wl.qwen7b_batch()
     s = w.shape
     pools = _pool_tensor(s, w.seed, wl)
@@ -987,26 +1085,20 @@ def run_qwen7b(args, kvx, wl):
     st.array[:] = 0
     ch_ld = kvx.chunks_array(w.load_chunks, ld.ptr)
     ch_st = kvx.chunks_array(w.store_chunks, st.ptr)
-    ctx_a, ctx_b = kvx.kvx_create(0, 64 << 20), kvx.kvx_create(0, 64 << 20)
-    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
-    Nl, Ns = w.load_bytes(), w.store_bytes()
+    return w, pools, pool, dev_tables, reqs, ld, st, ch_ld, ch_st
 
-    def load():
-        kvx.kvx_load_chunks(ctx_a, pool, reqs, ch_ld, stream=sa.cuda_stream)
 
-    def store():
-        kvx.kvx_store_chunks(ctx_b, pool, reqs, ch_st, stream=sb.cuda_stream)
-
-    load_ms = _timed(sa, load, 5)
-    store_ms = _timed(sb, store, 5)
+def concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, sa, sb, cfg_l, cfg_s, reps):
+    """The batched load on stream sa and the batched store on stream sb, issued together:
+    median (load span, store span, both) in ms from a common start event."""
     spans = []
-    for rep in range(5):
+    for _ in range(reps):
         torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         start.record(sa)
         sb.wait_event(start)
-        load()
-        store()
+        kvx.kvx_load_chunks(ctx_a, pool, reqs, ch_ld, cfg=cfg_l, stream=sa.cuda_stream)
+        kvx.kvx_store_chunks(ctx_b, pool, reqs, ch_st, cfg=cfg_s, stream=sb.cuda_stream)
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ea.record(sa)
         eb.record(sb)
@@ -1014,47 +1106,132 @@ def run_qwen7b(args, kvx, wl):
         spans.append((start.elapsed_time(ea), start.elapsed_time(eb)))
     assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
     assert kvx.kvx_get_status(ctx_b, sb.cuda_stream) == 0
-    # The same two batches in one exchange launch.
-    xcfg = parse_cfg(kvx, ctx_a, kvx.KVX_OP_EXCHANGE, args.exchange_cfg)
-    x_ms = _timed(sa, lambda: kvx.kvx_exchange_chunks(ctx_a, pool, reqs, ch_st, reqs, ch_ld,
-                                                       cfg=xcfg, stream=sa.cuda_stream), 5)
-    assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
-    la = statistics.median(x[0] for x in spans)
-    sbm = statistics.median(x[1] for x in spans)
-    both = statistics.median(max(x) for x in spans)
-    # Bidirectional copy-engine peak for context: 4 GiB each way at once.
-    hp = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
-    hp2 = torch.empty(4 << 30, dtype=torch.uint8, pin_memory=True)
-    dp = torch.empty(4 << 30, dtype=torch.uint8, device="cuda")
-    dp2 = torch.empty(4 << 30, dtype=torch.uint8, device="cuda")
-    bid = []
-    for rep in range(4):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        with torch.cuda.stream(sa):
-            dp.copy_(hp, non_blocking=True)
-        with torch.cuda.stream(sb):
-            hp2.copy_(dp2, non_blocking=True)
-        torch.cuda.synchronize()
-        bid.append(time.perf_counter() - t0)
-    _emit({"workload": "qwen7b_batched_partial_hits", "requests": len(w.load_requests),
+    return (statistics.median(x[0] for x in spans), statistics.median(x[1] for x in spans),
+            statistics.median(max(x) for x in spans))
+
+
+def qwen7b_measure(args, kvx, wl, link, reps=5, partition_sms=16):
+    """Batched partial hits: the load batch and the store batch alone, on two plain streams
+    at once, on two streams of two I/O partitions (green contexts) at once, and in one
+    exchange launch; each against the bound max(load / H2D, store / D2H, both / bidir)."""
+    w, pools, pool, dev_tables, reqs, ld, st, ch_ld, ch_st = qwen7b_setup(kvx, wl)
+    ctx_a, ctx_b = kvx.kvx_create(0, 64 << 20), kvx.kvx_create(0, 64 << 20)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    Nl, Ns = w.load_bytes(), w.store_bytes()
+    bound_ms = max(Nl / (link["h2d"] * GB), Ns / (link["d2h"] * GB),
+                   (Nl + Ns) / (link["bidir"] * GB)) * 1e3
+    load_ms = _timed(sa, lambda: kvx.kvx_load_chunks(ctx_a, pool, reqs, ch_ld,
+                                                     stream=sa.cuda_stream), reps)
+    store_ms = _timed(sb, lambda: kvx.kvx_store_chunks(ctx_b, pool, reqs, ch_st,
+                                                       stream=sb.cuda_stream), reps)
+    la, sbm, both = concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, sa, sb,
+                                    None, None, reps)
+    out = {"workload": "qwen7b_batched_partial_hits", "requests": len(w.load_requests),
            "load_bytes": Nl, "store_bytes": Ns,
            "load_chunks": len(w.load_chunks), "store_chunks": len(w.store_chunks),
+           "bound_ms": round(bound_ms, 3),
+           "bound_note": "max(load / H2D, store / D2H, (load + store) / bidirectional) with "
+                         "this run's measured link peaks",
            "load_alone_gbs": round(Nl / (load_ms * 1e-3) / GB, 2),
            "store_alone_gbs": round(Ns / (store_ms * 1e-3) / GB, 2),
-           "concurrent_load_gbs": round(Nl / (la * 1e-3) / GB, 2),
-           "concurrent_store_gbs": round(Ns / (sbm * 1e-3) / GB, 2),
-           "concurrent_aggregate_gbs": round((Nl + Ns) / (both * 1e-3) / GB, 2),
-           "concurrent_ms": round(both, 3),
-           "exchange_one_launch_ms": round(x_ms, 3),
-           "exchange_one_launch_aggregate_gbs": round((Nl + Ns) / (x_ms * 1e-3) / GB, 2),
-           "model_exchange_ms": round(kvx.kvx_estimate_pair_us(
-               kvx.kvx_default_link_model(), kvx.KVX_OP_EXCHANGE, Ns, Nl, 0, xcfg) * 1e-3, 3),
-           "memcpy_bidirectional_gbs": round(2 * (4 << 30) / statistics.median(bid) / GB, 2)})
+           "two_streams": {"load_gbs": round(Nl / (la * 1e-3) / GB, 2),
+                           "store_gbs": round(Ns / (sbm * 1e-3) / GB, 2),
+                           "aggregate_gbs": round((Nl + Ns) / (both * 1e-3) / GB, 2),
+                           "ms": round(both, 3), "frac_of_bound": round(bound_ms / both, 4)}}
+    # Two I/O partitions, one per stream, so the two kernels run on fixed disjoint SM sets.
+    try:
+        part = kvx.kvx_partition_create(0, partition_sms, -1, 0, io_groups=2)
+    except kvx.KvxError as e:
+        out["two_partitions"] = {"unavailable": str(e)}
+        part = None
+    if part is not None:
+        pa = torch.cuda.ExternalStream(part.io_streams[0])
+        pb = torch.cuda.ExternalStream(part.io_streams[1])
+        cfg_l = kvx.kvx_default_launch_cfg(ctx_a, kvx.KVX_OP_LOAD)
+        cfg_s = kvx.kvx_default_launch_cfg(ctx_b, kvx.KVX_OP_STORE)
+        cfg_l.sm_cap = cfg_s.sm_cap = 0  # each partition bounds its kernel's SMs
+        la2, sb2, both2 = concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, pa, pb,
+                                          cfg_l, cfg_s, reps)
+        out["two_partitions"] = {"io_sms": list(part.io_sms_list),
+                                 "load_gbs": round(Nl / (la2 * 1e-3) / GB, 2),
+                                 "store_gbs": round(Ns / (sb2 * 1e-3) / GB, 2),
+                                 "aggregate_gbs": round((Nl + Ns) / (both2 * 1e-3) / GB, 2),
+                                 "ms": round(both2, 3),
+                                 "frac_of_bound": round(bound_ms / both2, 4)}
+        torch.cuda.synchronize()
+        part.close()
+    xcfg = parse_cfg(kvx, ctx_a, kvx.KVX_OP_EXCHANGE, getattr(args, "exchange_cfg", ""))
+    x_ms = _timed(sa, lambda: kvx.kvx_exchange_chunks(ctx_a, pool, reqs, ch_st, reqs, ch_ld,
+                                                       cfg=xcfg, stream=sa.cuda_stream), reps)
+    assert kvx.kvx_get_status(ctx_a, sa.cuda_stream) == 0
+    out["exchange_one_launch"] = {
+        "ms": round(x_ms, 3), "aggregate_gbs": round((Nl + Ns) / (x_ms * 1e-3) / GB, 2),
+        "frac_of_bound": round(bound_ms / x_ms, 4),
+        "model_ms": round(kvx.kvx_estimate_pair_us(kvx.kvx_default_link_model(),
+                                                   kvx.KVX_OP_EXCHANGE, Ns, Nl, 0,
+                                                   xcfg) * 1e-3, 3)}
     ld.close()
     st.close()
     kvx.kvx_destroy(ctx_a)
     kvx.kvx_destroy(ctx_b)
+    del pools
+    return out
+
+
+def measure_link(dev, stream, gib=4, reps=8):
+    """Best-of-reps pinned cudaMemcpyAsync rates: H2D, D2H, and both at once (GB/s)."""
+    n = gib << 30
+    link, samples = {}, {}
+    hp = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dp = torch.empty(n, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for name, fn in (("h2d", lambda: dp.copy_(hp, non_blocking=True)),
+                         ("d2h", lambda: hp.copy_(dp, non_blocking=True))):
+            for _ in range(2):
+                fn()
+            t = EventTimer(stream)
+            for _ in range(reps):
+                e = t.start()
+                fn()
+                t.stop(e)
+            stream.synchronize()
+            gbs = [n / (ms * 1e-3) / GB for ms in t.ms()]
+            link[name] = round(max(gbs), 1)
+            samples[name] = [round(x, 1) for x in gbs]
+    hp2 = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dp2 = torch.empty(n, dtype=torch.uint8, device=dev)
+    s2 = torch.cuda.Stream(device=dev)
+    bid = []
+    for rep in range(reps + 1):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        s2.wait_event(e0)
+        first, second = (stream, s2) if rep % 2 else (s2, stream)
+        with torch.cuda.stream(first):
+            (dp.copy_(hp, non_blocking=True) if first is stream else
+             hp2.copy_(dp2, non_blocking=True))
+        with torch.cuda.stream(second):
+            (dp.copy_(hp, non_blocking=True) if second is stream else
+             hp2.copy_(dp2, non_blocking=True))
+        e1, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e1.record(stream)
+        e2.record(s2)
+        torch.cuda.synchronize()
+        if rep:
+            ms = max(e0.elapsed_time(e1), e0.elapsed_time(e2))
+            bid.append(2 * n / (ms * 1e-3) / GB)
+    link["bidir"] = round(max(bid), 1)
+    samples["bidir"] = [round(x, 1) for x in bid]
+    return link, samples
+
+
+def run_qwen7b(args, kvx, wl):
+    """64 requests with partial prefix hits: one batched load and one batched store at the
+    same time, on two plain streams, on two I/O partitions, and in one exchange launch."""
+    link, _ = measure_link(torch.device("cuda", 0), torch.cuda.Stream(), reps=4)
+    _emit({**qwen7b_measure(args, kvx, wl, link, partition_sms=args.partition_sms_qwen),
+           "link_peaks_gbs": link})
 
 
 def run_mla_sweep(args, kvx, wl):
