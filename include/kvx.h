@@ -199,7 +199,8 @@ typedef struct kvx_ctx kvx_ctx;
 /* ---------------------------------------------------------------- context */
 
 /* Create a context on `device` whose descriptor buffers hold up to
- * max_descriptor_bytes each (0 = 8 MiB; about 72 bytes per chunk).  Allocates four
+ * max_descriptor_bytes each (0 = 8 MiB; 64 bytes per chunk, 16 per request, 8 per pool
+ * layer).  Allocates four
  * pinned host + device descriptor buffers, a device status word and a non-blocking stream
  * on which each call copies its descriptors (the caller's stream waits for that copy with
  * an event, so the copy overlaps the previous kernel).  Calls therefore cannot be captured
@@ -365,8 +366,8 @@ kvx_status kvx_last_launch(const kvx_ctx *ctx, int64_t *items, int32_t *ctas,
 /* ---------------------------------------------------------------- allocation-free load */
 
 /* Size of the fixed scratch array behind kvx_load_chunks_noalloc: a 256-byte status
- * header plus the packed descriptors (about 72 bytes per chunk, 16 per request, 8 per
- * pool layer), so roughly 14,000 chunks per call. */
+ * header plus the packed descriptors (64 bytes per chunk, 16 per request, 8 per pool
+ * layer, each group padded to 128 bytes), so about 16,000 chunks per call. */
 #define KVX_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 /* kvx_load_chunks without a context and without allocating anything.  The pages have no
@@ -382,17 +383,21 @@ kvx_status kvx_last_launch(const kvx_ctx *ctx, int64_t *items, int32_t *ctas,
  * memory.
  *
  * Runs on the calling thread's current device.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  Each call copies its descriptors into the array
- * (from a static host image; the copy call returns once it has read it), which also
- * clears the status word, then launches the load kernel on `stream`.  All calls share
- * the one array and it keeps the last call's contents: calls whose work overlaps on the
- * GPU (for example on two streams without ordering between them) race on it.  Issue
- * them on one stream, or order them with events.
+ * array's device address (cudaGetSymbolAddress) with that device current.  Each call
+ * copies its descriptors into the array (from a static host image; the copy call returns
+ * once it has read it), which also clears the status word, then launches the load kernel
+ * on `stream` with the launch shape kvx_load_chunks would use for the same cfg.  A stream
+ * that is capturing is refused with KVX_ERR_INVALID_ARG before anything is done: a
+ * captured copy would read the host image again at replay, when it holds another call's
+ * descriptors.  All calls share the one array and it keeps the last call's contents:
+ * calls whose work overlaps on the GPU (for example on two streams without ordering
+ * between them) race on it.  Issue them on one stream, or order them with events.
  *
- * Arguments are those of kvx_load_chunks (validation level 1 always).  device_flags,
- * if not NULL, is a 4-byte aligned device-accessible word that the kernel ORs
- * KVX_DEV_* bits into (the caller clears it); when NULL the bits are dropped. */
+ * Arguments are those of kvx_load_chunks (validation level 1 always; the warp-segment
+ * mapping only, without overlap).  device_flags, if not NULL, is a 4-byte aligned
+ * device-accessible word that the kernel ORs KVX_DEV_* bits into (the caller clears it);
+ * when NULL they go to the array's status word, which the next call clears, so they are
+ * dropped. */
 kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_request *reqs, int n_req,
                                    const kvx_chunk *chunks, int n_chunks, int layer_begin,
                                    int layer_end, const kvx_launch_cfg *cfg,

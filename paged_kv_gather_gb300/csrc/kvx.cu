@@ -1301,6 +1301,17 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
                                               const kvx_launch_cfg *cfg, kvx_stream_t stream,
                                               uint32_t *device_flags)
 {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The descriptor copy below reads a static host image that the next call overwrites; a
+    // capturing stream would record that copy and replay whatever the image then holds.
+    // Refuse it before doing anything.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) {
+        cudaGetLastError();
+        return KVX_ERR_CUDA;
+    }
+    if (capture != cudaStreamCaptureStatusNone)
+        return KVX_ERR_INVALID_ARG;
     kvx_launch_cfg c;
     kvx_status st = resolve_cfg(nullptr, KVX_OP_LOAD, cfg, &c);
     if (st != KVX_OK)
@@ -1321,11 +1332,13 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
         cudaGetLastError();
         return KVX_ERR_CUDA;
     }
-    int sms = 0;
-    if (c.sm_cap == 0 &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    // Launch-shape input only (no buffers, no stream): the device's SM count, so that the
+    // same cfg gives the same launch as kvx_load_chunks.
+    kvx_ctx shape_ctx;
+    shape_ctx.device = dev;
+    if (cudaDeviceGetAttribute(&shape_ctx.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+        cudaSuccess)
         return KVX_ERR_CUDA;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (!g_noalloc_addr[dev]) {
@@ -1344,20 +1357,14 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
                           reinterpret_cast<char *>(g_noalloc_stage) + kNoallocHeader,
                           dev_block + kNoallocHeader);
     plan.status = device_flags ? device_flags : reinterpret_cast<unsigned int *>(dev_block);
+    apply_batch(KVX_OP_LOAD, c, &plan);
+    choose_split(&shape_ctx, c, &plan);
     if (plan.total_items == 0)
         return KVX_OK;
     if (cudaMemcpyAsync(dev_block, g_noalloc_stage, kNoallocHeader + lay.total,
                         cudaMemcpyHostToDevice, s) != cudaSuccess)
         return KVX_ERR_CUDA;
-    const int64_t warps_per_cta = c.threads / 32;
-    int64_t ctas = int64_t(c.sm_cap > 0 ? c.sm_cap : sms) * c.ctas_per_sm;
-    const int64_t needed = (plan.total_items + warps_per_cta - 1) / warps_per_cta;
-    if (ctas > needed)
-        ctas = needed;
-    void *args[] = {&plan};
-    if (cudaLaunchKernel(reinterpret_cast<const void *>(pick_kernel(c.unroll, KVX_DIR_SCATTER,
-                                                                    c.store_hint, plan.batch)),
-                         dim3(unsigned(ctas)), dim3(unsigned(c.threads)), args, 0, s) !=
+    if (launch_kernel(launch_shape(&shape_ctx, c, plan, KVX_DIR_SCATTER), plan, s) !=
         cudaSuccess)
         return KVX_ERR_CUDA;
     return KVX_OK;
