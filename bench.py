@@ -77,7 +77,8 @@ def parse():
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
                    choices=["store", "load", "gather", "scatter", "exchange", "roundtrip",
-                            "exchange_shared", "gather_cta", "load_bulk"],
+                            "exchange_shared", "gather_cta", "load_bulk", "store_bulk",
+                            "load_4sm"],
                    help="operation of --workload profile_small")
     p.add_argument("--groups", type=int, default=16,
                    help="chunk groups of the pipelined store/load round trip")
@@ -106,6 +107,8 @@ def parse():
     p.add_argument("--layers", type=int, default=80, help="llama70b: layers streamed")
     p.add_argument("--priorities", default="-1,0",
                    help="llama70b: load stream priorities (-1 high, 0 normal)")
+    p.add_argument("--timeline", action="store_true",
+                   help="llama70b: per-layer event times of the loads and GEMMs")
     p.add_argument("--partition-sms", default="8,16",
                    help="llama70b: I/O partition sizes (green contexts) to run; empty: none")
     p.add_argument("--partition-sms-qwen", type=int, default=16,
@@ -504,7 +507,8 @@ def mla_legs(kvx, wl, link, pages=(1, 16), chunk_bytes=1 << 20, reps=3):
 def llama70b_legs(kvx, wl, n_layers=16, reps=2):
     """Layer streaming of the Llama-3.1-70B-shaped prefix over its first n_layers layers
     under one bf16 8192^3 GEMM per layer: the bulk mapping on 5 and 4 SMs and the register
-    mapping on its default 16 SMs, each on a high-priority load stream."""
+    mapping on its default 16 SMs, each on a high-priority load stream, and the register
+    mapping on a 16-SM green-context I/O partition beside the GEMMs' compute partition."""
     w, pools, pool, pt, reqs, arena, per_layer = llama70b_setup(kvx, wl, n_layers)
     ctx = kvx.kvx_create(0)
     sb = torch.cuda.Stream()
@@ -523,13 +527,29 @@ def llama70b_legs(kvx, wl, n_layers=16, reps=2):
         cfg = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, cap, mapping)
         out[name] = layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes,
                                     cfg, sa, sb, gemm, gemm_ms, reps)
+    # The loads on a 16-SM green-context I/O partition, the GEMMs on the other SMs.
+    try:
+        part = kvx.kvx_partition_create(0, 16, -1, 0)
+    except kvx.KvxError as e:
+        out["partition_16sm"] = {"unavailable": str(e)}
+        part = None
+    if part is not None:
+        sa = torch.cuda.ExternalStream(part.io_stream)
+        sc = torch.cuda.ExternalStream(part.compute_stream)
+        cfg = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, 0)
+        out["partition_16sm"] = {"io_sms": part.io_sms, "compute_sms": part.compute_sms,
+                                 **layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers,
+                                                   layer_bytes, cfg, sa, sc, gemm, gemm_ms,
+                                                   reps)}
+        torch.cuda.synchronize()
+        part.close()
     arena.close()
     kvx.kvx_destroy(ctx)
     del pools, A, B, C
     return out
 
 
-def flat_extras(seq, few, mla, qwen, l70, link):
+def flat_extras(seq, few, mla, qwen, l70, evict, link):
     """Scalar summaries of the extra legs, for the roofline object of the JSON line."""
     f = {"store_gbs": seq["store"]["gbs"], "store_frac": seq["store"]["frac"],
          "load_gbs": seq["load"]["gbs"], "load_frac": seq["load"]["frac"]}
@@ -548,11 +568,16 @@ def flat_extras(seq, few, mla, qwen, l70, link):
         if "frac_of_bound" in tp:
             f["cfg4_two_partitions_frac_of_bound"] = tp["frac_of_bound"]
     if l70:
-        for k in ("bulk_5sm", "bulk_4sm", "segment_16sm"):
+        for k in ("bulk_5sm", "bulk_4sm", "segment_16sm", "partition_16sm"):
             r = l70[k]
+            if "load_overlap_gbs" not in r:
+                continue
             f[f"cfg3_{k}_load_overlap_frac"] = round(r["load_overlap_gbs"] / link["h2d"], 4)
             f[f"cfg3_{k}_gemm_slowdown_pct"] = r["gemm_slowdown_pct"]
             f[f"cfg3_{k}_e2e_vs_model"] = r["e2e_vs_model"]
+    if evict:
+        f["eviction_1sm_store_gbs"] = evict["store_under_decode_gbs"]
+        f["eviction_1sm_decode_slowdown_pct"] = evict["decode_slowdown_pct"]
     return f
 
 
@@ -787,11 +812,13 @@ def run_ours(args):
            "load": {"ms": round(load_ms, 4), "gbs": round(load_gbs, 2),
                     "peak": link["h2d"], "frac": round(load_gbs / link["h2d"], 4),
                     "traffic": recorded_traffic("load", "llama8b")}}
-    few = mla = qwen = l70 = None
+    few = mla = qwen = l70 = evict = None
     extra_clocks = None
     if world == 1 and not args.no_extras:
         few = few_sm_legs(kvx, ctx, stream, pool, reqs_src, reqs_dst, chunks_host,
                           s.num_layers, N, link)
+        evict = eviction_leg(kvx, ctx, pool, reqs_src, chunks_host, s.num_layers, N, w.seed,
+                             caps=(1,))[0]
         del pools
         torch.cuda.empty_cache()
         with ClockSampler(local) as ec:
@@ -844,14 +871,16 @@ def run_ours(args):
                                     "gbs": round(launch_gbs, 2), "bytes_per_launch": 2 * N,
                                     "items_per_launch": items, "ctas": ctas,
                                     "threads": threads},
-                     **flat_extras(seq, few, mla, qwen, l70, link),
+                     **flat_extras(seq, few, mla, qwen, l70, evict, link),
                      "flat_note": "store_/load_: the request stored, then loaded, alone on "
                                   "one stream (library defaults) against the one-way peaks; "
                                   "sm4_: the same on 4 SMs; cfg3_/cfg4_/cfg5_: the 70B "
                                   "layer streaming, batched partial hits and MLA legs of "
-                                  "extra_workloads"},
+                                  "extra_workloads; eviction_: a 1-SM store under a decode "
+                                  "GEMV loop"},
         "extra_workloads": {"few_sms": few, "mla_latent": mla, "qwen7b_batched": qwen,
-                            "llama70b_layer_streaming": l70, "clocks": extra_clocks},
+                            "llama70b_layer_streaming": l70, "background_eviction": evict,
+                            "clocks": extra_clocks},
         "exchange_pipeline": exchange_pipeline,
         "sequential": seq,
         "cfg": {"roundtrip": cfg_rt.as_dict(), "store": cfg_store.as_dict(),
@@ -923,10 +952,12 @@ def io_cfg(kvx, ctx, op, cap, mapping="segment", stages=0, stage_bytes=0):
 
 
 def layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes, cfg, io_stream,
-                    gemm_stream, gemm, gemm_alone_ms, reps=2):
+                    gemm_stream, gemm, gemm_alone_ms, reps=2, timeline=False):
     """Per-layer loads on io_stream; GEMM(l) on gemm_stream once load(l) is done (an event).
     Returns load GB/s alone and overlapped, the GEMM's mean time beside the loads against
-    gemm_alone_ms, end to end, and the I/O-time model's prediction for the same launches."""
+    gemm_alone_ms, end to end, and the I/O-time model's prediction for the same launches.
+    timeline: also the last repetition's per-layer event times (ms from its start) of each
+    load (its stream reaching the call, the load's end) and each GEMM (start, end)."""
     io_h = io_stream.cuda_stream
 
     def load_all():
@@ -942,8 +973,11 @@ def layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes, cfg,
         start.record(io_stream)
         gemm_stream.wait_event(start)
         gt = EventTimer(gemm_stream)
+        lt = EventTimer(io_stream)
         for l in range(n_layers):
+            e_l = lt.start()
             kvx.kvx_load_chunks(ctx, pool, reqs, per_layer[l], l, l + 1, cfg, io_h)
+            lt.stop(e_l)
             ev = torch.cuda.Event()
             ev.record(io_stream)
             gemm_stream.wait_event(ev)
@@ -959,6 +993,13 @@ def layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes, cfg,
         spans.append(start.elapsed_time(end_a))
         e2es.append(start.elapsed_time(end_b))
         gms.append(statistics.mean(gt.ms()))
+        if timeline:
+            rows = [{"layer": l,
+                     "load_start_ms": round(start.elapsed_time(a), 4),
+                     "load_end_ms": round(start.elapsed_time(b), 4),
+                     "gemm_start_ms": round(start.elapsed_time(c), 4),
+                     "gemm_end_ms": round(start.elapsed_time(d), 4)}
+                    for l, ((a, b), (c, d)) in enumerate(zip(lt.pairs, gt.pairs))]
     assert kvx.kvx_get_status(ctx, io_h) == 0
     g_ms = statistics.median(gms)
     model = kvx.kvx_default_link_model()
@@ -968,7 +1009,29 @@ def layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes, cfg,
     meas_e2e, _ = kvx.kvx_estimate_stream_us(alone_ms * 1e3 / n_layers, gemm_alone_ms * 1e3,
                                              n_layers)
     e2e = statistics.median(e2es)
-    return {"layers": n_layers, "layer_bytes": layer_bytes,
+    out = {}
+    if timeline:
+        med = lambda xs: round(statistics.median(xs), 4)  # noqa: E731
+        out["timeline"] = {
+            "layers": rows,
+            "load_ms_median": med([r["load_end_ms"] - r["load_start_ms"] for r in rows]),
+            "gemm_ms_median": med([r["gemm_end_ms"] - r["gemm_start_ms"] for r in rows]),
+            # how long after its load ended each GEMM started, and the GEMM's share of the
+            # next layer's load window spent beside it
+            "gemm_start_after_load_end_ms_median":
+                med([r["gemm_start_ms"] - r["load_end_ms"] for r in rows]),
+            "gemm_overlap_of_next_load_median":
+                med([max(0.0, min(rows[i]["gemm_end_ms"], rows[i + 1]["load_end_ms"]) -
+                         max(rows[i]["gemm_start_ms"], rows[i + 1]["load_start_ms"])) /
+                     (rows[i + 1]["load_end_ms"] - rows[i + 1]["load_start_ms"])
+                     for i in range(len(rows) - 1)] or [0.0]),
+            "load_gap_between_layers_ms_median":
+                med([rows[i + 1]["load_start_ms"] - rows[i]["load_end_ms"]
+                     for i in range(len(rows) - 1)] or [0.0]),
+            "compute_idle_ms": round(rows[0]["gemm_start_ms"] + sum(
+                max(0.0, rows[i + 1]["gemm_start_ms"] - rows[i]["gemm_end_ms"])
+                for i in range(len(rows) - 1)), 4)}
+    return {**out, "layers": n_layers, "layer_bytes": layer_bytes,
             "load_cfg": cfg.as_dict(),
             "load_alone_ms": round(alone_ms, 3),
             "load_alone_gbs": round(total / (alone_ms * 1e-3) / GB, 2),
@@ -1036,7 +1099,7 @@ def run_llama70b(args, kvx, wl):
         cfg = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, cap, args.mapping, args.stages,
                      args.stage_bytes)
         r = layer_streaming(kvx, ctx, pool, reqs, per_layer, s.num_layers, layer_bytes, cfg,
-                            sa, sb, gemm, gemm_ms)
+                            sa, sb, gemm, gemm_ms, timeline=args.timeline)
         _emit({"workload": "llama70b_layer_streaming", "chunk_tokens": args.chunk_tokens,
                "mapping": args.mapping, "sm_cap": cap,
                "load_stream_priority": "high" if prio < 0 else "normal", **r})
@@ -1059,7 +1122,7 @@ def run_llama70b(args, kvx, wl):
 
         g_part = _timed(sc, gemm_c, 20, warm=5)
         r = layer_streaming(kvx, ctx, pool, reqs, per_layer, s.num_layers, layer_bytes, cfg,
-                            sa, sc, gemm, gemm_ms)
+                            sa, sc, gemm, gemm_ms, timeline=args.timeline)
         _emit({"workload": "llama70b_layer_streaming", "chunk_tokens": args.chunk_tokens,
                "mapping": args.mapping, "partition": "green contexts",
                "io_sms": part.io_sms, "compute_sms": part.compute_sms,
@@ -1512,26 +1575,14 @@ def run_mla_blocks(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
-def run_eviction(args, kvx, wl):
-    """Background eviction: the llama8b request stored to host memory by a 1-, 2- or 4-SM
-    kernel on a low-priority stream while a decode-like, HBM-bound bf16 GEMV loop runs on
-    a high-priority stream; decode step time alone vs with the eviction running."""
-    w = wl.llama8b()
-    s = w.shape
-    pools = _pool_tensor(s, w.seed, wl)
-    pool = kvx.Pool.from_tensor(pools, s.page_size)
-    src = w.store_requests[0]
-    ps = torch.from_numpy(src.page_table).cuda()
-    rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
-    arena = kvx.HostBuffer(w.store_arena_bytes)
-    arena.array[:] = 0
-    ch = kvx.chunks_array(w.store_chunks, arena.ptr)
-    ctx = kvx.kvx_create(0)
-    N = w.store_bytes()
+def eviction_leg(kvx, ctx, pool, rs, ch, num_layers, N, seed, caps=(1, 2, 4)):
+    """Background eviction: a store of the request by a 1-, 2- or 4-SM kernel on a
+    low-priority stream while a decode-like, HBM-bound bf16 GEMV loop runs on a
+    high-priority stream; decode step time alone vs with the eviction running."""
     low = torch.cuda.Stream(priority=0)
     high = torch.cuda.Stream(priority=-1)
     g = torch.Generator(device="cuda")
-    g.manual_seed(w.seed)
+    g.manual_seed(seed)
     Wm = torch.randn(16384, 32768, device="cuda", dtype=torch.bfloat16, generator=g)  # 1 GiB
     x = torch.randn(32768, 1, device="cuda", dtype=torch.bfloat16, generator=g)
     y = torch.empty(16384, 1, device="cuda", dtype=torch.bfloat16)
@@ -1549,19 +1600,20 @@ def run_eviction(args, kvx, wl):
     e1.record(high)
     torch.cuda.synchronize()
     step_alone = e0.elapsed_time(e1) / 200
-    for cap in (1, 2, 4):
+    rows = []
+    for cap in caps:
         cfg = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_STORE)
         cfg.sm_cap = cap
         cfg.store_hint = kvx.KVX_HINT_DEFAULT
         # Store alone on the low-priority stream.
-        st_ms = _timed(low, lambda: kvx.kvx_store_chunks(ctx, pool, rs, ch, 0, s.num_layers,
+        st_ms = _timed(low, lambda: kvx.kvx_store_chunks(ctx, pool, rs, ch, 0, num_layers,
                                                          cfg, low.cuda_stream), 2, 1)
         n_steps = max(50, int(st_ms / step_alone))
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(low)
-        kvx.kvx_store_chunks(ctx, pool, rs, ch, 0, s.num_layers, cfg, low.cuda_stream)
+        kvx.kvx_store_chunks(ctx, pool, rs, ch, 0, num_layers, cfg, low.cuda_stream)
         a1.record(low)
         d0.record(high)
         decode(n_steps)
@@ -1569,14 +1621,34 @@ def run_eviction(args, kvx, wl):
         torch.cuda.synchronize()
         assert kvx.kvx_get_status(ctx, low.cuda_stream) == 0
         step_with = d0.elapsed_time(d1) / n_steps
-        _emit({"workload": "background_eviction", "sm_cap": cap,
-               "store_alone_gbs": round(N / (st_ms * 1e-3) / GB, 2),
-               "store_under_decode_gbs": round(N / (a0.elapsed_time(a1) * 1e-3) / GB, 2),
-               "decode_step_alone_ms": round(step_alone, 4),
-               "decode_step_with_eviction_ms": round(step_with, 4),
-               "decode_slowdown_pct": round(100 * (step_with / step_alone - 1), 2),
-               "decode_steps": n_steps,
-               "decode_gemv": "bf16 [16384 x 32768] x [32768], 1 GiB of weights per step"})
+        rows.append({"workload": "background_eviction", "sm_cap": cap,
+                     "store_alone_gbs": round(N / (st_ms * 1e-3) / GB, 2),
+                     "store_under_decode_gbs": round(N / (a0.elapsed_time(a1) * 1e-3) / GB, 2),
+                     "decode_step_alone_ms": round(step_alone, 4),
+                     "decode_step_with_eviction_ms": round(step_with, 4),
+                     "decode_slowdown_pct": round(100 * (step_with / step_alone - 1), 2),
+                     "decode_steps": n_steps,
+                     "decode_gemv": "bf16 [16384 x 32768] x [32768], 1 GiB of weights per "
+                                    "step"})
+    del Wm, x, y
+    return rows
+
+
+def run_eviction(args, kvx, wl):
+    """Background eviction of the llama8b request under a decode-like GEMV loop."""
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pool_tensor(s, w.seed, wl)
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    src = w.store_requests[0]
+    ps = torch.from_numpy(src.page_table).cuda()
+    rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+    arena = kvx.HostBuffer(w.store_arena_bytes)
+    arena.array[:] = 0
+    ch = kvx.chunks_array(w.store_chunks, arena.ptr)
+    ctx = kvx.kvx_create(0)
+    for row in eviction_leg(kvx, ctx, pool, rs, ch, s.num_layers, w.store_bytes(), w.seed):
+        _emit(row)
     arena.close()
     kvx.kvx_destroy(ctx)
 
@@ -1596,7 +1668,7 @@ def run_profile_small(args, kvx, wl):
     ctx = kvx.kvx_create(0)
     sh = torch.cuda.current_stream().cuda_stream
     if args.profile_op in ("store", "load", "exchange", "roundtrip", "exchange_shared",
-                           "load_bulk"):
+                           "load_bulk", "store_bulk", "load_4sm"):
         buf = kvx.HostBuffer(w.store_arena_bytes)
         buf.array[:] = 0
         ch = kvx.chunks_array(w.store_chunks, buf.ptr)
@@ -1611,9 +1683,14 @@ def run_profile_small(args, kvx, wl):
             q = len(w.store_chunks) // 4
             kvx.kvx_exchange_chunks(ctx, pool, rs, np.ascontiguousarray(ch[:q]), rd,
                                     np.ascontiguousarray(ch[q:]), stream=sh)
-        elif args.profile_op == "load_bulk":  # the load, bulk-copy staging mapping
-            c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD)
-            c.mapping, c.unroll, c.stage_bytes = kvx.KVX_MAP_BULK, 6, 32768
+        elif args.profile_op == "load_bulk":  # the load, bulk-copy mapping on 4 SMs
+            c = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, 4, "bulk", 3, 32768)
+            kvx.kvx_load_chunks(ctx, pool, rd, ch, cfg=c, stream=sh)
+        elif args.profile_op == "store_bulk":  # the store, bulk-copy mapping on 4 SMs
+            c = io_cfg(kvx, ctx, kvx.KVX_OP_STORE, 4, "bulk", 6, 16384)
+            kvx.kvx_store_chunks(ctx, pool, rs, ch, cfg=c, stream=sh)
+        elif args.profile_op == "load_4sm":  # the load, register mapping on 4 SMs
+            c = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, 4)
             kvx.kvx_load_chunks(ctx, pool, rd, ch, cfg=c, stream=sh)
         elif args.profile_op == "gather_cta":  # the HBM gather, CTA-per-segment mapping
             c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_GATHER_HBM)
