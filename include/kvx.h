@@ -420,11 +420,14 @@ kvx_status kvx_plan_count(const kvx_pool *pool, const kvx_request *reqs, int n_r
                           const kvx_chunk *chunks, int n_chunks, int layer_begin,
                           int layer_end, int64_t *n_segments, int64_t *n_bytes);
 
-/* Chunk-size policy: tokens and layers per chunk for a request's KV.
- * layer_streaming != 0 asks for per-layer chunks (one layer per chunk, for transfers
- * issued layer by layer); otherwise chunks hold all layers (page-first).  target_bytes
- * is the wanted chunk size, 0 = the library default.  tokens_per_chunk is always a
- * positive multiple of page_size, so no chunk boundary splits a page. */
+/* Chunk-size policy: tokens and layers per chunk for a request's KV ("Strata Guide",
+ * section "The Physics of I/O Bandwidth and Little's Law": transfers of 1-4 MB are what
+ * saturate a host link, where one page per layer is kilobytes).  layer_streaming != 0
+ * asks for per-layer chunks (one layer per chunk, for transfers issued layer by layer);
+ * otherwise chunks hold all layers (page-first).  target_bytes is the wanted chunk size,
+ * for instance a storage tier's preferred I/O size; 0 = the library default, 2 MiB.
+ * tokens_per_chunk is the largest positive multiple of page_size whose chunk fits
+ * target_bytes (one page when even that does not), so no chunk boundary splits a page. */
 kvx_status kvx_chunk_policy(const kvx_pool *pool, int layer_streaming, int64_t target_bytes,
                             int32_t *tokens_per_chunk, int32_t *layers_per_chunk);
 
