@@ -351,6 +351,79 @@ def test_bulk_mapping_multi_tile_ragged(ctx, stream, stages, stage_bytes, ctas):
         arena.close()
 
 
+@pytest.mark.parametrize("table", ["consecutive", "random"])
+def test_bulk_mapping_piece_cap_and_merged_runs(ctx, stream, table):
+    """The bulk mapping's two packing rules against the oracle.  16-byte tokens in
+    token-major chunks make every row its own piece, so each 32 KiB stage closes at its
+    32-piece cap long before it is full.  Pages placed back to back in the pool
+    ("consecutive") let pieces of neighbouring page segments merge into one bulk copy on the
+    page side, while layer-major chunks merge them on the chunk side."""
+    rng = np.random.default_rng(4242 if table == "random" else 4343)
+    L, KV, P, v = 2, 2, 8, 16
+    lens = [600, 77]
+    pages = [-(-n // P) for n in lens]
+    NP = 2 * sum(pages) + 5
+    order = np.arange(NP, dtype=np.int32) if table == "consecutive" else \
+        rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(order[at:at + npg].copy())
+        t_dst.append(order[at + sum(pages):at + sum(pages) + npg].copy())
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, 256, 0, L, wl.TOKEN_MAJOR if r == 0 else
+                                 wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    c = bulk(2, 1, 3, 32768)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    for op_s, op_l, where in (("store", "load", "host"), ("gather", "scatter", "device")):
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        dpool.fill_random(17)
+        arena = Arena(nbytes, where)
+        _store(ctx, op_s, dpool, src, specs, arena, 0, None, c, stream)
+        assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), op_s)
+        data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+        arena.write(data)
+        pre = dpool.host_copy()
+        _load(ctx, op_l, dpool, dst, specs, arena, 0, None, c, stream)
+        assert_pool_equal(dpool, expected_load(pre, dst, specs, data.copy()))
+        arena.close()
+
+
+def test_random_bulk_shapes(ctx, stream):
+    """60 random batches under random bulk-mapping shapes (SM cap, CTAs per SM, stages per
+    ring, stage size), store then load through host memory or gather then scatter in HBM."""
+    for seed in range(60):
+        rng = np.random.default_rng(77000 + seed)
+        shape, lens, tables, load_tables, specs, lb, le = random_case(rng)
+        L, KV, P, v, NP = (shape.num_layers, shape.kv_factor, shape.page_size,
+                           shape.token_bytes, shape.num_pages)
+        stages = int(rng.integers(2, 9))
+        max_units = (208 * 1024) // (2 * stages * 16)
+        stage_bytes = 16 * int(rng.integers(1, max_units + 1))
+        c = bulk(int(rng.integers(0, 7)), int(rng.integers(1, 3)), stages, stage_bytes)
+        nbytes = wl._arena_bytes(specs, shape)
+        src, dst = Requests(tables, lens), Requests(load_tables, lens)
+        op_s, op_l, where = (("store", "load", "host") if seed % 2 == 0 else
+                             ("gather", "scatter", "device"))
+        dpool = DevicePool.empty(L, KV, NP, P, v)
+        dpool.fill_random(seed + 5)
+        arena = Arena(nbytes, where)
+        what = f"seed {seed} cfg {c.as_dict()}"
+        _store(ctx, op_s, dpool, src, specs, arena, lb, le, c, stream)
+        assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes, lb, le),
+                           what)
+        data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+        arena.write(data)
+        pre = dpool.host_copy()
+        _load(ctx, op_l, dpool, dst, specs, arena, lb, le, c, stream)
+        assert_pool_equal(dpool, expected_load(pre, dst, specs, data.copy(), lb, le))
+        arena.close()
+
+
 def test_bulk_mapping_rejects_bad_stage_shapes(ctx, stream):
     dpool = DevicePool.empty(1, 1, 4, 1, 16)
     reqs = Requests([np.array([0], np.int32)], [1])
