@@ -1,12 +1,15 @@
-"""GPU parity at the full sizes of the five workloads, in the launch configuration the bench
-uses (the library defaults), every output byte checked against the CPU oracle.
+"""GPU parity at the full sizes of the five workloads, in the launch configurations the bench
+times (the library defaults, and the few-SM and partition legs), every output byte checked
+against the CPU oracle.
 
 Verification copies device tensors into pinned host memory and runs the oracle on them:
   llama8b       store, load, HBM gather/scatter and the per-page DMA baseline, all layers;
                 the headline round trip in one launch, and the exchange pipeline;
-  llama70b      80 layer-streamed loads, 1 MiB and 2 MiB per-layer chunks, every layer;
-  qwen7b_batch  one batched load and one batched store concurrently on two streams, and
-                both in one exchange launch;
+  llama8b       also the store and load on 4 SMs, bulk and register mappings;
+  llama70b      80 layer-streamed loads, 1 MiB and 2 MiB per-layer chunks, every layer, and
+                with the bulk mapping on 5 SMs;
+  qwen7b_batch  one batched load and one batched store concurrently on two streams (plain,
+                or two I/O partitions), and both in one exchange launch;
   mla_sweep     every page size x chunk size cell, store and load, kernel and DMA baseline;
   mla_blocks    per-block STRIPED objects: one store, then per-layer loads.
 """
@@ -209,10 +212,60 @@ def test_llama8b_roundtrip_in_one_launch_as_benchmarked(ctx):
 
 # ----------------------------------------------------------------------------- llama70b
 
-@pytest.mark.parametrize("tokens_per_chunk", [256, 512])
-def test_llama70b_layer_streamed_load_full_size(ctx, tokens_per_chunk):
+def _io_cfg(ctx, op, cap, mapping=None, stages=0, stage_bytes=0):
+    c = kvx.kvx_default_launch_cfg(ctx, op)
+    c.sm_cap = cap
+    if mapping is not None:
+        c.mapping, c.threads, c.unroll, c.stage_bytes = mapping, 0, stages, stage_bytes
+    return c
+
+
+@pytest.mark.parametrize("mapping", ["bulk", "segment"])
+def test_llama8b_store_and_load_on_4_sms_as_benchmarked(ctx, mapping):
+    """The full request stored and loaded on 4 SMs, in the launch configurations the bench's
+    4-SM legs time: the bulk mapping (store: two rings of 6 x 16 KiB, load: 3 x 32 KiB) and
+    the register mapping capped to 4 SMs."""
+    w = wl.llama8b()
+    s = w.shape
+    pools = _pools(s, w.seed)
+    hp = HostPool(pools, s.page_size)
+    src, dst = _requests(w.store_requests), _requests(w.load_requests)
+    nbytes = w.store_arena_bytes
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    if mapping == "bulk":
+        cs = _io_cfg(ctx, kvx.KVX_OP_STORE, 4, kvx.KVX_MAP_BULK, 6, 16384)
+        cl = _io_cfg(ctx, kvx.KVX_OP_LOAD, 4, kvx.KVX_MAP_BULK, 3, 32768)
+    else:
+        cs = _io_cfg(ctx, kvx.KVX_OP_STORE, 4)
+        cl = _io_cfg(ctx, kvx.KVX_OP_LOAD, 4)
+    arena = kvx.HostBuffer(nbytes + 4096)
+    arena.array[:] = CANARY
+    pool = kvx.Pool.from_tensor(pools, s.page_size)
+    torch.cuda.synchronize()
+    kvx.kvx_store_chunks(ctx, pool, src.array, kvx.chunks_array(w.store_chunks, arena.ptr), 0,
+                         s.num_layers, cs, sh)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    expect = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(hp.pool, src.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
+    assert_bytes_equal(arena.array, expect, f"llama8b store, {mapping}, 4 SMs")
+    kvx.kvx_load_chunks(ctx, pool, dst.array, kvx.chunks_array(w.load_chunks, arena.ptr), 0,
+                        s.num_layers, cl, sh)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    oracle.load(hp.pool, dst.oracle(), oracle_chunks(w.load_chunks, arena.array), threads=16)
+    _compare_pool(pools, hp.pool, f"llama8b load, {mapping}, 4 SMs")
+    arena.close()
+    hp.close()
+
+
+@pytest.mark.parametrize("tokens_per_chunk,mapping", [(256, None), (512, None),
+                                                      (256, "bulk")])
+def test_llama70b_layer_streamed_load_full_size(ctx, tokens_per_chunk, mapping):
     """80 per-layer loads on a high-priority stream, as the streamed prefill issues them;
-    per-layer chunks of 256 tokens (1 MiB, the closed form) and of 512 tokens (2 MiB)."""
+    per-layer chunks of 256 tokens (1 MiB, the closed form) and of 512 tokens (2 MiB); and
+    the bulk mapping on 5 SMs that the bench streams beside GEMMs."""
     w = wl.llama70b(tokens_per_chunk=tokens_per_chunk)
     s = w.shape
     assert w.load_bytes() == 20 << 30
@@ -226,8 +279,11 @@ def test_llama70b_layer_streamed_load_full_size(ctx, tokens_per_chunk):
     arrays = [kvx.chunks_array(cs, arena.ptr) for cs in per_layer]
     stream = torch.cuda.Stream(priority=-1)
     pool = kvx.Pool.from_tensor(pools, s.page_size)
+    cfg = None if mapping is None else _io_cfg(ctx, kvx.KVX_OP_LOAD, 5, kvx.KVX_MAP_BULK)
+    torch.cuda.synchronize()
     for l in range(s.num_layers):
-        kvx.kvx_load_chunks(ctx, pool, dst.array, arrays[l], l, l + 1, stream=stream.cuda_stream)
+        kvx.kvx_load_chunks(ctx, pool, dst.array, arrays[l], l, l + 1, cfg,
+                            stream=stream.cuda_stream)
     stream.synchronize()
     assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
     exp_layer = [np.empty((s.num_pages, s.page_size, s.token_bytes), np.uint8) for _ in range(2)]
@@ -247,7 +303,10 @@ def test_llama70b_layer_streamed_load_full_size(ctx, tokens_per_chunk):
 
 # ----------------------------------------------------------------------------- qwen7b_batch
 
-def test_qwen7b_batched_concurrent_load_and_store_full_size(ctx):
+@pytest.mark.parametrize("placement", ["streams", "partitions"])
+def test_qwen7b_batched_concurrent_load_and_store_full_size(ctx, placement):
+    """The batched load and store at once on two plain streams, or on the streams of two
+    16-SM I/O partitions (green contexts), as the bench measures them."""
     w = wl.qwen7b_batch()
     s = w.shape
     pools = _pools(s, w.seed)
@@ -259,18 +318,31 @@ def test_qwen7b_batched_concurrent_load_and_store_full_size(ctx):
     st = kvx.HostBuffer(w.store_arena_bytes + 4096)
     st.array[:] = CANARY
     ctx2 = kvx.kvx_create(0, 64 << 20)  # one context per concurrent stream
+    part = None
     try:
-        sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+        cl = cs = None
+        if placement == "partitions":
+            part = kvx.kvx_partition_create(0, 16, -1, 0, io_groups=2)
+            sa = torch.cuda.ExternalStream(part.io_streams[0])
+            sb = torch.cuda.ExternalStream(part.io_streams[1])
+            cl = _io_cfg(ctx, kvx.KVX_OP_LOAD, 0)  # each partition bounds its kernel's SMs
+            cs = _io_cfg(ctx2, kvx.KVX_OP_STORE, 0)
+        else:
+            sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
         pool = kvx.Pool.from_tensor(pools, s.page_size)
+        torch.cuda.synchronize()
         kvx.kvx_load_chunks(ctx, pool, reqs.array, kvx.chunks_array(w.load_chunks, ld.ptr),
-                            stream=sa.cuda_stream)
+                            cfg=cl, stream=sa.cuda_stream)
         kvx.kvx_store_chunks(ctx2, pool, reqs.array, kvx.chunks_array(w.store_chunks, st.ptr),
-                             stream=sb.cuda_stream)
+                             cfg=cs, stream=sb.cuda_stream)
         torch.cuda.synchronize()
         assert kvx.kvx_get_status(ctx, sa.cuda_stream) == 0
         assert kvx.kvx_get_status(ctx2, sb.cuda_stream) == 0
     finally:
         kvx.kvx_destroy(ctx2)
+        if part is not None:
+            torch.cuda.synchronize()
+            part.close()
     expect = np.full(w.store_arena_bytes + 4096, CANARY, np.uint8)
     oracle.store(host_pool, reqs.oracle(), oracle_chunks(w.store_chunks, expect), threads=16)
     assert_bytes_equal(st.array, expect, "qwen7b batched store")
