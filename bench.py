@@ -506,7 +506,7 @@ def mla_legs(kvx, wl, link, pages=(1, 16), chunk_bytes=1 << 20, reps=3):
 
 def llama70b_legs(kvx, wl, n_layers=16, reps=2):
     """Layer streaming of the Llama-3.1-70B-shaped prefix over its first n_layers layers
-    under one bf16 8192^3 GEMM per layer: the bulk mapping on 5 and 4 SMs and the register
+    under one bf16 8192^3 GEMM per layer: the bulk mapping on 6, 5 and 4 SMs and the register
     mapping on its default 16 SMs, each on a high-priority load stream, and the register
     mapping on a 16-SM green-context I/O partition beside the GEMMs' compute partition."""
     w, pools, pool, pt, reqs, arena, per_layer = llama70b_setup(kvx, wl, n_layers)
@@ -521,8 +521,8 @@ def llama70b_legs(kvx, wl, n_layers=16, reps=2):
     with torch.cuda.stream(sb):
         gemm_ms = _timed(sb, gemm, 20, warm=5)
     out = {"layers": n_layers, "layer_bytes": layer_bytes, "gemm_alone_ms": round(gemm_ms, 4)}
-    for name, mapping, cap in (("bulk_5sm", "bulk", 5), ("bulk_4sm", "bulk", 4),
-                               ("segment_16sm", "segment", 16)):
+    for name, mapping, cap in (("bulk_6sm", "bulk", 6), ("bulk_5sm", "bulk", 5),
+                               ("bulk_4sm", "bulk", 4), ("segment_16sm", "segment", 16)):
         sa = torch.cuda.Stream(priority=-1)
         cfg = io_cfg(kvx, ctx, kvx.KVX_OP_LOAD, cap, mapping)
         out[name] = layer_streaming(kvx, ctx, pool, reqs, per_layer, n_layers, layer_bytes,
@@ -568,7 +568,7 @@ def flat_extras(seq, few, mla, qwen, l70, evict, link):
         if "frac_of_bound" in tp:
             f["cfg4_two_partitions_frac_of_bound"] = tp["frac_of_bound"]
     if l70:
-        for k in ("bulk_5sm", "bulk_4sm", "segment_16sm", "partition_16sm"):
+        for k in ("bulk_6sm", "bulk_5sm", "bulk_4sm", "segment_16sm", "partition_16sm"):
             r = l70[k]
             if "load_overlap_gbs" not in r:
                 continue
