@@ -22,7 +22,13 @@ Also measured in the same run and printed on the same JSON line:
   cpu_baseline       the CPU oracle on a bounded sample of the same workload, all host cores
                      and one;
   e2e                the same step timed on the host clock through the C ABI, with the page
-                     tables uploaded from pinned host memory and the status word read back.
+                     tables uploaded from pinned host memory and the status word read back;
+  extra_workloads    after the timed region, on one GPU: the same store and load on 4 SMs
+                     (bulk-copy and register mappings); the MLA latent at 1- and 16-token
+                     pages; the batched partial hits (two streams, two I/O partitions, one
+                     exchange launch); 16 layers of the 70B-shaped layer streaming under
+                     GEMMs; a 1-SM background eviction under a decode GEMV loop.  Scalar
+                     summaries of these also sit in the roofline object.
 
 --workload selects the other measurement modes (layer streaming, batched partial hits, the
 MLA sweeps, launch-shape sweeps, transfer sizes, the round trip beside GEMMs, background
