@@ -56,3 +56,34 @@ def test_committed_traffic_records_name_a_source_hash():
         assert len(f["source_sha"]) == 16 and int(f["dram_bytes_per_launch"]) > 0
         kernels.add(f["kernel"])
     assert {"store", "load", "transform_gather", "transform_scatter", "roundtrip"} <= kernels
+
+
+def test_flat_extras_are_scalars_named_for_their_leg():
+    """The extra legs' summaries go into the JSON line's roofline object, where a parser
+    that keeps only scalar fields must still find them: every value is a number."""
+    link = {"h2d": 211.6, "d2h": 193.7, "bidir": 343.1}
+    seq = {"store": {"gbs": 193.0, "frac": 0.996}, "load": {"gbs": 211.0, "frac": 0.997}}
+    few = {k: {"gbs": 200.0, "frac": 0.95, "cfg": {"sm_cap": 4}}
+           for k in ("load_bulk", "store_bulk", "load_segment", "store_segment")}
+    mla = {"p1": {"store_frac": 0.96, "load_frac": 0.99},
+           "p16": {"store_frac": 0.99, "load_frac": 0.99}}
+    qwen = {"bound_ms": 51.0, "exchange_one_launch": {"frac_of_bound": 0.978},
+            "two_streams": {"frac_of_bound": 0.93},
+            "two_streams_store_8sm": {"frac_of_bound": 0.975},
+            "two_partitions": {"unavailable": "no green contexts"}}
+    leg = {"load_overlap_gbs": 200.0, "gemm_slowdown_pct": 3.5, "e2e_vs_model": 1.02}
+    l70 = {"bulk_6sm": leg, "bulk_5sm": leg, "bulk_4sm": leg, "segment_16sm": leg,
+           "partition_16sm": {"unavailable": "no green contexts"}}
+    evict = {"store_under_decode_gbs": 42.4, "decode_slowdown_pct": 0.8}
+    f = bench.flat_extras(seq, few, mla, qwen, l70, evict, link)
+    assert f and all(isinstance(v, (int, float)) for v in f.values())
+    assert f["store_frac"] == 0.996 and f["load_frac"] == 0.997
+    assert f["sm4_load_bulk_frac"] == 0.95 and f["cfg5_mla_p1_store_frac"] == 0.96
+    assert f["cfg4_exchange_frac_of_bound"] == 0.978
+    assert "cfg4_two_partitions_frac_of_bound" not in f  # an unavailable leg is left out
+    assert f["cfg3_bulk_5sm_load_overlap_frac"] == round(200.0 / 211.6, 4)
+    assert "cfg3_partition_16sm_gemm_slowdown_pct" not in f
+    assert f["eviction_1sm_decode_slowdown_pct"] == 0.8
+    # Without the extra legs only the per-direction figures remain.
+    assert set(bench.flat_extras(seq, None, None, None, None, None, link)) == {
+        "store_gbs", "store_frac", "load_gbs", "load_frac"}
