@@ -2,9 +2,10 @@
  * roundtrip_gpu.c -- a plain C99 user of the library on the GPU, with no Python and no
  * torch: device pools from cudaMalloc, chunks from kvx_host_alloc, one kvx_roundtrip_chunks
  * (store the request's pages into host chunks, load them into other pages, one launch),
- * then one kvx_transform_hbm gather of the loaded pages into device chunks.  Every byte of
- * the chunks and of the pools is compared with the CPU oracle (oracle/kv_oracle.c, compiled
- * into this test program), run on host copies of the same inputs.
+ * then one kvx_transform_hbm gather of the loaded pages into device chunks, then a store and
+ * a load with the bulk-copy mapping on 2 SMs.  Every byte of the chunks and of the pools is
+ * compared with the CPU oracle (oracle/kv_oracle.c, compiled into this test program), run on
+ * host copies of the same inputs.
  *
  * Prints "name value" lines and exits 0 only when every comparison holds.
  */
@@ -197,6 +198,46 @@ int main(void)
         return 5;
     CHECK_CUDA(cudaMemcpy(got, dev_arena, total, cudaMemcpyDeviceToHost));
     compare("transform_chunks", got, exp_arena, total);
+
+    /* The bulk-copy mapping on 2 SMs: store the destination pages into a second host arena
+     * (the oracle's expectation is the arena just compared), then load that arena into the
+     * source pages. */
+    unsigned char *arena2 = NULL;
+    CHECK_KVX(NULL, kvx_host_alloc((void **)&arena2, total));
+    memset(arena2, CANARY, total);
+    for (int c = 0; c < NCHUNK; ++c)
+        chunks[c].ptr = arena2 + off[c];
+    kvx_launch_cfg bcfg;
+    CHECK_KVX(ctx, kvx_default_launch_cfg(ctx, KVX_OP_STORE, &bcfg));
+    bcfg.sm_cap = 2;
+    bcfg.mapping = KVX_MAP_BULK;
+    bcfg.threads = 0;
+    bcfg.unroll = 3;
+    bcfg.stage_bytes = 4096;
+    CHECK_KVX(ctx, kvx_store_chunks(ctx, &pool, &dst, 1, chunks, NCHUNK, 0, L, &bcfg, NULL));
+    CHECK_CUDA(cudaDeviceSynchronize());
+    CHECK_KVX(ctx, kvx_get_status(ctx, NULL, &flags));
+    printf("bulk_store_device_flags %u\n", flags);
+    compare("bulk_store_chunks", arena2, exp_arena, total);
+    CHECK_KVX(ctx, kvx_default_launch_cfg(ctx, KVX_OP_LOAD, &bcfg));
+    bcfg.sm_cap = 2;
+    bcfg.mapping = KVX_MAP_BULK;
+    bcfg.threads = 0;
+    bcfg.unroll = 3;
+    bcfg.stage_bytes = 4096;
+    CHECK_KVX(ctx, kvx_load_chunks(ctx, &pool, &src, 1, chunks, NCHUNK, 0, L, &bcfg, NULL));
+    CHECK_CUDA(cudaDeviceSynchronize());
+    CHECK_KVX(ctx, kvx_get_status(ctx, NULL, &flags));
+    printf("bulk_load_device_flags %u\n", flags);
+    if (ora_load(&oexp, &osrc, 1, ochunks, NCHUNK, 0, L) != ORA_OK)
+        return 5;
+    for (int i = 0; i < KV * L; ++i) {
+        CHECK_CUDA(cudaMemcpy(got, dev_pools[i], pool_bytes, cudaMemcpyDeviceToHost));
+        char name[32];
+        snprintf(name, sizeof name, "bulk_load_pool%d", i);
+        compare(name, got, exp_pools[i], pool_bytes);
+    }
+    kvx_host_free(arena2);
 
     kvx_destroy(ctx);
     CHECK_CUDA(cudaFree(dev_arena));

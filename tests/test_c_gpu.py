@@ -31,7 +31,7 @@ def _cuda_lib_dir(cuda: str) -> str:
     pytest.skip(f"no libcudart.so under {cuda}")
 
 
-def test_c_program_round_trip_and_transform(tmp_path):
+def test_c_program_round_trip_transform_and_bulk_mapping(tmp_path):
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
@@ -54,3 +54,6 @@ def test_c_program_round_trip_and_transform(tmp_path):
     assert out["roundtrip_chunks_mismatches"] == "0"
     assert out["transform_chunks_mismatches"] == "0"
     assert all(out[f"roundtrip_pool{i}_mismatches"] == "0" for i in range(6))
+    assert out["bulk_store_device_flags"] == "0" and out["bulk_load_device_flags"] == "0"
+    assert out["bulk_store_chunks_mismatches"] == "0"
+    assert all(out[f"bulk_load_pool{i}_mismatches"] == "0" for i in range(6))
