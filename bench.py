@@ -880,6 +880,10 @@ def run_ours(args):
                                     "items_per_launch": items, "ctas": ctas,
                                     "threads": threads},
                      **flat_extras(seq, few, mla, qwen, l70, evict, link),
+                     **({"extras_sm_mhz": extra_clocks.get("sm_mhz"),
+                         "extras_sm_max_mhz": extra_clocks.get("sm_max_mhz"),
+                         "extras_clock_reasons": ",".join(extra_clocks.get("reasons") or [])
+                         or "none"} if extra_clocks else {}),
                      "flat_note": "store_/load_: the request stored, then loaded, alone on "
                                   "one stream (library defaults) against the one-way peaks; "
                                   "sm4_: the same on 4 SMs; cfg3_/cfg4_/cfg5_: the 70B "
