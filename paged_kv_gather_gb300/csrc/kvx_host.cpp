@@ -527,7 +527,8 @@ kvx_status kvx_estimate_us(const kvx_link_model *m, int op, int64_t bytes,
     const double sms = sm_cap > 0 && sm_cap < m->num_sms ? sm_cap : m->num_sms;
     // Bytes in flight per CTA: threads x unroll 16-byte units (registers), or for the bulk
     // mapping its two rings' loading stages, 2 x (stages - 1) x stage_bytes.
-    const double per_cta = bulk ? 2.0 * (unroll - 1) * stage_bytes : threads * (double)unroll * 16.0;
+    const double per_cta =
+        bulk ? 2.0 * (unroll - 1) * stage_bytes : threads * (double)unroll * 16.0;
     const double in_flight = sms * ctas * per_cta;  // bytes
     const double little_gbs = in_flight / (m->latency_us * 1e3);           // B/ns = GB/s
     double peak;

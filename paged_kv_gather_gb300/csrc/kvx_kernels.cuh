@@ -572,16 +572,17 @@ CtaFn pick_cta(int unroll, int dir, int hint)
 // stage (cp.async.bulk global -> shared, completing on the stage's mbarrier with transaction
 // bytes) and writes it out (cp.async.bulk shared -> global, one bulk group per stage), with
 // one copy per run of pieces that lie back to back on that side: a stage's host side is
-// then usually one copy, and only its page side needs one copy per page segment.  Each lane keeps n_stages - 1 stages loading while the next fills; two lanes keep
-// their issue costs (a bulk copy occupies its issuing thread for a few hundred cycles) from
-// adding up.  Every wait is bounded (about one second): on expiry the kernel flags
+// then usually one copy, and only its page side needs one copy per page segment.  Each
+// lane keeps n_stages - 1 stages loading while the next fills; two lanes keep their issue
+// costs (a bulk copy occupies its issuing thread for a few hundred cycles) from adding up.
+// Every wait is bounded (about one second): on expiry the kernel flags
 // KVX_DEV_WAIT_TIMEOUT, issues nothing more, waits (again bounded) for the copies it issued
 // and exits.
 
 constexpr int kBulkLanes = 2;         // copy lanes per CTA, each with its own ring
 constexpr int kBulkMaxStages = 8;     // stages per ring
 constexpr int kBulkQueue = 4;         // resolved batches of 32 segments between the warps
-constexpr int kBulkStagePieces = 32;  // bulk copies per stage at most
+constexpr int kBulkStagePieces = 32;  // pieces per stage at most
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
