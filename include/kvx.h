@@ -230,7 +230,9 @@ kvx_status kvx_default_launch_cfg(const kvx_ctx *ctx, int op, kvx_launch_cfg *cf
 /* store: gather every covered (layer, kv, token) vector from the page pools into the
  * chunks ("Strata Guide", section "Non-Intrusive Resource Sizing": eviction to host
  * memory; "Tutti", section 7: store_layer(layer_id, block_ids)).  Chunks live in mapped
- * pinned host memory.  cfg may be NULL (defaults).  Asynchronous on `stream`.
+ * pinned host memory.  cfg may be NULL: the defaults of kvx_default_launch_cfg, except that
+ * page segments (page_size x token_bytes) shorter than 4 KiB get 32 SMs instead of 16, since
+ * a warp then moves one short segment per pass.  Asynchronous on `stream`.
  * A store issued beside a load that needs the whole host-to-device peak (a prefetch on
  * another stream) takes link bandwidth from it in proportion to its SMs (on GB300 about
  * 10 GB/s per SM while the other direction is saturated), and where two kernels land on
@@ -246,7 +248,7 @@ kvx_status kvx_store_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
  * tables ("Strata Guide", section "Step 1: High-Performance GPU-Assisted I/O CUDA
  * Kernel"; "Tutti", section 7: retrieve_layer(layer_id, block_ids)).  Destination slots
  * must be disjoint across the batch (checked at validation level 2).  Slots of a page
- * past the request's last token are not written. */
+ * past the request's last token are not written.  cfg = NULL: as for kvx_store_chunks. */
 kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *reqs,
                            int n_req, const kvx_chunk *chunks, int n_chunks,
                            int layer_begin, int layer_end, const kvx_launch_cfg *cfg,
@@ -309,7 +311,7 @@ kvx_status kvx_transform_hbm(kvx_ctx *ctx, int dir, const kvx_pool *pool,
 /* ---------------------------------------------------------------- prepared plans */
 
 /* A store, load or transform (op = KVX_OP_STORE .. KVX_OP_SCATTER_HBM) validated and
- * packed once.  kvx_plan_create allocates device memory of its own for the descriptors,
+ * packed once (cfg as for the call it prepares).  kvx_plan_create allocates device memory of its own for the descriptors,
  * copies them there on `stream` and waits for the copy.  kvx_plan_launch then only
  * enqueues the kernel: no validation, no host packing, no descriptor copy, no slot wait,
  * so repeated transfers (the same per-layer batches every prefill, for instance) cost one

@@ -23,6 +23,8 @@ const int kSlots = 4;
 const size_t kDefaultDescriptorBytes = 8u << 20;
 const int kDefaultStageBytes = 32 << 10;
 const int kDefaultStages = 3;  // per copy lane of the bulk mapping
+const int64_t kShortSegmentBytes = 4096;  // store/load without a cfg: below this, 32 SMs
+const int kShortSegmentSms = 32;
 const int64_t kMaxBulkSmem = 208 << 10;  // the rings; the CTA's other shared state is ~14 KiB
 
 struct Slot {
@@ -403,6 +405,18 @@ void apply_batch(int op, const kvx_launch_cfg &cfg, Plan *plan)
         plan->batch = 2;
 }
 
+// With no configuration given, a store or load of page segments shorter than
+// kShortSegmentBytes runs on 32 SMs instead of the default 16, as the round trip does for
+// its short segments: a warp then moves one short segment per pass and the link needs more
+// warps to keep enough host accesses in flight.  Call after validation (the pool is sound).
+void short_segment_grid(int op, const kvx_launch_cfg *user, const kvx_pool *pool,
+                        kvx_launch_cfg *cfg)
+{
+    if (!user && (op == KVX_OP_STORE || op == KVX_OP_LOAD) &&
+        int64_t(pool->page_size) * pool->token_bytes < kShortSegmentBytes)
+        cfg->sm_cap = kShortSegmentSms;
+}
+
 int op_dir(int op)
 {
     return (op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM) ? KVX_DIR_SCATTER : KVX_DIR_GATHER;
@@ -423,6 +437,7 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
                        ctx->validation, true, ctx->err, sizeof ctx->err);
     if (st != KVX_OK)
         return st;
+    short_segment_grid(op, user_cfg, pool, &cfg);
     DeviceGuard guard(ctx->device);
     if (!guard.ok)
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
@@ -755,6 +770,7 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
                        ctx->validation, true, ctx->err, sizeof ctx->err);
     if (st != KVX_OK)
         return st;
+    short_segment_grid(op, user_cfg, pool, &cfg);
     DeviceGuard guard(ctx->device);
     if (!guard.ok)
         return set_err(ctx, KVX_ERR_CUDA, "cannot make device %d current", ctx->device);
@@ -1322,6 +1338,7 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
                        1, false, nullptr, 0);
     if (st != KVX_OK)
         return st;
+    short_segment_grid(KVX_OP_LOAD, cfg, pool, &c);
     if (device_flags && (reinterpret_cast<uintptr_t>(device_flags) & 3u))
         return KVX_ERR_ALIGNMENT;
     const kvx::PackedLayout lay = kvx::packed_layout(pool, n_req, n_chunks);

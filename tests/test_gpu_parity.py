@@ -424,6 +424,48 @@ def test_random_bulk_shapes(ctx, stream):
         arena.close()
 
 
+@pytest.mark.parametrize("v,P,cfg_given,ctas", [(256, 8, False, 32), (256, 8, True, 16),
+                                                (1024, 8, False, 16), (1024, 2, False, 32)])
+def test_store_load_default_grid_follows_segment_size(ctx, stream, v, P, cfg_given, ctas):
+    """With no configuration, a store or load of page segments shorter than 4 KiB runs on 32
+    SMs (one CTA each), longer ones on the default 16; an explicit configuration keeps its
+    own SM cap, and a plan follows the same rule.  Checked against the oracle either way."""
+    rng = np.random.default_rng(8400 + v + P + int(cfg_given))
+    L, KV, T = 8, 2, 16384  # enough segments for 32 CTAs of 32 warps resolving 16 each
+    npg = T // P
+    NP = 2 * npg + 3
+    perm = rng.permutation(NP).astype(np.int32)
+    src, dst = Requests([perm[:npg]], [T]), Requests([perm[npg:2 * npg]], [T])
+    specs = wl.split_tokens(0, 0, T, 256, 0, L, wl.LAYER_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(8401)
+    arena = Arena(nbytes, "host")
+    cs = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_STORE) if cfg_given else None
+    cl = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD) if cfg_given else None
+    _store(ctx, "store", dpool, src, specs, arena, 0, None, cs, stream)
+    assert kvx.kvx_last_launch(ctx)[1] == ctas
+    assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), "store")
+    data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+    arena.write(data)
+    pre = dpool.host_copy()
+    _load(ctx, "load", dpool, dst, specs, arena, 0, None, cl, stream)
+    assert kvx.kvx_last_launch(ctx)[1] == ctas
+    assert_pool_equal(dpool, expected_load(pre, dst, specs, data.copy()))
+    # A prepared load plan made without a configuration takes the same grid.
+    plan = kvx.kvx_plan_create(ctx, kvx.KVX_OP_LOAD, dpool.pool, dst.array,
+                               kvx.chunks_array(specs, arena.ptr), cfg=cl,
+                               stream=stream.cuda_stream)
+    kvx.kvx_plan_launch(plan, stream.cuda_stream)
+    stream.synchronize()
+    kvx.kvx_plan_destroy(plan)
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    assert_pool_equal(dpool, expected_load(pre, dst, specs, data.copy()))
+    arena.close()
+
+
 def test_bulk_mapping_rejects_bad_stage_shapes(ctx, stream):
     dpool = DevicePool.empty(1, 1, 4, 1, 16)
     reqs = Requests([np.array([0], np.int32)], [1])
