@@ -1561,6 +1561,12 @@ def run_mla_blocks(args, kvx, wl):
                 kvx.kvx_plan_launch(pl, sh)
 
         overlap_ms = _timed(stream, per_layer_overlap, 5)
+
+        def per_layer_calls_overlap():
+            for l in range(s.num_layers):
+                kvx.kvx_load_chunks(ctx, pool, rd, ch, l, l + 1, oc, sh)
+
+        ocall_ms = _timed(stream, per_layer_calls_overlap, 5)
         ograph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(ograph, stream=stream):
             cs = torch.cuda.current_stream().cuda_stream
@@ -1590,6 +1596,7 @@ def run_mla_blocks(args, kvx, wl):
                "store_gbs": round(N / (st_ms * 1e-3) / GB, 2),
                "per_layer_load_gbs": round(N / (ld_ms * 1e-3) / GB, 2),
                "per_layer_load_ms": round(ld_ms / s.num_layers, 4),
+               "per_layer_load_overlap_gbs": round(N / (ocall_ms * 1e-3) / GB, 2),
                "per_layer_plans_gbs": round(N / (plan_ms * 1e-3) / GB, 2),
                "per_layer_graph_gbs": round(N / (graph_ms * 1e-3) / GB, 2),
                "per_layer_plans_overlap_gbs": round(N / (overlap_ms * 1e-3) / GB, 2),

@@ -181,8 +181,10 @@ typedef struct kvx_launch_cfg {
                              kernel, so events recorded after it keep their meaning.  Use it
                              only when this transfer touches no memory the previous kernel
                              writes and writes none it reads (for example consecutive
-                             per-layer loads).  Store, load and transform with the
-                             warp-segment mapping; 0 elsewhere.  0 = off (default) */
+                             per-layer loads).  A call made with it waits on the host for
+                             its descriptor copy (a few microseconds) before it enqueues the
+                             kernel.  Store, load and transform with the warp-segment
+                             mapping; 0 elsewhere.  0 = off (default) */
 } kvx_launch_cfg;
 
 typedef struct kvx_ctx kvx_ctx;

@@ -79,8 +79,12 @@ kvx_status cuda_err(kvx_ctx *ctx, cudaError_t e, const char *what)
 
 // Copy a call's packed descriptors into its slot on the context's copy stream (zeroing
 // `zero_bytes` at `zero_off` after them), and make the caller's stream wait for that.
+// settle: the host waits for the copy first (a few microseconds), so that the caller's
+// stream waits on an event that has already completed.  An overlapped launch needs that: a
+// wait on a copy still in flight keeps it from starting before the kernel ahead of it ends,
+// where a completed one does not.
 cudaError_t stage(kvx_ctx *ctx, Slot &slot, size_t bytes, size_t zero_off, size_t zero_bytes,
-                  cudaStream_t s)
+                  cudaStream_t s, bool settle = false)
 {
     cudaError_t e = cudaMemcpyAsync(slot.dev, slot.host, bytes, cudaMemcpyHostToDevice,
                                     ctx->copy_stream);
@@ -88,6 +92,8 @@ cudaError_t stage(kvx_ctx *ctx, Slot &slot, size_t bytes, size_t zero_off, size_
         e = cudaMemsetAsync(slot.dev + zero_off, 0, zero_bytes, ctx->copy_stream);
     if (e == cudaSuccess)
         e = cudaEventRecord(slot.staged, ctx->copy_stream);
+    if (e == cudaSuccess && settle)
+        e = cudaEventSynchronize(slot.staged);
     if (e == cudaSuccess)
         e = cudaStreamWaitEvent(s, slot.staged, 0);
     return e;
@@ -454,11 +460,11 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     if (plan.total_items == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = stage(ctx, *slot, lay.total, 0, 0, s);
-    if (e != cudaSuccess)
-        return cuda_err(ctx, e, "descriptor copy");
     const LaunchShape shape =
         launch_shape(ctx, cfg, plan, dir, use_w32(op, cfg, pool, chunks, n_chunks));
+    cudaError_t e = stage(ctx, *slot, lay.total, 0, 0, s, shape.overlap);
+    if (e != cudaSuccess)
+        return cuda_err(ctx, e, "descriptor copy");
     e = launch_kernel(shape, plan, s);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "kernel launch");

@@ -159,6 +159,49 @@ def test_overlapped_per_layer_calls(ctx, stream, op):
     arena.close()
 
 
+def test_overlapped_layer_load_calls_complete_in_order(ctx, stream):
+    """Per-layer load calls launched to overlap, three passes back to back onto the same
+    pages: an event recorded after the fourth layer of the last pass means layers 0-3 hold
+    that pass's bytes (each pass loads other host bytes), and the whole pool matches the
+    oracle."""
+    NP, src, dst, specs, nbytes = _layer_case(9300)
+    dpool = DevicePool.empty(L, KV, NP, P, V)
+    dpool.fill_random(9301)
+    pre = dpool.host_copy()
+    arenas = [Arena(nbytes, "host") for _ in range(3)]
+    try:
+        datas = []
+        for i, a in enumerate(arenas):
+            d = np.random.default_rng(9302 + i).integers(0, 256, nbytes + 4096, dtype=np.uint8)
+            a.write(d)
+            datas.append(d)
+        torch.cuda.synchronize()
+        c = _overlap_cfg(ctx, kvx.KVX_OP_LOAD)
+        ev = torch.cuda.Event()
+        for i, a in enumerate(arenas):
+            ch = kvx.chunks_array(specs, a.ptr)
+            for layer in range(L):
+                kvx.kvx_load_chunks(ctx, dpool.pool, dst.array, ch, layer, layer + 1, c,
+                                    stream.cuda_stream)
+                if i == 2 and layer == 3:
+                    ev.record(stream)
+        side = torch.cuda.Stream()
+        side.wait_event(ev)
+        with torch.cuda.stream(side):
+            early = dpool.tensor[:, :4].clone()
+        torch.cuda.synchronize()
+        assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+        oracle.load(pre, dst.oracle(), oracle_chunks(specs, datas[-1].copy()))
+        got = early.cpu().numpy()
+        for layer in range(4):
+            assert np.array_equal(got[0, layer], pre.pools[0][layer]), \
+                f"layer {layer} not complete at the event after layer 3"
+        assert_pool_equal(dpool, pre)
+    finally:
+        for a in arenas:
+            a.close()
+
+
 def test_overlap_rejected_where_not_supported(ctx, stream):
     """overlap = 1 is refused, with nothing launched, outside single transfers on the
     warp-segment mapping: exchange, round trip, CTA and bulk mappings, the allocation-free
