@@ -78,7 +78,7 @@ def parse():
                    choices=["llama8b", "llama70b", "qwen7b_batch", "mla_sweep", "sm_sweep",
                             "transform_sweep", "profile_small", "batch_sweep", "mla_blocks",
                             "roundtrip_sweep", "size_sweep", "roundtrip_under_gemm",
-                            "eviction"],
+                            "eviction", "token_major"],
                    help="llama8b is the headline line; the others print measurement lines of "
                         "the other workloads (not the headline)")
     p.add_argument("--profile-op", default="load",
@@ -1503,6 +1503,50 @@ def run_batch_sweep(args, kvx, wl):
     kvx.kvx_destroy(ctx)
 
 
+def run_token_major(args, kvx, wl):
+    """Store and load of the MLA latent (1, 2 and 16 tokens per page) and of the llama8b
+    request in token-major chunks of about 2 MiB over all layers, whose page segments of more
+    than one token are strided rows on the chunk side, on 4 and 16 SMs and without a
+    configuration."""
+    ctx = kvx.kvx_create(0, 64 << 20)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    for name, P in (("mla", 1), ("mla", 2), ("mla", 16), ("llama8b", 16)):
+        w = wl.mla_sweep(P, 1 << 20) if name == "mla" else wl.llama8b()
+        s = w.shape
+        tpc = max((2 << 20) // (s.token_bytes * s.num_layers * s.kv_factor), 16)
+        specs = wl.split_tokens(0, 0, w.store_requests[0].n_tokens, tpc, 0, s.num_layers,
+                                wl.TOKEN_MAJOR)
+        wl.place_chunks(specs, s)
+        pools = _pool_tensor(s, w.seed, wl)
+        pool = kvx.Pool.from_tensor(pools, s.page_size)
+        src, dst = w.store_requests[0], w.load_requests[0]
+        ps, pd = torch.from_numpy(src.page_table).cuda(), torch.from_numpy(dst.page_table).cuda()
+        rs = kvx.requests_array([(ps.data_ptr(), src.page_table, src.n_tokens)])
+        rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
+        arena = kvx.HostBuffer(wl._arena_bytes(specs, s))
+        arena.array[:] = 0
+        ch = kvx.chunks_array(specs, arena.ptr)
+        N = sum(c.nbytes(s) for c in specs)
+        for cap in (4, 16, None):
+            row = {"workload": f"{name}_token_major", "page_size": P, "chunks": len(specs),
+                   "sm_cap": cap if cap else "default"}
+            for op_name, op, fn, rq in (("store", kvx.KVX_OP_STORE, kvx.kvx_store_chunks, rs),
+                                        ("load", kvx.KVX_OP_LOAD, kvx.kvx_load_chunks, rd)):
+                c = None
+                if cap:
+                    c = kvx.kvx_default_launch_cfg(ctx, op)
+                    c.sm_cap = cap
+                ms = _timed(stream, lambda: fn(ctx, pool, rq, ch, 0, s.num_layers, c, sh), 3)
+                row[f"{op_name}_gbs"] = round(N / (ms * 1e-3) / GB, 2)
+            _emit(row)
+        arena.close()
+        del pools
+        torch.cuda.empty_cache()
+    assert kvx.kvx_get_status(ctx, sh) == 0
+    kvx.kvx_destroy(ctx)
+
+
 def run_mla_blocks(args, kvx, wl):
     """Per-block object layout (STRIPED chunks, one per page, 61 layer objects each,
     4096-aligned): one store of all layers, 61 per-layer loads, and the per-object DMA
@@ -2092,7 +2136,7 @@ def run_workload(args):
     {"llama70b": run_llama70b, "qwen7b_batch": run_qwen7b, "mla_sweep": run_mla_sweep,
      "sm_sweep": run_sm_sweep, "transform_sweep": run_transform_sweep,
      "profile_small": run_profile_small, "batch_sweep": run_batch_sweep,
-     "mla_blocks": run_mla_blocks, "eviction": run_eviction,
+     "mla_blocks": run_mla_blocks, "eviction": run_eviction, "token_major": run_token_major,
      "roundtrip_sweep": run_roundtrip_sweep, "size_sweep": run_size_sweep,
      "roundtrip_under_gemm": run_roundtrip_under_gemm}[args.workload](
         args, kvx, wl)

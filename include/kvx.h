@@ -165,8 +165,10 @@ typedef struct kvx_launch_cfg {
     int32_t unroll;       /* warp-segment and CTA mappings: 16-byte loads in flight per
                              thread before its stores (1, 2, 4 or 8; where
                              kvx_transform_hbm moves 32-byte units, max(unroll / 2, 1)
-                             32-byte loads); bulk mapping: shared-memory stages of each of
-                             its two rings (2..8).  0 = default (bulk: 3) */
+                             32-byte loads; a single transfer whose chunks include a
+                             token-major one of several (layer, kv) slabs walks its strided
+                             rows min(unroll, 4) deep); bulk mapping: shared-memory stages
+                             of each of its two rings (2..8).  0 = default (bulk: 3) */
     int32_t store_hint;   /* KVX_HINT_* (warp-segment and CTA mappings) */
     int32_t mapping;      /* KVX_MAP_* */
     int32_t stage_bytes;  /* bulk mapping: bytes per shared-memory stage, a multiple of 16;

@@ -274,8 +274,23 @@ bool use_w32(int op, const kvx_launch_cfg &cfg, const kvx_pool *pool, const kvx_
            cfg.mapping == KVX_MAP_WARP_SEGMENT && aligned32(pool, chunks, n_chunks);
 }
 
+// The row-walking segment kernel (kvx_rows_kernel): a warp-segment launch, not with 32-byte
+// accesses, whose chunks include a token-major one of more than one (layer, kv) slab, so
+// that page segments of more than one token are strided on the chunk side.
+bool use_rows(const kvx_launch_cfg &cfg, const kvx_pool *pool, const kvx_chunk *chunks,
+              int n_chunks, bool w32)
+{
+    if (w32 || cfg.mapping != KVX_MAP_WARP_SEGMENT || pool->page_size == 1)
+        return false;
+    for (int c = 0; c < n_chunks; ++c)
+        if (chunks[c].layout == KVX_CHUNK_TOKEN_MAJOR &&
+            int64_t(chunks[c].n_layers) * pool->kv_factor > 1)
+            return true;
+    return false;
+}
+
 LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &plan, int dir,
-                         bool w32 = false)
+                         bool w32 = false, bool rows = false)
 {
     LaunchShape sh;
     const int64_t warps_per_cta = cfg.threads / 32;
@@ -310,7 +325,7 @@ LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Pl
         sh.threads = cfg.threads;
     } else if (cfg.mapping == KVX_MAP_WARP_SEGMENT) {
         sh.fn = reinterpret_cast<const void *>(
-            pick_kernel(cfg.unroll, dir, cfg.store_hint, plan.batch, w32, sh.overlap));
+            pick_kernel(cfg.unroll, dir, cfg.store_hint, plan.batch, w32, sh.overlap, rows));
         sh.threads = cfg.threads;
     }
     return sh;
@@ -460,8 +475,9 @@ kvx_status launch(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx_request 
     if (plan.total_items == 0)
         return KVX_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const LaunchShape shape =
-        launch_shape(ctx, cfg, plan, dir, use_w32(op, cfg, pool, chunks, n_chunks));
+    const bool w32 = use_w32(op, cfg, pool, chunks, n_chunks);
+    const LaunchShape shape = launch_shape(ctx, cfg, plan, dir, w32,
+                                           use_rows(cfg, pool, chunks, n_chunks, w32));
     cudaError_t e = stage(ctx, *slot, lay.total, 0, 0, s, shape.overlap);
     if (e != cudaSuccess)
         return cuda_err(ctx, e, "descriptor copy");
@@ -804,7 +820,9 @@ kvx_status kvx_plan_create(kvx_ctx *ctx, int op, const kvx_pool *pool, const kvx
         delete p;
         return cuda_err(ctx, e, "plan descriptor copy");
     }
-    p->shape = launch_shape(ctx, cfg, p->plan, dir, use_w32(op, cfg, pool, chunks, n_chunks));
+    const bool w32 = use_w32(op, cfg, pool, chunks, n_chunks);
+    p->shape = launch_shape(ctx, cfg, p->plan, dir, w32,
+                            use_rows(cfg, pool, chunks, n_chunks, w32));
     *out = p;
     return KVX_OK;
 }
@@ -1387,8 +1405,9 @@ extern "C" kvx_status kvx_load_chunks_noalloc(const kvx_pool *pool, const kvx_re
     if (cudaMemcpyAsync(dev_block, g_noalloc_stage, kNoallocHeader + lay.total,
                         cudaMemcpyHostToDevice, s) != cudaSuccess)
         return KVX_ERR_CUDA;
-    if (launch_kernel(launch_shape(&shape_ctx, c, plan, KVX_DIR_SCATTER), plan, s) !=
-        cudaSuccess)
+    if (launch_kernel(launch_shape(&shape_ctx, c, plan, KVX_DIR_SCATTER, false,
+                                   use_rows(c, pool, chunks, n_chunks, false)),
+                      plan, s) != cudaSuccess)
         return KVX_ERR_CUDA;
     return KVX_OK;
 }

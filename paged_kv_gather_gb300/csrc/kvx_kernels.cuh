@@ -242,7 +242,7 @@ __device__ __forceinline__ bool segment_of(const Plan &p, int c, int64_t item, b
     sg.s_pitch = DIR == KVX_DIR_GATHER ? v : ch.row_stride;
     sg.d_pitch = DIR == KVX_DIR_GATHER ? ch.row_stride : v;
     sg.rows = te - tb;
-    sg.contiguous = ch.row_stride == v;
+    sg.contiguous = ch.row_stride == v || te - tb == 1;  // one row is one run
     return true;
 }
 
@@ -375,6 +375,125 @@ __global__ void __launch_bounds__(1024, 1) kvx_segment_overlap_kernel(const Plan
     const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     allow_next_launch();
     run_segments<U, DIR, HINT, BATCHED, W32>(p, warp, n_warps, lane);
+    wait_previous_grid();
+}
+
+// Strided rows: `rows` rows of n16_row 16-byte units, row r at src + r * s_pitch and
+// dst + r * d_pitch.  The units of all rows form one sequence that the warp walks as it
+// walks a contiguous run (lane i owns units i, i + 32, ...), with U loads in flight per lane
+// across row boundaries, so a page of short rows costs a host round trip per pass of 32 U
+// units rather than one (or more) per row.  A lane's position advances 32 units at a time:
+// dr rows and dc units, plus one row when the unit index within the row wraps.
+template <int U, int HINT, bool NC>
+__device__ __forceinline__ void copy_rows(const char *src, char *dst, int64_t s_pitch,
+                                          int64_t d_pitch, int rows, int n16_row, int lane)
+{
+    const int total = rows * n16_row;
+    const int dr = 32 / n16_row, dc = 32 - dr * n16_row;
+    const int64_t s_step = dr * s_pitch + dc * 16, d_step = dr * d_pitch + dc * 16;
+    const int64_t s_wrap = s_pitch - int64_t(n16_row) * 16;
+    const int64_t d_wrap = d_pitch - int64_t(n16_row) * 16;
+    const int row0 = lane / n16_row;
+    int col = lane - row0 * n16_row;
+    int64_t s_off = row0 * s_pitch + col * 16, d_off = row0 * d_pitch + col * 16;
+    for (int j = lane; j < total; j += 32 * U) {
+        uint4 r[U];
+        int c = col;
+        int64_t o = s_off;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (j + 32 * u < total)
+                r[u] = ld_v4<NC>(reinterpret_cast<const uint4 *>(src + o));
+            o += s_step;
+            c += dc;
+            if (c >= n16_row) {
+                c -= n16_row;
+                o += s_wrap;
+            }
+        }
+        s_off = o;
+        c = col;
+        o = d_off;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (j + 32 * u < total)
+                st_v4<HINT>(reinterpret_cast<uint4 *>(dst + o), r[u]);
+            o += d_step;
+            c += dc;
+            if (c >= n16_row) {
+                c -= n16_row;
+                o += d_wrap;
+            }
+        }
+        d_off = o;
+        col = c;
+    }
+}
+
+// A segment of a launch with token-major chunks: strided rows walked as one sequence, and a
+// contiguous segment as one row (one code path, so the kernel holds one copy loop).
+template <int U, int HINT>
+__device__ __forceinline__ void copy_segment_rows(const Segment &sg, int64_t v, int lane)
+{
+    if (sg.contiguous)
+        copy_rows<U, HINT, true>(sg.src, sg.dst, 0, 0, 1, int((int64_t(sg.rows) * v) >> 4),
+                                 lane);
+    else
+        copy_rows<U, HINT, true>(sg.src, sg.dst, sg.s_pitch, sg.d_pitch, sg.rows, int(v >> 4),
+                                 lane);
+}
+
+// The warp-segment walk of run_segments for launches whose chunks include token-major ones
+// of more than one (layer, kv) slab: their page segments are strided on the chunk side, and
+// the plain copy moves such a segment one row and one unit per lane at a time.
+template <int U, int DIR, int HINT, bool BATCHED>
+__device__ __forceinline__ void run_row_segments(const Plan &p)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int64_t v = p.token_bytes;
+    if (!BATCHED) {
+        for (int64_t item = warp; item < p.total_items; item += n_warps) {
+            Segment sg;
+            if (resolve_segment<DIR>(p, item, lane, sg))
+                copy_segment_rows<U, HINT>(sg, v, lane);
+        }
+        return;
+    }
+    const int B = p.batch;
+    for (int64_t base = warp * B; base < p.total_items; base += n_warps * B) {
+        const int64_t mine = base + lane;
+        Segment sg;
+        sg.src = nullptr;
+        sg.dst = nullptr;
+        sg.s_pitch = sg.d_pitch = 0;
+        sg.rows = 0;
+        sg.contiguous = true;
+        bool ok = false;
+        if (lane < B && mine < p.total_items)
+            ok = segment_of<DIR>(p, find_chunk_lane(p.item_begin, p.n_chunks, mine), mine, true,
+                                 sg);
+        const unsigned valid = __ballot_sync(0xffffffffu, ok);
+        for (int k = 0; k < B; ++k) {
+            const Segment s = shfl_segment(sg, k);
+            if (valid & (1u << k))
+                copy_segment_rows<U, HINT>(s, v, lane);
+        }
+    }
+}
+
+template <int U, int DIR, int HINT, bool BATCHED>
+__global__ void __launch_bounds__(1024, 1) kvx_rows_kernel(const Plan p)
+{
+    run_row_segments<U, DIR, HINT, BATCHED>(p);
+}
+
+template <int U, int DIR, int HINT, bool BATCHED>
+__global__ void __launch_bounds__(1024, 1) kvx_rows_overlap_kernel(const Plan p)
+{
+    allow_next_launch();
+    run_row_segments<U, DIR, HINT, BATCHED>(p);
     wait_previous_grid();
 }
 
@@ -1210,12 +1329,47 @@ KernelFn pick_unroll(int unroll, int dir, int hint, bool overlap)
     return nullptr;
 }
 
-// The warp-segment kernel for (unroll, direction, hint), batched when more than one
-// segment is resolved per warp at once, with 32-byte accesses when w32, and the overlapped
-// variant when overlap.
-KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1, bool w32 = false,
-                     bool overlap = false)
+template <int U, int DIR, int HINT, bool BATCHED>
+KernelFn rows_fn(bool overlap)
 {
+    return overlap ? kvx_rows_overlap_kernel<U, DIR, HINT, BATCHED>
+                   : kvx_rows_kernel<U, DIR, HINT, BATCHED>;
+}
+
+template <int U, bool BATCHED>
+KernelFn pick_rows_hint_dir(int dir, int hint, bool overlap)
+{
+    if (dir == KVX_DIR_GATHER)
+        return hint == KVX_HINT_STREAMING ? rows_fn<U, KVX_DIR_GATHER, 1, BATCHED>(overlap)
+                                          : rows_fn<U, KVX_DIR_GATHER, 0, BATCHED>(overlap);
+    return hint == KVX_HINT_STREAMING ? rows_fn<U, KVX_DIR_SCATTER, 1, BATCHED>(overlap)
+                                      : rows_fn<U, KVX_DIR_SCATTER, 0, BATCHED>(overlap);
+}
+
+// The row-walking kernel holds at most 4 loads in flight per lane: its position arithmetic
+// leaves no registers for 8 at 1024 threads per CTA.
+template <bool BATCHED>
+KernelFn pick_rows(int unroll, int dir, int hint, bool overlap)
+{
+    switch (unroll) {
+    case 1: return pick_rows_hint_dir<1, BATCHED>(dir, hint, overlap);
+    case 2: return pick_rows_hint_dir<2, BATCHED>(dir, hint, overlap);
+    case 4:
+    case 8: return pick_rows_hint_dir<4, BATCHED>(dir, hint, overlap);
+    }
+    return nullptr;
+}
+
+// The warp-segment kernel for (unroll, direction, hint), batched when more than one
+// segment is resolved per warp at once, with 32-byte accesses when w32, walking strided
+// rows as one sequence when rows (launches with token-major chunks; not with w32), and the
+// overlapped variant when overlap.
+KernelFn pick_kernel(int unroll, int dir, int hint, int batch = 1, bool w32 = false,
+                     bool overlap = false, bool rows = false)
+{
+    if (rows && !w32)
+        return batch > 1 ? pick_rows<true>(unroll, dir, hint, overlap)
+                         : pick_rows<false>(unroll, dir, hint, overlap);
     if (w32)
         return batch > 1 ? pick_unroll<true, true>(unroll, dir, hint, overlap)
                          : pick_unroll<false, true>(unroll, dir, hint, overlap);

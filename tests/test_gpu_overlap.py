@@ -202,6 +202,51 @@ def test_overlapped_layer_load_calls_complete_in_order(ctx, stream):
             a.close()
 
 
+@pytest.mark.parametrize("op", ["store", "load"])
+def test_overlapped_token_major_layer_calls(ctx, stream, op):
+    """Per-layer calls on token-major chunks of K and V (pages of strided rows: the
+    row-walking kernel's overlapped variant), against the oracle."""
+    rng = np.random.default_rng(9400)
+    KV2, npg = 2, T // P
+    NP = 2 * npg + 3
+    perm = rng.permutation(NP).astype(np.int32)
+    src, dst = Requests([perm[:npg]], [T]), Requests([perm[npg:2 * npg]], [T])
+    specs = []
+    for layer in range(L):
+        specs += wl.split_tokens(0, 0, T, 200, layer, 1, wl.TOKEN_MAJOR)
+    shape = wl.KVShape(L, KV2, 1, V, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    dpool = DevicePool.empty(L, KV2, NP, P, V)
+    dpool.fill_random(9401)
+    arena = Arena(nbytes, "host")
+    try:
+        ch = kvx.chunks_array(specs, arena.ptr)
+        if op == "store":
+            c = _overlap_cfg(ctx, kvx.KVX_OP_STORE)
+            for layer in range(L):
+                kvx.kvx_store_chunks(ctx, dpool.pool, src.array, ch, layer, layer + 1, c,
+                                     stream.cuda_stream)
+            stream.synchronize()
+            assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+            assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), op)
+        else:
+            data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+            arena.write(data)
+            torch.cuda.synchronize()
+            pre = dpool.host_copy()
+            c = _overlap_cfg(ctx, kvx.KVX_OP_LOAD)
+            for layer in range(L):
+                kvx.kvx_load_chunks(ctx, dpool.pool, dst.array, ch, layer, layer + 1, c,
+                                    stream.cuda_stream)
+            stream.synchronize()
+            assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+            oracle.load(pre, dst.oracle(), oracle_chunks(specs, data.copy()))
+            assert_pool_equal(dpool, pre)
+    finally:
+        arena.close()
+
+
 def test_overlap_rejected_where_not_supported(ctx, stream):
     """overlap = 1 is refused, with nothing launched, outside single transfers on the
     warp-segment mapping: exchange, round trip, CTA and bulk mappings, the allocation-free

@@ -199,9 +199,12 @@ def test_random_launch_shapes(ctx, stream):
 @pytest.mark.parametrize("unroll", [1, 2, 4, 8])
 @pytest.mark.parametrize("hint", [0, 1])
 @pytest.mark.parametrize("batch", [1, 7, 32])
-def test_every_kernel_variant(ctx, stream, unroll, hint, batch):
+@pytest.mark.parametrize("layout", ["layer", "token"])
+def test_every_kernel_variant(ctx, stream, unroll, hint, batch, layout):
     """Every (unroll, hint, direction) instantiation, one and several segments resolved per
-    warp, on a multi-tile ragged batch."""
+    warp, on a multi-tile ragged batch.  layout "token": token-major chunks over all layers
+    (pages of strided rows, the row-walking kernel), with one layer-major chunk in the same
+    launch so that kernel copies contiguous segments too."""
     rng = np.random.default_rng(77 + unroll * 10 + hint)
     L, KV, P, v = 3, 2, 16, 2048
     lens = [1000, 333, 17]
@@ -215,7 +218,8 @@ def test_every_kernel_variant(ctx, stream, unroll, hint, batch):
         at += npg
     specs = []
     for r, n in enumerate(lens):
-        specs += wl.split_tokens(r, 0, n, 100, 0, L, wl.LAYER_MAJOR)
+        lay = wl.TOKEN_MAJOR if layout == "token" and r != 1 else wl.LAYER_MAJOR
+        specs += wl.split_tokens(r, 0, n, 100, 0, L, lay)
     shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
     wl.place_chunks(specs, shape)
     nbytes = wl._arena_bytes(specs, shape)
