@@ -274,19 +274,25 @@ bool use_w32(int op, const kvx_launch_cfg &cfg, const kvx_pool *pool, const kvx_
            cfg.mapping == KVX_MAP_WARP_SEGMENT && aligned32(pool, chunks, n_chunks);
 }
 
-// The row-walking segment kernel (kvx_rows_kernel): a warp-segment launch, not with 32-byte
-// accesses, whose chunks include a token-major one of more than one (layer, kv) slab, so
-// that page segments of more than one token are strided on the chunk side.
-bool use_rows(const kvx_launch_cfg &cfg, const kvx_pool *pool, const kvx_chunk *chunks,
-              int n_chunks, bool w32)
+// Whether page segments of more than one token are strided on the chunk side: the chunks
+// include a token-major one of more than one (layer, kv) slab.
+bool strided_rows(const kvx_pool *pool, const kvx_chunk *chunks, int n_chunks)
 {
-    if (w32 || cfg.mapping != KVX_MAP_WARP_SEGMENT || pool->page_size == 1)
+    if (pool->page_size == 1)
         return false;
     for (int c = 0; c < n_chunks; ++c)
         if (chunks[c].layout == KVX_CHUNK_TOKEN_MAJOR &&
             int64_t(chunks[c].n_layers) * pool->kv_factor > 1)
             return true;
     return false;
+}
+
+// The row-walking segment kernel (kvx_rows_kernel): a warp-segment launch, not with 32-byte
+// accesses, with strided rows.
+bool use_rows(const kvx_launch_cfg &cfg, const kvx_pool *pool, const kvx_chunk *chunks,
+              int n_chunks, bool w32)
+{
+    return !w32 && cfg.mapping == KVX_MAP_WARP_SEGMENT && strided_rows(pool, chunks, n_chunks);
 }
 
 LaunchShape launch_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &plan, int dir,
@@ -631,7 +637,7 @@ int64_t roundtrip_units(const Plan &ps, int slices)
 // `sync` (sync_bytes(), zeroed before each launch).  False when the units do not fit the
 // kernel's 32-bit unit indices.
 bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, int slices,
-                     char *sync, RoundTripSync *sy, LaunchShape *sh)
+                     char *sync, RoundTripSync *sy, LaunchShape *sh, bool rows)
 {
     sy->slices = slices;
     sy->unit_items = sy->slices > 1 ? 1 : ps.batch;
@@ -650,7 +656,7 @@ bool roundtrip_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &
     sy->wait_ns = kWaitLimitNs;
     sh->ctas = ctas;
     sh->threads = cfg.threads;
-    sh->fn = reinterpret_cast<const void *>(pick_roundtrip(cfg.unroll, ps.batch > 1));
+    sh->fn = reinterpret_cast<const void *>(pick_roundtrip(cfg.unroll, ps.batch > 1, rows));
     return true;
 }
 
@@ -735,7 +741,8 @@ kvx_status launch_roundtrip(kvx_ctx *ctx, const kvx_pool *pool, const kvx_reques
                        (long long)ps.total_items, sync_off + sync_bytes, ctx->slot_bytes);
     RoundTripSync sy;
     LaunchShape shape;
-    if (!roundtrip_setup(ctx, cfg, ps, rule.slices, slot->dev + sync_off, &sy, &shape))
+    if (!roundtrip_setup(ctx, cfg, ps, rule.slices, slot->dev + sync_off, &sy, &shape,
+                         strided_rows(pool, chunks, n_chunks)))
         return set_err(ctx, KVX_ERR_CAPACITY, "round trip of %lld segments (%d per unit) has "
                        "2^31 units or more", (long long)ps.total_items, ps.batch);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -944,7 +951,7 @@ kvx_status kvx_plan_create_roundtrip(kvx_ctx *ctx, const kvx_pool *pool,
     p->plan.batch = p->load.batch = rule.batch;
     // The unit count was checked above, so the setup cannot fail here.
     roundtrip_setup(ctx, cfg, p->plan, rule.slices, p->dev + 2 * lay.total, &p->rsync,
-                    &p->shape);
+                    &p->shape, strided_rows(pool, chunks, n_chunks));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = cudaMemcpyAsync(p->dev, host.data(), 2 * lay.total, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)

@@ -432,15 +432,33 @@ __device__ __forceinline__ void copy_rows(const char *src, char *dst, int64_t s_
 
 // A segment of a launch with token-major chunks: strided rows walked as one sequence, and a
 // contiguous segment as one row (one code path, so the kernel holds one copy loop).
-template <int U, int HINT>
+template <int U, int HINT, bool NC = true>
 __device__ __forceinline__ void copy_segment_rows(const Segment &sg, int64_t v, int lane)
 {
     if (sg.contiguous)
-        copy_rows<U, HINT, true>(sg.src, sg.dst, 0, 0, 1, int((int64_t(sg.rows) * v) >> 4),
-                                 lane);
+        copy_rows<U, HINT, NC>(sg.src, sg.dst, 0, 0, 1, int((int64_t(sg.rows) * v) >> 4), lane);
     else
-        copy_rows<U, HINT, true>(sg.src, sg.dst, sg.s_pitch, sg.d_pitch, sg.rows, int(v >> 4),
-                                 lane);
+        copy_rows<U, HINT, NC>(sg.src, sg.dst, sg.s_pitch, sg.d_pitch, sg.rows, int(v >> 4),
+                               lane);
+}
+
+// The row walk as a call of its own, for the round trip: inlined there for both directions
+// beside the unit scheduling, it spilled.
+template <int U, int HINT, bool NC>
+__device__ __noinline__ void copy_segment_rows_call(const Segment sg, int64_t v, int lane)
+{
+    copy_segment_rows<U, HINT, NC>(sg, v, lane);
+}
+
+// One segment of a round trip: the row walk (out of line) in the variants for token-major
+// chunks, the plain copy otherwise.
+template <int U, int HINT, bool NC, bool ROWS>
+__device__ __forceinline__ void copy_any_segment(const Segment &sg, int64_t v, int lane)
+{
+    if (ROWS)
+        copy_segment_rows_call<U, HINT, NC>(sg, v, lane);
+    else
+        copy_segment<U, HINT, NC>(sg, v, lane);
 }
 
 // The warp-segment walk of run_segments for launches whose chunks include token-major ones
@@ -1122,8 +1140,9 @@ __device__ __forceinline__ int next_unit(const RoundTripSync &sy, unsigned lag, 
 
 // Items [first, first + count) of plan p, warp-collective (count is 1 unless BATCHED).
 // With slices > 1 (not BATCHED), only rows [k r / slices, (k + 1) r / slices) of the one
-// item's r rows, k = slice.  NC = false for bytes written earlier in the same launch.
-template <int U, int DIR, int HINT, bool BATCHED, bool NC>
+// item's r rows, k = slice.  NC = false for bytes written earlier in the same launch.  ROWS:
+// strided rows walked as one sequence (chunks include token-major ones of several slabs).
+template <int U, int DIR, int HINT, bool BATCHED, bool NC, bool ROWS = false>
 __device__ __forceinline__ void copy_items(const Plan &p, int64_t first, int count, int lane,
                                            int slices = 1, int slice = 0)
 {
@@ -1139,7 +1158,7 @@ __device__ __forceinline__ void copy_items(const Plan &p, int64_t first, int cou
                 sg.rows = r1 - r0;
             }
             if (sg.rows > 0)
-                copy_segment<U, HINT, NC>(sg, v, lane);
+                copy_any_segment<U, HINT, NC, ROWS>(sg, v, lane);
         }
         return;
     }
@@ -1159,11 +1178,11 @@ __device__ __forceinline__ void copy_items(const Plan &p, int64_t first, int cou
     for (int k = 0; k < count; ++k) {
         const Segment sk = shfl_segment(sg, k);
         if (valid & (1u << k))
-            copy_segment<U, HINT, NC>(sk, v, lane);
+            copy_any_segment<U, HINT, NC, ROWS>(sk, v, lane);
     }
 }
 
-template <int U, bool BATCHED>
+template <int U, bool BATCHED, bool ROWS>
 __global__ void __launch_bounds__(1024, 1)
     kvx_roundtrip_kernel(const Plan ps, const Plan pl, const RoundTripSync sy)
 {
@@ -1196,11 +1215,12 @@ __global__ void __launch_bounds__(1024, 1)
         }
         if (what == kUnitLoad) {
             // Short (batched) segments fill at most a few loads per lane: four are enough.
-            copy_items<(BATCHED && U > 4 ? 4 : U), KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED,
-                       false>(pl, first, count, lane, sy.slices, slice);
+            copy_items<((BATCHED || ROWS) && U > 4 ? 4 : U), KVX_DIR_SCATTER,
+                       KVX_HINT_STREAMING, BATCHED, false, ROWS>(pl, first, count, lane,
+                                                                 sy.slices, slice);
         } else {
             // HBM reads need fewer bytes in flight than host reads: four loads per lane.
-            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
+            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true, ROWS>(
                 ps, first, count, lane, sy.slices, slice);
             // Each lane's host writes are performed at GPU scope, then lane 0 publishes the
             // unit with a release (the fence costs nothing measurable, and it keeps the
@@ -1286,13 +1306,35 @@ DuplexFn pick_duplex(int unroll, bool batched)
 
 typedef void (*RoundTripFn)(Plan, Plan, RoundTripSync);
 
-RoundTripFn pick_roundtrip(int unroll, bool batched)
+// The round-trip kernel for (unroll, batched), walking strided rows as one sequence when rows
+// (chunks include a token-major one of several slabs) and the segments are long enough to
+// take one unit each: there the plain copy's row at a time costs most.  The row walk holds
+// at most 4 loads in flight per lane, and batched round trips keep the plain copy (the walk
+// beside a batch's descriptors spilled).
+RoundTripFn pick_roundtrip(int unroll, bool batched, bool rows = false)
 {
+    if (rows && !batched) {
+        switch (unroll) {
+        case 1: return kvx_roundtrip_kernel<1, false, true>;
+        case 2: return kvx_roundtrip_kernel<2, false, true>;
+        case 4:
+        case 8: return kvx_roundtrip_kernel<4, false, true>;
+        }
+        return nullptr;
+    }
     switch (unroll) {
-    case 1: return batched ? kvx_roundtrip_kernel<1, true> : kvx_roundtrip_kernel<1, false>;
-    case 2: return batched ? kvx_roundtrip_kernel<2, true> : kvx_roundtrip_kernel<2, false>;
-    case 4: return batched ? kvx_roundtrip_kernel<4, true> : kvx_roundtrip_kernel<4, false>;
-    case 8: return batched ? kvx_roundtrip_kernel<8, true> : kvx_roundtrip_kernel<8, false>;
+    case 1:
+        return batched ? kvx_roundtrip_kernel<1, true, false>
+                       : kvx_roundtrip_kernel<1, false, false>;
+    case 2:
+        return batched ? kvx_roundtrip_kernel<2, true, false>
+                       : kvx_roundtrip_kernel<2, false, false>;
+    case 4:
+        return batched ? kvx_roundtrip_kernel<4, true, false>
+                       : kvx_roundtrip_kernel<4, false, false>;
+    case 8:
+        return batched ? kvx_roundtrip_kernel<8, true, false>
+                       : kvx_roundtrip_kernel<8, false, false>;
     }
     return nullptr;
 }
