@@ -538,7 +538,7 @@ cudaError_t launch_duplex_kernel(const LaunchShape &sh, Plan ps, Plan pl, Duplex
 
 // Exchange grid: sm_cap covers both directions, half of the CTAs per direction.
 LaunchShape exchange_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps,
-                           const Plan &pl)
+                           const Plan &pl, bool rows)
 {
     LaunchShape sh;
     const int64_t warps_per_cta = cfg.threads / 32;
@@ -553,7 +553,7 @@ LaunchShape exchange_shape(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const 
         role = per_dir;
     sh.ctas = 2 * role;
     sh.threads = cfg.threads;
-    sh.fn = reinterpret_cast<const void *>(pick_exchange(cfg.unroll, ps.batch, pl.batch));
+    sh.fn = reinterpret_cast<const void *>(pick_exchange(cfg.unroll, ps.batch, pl.batch, rows));
     return sh;
 }
 
@@ -619,7 +619,9 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
         e = stage(ctx, *slot, total, 0, 0, s);
         if (e != cudaSuccess)
             return cuda_err(ctx, e, "descriptor copy");
-        shape = exchange_shape(ctx, cfg, ps, pl);
+        shape = exchange_shape(ctx, cfg, ps, pl,
+                               strided_rows(pool, schunks, n_schunks) ||
+                                   strided_rows(pool, lchunks, n_lchunks));
         e = launch_exchange_kernel(shape, ps, pl, s);
     }
     if (e != cudaSuccess)
@@ -887,7 +889,9 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
     }
     p->shared = exchange_shared(p->plan, p->load);
     if (!p->shared) {
-        p->shape = exchange_shape(ctx, cfg, p->plan, p->load);
+        p->shape = exchange_shape(ctx, cfg, p->plan, p->load,
+                                  strided_rows(pool, schunks, n_schunks) ||
+                                      strided_rows(pool, lchunks, n_lchunks));
     } else if (!duplex_setup(ctx, cfg, p->plan, p->load,
                              reinterpret_cast<unsigned *>(p->dev + total), &p->sync, &p->shape)) {
         cudaFree(p->dev);

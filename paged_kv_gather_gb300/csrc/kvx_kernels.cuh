@@ -465,11 +465,9 @@ __device__ __forceinline__ void copy_any_segment(const Segment &sg, int64_t v, i
 // of more than one (layer, kv) slab: their page segments are strided on the chunk side, and
 // the plain copy moves such a segment one row and one unit per lane at a time.
 template <int U, int DIR, int HINT, bool BATCHED>
-__device__ __forceinline__ void run_row_segments(const Plan &p)
+__device__ __forceinline__ void run_row_segments(const Plan &p, int64_t warp, int64_t n_warps,
+                                                 int lane)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int64_t v = p.token_bytes;
     if (!BATCHED) {
         for (int64_t item = warp; item < p.total_items; item += n_warps) {
@@ -504,14 +502,20 @@ __device__ __forceinline__ void run_row_segments(const Plan &p)
 template <int U, int DIR, int HINT, bool BATCHED>
 __global__ void __launch_bounds__(1024, 1) kvx_rows_kernel(const Plan p)
 {
-    run_row_segments<U, DIR, HINT, BATCHED>(p);
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    run_row_segments<U, DIR, HINT, BATCHED>(p, warp, n_warps, lane);
 }
 
 template <int U, int DIR, int HINT, bool BATCHED>
 __global__ void __launch_bounds__(1024, 1) kvx_rows_overlap_kernel(const Plan p)
 {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     allow_next_launch();
-    run_row_segments<U, DIR, HINT, BATCHED>(p);
+    run_row_segments<U, DIR, HINT, BATCHED>(p, warp, n_warps, lane);
     wait_previous_grid();
 }
 
@@ -562,7 +566,8 @@ __global__ void __launch_bounds__(1024, 1) kvx_split_overlap_kernel(const Plan p
 // block scheduler spreads both directions evenly over the SMs the launch gets instead of
 // giving each direction its own contiguous block of SMs (two separate kernels), which
 // lets the two directions of the host link run at full rate together.
-template <int U, bool BATCHED_S, bool BATCHED_L>
+// ROWS: the row walk of run_row_segments (chunks include token-major ones of several slabs).
+template <int U, bool BATCHED_S, bool BATCHED_L, bool ROWS = false>
 __global__ void __launch_bounds__(1024, 1) kvx_exchange_kernel(const Plan ps, const Plan pl)
 {
     const int lane = threadIdx.x & 31;
@@ -571,11 +576,20 @@ __global__ void __launch_bounds__(1024, 1) kvx_exchange_kernel(const Plan ps, co
     const int64_t warp = role_cta * wpc + (threadIdx.x >> 5);
     if ((blockIdx.x & 1) == 0) {
         const int64_t ctas = (int64_t(gridDim.x) + 1) >> 1;
-        run_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S>(ps, warp, ctas * wpc, lane);
+        if (ROWS)
+            run_row_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S>(ps, warp,
+                                                                            ctas * wpc, lane);
+        else
+            run_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S>(ps, warp, ctas * wpc,
+                                                                        lane);
     } else {
         const int64_t ctas = int64_t(gridDim.x) >> 1;
-        run_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L>(pl, warp, ctas * wpc,
-                                                                        lane);
+        if (ROWS)
+            run_row_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L>(
+                pl, warp, ctas * wpc, lane);
+        else
+            run_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L>(pl, warp,
+                                                                            ctas * wpc, lane);
     }
 }
 
@@ -1449,21 +1463,35 @@ KernelFn pick_split(int unroll, int dir, int hint, bool overlap = false)
 
 typedef void (*ExchangeFn)(Plan, Plan);
 
-template <int U>
+template <int U, bool ROWS>
 ExchangeFn pick_exchange_u(bool bs, bool bl)
 {
     if (bs)
-        return bl ? kvx_exchange_kernel<U, true, true> : kvx_exchange_kernel<U, true, false>;
-    return bl ? kvx_exchange_kernel<U, false, true> : kvx_exchange_kernel<U, false, false>;
+        return bl ? kvx_exchange_kernel<U, true, true, ROWS>
+                  : kvx_exchange_kernel<U, true, false, ROWS>;
+    return bl ? kvx_exchange_kernel<U, false, true, ROWS>
+              : kvx_exchange_kernel<U, false, false, ROWS>;
 }
 
-ExchangeFn pick_exchange(int unroll, int batch_s, int batch_l)
+// The role-split exchange kernel; rows: the row-walking variant (at most 4 loads in flight
+// per lane), for chunks that include a token-major one of several slabs.
+ExchangeFn pick_exchange(int unroll, int batch_s, int batch_l, bool rows = false)
 {
+    const bool bs = batch_s > 1, bl = batch_l > 1;
+    if (rows) {
+        switch (unroll) {
+        case 1: return pick_exchange_u<1, true>(bs, bl);
+        case 2: return pick_exchange_u<2, true>(bs, bl);
+        case 4:
+        case 8: return pick_exchange_u<4, true>(bs, bl);
+        }
+        return nullptr;
+    }
     switch (unroll) {
-    case 1: return pick_exchange_u<1>(batch_s > 1, batch_l > 1);
-    case 2: return pick_exchange_u<2>(batch_s > 1, batch_l > 1);
-    case 4: return pick_exchange_u<4>(batch_s > 1, batch_l > 1);
-    case 8: return pick_exchange_u<8>(batch_s > 1, batch_l > 1);
+    case 1: return pick_exchange_u<1, false>(bs, bl);
+    case 2: return pick_exchange_u<2, false>(bs, bl);
+    case 4: return pick_exchange_u<4, false>(bs, bl);
+    case 8: return pick_exchange_u<8, false>(bs, bl);
     }
     return nullptr;
 }
