@@ -84,7 +84,8 @@ def parse():
     p.add_argument("--profile-op", default="load",
                    choices=["store", "load", "gather", "scatter", "exchange", "roundtrip",
                             "exchange_shared", "gather_cta", "load_bulk", "store_bulk",
-                            "load_4sm"],
+                            "load_4sm", "store_token_major", "load_token_major",
+                            "roundtrip_token_major"],
                    help="operation of --workload profile_small")
     p.add_argument("--groups", type=int, default=16,
                    help="chunk groups of the pipelined store/load round trip")
@@ -1736,7 +1737,8 @@ def run_eviction(args, kvx, wl):
 def run_profile_small(args, kvx, wl):
     """A small case for ncu captures: the Llama-3.1-8B shape cut to 8192 tokens (1 GiB per
     direction, above the 129 MB L2) in a 1024-page pool (2 GiB), one operation 3 times
-    with the library's default launch configuration."""
+    with the library's default launch configuration.  The *_token_major operations use
+    token-major chunks of 16 tokens over all layers instead of the layer-major ones."""
     w = wl.llama8b(num_pages=1024, n_tokens=8192)
     s = w.shape
     pools = _pool_tensor(s, w.seed, wl)
@@ -1747,17 +1749,23 @@ def run_profile_small(args, kvx, wl):
     rd = kvx.requests_array([(pd.data_ptr(), dst.page_table, dst.n_tokens)])
     ctx = kvx.kvx_create(0)
     sh = torch.cuda.current_stream().cuda_stream
+    specs = w.store_chunks
+    if args.profile_op.endswith("_token_major"):  # 16-token chunks over all layers (2 MiB)
+        specs = wl.split_tokens(0, 0, src.n_tokens, 16, 0, s.num_layers, wl.TOKEN_MAJOR)
+        wl.place_chunks(specs, s)
     if args.profile_op in ("store", "load", "exchange", "roundtrip", "exchange_shared",
-                           "load_bulk", "store_bulk", "load_4sm"):
-        buf = kvx.HostBuffer(w.store_arena_bytes)
+                           "load_bulk", "store_bulk", "load_4sm", "store_token_major",
+                           "load_token_major", "roundtrip_token_major"):
+        buf = kvx.HostBuffer(wl._arena_bytes(specs, s))
         buf.array[:] = 0
-        ch = kvx.chunks_array(w.store_chunks, buf.ptr)
+        ch = kvx.chunks_array(specs, buf.ptr)
     else:
         dchunk = torch.zeros(w.store_arena_bytes, dtype=torch.uint8, device="cuda")
         ch = kvx.chunks_array(w.store_chunks, dchunk.data_ptr())
     half = len(w.store_chunks) // 2
     for _ in range(3):
-        if args.profile_op == "roundtrip":  # store every chunk and load it into other pages
+        if args.profile_op in ("roundtrip", "roundtrip_token_major"):
+            # store every chunk and load it into other pages
             kvx.kvx_roundtrip_chunks(ctx, pool, rs, rd, ch, stream=sh)
         elif args.profile_op == "exchange_shared":  # store a quarter, load three quarters
             q = len(w.store_chunks) // 4
@@ -1779,9 +1787,9 @@ def run_profile_small(args, kvx, wl):
         elif args.profile_op == "exchange":  # store the first half, load the second half
             kvx.kvx_exchange_chunks(ctx, pool, rs, np.ascontiguousarray(ch[:half]), rd,
                                     np.ascontiguousarray(ch[half:]), stream=sh)
-        elif args.profile_op == "store":
+        elif args.profile_op in ("store", "store_token_major"):
             kvx.kvx_store_chunks(ctx, pool, rs, ch, stream=sh)
-        elif args.profile_op == "load":
+        elif args.profile_op in ("load", "load_token_major"):
             kvx.kvx_load_chunks(ctx, pool, rd, ch, stream=sh)
         else:
             d = kvx.KVX_DIR_GATHER if args.profile_op == "gather" else kvx.KVX_DIR_SCATTER
@@ -1790,7 +1798,8 @@ def run_profile_small(args, kvx, wl):
     torch.cuda.synchronize()
     assert kvx.kvx_get_status(ctx, sh) == 0
     items, ctas, threads, _ = kvx.kvx_last_launch(ctx)
-    _emit({"workload": "profile_small", "op": args.profile_op, "bytes": w.store_bytes(),
+    _emit({"workload": "profile_small", "op": args.profile_op,
+           "bytes": sum(c.nbytes(s) for c in specs),
            "items": items, "ctas": ctas, "threads": threads})
     kvx.kvx_destroy(ctx)
 
