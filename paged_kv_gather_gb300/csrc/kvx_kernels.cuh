@@ -14,8 +14,10 @@
 // (section "Non-Intrusive Resource Sizing"); the HBM-only transform uses every SM.
 //
 // Kernels: kvx_segment_kernel (store, load, HBM gather/scatter; the default mapping),
+// kvx_rows_kernel (the same for chunks whose page segments are strided rows),
 // kvx_split_kernel (the same for batches with fewer segments than warps, in row slices),
-// their overlapped variants kvx_segment_overlap_kernel and kvx_split_overlap_kernel,
+// their overlapped variants kvx_segment_overlap_kernel, kvx_rows_overlap_kernel and
+// kvx_split_overlap_kernel,
 // kvx_exchange_kernel and kvx_duplex_kernel (a store batch and a load batch in one launch),
 // kvx_roundtrip_kernel (store, then load the same chunks elsewhere, ordered per unit inside
 // the launch), and two alternative mappings of a single transfer: kvx_cta_kernel (a whole
