@@ -571,8 +571,9 @@ def flat_extras(seq, few, mla, qwen, l70, evict, link):
         f["cfg4_qwen7b_bound_ms"] = qwen["bound_ms"]
         f["cfg4_exchange_frac_of_bound"] = qwen["exchange_one_launch"]["frac_of_bound"]
         f["cfg4_two_streams_frac_of_bound"] = qwen["two_streams"]["frac_of_bound"]
-        f["cfg4_two_streams_store_8sm_frac_of_bound"] = \
-            qwen["two_streams_store_8sm"]["frac_of_bound"]
+        for cap in (8, 6):
+            f[f"cfg4_two_streams_store_{cap}sm_frac_of_bound"] = \
+                qwen[f"two_streams_store_{cap}sm"]["frac_of_bound"]
         tp = qwen.get("two_partitions", {})
         if "frac_of_bound" in tp:
             f["cfg4_two_partitions_frac_of_bound"] = tp["frac_of_bound"]
@@ -1188,7 +1189,7 @@ def concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, sa, sb, cfg_l, 
 
 def qwen7b_measure(args, kvx, wl, link, reps=5, partition_sms=16):
     """Batched partial hits: the load batch and the store batch alone, on two plain streams
-    at once (default grids, and the store on 8 SMs), on two streams of two I/O partitions
+    at once (default grids, and the store on 8 and on 6 SMs), on two streams of two I/O partitions
     (green contexts) at once, and in one exchange launch; each against the bound
     max(load / H2D, store / D2H, both / bidir)."""
     w, pools, pool, dev_tables, reqs, ld, st, ch_ld, ch_st = qwen7b_setup(kvx, wl)
@@ -1218,15 +1219,16 @@ def qwen7b_measure(args, kvx, wl, link, reps=5, partition_sms=16):
     # Two plain streams with the store on 8 SMs: beside a load that saturates H2D a store
     # gets about 10 GB/s per SM, so 8 SMs finish it well inside the bound while taking no
     # link bandwidth the load needs; on its default 16 SMs it takes ~160 GB/s from the load.
-    cfg_s8 = kvx.kvx_default_launch_cfg(ctx_b, kvx.KVX_OP_STORE)
-    cfg_s8.sm_cap = 8
-    la8, sb8, both8 = concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, sa, sb,
-                                      None, cfg_s8, reps)
-    out["two_streams_store_8sm"] = {"load_gbs": round(Nl / (la8 * 1e-3) / GB, 2),
-                                    "store_gbs": round(Ns / (sb8 * 1e-3) / GB, 2),
-                                    "aggregate_gbs": round((Nl + Ns) / (both8 * 1e-3) / GB, 2),
-                                    "ms": round(both8, 3),
-                                    "frac_of_bound": round(bound_ms / both8, 4)}
+    for cap in (8, 6):
+        cfg_sc = kvx.kvx_default_launch_cfg(ctx_b, kvx.KVX_OP_STORE)
+        cfg_sc.sm_cap = cap
+        lac, sbc, bothc = concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, sa, sb,
+                                          None, cfg_sc, reps)
+        out[f"two_streams_store_{cap}sm"] = {
+            "load_gbs": round(Nl / (lac * 1e-3) / GB, 2),
+            "store_gbs": round(Ns / (sbc * 1e-3) / GB, 2),
+            "aggregate_gbs": round((Nl + Ns) / (bothc * 1e-3) / GB, 2),
+            "ms": round(bothc, 3), "frac_of_bound": round(bound_ms / bothc, 4)}
     # Two I/O partitions, one per stream, so the two kernels run on fixed disjoint SM sets.
     try:
         part = kvx.kvx_partition_create(0, partition_sms, -1, 0, io_groups=2)

@@ -70,6 +70,7 @@ def test_flat_extras_are_scalars_named_for_their_leg():
     qwen = {"bound_ms": 51.0, "exchange_one_launch": {"frac_of_bound": 0.978},
             "two_streams": {"frac_of_bound": 0.93},
             "two_streams_store_8sm": {"frac_of_bound": 0.975},
+            "two_streams_store_6sm": {"frac_of_bound": 0.977},
             "two_partitions": {"unavailable": "no green contexts"}}
     leg = {"load_overlap_gbs": 200.0, "gemm_slowdown_pct": 3.5, "e2e_vs_model": 1.02}
     l70 = {"bulk_6sm": leg, "bulk_5sm": leg, "bulk_4sm": leg, "segment_16sm": leg,
@@ -80,6 +81,7 @@ def test_flat_extras_are_scalars_named_for_their_leg():
     assert f["store_frac"] == 0.996 and f["load_frac"] == 0.997
     assert f["sm4_load_bulk_frac"] == 0.95 and f["cfg5_mla_p1_store_frac"] == 0.96
     assert f["cfg4_exchange_frac_of_bound"] == 0.978
+    assert f["cfg4_two_streams_store_6sm_frac_of_bound"] == 0.977
     assert "cfg4_two_partitions_frac_of_bound" not in f  # an unavailable leg is left out
     assert f["cfg3_bulk_5sm_load_overlap_frac"] == round(200.0 / 211.6, 4)
     assert "cfg3_partition_16sm_gemm_slowdown_pct" not in f
