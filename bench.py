@@ -571,7 +571,7 @@ def flat_extras(seq, few, mla, qwen, l70, evict, link):
         f["cfg4_qwen7b_bound_ms"] = qwen["bound_ms"]
         f["cfg4_exchange_frac_of_bound"] = qwen["exchange_one_launch"]["frac_of_bound"]
         f["cfg4_two_streams_frac_of_bound"] = qwen["two_streams"]["frac_of_bound"]
-        for cap in (8, 6):
+        for cap in (16, 6):
             f[f"cfg4_two_streams_store_{cap}sm_frac_of_bound"] = \
                 qwen[f"two_streams_store_{cap}sm"]["frac_of_bound"]
         tp = qwen.get("two_partitions", {})
@@ -1189,9 +1189,9 @@ def concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, sa, sb, cfg_l, 
 
 def qwen7b_measure(args, kvx, wl, link, reps=5, partition_sms=16):
     """Batched partial hits: the load batch and the store batch alone, on two plain streams
-    at once (default grids, and the store on 8 and on 6 SMs), on two streams of two I/O partitions
-    (green contexts) at once, and in one exchange launch; each against the bound
-    max(load / H2D, store / D2H, both / bidir)."""
+    at once (default grids, the store on 8 SMs; and the store on 16 or 6 SMs), on the streams
+    of two I/O partitions (green contexts) at once, and in one exchange launch; each against
+    the bound max(load / H2D, store / D2H, both / bidir)."""
     w, pools, pool, dev_tables, reqs, ld, st, ch_ld, ch_st = qwen7b_setup(kvx, wl)
     ctx_a, ctx_b = kvx.kvx_create(0, 64 << 20), kvx.kvx_create(0, 64 << 20)
     sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
@@ -1216,10 +1216,11 @@ def qwen7b_measure(args, kvx, wl, link, reps=5, partition_sms=16):
                            "store_gbs": round(Ns / (sbm * 1e-3) / GB, 2),
                            "aggregate_gbs": round((Nl + Ns) / (both * 1e-3) / GB, 2),
                            "ms": round(both, 3), "frac_of_bound": round(bound_ms / both, 4)}}
-    # Two plain streams with the store on 8 SMs: beside a load that saturates H2D a store
-    # gets about 10 GB/s per SM, so 8 SMs finish it well inside the bound while taking no
-    # link bandwidth the load needs; on its default 16 SMs it takes ~160 GB/s from the load.
-    for cap in (8, 6):
+    # Two plain streams with the store on 16 or 6 SMs instead of its default 8: beside a load
+    # that saturates H2D a store gets about 10 GB/s per SM, so 6-8 SMs finish it well inside
+    # the bound while taking no link bandwidth the load needs; on 16 SMs it takes ~160 GB/s
+    # from the load.
+    for cap in (16, 6):
         cfg_sc = kvx.kvx_default_launch_cfg(ctx_b, kvx.KVX_OP_STORE)
         cfg_sc.sm_cap = cap
         lac, sbc, bothc = concurrent_pair(kvx, ctx_a, ctx_b, pool, reqs, ch_ld, ch_st, sa, sb,

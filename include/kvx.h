@@ -235,15 +235,16 @@ kvx_status kvx_default_launch_cfg(const kvx_ctx *ctx, int op, kvx_launch_cfg *cf
 /* store: gather every covered (layer, kv, token) vector from the page pools into the
  * chunks ("Strata Guide", section "Non-Intrusive Resource Sizing": eviction to host
  * memory; "Tutti", section 7: store_layer(layer_id, block_ids)).  Chunks live in mapped
- * pinned host memory.  cfg may be NULL: the defaults of kvx_default_launch_cfg, except that
- * page segments (page_size x token_bytes) shorter than 4 KiB get 32 SMs instead of 16, since
- * a warp then moves one short segment per pass.  Asynchronous on `stream`.
+ * pinned host memory.  cfg may be NULL: the defaults of kvx_default_launch_cfg (8 SMs,
+ * which carry the device-to-host peak on GB300), except that page segments
+ * (page_size x token_bytes) shorter than 4 KiB get 32 SMs, since a warp then moves one
+ * short segment per pass.  Asynchronous on `stream`.
  * A store issued beside a load that needs the whole host-to-device peak (a prefetch on
  * another stream) takes link bandwidth from it in proportion to its SMs (on GB300 about
- * 10 GB/s per SM while the other direction is saturated), and where two kernels land on
- * the GPU varies from run to run.  Issue both batches with kvx_exchange_chunks, which
- * shares one grid between them; capping the store's SMs (cfg->sm_cap) at what it needs to
- * finish in time is the fallback for batches that cannot be issued together. */
+ * 10 GB/s per SM while the other direction is saturated), which is why the default grid
+ * stays at 8 SMs; where two kernels land on the GPU still varies from run to run.  Batches
+ * that can be issued together are best issued with kvx_exchange_chunks, which shares one
+ * grid between them. */
 kvx_status kvx_store_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request *reqs,
                             int n_req, const kvx_chunk *chunks, int n_chunks,
                             int layer_begin, int layer_end, const kvx_launch_cfg *cfg,

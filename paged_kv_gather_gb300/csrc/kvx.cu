@@ -128,8 +128,9 @@ void defaults_for(const kvx_ctx *ctx, int op, kvx_launch_cfg *c)
     c->batch = 0;
     c->overlap = 0;
     switch (op) {
-    case KVX_OP_STORE:
-        c->sm_cap = 16;
+    case KVX_OP_STORE:  // 8 SMs carry the device-to-host peak (about 45 GB/s each) and
+                        // leave a concurrent load its own
+        c->sm_cap = 8;
         c->ctas_per_sm = 1;
         c->threads = 1024;
         c->unroll = 8;
@@ -433,7 +434,7 @@ void apply_batch(int op, const kvx_launch_cfg &cfg, Plan *plan)
 }
 
 // With no configuration given, a store or load of page segments shorter than
-// kShortSegmentBytes runs on 32 SMs instead of the default 16, as the round trip does for
+// kShortSegmentBytes runs on 32 SMs instead of the default 8 or 16, as the round trip does for
 // its short segments: a warp then moves one short segment per pass and the link needs more
 // warps to keep enough host accesses in flight.  Call after validation (the pool is sound).
 void short_segment_grid(int op, const kvx_launch_cfg *user, const kvx_pool *pool,

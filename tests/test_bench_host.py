@@ -69,7 +69,7 @@ def test_flat_extras_are_scalars_named_for_their_leg():
            "p16": {"store_frac": 0.99, "load_frac": 0.99}}
     qwen = {"bound_ms": 51.0, "exchange_one_launch": {"frac_of_bound": 0.978},
             "two_streams": {"frac_of_bound": 0.93},
-            "two_streams_store_8sm": {"frac_of_bound": 0.975},
+            "two_streams_store_16sm": {"frac_of_bound": 0.92},
             "two_streams_store_6sm": {"frac_of_bound": 0.977},
             "two_partitions": {"unavailable": "no green contexts"}}
     leg = {"load_overlap_gbs": 200.0, "gemm_slowdown_pct": 3.5, "e2e_vs_model": 1.02}

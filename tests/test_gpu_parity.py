@@ -428,12 +428,16 @@ def test_random_bulk_shapes(ctx, stream):
         arena.close()
 
 
-@pytest.mark.parametrize("v,P,cfg_given,ctas", [(256, 8, False, 32), (256, 8, True, 16),
-                                                (1024, 8, False, 16), (1024, 2, False, 32)])
-def test_store_load_default_grid_follows_segment_size(ctx, stream, v, P, cfg_given, ctas):
+@pytest.mark.parametrize("v,P,cfg_given,ctas_s,ctas_l", [(256, 8, False, 32, 32),
+                                                          (256, 8, True, 8, 16),
+                                                          (1024, 8, False, 8, 16),
+                                                          (1024, 2, False, 32, 32)])
+def test_store_load_default_grid_follows_segment_size(ctx, stream, v, P, cfg_given, ctas_s,
+                                                      ctas_l):
     """With no configuration, a store or load of page segments shorter than 4 KiB runs on 32
-    SMs (one CTA each), longer ones on the default 16; an explicit configuration keeps its
-    own SM cap, and a plan follows the same rule.  Checked against the oracle either way."""
+    SMs (one CTA each), longer ones on the defaults (8 SMs for a store, 16 for a load); an
+    explicit configuration keeps its own SM cap, and a plan follows the same rule.  Checked
+    against the oracle either way."""
     rng = np.random.default_rng(8400 + v + P + int(cfg_given))
     L, KV, T = 8, 2, 16384  # enough segments for 32 CTAs of 32 warps resolving 16 each
     npg = T // P
@@ -450,13 +454,13 @@ def test_store_load_default_grid_follows_segment_size(ctx, stream, v, P, cfg_giv
     cs = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_STORE) if cfg_given else None
     cl = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_LOAD) if cfg_given else None
     _store(ctx, "store", dpool, src, specs, arena, 0, None, cs, stream)
-    assert kvx.kvx_last_launch(ctx)[1] == ctas
+    assert kvx.kvx_last_launch(ctx)[1] == ctas_s
     assert_bytes_equal(arena.numpy(), expected_store(dpool, src, specs, nbytes), "store")
     data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
     arena.write(data)
     pre = dpool.host_copy()
     _load(ctx, "load", dpool, dst, specs, arena, 0, None, cl, stream)
-    assert kvx.kvx_last_launch(ctx)[1] == ctas
+    assert kvx.kvx_last_launch(ctx)[1] == ctas_l
     assert_pool_equal(dpool, expected_load(pre, dst, specs, data.copy()))
     # A prepared load plan made without a configuration takes the same grid.
     plan = kvx.kvx_plan_create(ctx, kvx.KVX_OP_LOAD, dpool.pool, dst.array,

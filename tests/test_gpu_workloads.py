@@ -303,10 +303,10 @@ def test_llama70b_layer_streamed_load_full_size(ctx, tokens_per_chunk, mapping):
 
 # ----------------------------------------------------------------------------- qwen7b_batch
 
-@pytest.mark.parametrize("placement", ["streams", "store_8sm", "store_6sm", "partitions"])
+@pytest.mark.parametrize("placement", ["streams", "store_16sm", "store_6sm", "partitions"])
 def test_qwen7b_batched_concurrent_load_and_store_full_size(ctx, placement):
     """The batched load and store at once on two plain streams (default grids, or the store
-    on 8 or 6 SMs), or on the streams of two 16-SM I/O partitions (green contexts), as the
+    on 16 or 6 SMs), or on the streams of two 16-SM I/O partitions (green contexts), as the
     bench measures them."""
     w = wl.qwen7b_batch()
     s = w.shape
@@ -330,8 +330,8 @@ def test_qwen7b_batched_concurrent_load_and_store_full_size(ctx, placement):
             cs = _io_cfg(ctx2, kvx.KVX_OP_STORE, 0)
         else:
             sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
-            if placement in ("store_8sm", "store_6sm"):
-                cs = _io_cfg(ctx2, kvx.KVX_OP_STORE, int(placement[6]))
+            if placement in ("store_16sm", "store_6sm"):
+                cs = _io_cfg(ctx2, kvx.KVX_OP_STORE, int(placement[6:-2]))
         pool = kvx.Pool.from_tensor(pools, s.page_size)
         torch.cuda.synchronize()
         kvx.kvx_load_chunks(ctx, pool, reqs.array, kvx.chunks_array(w.load_chunks, ld.ptr),
