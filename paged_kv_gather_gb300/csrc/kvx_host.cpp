@@ -511,7 +511,8 @@ kvx_status kvx_estimate_us(const kvx_link_model *m, int op, int64_t bytes,
         return KVX_ERR_INVALID_ARG;
     // The operation's defaults when no configuration is given (kept in step with the
     // library's kvx_default_launch_cfg).
-    int sm_cap = op <= KVX_OP_LOAD ? 16 : 0, ctas = op <= KVX_OP_LOAD ? 1 : 2;
+    int sm_cap = op == KVX_OP_STORE ? 8 : (op == KVX_OP_LOAD ? 16 : 0);
+    int ctas = op <= KVX_OP_LOAD ? 1 : 2;
     int threads = op <= KVX_OP_LOAD ? 1024 : 256, unroll = op <= KVX_OP_LOAD ? 8 : 4;
     bool bulk = false;
     double stage_bytes = 32768.0;

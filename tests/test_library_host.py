@@ -275,6 +275,16 @@ def test_estimator_littles_law_and_link_cap():
     c.sm_cap = 4
     us = kvx.kvx_estimate_us(m, kvx.KVX_OP_LOAD, N, c)
     assert N / ((us - m.launch_us) * 1e3) == pytest.approx(min(m.h2d_gbs, 4 * 4 * 32768 / 2600.0))
+    # Without a configuration: the defaults, a store on 8 SMs and a load on 16 (both already
+    # at their link's peak by Little's law).
+    for op, sms in ((kvx.KVX_OP_STORE, 8), (kvx.KVX_OP_LOAD, 16)):
+        c = kvx.kvx_launch_cfg()
+        c.sm_cap, c.ctas_per_sm, c.threads, c.unroll = sms, 1, 1024, 8
+        assert kvx.kvx_estimate_us(m, op, N, None) == pytest.approx(
+            kvx.kvx_estimate_us(m, op, N, c))
+    c.sm_cap = 2  # a quarter of the store's default grid: below the D2H peak
+    assert kvx.kvx_estimate_us(m, kvx.KVX_OP_STORE, N, c) > kvx.kvx_estimate_us(
+        m, kvx.KVX_OP_STORE, N, None)
     # The HBM transform moves 2N through HBM at the copy peak, whatever the SM cap.
     us = kvx.kvx_estimate_us(m, kvx.KVX_OP_GATHER_HBM, N, None)
     assert us == pytest.approx(m.launch_us + 2 * N / (m.hbm_gbs * 1e3))
