@@ -444,8 +444,9 @@ __device__ __forceinline__ void copy_segment_rows(const Segment &sg, int64_t v, 
                                lane);
 }
 
-// The row walk as a call of its own, for the round trip: inlined there for both directions
-// beside the unit scheduling, it spilled.
+// The row walk as a call of its own, for the kernels that move both directions (the round
+// trip and the exchange): inlined there twice, beside their other state, it spilled, and
+// the spills cost the token-major exchange a quarter of its bandwidth.
 template <int U, int HINT, bool NC>
 __device__ __noinline__ void copy_segment_rows_call(const Segment sg, int64_t v, int lane)
 {
@@ -463,10 +464,21 @@ __device__ __forceinline__ void copy_any_segment(const Segment &sg, int64_t v, i
         copy_segment<U, HINT, NC>(sg, v, lane);
 }
 
+// One segment of run_row_segments: the row walk inline, or out of line when CALL.
+template <int U, int HINT, bool CALL>
+__device__ __forceinline__ void copy_row_segment(const Segment &sg, int64_t v, int lane)
+{
+    if (CALL)
+        copy_segment_rows_call<U, HINT, true>(sg, v, lane);
+    else
+        copy_segment_rows<U, HINT>(sg, v, lane);
+}
+
 // The warp-segment walk of run_segments for launches whose chunks include token-major ones
 // of more than one (layer, kv) slab: their page segments are strided on the chunk side, and
-// the plain copy moves such a segment one row and one unit per lane at a time.
-template <int U, int DIR, int HINT, bool BATCHED>
+// the plain copy moves such a segment one row and one unit per lane at a time.  CALL: the
+// walk out of line (copy_segment_rows_call).
+template <int U, int DIR, int HINT, bool BATCHED, bool CALL = false>
 __device__ __forceinline__ void run_row_segments(const Plan &p, int64_t warp, int64_t n_warps,
                                                  int lane)
 {
@@ -475,7 +487,7 @@ __device__ __forceinline__ void run_row_segments(const Plan &p, int64_t warp, in
         for (int64_t item = warp; item < p.total_items; item += n_warps) {
             Segment sg;
             if (resolve_segment<DIR>(p, item, lane, sg))
-                copy_segment_rows<U, HINT>(sg, v, lane);
+                copy_row_segment<U, HINT, CALL>(sg, v, lane);
         }
         return;
     }
@@ -496,7 +508,7 @@ __device__ __forceinline__ void run_row_segments(const Plan &p, int64_t warp, in
         for (int k = 0; k < B; ++k) {
             const Segment s = shfl_segment(sg, k);
             if (valid & (1u << k))
-                copy_segment_rows<U, HINT>(s, v, lane);
+                copy_row_segment<U, HINT, CALL>(s, v, lane);
         }
     }
 }
@@ -568,7 +580,8 @@ __global__ void __launch_bounds__(1024, 1) kvx_split_overlap_kernel(const Plan p
 // block scheduler spreads both directions evenly over the SMs the launch gets instead of
 // giving each direction its own contiguous block of SMs (two separate kernels), which
 // lets the two directions of the host link run at full rate together.
-// ROWS: the row walk of run_row_segments (chunks include token-major ones of several slabs).
+// ROWS: the row walk of run_row_segments, out of line (chunks include token-major ones of
+// several slabs).
 template <int U, bool BATCHED_S, bool BATCHED_L, bool ROWS = false>
 __global__ void __launch_bounds__(1024, 1) kvx_exchange_kernel(const Plan ps, const Plan pl)
 {
@@ -579,15 +592,15 @@ __global__ void __launch_bounds__(1024, 1) kvx_exchange_kernel(const Plan ps, co
     if ((blockIdx.x & 1) == 0) {
         const int64_t ctas = (int64_t(gridDim.x) + 1) >> 1;
         if (ROWS)
-            run_row_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S>(ps, warp,
-                                                                            ctas * wpc, lane);
+            run_row_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S, true>(
+                ps, warp, ctas * wpc, lane);
         else
             run_segments<U, KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED_S>(ps, warp, ctas * wpc,
                                                                         lane);
     } else {
         const int64_t ctas = int64_t(gridDim.x) >> 1;
         if (ROWS)
-            run_row_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L>(
+            run_row_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L, true>(
                 pl, warp, ctas * wpc, lane);
         else
             run_segments<U, KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED_L>(pl, warp,
