@@ -1511,7 +1511,8 @@ def run_token_major(args, kvx, wl):
     """Store and load of the MLA latent (1, 2 and 16 tokens per page) and of the llama8b
     request in token-major chunks of about 2 MiB over all layers, whose page segments of more
     than one token are strided rows on the chunk side, on 4 and 16 SMs and without a
-    configuration, and the one-launch round trip without a configuration."""
+    configuration, and the one-launch round trip and an exchange of two such batches
+    without a configuration."""
     ctx = kvx.kvx_create(0, 64 << 20)
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
@@ -1543,10 +1544,19 @@ def run_token_major(args, kvx, wl):
                     c.sm_cap = cap
                 ms = _timed(stream, lambda: fn(ctx, pool, rq, ch, 0, s.num_layers, c, sh), 3)
                 row[f"{op_name}_gbs"] = round(N / (ms * 1e-3) / GB, 2)
-            if cap is None:  # the one-launch round trip, both directions
+            if cap is None:
+                # The one-launch round trip, both directions; and an exchange storing the
+                # request into the chunks while loading a second arena into the other pages.
                 ms = _timed(stream, lambda: kvx.kvx_roundtrip_chunks(
                     ctx, pool, rs, rd, ch, 0, s.num_layers, None, sh), 3)
                 row["roundtrip_gbs"] = round(2 * N / (ms * 1e-3) / GB, 2)
+                other = kvx.HostBuffer(wl._arena_bytes(specs, s))
+                other.array[:] = 0
+                ch2 = kvx.chunks_array(specs, other.ptr)
+                ms = _timed(stream, lambda: kvx.kvx_exchange_chunks(
+                    ctx, pool, rs, ch, rd, ch2, 0, s.num_layers, None, sh), 3)
+                row["exchange_gbs"] = round(2 * N / (ms * 1e-3) / GB, 2)
+                other.close()
             _emit(row)
         arena.close()
         del pools
