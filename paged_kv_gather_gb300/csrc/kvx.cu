@@ -508,7 +508,7 @@ bool exchange_shared(const Plan &ps, const Plan &pl)
 
 // Work counters and grid of a shared exchange; `next` is a zeroed 256-byte device word.
 bool duplex_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps, const Plan &pl,
-                  unsigned *next, DuplexSync *sy, LaunchShape *sh)
+                  unsigned *next, DuplexSync *sy, LaunchShape *sh, bool rows)
 {
     sy->unit_items = ps.batch;
     sy->units_s = (ps.total_items + sy->unit_items - 1) / sy->unit_items;
@@ -525,7 +525,7 @@ bool duplex_setup(const kvx_ctx *ctx, const kvx_launch_cfg &cfg, const Plan &ps,
         ctas = needed;
     sh->ctas = ctas;
     sh->threads = cfg.threads;
-    sh->fn = reinterpret_cast<const void *>(pick_duplex(cfg.unroll, ps.batch > 1));
+    sh->fn = reinterpret_cast<const void *>(pick_duplex(cfg.unroll, ps.batch > 1, rows));
     return true;
 }
 
@@ -604,10 +604,12 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     LaunchShape shape;
+    const bool rows =
+        strided_rows(pool, schunks, n_schunks) || strided_rows(pool, lchunks, n_lchunks);
     if (exchange_shared(ps, pl)) {
         DuplexSync sy;
         if (!duplex_setup(ctx, cfg, ps, pl, reinterpret_cast<unsigned *>(slot->dev + total), &sy,
-                          &shape))
+                          &shape, rows))
             return set_err(ctx, KVX_ERR_CAPACITY, "exchange batches of %lld and %lld segments "
                            "(%d and %d per warp) do not fit one shared launch",
                            (long long)ps.total_items, (long long)pl.total_items, ps.batch,
@@ -620,9 +622,7 @@ kvx_status launch_exchange(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
         e = stage(ctx, *slot, total, 0, 0, s);
         if (e != cudaSuccess)
             return cuda_err(ctx, e, "descriptor copy");
-        shape = exchange_shape(ctx, cfg, ps, pl,
-                               strided_rows(pool, schunks, n_schunks) ||
-                                   strided_rows(pool, lchunks, n_lchunks));
+        shape = exchange_shape(ctx, cfg, ps, pl, rows);
         e = launch_exchange_kernel(shape, ps, pl, s);
     }
     if (e != cudaSuccess)
@@ -889,12 +889,13 @@ kvx_status kvx_plan_create_exchange(kvx_ctx *ctx, const kvx_pool *pool,
         return cuda_err(ctx, e, "plan descriptor copy");
     }
     p->shared = exchange_shared(p->plan, p->load);
+    const bool rows =
+        strided_rows(pool, schunks, n_schunks) || strided_rows(pool, lchunks, n_lchunks);
     if (!p->shared) {
-        p->shape = exchange_shape(ctx, cfg, p->plan, p->load,
-                                  strided_rows(pool, schunks, n_schunks) ||
-                                      strided_rows(pool, lchunks, n_lchunks));
+        p->shape = exchange_shape(ctx, cfg, p->plan, p->load, rows);
     } else if (!duplex_setup(ctx, cfg, p->plan, p->load,
-                             reinterpret_cast<unsigned *>(p->dev + total), &p->sync, &p->shape)) {
+                             reinterpret_cast<unsigned *>(p->dev + total), &p->sync, &p->shape,
+                             rows)) {
         cudaFree(p->dev);
         delete p;
         return set_err(ctx, KVX_ERR_CAPACITY, "exchange batches do not fit one shared launch");

@@ -1292,7 +1292,7 @@ __device__ __forceinline__ long long next_duplex_unit(const DuplexSync &sy, int 
     return -1;
 }
 
-template <int U, bool BATCHED>
+template <int U, bool BATCHED, bool ROWS = false>
 __global__ void __launch_bounds__(1024, 1)
     kvx_duplex_kernel(const Plan ps, const Plan pl, const DuplexSync sy)
 {
@@ -1310,11 +1310,11 @@ __global__ void __launch_bounds__(1024, 1)
         if (what == kUnitLoad) {
             const int count = int(min(int64_t(sy.unit_items), pl.total_items - first));
             // Short (batched) segments fill at most a few loads per lane: four are enough.
-            copy_items<(BATCHED && U > 4 ? 4 : U), KVX_DIR_SCATTER, KVX_HINT_STREAMING, BATCHED,
-                       true>(pl, first, count, lane);
+            copy_items<((BATCHED || ROWS) && U > 4 ? 4 : U), KVX_DIR_SCATTER,
+                       KVX_HINT_STREAMING, BATCHED, true, ROWS>(pl, first, count, lane);
         } else {
             const int count = int(min(int64_t(sy.unit_items), ps.total_items - first));
-            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true>(
+            copy_items<(U > 4 ? 4 : U), KVX_DIR_GATHER, KVX_HINT_DEFAULT, BATCHED, true, ROWS>(
                 ps, first, count, lane);
         }
     }
@@ -1322,8 +1322,20 @@ __global__ void __launch_bounds__(1024, 1)
 
 typedef void (*DuplexFn)(Plan, Plan, DuplexSync);
 
-DuplexFn pick_duplex(int unroll, bool batched)
+// The shared-work exchange kernel for (unroll, batched); rows: strided token-major rows
+// walked as one sequence, out of line and at most 4 loads deep, for segments of one unit
+// each (batched ones keep the plain copy, as in the round trip).
+DuplexFn pick_duplex(int unroll, bool batched, bool rows = false)
 {
+    if (rows && !batched) {
+        switch (unroll) {
+        case 1: return kvx_duplex_kernel<1, false, true>;
+        case 2: return kvx_duplex_kernel<2, false, true>;
+        case 4:
+        case 8: return kvx_duplex_kernel<4, false, true>;
+        }
+        return nullptr;
+    }
     switch (unroll) {
     case 1: return batched ? kvx_duplex_kernel<1, true> : kvx_duplex_kernel<1, false>;
     case 2: return batched ? kvx_duplex_kernel<2, true> : kvx_duplex_kernel<2, false>;

@@ -528,6 +528,41 @@ def test_exchange_store_and_load_in_one_launch(ctx, stream, seed):
     inp.close()
 
 
+@pytest.mark.parametrize("load_share", [1.0, 0.3])
+def test_exchange_token_major_pages(ctx, stream, load_share):
+    """Exchanges of token-major chunks over all layers, 32 KiB pages of strided rows: equal
+    batches (the role-split kernel) and a load of 30 % of the store (the shared-work kernel),
+    both through their row-walking variants; each output against the oracle."""
+    rng = np.random.default_rng(7300 + int(load_share * 10))
+    L, KV, P, v, T = 4, 2, 16, 2048, 1024
+    npg = T // P
+    NP = 2 * npg + 5
+    perm = rng.permutation(NP).astype(np.int32)
+    src, dst = Requests([perm[:npg]], [T]), Requests([perm[npg:2 * npg]], [T])
+    specs = wl.split_tokens(0, 0, T, 64, 0, L, wl.TOKEN_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    load_specs = specs[:max(1, int(len(specs) * load_share))]
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(7301)
+    out, inp = Arena(nbytes, "host"), Arena(nbytes, "host")
+    data = rng.integers(0, 256, nbytes + 4096, dtype=np.uint8)
+    inp.write(data)
+    pre = dpool.host_copy()
+    kvx.kvx_exchange_chunks(ctx, dpool.pool, src.array, kvx.chunks_array(specs, out.ptr),
+                            dst.array, kvx.chunks_array(load_specs, inp.ptr),
+                            stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+    assert_bytes_equal(out.numpy(), exp, "exchange store")
+    assert_pool_equal(dpool, expected_load(pre, dst, load_specs, data.copy()))
+    out.close()
+    inp.close()
+
+
 def test_exchange_rejects_a_load_into_the_store_sources(ctx, stream):
     L, KV, P, v, NP = 2, 2, 4, 64, 8
     dpool = DevicePool.empty(L, KV, NP, P, v)
