@@ -1198,6 +1198,51 @@ def test_roundtrip_in_one_launch(ctx, stream, seed):
     arena.close()
 
 
+@pytest.mark.parametrize("P,sm_cap", [(2, 0), (4, 0), (4, 8), (16, 0)])
+def test_roundtrip_token_major_pages(ctx, stream, P, sm_cap):
+    """Round trips of token-major chunks over all layers (pages of strided 1152-byte rows):
+    batched units of short pages (2 and 4 tokens, on the default 32 SMs or on 8) and one
+    segment per unit (16 tokens), through the round trip's row-walking variants; chunks and
+    pages against the oracle."""
+    rng = np.random.default_rng(8200 + P + sm_cap)
+    L, KV, v = 3, 1, 1152
+    lens = [800, 37, 2 * P + 1]
+    pages = [-(-n // P) for n in lens]
+    NP = 2 * sum(pages) + 5
+    perm = rng.permutation(NP).astype(np.int32)
+    t_src, t_dst, at = [], [], 0
+    for npg in pages:
+        t_src.append(perm[at:at + npg])
+        t_dst.append(perm[sum(pages) + at:sum(pages) + at + npg])
+        at += npg
+    specs = []
+    for r, n in enumerate(lens):
+        specs += wl.split_tokens(r, 0, n, 96, 0, L, wl.TOKEN_MAJOR)
+    shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
+    wl.place_chunks(specs, shape)
+    nbytes = wl._arena_bytes(specs, shape)
+    src, dst = Requests(t_src, lens), Requests(t_dst, lens)
+    dpool = DevicePool.empty(L, KV, NP, P, v)
+    dpool.fill_random(8201 + P)
+    pre = dpool.host_copy()
+    arena = Arena(nbytes, "host")
+    c = None
+    if sm_cap:
+        c = kvx.kvx_default_launch_cfg(ctx, kvx.KVX_OP_ROUNDTRIP)
+        c.sm_cap = sm_cap
+    kvx.kvx_roundtrip_chunks(ctx, dpool.pool, src.array, dst.array,
+                             kvx.chunks_array(specs, arena.ptr), cfg=c,
+                             stream=stream.cuda_stream)
+    stream.synchronize()
+    assert kvx.kvx_get_status(ctx, stream.cuda_stream) == 0
+    exp = np.full(nbytes + 4096, CANARY, np.uint8)
+    oracle.store(pre, src.oracle(), oracle_chunks(specs, exp))
+    assert_bytes_equal(arena.numpy(), exp, "token-major round trip chunks")
+    oracle.load(pre, dst.oracle(), oracle_chunks(specs, exp))
+    assert_pool_equal(dpool, pre)
+    arena.close()
+
+
 @pytest.mark.parametrize("v,P,layout", [(1152, 64, 0), (1152, 64, 1), (1152, 64, 2),
                                          (4096, 16, 0), (2048, 32, 1), (1152, 29, 2)])
 def test_roundtrip_long_segments_in_row_slices(ctx, stream, v, P, layout):
