@@ -106,8 +106,8 @@ typedef struct kvx_pool {
     int32_t page_size;     /* tokens per page, > 0 */
     int32_t num_pages;     /* pages in each pool, > 0 */
     int64_t token_bytes;   /* one token's vector in one pool (heads x head_dim x dtype
-                              bytes); a positive multiple of 16, and a page
-                              (page_size x token_bytes) at most 16 GiB */
+                              bytes); a positive multiple of 16 up to 1 GiB, and a
+                              page (page_size x token_bytes) at most 16 GiB */
     void *const *k_pages;  /* HOST array [num_layers] of device pointers: layer l's K pool
                               [num_pages][page_size][token_bytes], 16-byte aligned */
     void *const *v_pages;  /* same for V; ignored (may be NULL) when kv_factor == 1 */

@@ -30,8 +30,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool op_is_scatter(int op) { return op == KVX_OP_LOAD || op == KVX_OP_SCATTER_HBM; }
 
-// Largest page (page_size x token_bytes) a pool may have: 2^30 16-byte units.
+// Largest page (page_size x token_bytes) a pool may have: 2^30 16-byte units; and the
+// largest token.
 constexpr int64_t kMaxPageBytes = int64_t(1) << 34;
+constexpr int64_t kMaxTokenBytes = int64_t(1) << 30;
 
 int64_t pages_of(int64_t n_tokens, int64_t page_size)
 {
@@ -94,9 +96,11 @@ kvx_status validate(const kvx_pool *pool, const kvx_request *reqs, int n_req,
     if (pool->token_bytes % 16 != 0)
         return fail(KVX_ERR_ALIGNMENT, msg, len, "token_bytes %lld is not a multiple of 16",
                     (long long)pool->token_bytes);
-    // The kernels count a page segment's 16-byte units in 32 bits.
-    if (int64_t(pool->page_size) * pool->token_bytes > kMaxPageBytes)
-        return fail(KVX_ERR_INVALID_ARG, msg, len, "a page of %d x %lld bytes exceeds 16 GiB",
+    // The kernels count a page segment's 16-byte units, and a token's bytes, in 32 bits.
+    if (int64_t(pool->page_size) * pool->token_bytes > kMaxPageBytes ||
+        pool->token_bytes > kMaxTokenBytes)
+        return fail(KVX_ERR_INVALID_ARG, msg, len,
+                    "a page of %d x %lld bytes exceeds 16 GiB, or a token 1 GiB",
                     pool->page_size, (long long)pool->token_bytes);
     if (!pool->k_pages || (pool->kv_factor == 2 && !pool->v_pages))
         return fail(KVX_ERR_INVALID_ARG, msg, len, "pool layer pointer array is NULL");

@@ -96,11 +96,14 @@ def test_validate_accepts_a_good_batch():
     ("negative", kvx.KVX_ERR_INVALID_ARG),
     ("null_table", kvx.KVX_ERR_INVALID_ARG),
     ("page_bytes", kvx.KVX_ERR_INVALID_ARG),
+    ("token_bytes_max", kvx.KVX_ERR_INVALID_ARG),
 ])
 def test_validate_rejects(case, status):
     b = FakeBatch(v=40 if case == "token_bytes" else 256)
     if case == "page_bytes":  # a page of 2^16 tokens x 512 KiB = 32 GiB
         b = FakeBatch(P=1 << 16, v=1 << 19)
+    elif case == "token_bytes_max":  # one token of 2 GiB in a page of one
+        b = FakeBatch(P=1, v=1 << 31)
     reqs = b.reqs([(np.arange(8, dtype=np.int32), 128)])
     spec = [0, 0, 64, 0, 4, 0, 0]
     lb, le = 0, None
