@@ -745,16 +745,18 @@ def test_round_trips_and_exchanges_in_flight_on_two_streams(ctx):
 
 # ----------------------------------------------------------------------------- errors
 
-def test_in_kernel_page_check_skips_and_reports(ctx, stream):
+@pytest.mark.parametrize("layout", [wl.LAYER_MAJOR, wl.TOKEN_MAJOR])
+def test_in_kernel_page_check_skips_and_reports(ctx, stream, layout):
     """A device page table naming a page past the pool: that segment is skipped, flagged,
-    and everything else is still moved (validation level 1 does not read page tables)."""
+    and everything else is still moved (validation level 1 does not read page tables).
+    Token-major chunks take the row-walking kernel."""
     L, KV, P, v, NP = 2, 2, 8, 64, 8
     dpool = DevicePool.empty(L, KV, NP, P, v)
     dpool.fill_random(12)
     good = np.array([5, 2], np.int32)
     bad = np.array([5, NP + 1000], np.int32)
     reqs = Requests([bad], [16], host_copy=False)
-    specs = [wl.ChunkSpec(0, 0, 8, 0, L, 0), wl.ChunkSpec(0, 8, 8, 0, L, 0)]
+    specs = [wl.ChunkSpec(0, 0, 8, 0, L, layout), wl.ChunkSpec(0, 8, 8, 0, L, layout)]
     shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
     wl.place_chunks(specs, shape)
     nbytes = wl._arena_bytes(specs, shape)
@@ -771,10 +773,12 @@ def test_in_kernel_page_check_skips_and_reports(ctx, stream):
     arena.close()
 
 
-def test_roundtrip_page_check_skips_and_reports(ctx, stream):
+@pytest.mark.parametrize("layout", [wl.LAYER_MAJOR, wl.TOKEN_MAJOR])
+def test_roundtrip_page_check_skips_and_reports(ctx, stream, layout):
     """Round trip whose source table names a page past the pool: that store segment is
     skipped and flagged, its load still runs after it (reading the untouched chunk bytes),
-    and every other segment makes the full round trip."""
+    and every other segment makes the full round trip.  Token-major chunks take the round
+    trip's row-walking variant."""
     L, KV, P, v, NP = 2, 2, 8, 64, 8
     dpool = DevicePool.empty(L, KV, NP, P, v)
     dpool.fill_random(13)
@@ -782,7 +786,7 @@ def test_roundtrip_page_check_skips_and_reports(ctx, stream):
     dst_table = np.array([1, 3], np.int32)
     src = Requests([bad_src], [16], host_copy=False)
     dst = Requests([dst_table], [16])
-    specs = [wl.ChunkSpec(0, 0, 8, 0, L, 0), wl.ChunkSpec(0, 8, 8, 0, L, 0)]
+    specs = [wl.ChunkSpec(0, 0, 8, 0, L, layout), wl.ChunkSpec(0, 8, 8, 0, L, layout)]
     shape = wl.KVShape(L, KV, 1, v, "fp8_e4m3", P, NP)
     wl.place_chunks(specs, shape)
     nbytes = wl._arena_bytes(specs, shape)
