@@ -32,6 +32,10 @@
  *   A call moves only layers inside its window [layer_begin, layer_end) (half-open),
  *   intersected with each chunk's own layers; chunk offsets stay relative to the chunk's
  *   own layer_begin.
+ *   In a TOKEN_MAJOR chunk of more than one (layer, kv) slab, a page of several tokens is
+ *   a set of strided rows on the chunk side.  Every transfer moves them at the same link
+ *   rate as the other layouts on its default grid, but on a few SMs loads from strided
+ *   host rows run at about half the rate of contiguous ones.
  *
  * Ownership.  The caller owns the pools, page tables, chunk memory and streams.  A
  * kvx_ctx owns only a small ring of descriptor buffers (pinned host + device), a device
