@@ -33,9 +33,10 @@
  *   intersected with each chunk's own layers; chunk offsets stay relative to the chunk's
  *   own layer_begin.
  *   In a TOKEN_MAJOR chunk of more than one (layer, kv) slab, a page of several tokens is
- *   a set of strided rows on the chunk side.  Every transfer moves them at the same link
- *   rate as the other layouts on its default grid, but on a few SMs loads from strided
- *   host rows run at about half the rate of contiguous ones.
+ *   a set of strided rows on the chunk side.  On their default grids stores and round
+ *   trips move such pages at the rates of the other layouts, and loads and exchanges
+ *   within 2-4 %; on a few SMs, loads from strided host rows run at about half the rate
+ *   of contiguous ones.
  *
  * Ownership.  The caller owns the pools, page tables, chunk memory and streams.  A
  * kvx_ctx owns only a small ring of descriptor buffers (pinned host + device), a device
