@@ -273,9 +273,11 @@ kvx_status kvx_load_chunks(kvx_ctx *ctx, const kvx_pool *pool, const kvx_request
  * kvx_load_chunks; either may be empty.  The store's source slots and the load's
  * destination slots must not meet for a common layer (checked at validation level 2).
  * cfg->sm_cap counts the SMs of both directions together (default 40).  Batches of
- * similar size (within 1.5x in segments) split the CTAs by direction, half each; otherwise
- * every warp takes units of both batches, so the larger one keeps the whole grid after the
- * smaller one is done.  Either way, nothing in the launch waits on anything else. */
+ * similar size (within 1.5x in segments) of page segments of 4 KiB or more split the CTAs
+ * by direction, half each; otherwise every warp takes units of both batches, so the larger
+ * one keeps the whole grid after the smaller one is done, and short segments of both
+ * directions are in flight in every warp.  Either way, nothing in the launch waits on
+ * anything else. */
 kvx_status kvx_exchange_chunks(kvx_ctx *ctx, const kvx_pool *pool,
                                const kvx_request *store_reqs, int n_store_req,
                                const kvx_chunk *store_chunks, int n_store_chunks,
